@@ -1,0 +1,133 @@
+"""Float64 CPU oracle for the FAVOR+ forward pass -- test infrastructure only.
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  It shares no code with the CUDA
+library (``favor_random_feature_gb300``) and never imports it.
+
+The arithmetic lives in ``favor_oracle.c`` (plain C, float64, OpenMP over
+heads).  This wrapper only compiles it (``build``) and marshals numpy arrays
+to it.  Each function of the C file cites the passage of the pages it
+follows.  Pins (tests/test_oracle.py) tie it to things other than itself:
+the page's printed demo table, the closed-form kernel identity, brute-force
+O(L^2) attention, Monte-Carlo unbiasedness with O(1/m) variance, the
+softmax limit for large m, positivity, and invariances.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "favor_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+
+MAP_POSITIVE, MAP_TRIG, MAP_ELU1 = 0, 1, 2
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile favor_oracle.c to oracle/_build/liboracle.so (gcc, float64,
+    no FP contraction so results agree across host architectures)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    base = ["gcc", "-O2", "-std=c99", "-ffp-contract=off", "-fPIC", "-shared",
+            _SRC, "-o", _LIB_PATH + ".tmp", "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True,
+                       capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(_LIB_PATH + ".tmp", _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        P = ctypes.POINTER(ctypes.c_double)
+        lib.oracle_features.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_int, P]
+        lib.oracle_features.restype = ctypes.c_int
+        lib.oracle_forward.argtypes = [P, P, P, P, P, P] + [ctypes.c_int] * 8 + [
+            ctypes.POINTER(ctypes.c_int), ctypes.c_int]
+        lib.oracle_forward.restype = ctypes.c_int
+        lib.oracle_feature_dim.argtypes = [ctypes.c_int] * 3
+        lib.oracle_feature_dim.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _dp(a):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double)) if a is not None else None
+
+
+def feature_dim(feature_map: int, d: int, m: int) -> int:
+    return _load().oracle_feature_dim(feature_map, d, m)
+
+
+def features(x, omega, feature_map: int = MAP_POSITIVE):
+    """phi of the rows of x [n][d] with projection omega [m][d] -> [n][r] (float64)."""
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    n, d = x.shape
+    if feature_map == MAP_ELU1:
+        om, m = None, d
+    else:
+        om = np.ascontiguousarray(omega, dtype=np.float64)
+        m = om.shape[0]
+        assert om.shape[1] == d
+    r = lib.oracle_feature_dim(feature_map, d, m)
+    phi = np.empty((n, r), dtype=np.float64)
+    rc = lib.oracle_features(_dp(x), _dp(om), n, d, m, feature_map, _dp(phi))
+    if rc:
+        raise FloatingPointError(f"oracle_features failed ({rc}): exponent out of range")
+    return phi
+
+
+def forward(q, k, v, omega, causal: bool, feature_map: int = MAP_POSITIVE,
+            heads=None, return_den: bool = False):
+    """FAVOR+ attention forward in float64.
+
+    q, k: [B][H][L][d]; v: [B][H][L][dv]; omega: [H][m][d] (None for elu1).
+    heads: optional iterable of flat head indices b*H+h; only those heads'
+    rows are computed (the others are left NaN).  Returns out [B][H][L][dv]
+    (and den [B][H][L] with return_den)."""
+    lib = _load()
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    k = np.ascontiguousarray(k, dtype=np.float64)
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    B, H, L, d = q.shape
+    dv = v.shape[-1]
+    assert k.shape == q.shape and v.shape[:3] == q.shape[:3]
+    if feature_map == MAP_ELU1:
+        om, m = None, d
+    else:
+        om = np.ascontiguousarray(omega, dtype=np.float64)
+        assert om.shape[0] == H and om.shape[2] == d
+        m = om.shape[1]
+    out = np.full((B, H, L, dv), np.nan, dtype=np.float64)
+    den = np.full((B, H, L), np.nan, dtype=np.float64) if return_den else None
+    if heads is not None:
+        hl = np.ascontiguousarray(np.asarray(list(heads), dtype=np.int32))
+        hp, nh = hl.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), len(hl)
+    else:
+        hp, nh = None, 0
+    rc = lib.oracle_forward(_dp(q), _dp(k), _dp(v), _dp(om), _dp(out), _dp(den),
+                            B, H, L, d, dv, m, int(bool(causal)), feature_map, hp, nh)
+    if rc:
+        raise FloatingPointError(f"oracle_forward failed ({rc})")
+    return (out, den) if return_den else out
+
+
+def threads_used() -> int:
+    """OpenMP threads the oracle runs with (OMP_NUM_THREADS or all cores)."""
+    env = os.environ.get("OMP_NUM_THREADS")
+    return int(env) if env else (os.cpu_count() or 1)

@@ -1,0 +1,328 @@
+"""Pins for the float64 oracle: each test ties it to something other than
+itself -- a table the pages print, a closed form, brute force on tiny inputs,
+a Monte-Carlo statement the pages make, or an invariant of the definition.
+CPU only."""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from favor_inputs import (CAUSAL8K, DEMO64, MAP_ELU1, MAP_POSITIVE, MAP_TRIG,
+                          bf16_bits, bf16_to_f32, make_inputs,
+                          omega_block_orthogonal, omega_iid)
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------------------
+# independent closed forms used by the pins (not the oracle's code path)
+# ---------------------------------------------------------------------------
+def kernel_positive_closed(q, k, om):
+    """(1/m) sum_i exp(w_i.(q+k) - (|q|^2+|k|^2)/2): the product of two
+    positive features written as one sum (spec closed form)."""
+    m = om.shape[0]
+    s = om @ (q + k)
+    return np.sum(np.exp(s - (q @ q + k @ k) / 2.0)) / m
+
+
+def kernel_trig_closed(q, k, om):
+    """(1/m) sum_i cos(w_i.(q-k)): sin a sin b + cos a cos b = cos(a-b)."""
+    m = om.shape[0]
+    return np.sum(np.cos(om @ (q - k))) / m
+
+
+def brute_attention(Amat, V, causal):
+    """O(L^2) attention with an explicit kernel matrix A_ij; lower triangle
+    (diagonal included) when causal."""
+    if causal:
+        Amat = np.tril(Amat)
+    return (Amat @ V) / (Amat @ np.ones(Amat.shape[1]))[:, None]
+
+
+def softmax_attention(Q, K, V, scale):
+    S = (Q @ K.T) * scale
+    S = S - S.max(axis=1, keepdims=True)
+    P = np.exp(S)
+    P /= P.sum(axis=1, keepdims=True)
+    return P @ V
+
+
+# ---------------------------------------------------------------------------
+# golden: the printed demo table of the Performer page, Out[27]
+# ---------------------------------------------------------------------------
+def test_page_demo_table_reproduced():
+    rows = [l.split() for l in open(os.path.join(GOLDEN, "performer_page_demo_table.txt"))
+            if l.strip() and not l.startswith("#")]
+    inp = make_inputs(DEMO64)
+    Q = inp.q32[0, 0].astype(np.float64)
+    K = inp.k32[0, 0].astype(np.float64)
+    V = inp.v32[0, 0].astype(np.float64)
+    n, d = Q.shape
+    ref = softmax_attention(Q, K, V, 1.0 / math.sqrt(d))
+    for m_s, cos_s, mse_s in rows:
+        m = int(m_s)
+        # the page's own projection: seed 0, randn(d, m) / sqrt(d)
+        W = np.random.RandomState(0).randn(d, m) / np.sqrt(d)
+        out = oracle.forward(Q[None, None], K[None, None], V[None, None], W.T[None],
+                             causal=False)[0, 0]
+        cos = np.mean([np.dot(ref[i], out[i]) / (np.linalg.norm(ref[i]) * np.linalg.norm(out[i]))
+                       for i in range(n)])
+        mse = np.mean((ref - out) ** 2)
+        assert f"{cos:.4f}" == cos_s, (m, cos, cos_s)
+        assert f"{mse:.6f}" == mse_s, (m, mse, mse_s)
+
+
+# ---------------------------------------------------------------------------
+# C1: closed form of phi(q)^T phi(k)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("d,m", [(32, 256), (64, 64), (128, 512)])
+def test_positive_features_closed_form(d, m):
+    rng = np.random.default_rng(7)
+    om = rng.standard_normal((m, d))
+    x = rng.standard_normal((6, d)) * d ** -0.25
+    phi = oracle.features(x, om, MAP_POSITIVE)
+    assert phi.shape == (6, m)
+    for a in range(3):
+        for b in range(3, 6):
+            got = phi[a] @ phi[b]
+            want = kernel_positive_closed(x[a], x[b], om)
+            assert abs(got - want) <= 1e-13 * abs(want)
+
+
+def test_trig_features_closed_form_and_order():
+    rng = np.random.default_rng(8)
+    d, m = 16, 64
+    om = rng.standard_normal((m, d))
+    x = rng.standard_normal((4, d)) * 0.5
+    phi = oracle.features(x, om, MAP_TRIG)
+    assert phi.shape == (4, 2 * m)
+    # interleaved [sin(w1.x), cos(w1.x), ...] / sqrt(m), as printed
+    p = om @ x[0]
+    assert np.allclose(phi[0, 0::2] * math.sqrt(m), np.sin(p), rtol=0, atol=1e-14)
+    assert np.allclose(phi[0, 1::2] * math.sqrt(m), np.cos(p), rtol=0, atol=1e-14)
+    for a, b in [(0, 1), (2, 3), (1, 3)]:
+        assert abs(phi[a] @ phi[b] - kernel_trig_closed(x[a], x[b], om)) <= 1e-14
+
+
+def test_elu1_features_piecewise():
+    x = np.array([[-2.0, -1e-300, 0.0, 1e-300, 0.5, 3.0]])
+    phi = oracle.features(x, None, MAP_ELU1)
+    # x+1 for x>0, e^x for x<=0; continuous at 0
+    want = [math.exp(-2.0), 1.0, 1.0, 1.0, 1.5, 4.0]
+    assert np.allclose(phi[0], want, rtol=1e-15, atol=0)
+
+
+# ---------------------------------------------------------------------------
+# C2 / C7: brute-force O(L^2) attention with the explicit kernel matrix
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("fmap", [MAP_POSITIVE, MAP_TRIG, MAP_ELU1])
+def test_bruteforce_kernel_attention(causal, fmap):
+    rng = np.random.default_rng(11 + fmap)
+    H, L, d, dv, m = 2, 40, 16, 8, 32
+    q = rng.standard_normal((1, H, L, d)) * d ** -0.25
+    k = rng.standard_normal((1, H, L, d)) * d ** -0.25
+    v = rng.standard_normal((1, H, L, dv))
+    if fmap == MAP_TRIG:
+        # small inputs keep the trig denominators well away from zero
+        q *= 0.3
+        k *= 0.3
+    om = rng.standard_normal((H, m, d)) if fmap != MAP_ELU1 else None
+    out = oracle.forward(q, k, v, om, causal=causal, feature_map=fmap)
+    for h in range(H):
+        A = np.empty((L, L))
+        for i in range(L):
+            for j in range(L):
+                if fmap == MAP_POSITIVE:
+                    A[i, j] = kernel_positive_closed(q[0, h, i], k[0, h, j], om[h])
+                elif fmap == MAP_TRIG:
+                    A[i, j] = kernel_trig_closed(q[0, h, i], k[0, h, j], om[h])
+                else:
+                    fq = np.where(q[0, h, i] > 0, q[0, h, i] + 1.0, np.exp(q[0, h, i]))
+                    fk = np.where(k[0, h, j] > 0, k[0, h, j] + 1.0, np.exp(k[0, h, j]))
+                    A[i, j] = fq @ fk
+        ref = brute_attention(A, v[0, h], causal)
+        err = np.max(np.abs(out[0, h] - ref)) / np.max(np.abs(ref))
+        assert err <= 1e-12, err
+
+
+def test_causal_reduces_to_noncausal_at_last_row_and_v0_at_first():
+    inp = make_inputs(CAUSAL8K, L=50, B=1, H=2)
+    args = (inp.q32, inp.k32, inp.v32, inp.omega)
+    oc = oracle.forward(*args, causal=True)
+    on = oracle.forward(*args, causal=False)
+    assert np.allclose(oc[:, :, -1], on[:, :, -1], rtol=1e-13, atol=1e-15)
+    # row 0 attends only to key 0: out_0 = v_0 (up to one rounding)
+    assert np.allclose(oc[:, :, 0], inp.v32[:, :, 0], rtol=1e-14, atol=1e-15)
+
+
+# ---------------------------------------------------------------------------
+# C3: Monte-Carlo unbiasedness and O(1/m) variance (pages: E[phi(q)^T phi(k)]
+# = exp(q^T k); "variance decreases as O(1/m)")
+# ---------------------------------------------------------------------------
+def _mc_estimates(q, k, m, T, seed, fmap=MAP_POSITIVE, orth=False):
+    rng = np.random.default_rng(seed)
+    d = q.shape[0]
+    x = np.stack([q, k])
+    est = np.empty(T)
+    for t in range(T):
+        if orth:
+            om = omega_block_orthogonal(rng, 1, m, d)[0].astype(np.float64)
+        else:
+            om = rng.standard_normal((m, d))
+        phi = oracle.features(x, om, fmap)
+        est[t] = phi[0] @ phi[1]
+    return est
+
+
+def _qk_pair(d, seed, scale):
+    rng = np.random.default_rng(seed)
+    return rng.standard_normal(d) * scale, rng.standard_normal(d) * scale
+
+
+def test_monte_carlo_unbiased_and_variance_1_over_m():
+    d = 8
+    q, k = _qk_pair(d, 3, 0.25)
+    target = math.exp(q @ k)
+    var1 = math.exp(2 * q @ k) * (math.exp((q + k) @ (q + k)) - 1.0)  # one feature
+    T = 3000
+    ms = [16, 32, 64, 128, 256]
+    variances = []
+    for i, m in enumerate(ms):
+        est = _mc_estimates(q, k, m, T, 100 + i)
+        se = math.sqrt(var1 / m / T)
+        assert abs(est.mean() - target) <= 5 * se, (m, est.mean(), target, se)
+        s2 = est.var(ddof=1)
+        assert abs(s2 / (var1 / m) - 1.0) < 0.2, (m, s2, var1 / m)
+        variances.append(s2)
+    slope = np.polyfit(np.log(ms), np.log(variances), 1)[0]
+    assert abs(slope + 1.0) < 0.1, slope
+
+
+def test_monte_carlo_orthogonal_unbiased_and_not_worse():
+    d = 8
+    q, k = _qk_pair(d, 5, 0.25)
+    target = math.exp(q @ k)
+    var1 = math.exp(2 * q @ k) * (math.exp((q + k) @ (q + k)) - 1.0)
+    m, T = 16, 3000
+    est_o = _mc_estimates(q, k, m, T, 7, orth=True)
+    est_i = _mc_estimates(q, k, m, T, 8, orth=False)
+    se = math.sqrt(var1 / m / T)
+    assert abs(est_o.mean() - target) <= 5 * se
+    # orthogonal rows: variance no larger than iid (soft, 20% slack)
+    assert est_o.var() <= 1.2 * est_i.var()
+
+
+def test_monte_carlo_trig_gaussian_kernel():
+    d = 8
+    q, k = _qk_pair(d, 9, 0.3)
+    dl = (q - k) @ (q - k)
+    target = math.exp(-dl / 2)
+    var1 = (1 + math.exp(-2 * dl)) / 2 - math.exp(-dl)
+    m, T = 32, 3000
+    est = _mc_estimates(q, k, m, T, 10, fmap=MAP_TRIG)
+    se = math.sqrt(var1 / m / T)
+    assert abs(est.mean() - target) <= 5 * se
+    assert abs(est.var(ddof=1) / (var1 / m) - 1.0) < 0.2
+
+
+# ---------------------------------------------------------------------------
+# C6: textbook limit -- large m approaches exact softmax attention exp(q^T k)
+# ---------------------------------------------------------------------------
+def test_large_m_approaches_softmax_attention():
+    rng = np.random.default_rng(21)
+    L, d, dv = 12, 8, 4
+    # |q+k|^2 ~ 2: the per-feature variance factor exp(|q+k|^2)-1 stays small
+    q = rng.standard_normal((L, d)) * 0.35
+    k = rng.standard_normal((L, d)) * 0.35
+    v = rng.standard_normal((L, dv))
+    ref = softmax_attention(q, k, v, 1.0)      # logits q^T k, inputs pre-scaled
+    errs = {}
+    for m in (256, 65536):
+        om = rng.standard_normal((1, m, d))
+        out = oracle.forward(q[None, None], k[None, None], v[None, None], om, causal=False)[0, 0]
+        errs[m] = np.max(np.abs(out - ref))
+    assert errs[65536] < 0.02
+    assert errs[65536] < errs[256] / 4
+
+
+# ---------------------------------------------------------------------------
+# C4 / C5: positivity and invariances
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("fmap", [MAP_POSITIVE, MAP_ELU1])
+def test_features_and_denominators_positive(fmap):
+    inp = make_inputs(CAUSAL8K, L=64, B=1, H=2)
+    om = inp.omega if fmap == MAP_POSITIVE else None
+    for h in range(2):
+        phi = oracle.features(inp.q32[0, h], om[h] if om is not None else None, fmap)
+        assert np.all(phi > 0)
+    for causal in (False, True):
+        out, den = oracle.forward(inp.q32, inp.k32, inp.v32, om, causal=causal,
+                                  feature_map=fmap, return_den=True)
+        assert np.all(den > 0)
+        # a convex combination of the v rows: inside their column range
+        vmin = inp.v32.min(axis=2, keepdims=True)
+        vmax = inp.v32.max(axis=2, keepdims=True)
+        assert np.all(out >= vmin - 1e-12) and np.all(out <= vmax + 1e-12)
+
+
+def test_constant_values_reproduced():
+    inp = make_inputs(CAUSAL8K, L=30, B=1, H=1)
+    v = np.broadcast_to(np.arange(64.0)[None, None, None, :] - 20.0, inp.v32.shape)
+    for causal in (False, True):
+        out = oracle.forward(inp.q32, inp.k32, v, inp.omega, causal=causal)
+        assert np.allclose(out, v, rtol=1e-13, atol=1e-12)
+
+
+def test_permuting_omega_rows_is_invariant():
+    inp = make_inputs(CAUSAL8K, L=33, B=1, H=1)
+    perm = np.random.default_rng(0).permutation(inp.omega.shape[1])
+    for causal in (False, True):
+        a = oracle.forward(inp.q32, inp.k32, inp.v32, inp.omega, causal=causal)
+        b = oracle.forward(inp.q32, inp.k32, inp.v32, inp.omega[:, perm], causal=causal)
+        assert np.allclose(a, b, rtol=1e-12, atol=1e-13)
+
+
+def test_head_subset_matches_full():
+    inp = make_inputs(CAUSAL8K, L=20, B=2, H=3)
+    full = oracle.forward(inp.q32, inp.k32, inp.v32, inp.omega, causal=True)
+    sub = oracle.forward(inp.q32, inp.k32, inp.v32, inp.omega, causal=True, heads=[4, 1])
+    flat_f = full.reshape(6, 20, 64)
+    flat_s = sub.reshape(6, 20, 64)
+    assert np.array_equal(flat_f[[1, 4]], flat_s[[1, 4]])
+    assert np.isnan(flat_s[0]).all()
+
+
+# ---------------------------------------------------------------------------
+# the input generators: bf16 rounding and block-orthogonal omega
+# ---------------------------------------------------------------------------
+def test_bf16_rounding_matches_torch():
+    torch = pytest.importorskip("torch")
+    x = np.random.default_rng(0).standard_normal(100000).astype(np.float32) * 7
+    x[:4] = [1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -1.0 - 2 ** -8, 0.0]   # ties
+    got = bf16_bits(x)
+    want = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, want)
+    back = bf16_to_f32(got)
+    assert np.all(np.abs(back - x) <= np.abs(x) * 2.0 ** -8)
+
+
+def test_block_orthogonal_omega():
+    from scipy import stats
+    rng = np.random.default_rng(3)
+    d, m = 16, 40
+    om = omega_block_orthogonal(rng, 50, m, d).astype(np.float64)
+    for h in range(3):
+        for b0, b1 in [(0, 16), (16, 32), (32, 40)]:
+            blk = om[h, b0:b1]
+            n = blk / np.linalg.norm(blk, axis=1, keepdims=True)
+            g = n @ n.T
+            assert np.allclose(g, np.eye(b1 - b0), atol=1e-6)   # fp32 storage
+    # row lengths ~ chi(d)
+    lengths = np.linalg.norm(om.reshape(-1, d), axis=1)
+    assert stats.kstest(lengths, stats.chi(d).cdf).pvalue > 1e-3
+    # iid draws are N(0,1) entries
+    iid = omega_iid(rng, 4, 64, d).ravel()
+    assert stats.kstest(iid, "norm").pvalue > 1e-3
