@@ -1,0 +1,337 @@
+"""Benchmark of the FAVOR+ attention forward pass on GB300 (one JSON line).
+
+A step is one forward pass (feature maps, state reduction, causal scan or
+non-causal output, normalisation) over the whole workload, inputs resident
+in HBM.  Default workload: causal, B=4, H=16, L=8192, d=dv=64, m=256,
+block-orthogonal omega, bf16 inputs (synthetic, seeded).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload causal8k|nc4096|long64k|long64k_nc|sweep16k]
+
+--impl reference times the float64 CPU oracle (the slow, obviously correct
+statement of the method) on bounded samples of the same workload.
+Multi-GPU (torchrun): every rank runs its own replica of the workload (the
+path shards over heads with no exchange), value = all ranks' tokens / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "FAVOR+ fwd tokens/sec (B·H·L/s) at L=8192 causal m=256; % of roofline"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def workload(name):
+    from favor_inputs import CAUSAL8K, LONG64K, NC4096, SWEEP16K
+    table = {
+        "causal8k": (CAUSAL8K, True),
+        "nc4096": (NC4096, False),
+        "long64k": (LONG64K, True),
+        "long64k_nc": (LONG64K, False),
+        "sweep16k": (SWEEP16K, True),
+    }
+    return table[name]
+
+
+def describe(w, causal):
+    return {
+        "workload": f"{w.name}: B={w.B} H={w.H} L={w.L} d={w.d} dv={w.dv} m={w.m} "
+                    f"{'causal' if causal else 'non-causal'} positive-features "
+                    f"omega={w.omega} seed={w.seed}",
+        "B": w.B, "H": w.H, "L": w.L, "d": w.d, "dv": w.dv, "m": w.m, "causal": causal,
+        "feature_map": "positive", "omega": w.omega,
+        "inputs": "bf16 q,k,v; fp32 omega; fp32 out",
+        "l2": "flushed between steps (256 MiB write, outside the timed events); "
+              "step inputs+outputs exceed L2",
+    }
+
+
+def per_token(w):
+    """Algorithmic work per token: flops, HBM bytes, exps (positive map)."""
+    flops = 2 * w.m * (2 * w.d + 2 * w.dv)
+    hbm = 2 * (2 * w.d + w.dv) + 4 * w.dv
+    exps = 2 * w.m
+    return flops, hbm, exps
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), float(j["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples (host timestamped) while the benchmark runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(gpu_index), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        win = [s for t, s in self.samples if t0 - 0.25 <= t <= t1 + 0.25]
+        if not win:
+            win = [s for _, s in self.samples[-5:]]
+        sm = [float(s[1]) for s in win if s[1].replace(".", "").isdigit()]
+        mx = [float(s[2]) for s in win if s[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for s in win for n, v in zip(names, s[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(win)}
+
+
+def cpu_baseline(inp, causal, heads_per_sample=None):
+    """The float64 oracle, as it stands, on a bounded sample of the workload."""
+    import oracle
+    w = inp.w
+    cores = oracle.threads_used()
+    n = heads_per_sample or min(w.B * w.H, 2 * cores)
+    # the first n heads as a batch of one: q/k/v [1][n][L][.], omega [n][m][d]
+    sel = lambda a: a.reshape(w.B * w.H, w.L, a.shape[-1])[:n][None]
+    q, k, v = sel(inp.q32), sel(inp.k32), sel(inp.v32)
+    om = inp.omega[[h % w.H for h in range(n)]]
+    t0 = time.perf_counter()
+    oracle.forward(q, k, v, om, causal=causal)
+    dt = time.perf_counter() - t0
+    return {"value": n * w.L / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} of {w.B * w.H} heads x L={w.L} (float64 C oracle, OpenMP over heads)",
+            "seconds": dt}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    from favor_inputs import make_inputs
+    w, causal = workload(args.workload)
+    if args.workload == "long64k_nc":
+        causal = False
+    inp = make_inputs(w)
+    cores = oracle.threads_used()
+    n = min(w.B * w.H, cores)
+    for _ in range(args.warmup):
+        cpu_baseline(inp, causal, heads_per_sample=n)
+    times = []
+    for _ in range(args.steps):
+        r = cpu_baseline(inp, causal, heads_per_sample=n)
+        times.append(r["seconds"])
+    ms = 1000 * statistics.mean(times)
+    value = n * w.L / (ms / 1000)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": describe(w, causal),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n} of {w.B * w.H} heads x L={w.L} per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    from favor_random_feature_gb300 import build as fbuild
+    fbuild.build()
+    import favor_random_feature_gb300 as fv
+    from favor_inputs import make_inputs
+
+    w, causal = workload(args.workload)
+    if args.workload == "long64k_nc":
+        causal = False
+    inp = make_inputs(w.with_(seed=w.seed + 1000 * rank)) if rank else make_inputs(w)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(
+        torch.bfloat16).cuda()
+    q, k, v = dev(inp.q), dev(inp.k), dev(inp.v)
+    om = torch.from_numpy(np.ascontiguousarray(inp.omega)).cuda()
+    out = torch.empty((w.B, w.H, w.L, w.dv), dtype=torch.float32, device="cuda")
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    call = lambda: fv.favor_attn_forward(q, k, v, om, out, w.B, w.H, w.L, w.d, w.dv, w.m,
+                                         int(causal), 0, stream)
+
+    def check(rc):
+        if rc != fv.FAVOR_OK:
+            raise fv.FavorError(rc, "favor_attn_forward")
+
+    for _ in range(max(3, args.warmup)):
+        check(call())
+    torch.cuda.synchronize()
+    st = fv.favor_get_device_status(stream)
+    if st != fv.FAVOR_OK:
+        raise fv.FavorError(st, "device status")
+
+    sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                           else os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local])
+    # soak so that the clock samples see the GPU under load
+    t_soak = time.time()
+    while time.time() - t_soak < 1.0:
+        check(call())
+        torch.cuda.synchronize()
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    fv.favor_stats_enable(True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        check(call())
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if dist:
+        dist.barrier()
+    stats = fv.favor_stats_read()
+    fv.favor_stats_enable(False)
+    sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    ms = statistics.mean(step_ms)
+    dom_ms = stats.dominant_ms / max(1, stats.dominant_launches)
+    if dist:
+        t = torch.tensor([ms, dom_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, dom_ms = t.tolist()
+    tokens = w.B * w.H * w.L
+    value = world * tokens / (ms / 1000.0)
+
+    flops_tok, bytes_tok, exps_tok = per_token(w)
+    hbm_gbs, tflops, src = peaks()
+    achieved = bytes_tok * tokens / (dom_ms / 1000.0) / 1e9
+    roof_ms = max(flops_tok * tokens / (tflops * 1e12), bytes_tok * tokens / (hbm_gbs * 1e9)) * 1e3
+
+    # end to end through the host-buffer entry point (pinned host memory)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory().numpy()
+    hq, hk, hv = pin(inp.q), pin(inp.k), pin(inp.v)
+    hom = pin(np.ascontiguousarray(inp.omega, dtype=np.float32))
+    hout = torch.empty((w.B, w.H, w.L, w.dv), dtype=torch.float32).pin_memory().numpy()
+    ecall = lambda: fv.favor_attn_forward_host(hq, hk, hv, hom, hout, w.B, w.H, w.L, w.d, w.dv,
+                                               w.m, int(causal), 0, stream)
+    for _ in range(2):
+        check(ecall())
+    e2e_steps = max(3, min(args.steps, 20))
+    if dist:
+        dist.barrier()
+    te0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        check(ecall())
+    te = (time.perf_counter() - te0) / e2e_steps
+    if dist:
+        t = torch.tensor([te], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        te = t.item()
+    h2d = inp.q.nbytes + inp.k.nbytes + inp.v.nbytes + hom.nbytes
+    d2h = hout.nbytes
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": describe(w, causal),
+        "roofline": {
+            "bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+            "frac": achieved / hbm_gbs, "traffic": None,
+            "kernel": stats.dominant_kernel.decode() if stats.dominant_kernel else None,
+            "kernel_ms": dom_ms, "peak_source": src,
+            "algorithmic_bytes_per_launch": bytes_tok * tokens,
+            "step_roofline_ms": roof_ms, "step_frac": roof_ms / ms,
+        },
+        "e2e": {"value": world * tokens / te, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(stats.kernel_launches),
+        "clocks": sampler.summary(t0, t1),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = cpu_baseline(inp, causal)
+        cb.pop("seconds", None)
+        line["cpu_baseline"] = cb
+    if rank == 0:
+        print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="causal8k",
+                    choices=["causal8k", "nc4096", "long64k", "long64k_nc", "sweep16k"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,325 @@
+// favor_abi.cu -- the extern "C" boundary of libfavor: argument validation,
+// the per-device workspace, the device status word and dispatch to the
+// tensor-core path (bf16 inputs) or the fp32 SIMT path.
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "favor_internal.h"
+
+namespace favor {
+
+static __device__ int g_device_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    void *ws = nullptr;
+    size_t ws_bytes = 0;
+    void *stage = nullptr;     // host-API staging buffer
+    size_t stage_bytes = 0;
+    int *status = nullptr;     // device address of g_device_status
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+int current_device(int *dev) {
+    if (cudaGetDevice(dev) != cudaSuccess) return FAVOR_ERR_CUDA;
+    if (*dev < 0 || *dev >= kMaxDevices) return FAVOR_ERR_UNSUPPORTED;
+    return FAVOR_OK;
+}
+
+// Grow-only device buffer; frees the old one after a device sync.
+void *grow(void **buf, size_t *have, size_t bytes, int *status) {
+    if (*buf && *have >= bytes) return *buf;
+    if (*buf) {
+        cudaDeviceSynchronize();
+        cudaFree(*buf);
+        *buf = nullptr;
+        *have = 0;
+    }
+    size_t want = bytes < (size_t(1) << 20) ? (size_t(1) << 20) : bytes;
+    if (cudaMalloc(buf, want) != cudaSuccess) {
+        cudaGetLastError();
+        *buf = nullptr;
+        *status = FAVOR_ERR_NOMEM;
+        return nullptr;
+    }
+    *have = want;
+    return *buf;
+}
+
+bool is_aligned(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void *a, size_t an, const void *b, size_t bn) {
+    uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + bn && b0 < a0 + an;
+}
+
+}  // namespace
+
+void *workspace(size_t bytes, int *status) {
+    int dev;
+    int rc = current_device(&dev);
+    if (rc) { *status = rc; return nullptr; }
+    std::lock_guard<std::mutex> lk(g_mu);
+    return grow(&g_dev[dev].ws, &g_dev[dev].ws_bytes, bytes, status);
+}
+
+int *device_status_ptr() {
+    int dev;
+    if (current_device(&dev)) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_dev[dev].status) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        g_dev[dev].status = static_cast<int *>(p);
+    }
+    return g_dev[dev].status;
+}
+
+// ---- measurement hook ------------------------------------------------------
+namespace {
+struct Recorder {
+    std::mutex mu;
+    bool enabled = false;
+    std::vector<cudaEvent_t> ev;   // pairs: [2i] begin, [2i+1] end
+    size_t used = 0;               // events recorded so far
+    const char *kernel = "";
+    std::atomic<long long> launches{0};
+};
+Recorder g_rec;
+}  // namespace
+
+void stats_begin(cudaStream_t s, const char *kernel) {
+    std::lock_guard<std::mutex> lk(g_rec.mu);
+    if (!g_rec.enabled) return;
+    if (g_rec.used + 2 > g_rec.ev.size()) {
+        for (int i = 0; i < 2; ++i) {
+            cudaEvent_t e;
+            if (cudaEventCreate(&e) != cudaSuccess) { cudaGetLastError(); return; }
+            g_rec.ev.push_back(e);
+        }
+    }
+    g_rec.kernel = kernel;
+    cudaEventRecord(g_rec.ev[g_rec.used], s);
+}
+
+void stats_end(cudaStream_t s) {
+    std::lock_guard<std::mutex> lk(g_rec.mu);
+    if (!g_rec.enabled || g_rec.used + 2 > g_rec.ev.size()) return;
+    cudaEventRecord(g_rec.ev[g_rec.used + 1], s);
+    g_rec.used += 2;
+}
+
+void stats_count_launch() {
+    if (g_rec.enabled) g_rec.launches.fetch_add(1, std::memory_order_relaxed);
+}
+
+int make_problem(int B, int H, int L, int d, int dv, int m, int causal, int map, Problem *p) {
+    if (B < 1 || H < 1 || L < 1) return FAVOR_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FAVOR_ERR_INVALID_ARG;
+    if (map < FAVOR_MAP_POSITIVE || map > FAVOR_MAP_ELU1) return FAVOR_ERR_INVALID_ARG;
+    if (d != 32 && d != 64 && d != 128) return FAVOR_ERR_UNSUPPORTED;
+    if (dv != 32 && dv != 64 && dv != 128) return FAVOR_ERR_UNSUPPORTED;
+    if (map == FAVOR_MAP_ELU1) {
+        if (m != d) return FAVOR_ERR_INVALID_ARG;
+    } else {
+        if (m < 1) return FAVOR_ERR_INVALID_ARG;
+        if (m % 16 != 0) return FAVOR_ERR_UNSUPPORTED;
+        if (m > 4096) return FAVOR_ERR_UNSUPPORTED;
+    }
+    long long rows = (long long)B * H * L;
+    if (rows * (d > dv ? d : dv) > 0x7fffffffLL) return FAVOR_ERR_UNSUPPORTED;
+    p->B = B; p->H = H; p->L = L; p->d = d; p->dv = dv; p->m = m;
+    p->causal = causal;
+    p->map = map;
+    p->BH = B * H;
+    p->nproj = map == FAVOR_MAP_ELU1 ? d : m;
+    p->r = map == FAVOR_MAP_TRIG ? 2 * m : (map == FAVOR_MAP_ELU1 ? d : m);
+    return FAVOR_OK;
+}
+
+int check_ptr(const void *p, bool allow_null) {
+    if (!p) return allow_null ? FAVOR_OK : FAVOR_ERR_INVALID_ARG;
+    return is_aligned(p) ? FAVOR_OK : FAVOR_ERR_INVALID_ARG;
+}
+
+static int validate(const void *q, const void *k, const void *v, const float *omega,
+                    const float *out, size_t esize, const Problem &p) {
+    int rc;
+    if ((rc = check_ptr(q, false)) || (rc = check_ptr(k, false)) || (rc = check_ptr(v, false)) ||
+        (rc = check_ptr(out, false)))
+        return rc;
+    if ((rc = check_ptr(omega, p.map == FAVOR_MAP_ELU1))) return rc;
+    size_t rows = (size_t)p.BH * p.L;
+    size_t out_bytes = rows * p.dv * sizeof(float);
+    if (overlaps(out, out_bytes, q, rows * p.d * esize) ||
+        overlaps(out, out_bytes, k, rows * p.d * esize) ||
+        overlaps(out, out_bytes, v, rows * p.dv * esize) ||
+        (omega && overlaps(out, out_bytes, omega, (size_t)p.H * p.nproj * p.d * sizeof(float))))
+        return FAVOR_ERR_INVALID_ARG;
+    return FAVOR_OK;
+}
+
+}  // namespace favor
+
+using namespace favor;
+
+extern "C" int favor_feature_dim(int feature_map, int d, int m) {
+    if (feature_map == FAVOR_MAP_POSITIVE) return m >= 1 ? m : -1;
+    if (feature_map == FAVOR_MAP_TRIG) return m >= 1 ? 2 * m : -1;
+    if (feature_map == FAVOR_MAP_ELU1) return (d >= 1 && m == d) ? d : -1;
+    return -1;
+}
+
+extern "C" int favor_attn_forward(const void *q, const void *k, const void *v, const float *omega,
+                                  float *out, int B, int H, int L, int d, int dv, int m,
+                                  int causal, int feature_map, cudaStream_t stream) {
+    Problem p;
+    int rc = make_problem(B, H, L, d, dv, m, causal, feature_map, &p);
+    if (rc) return rc;
+    if ((rc = validate(q, k, v, omega, out, 2, p))) return rc;
+    if (tc_supported(p)) return tc_forward(q, k, v, omega, out, p, stream);
+    return simt_forward(q, k, v, true, omega, out, p, stream);
+}
+
+extern "C" int favor_attn_forward_f32(const float *q, const float *k, const float *v,
+                                      const float *omega, float *out, int B, int H, int L, int d,
+                                      int dv, int m, int causal, int feature_map,
+                                      cudaStream_t stream) {
+    Problem p;
+    int rc = make_problem(B, H, L, d, dv, m, causal, feature_map, &p);
+    if (rc) return rc;
+    if ((rc = validate(q, k, v, omega, out, 4, p))) return rc;
+    return simt_forward(q, k, v, false, omega, out, p, stream);
+}
+
+extern "C" int favor_attn_forward_host(const void *q, const void *k, const void *v,
+                                       const float *omega, float *out, int B, int H, int L, int d,
+                                       int dv, int m, int causal, int feature_map,
+                                       cudaStream_t stream) {
+    Problem p;
+    int rc = make_problem(B, H, L, d, dv, m, causal, feature_map, &p);
+    if (rc) return rc;
+    if (!q || !k || !v || !out || (!omega && feature_map != FAVOR_MAP_ELU1))
+        return FAVOR_ERR_INVALID_ARG;
+    const size_t rows = (size_t)p.BH * p.L;
+    const size_t qb = rows * p.d * 2, vb = rows * p.dv * 2, ob = rows * p.dv * 4;
+    const size_t wb = omega ? (size_t)p.H * p.nproj * p.d * 4 : 0;
+    const size_t need = carve_bytes<char>(qb) * 2 + carve_bytes<char>(vb) + carve_bytes<char>(wb) +
+                       carve_bytes<char>(ob);
+    int dev;
+    if ((rc = current_device(&dev))) return rc;
+    char *stage;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        stage = static_cast<char *>(grow(&g_dev[dev].stage, &g_dev[dev].stage_bytes, need, &rc));
+    }
+    if (!stage) return rc;
+    Carve cv{stage, 0};
+    char *dq = cv.take<char>(qb), *dk = cv.take<char>(qb), *dvp = cv.take<char>(vb);
+    float *dw = omega ? reinterpret_cast<float *>(cv.take<char>(wb)) : nullptr;
+    float *dout = reinterpret_cast<float *>(cv.take<char>(ob));
+    if (cudaMemcpyAsync(dq, q, qb, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+        cudaMemcpyAsync(dk, k, qb, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+        cudaMemcpyAsync(dvp, v, vb, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+        (dw && cudaMemcpyAsync(dw, omega, wb, cudaMemcpyHostToDevice, stream) != cudaSuccess))
+        return FAVOR_ERR_CUDA;
+    rc = favor_attn_forward(dq, dk, dvp, dw, dout, B, H, L, d, dv, m, causal, feature_map, stream);
+    if (rc) return rc;
+    if (cudaMemcpyAsync(out, dout, ob, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return FAVOR_ERR_CUDA;
+    return cuda_status(cudaStreamSynchronize(stream));
+}
+
+extern "C" int favor_feature_map(const void *x, const float *omega, float *phi, float *log_scale,
+                                 int B, int H, int L, int d, int m, int feature_map, int is_key,
+                                 cudaStream_t stream) {
+    (void)is_key;
+    Problem p;
+    int rc = make_problem(B, H, L, d, d, m, 0, feature_map, &p);
+    if (rc) return rc;
+    if ((rc = check_ptr(x, false)) || (rc = check_ptr(phi, false)) ||
+        (rc = check_ptr(log_scale, false)) ||
+        (rc = check_ptr(omega, feature_map == FAVOR_MAP_ELU1)))
+        return rc;
+    return simt_feature_map(x, true, omega, phi, log_scale, p, stream);
+}
+
+extern "C" int favor_get_device_status(cudaStream_t stream) {
+    int *sp = device_status_ptr();
+    if (!sp) return FAVOR_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return FAVOR_ERR_CUDA;
+    int h = 0;
+    if (cudaMemcpy(&h, sp, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FAVOR_ERR_CUDA;
+    int zero = 0;
+    if (cudaMemcpy(sp, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return FAVOR_ERR_CUDA;
+    return h;
+}
+
+extern "C" const char *favor_strerror(int status) {
+    switch (status) {
+        case FAVOR_OK: return "FAVOR_OK";
+        case FAVOR_ERR_INVALID_ARG: return "FAVOR_ERR_INVALID_ARG: invalid argument";
+        case FAVOR_ERR_UNSUPPORTED: return "FAVOR_ERR_UNSUPPORTED: shape not supported";
+        case FAVOR_ERR_CUDA: return "FAVOR_ERR_CUDA: CUDA runtime error";
+        case FAVOR_ERR_TIMEOUT: return "FAVOR_ERR_TIMEOUT: bounded device wait expired";
+        case FAVOR_ERR_NOMEM: return "FAVOR_ERR_NOMEM: workspace allocation failed";
+        default: return "unknown favor status";
+    }
+}
+
+extern "C" int favor_stats_enable(int enable) {
+    std::lock_guard<std::mutex> lk(g_rec.mu);
+    g_rec.enabled = enable != 0;
+    if (g_rec.enabled) {
+        g_rec.used = 0;
+        g_rec.launches.store(0);
+        g_rec.kernel = "";
+    }
+    return FAVOR_OK;
+}
+
+extern "C" int favor_stats_read(favor_stats_t *out) {
+    if (!out) return FAVOR_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(g_rec.mu);
+    double total = 0.0;
+    for (size_t i = 0; i + 1 < g_rec.used; i += 2) {
+        if (cudaEventSynchronize(g_rec.ev[i + 1]) != cudaSuccess) return FAVOR_ERR_CUDA;
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, g_rec.ev[i], g_rec.ev[i + 1]) != cudaSuccess)
+            return FAVOR_ERR_CUDA;
+        total += ms;
+    }
+    out->dominant_ms = total;
+    out->dominant_launches = (int)(g_rec.used / 2);
+    out->kernel_launches = g_rec.launches.load();
+    out->dominant_kernel = g_rec.kernel;
+    return FAVOR_OK;
+}
+
+extern "C" void favor_release_workspace(void) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    int cur = 0;
+    cudaGetDevice(&cur);
+    for (int dev = 0; dev < kMaxDevices; ++dev) {
+        DeviceState &s = g_dev[dev];
+        if (!s.ws && !s.stage) continue;
+        cudaSetDevice(dev);
+        cudaDeviceSynchronize();
+        if (s.ws) cudaFree(s.ws);
+        if (s.stage) cudaFree(s.stage);
+        s.ws = s.stage = nullptr;
+        s.ws_bytes = s.stage_bytes = 0;
+    }
+    cudaSetDevice(cur);
+}

@@ -1,0 +1,71 @@
+// favor_internal.h -- declarations shared by the libfavor translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "favor.h"
+
+namespace favor {
+
+// Problem description after host validation.
+struct Problem {
+    int B, H, L, d, dv, m;
+    int causal;
+    int map;      // favor_feature_map_t
+    int nproj;    // projections per token: m (positive, trig) or d (elu1)
+    int r;        // feature columns: m, 2m or d
+    int BH;       // B * H
+};
+
+int make_problem(int B, int H, int L, int d, int dv, int m, int causal, int map, Problem *p);
+int check_ptr(const void *p, bool allow_null);
+
+// Per-device workspace, grown on demand.  Returns nullptr on failure.
+void *workspace(size_t bytes, int *status);
+// Device status word (FAVOR_OK / FAVOR_ERR_TIMEOUT), written by bounded waits.
+int *device_status_ptr();
+
+// Bump allocator over a workspace block (256-byte aligned slices).
+struct Carve {
+    char *base;
+    size_t off;
+    template <typename T> T *take(size_t count) {
+        size_t bytes = (count * sizeof(T) + 255) & ~size_t(255);
+        T *p = reinterpret_cast<T *>(base + off);
+        off += bytes;
+        return p;
+    }
+};
+template <typename T> size_t carve_bytes(size_t count) {
+    return (count * sizeof(T) + 255) & ~size_t(255);
+}
+
+// SIMT path (fp32 arithmetic; input element type float or bf16 bits).
+int simt_forward(const void *q, const void *k, const void *v, bool bf16_in, const float *omega,
+                 float *out, const Problem &p, cudaStream_t stream);
+int simt_feature_map(const void *x, bool bf16_in, const float *omega, float *phi,
+                     float *log_scale, const Problem &p, cudaStream_t stream);
+
+// Tensor-core path (tcgen05, fp16 operands, fp32 accumulation); returns
+// FAVOR_ERR_UNSUPPORTED for shapes it does not cover.
+bool tc_supported(const Problem &p);
+int tc_forward(const void *q, const void *k, const void *v, const float *omega, float *out,
+               const Problem &p, cudaStream_t stream);
+
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? FAVOR_OK : FAVOR_ERR_CUDA; }
+
+// Measurement hook: event pair around the dominant kernel, launch counter.
+void stats_begin(cudaStream_t s, const char *kernel);
+void stats_end(cudaStream_t s);
+void stats_count_launch();
+
+}  // namespace favor
+
+#define FAVOR_LAUNCH_CHECK()                                      \
+    do {                                                          \
+        cudaError_t e_ = cudaGetLastError();                      \
+        if (e_ != cudaSuccess) return FAVOR_ERR_CUDA;             \
+        ::favor::stats_count_launch();                            \
+    } while (0)

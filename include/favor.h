@@ -1,0 +1,144 @@
+/*
+ * favor.h -- C ABI of libfavor, the GB300 (sm_103a) FAVOR+ attention forward pass.
+ *
+ * What is computed (per head h, b):
+ *
+ *   positive random features (FAVOR+)
+ *     phi(x) = exp(-|x|^2/2)/sqrt(m) [exp(w_1.x), ..., exp(w_m.x)]          (r = m)
+ *       -- "Linear Attention > Performer: Unbiased Softmax Approximation", the
+ *          phi(x) equation; "Linear Attention > Kernel Feature Maps", section 4.
+ *   random Fourier features
+ *     phi(x) = 1/sqrt(m) [sin(w_1.x), cos(w_1.x), ..., sin(w_m.x), cos(w_m.x)]  (r = 2m)
+ *       -- "Kernel Feature Maps", section 3.
+ *   ELU + 1
+ *     phi(x)_j = x_j + 1 (x_j > 0), exp(x_j) (x_j <= 0), no projection     (r = d, m must equal d)
+ *       -- "Kernel Feature Maps", section 1.
+ *
+ *   non-causal:  out_i = phi(q_i)^T (sum_j phi(k_j) v_j^T) / phi(q_i)^T (sum_j phi(k_j))
+ *       -- Performer page In[25] (performer_attention, with eps = 0) and the
+ *          Performer study notes, "Core points" steps 4-5.
+ *   causal:      S_i = sum_{j<=i} phi(k_j) v_j^T,  z_i = sum_{j<=i} phi(k_j),
+ *                out_i = phi(q_i)^T S_i / phi(q_i)^T z_i   (diagonal included)
+ *       -- Performer study notes, "Case 2: the causal version" (prefix sum),
+ *          with the linear denominator of "Core points" step 5.
+ *
+ * Every kernel stabilises the exponentials (a per-row query maximum and a
+ * per-head running key maximum); both cancel exactly in the ratio, so the
+ * result is the definition above.
+ *
+ * Conventions common to all entry points
+ *   - All tensors are dense, row-major, contiguous:
+ *       q, k   [B][H][L][d]
+ *       v      [B][H][L][dv]
+ *       omega  [H][m][d]  fp32, one random projection per head, shared by the
+ *              batch (rows w_i; drawn by the caller, iid N(0,I) or
+ *              block-orthogonal).  Ignored (may be NULL) for FAVOR_MAP_ELU1.
+ *       out    [B][H][L][dv] fp32.
+ *   - Device pointers must be 16-byte aligned; out must not alias an input.
+ *   - The caller owns every buffer and the stream.  The library owns a
+ *     per-device workspace that it grows on demand (cudaMalloc outside any
+ *     stream capture) and frees in favor_release_workspace().
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream) unless
+ *     stated otherwise.  Argument errors are detected on the host and
+ *     returned before anything is launched.  A launch failure returns
+ *     FAVOR_ERR_CUDA.  Kernels that wait on an mbarrier give up after a
+ *     bounded number of polls and record FAVOR_ERR_TIMEOUT in a device status
+ *     word that favor_get_device_status() reads.
+ *   - Supported: B, H, L >= 1; d, dv in {32, 64, 128}; m >= 1 and m % 16 == 0
+ *     (positive, trig); m == d (elu1).  B*H*L*max(d,dv) must fit in int32
+ *     element offsets per tensor (checked).
+ */
+#ifndef FAVOR_H
+#define FAVOR_H
+
+#include <cuda_runtime.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FAVOR_OK = 0,
+    FAVOR_ERR_INVALID_ARG = -1, /* null pointer, bad size, misalignment, aliasing */
+    FAVOR_ERR_UNSUPPORTED = -2, /* valid but outside the supported shapes       */
+    FAVOR_ERR_CUDA = -3,        /* a CUDA runtime call or launch failed          */
+    FAVOR_ERR_TIMEOUT = -4,     /* a bounded device-side wait expired            */
+    FAVOR_ERR_NOMEM = -5        /* workspace allocation failed                   */
+} favor_status_t;
+
+typedef enum {
+    FAVOR_MAP_POSITIVE = 0, /* FAVOR+ positive random features, r = m  */
+    FAVOR_MAP_TRIG = 1,     /* sin/cos random Fourier features, r = 2m */
+    FAVOR_MAP_ELU1 = 2      /* elu(x) + 1, r = d (m must equal d)      */
+} favor_feature_map_t;
+
+/* FAVOR attention forward, bf16 q/k/v (raw bf16 bit patterns), fp32 omega
+ * and fp32 out, all device pointers.  causal: 0 = non-causal contraction,
+ * 1 = causal prefix-state form.  feature_map: favor_feature_map_t.
+ * The hot path: tcgen05 tensor-core kernels with fp16 operands and fp32
+ * accumulation.  Returns favor_status_t. */
+int favor_attn_forward(const void *q, const void *k, const void *v, const float *omega,
+                       float *out, int B, int H, int L, int d, int dv, int m, int causal,
+                       int feature_map, cudaStream_t stream);
+
+/* Same operation and parameters with fp32 q/k/v: computed entirely in fp32
+ * (FFMA, accurate expf/sincosf) by SIMT kernels.  Returns favor_status_t. */
+int favor_attn_forward_f32(const float *q, const float *k, const float *v, const float *omega,
+                           float *out, int B, int H, int L, int d, int dv, int m, int causal,
+                           int feature_map, cudaStream_t stream);
+
+/* End-to-end variant of favor_attn_forward on HOST buffers (q/k/v bf16 bits,
+ * omega and out fp32; pinned memory gives the fastest copies).  Copies the
+ * inputs to a library-owned device staging area on `stream`, runs the
+ * forward pass, copies out back and synchronises `stream` before returning.
+ * Not for use inside a stream capture.  Returns favor_status_t. */
+int favor_attn_forward_host(const void *q, const void *k, const void *v, const float *omega,
+                            float *out, int B, int H, int L, int d, int dv, int m, int causal,
+                            int feature_map, cudaStream_t stream);
+
+/* The feature map alone (test and inspection aid), bf16 x [B][H][L][d]:
+ * phi [B][H][L][r] fp32 and log_scale [B][H][L] fp32 such that the exact
+ * feature is phi * exp(log_scale) (phi is the stabilised feature: for the
+ * positive map the row maximum of phi is 1).  r follows feature_map; the trig
+ * features come in the printed interleaved order.  is_key is accepted for
+ * symmetry and does not change the result.  Returns favor_status_t. */
+int favor_feature_map(const void *x, const float *omega, float *phi, float *log_scale, int B,
+                      int H, int L, int d, int m, int feature_map, int is_key,
+                      cudaStream_t stream);
+
+/* Synchronises `stream`, returns and clears the device status word
+ * (FAVOR_OK or FAVOR_ERR_TIMEOUT), or FAVOR_ERR_CUDA if the sync failed. */
+int favor_get_device_status(cudaStream_t stream);
+
+/* Human-readable name of a favor_status_t value (static string). */
+const char *favor_strerror(int status);
+
+/* Frees the workspace of every device this process used (synchronises the
+ * device first).  The next forward call re-allocates. */
+void favor_release_workspace(void);
+
+/* Number of feature columns r for a map, or -1 if the arguments are invalid. */
+int favor_feature_dim(int feature_map, int d, int m);
+
+/* Measurement hook (no counterpart on the pages): while enabled, every
+ * forward call records a CUDA event pair on its stream around its dominant
+ * kernel (the causal scan, or the non-causal output kernel), and every
+ * kernel launch of the library is counted.  favor_stats_enable(1) starts a
+ * fresh recording, favor_stats_enable(0) stops it.  favor_stats_read()
+ * synchronises the recorded events and reports the summed dominant-kernel
+ * time (ms), the number of timed launches and the kernel launches counted
+ * since recording started.  Host-side state, one recorder per process. */
+typedef struct {
+    double dominant_ms;
+    int dominant_launches;
+    long long kernel_launches;
+    const char *dominant_kernel; /* name of the kernel the events bracket */
+} favor_stats_t;
+int favor_stats_enable(int enable);
+int favor_stats_read(favor_stats_t *out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FAVOR_H */

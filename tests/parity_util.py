@@ -1,0 +1,89 @@
+"""Helpers shared by the GPU parity tests: move seeded inputs to the device,
+call the library through its C ABI, and measure the per-row normwise error
+against the float64 oracle."""
+import numpy as np
+
+import favor_random_feature_gb300 as fv
+from favor_inputs import MAP_ELU1, MAP_TRIG
+
+
+def to_device(inp):
+    import torch
+    w = inp.w
+    if w.dtype == "bf16":
+        conv = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(
+            torch.bfloat16).cuda()
+    else:
+        conv = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+    om = None
+    if inp.omega is not None and w.feature_map != MAP_ELU1:
+        om = torch.from_numpy(np.ascontiguousarray(inp.omega, dtype=np.float32)).cuda()
+    return conv(inp.q), conv(inp.k), conv(inp.v), om
+
+
+def run_gpu(inp, causal, feature_map, entry=None):
+    """Run the forward pass through the C ABI; returns out as float64 numpy."""
+    import torch
+    w = inp.w
+    q, k, v, om = to_device(inp)
+    out = torch.full((w.B, w.H, w.L, w.dv), float("nan"), dtype=torch.float32, device="cuda")
+    m = w.d if feature_map == MAP_ELU1 else w.m
+    if entry is None:
+        entry = fv.favor_attn_forward if w.dtype == "bf16" else fv.favor_attn_forward_f32
+    stream = torch.cuda.current_stream()
+    rc = entry(q, k, v, om, out, w.B, w.H, w.L, w.d, w.dv, m, int(causal), feature_map, stream)
+    assert rc == fv.FAVOR_OK, fv.strerror(rc)
+    st = fv.favor_get_device_status(stream)
+    assert st == fv.FAVOR_OK, fv.strerror(st)
+    return out.cpu().numpy().astype(np.float64)
+
+
+def oracle_ref(inp, causal, feature_map, heads=None, return_den=False):
+    import oracle
+    om = None if feature_map == MAP_ELU1 else inp.omega
+    return oracle.forward(inp.q32, inp.k32, inp.v32, om, causal=causal,
+                          feature_map=feature_map, heads=heads, return_den=return_den)
+
+
+def row_errors(out, ref):
+    """e_i = |o_i - ref_i|_2 / |ref_i|_2 per row (rows of ref that are NaN are skipped)."""
+    out = out.reshape(-1, out.shape[-1])
+    ref = ref.reshape(-1, ref.shape[-1])
+    keep = ~np.isnan(ref).any(axis=1)
+    out, ref = out[keep], ref[keep]
+    assert np.isfinite(out).all(), "non-finite GPU output"
+    return np.linalg.norm(out - ref, axis=1) / np.linalg.norm(ref, axis=1)
+
+
+def trig_condition(inp, heads=None):
+    """kappa_i = (|phi(q_i)|^T sum_j |phi(k_j)|) / |phi(q_i)^T z| for the trig map
+    (non-causal sums), used to select well-conditioned rows."""
+    import oracle
+    w = inp.w
+    BH = w.B * w.H
+    q = inp.q32.reshape(BH, w.L, w.d)
+    k = inp.k32.reshape(BH, w.L, w.d)
+    kap = np.full((BH, w.L), np.inf)
+    for bh in (range(BH) if heads is None else heads):
+        om = inp.omega[bh % w.H]
+        pq = oracle.features(q[bh], om, MAP_TRIG)
+        pk = oracle.features(k[bh], om, MAP_TRIG)
+        kap[bh] = (np.abs(pq) @ np.abs(pk).sum(0)) / np.abs(pq @ pk.sum(0))
+    return kap.reshape(w.B, w.H, w.L)
+
+
+def causal_trig_condition(inp, heads=None):
+    import oracle
+    w = inp.w
+    BH = w.B * w.H
+    q = inp.q32.reshape(BH, w.L, w.d)
+    k = inp.k32.reshape(BH, w.L, w.d)
+    kap = np.full((BH, w.L), np.inf)
+    for bh in (range(BH) if heads is None else heads):
+        om = inp.omega[bh % w.H]
+        pq = oracle.features(q[bh], om, MAP_TRIG)
+        pk = oracle.features(k[bh], om, MAP_TRIG)
+        zabs = np.cumsum(np.abs(pk), axis=0)
+        z = np.cumsum(pk, axis=0)
+        kap[bh] = np.sum(np.abs(pq) * zabs, axis=1) / np.abs(np.sum(pq * z, axis=1))
+    return kap.reshape(w.B, w.H, w.L)

@@ -1,0 +1,222 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the float64
+oracle on the same seeded inputs and the same omega.
+
+Metric (per row): e_i = |o_i - ref_i|_2 / |ref_i|_2.
+  fp32 inputs: max_i e_i <= 1e-4.
+  bf16 inputs: max_i e_i <= 2e-2 and mean_i e_i <= 2e-3.
+Trig rows are compared where the denominator is well conditioned
+(kappa <= 10); the others are only checked to be finite.
+"""
+import numpy as np
+import pytest
+
+from favor_inputs import (CAUSAL8K, DEMO64, LONG64K, MAP_ELU1, MAP_POSITIVE, MAP_TRIG, NC4096,
+                          SWEEP16K, make_inputs, sweep_variants)
+from parity_util import (causal_trig_condition, oracle_ref, row_errors, run_gpu, to_device,
+                         trig_condition)
+
+pytestmark = pytest.mark.gpu
+
+F32_MAX = 1e-4
+BF16_MAX = 2e-2
+BF16_MEAN = 2e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from favor_random_feature_gb300 import build
+    build.build()
+
+
+def check_bf16(e, what):
+    assert e.max() <= BF16_MAX and e.mean() <= BF16_MEAN, \
+        f"{what}: max {e.max():.3e} mean {e.mean():.3e}"
+
+
+# ---------------------------------------------------------------------------
+# fp32 entry point: the page's demo (B=H=1, L=64, d=32, m=256), 1e-4
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("fmap", [MAP_POSITIVE, MAP_TRIG, MAP_ELU1])
+def test_demo64_fp32(causal, fmap):
+    w = DEMO64.with_(feature_map=fmap, m=32 if fmap == MAP_ELU1 else 256)
+    inp = make_inputs(w)
+    out = run_gpu(inp, causal, fmap)
+    ref = oracle_ref(inp, causal, fmap)
+    e = row_errors(out, ref)
+    assert e.max() <= F32_MAX, e.max()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp32_multihead_ragged(causal):
+    w = NC4096.with_(dtype="f32")
+    inp = make_inputs(w, L=333, B=2, H=3)
+    e = row_errors(run_gpu(inp, causal, MAP_POSITIVE), oracle_ref(inp, causal, MAP_POSITIVE))
+    assert e.max() <= F32_MAX, e.max()
+
+
+# ---------------------------------------------------------------------------
+# bf16 entry point, reduced sizes (several 128-token tiles + a ragged tail)
+# ---------------------------------------------------------------------------
+REDUCED = [
+    (NC4096, False, 1000),
+    (CAUSAL8K, True, 1000),
+    (LONG64K, True, 1300),
+    (LONG64K, False, 1300),
+]
+
+
+@pytest.mark.parametrize("w,causal,L", REDUCED, ids=lambda x: getattr(x, "name", str(x)))
+def test_bf16_reduced(w, causal, L):
+    inp = make_inputs(w, L=L, B=1, H=3)
+    e = row_errors(run_gpu(inp, causal, MAP_POSITIVE), oracle_ref(inp, causal, MAP_POSITIVE))
+    check_bf16(e, f"{w.name} L={L} causal={causal}")
+
+
+@pytest.mark.parametrize("w", sweep_variants(), ids=lambda w: w.name)
+def test_sweep_reduced(w):
+    inp = make_inputs(w, L=700, B=1, H=2)
+    fmap = w.feature_map
+    out = run_gpu(inp, True, fmap)
+    ref = oracle_ref(inp, True, fmap)
+    if fmap == MAP_TRIG:
+        kap = causal_trig_condition(inp)
+        good = kap <= 10
+        assert np.isfinite(out).all()
+        assert good.mean() > 0.3
+        e = row_errors(out[good][:, None, None, :], ref[good][:, None, None, :])
+    else:
+        e = row_errors(out, ref)
+    check_bf16(e, w.name)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_trig_noncausal_and_causal_small(causal):
+    w = SWEEP16K.with_(m=64, feature_map=MAP_TRIG, d=64, dv=64)
+    inp = make_inputs(w, L=400, B=1, H=2)
+    out = run_gpu(inp, causal, MAP_TRIG)
+    ref = oracle_ref(inp, causal, MAP_TRIG)
+    kap = causal_trig_condition(inp) if causal else trig_condition(inp)
+    good = kap <= 10
+    e = row_errors(out[good][:, None, None, :], ref[good][:, None, None, :])
+    check_bf16(e, "trig")
+
+
+# ---------------------------------------------------------------------------
+# edge cases
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("L", [1, 2, 127, 128, 129, 255, 257])
+@pytest.mark.parametrize("causal", [False, True])
+def test_short_and_ragged_lengths(L, causal):
+    inp = make_inputs(CAUSAL8K, L=L, B=1, H=2)
+    e = row_errors(run_gpu(inp, causal, MAP_POSITIVE), oracle_ref(inp, causal, MAP_POSITIVE))
+    assert e.max() <= BF16_MAX, e.max()
+
+
+@pytest.mark.parametrize("d,dv,m", [(32, 32, 16), (32, 128, 64), (128, 32, 128), (64, 128, 256),
+                                    (128, 64, 32)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_head_dims(d, dv, m, causal):
+    w = CAUSAL8K.with_(d=d, dv=dv, m=m, omega="iid")
+    inp = make_inputs(w, L=300, B=2, H=1)
+    e = row_errors(run_gpu(inp, causal, MAP_POSITIVE), oracle_ref(inp, causal, MAP_POSITIVE))
+    check_bf16(e, f"d={d} dv={dv} m={m}")
+
+
+def test_causal_first_row_is_v0_and_last_row_matches_noncausal():
+    inp = make_inputs(CAUSAL8K, L=300, B=1, H=2)
+    oc = run_gpu(inp, True, MAP_POSITIVE)
+    on = run_gpu(inp, False, MAP_POSITIVE)
+    v0 = inp.v32[:, :, 0].astype(np.float64)
+    assert np.max(np.abs(oc[:, :, 0] - v0)) <= 2e-2 * np.max(np.abs(v0))
+    e = row_errors(oc[:, :, -1:], on[:, :, -1:])
+    assert e.max() <= 1e-2
+
+
+def test_deterministic():
+    inp = make_inputs(CAUSAL8K, L=600, B=1, H=2)
+    a = run_gpu(inp, True, MAP_POSITIVE)
+    b = run_gpu(inp, True, MAP_POSITIVE)
+    assert np.array_equal(a, b)
+
+
+def test_constant_values():
+    inp = make_inputs(CAUSAL8K, L=200, B=1, H=1)
+    from favor_inputs import bf16_bits, bf16_to_f32
+    vals = np.broadcast_to((np.arange(64, dtype=np.float32) - 20) / 8, inp.v32.shape).copy()
+    inp.v = bf16_bits(vals)
+    inp.v32 = bf16_to_f32(inp.v)
+    for causal in (False, True):
+        out = run_gpu(inp, causal, MAP_POSITIVE)
+        assert np.allclose(out, inp.v32, rtol=5e-3, atol=5e-3)
+
+
+# ---------------------------------------------------------------------------
+# the other entry points
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("fmap", [MAP_POSITIVE, MAP_TRIG, MAP_ELU1])
+def test_feature_map_entry(fmap):
+    import torch
+    import favor_random_feature_gb300 as fv
+    import oracle
+    w = CAUSAL8K.with_(feature_map=fmap, m=64 if fmap == MAP_ELU1 else 128)
+    inp = make_inputs(w, L=150, B=1, H=2)
+    q, _, _, om = to_device(inp)
+    r = fv.favor_feature_dim(fmap, w.d, w.m)
+    phi = torch.empty((1, 2, 150, r), dtype=torch.float32, device="cuda")
+    ls = torch.empty((1, 2, 150), dtype=torch.float32, device="cuda")
+    rc = fv.favor_feature_map(q, om, phi, ls, 1, 2, 150, w.d, w.m, fmap, 0,
+                              torch.cuda.current_stream())
+    assert rc == 0
+    got = phi.cpu().numpy().astype(np.float64) * np.exp(ls.cpu().numpy().astype(np.float64))[..., None]
+    for h in range(2):
+        want = oracle.features(inp.q32[0, h], None if fmap == MAP_ELU1 else inp.omega[h], fmap)
+        assert np.allclose(got[0, h], want, rtol=1e-4, atol=1e-6 * np.abs(want).max())
+
+
+def test_host_entry_matches_device_entry():
+    import favor_random_feature_gb300 as fv
+    inp = make_inputs(CAUSAL8K, L=500, B=1, H=2)
+    w = inp.w
+    dev = run_gpu(inp, True, MAP_POSITIVE)
+    out = np.empty((w.B, w.H, w.L, w.dv), dtype=np.float32)
+    om = np.ascontiguousarray(inp.omega, dtype=np.float32)
+    rc = fv.favor_attn_forward_host(inp.q, inp.k, inp.v, om, out, w.B, w.H, w.L, w.d, w.dv,
+                                    w.m, 1, MAP_POSITIVE)
+    assert rc == 0, fv.strerror(rc)
+    assert np.array_equal(out.astype(np.float64), dev)
+
+
+# ---------------------------------------------------------------------------
+# full sizes, in the benchmark's launch configuration; oracle on sampled heads
+# ---------------------------------------------------------------------------
+FULL = [
+    (NC4096, False, [0, 95]),
+    (CAUSAL8K, True, [0, 37, 63]),
+    (LONG64K, True, [0, 7]),
+    (LONG64K, False, [3]),
+]
+
+
+@pytest.mark.parametrize("w,causal,heads", FULL, ids=lambda x: getattr(x, "name", str(x)))
+def test_full_size_sampled_heads(w, causal, heads):
+    inp = make_inputs(w)
+    out = run_gpu(inp, causal, MAP_POSITIVE)
+    ref = oracle_ref(inp, causal, MAP_POSITIVE, heads=heads)
+    BH = w.B * w.H
+    e = row_errors(out.reshape(BH, w.L, w.dv)[heads], ref.reshape(BH, w.L, w.dv)[heads])
+    check_bf16(e, w.name)
+    assert np.isfinite(out).all()
+
+
+@pytest.mark.parametrize("m", [64, 512])
+def test_full_size_sweep_sampled(m):
+    w = SWEEP16K.with_(m=m)
+    inp = make_inputs(w)
+    out = run_gpu(inp, True, MAP_POSITIVE)
+    ref = oracle_ref(inp, True, MAP_POSITIVE, heads=[5])
+    e = row_errors(out.reshape(16, w.L, w.dv)[[5]], ref.reshape(16, w.L, w.dv)[[5]])
+    check_bf16(e, w.name)
