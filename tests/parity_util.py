@@ -87,3 +87,33 @@ def causal_trig_condition(inp, heads=None):
         z = np.cumsum(pk, axis=0)
         kap[bh] = np.sum(np.abs(pq) * zabs, axis=1) / np.abs(np.sum(pq * z, axis=1))
     return kap.reshape(w.B, w.H, w.L)
+
+
+def scaled_inputs(inp, s):
+    """The same inputs with q and k multiplied by s (re-rounded to the storage type)."""
+    import copy
+    from favor_inputs import bf16_bits, bf16_to_f32
+    out = copy.copy(inp)
+    if inp.w.dtype == "bf16":
+        out.q = bf16_bits(inp.q32 * np.float32(s))
+        out.k = bf16_bits(inp.k32 * np.float32(s))
+        out.q32, out.k32 = bf16_to_f32(out.q), bf16_to_f32(out.k)
+    else:
+        out.q = out.q32 = (inp.q32 * np.float32(s)).astype(np.float32)
+        out.k = out.k32 = (inp.k32 * np.float32(s)).astype(np.float32)
+    return out
+
+
+def conditioned_errors(out, ref, kappa, v32):
+    """Error of each row relative to its condition: |o_i - ref_i| /
+    (kappa_i (max_j |v_j| + |ref_i|)).  For a result computed from features
+    perturbed by a relative eps, this is at most about eps, however close the
+    denominator comes to zero (used for the sin/cos map, whose denominators
+    are not bounded away from zero)."""
+    dv = out.shape[-1]
+    o = out.reshape(-1, dv)
+    r = ref.reshape(-1, dv)
+    k = kappa.reshape(-1)
+    vmax = np.linalg.norm(v32.reshape(-1, dv), axis=1).max()
+    assert np.isfinite(o).all(), "non-finite GPU output"
+    return np.linalg.norm(o - r, axis=1) / (k * (vmax + np.linalg.norm(r, axis=1)))
