@@ -224,3 +224,23 @@ def test_full_size_sweep_sampled(m):
     ref = oracle_ref(inp, True, MAP_POSITIVE, heads=[5])
     e = row_errors(out.reshape(16, w.L, w.dv)[[5]], ref.reshape(16, w.L, w.dv)[[5]])
     check_bf16(e, w.name)
+
+
+# ---------------------------------------------------------------------------
+# the bf16 entry point runs the tensor-core kernels for the benchmark shapes
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("w,causal,kernel", [(CAUSAL8K, True, "tc_causal"),
+                                             (NC4096, False, "tc_output"),
+                                             (SWEEP16K.with_(m=128), True, "tc_causal")],
+                         ids=["causal", "noncausal", "d128"])
+def test_tensor_core_path_taken(w, causal, kernel):
+    import favor_random_feature_gb300 as fv
+    inp = make_inputs(w, L=512, B=1, H=2)
+    fv.favor_stats_enable(True)
+    try:
+        run_gpu(inp, causal, MAP_POSITIVE)
+        st = fv.favor_stats_read()
+    finally:
+        fv.favor_stats_enable(False)
+    assert st.dominant_kernel.decode() == kernel
+    assert st.dominant_launches == 1 and st.kernel_launches >= 3
