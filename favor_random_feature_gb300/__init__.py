@@ -29,6 +29,7 @@ FAVOR_MAP_ELU1 = 2
 
 EXPORTS = (
     "favor_attn_forward",
+    "favor_attn_forward_noalloc",
     "favor_attn_forward_f32",
     "favor_attn_forward_host",
     "favor_feature_map",
@@ -65,7 +66,8 @@ def lib() -> ctypes.CDLL:
         L = ctypes.CDLL(LIB_PATH)
         vp, i, fp = ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p
         fwd = [vp, vp, vp, fp, fp] + [i] * 8 + [vp]
-        for name in ("favor_attn_forward", "favor_attn_forward_f32", "favor_attn_forward_host"):
+        for name in ("favor_attn_forward", "favor_attn_forward_f32", "favor_attn_forward_host",
+                     "favor_attn_forward_noalloc"):
             getattr(L, name).argtypes = fwd
             getattr(L, name).restype = i
         L.favor_feature_map.argtypes = [vp, fp, fp, fp] + [i] * 7 + [vp]
@@ -114,6 +116,13 @@ def favor_attn_forward(q, k, v, omega, out, B, H, L, d, dv, m, causal, feature_m
     return lib().favor_attn_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(omega), _ptr(out),
                                     B, H, L, d, dv, m, int(causal), int(feature_map),
                                     _stream(stream))
+
+
+def favor_attn_forward_noalloc(q, k, v, omega, out, B, H, L, d, dv, m, causal, feature_map,
+                               stream=None):
+    return lib().favor_attn_forward_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(omega), _ptr(out),
+                                            B, H, L, d, dv, m, int(causal), int(feature_map),
+                                            _stream(stream))
 
 
 def favor_attn_forward_f32(q, k, v, omega, out, B, H, L, d, dv, m, causal, feature_map,

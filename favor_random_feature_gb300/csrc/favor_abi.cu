@@ -153,8 +153,8 @@ int check_ptr(const void *p, bool allow_null) {
     return is_aligned(p) ? FAVOR_OK : FAVOR_ERR_INVALID_ARG;
 }
 
-static int validate(const void *q, const void *k, const void *v, const float *omega,
-                    const float *out, size_t esize, const Problem &p) {
+int validate_args(const void *q, const void *k, const void *v, const float *omega,
+                  const float *out, size_t esize, const Problem &p) {
     int rc;
     if ((rc = check_ptr(q, false)) || (rc = check_ptr(k, false)) || (rc = check_ptr(v, false)) ||
         (rc = check_ptr(out, false)))
@@ -187,7 +187,7 @@ extern "C" int favor_attn_forward(const void *q, const void *k, const void *v, c
     Problem p;
     int rc = make_problem(B, H, L, d, dv, m, causal, feature_map, &p);
     if (rc) return rc;
-    if ((rc = validate(q, k, v, omega, out, 2, p))) return rc;
+    if ((rc = validate_args(q, k, v, omega, out, 2, p))) return rc;
     if (tc_supported(p)) return tc_forward(q, k, v, omega, out, p, stream);
     return simt_forward(q, k, v, true, omega, out, p, stream);
 }
@@ -199,7 +199,7 @@ extern "C" int favor_attn_forward_f32(const float *q, const float *k, const floa
     Problem p;
     int rc = make_problem(B, H, L, d, dv, m, causal, feature_map, &p);
     if (rc) return rc;
-    if ((rc = validate(q, k, v, omega, out, 4, p))) return rc;
+    if ((rc = validate_args(q, k, v, omega, out, 4, p))) return rc;
     return simt_forward(q, k, v, false, omega, out, p, stream);
 }
 

@@ -53,6 +53,15 @@ int simt_feature_map(const void *x, bool bf16_in, const float *omega, float *phi
 bool tc_supported(const Problem &p);
 int tc_forward(const void *q, const void *k, const void *v, const float *omega, float *out,
                const Problem &p, cudaStream_t stream);
+// Scratch bytes the tensor-core path needs for a problem, and the path run on
+// caller-provided scratch (FAVOR_ERR_UNSUPPORTED if ws_bytes is too small).
+size_t tc_scratch_bytes(const Problem &p);
+int tc_run(const void *q, const void *k, const void *v, const float *omega, float *out,
+           const Problem &p, cudaStream_t stream, void *ws, size_t ws_bytes);
+// Host argument checks shared by the forward entry points (esize = bytes per
+// q/k/v element).
+int validate_args(const void *q, const void *k, const void *v, const float *omega,
+                  const float *out, size_t esize, const Problem &p);
 
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? FAVOR_OK : FAVOR_ERR_CUDA; }
 

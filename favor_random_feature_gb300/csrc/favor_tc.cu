@@ -1289,39 +1289,66 @@ bool tc_supported(const Problem &p) {
     return encoder() != nullptr;
 }
 
-int tc_forward(const void *q, const void *k, const void *v, const float *omega, float *out,
-               const Problem &p, cudaStream_t st) {
+namespace {
+struct Plan {
+    int G, seg_len, nstate, nvb, nchunk;
+    size_t img_bytes, per_state, bytes;
+};
+
+Plan make_plan(const Problem &p) {
     const Geo g = make_geo(p);
-    const int nvb = p.dv / 64;
-    const int nchunk = (p.L + kC - 1) / kC;
+    Plan pl;
+    pl.nvb = p.dv / 64;
+    pl.nchunk = (p.L + kC - 1) / kC;
     const int sms = num_sms();
-    // segments: multiples of 128 tokens
+    // segments: whole 128-token chunks, about one CTA per SM in the scan
     int G;
     if (p.causal) {
-        G = (int)std::lround((double)sms / (p.BH * nvb));
+        G = (int)std::lround((double)sms / (p.BH * pl.nvb));
     } else {
         G = (int)std::lround(2.0 * sms / (p.BH * g.n_ft));
     }
-    G = std::max(1, std::min(G, nchunk));
-    const int seg_chunks = (nchunk + G - 1) / G;
-    G = (nchunk + seg_chunks - 1) / seg_chunks;
-    const int seg_len = seg_chunks * kC;
-    const int nstate = p.causal ? G - 1 : G;
-
-    // workspace
-    const size_t img_bytes = (size_t)p.H * p.nproj * p.d * 2;
-    const size_t per_state = (size_t)p.r * (p.dv + 1);
-    size_t bytes = carve_bytes<uint8_t>(img_bytes) +
-                   carve_bytes<float>((size_t)p.BH * std::max(1, nstate) * per_state) +
-                   carve_bytes<float>((size_t)p.BH * std::max(1, nstate) * g.n_ft * 4);
+    G = std::max(1, std::min(G, pl.nchunk));
+    const int seg_chunks = (pl.nchunk + G - 1) / G;
+    pl.G = (pl.nchunk + seg_chunks - 1) / seg_chunks;
+    pl.seg_len = seg_chunks * kC;
+    pl.nstate = p.causal ? pl.G - 1 : pl.G;
+    pl.img_bytes = (size_t)p.H * p.nproj * p.d * 2;
+    pl.per_state = (size_t)p.r * (p.dv + 1);
+    size_t bytes = carve_bytes<uint8_t>(pl.img_bytes) +
+                   carve_bytes<float>((size_t)p.BH * std::max(1, pl.nstate) * pl.per_state) +
+                   carve_bytes<float>((size_t)p.BH * std::max(1, pl.nstate) * g.n_ft * 4);
     if (p.causal)
-        bytes += carve_bytes<float>((size_t)p.BH * G * per_state) + carve_bytes<float>((size_t)p.BH * G * 4);
+        bytes += carve_bytes<float>((size_t)p.BH * pl.G * pl.per_state) +
+                 carve_bytes<float>((size_t)p.BH * pl.G * 4);
     else
-        bytes += carve_bytes<uint8_t>((size_t)p.BH * nvb * p.r * 128) + carve_bytes<float>((size_t)p.BH * p.r) +
-                 carve_bytes<float>(p.BH);
+        bytes += carve_bytes<uint8_t>((size_t)p.BH * pl.nvb * p.r * 128) +
+                 carve_bytes<float>((size_t)p.BH * p.r) + carve_bytes<float>(p.BH);
+    pl.bytes = bytes;
+    return pl;
+}
+}  // namespace
+
+size_t tc_scratch_bytes(const Problem &p) { return make_plan(p).bytes; }
+
+int tc_forward(const void *q, const void *k, const void *v, const float *omega, float *out,
+               const Problem &p, cudaStream_t st) {
     int status = FAVOR_OK;
+    const size_t bytes = tc_scratch_bytes(p);
     void *ws = workspace(bytes, &status);
     if (!ws) return status;
+    return tc_run(q, k, v, omega, out, p, st, ws, bytes);
+}
+
+int tc_run(const void *q, const void *k, const void *v, const float *omega, float *out,
+           const Problem &p, cudaStream_t st, void *ws, size_t ws_bytes) {
+    const Geo g = make_geo(p);
+    const Plan pl = make_plan(p);
+    if (ws_bytes < pl.bytes) return FAVOR_ERR_UNSUPPORTED;
+    const int nvb = pl.nvb, nchunk = pl.nchunk, G = pl.G, seg_len = pl.seg_len,
+              nstate = pl.nstate;
+    const int sms = num_sms();
+    const size_t img_bytes = pl.img_bytes, per_state = pl.per_state;
     int *dstat = device_status_ptr();
     Carve cv{static_cast<char *>(ws), 0};
     uint8_t *img = cv.take<uint8_t>(img_bytes);

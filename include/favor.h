@@ -81,6 +81,24 @@ int favor_attn_forward(const void *q, const void *k, const void *v, const float 
                        float *out, int B, int H, int L, int d, int dv, int m, int causal,
                        int feature_map, cudaStream_t stream);
 
+/* No counterpart on the pages: favor_attn_forward for callers that must not
+ * allocate device memory on the call path -- a process whose framework has
+ * reserved the GPU's memory in its own caching pool (a further cudaMalloc
+ * fails), or a serving loop that cannot take the device-wide synchronisation
+ * of cudaMalloc/cudaFree mid-request.  Same parameters and result as
+ * favor_attn_forward; it never calls cudaMalloc, cudaFree or an allocating
+ * routine.  Its scratch is a fixed 16 MiB array in the library's device
+ * memory, held on every GPU that loads the library until the process exits.
+ * Returns FAVOR_ERR_UNSUPPORTED for a shape the tensor-core kernels do not
+ * cover or whose scratch (per-head fp16 W image, segment states) exceeds
+ * 16 MiB -- e.g. B=4, H=16, L=8192, d=dv=64, m=256 causal fits.  The first
+ * call on a device looks the array's device address up (make it before any
+ * stream capture).  All calls share the array: calls whose kernels overlap
+ * on the GPU race on it.  Nothing in it needs clearing between calls. */
+int favor_attn_forward_noalloc(const void *q, const void *k, const void *v, const float *omega,
+                               float *out, int B, int H, int L, int d, int dv, int m, int causal,
+                               int feature_map, cudaStream_t stream);
+
 /* Same operation and parameters with fp32 q/k/v: computed entirely in fp32
  * (FFMA, accurate expf/sincosf) by SIMT kernels.  Returns favor_status_t. */
 int favor_attn_forward_f32(const float *q, const float *k, const float *v, const float *omega,
