@@ -194,8 +194,9 @@ __device__ __forceinline__ void sincos_reduced(float x, float &s, float &c) {
 __device__ __forceinline__ float elu1(float p) { return p > 0.f ? p + 1.f : ex2(p * kLog2e); }
 
 // ---------------------------------------------------------------------------
-// W image: fp16, 128B-swizzled K-major blocks [nproj][64] per 64 columns of d,
-// scaled by log2(e) for the positive map; the identity for elu1.
+// W image: fp16, 128B-swizzled MN-major atoms [d][64] per 64 projections
+// (the B operand of P = X W^T with K = d), scaled by log2(e) for the
+// positive map; the identity for elu1.
 // ---------------------------------------------------------------------------
 __global__ void tc_prep_omega(const float *__restrict__ omega, uint8_t *__restrict__ img, int H,
                               int nproj, int d, int map) {
@@ -207,8 +208,8 @@ __global__ void tc_prep_omega(const float *__restrict__ omega, uint8_t *__restri
         float w;
         if (map == FAVOR_MAP_ELU1) w = (p == j) ? 1.f : 0.f;
         else w = omega[(size_t)h * per + e] * (map == FAVOR_MAP_POSITIVE ? kLog2e : 1.f);
-        uint8_t *blk = img + (size_t)h * per * 2 + (size_t)(j / 64) * nproj * 128;
-        *reinterpret_cast<__half *>(blk + sw128_offset(p, j % 64)) = __float2half_rn(w);
+        uint8_t *atom = img + (size_t)h * per * 2 + (size_t)(p / 64) * d * 128;
+        *reinterpret_cast<__half *>(atom + sw128_offset(j, p % 64)) = __float2half_rn(w);
     }
 }
 
@@ -328,17 +329,19 @@ __device__ void key_tile_prepare(uint8_t *xk, int nd, float *nk, float *part) {
 // ---------------------------------------------------------------------------
 // P[:, 128 t .. ] = X W_tile^T for feature tiles [t0, t0 + nt); X K-major
 // [128][d] in nd blocks; W image K-major [nproj][64] per d block.
-// W image in smem: K-major blocks of w_rows rows per 64 columns of d.
+// W image in smem: MN-major atoms [d][64] of 64 projections, the first one
+// holding projection 0 of the image.
 __device__ __forceinline__ void issue_projection(const Geo &g, uint32_t tmem, uint32_t x_s,
                                                  uint32_t w_s, int w_rows, int t0, int nt, int col0) {
-    const uint32_t idesc = idesc_f16(128, g.np_tile, 0, 0);
+    (void)w_rows;
+    const uint32_t idesc = idesc_f16(128, g.np_tile, 0, 1);
     const int nk = g.d / 16;
     for (int t = 0; t < nt; ++t) {
         const int p0 = (t0 + t) * g.np_tile;
         for (int kk = 0; kk < nk; ++kk) {
             uint64_t a = smem_desc(x_s + (kk >> 2) * kBlk + (kk & 3) * 32, 16, 1024);
-            uint64_t b = smem_desc(w_s + (kk >> 2) * (uint32_t)w_rows * 128 + p0 * 128 + (kk & 3) * 32,
-                                   16, 1024);
+            uint64_t b = smem_desc(w_s + (p0 / 64) * (uint32_t)g.d * 128 + kk * 2048,
+                                   (uint32_t)g.d * 128, 1024);
             mma_f16(tmem + col0 + 128 * t, a, b, idesc, kk > 0);
         }
     }
@@ -420,13 +423,10 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     bool alive = true;
 
     if (threadIdx.x == 0) {
-        // W rows of this feature tile: np_tile rows per d block
-        const uint32_t wbytes = (uint32_t)g.np_tile * 128;
-        mbar_arrive_expect_tx(&bars[0], wbytes * nd);
-        for (int b = 0; b < nd; ++b)
-            bulk_load(w + b * wbytes, a.omg + (size_t)head * g.nproj * g.d * 2 +
-                                          (size_t)b * g.nproj * 128 + (size_t)ft * wbytes,
-                      wbytes, &bars[0]);
+        // W atoms of this feature tile (np_tile projections, contiguous)
+        const uint32_t wbytes = (uint32_t)g.np_tile * g.d * 2;
+        mbar_arrive_expect_tx(&bars[0], wbytes);
+        bulk_load(w, a.omg + (size_t)head * g.nproj * g.d * 2 + (size_t)ft * wbytes, wbytes, &bars[0]);
         if (nchunk > 0) {
             mbar_arrive_expect_tx(&bars[1], kBlk * nd);
             for (int b = 0; b < nd; ++b) tma_load_3d(xk + b * kBlk, &tm_k, &bars[1], 64 * b, t_begin, bh);
@@ -875,315 +875,613 @@ tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
 }
 
 // ---------------------------------------------------------------------------
-// tc_causal: the chunked causal scan.  Grid (segments, dv tiles, heads).
-// TMEM columns: P / A [0, 256), A V at [128, 192), phi_Q S at [256, 320),
-// state tiles [320 + 96 t, ...): 64 values, then z (the MMA writes 16 copies
-// of z; the slot keeps 32 columns so 32-wide loads and stores stay inside it).
+// tc_causal: the chunked causal scan, warp-specialised.
+// Grid (segments, dv tiles, heads); 544 threads:
+//   warp 0, lane 0  -- issues every TMA copy and tcgen05 MMA in order, waiting
+//                      on mbarriers for the buffers it reuses;
+//   warps 1..16     -- the epilogue group (512 threads, named barrier 1); warp
+//                      w serves TMEM lane quarter w % 4 and column quarter
+//                      (w - 1) / 4.
+// Per chunk the tensor core runs: P_K = K W^T and P_Q = Q W^T (N = all
+// projections); one N = 144 MMA with A = phi(Q) from TMEM against the rows
+// [phi(K); sigma z^T] -> [A | phi_Q z]; phi_Q (sigma S) (N = 64, the state
+// operand MN-major); A V with the row-scaled masked A from TMEM; and
+// S += phi(K)^T [V | 1] (N = 80) per 128 features.  The epilogue turns projections into features, the state into
+// its fp16 operand rows, A into its masked, row-scaled fp16 form, and the
+// accumulators into out.
 // ---------------------------------------------------------------------------
+constexpr int kEpi = 512;
+constexpr int kCausalThreads = 32 + kEpi;
+constexpr int kKbRows = 144;                     // phi_K keys 128 | z 1 | pad 15
+constexpr uint32_t kKbBlk = kKbRows * 128;       // one 64-feature block of the KB operand
+
 struct CausalArgs {
     Geo g;
     int H, L, seg_len, nseg;
-    const uint8_t *omg;
+    const uint8_t *omg;            // MN-major W images
     const float *s_in, *meta_in;   // [BH][nseg][r][dv+1], [BH][nseg][4] (segment 0 unused)
     int *status;
-    uint32_t o_w, o_xq, o_xk, o_xv, o_phq, o_phk, o_ones, o_small, tmem_cols;
+    uint32_t o_w, o_x, o_v, o_kb, o_sop, o_small, tmem_cols;
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
-tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_out,
-          const CausalArgs a) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+// TMEM columns: P [0, 256) | phi_Q packed [0, r/2) | B [0, 64) | D_I [64, 128) |
+// A [128, 256) | phi_Q z [256, 272) | phi_Q S [272, 336) | state tiles
+constexpr int kColP = 0, kColB = 0, kColDI = 64, kColBig = 128, kColDD = 256, kColDX = 272,
+              kColS = 336, kSStride = 80;
+
+__device__ __forceinline__ float grp_max(float v, float *red, int ew) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    group_sync(kEpi);
+    if ((threadIdx.x & 31) == 0) red[ew] = v;
+    group_sync(kEpi);
+    float r = red[0];
+#pragma unroll
+    for (int i = 1; i < kEpi / 32; ++i) r = fmaxf(r, red[i]);
+    return r;
+}
+
+// Bounded mbarrier wait that also gives up at once when another thread of
+// the CTA has already timed out (*abort set), so that every thread keeps
+// running the same sequence of group barriers and the kernel still ends.
+__device__ __forceinline__ bool ewait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort) return false;
+        if (clock64() - t0 > kWaitLimit) {
+            *abort = 1;
+            return false;
+        }
+    }
+    return true;
+}
+
+// (max of a, sum of b) over the epilogue group; red holds 32 floats
+__device__ __forceinline__ void grp_maxsum(float a, float b, float *red, int ew, float &mx, float &sm) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+        b += __shfl_xor_sync(0xffffffffu, b, o);
+    }
+    group_sync(kEpi);
+    if ((threadIdx.x & 31) == 0) {
+        red[ew] = a;
+        red[16 + ew] = b;
+    }
+    group_sync(kEpi);
+    mx = red[0];
+    sm = 0.f;
+#pragma unroll
+    for (int i = 0; i < kEpi / 32; ++i) {
+        mx = fmaxf(mx, red[i]);
+        sm += red[16 + i];
+    }
+}
+
+__device__ __forceinline__ float grp_sum(float v, float *red, int ew) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    group_sync(kEpi);
+    if ((threadIdx.x & 31) == 0) red[ew] = v;
+    group_sync(kEpi);
+    float r = 0.f;
+#pragma unroll
+    for (int i = 0; i < kEpi / 32; ++i) r += red[i];
+    return r;
+}
+
+// In-place bf16 -> fp16 conversion of a [128][64 nblk] tile by 512 threads:
+// thread e converts two 16-byte chunks of row e % 128 per block (chunk index
+// rotated with the row).  Returns the partial sum of squares and max |x|.
+__device__ __forceinline__ float convert_tile_512(uint8_t *tile, int nblk, int e, float &amax) {
+    const int row = e & 127, part = e >> 7;
+    float sumsq = 0.f;
+    amax = 0.f;
+    for (int b = 0; b < nblk; ++b) {
+        uint8_t *rp = tile + b * kBlk + row * 128;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int p = (part * 2 + c + row) & 7;
+            uint4 *ptr = reinterpret_cast<uint4 *>(rp + p * 16);
+            uint4 u = *ptr;
+            uint32_t w[4] = {u.x, u.y, u.z, u.w}, o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
+                sumsq = fmaf(lo, lo, fmaf(hi, hi, sumsq));
+                amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
+                o[i] = pack_half2(lo, hi);
+            }
+            *ptr = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+    return sumsq;
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[N]) {
+    static_assert(N == 16 || N == 32, "");
+    if constexpr (N == 32) tmem_ld32(taddr, v);
+    else tmem_ld16(taddr, v);
+}
+
+// 8 fp16 features (one 16-byte chunk) of a key row into the KB operand
+__device__ __forceinline__ void kb_store8(uint8_t *kb, int row, int f, const float *v) {
+    uint4 u = make_uint4(pack_half2(v[0], v[1]), pack_half2(v[2], v[3]), pack_half2(v[4], v[5]),
+                         pack_half2(v[6], v[7]));
+    *reinterpret_cast<uint4 *>(kb + (size_t)(f >> 6) * kKbBlk + sw128_offset(row, f & 63)) = u;
+}
+
+// NC = projection columns per epilogue thread (a quarter of the projections)
+template <int NC>
+__device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
+                            const CUtensorMap *tm_q, const CUtensorMap *tm_k,
+                            const CUtensorMap *tm_v, const CUtensorMap *tm_out) {
     const Geo &g = a.g;
     const int seg = blockIdx.x, dvt = blockIdx.y, bh = blockIdx.z, head = bh % a.H;
     const int t_begin = seg * a.seg_len, t_end = min(a.L, t_begin + a.seg_len);
     const int nchunk = (t_end - t_begin + kC - 1) / kC;
     const int nd = g.d / 64, nft = g.n_ft;
-    uint8_t *w = sm + a.o_w, *xq = sm + a.o_xq, *xk = sm + a.o_xk, *xv = sm + a.o_xv,
-            *phq = sm + a.o_phq, *phk = sm + a.o_phk, *ones = sm + a.o_ones;
-    uint8_t *sop = xq;      // state operand [r][64] fp16 (aliases the Q and K tiles)
-    uint8_t *bhat = phq;    // normalised intra-chunk matrix (aliases phi_Q)
-    uint8_t *stage = phk;   // output staging (aliases phi_K)
+    const uint32_t xb = (uint32_t)kC * g.d * 2;
+    uint8_t *w = sm + a.o_w, *xq = sm + a.o_x, *xk = xq + xb, *xv = sm + a.o_v, *kb = sm + a.o_kb,
+            *sop = sm + a.o_sop;
+    uint8_t *stage = sop;  // output staging aliases the state operand (dead after phi_Q S)
     float *small = reinterpret_cast<float *>(sm + a.o_small);
-    float *zs = small;                  // [256]
-    float *nk = small + 256;            // [128]
-    float *part = small + 384;          // [256]
-    float *dpart = small + 640;         // [256] den_inter partials
-    float *rho = small + 896;           // [128]
-    float *deni = small + 1024;         // [128]
-    float *red = small + 1152;          // [8]
-    float *sc = small + 1160;           // scalars: 0 R, 1 zmax, 2 vmax, 3 alpha_pending
-    uint64_t *bars = reinterpret_cast<uint64_t *>(small + 1168);   // 0 w, 1 qk, 2 v, 3 mma
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(small + 1184);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = warp & 3, h = warp >> 2;
-    const int row = q * 32 + lane;
-    const int col_a = 0, col_da = 128, col_di = 256, col_s = 320, s_stride = 96;
+    float *nk = small;             // [128]
+    float *part = small + 128;     // [4][128]
+    float *part2 = small + 640;    // [4][128]
+    float *red = small + 1152;     // [32]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(small + 1184);
+    uint64_t *bar_w = &bars[0], *bar_x = &bars[1], *bar_v = &bars[2], *bar_pk = &bars[3],
+             *bar_pq = &bars[4], *bar_a = &bars[5], *bar_av = &bars[6], *bar_avs = &bars[7];
+    uint64_t *e_x = &bars[8], *e_k = &bars[9], *e_sop = &bars[10], *e_q = &bars[11],
+             *e_v = &bars[12], *e_b = &bars[13], *e_out = &bars[14];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    volatile int *abortp = reinterpret_cast<volatile int *>(small + 1224);
+    bool alive = true;
 
-    for (int i = threadIdx.x; i < 4096 / 16; i += kThreads)
-        reinterpret_cast<uint4 *>(ones)[i] = make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
-        fence_mbar_init();
+    if (warp == 0) {
+        // ======================= control thread =======================
+        if (lane == 0) {
+            const uint32_t w_s = smem_u32(w), xq_s = smem_u32(xq), xk_s = smem_u32(xk),
+                           v_s = smem_u32(xv), kb_s = smem_u32(kb), sop_s = smem_u32(sop);
+            const uint32_t wbytes = (uint32_t)g.nproj * g.d * 2;
+            auto load_x = [&](int c) {
+                mbar_arrive_expect_tx(bar_x, 2 * xb);
+                for (int b = 0; b < nd; ++b) {
+                    tma_load_3d(xq + b * kBlk, tm_q, bar_x, 64 * b, t_begin + c * kC, bh);
+                    tma_load_3d(xk + b * kBlk, tm_k, bar_x, 64 * b, t_begin + c * kC, bh);
+                }
+            };
+            auto load_v = [&](int c) {
+                mbar_arrive_expect_tx(bar_v, kBlk);
+                tma_load_3d(xv, tm_v, bar_v, 64 * dvt, t_begin + c * kC, bh);
+            };
+            // P = X W^T over all projections (W MN-major: atoms of 64 projections)
+            auto issue_proj = [&](uint32_t x_s) {
+                const uint32_t idesc = idesc_f16(128, g.nproj, 0, 1);
+                for (int kk = 0; kk < g.d / 16; ++kk)
+                    mma_f16(tmem + kColP, smem_desc(x_s + (kk >> 2) * kBlk + (kk & 3) * 32, 16, 1024),
+                            smem_desc(w_s + kk * 2048, (uint32_t)g.d * 128, 1024), idesc, kk > 0);
+            };
+            if (nchunk > 0) {
+                mbar_arrive_expect_tx(bar_w, wbytes);
+                bulk_load(w, a.omg + (size_t)head * wbytes, wbytes, bar_w);
+                load_x(0);
+                load_v(0);
+                alive = ewait(bar_w, 0, abortp);
+            }
+            for (int c = 0; c < nchunk && alive; ++c) {
+                const uint32_t ph = c & 1;
+                if (c == 0) {
+                    if (!(alive = ewait(e_x, 0, abortp))) break;
+                    tc_fence_after();
+                    issue_proj(xk_s);
+                    mma_commit(bar_pk);
+                }
+                if (!(alive = ewait(e_k, ph, abortp))) break;
+                tc_fence_after();
+                issue_proj(xq_s);
+                mma_commit(bar_pq);
+                if (!(alive = ewait(bar_pq, ph, abortp))) break;
+                if (c + 1 < nchunk) load_x(c + 1);
+                // [A | phi_Q z] = phi_Q [phi_K ; z]^T and phi_Q (sigma S)
+                if (!(alive = ewait(e_sop, ph, abortp))) break;
+                if (!(alive = ewait(e_q, ph, abortp))) break;
+                tc_fence_after();
+                {
+                    const uint32_t idesc = idesc_f16(128, kKbRows, 0, 0);
+                    for (int kk = 0; kk < g.r / 16; ++kk)
+                        mma_f16_ts(tmem + kColBig, tmem + 8 * kk,
+                                   smem_desc(kb_s + (kk >> 2) * kKbBlk + (kk & 3) * 32, 16, 1024), idesc, kk > 0);
+                    const uint32_t idx = idesc_f16(128, 64, 0, 1);
+                    for (int kk = 0; kk < g.r / 16; ++kk)
+                        mma_f16_ts(tmem + kColDX, tmem + 8 * kk, smem_desc(sop_s + kk * 2048, kBlk, 1024), idx, kk > 0);
+                }
+                mma_commit(bar_a);
+                // A V and S += phi_K^T [V | 1]
+                if (!(alive = ewait(e_v, ph, abortp))) break;
+                if (!(alive = ewait(e_b, ph, abortp))) break;
+                tc_fence_after();
+                {
+                    const uint32_t idv = idesc_f16(128, 64, 0, 1);
+                    for (int kk = 0; kk < kC / 16; ++kk)
+                        mma_f16_ts(tmem + kColDI, tmem + kColB + 8 * kk, smem_desc(v_s + kk * 2048, kBlk, 1024), idv, kk > 0);
+                    mma_commit(bar_av);
+                    const uint32_t ids = idesc_f16(128, 80, 1, 1);
+                    for (int t = 0; t < nft; ++t)
+                        for (int kk = 0; kk < kC / 16; ++kk)
+                            mma_f16(tmem + kColS + t * kSStride,
+                                    smem_desc(kb_s + (2 * t) * kKbBlk + kk * 2048, kKbBlk, 1024),
+                                    smem_desc(v_s + kk * 2048, kBlk, 1024), ids, 1);
+                }
+                mma_commit(bar_avs);
+                if (c + 1 < nchunk) {
+                    // next chunk's key projection once D_I has been read (A V done)
+                    if (!(alive = ewait(e_x, (c + 1) & 1, abortp))) break;
+                    if (!(alive = ewait(e_out, ph, abortp))) break;
+                    tc_fence_after();
+                    issue_proj(xk_s);
+                    mma_commit(bar_pk);
+                    if (!(alive = ewait(bar_avs, ph, abortp))) break;
+                    load_v(c + 1);
+                }
+            }
+            if (!alive) set_status(a.status, FAVOR_ERR_TIMEOUT);
+        }
+        return;
+    }
+    // ======================= epilogue group =======================
+    const int e = threadIdx.x - 32, ew = e >> 5;
+    const int q = (ew + 1) & 3, j = ew >> 2;
+    const int row = q * 32 + lane;
+    constexpr int NF = NC;                 // features per thread (positive / elu); trig: 2 NC
+    float R, zmax, vmax;
+    {
         const float *m = a.meta_in + ((size_t)bh * a.nseg + seg) * 4;
         const bool has_in = seg > 0;
-        sc[0] = has_in ? m[0] : (g.map == FAVOR_MAP_POSITIVE ? -INFINITY : 0.f);
-        sc[1] = has_in ? m[1] : 0.f;
-        sc[2] = has_in ? m[2] : 0.f;
-        sc[3] = 1.f;
+        R = has_in ? m[0] : (g.map == FAVOR_MAP_POSITIVE ? -INFINITY : 0.f);
+        zmax = has_in ? m[1] : 0.f;
+        vmax = has_in ? m[2] : 0.f;
     }
+    // initial state (S_in or zero): tile t, lanes = features, 16 value columns per thread
+    for (int t = 0; t < nft; ++t) {
+        const int f = t * 128 + row;
+        const float *src = (seg > 0) ? a.s_in + (((size_t)bh * a.nseg + seg) * g.r + f) * (g.dv + 1) : nullptr;
+        uint32_t v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(src ? src[64 * dvt + 16 * j + i] : 0.f);
+        tmem_st16(tm_addr(tmem, q, kColS + t * kSStride + 16 * j), v);
+        if (j == 0) {
+            const float zval = src ? src[g.dv] : 0.f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(zval);
+            tmem_st16(tm_addr(tmem, q, kColS + t * kSStride + 64), v);
+        }
+    }
+    tmem_st_wait();
+    // pad rows 129..143 of every KB block start at zero (later chunks' output
+    // staging may overwrite them; they only feed accumulator columns never read)
+    for (int i = e; i < (g.r / 64) * 15 * 8; i += kEpi) {
+        const int blk = i / 120, rr = 129 + (i % 120) / 8, ch = i % 8;
+        *reinterpret_cast<uint4 *>(kb + (size_t)blk * kKbBlk + rr * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+    }
+    auto convert_x = [&](int c) -> bool {
+        const bool ok_x = ewait(bar_x, c & 1, abortp);
+        float am;
+        convert_tile_512(xq, nd, e, am);
+        const float ss = convert_tile_512(xk, nd, e, am);
+        part[(e >> 7) * 128 + (e & 127)] = ss;
+        group_sync(kEpi);
+        if (e < 128) nk[e] = 0.5f * kLog2e * (part[e] + part[128 + e] + part[256 + e] + part[384 + e]);
+        fence_async_smem();
+        mbar_arrive(e_x);
+        return ok_x;
+    };
+    if (nchunk > 0) alive = convert_x(0);
+    for (int c = 0; c < nchunk; ++c) {
+        const uint32_t ph = c & 1;
+        const int tc0 = t_begin + c * kC;
+        const int valid = min(kC, t_end - tc0);
+        const bool ok = row < valid;
+        // ---------------- key features -> KB rows 0..127 ----------------
+        alive &= ewait(bar_pk, ph, abortp);
+        tc_fence_after();
+        float pv[NC];
+#pragma unroll
+        for (int b = 0; b < NC / 16; ++b) {
+            float t16[16];
+            tmem_ld16(tm_addr(tmem, q, kColP + NC * j + 16 * b), t16);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pv[16 * b + i] = t16[i];
+        }
+        tmem_ld_wait();
+        tc_fence_before();
+        const float nkr = nk[row];
+        float alpha = 1.f, mf = 0.f;
+        if (g.map == FAVOR_MAP_POSITIVE) {
+            if (R == -INFINITY) {
+                float mx = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < NC; ++i) mx = fmaxf(mx, pv[i]);
+                R = grp_max(ok ? mx - nkr : -INFINITY, red, ew) - kShift;
+                alpha = 0.f;
+            }
+            float off = nkr + R;
+            float lmax = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < NC; ++i) lmax = fmaxf(lmax, pv[i] - off);
+            if (group_or(ok && lmax > kShift + kSlack, kEpi)) {
+                // a key beyond the reference (rare): move the reference to it
+                const float top = grp_max(ok ? lmax : -INFINITY, red, ew);
+                const float Rn = R + (top - kShift);
+                alpha *= ex2(R - Rn);
+                R = Rn;
+                off = nkr + R;
+            }
+#pragma unroll
+            for (int b = 0; b < NC / 8; ++b) {
+                float v[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    v[i] = ok ? ex2(pv[8 * b + i] - off) : 0.f;
+                    mf = fmaxf(mf, v[i]);
+                }
+                kb_store8(kb, row, NC * j + 8 * b, v);
+            }
+        } else if (g.map == FAVOR_MAP_TRIG) {
+            // projection p -> features 128 (p / 64) + p % 64 (sin) and that + 64
+            // (cos): each 128-feature tile holds the sin and cos of 64 projections
+            const int fs = 128 * ((NC * j) / 64) + (NC * j) % 64;
+#pragma unroll
+            for (int b = 0; b < NC / 8; ++b) {
+                float s8[8], c8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (ok) sincos_reduced(pv[8 * b + i], s8[i], c8[i]);
+                    else s8[i] = c8[i] = 0.f;
+                    mf = fmaxf(mf, fmaxf(fabsf(s8[i]), fabsf(c8[i])));
+                }
+                kb_store8(kb, row, fs + 8 * b, s8);
+                kb_store8(kb, row, fs + 64 + 8 * b, c8);
+            }
+        } else {
+#pragma unroll
+            for (int b = 0; b < NC / 8; ++b) {
+                float v[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    v[i] = ok ? elu1(pv[8 * b + i]) : 0.f;
+                    mf = fmaxf(mf, v[i]);
+                }
+                kb_store8(kb, row, NC * j + 8 * b, v);
+            }
+        }
+        fence_async_smem();
+        mbar_arrive(e_k);
+        // ---------------- state -> fp16 operand (MN-major), z -> KB row 128 ----------------
+        if (e == 0) bulk_wait_read0();   // the previous chunk's output staging has been read
+        group_sync(kEpi);
+        const float zb = zmax * alpha;
+        const float bound = zb * fmaxf(vmax, 1.f);
+        const float sigma = bound > 0.f ? exp2f(floorf(log2f(kSigmaTarget / bound))) : 1.f;
+        for (int t = 0; t < nft; ++t) {
+            const int f = t * 128 + row;
+            float v[16];
+            tmem_ld16(tm_addr(tmem, q, kColS + t * kSStride + 16 * j), v);
+            tmem_ld_wait();
+            if (alpha != 1.f) {
+                uint32_t u[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(v[i] * alpha);
+                tmem_st16(tm_addr(tmem, q, kColS + t * kSStride + 16 * j), u);
+            }
+            const float sc = alpha * sigma;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+                *reinterpret_cast<uint4 *>(sop + sw128_offset(f, 16 * j + 8 * hh)) =
+                    make_uint4(pack_half2(v[8 * hh + 0] * sc, v[8 * hh + 1] * sc), pack_half2(v[8 * hh + 2] * sc, v[8 * hh + 3] * sc),
+                               pack_half2(v[8 * hh + 4] * sc, v[8 * hh + 5] * sc), pack_half2(v[8 * hh + 6] * sc, v[8 * hh + 7] * sc));
+            if (j == 0) {
+                float zv[16];
+                tmem_ld16(tm_addr(tmem, q, kColS + t * kSStride + 64), zv);
+                tmem_ld_wait();
+                const float zval = zv[0] * alpha;
+                if (alpha != 1.f) {
+                    uint32_t u[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(zval);
+                    tmem_st16(tm_addr(tmem, q, kColS + t * kSStride + 64), u);
+                }
+                *reinterpret_cast<__half *>(kb + (size_t)(f >> 6) * kKbBlk + sw128_offset(128, f & 63)) =
+                    __float2half_rn(zval * sigma);
+            }
+        }
+        tmem_st_wait();
+        zmax = zb;
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(e_sop);
+        // ---------------- query features -> phi_Q in TMEM [0, r/2) ----------------
+        alive &= ewait(bar_pq, ph, abortp);
+        tc_fence_after();
+#pragma unroll
+        for (int b = 0; b < NC / 16; ++b) {
+            float t16[16];
+            tmem_ld16(tm_addr(tmem, q, kColP + NC * j + 16 * b), t16);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pv[16 * b + i] = t16[i];
+        }
+        tmem_ld_wait();
+        float qoff = 0.f;
+        if (g.map == FAVOR_MAP_POSITIVE) {
+            float mx = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < NC; ++i) mx = fmaxf(mx, pv[i]);
+            part[j * 128 + row] = mx;
+        }
+        tc_fence_before();
+        group_sync(kEpi);   // every projection column read: phi_Q may now overwrite them
+        tc_fence_after();
+        if (g.map == FAVOR_MAP_POSITIVE) {
+            qoff = fmaxf(fmaxf(part[row], part[128 + row]), fmaxf(part[256 + row], part[384 + row])) - kShift;
+#pragma unroll
+            for (int b = 0; b < NC / 32; ++b) {
+                uint32_t o[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    o[i] = pack_half2(ex2(pv[32 * b + 2 * i] - qoff), ex2(pv[32 * b + 2 * i + 1] - qoff));
+                tmem_st16(tm_addr(tmem, q, (NC * j + 32 * b) / 2), o);
+            }
+        } else if (g.map == FAVOR_MAP_TRIG) {
+            // same feature order as the keys; 16 projections give 8 packed
+            // columns of sin and 8 of cos
+            const int fs = 128 * ((NC * j) / 64) + (NC * j) % 64;
+#pragma unroll
+            for (int b = 0; b < NC / 16; ++b) {
+                uint32_t os[8], oc[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    float s0, c0, s1, c1;
+                    sincos_reduced(pv[16 * b + 2 * i], s0, c0);
+                    sincos_reduced(pv[16 * b + 2 * i + 1], s1, c1);
+                    os[i] = pack_half2(s0, s1);
+                    oc[i] = pack_half2(c0, c1);
+                }
+                tmem_st8(tm_addr(tmem, q, (fs + 16 * b) / 2), os);
+                tmem_st8(tm_addr(tmem, q, (fs + 64 + 16 * b) / 2), oc);
+            }
+        } else {
+#pragma unroll
+            for (int b = 0; b < NC / 32; ++b) {
+                uint32_t o[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    o[i] = pack_half2(elu1(pv[32 * b + 2 * i]), elu1(pv[32 * b + 2 * i + 1]));
+                tmem_st16(tm_addr(tmem, q, (NC * j + 32 * b) / 2), o);
+            }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(e_q);
+        // ---------------- V -> fp16, running max |v| ----------------
+        alive &= ewait(bar_v, ph, abortp);
+        {
+            float am;
+            convert_tile_512(xv, 1, e, am);
+            // one reduction: max |v| of this chunk and the key mass of its phi_K
+            // (sum over keys of the largest feature), the bound on the next z
+            float vm, ms;
+            grp_maxsum(am, mf, red, ew, vm, ms);
+            vmax = fmaxf(vmax, vm);
+            zmax += ms;
+        }
+        fence_async_smem();
+        mbar_arrive(e_v);
+        // ---------------- next chunk's Q, K ----------------
+        if (c + 1 < nchunk) alive &= convert_x(c + 1);
+        // ---------------- intra-chunk matrix -> masked, row-scaled, TMEM ----------------
+        alive &= ewait(bar_a, ph, abortp);
+        tc_fence_after();
+        float av[32];
+        tmem_ld32(tm_addr(tmem, q, kColBig + 32 * j), av);
+        tmem_ld_wait();
+        const int limit = min(row, valid - 1) - 32 * j;
+        float rs = 0.f, rm = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const float x = i <= limit ? av[i] : 0.f;
+            av[i] = x;
+            rs += x;
+            rm = fmaxf(rm, fabsf(x));
+        }
+        part[j * 128 + row] = rs;
+        part2[j * 128 + row] = rm;
+        group_sync(kEpi);
+        const float den_intra = (part[row] + part[128 + row]) + (part[256 + row] + part[384 + row]);
+        const float rmax = fmaxf(fmaxf(part2[row], part2[128 + row]), fmaxf(part2[256 + row], part2[384 + row]));
+        const float rho = rmax > 0.f ? exp2f(-floorf(log2f(rmax))) : 1.f;
+        {
+            uint32_t o[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] = pack_half2(av[2 * i] * rho, av[2 * i + 1] * rho);
+            tmem_st16(tm_addr(tmem, q, kColB + 16 * j), o);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(e_b);
+        // ---------------- output ----------------
+        alive &= ewait(bar_av, ph, abortp);
+        tc_fence_after();
+        {
+            float di[16], dx[16], dd[16];
+            tmem_ld16(tm_addr(tmem, q, kColDI + 16 * j), di);
+            tmem_ld16(tm_addr(tmem, q, kColDX + 16 * j), dx);
+            tmem_ld16(tm_addr(tmem, q, kColDD), dd);
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(e_out);
+            const float inv_sigma = 1.f / sigma;
+            const float id = 1.f / (den_intra + dd[0] * inv_sigma);
+            const float ir = 1.f / rho;
+            // output columns 16 j .. 16 j + 15 -> staging half (16 j) / 32, chunks of 4
+            uint8_t *half = stage + (size_t)((16 * j) >> 5) * kBlk;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const int col = (16 * j + 4 * cc) & 31;
+                const int p = (col >> 2) ^ (row & 7);
+                float4 o4;
+                o4.x = fmaf(di[4 * cc + 0], ir, dx[4 * cc + 0] * inv_sigma) * id;
+                o4.y = fmaf(di[4 * cc + 1], ir, dx[4 * cc + 1] * inv_sigma) * id;
+                o4.z = fmaf(di[4 * cc + 2], ir, dx[4 * cc + 2] * inv_sigma) * id;
+                o4.w = fmaf(di[4 * cc + 3], ir, dx[4 * cc + 3] * inv_sigma) * id;
+                *reinterpret_cast<float4 *>(half + row * 128 + p * 16) = o4;
+            }
+        }
+        fence_async_smem();
+        group_sync(kEpi);
+        if (e == 0 && !*abortp) {
+            tma_store_3d(tm_out, stage, 64 * dvt, tc0, bh);
+            tma_store_3d(tm_out, stage + kBlk, 64 * dvt + 32, tc0, bh);
+            bulk_commit();
+        }
+    }
+    if (e == 0) bulk_wait0();
+    if (!alive) set_status(a.status, FAVOR_ERR_TIMEOUT);
+}
+
+__global__ void __launch_bounds__(kCausalThreads, 1)
+tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_out,
+          const CausalArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float *small = reinterpret_cast<float *>(sm + a.o_small);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(small + 1184);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(small + 1220);
+    volatile int *abortp = reinterpret_cast<volatile int *>(small + 1224);
+    if (threadIdx.x == 0) *abortp = 0;
+    const int warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 8; ++i) mbar_init(&bars[i], 1);
+        for (int i = 8; i < 15; ++i) mbar_init(&bars[i], kEpi);
+        fence_mbar_init();
+    }
+    // ones atom after the V tile: the z column of S += phi_K^T [V | 1]
+    uint8_t *ones = sm + a.o_v + kBlk;
+    for (int i = threadIdx.x; i < (int)(kBlk / 16); i += kCausalThreads)
+        reinterpret_cast<uint4 *>(ones)[i] = make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
     if (warp == 0) tmem_alloc(tslot, a.tmem_cols);
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    if (threadIdx.x == 0) {
-        const uint32_t wbytes = (uint32_t)g.nproj * g.d * 2;
-        mbar_arrive_expect_tx(&bars[0], wbytes);
-        bulk_load(w, a.omg + (size_t)head * wbytes, wbytes, &bars[0]);
-        if (nchunk > 0) {
-            mbar_arrive_expect_tx(&bars[1], 2 * kBlk * nd);
-            for (int b = 0; b < nd; ++b) {
-                tma_load_3d(xq + b * kBlk, &tm_q, &bars[1], 64 * b, t_begin, bh);
-                tma_load_3d(xk + b * kBlk, &tm_k, &bars[1], 64 * b, t_begin, bh);
-            }
-            mbar_arrive_expect_tx(&bars[2], kBlk);
-            tma_load_3d(xv, &tm_v, &bars[2], 64 * dvt, t_begin, bh);
-        }
-    }
-    // initial state: S_in of this segment (or zero) -> TMEM state tiles
-    for (int t = 0; t < nft; ++t) {
-        const int f = t * 128 + row;
-        const float *src = (seg > 0) ? a.s_in + (((size_t)bh * a.nseg + seg) * g.r + f) * (g.dv + 1) : nullptr;
-        float v[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = src ? src[64 * dvt + 32 * h + i] : 0.f;
-        tmem_st32(tm_addr(tmem, q, col_s + t * s_stride + 32 * h), v);
-        if (h == 0) {
-            const float zval = src ? src[g.dv] : 0.f;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = zval;
-            tmem_st32(tm_addr(tmem, q, col_s + t * s_stride + 64), v);
-        }
-    }
-    tmem_st_wait();
-    bool alive = mbar_wait(&bars[0], 0, kWaitLimit);
-    uint32_t ph_qk = 0, ph_v = 0, ph_m = 0;
-    const uint32_t w_s = smem_u32(w), xq_s = smem_u32(xq), xk_s = smem_u32(xk), xv_s = smem_u32(xv),
-                   phq_s = smem_u32(phq), phk_s = smem_u32(phk), ones_s = smem_u32(ones),
-                   sop_s = smem_u32(sop), bhat_s = smem_u32(bhat);
-    KeyEpi ep{&sc[0], nk, part, red};
-
-    for (int c = 0; c < nchunk; ++c) {
-        const int tc0 = t_begin + c * kC;
-        const int valid = min(kC, t_end - tc0);
-        // (1) Q, K tiles -> fp16; key norms
-        alive = alive && mbar_wait(&bars[1], ph_qk, kWaitLimit);
-        ph_qk ^= 1;
-        if (__syncthreads_or(!alive)) break;
-        key_tile_prepare(xk, nd, nk, part);
-        {
-            float ss, am;
-            convert_tile(xq, nd, ss, am);
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        // (2) P_K
-        if (threadIdx.x == 0) {
-            issue_projection(g, tmem, xk_s, w_s, g.nproj, 0, nft, 0);
-            mma_commit(&bars[3]);
-        }
-        alive = mbar_wait(&bars[3], ph_m, kWaitLimit);
-        ph_m ^= 1;
-        if (__syncthreads_or(!alive)) break;
-        tc_fence_after();
-        // (3) key features (may raise the key reference)
-        float mass;
-        float alpha = key_features(g, tmem, 0, nft, phk, valid, ep, &mass);
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        // (4) P_Q
-        if (threadIdx.x == 0) {
-            issue_projection(g, tmem, xq_s, w_s, g.nproj, 0, nft, 0);
-            mma_commit(&bars[3]);
-        }
-        alive = mbar_wait(&bars[3], ph_m, kWaitLimit);
-        ph_m ^= 1;
-        if (__syncthreads_or(!alive)) break;
-        tc_fence_after();
-        // (5) state -> fp16 operand (Q/K tiles are free now), z -> smem
-        {
-            float zmax = sc[1] * alpha;
-            const float vmax = sc[2];
-            const float bound = zmax * vmax;
-            const float sigma = bound > 0.f ? exp2f(floorf(log2f(kSigmaTarget / bound))) : 1.f;
-            for (int t = 0; t < nft; ++t) {
-                const int f = t * 128 + row;
-                float v[32];
-                tmem_ld32(tm_addr(tmem, q, col_s + t * s_stride + 32 * h), v);
-                tmem_ld_wait();
-                if (alpha != 1.f) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] *= alpha;
-                    tmem_st32(tm_addr(tmem, q, col_s + t * s_stride + 32 * h), v);
-                }
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] *= sigma;
-                store_row32(sop, f, 32 * h, v);
-                if (h == 0) {
-                    float zv[32];
-                    tmem_ld32(tm_addr(tmem, q, col_s + t * s_stride + 64), zv);
-                    tmem_ld_wait();
-                    const float zval = zv[0] * alpha;
-                    zs[f] = zval;
-                    if (alpha != 1.f) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) zv[i] = zval;
-                        tmem_st32(tm_addr(tmem, q, col_s + t * s_stride + 64), zv);
-                    }
-                }
-            }
-            tmem_st_wait();
-            if (threadIdx.x == 0) {
-                sc[1] = zmax + mass;   // bound on max_f z_f after this chunk's update
-                sc[4] = sigma;
-            }
-        }
-        fence_async_smem();
-        __syncthreads();
-        const float sigma = sc[4];
-        // (6) query features (+ phi_q . z)
-        float den = query_features(g, tmem, phq, zs, part);
-        dpart[h * 128 + row] = den;
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        // (7) A = phi_Q phi_K^T, D_inter = phi_Q S_op
-        if (threadIdx.x == 0) {
-            const uint32_t idesc = idesc_f16(128, 128, 0, 0);
-            for (int kk = 0; kk < g.r / 16; ++kk) {
-                uint64_t aa = smem_desc(phq_s + (kk >> 2) * kBlk + (kk & 3) * 32, 16, 1024);
-                uint64_t bb = smem_desc(phk_s + (kk >> 2) * kBlk + (kk & 3) * 32, 16, 1024);
-                mma_f16(tmem + col_a, aa, bb, idesc, kk > 0);
-            }
-            issue_inter(g, tmem + col_di, phq_s, sop_s, 0);
-            mma_commit(&bars[3]);
-        }
-        alive = mbar_wait(&bars[3], ph_m, kWaitLimit);
-        ph_m ^= 1;
-        if (__syncthreads_or(!alive)) break;
-        tc_fence_after();
-        // Q/K tiles and the state operand are free: prefetch the next chunk's Q, K
-        if (threadIdx.x == 0 && c + 1 < nchunk) {
-            mbar_arrive_expect_tx(&bars[1], 2 * kBlk * nd);
-            for (int b = 0; b < nd; ++b) {
-                tma_load_3d(xq + b * kBlk, &tm_q, &bars[1], 64 * b, tc0 + kC, bh);
-                tma_load_3d(xk + b * kBlk, &tm_k, &bars[1], 64 * b, tc0 + kC, bh);
-            }
-        }
-        // (8) intra-chunk matrix: causal mask, row sums, per-row power-of-two scale
-        {
-            float s = 0.f, mx = 0.f;
-            for (int cc = 0; cc < 2; ++cc) {
-                float v[32];
-                tmem_ld32(tm_addr(tmem, q, col_a + 64 * h + 32 * cc), v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int j = 64 * h + 32 * cc + i;
-                    float x = (j <= row && j < valid) ? v[i] : 0.f;
-                    s += x;
-                    mx = fmaxf(mx, fabsf(x));
-                }
-            }
-            part[h * 128 + row] = s;
-            __syncthreads();
-            const float rs = part[row] + part[128 + row];
-            __syncthreads();
-            part[h * 128 + row] = mx;
-            __syncthreads();
-            const float rm = fmaxf(part[row], part[128 + row]);
-            const float r_scale = rm > 0.f ? exp2f(-floorf(log2f(rm))) : 1.f;
-            if (h == 0) {
-                deni[row] = rs;
-                rho[row] = r_scale;
-            }
-            uint8_t *blk = bhat + (size_t)h * kBlk;
-            for (int cc = 0; cc < 2; ++cc) {
-                float v[32];
-                tmem_ld32(tm_addr(tmem, q, col_a + 64 * h + 32 * cc), v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int j = 64 * h + 32 * cc + i;
-                    v[i] = (j <= row && j < valid) ? v[i] * r_scale : 0.f;
-                }
-                store_row32(blk, row, 32 * cc, v);
-            }
-        }
-        // V tile -> fp16, running max |v|
-        alive = alive && mbar_wait(&bars[2], ph_v, kWaitLimit);
-        ph_v ^= 1;
-        if (__syncthreads_or(!alive)) break;
-        {
-            float ss, am;
-            convert_tile(xv, 1, ss, am);
-            const float vm = cta_max(am, red);
-            if (threadIdx.x == 0) sc[2] = fmaxf(sc[2], vm);
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        // (9) D_intra = B V ; S += phi_K^T V ; z += phi_K^T 1
-        if (threadIdx.x == 0) {
-            const uint32_t idesc = idesc_f16(128, 64, 0, 1);
-            for (int kk = 0; kk < kC / 16; ++kk) {
-                uint64_t aa = smem_desc(bhat_s + (kk >> 2) * kBlk + (kk & 3) * 32, 16, 1024);
-                uint64_t bb = smem_desc(xv_s + kk * 2048, kBlk, 1024);
-                mma_f16(tmem + col_da, aa, bb, idesc, kk > 0);
-            }
-            issue_state_update(tmem, phk_s, xv_s, ones_s, nft, col_s, s_stride, 1);
-            mma_commit(&bars[3]);
-        }
-        alive = mbar_wait(&bars[3], ph_m, kWaitLimit);
-        ph_m ^= 1;
-        if (__syncthreads_or(!alive)) break;
-        tc_fence_after();
-        if (threadIdx.x == 0 && c + 1 < nchunk) {
-            mbar_arrive_expect_tx(&bars[2], kBlk);
-            tma_load_3d(xv, &tm_v, &bars[2], 64 * dvt, tc0 + kC, bh);
-        }
-        // (10) out = (D_intra / rho + D_inter / sigma) / (den_intra + den_inter)
-        {
-            float di[32], da[32];
-            tmem_ld32(tm_addr(tmem, q, col_da + 32 * h), da);
-            tmem_ld32(tm_addr(tmem, q, col_di + 32 * h), di);
-            tmem_ld_wait();
-            const float dn = deni[row] + dpart[row] + dpart[128 + row];
-            const float inv = 1.f / dn, ia = 1.f / rho[row], is = 1.f / sigma;
-            float o[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = fmaf(da[i], ia, di[i] * is) * inv;
-            stage_out(stage, row, h, o);
-        }
-        fence_async_smem();
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            tma_store_3d(&tm_out, stage, 64 * dvt, tc0, bh);
-            tma_store_3d(&tm_out, stage + kBlk, 64 * dvt + 32, tc0, bh);
-            bulk_commit();
-            bulk_wait_read0();   // phi_K of the next chunk reuses the staging area
-        }
-        __syncthreads();
-    }
-    if (threadIdx.x == 0) bulk_wait0();
-    if (!alive) set_status(a.status, FAVOR_ERR_TIMEOUT);
+    const int nc = a.g.nproj / 4;
+    if (nc == 64) causal_body<64>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
+    else if (nc == 32) causal_body<32>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
+    else causal_body<16>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1210,19 +1508,17 @@ Geo make_geo(const Problem &p) {
 }
 
 struct CausalLayout {
-    uint32_t o_w, o_xq, o_xk, o_xv, o_phq, o_phk, o_ones, o_small, bytes;
+    uint32_t o_w, o_x, o_v, o_kb, o_sop, o_small, bytes;
 };
 CausalLayout causal_layout(const Geo &g) {
     CausalLayout l;
     uint32_t o = 0;
     l.o_w = o; o = align1k(o + (uint32_t)g.nproj * g.d * 2);
-    l.o_xq = o; o = align1k(o + (uint32_t)kC * g.d * 2);
-    l.o_xk = o; o = align1k(o + (uint32_t)kC * g.d * 2);
-    l.o_xv = o; o = align1k(o + kBlk);
-    l.o_phq = o; o = align1k(o + (uint32_t)kC * g.r * 2);
-    l.o_phk = o; o = align1k(o + (uint32_t)kC * g.r * 2);
-    l.o_ones = o; o = align1k(o + 4096);
-    l.o_small = o; o = align1k(o + 1200 * 4);
+    l.o_x = o; o = align1k(o + 2u * kC * g.d * 2);
+    l.o_v = o; o = align1k(o + 2 * kBlk);                   // V tile + ones atom
+    l.o_kb = o; o = align1k(o + (uint32_t)(g.r / 64) * kKbBlk);
+    l.o_sop = o; o = align1k(o + std::max<uint32_t>((uint32_t)g.r * 128, 2 * kBlk));
+    l.o_small = o; o = align1k(o + 1232 * 4);
     l.bytes = o + 1024;
     return l;
 }
@@ -1419,14 +1715,15 @@ int tc_run(const void *q, const void *k, const void *v, const float *omega, floa
     }
     CausalLayout cl = causal_layout(g);
     CausalArgs a;
-    a.g = g; a.H = p.H; a.L = p.L; a.seg_len = seg_len; a.nseg = G;
+    a.g = g;
+    a.H = p.H; a.L = p.L; a.seg_len = seg_len; a.nseg = G;
     a.omg = img; a.s_in = s_in; a.meta_in = meta_in; a.status = dstat;
-    a.o_w = cl.o_w; a.o_xq = cl.o_xq; a.o_xk = cl.o_xk; a.o_xv = cl.o_xv; a.o_phq = cl.o_phq;
-    a.o_phk = cl.o_phk; a.o_ones = cl.o_ones; a.o_small = cl.o_small; a.tmem_cols = 512;
+    a.o_w = cl.o_w; a.o_x = cl.o_x; a.o_v = cl.o_v; a.o_kb = cl.o_kb; a.o_sop = cl.o_sop; a.o_small = cl.o_small;
+    a.tmem_cols = 512;
     if (cudaFuncSetAttribute(tc_causal, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cl.bytes) != cudaSuccess)
         return FAVOR_ERR_CUDA;
     stats_begin(st, "tc_causal");
-    tc_causal<<<dim3(G, nvb, p.BH), kThreads, cl.bytes, st>>>(mq, mk, mv, mo, a);
+    tc_causal<<<dim3(G, nvb, p.BH), kCausalThreads, cl.bytes, st>>>(mq, mk, mv, mo, a);
     stats_end(st);
     FAVOR_LAUNCH_CHECK();
     return FAVOR_OK;
