@@ -95,31 +95,6 @@ __device__ __forceinline__ void set_status(int *status, int code) {
     if (status) atomicExch(status, code);
 }
 
-// warp + CTA reductions over kThreads threads; `red` holds 8 floats.
-__device__ __forceinline__ float cta_max(float v, float *red) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    float r = red[0];
-#pragma unroll
-    for (int i = 1; i < kThreads / 32; ++i) r = fmaxf(r, red[i]);
-    return r;
-}
-
-__device__ __forceinline__ float cta_sum(float v, float *red) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    float r = 0.f;
-#pragma unroll
-    for (int i = 0; i < kThreads / 32; ++i) r += red[i];
-    return r;
-}
-
 // In-place bf16 -> fp16 conversion of a [128][64*nblk] tile (128B-swizzled
 // blocks of 16 KB).  Thread (row = tid % 128, half = tid / 128) converts four
 // 16-byte chunks of its row per block, rotating the chunk index with the row
@@ -214,117 +189,6 @@ __global__ void tc_prep_omega(const float *__restrict__ omega, uint8_t *__restri
 }
 
 // ---------------------------------------------------------------------------
-// Key feature epilogue (shared by tc_state and tc_causal).
-// P (projections) for n_tiles feature tiles sits in TMEM columns [128 t, ...).
-// Writes fp16 key features for tokens < valid into phk (K-major blocks of 64
-// features, two per tile), zeros for the rest.  Positive map: updates the
-// key reference *R (log2 units) when this chunk exceeds it; returns the
-// factor alpha = 2^(R_old - R_new) the existing state must be scaled by (1
-// if unchanged) and the chunk's key mass (sum over tokens of the largest
-// feature) in *mass.
-// ---------------------------------------------------------------------------
-struct KeyEpi {
-    float *R;        // smem scalar
-    float *nk;       // [128] |k|^2 log2e / 2
-    float *part;     // [2][128] half-row partials
-    float *red;      // [8]
-};
-
-__device__ float key_features(const Geo &g, uint32_t tmem, int first_tile, int n_tiles,
-                              uint8_t *phk, int valid, const KeyEpi &ep, float *mass) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int q = warp & 3, h = warp >> 2;
-    const int row = q * 32 + lane;
-    const bool ok = row < valid;
-    float alpha = 1.f;
-    float mf = 0.f;   // largest feature of this row (this thread's columns)
-    if (g.map == FAVOR_MAP_POSITIVE) {
-        // pass 1: row maximum of w.k (log2 units)
-        float mx = -INFINITY;
-        for (int t = 0; t < n_tiles; ++t) {
-            for (int c = 0; c < 2; ++c) {
-                float v[32];
-                tmem_ld32(tm_addr(tmem, q, 128 * (first_tile + t) + 64 * h + 32 * c), v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, v[i]);
-            }
-        }
-        float lam = ok ? mx - ep.nk[row] : -INFINITY;
-        float mu = cta_max(lam, ep.red);
-        float Rold = *ep.R;
-        float Rnew = Rold;
-        if (mu > -INFINITY && (Rold == -INFINITY || mu > Rold + kShift + kSlack)) Rnew = mu - kShift;
-        __syncthreads();
-        if (threadIdx.x == 0) *ep.R = Rnew;
-        alpha = (Rold == -INFINITY) ? 0.f : ex2(Rold - Rnew);
-        const float off = (ok ? ep.nk[row] : 0.f) + Rnew;
-        // pass 2: features
-        for (int t = 0; t < n_tiles; ++t) {
-            uint8_t *blk = phk + (size_t)(2 * t + h) * kBlk;
-            for (int c = 0; c < 2; ++c) {
-                float v[32];
-                tmem_ld32(tm_addr(tmem, q, 128 * (first_tile + t) + 64 * h + 32 * c), v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    v[i] = ok ? ex2(v[i] - off) : 0.f;
-                    mf = fmaxf(mf, v[i]);
-                }
-                store_row32(blk, row, 32 * c, v);
-            }
-        }
-    } else if (g.map == FAVOR_MAP_TRIG) {
-        // projection tile t holds 64 columns: sin -> block 2t, cos -> block 2t+1
-        for (int t = 0; t < n_tiles; ++t) {
-            float v[32], s[32], co[32];
-            tmem_ld32(tm_addr(tmem, q, 128 * (first_tile + t) + 32 * h), v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                if (ok) sincos_reduced(v[i], s[i], co[i]);
-                else s[i] = co[i] = 0.f;
-                mf = fmaxf(mf, fmaxf(fabsf(s[i]), fabsf(co[i])));
-            }
-            store_row32(phk + (size_t)(2 * t) * kBlk, row, 32 * h, s);
-            store_row32(phk + (size_t)(2 * t + 1) * kBlk, row, 32 * h, co);
-        }
-    } else {
-        for (int t = 0; t < n_tiles; ++t) {
-            uint8_t *blk = phk + (size_t)(2 * t + h) * kBlk;
-            for (int c = 0; c < 2; ++c) {
-                float v[32];
-                tmem_ld32(tm_addr(tmem, q, 128 * (first_tile + t) + 64 * h + 32 * c), v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    v[i] = ok ? elu1(v[i]) : 0.f;
-                    mf = fmaxf(mf, v[i]);
-                }
-                store_row32(blk, row, 32 * c, v);
-            }
-        }
-    }
-    // per-row largest feature (combine the two column halves), then the chunk mass
-    ep.part[h * 128 + row] = mf;
-    __syncthreads();
-    float rowmax = fmaxf(ep.part[row], ep.part[128 + row]);
-    float m = cta_sum(h == 0 ? rowmax : 0.f, ep.red);
-    *mass = m;
-    return alpha;
-}
-
-// Convert a key tile in place and publish |k|^2 log2e / 2 per row.
-__device__ void key_tile_prepare(uint8_t *xk, int nd, float *nk, float *part) {
-    float ss, am;
-    convert_tile(xk, nd, ss, am);
-    const int row = threadIdx.x & 127, half = threadIdx.x >> 7;
-    part[half * 128 + row] = ss;
-    __syncthreads();
-    if (half == 0) nk[row] = 0.5f * kLog2e * (part[row] + part[128 + row]);
-}
-
-// ---------------------------------------------------------------------------
 // MMA issue helpers (one thread)
 // ---------------------------------------------------------------------------
 // P[:, 128 t .. ] = X W_tile^T for feature tiles [t0, t0 + nt); X K-major
@@ -347,46 +211,83 @@ __device__ __forceinline__ void issue_projection(const Geo &g, uint32_t tmem, ui
     }
 }
 
-// S_tile[t] (M = 128 features, N = 64 values) += phi_K^T V and z += phi_K^T 1,
-// for feature tiles t in [0, nt); phk blocks (2t, 2t+1) are the MN-major A
-// operand; V (MN-major, one 64-wide block) and the ones block (K-major [16][128]).
-__device__ __forceinline__ void issue_state_update(uint32_t tmem, uint32_t phk_s, uint32_t v_s,
-                                                   uint32_t ones_s, int nt, int col_s,
-                                                   int stride_cols, int nvblk) {
-    for (int t = 0; t < nt; ++t) {
-        for (int vb = 0; vb < nvblk; ++vb) {
-            const uint32_t idesc = idesc_f16(128, 64, 1, 1);
-            for (int kk = 0; kk < kC / 16; ++kk) {
-                uint64_t a = smem_desc(phk_s + (2 * t) * kBlk + kk * 2048, kBlk, 1024);
-                uint64_t b = smem_desc(v_s + vb * kBlk + kk * 2048, kBlk, 1024);
-                mma_f16(tmem + col_s + t * stride_cols + 64 * vb, a, b, idesc, 1);
+// ---------------------------------------------------------------------------
+// tc_state: per (feature tile, segment, head) the segment state
+//   S[f][c] = sum_t phi(k_t)_f v_t[c],  z[f] = sum_t phi(k_t)_f
+// at the key reference R, written as fp32 [f][dv + 1] plus (R, max z, max|v|,
+// max|S|) of the tile.
+// Warp 0 lane 0 issues every TMA copy and MMA; warps 1..8 (256 threads,
+// named barrier 1) convert tiles and compute features.  Projections P[2]
+// alternate in TMEM; K, V and phi_K are double-buffered in shared memory, so
+// the projection of chunk c+1 and the state update of chunk c run while the
+// epilogue works on the features of the next chunk.
+// ---------------------------------------------------------------------------
+constexpr int kStEpi = 256;
+constexpr int kStateThreads = 32 + kStEpi;
+
+struct StateArgs {
+    Geo g;
+    int H, L, seg_len, nseg, nvs;      // nvs: V buffers (1 or 2)
+    const uint8_t *omg;                // MN-major W images
+    float *state;                      // [BH][nseg][r][dv+1]
+    float *meta;                       // [BH][nseg][n_ft][4]: R, max z, max|v|, max|S|
+    int *status;
+    uint32_t o_w, o_xk, o_xv, o_phk, o_small, xv_stride, tmem_cols;
+};
+
+// in-place bf16 -> fp16 conversion of a [128][64 nblk] tile by 256 threads
+// (thread e: row e % 128, four 16-byte chunks of it per block)
+__device__ __forceinline__ void convert_tile_256(uint8_t *tile, int nblk, int e, float &sumsq,
+                                                 float &amax) {
+    const int row = e & 127, half = e >> 7;
+    sumsq = 0.f;
+    amax = 0.f;
+    for (int b = 0; b < nblk; ++b) {
+        uint8_t *rp = tile + b * kBlk + row * 128;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int p = (half * 4 + c + row) & 7;
+            uint4 *ptr = reinterpret_cast<uint4 *>(rp + p * 16);
+            uint4 u = *ptr;
+            uint32_t w[4] = {u.x, u.y, u.z, u.w}, o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
+                sumsq = fmaf(lo, lo, fmaf(hi, hi, sumsq));
+                amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
+                o[i] = pack_half2(lo, hi);
             }
-        }
-        const uint32_t idz = idesc_f16(128, 16, 1, 0);
-        for (int kk = 0; kk < kC / 16; ++kk) {
-            uint64_t a = smem_desc(phk_s + (2 * t) * kBlk + kk * 2048, kBlk, 1024);
-            uint64_t b = smem_desc(ones_s + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024);
-            mma_f16(tmem + col_s + t * stride_cols + 64 * nvblk, a, b, idz, 1);
+            *ptr = make_uint4(o[0], o[1], o[2], o[3]);
         }
     }
 }
 
-// ---------------------------------------------------------------------------
-// tc_state: per (feature tile, segment, head) the segment state
-//   S[f][c] = sum_t phi(k_t)_f v_t[c],  z[f] = sum_t phi(k_t)_f
-// at key reference R, written as fp32 [f][dv + 1] plus (R, mass, vmax).
-// ---------------------------------------------------------------------------
-struct StateArgs {
-    Geo g;
-    int H, L, seg_len, nseg;
-    const uint8_t *omg;       // [H] images
-    float *state;             // [BH][nseg][r][dv+1]
-    float *meta;              // [BH][nseg][n_ft][4]: R, mass, vmax, -
-    int *status;
-    uint32_t o_w, o_xk, o_xv, o_phk, o_ones, o_small, tmem_cols;
-};
+__device__ __forceinline__ float st_grp_max(float v, float *red, int ew) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    group_sync(kStEpi);
+    if ((threadIdx.x & 31) == 0) red[ew] = v;
+    group_sync(kStEpi);
+    float r = red[0];
+#pragma unroll
+    for (int i = 1; i < kStEpi / 32; ++i) r = fmaxf(r, red[i]);
+    return r;
+}
 
-__global__ void __launch_bounds__(kThreads, 1)
+__device__ __forceinline__ bool st_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort) return false;
+        if (clock64() - t0 > kWaitLimit) {
+            *abort = 1;
+            return false;
+        }
+    }
+    return true;
+}
+
+__global__ void __launch_bounds__(kStateThreads, 1)
 tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
          const StateArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -395,22 +296,32 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     const int ft = blockIdx.x, seg = blockIdx.y, bh = blockIdx.z, head = bh % a.H;
     const int t_begin = seg * a.seg_len, t_end = min(a.L, t_begin + a.seg_len);
     const int nchunk = (t_end - t_begin + kC - 1) / kC;
-    const int nd = g.d / 64, nvb = g.dv / 64;
-    uint8_t *w = sm + a.o_w, *xk = sm + a.o_xk, *xv = sm + a.o_xv, *phk = sm + a.o_phk,
-            *ones = sm + a.o_ones;
+    const int nd = g.d / 64, nvb = g.dv / 64, NSV = a.nvs;
+    const uint32_t xkb = (uint32_t)kC * g.d * 2;
+    uint8_t *w = sm + a.o_w, *xk = sm + a.o_xk, *xv = sm + a.o_xv, *phk = sm + a.o_phk;
     float *small = reinterpret_cast<float *>(sm + a.o_small);
-    float *nk = small, *part = small + 128, *red = small + 384, *Rp = small + 392;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(small + 400);   // 0: w, 1: k, 2: v, 3: mma
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(small + 408);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = warp & 3, h = warp >> 2;
+    float *nk = small;              // [2][128]
+    float *part = small + 256;      // [2][128]
+    float *red = small + 512;       // [8]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(small + 528);
+    uint64_t *bar_w = &bars[0], *bar_k = &bars[1] /*[2]*/, *bar_v = &bars[3] /*[2]*/,
+             *bar_pk = &bars[5] /*[2]*/, *bar_s = &bars[7] /*[2]*/, *e_x = &bars[9], *e_k = &bars[10];
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(small + 560);
+    volatile int *abortp = reinterpret_cast<volatile int *>(small + 562);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int col_s = 256;          // state tile: dv values, then 16 copies of z
 
-    // ones block for the z column
-    for (int i = threadIdx.x; i < 4096 / 16; i += kThreads)
-        reinterpret_cast<uint4 *>(ones)[i] = make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < 9; ++i) mbar_init(&bars[i], 1);
+        for (int i = 9; i < 11; ++i) mbar_init(&bars[i], kStEpi);
         fence_mbar_init();
-        *Rp = -INFINITY;
+        *abortp = 0;
+    }
+    // ones atom after the V blocks of each V buffer (the z column)
+    for (int s = 0; s < NSV; ++s) {
+        uint8_t *ones = xv + (size_t)s * a.xv_stride + (size_t)nvb * kBlk;
+        for (int i = threadIdx.x; i < (int)(kBlk / 16); i += kStateThreads)
+            reinterpret_cast<uint4 *>(ones)[i] = make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
     }
     if (warp == 0) tmem_alloc(tslot, a.tmem_cols);
     fence_async_smem();
@@ -418,125 +329,232 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const int col_s = 128;                   // S at [128, 128 + dv), z at [128 + dv, +16)
-    uint32_t ph_k = 0, ph_v = 0, ph_m = 0;
     bool alive = true;
 
-    if (threadIdx.x == 0) {
-        // W atoms of this feature tile (np_tile projections, contiguous)
-        const uint32_t wbytes = (uint32_t)g.np_tile * g.d * 2;
-        mbar_arrive_expect_tx(&bars[0], wbytes);
-        bulk_load(w, a.omg + (size_t)head * g.nproj * g.d * 2 + (size_t)ft * wbytes, wbytes, &bars[0]);
-        if (nchunk > 0) {
-            mbar_arrive_expect_tx(&bars[1], kBlk * nd);
-            for (int b = 0; b < nd; ++b) tma_load_3d(xk + b * kBlk, &tm_k, &bars[1], 64 * b, t_begin, bh);
-            mbar_arrive_expect_tx(&bars[2], kBlk * nvb);
-            for (int b = 0; b < nvb; ++b) tma_load_3d(xv + b * kBlk, &tm_v, &bars[2], 64 * b, t_begin, bh);
+    if (warp == 0) {
+        if (lane == 0 && nchunk > 0) {
+            const uint32_t w_s = smem_u32(w), xk_s = smem_u32(xk), xv_s = smem_u32(xv), phk_s = smem_u32(phk);
+            const uint32_t wbytes = (uint32_t)g.np_tile * g.d * 2;
+            auto load_k = [&](int c) {
+                uint64_t *bar = &bar_k[c & 1];
+                mbar_arrive_expect_tx(bar, xkb);
+                for (int b = 0; b < nd; ++b)
+                    tma_load_3d(xk + (size_t)(c & 1) * xkb + b * kBlk, &tm_k, bar, 64 * b, t_begin + c * kC, bh);
+            };
+            auto load_v = [&](int c) {
+                const int s = c % NSV;
+                mbar_arrive_expect_tx(&bar_v[s], (uint32_t)nvb * kBlk);
+                for (int b = 0; b < nvb; ++b)
+                    tma_load_3d(xv + (size_t)s * a.xv_stride + b * kBlk, &tm_v, &bar_v[s], 64 * b, t_begin + c * kC, bh);
+            };
+            auto issue_proj = [&](int c) {
+                const uint32_t idesc = idesc_f16(128, g.np_tile, 0, 1);
+                const uint32_t x_s = xk_s + (uint32_t)(c & 1) * xkb;
+                for (int kk = 0; kk < g.d / 16; ++kk)
+                    mma_f16(tmem + 128 * (c & 1), smem_desc(x_s + (kk >> 2) * kBlk + (kk & 3) * 32, 16, 1024),
+                            smem_desc(w_s + kk * 2048, (uint32_t)g.d * 128, 1024), idesc, kk > 0);
+                mma_commit(&bar_pk[c & 1]);
+            };
+            mbar_arrive_expect_tx(bar_w, wbytes);
+            bulk_load(w, a.omg + (size_t)head * g.nproj * g.d * 2 + (size_t)ft * wbytes, wbytes, bar_w);
+            load_k(0);
+            load_v(0);
+            if (nchunk > 1) {
+                load_k(1);
+                if (NSV == 2) load_v(1);
+            }
+            alive = st_wait(bar_w, 0, abortp) && st_wait(e_x, 0, abortp);
+            if (alive) {
+                tc_fence_after();
+                issue_proj(0);
+            }
+            for (int c = 0; c < nchunk && alive; ++c) {
+                if (c + 1 < nchunk) {
+                    if (!(alive = st_wait(e_x, (c + 1) & 1, abortp))) break;
+                    tc_fence_after();
+                    issue_proj(c + 1);
+                }
+                if (c + 2 < nchunk) {
+                    // K buffer c % 2 is free once P_K(c) is done: refill it early,
+                    // a whole chunk of epilogue work ahead of its use
+                    if (!(alive = st_wait(&bar_pk[c & 1], (c >> 1) & 1, abortp))) break;
+                    load_k(c + 2);
+                }
+                if (!(alive = st_wait(e_k, c & 1, abortp))) break;
+                tc_fence_after();
+                {
+                    const uint32_t idesc = idesc_f16(128, g.dv + 16, 1, 1);
+                    const uint32_t a_s = phk_s + (uint32_t)(c & 1) * 2 * kBlk;
+                    const uint32_t b_s = xv_s + (uint32_t)(c % NSV) * a.xv_stride;
+                    for (int kk = 0; kk < kC / 16; ++kk)
+                        mma_f16(tmem + col_s, smem_desc(a_s + kk * 2048, kBlk, 1024),
+                                smem_desc(b_s + kk * 2048, kBlk, 1024), idesc, 1);
+                    mma_commit(&bar_s[c & 1]);
+                }
+                const int nextv = c + NSV;
+                if (nextv < nchunk) {
+                    if (!(alive = st_wait(&bar_s[c & 1], (c >> 1) & 1, abortp))) break;
+                    load_v(nextv);
+                }
+            }
+            if (!alive) set_status(a.status, FAVOR_ERR_TIMEOUT);
         }
-    }
-    // zero S and z
-    {
-        float zero[32];
+    } else {
+        const int e = threadIdx.x - 32, ew = e >> 5;
+        const int q = (ew + 1) & 3, h = ew >> 2;
+        const int row = q * 32 + lane;
+        float R = g.map == FAVOR_MAP_POSITIVE ? -INFINITY : 0.f;
+        float vmax = 0.f;
+        // zero state and z
+        {
+            float zero[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) zero[i] = 0.f;
-        for (int c = 32 * h; c < g.dv + 16; c += 64) tmem_st32(tm_addr(tmem, q, col_s + c), zero);
-        tmem_st_wait();
-    }
-    alive = mbar_wait(&bars[0], 0, kWaitLimit);
-    float mass_total = 0.f, vmax = 0.f;
-    const uint32_t w_s = smem_u32(w), xk_s = smem_u32(xk), xv_s = smem_u32(xv),
-                   phk_s = smem_u32(phk), ones_s = smem_u32(ones);
-    KeyEpi ep{Rp, nk, part, red};
-
-    for (int c = 0; c < nchunk; ++c) {
-        const int tc0 = t_begin + c * kC;
-        const int valid = min(kC, t_end - tc0);
-        alive = alive && mbar_wait(&bars[1], ph_k, kWaitLimit);
-        ph_k ^= 1;
-        if (__syncthreads_or(!alive)) break;
-        key_tile_prepare(xk, nd, nk, part);
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        if (threadIdx.x == 0) {
-            issue_projection(g, tmem, xk_s, w_s, g.np_tile, 0, 1, 0);
-            mma_commit(&bars[3]);
+            for (int i = 0; i < 32; ++i) zero[i] = 0.f;
+            for (int cc = 32 * h; cc < g.dv + 16; cc += 64) tmem_st32(tm_addr(tmem, q, col_s + cc), zero);
+            tmem_st_wait();
         }
-        alive = mbar_wait(&bars[3], ph_m, kWaitLimit);
-        ph_m ^= 1;
-        if (__syncthreads_or(!alive)) break;
-        tc_fence_after();
-        // the K tile is free: prefetch the next one
-        if (threadIdx.x == 0 && c + 1 < nchunk) {
-            mbar_arrive_expect_tx(&bars[1], kBlk * nd);
-            for (int b = 0; b < nd; ++b) tma_load_3d(xk + b * kBlk, &tm_k, &bars[1], 64 * b, tc0 + kC, bh);
-        }
-        float mass;
-        float alpha = key_features(g, tmem, 0, 1, phk, valid, ep, &mass);
-        if (alpha != 1.f) {
-            // rescale the running state to the new reference
-            for (int cc = 32 * h; cc < g.dv + 16; cc += 64) {
-                float v[32];
-                tmem_ld32(tm_addr(tmem, q, col_s + cc), v);
+        auto convert_k = [&](int c) -> bool {
+            bool ok = st_wait(&bar_k[c & 1], (c >> 1) & 1, abortp);
+            float ss, am;
+            convert_tile_256(xk + (size_t)(c & 1) * xkb, nd, e, ss, am);
+            part[(e >> 7) * 128 + (e & 127)] = ss;
+            group_sync(kStEpi);
+            if (e < 128) nk[(c & 1) * 128 + e] = 0.5f * kLog2e * (part[e] + part[128 + e]);
+            fence_async_smem();
+            mbar_arrive(e_x);
+            return ok;
+        };
+        if (nchunk > 0) alive = convert_k(0);
+        for (int c = 0; c < nchunk; ++c) {
+            const int tc0 = t_begin + c * kC;
+            const int valid = min(kC, t_end - tc0);
+            const bool ok = row < valid;
+            if (c + 1 < nchunk) alive &= convert_k(c + 1);
+            // P_K(c) ready; phi_K buffer c % 2 free once the state update of c - 2 is done
+            alive &= st_wait(&bar_pk[c & 1], (c >> 1) & 1, abortp);
+            if (c >= 2) alive &= st_wait(&bar_s[c & 1], ((c - 2) >> 1) & 1, abortp);
+            tc_fence_after();
+            group_sync(kStEpi);   // norms of this chunk visible
+            uint8_t *phb = phk + (size_t)(c & 1) * 2 * kBlk;
+            const int pcol = 128 * (c & 1);
+            if (g.map == FAVOR_MAP_POSITIVE) {
+                float pv[64];
+                {
+                    float t0[32], t1[32];
+                    tmem_ld32(tm_addr(tmem, q, pcol + 64 * h), t0);
+                    tmem_ld32(tm_addr(tmem, q, pcol + 64 * h + 32), t1);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) { pv[i] = t0[i]; pv[32 + i] = t1[i]; }
+                }
+                const float nkr = nk[(c & 1) * 128 + row];
+                float alpha = 1.f;
+                if (R == -INFINITY) {
+                    float mx = -INFINITY;
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) mx = fmaxf(mx, pv[i]);
+                    R = st_grp_max(ok ? mx - nkr : -INFINITY, red, ew) - kShift;
+                }
+                float off = nkr + R;
+                float lmax = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < 64; ++i) lmax = fmaxf(lmax, pv[i] - off);
+                if (group_or(ok && lmax > kShift + kSlack, kStEpi)) {
+                    const float top = st_grp_max(ok ? lmax : -INFINITY, red, ew);
+                    const float Rn = R + (top - kShift);
+                    alpha = ex2(R - Rn);
+                    R = Rn;
+                    off = nkr + R;
+                    // rescale the running state: wait for the last state update
+                    if (c >= 1) alive &= st_wait(&bar_s[(c - 1) & 1], ((c - 1) >> 1) & 1, abortp);
+                    tc_fence_after();
+                    for (int cc = 32 * h; cc < g.dv + 16; cc += 64) {
+                        float v[32];
+                        tmem_ld32(tm_addr(tmem, q, col_s + cc), v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] *= alpha;
+                        tmem_st32(tm_addr(tmem, q, col_s + cc), v);
+                    }
+                    tmem_st_wait();
+                }
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+                    float v[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = ok ? ex2(pv[32 * b + i] - off) : 0.f;
+                    store_row32(phb + (size_t)h * kBlk, row, 32 * b, v);
+                }
+            } else if (g.map == FAVOR_MAP_TRIG) {
+                float v[32], s[32], co[32];
+                tmem_ld32(tm_addr(tmem, q, pcol + 32 * h), v);
                 tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] *= alpha;
-                tmem_st32(tm_addr(tmem, q, col_s + cc), v);
+                for (int i = 0; i < 32; ++i) {
+                    if (ok) sincos_reduced(v[i], s[i], co[i]);
+                    else s[i] = co[i] = 0.f;
+                }
+                store_row32(phb, row, 32 * h, s);
+                store_row32(phb + kBlk, row, 32 * h, co);
+            } else {
+                for (int b = 0; b < 2; ++b) {
+                    float v[32];
+                    tmem_ld32(tm_addr(tmem, q, pcol + 64 * h + 32 * b), v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = ok ? elu1(v[i]) : 0.f;
+                    store_row32(phb + (size_t)h * kBlk, row, 32 * b, v);
+                }
             }
-            tmem_st_wait();
-            mass_total *= alpha;
+            // V(c) -> fp16
+            alive &= st_wait(&bar_v[c % NSV], NSV == 2 ? ((c >> 1) & 1) : (c & 1), abortp);
+            {
+                float ss, am;
+                convert_tile_256(xv + (size_t)(c % NSV) * a.xv_stride, nvb, e, ss, am);
+                vmax = fmaxf(vmax, am);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(e_k);
         }
-        mass_total += mass;
-        alive = alive && mbar_wait(&bars[2], ph_v, kWaitLimit);
-        ph_v ^= 1;
-        if (__syncthreads_or(!alive)) break;
-        float ss, am;
-        convert_tile(xv, nvb, ss, am);
-        vmax = fmaxf(vmax, cta_max(am, red));
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
+        // the last state update, then S, z -> global with the tile's max |S| and max z
+        if (nchunk > 0) alive &= st_wait(&bar_s[(nchunk - 1) & 1], ((nchunk - 1) >> 1) & 1, abortp);
         tc_fence_after();
-        if (threadIdx.x == 0) {
-            issue_state_update(tmem, phk_s, xv_s, ones_s, 1, col_s, 0, nvb);
-            mma_commit(&bars[3]);
-        }
-        alive = mbar_wait(&bars[3], ph_m, kWaitLimit);
-        ph_m ^= 1;
-        if (__syncthreads_or(!alive)) break;
-        tc_fence_after();
-        if (threadIdx.x == 0 && c + 1 < nchunk) {
-            mbar_arrive_expect_tx(&bars[2], kBlk * nvb);
-            for (int b = 0; b < nvb; ++b) tma_load_3d(xv + b * kBlk, &tm_v, &bars[2], 64 * b, tc0 + kC, bh);
-        }
-    }
-    if (alive) {
-        // S, z -> global: thread (q, lane) owns feature ft*128 + 32q + lane; halves split columns
-        const int f = ft * 128 + q * 32 + lane;
+        const int f = ft * 128 + row;
         float *dst = a.state + (((size_t)bh * a.nseg + seg) * g.r + f) * (g.dv + 1);
+        const bool write = alive && !*abortp;
+        float smax = 0.f, zval = 0.f;
         for (int cc = 32 * h; cc < g.dv; cc += 64) {
             float v[32];
             tmem_ld32(tm_addr(tmem, q, col_s + cc), v);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) dst[cc + i] = v[i];
+            for (int i = 0; i < 32; ++i) {
+                smax = fmaxf(smax, fabsf(v[i]));
+                if (write) dst[cc + i] = v[i];
+            }
         }
-        if (h == 0) {
+        {
             float v[16];
             tmem_ld16(tm_addr(tmem, q, col_s + g.dv), v);
             tmem_ld_wait();
-            dst[g.dv] = v[0];
+            zval = fabsf(v[0]);
+            if (write && h == 0) dst[g.dv] = v[0];
         }
-        if (threadIdx.x == 0) {
-            float *m = a.meta + (((size_t)bh * a.nseg + seg) * g.n_ft + ft) * 4;
-            m[0] = *Rp;
-            m[1] = mass_total;
-            m[2] = vmax;
-            m[3] = 0.f;
+        const float vm = st_grp_max(vmax, red, ew);
+        const float sm_all = st_grp_max(smax, red, ew);
+        const float zm = st_grp_max(zval, red, ew);
+        if (write) {
+            if (e == 0) {
+                float *m = a.meta + (((size_t)bh * a.nseg + seg) * g.n_ft + ft) * 4;
+                m[0] = R;
+                m[1] = zm;
+                m[2] = vm;
+                m[3] = sm_all;
+            }
+        } else {
+            set_status(a.status, FAVOR_ERR_TIMEOUT);
         }
-    } else {
-        set_status(a.status, FAVOR_ERR_TIMEOUT);
     }
     tc_fence_before();
     __syncthreads();
@@ -545,17 +563,20 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
 }
 
 // ---------------------------------------------------------------------------
-// tc_combine: fixed-order combination of segment states.
-//  non-causal (one block per head): KV = sum_g S_g 2^(R_g - R*), z likewise;
-//    sigma = power of two with max|sigma KV| <= 16384; writes the fp16 state
+// tc_combine: fixed-order combination of segment states, rescaled to one key
+// reference R* (the largest of the segments'), grid (heads, outputs, slices):
+//  non-causal: KV = sum_g S_g 2^(R_g - R*), z likewise; sigma is a power of
+//    two with sigma * (bound on max |KV|) <= 16384; writes the fp16 state
 //    operand image [nvb][r][64] (128B-swizzled MN-major), z (fp32), sigma.
-//  causal (block per head and segment s >= 1): S_in(s) = sum_{g<s} ..., fp32
-//    [r][dv+1], plus (R_in, max_f z_f, vmax_in).
+//  causal (output s for segment s + 1): S_in = sum_{g <= s} ..., fp32
+//    [r][dv+1], with (R*, bound on max z, max |v|).
+// The bounds come from each segment tile's max z and max |S|.
 // ---------------------------------------------------------------------------
 struct CombineArgs {
     Geo g;
     int nseg;              // segment states available
     int causal;
+    int slice;             // elements per block
     const float *state, *meta;
     uint8_t *sop;          // non-causal: [BH][nvb][r][64] fp16 image
     float *zout;           // non-causal: [BH][r]
@@ -568,90 +589,73 @@ __global__ void tc_combine(const CombineArgs a) {
     const Geo &g = a.g;
     const int bh = blockIdx.x;
     const int upto = a.causal ? blockIdx.y + 1 : a.nseg;   // segments [0, upto)
-    __shared__ float red[32];
-    __shared__ float sh_R;
+    constexpr int kMaxScale = 256;
+    __shared__ float scale[kMaxScale];
+    __shared__ float sh[4];   // R*, z bound, |S| bound, vmax
     const float *meta = a.meta + (size_t)bh * a.nseg * g.n_ft * 4;
-    // reference: max over segments and feature tiles
-    float R = -INFINITY;
-    for (int i = threadIdx.x; i < upto * g.n_ft; i += blockDim.x) R = fmaxf(R, meta[i * 4]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) R = fmaxf(R, __shfl_xor_sync(0xffffffffu, R, o));
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = R;
-    __syncthreads();
+    const int nsc = upto * g.n_ft;
     if (threadIdx.x == 0) {
-        float r = -INFINITY;
-        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) r = fmaxf(r, red[i]);
-        sh_R = r;
+        float R = -INFINITY, vmax = 0.f;
+        for (int i = 0; i < nsc; ++i) {
+            R = fmaxf(R, meta[i * 4]);
+            vmax = fmaxf(vmax, meta[i * 4 + 2]);
+        }
+        float zb = 0.f, sb = 0.f;
+        for (int gi = 0; gi < upto; ++gi) {
+            float zt = 0.f, st = 0.f;
+            for (int t = 0; t < g.n_ft; ++t) {
+                const float *m = meta + (gi * g.n_ft + t) * 4;
+                float sc = 1.f;
+                if (g.map == FAVOR_MAP_POSITIVE) sc = (m[0] == -INFINITY || R == -INFINITY) ? 0.f : ex2(m[0] - R);
+                if (gi * g.n_ft + t < kMaxScale) scale[gi * g.n_ft + t] = sc;
+                zt = fmaxf(zt, m[1] * sc);
+                st = fmaxf(st, m[3] * sc);
+            }
+            zb += zt;
+            sb += st;
+        }
+        sh[0] = g.map == FAVOR_MAP_POSITIVE ? R : 0.f;
+        sh[1] = zb;
+        sh[2] = sb;
+        sh[3] = vmax;
     }
-    __syncthreads();
-    R = sh_R;
     __syncthreads();
     const int W = g.dv + 1;
     const size_t per = (size_t)g.r * W;
     const float *st = a.state + (size_t)bh * a.nseg * per;
-    float amax = 0.f, zmax = 0.f, vmax = 0.f;
-    // pass 1: sums into the output buffer (causal) or registers-free second pass (non-causal)
-    float *dst = a.causal ? a.s_in + ((size_t)bh * (a.nseg + 1) + upto) * per : nullptr;
-    for (size_t e = threadIdx.x; e < per; e += blockDim.x) {
-        const int f = (int)(e / W), c = (int)(e % W);
-        const int ftile = f / 128;
-        float s = 0.f;
-        for (int gi = 0; gi < upto; ++gi) {
-            float Rg = meta[(gi * g.n_ft + ftile) * 4];
-            float sc = (Rg == -INFINITY || R == -INFINITY) ? 0.f : ex2(Rg - R);
-            if (g.map != FAVOR_MAP_POSITIVE) sc = 1.f;
-            s += st[gi * per + e] * sc;
-        }
-        if (c < g.dv) amax = fmaxf(amax, fabsf(s));
-        else zmax = fmaxf(zmax, fabsf(s));
-        if (a.causal) {
-            dst[e] = s;
-        } else if (c == g.dv) {
-            a.zout[(size_t)bh * g.r + f] = s;
-        }
-    }
-    for (int gi = threadIdx.x; gi < upto * g.n_ft; gi += blockDim.x) vmax = fmaxf(vmax, meta[gi * 4 + 2]);
-    // block maxima
-    float vals[3] = {amax, zmax, vmax};
-    for (int k = 0; k < 3; ++k) {
-        float v = vals[k];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-        __syncthreads();
-        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-        __syncthreads();
-        float r = 0.f;
-        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) r = fmaxf(r, red[i]);
-        vals[k] = r;
-    }
+    const size_t e0 = (size_t)blockIdx.z * a.slice, e1 = min(per, e0 + a.slice);
     if (a.causal) {
-        if (threadIdx.x == 0) {
+        float *dst = a.s_in + ((size_t)bh * (a.nseg + 1) + upto) * per;
+        for (size_t e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
+            const int ftile = (int)(e / W) / 128;
+            float sum = 0.f;
+            for (int gi = 0; gi < upto; ++gi) sum += st[gi * per + e] * scale[gi * g.n_ft + ftile];
+            dst[e] = sum;
+        }
+        if (blockIdx.z == 0 && threadIdx.x == 0) {
             float *m = a.meta_in + ((size_t)bh * (a.nseg + 1) + upto) * 4;
-            m[0] = (g.map == FAVOR_MAP_POSITIVE) ? R : 0.f;
-            m[1] = vals[1];
-            m[2] = vals[2];
+            m[0] = sh[0];
+            m[1] = sh[1];
+            m[2] = sh[3];
             m[3] = 0.f;
         }
         return;
     }
-    // non-causal: sigma and the fp16 operand image (second pass over the sums)
-    float sigma = 1.f;
-    if (vals[0] > 0.f) sigma = exp2f(floorf(log2f(kSigmaTarget / vals[0])));
-    if (threadIdx.x == 0) a.sig[bh] = sigma;
+    const float sb = sh[2];
+    const float sigma = sb > 0.f ? exp2f(floorf(log2f(kSigmaTarget / sb))) : 1.f;
+    if (blockIdx.z == 0 && threadIdx.x == 0) a.sig[bh] = sigma;
     const int nvb = g.dv / 64;
     uint8_t *img = a.sop + (size_t)bh * nvb * g.r * 128;
-    for (size_t e = threadIdx.x; e < (size_t)g.r * g.dv; e += blockDim.x) {
-        const int f = (int)(e / g.dv), c = (int)(e % g.dv);
+    for (size_t e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
+        const int f = (int)(e / W), c = (int)(e % W);
         const int ftile = f / 128;
-        float s = 0.f;
-        for (int gi = 0; gi < upto; ++gi) {
-            float Rg = meta[(gi * g.n_ft + ftile) * 4];
-            float sc = (Rg == -INFINITY || R == -INFINITY) ? 0.f : ex2(Rg - R);
-            if (g.map != FAVOR_MAP_POSITIVE) sc = 1.f;
-            s += st[gi * per + (size_t)f * W + c] * sc;
-        }
-        *reinterpret_cast<__half *>(img + (size_t)(c / 64) * g.r * 128 + sw128_offset(f, c % 64)) =
-            __float2half_rn(s * sigma);
+        float sum = 0.f;
+        for (int gi = 0; gi < upto; ++gi) sum += st[gi * per + e] * scale[gi * g.n_ft + ftile];
+        if (c == g.dv)
+            a.zout[(size_t)bh * g.r + f] = sum;
+        else
+            *reinterpret_cast<__half *>(img + (size_t)(c / 64) * g.r * 128 + sw128_offset(f, c % 64)) =
+                __float2half_rn(sum * sigma);
     }
 }
 
@@ -959,18 +963,6 @@ __device__ __forceinline__ void grp_maxsum(float a, float b, float *red, int ew,
     }
 }
 
-__device__ __forceinline__ float grp_sum(float v, float *red, int ew) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    group_sync(kEpi);
-    if ((threadIdx.x & 31) == 0) red[ew] = v;
-    group_sync(kEpi);
-    float r = 0.f;
-#pragma unroll
-    for (int i = 0; i < kEpi / 32; ++i) r += red[i];
-    return r;
-}
-
 // In-place bf16 -> fp16 conversion of a [128][64 nblk] tile by 512 threads:
 // thread e converts two 16-byte chunks of row e % 128 per block (chunk index
 // rotated with the row).  Returns the partial sum of squares and max |x|.
@@ -1136,7 +1128,6 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
     const int e = threadIdx.x - 32, ew = e >> 5;
     const int q = (ew + 1) & 3, j = ew >> 2;
     const int row = q * 32 + lane;
-    constexpr int NF = NC;                 // features per thread (positive / elu); trig: 2 NC
     float R, zmax, vmax;
     {
         const float *m = a.meta_in + ((size_t)bh * a.nseg + seg) * 4;
@@ -1524,18 +1515,23 @@ CausalLayout causal_layout(const Geo &g) {
 }
 
 struct StateLayout {
-    uint32_t o_w, o_xk, o_xv, o_phk, o_ones, o_small, bytes;
+    uint32_t o_w, o_xk, o_xv, o_phk, o_small, xv_stride, bytes;
+    int nvs;
 };
 StateLayout state_layout(const Geo &g) {
     StateLayout l;
-    uint32_t o = 0;
-    l.o_w = o; o = align1k(o + (uint32_t)g.np_tile * g.d * 2);
-    l.o_xk = o; o = align1k(o + (uint32_t)kC * g.d * 2);
-    l.o_xv = o; o = align1k(o + (uint32_t)kC * g.dv * 2);
-    l.o_phk = o; o = align1k(o + 2 * kBlk);
-    l.o_ones = o; o = align1k(o + 4096);
-    l.o_small = o; o = align1k(o + 420 * 4);
-    l.bytes = o + 1024;
+    for (int nvs = 2; nvs >= 1; --nvs) {
+        uint32_t o = 0;
+        l.o_w = o; o = align1k(o + (uint32_t)g.np_tile * g.d * 2);
+        l.o_xk = o; o = align1k(o + 2u * kC * g.d * 2);
+        l.xv_stride = (uint32_t)(g.dv / 64 + 1) * kBlk;       // V blocks + ones atom
+        l.o_xv = o; o = align1k(o + (uint32_t)nvs * l.xv_stride);
+        l.o_phk = o; o = align1k(o + 4 * kBlk);
+        l.o_small = o; o = align1k(o + 576 * 4);
+        l.bytes = o + 1024;
+        l.nvs = nvs;
+        if (l.bytes <= 232448) break;
+    }
     return l;
 }
 
@@ -1604,7 +1600,8 @@ Plan make_plan(const Problem &p) {
     } else {
         G = (int)std::lround(2.0 * sms / (p.BH * g.n_ft));
     }
-    G = std::max(1, std::min(G, pl.nchunk));
+    // at most 64 segments: the combine keeps one scale per (segment, feature tile)
+    G = std::max(1, std::min(std::min(G, pl.nchunk), 64));
     const int seg_chunks = (pl.nchunk + G - 1) / G;
     pl.G = (pl.nchunk + seg_chunks - 1) / seg_chunks;
     pl.seg_len = seg_chunks * kC;
@@ -1665,14 +1662,13 @@ int tc_run(const void *q, const void *k, const void *v, const float *omega, floa
     if (nstate > 0) {
         StateLayout sl = state_layout(g);
         StateArgs sa;
-        sa.g = g; sa.H = p.H; sa.L = p.L; sa.seg_len = seg_len; sa.nseg = nstate;
+        sa.g = g; sa.H = p.H; sa.L = p.L; sa.seg_len = seg_len; sa.nseg = nstate; sa.nvs = sl.nvs;
         sa.omg = img; sa.state = state; sa.meta = meta; sa.status = dstat;
         sa.o_w = sl.o_w; sa.o_xk = sl.o_xk; sa.o_xv = sl.o_xv; sa.o_phk = sl.o_phk;
-        sa.o_ones = sl.o_ones; sa.o_small = sl.o_small;
-        sa.tmem_cols = (128 + p.dv + 16) <= 256 ? 256 : 512;
+        sa.o_small = sl.o_small; sa.xv_stride = sl.xv_stride; sa.tmem_cols = 512;
         if (cudaFuncSetAttribute(tc_state, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sl.bytes) != cudaSuccess)
             return FAVOR_ERR_CUDA;
-        tc_state<<<dim3(g.n_ft, nstate, p.BH), kThreads, sl.bytes, st>>>(mk, mv, sa);
+        tc_state<<<dim3(g.n_ft, nstate, p.BH), kStateThreads, sl.bytes, st>>>(mk, mv, sa);
         FAVOR_LAUNCH_CHECK();
     }
 
@@ -1683,7 +1679,9 @@ int tc_run(const void *q, const void *k, const void *v, const float *omega, floa
         CombineArgs ca{};
         ca.g = g; ca.nseg = nstate; ca.causal = 0; ca.state = state; ca.meta = meta;
         ca.sop = sop; ca.zout = z; ca.sig = sig;
-        tc_combine<<<dim3(p.BH, 1), 256, 0, st>>>(ca);
+        ca.slice = 2048;
+        const int nsl = (int)((per_state + ca.slice - 1) / ca.slice);
+        tc_combine<<<dim3(p.BH, 1, nsl), 256, 0, st>>>(ca);
         FAVOR_LAUNCH_CHECK();
         OutputLayout ol = output_layout(g);
         OutputArgs oa;
@@ -1710,7 +1708,9 @@ int tc_run(const void *q, const void *k, const void *v, const float *omega, floa
         CombineArgs ca{};
         ca.g = g; ca.nseg = nstate; ca.causal = 1; ca.state = state; ca.meta = meta;
         ca.s_in = s_in; ca.meta_in = meta_in;
-        tc_combine<<<dim3(p.BH, G - 1), 256, 0, st>>>(ca);
+        ca.slice = 2048;
+        const int nsl = (int)((per_state + ca.slice - 1) / ca.slice);
+        tc_combine<<<dim3(p.BH, G - 1, nsl), 256, 0, st>>>(ca);
         FAVOR_LAUNCH_CHECK();
     }
     CausalLayout cl = causal_layout(g);
