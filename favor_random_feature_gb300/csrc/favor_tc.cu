@@ -42,6 +42,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kShift = 8.0f * 1.4426950408889634f;   // e^8 headroom (log2 units)
 constexpr float kSlack = 2.0f * 1.4426950408889634f;   // tolerated excess before re-referencing
 constexpr float kSigmaTarget = 16384.f;  // bound for |sigma * S| in the fp16 state operand
+constexpr float kMaxFeature = 22026.4658f;  // e^10 = 2^(kShift + kSlack): largest key feature kept
 constexpr long long kWaitLimit = 1ll << 32;             // ~2 s of clock cycles
 constexpr uint32_t kBlk = 16384;        // one [128][64] fp16 block (128B swizzle)
 
@@ -965,7 +966,9 @@ __device__ __forceinline__ void grp_maxsum(float a, float b, float *red, int ew,
 
 // In-place bf16 -> fp16 conversion of a [128][64 nblk] tile by 512 threads:
 // thread e converts two 16-byte chunks of row e % 128 per block (chunk index
-// rotated with the row).  Returns the partial sum of squares and max |x|.
+// rotated with the row).  SQ / AMAX select the statistics it also returns:
+// the partial sum of squares (key norms) and max |x| (values).
+template <bool SQ, bool AMAX>
 __device__ __forceinline__ float convert_tile_512(uint8_t *tile, int nblk, int e, float &amax) {
     const int row = e & 127, part = e >> 7;
     float sumsq = 0.f;
@@ -981,8 +984,8 @@ __device__ __forceinline__ float convert_tile_512(uint8_t *tile, int nblk, int e
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
-                sumsq = fmaf(lo, lo, fmaf(hi, hi, sumsq));
-                amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
+                if (SQ) sumsq = fmaf(lo, lo, fmaf(hi, hi, sumsq));
+                if (AMAX) amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
                 o[i] = pack_half2(lo, hi);
             }
             *ptr = make_uint4(o[0], o[1], o[2], o[3]);
@@ -1026,7 +1029,7 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
     float *red = small + 1152;     // [32]
     uint64_t *bars = reinterpret_cast<uint64_t *>(small + 1184);
     uint64_t *bar_w = &bars[0], *bar_x = &bars[1], *bar_v = &bars[2], *bar_pk = &bars[3],
-             *bar_pq = &bars[4], *bar_a = &bars[5], *bar_av = &bars[6], *bar_avs = &bars[7];
+             *bar_pq = &bars[4], *bar_a = &bars[5], *bar_av = &bars[6];   // bars[7] unused
     uint64_t *e_x = &bars[8], *e_k = &bars[9], *e_sop = &bars[10], *e_q = &bars[11],
              *e_v = &bars[12], *e_b = &bars[13], *e_out = &bars[14];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1092,15 +1095,11 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
                         mma_f16_ts(tmem + kColDX, tmem + 8 * kk, smem_desc(sop_s + kk * 2048, kBlk, 1024), idx, kk > 0);
                 }
                 mma_commit(bar_a);
-                // A V and S += phi_K^T [V | 1]
+                // S += phi_K^T [V | 1] as soon as V is converted: it runs while
+                // the epilogue masks and scales the intra-chunk matrix
                 if (!(alive = ewait(e_v, ph, abortp))) break;
-                if (!(alive = ewait(e_b, ph, abortp))) break;
                 tc_fence_after();
                 {
-                    const uint32_t idv = idesc_f16(128, 64, 0, 1);
-                    for (int kk = 0; kk < kC / 16; ++kk)
-                        mma_f16_ts(tmem + kColDI, tmem + kColB + 8 * kk, smem_desc(v_s + kk * 2048, kBlk, 1024), idv, kk > 0);
-                    mma_commit(bar_av);
                     const uint32_t ids = idesc_f16(128, 80, 1, 1);
                     for (int t = 0; t < nft; ++t)
                         for (int kk = 0; kk < kC / 16; ++kk)
@@ -1108,15 +1107,23 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
                                     smem_desc(kb_s + (2 * t) * kKbBlk + kk * 2048, kKbBlk, 1024),
                                     smem_desc(v_s + kk * 2048, kBlk, 1024), ids, 1);
                 }
-                mma_commit(bar_avs);
+                // A V
+                if (!(alive = ewait(e_b, ph, abortp))) break;
+                tc_fence_after();
+                {
+                    const uint32_t idv = idesc_f16(128, 64, 0, 1);
+                    for (int kk = 0; kk < kC / 16; ++kk)
+                        mma_f16_ts(tmem + kColDI, tmem + kColB + 8 * kk, smem_desc(v_s + kk * 2048, kBlk, 1024), idv, kk > 0);
+                    mma_commit(bar_av);   // covers the state update issued before it
+                }
                 if (c + 1 < nchunk) {
-                    // next chunk's key projection once D_I has been read (A V done)
+                    // next chunk's key projection once D_I has been read
                     if (!(alive = ewait(e_x, (c + 1) & 1, abortp))) break;
                     if (!(alive = ewait(e_out, ph, abortp))) break;
                     tc_fence_after();
                     issue_proj(xk_s);
                     mma_commit(bar_pk);
-                    if (!(alive = ewait(bar_avs, ph, abortp))) break;
+                    if (!(alive = ewait(bar_av, ph, abortp))) break;
                     load_v(c + 1);
                 }
             }
@@ -1161,8 +1168,8 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
     auto convert_x = [&](int c) -> bool {
         const bool ok_x = ewait(bar_x, c & 1, abortp);
         float am;
-        convert_tile_512(xq, nd, e, am);
-        const float ss = convert_tile_512(xk, nd, e, am);
+        convert_tile_512<false, false>(xq, nd, e, am);
+        const float ss = convert_tile_512<true, false>(xk, nd, e, am);
         part[(e >> 7) * 128 + (e & 127)] = ss;
         group_sync(kEpi);
         if (e < 128) nk[e] = 0.5f * kLog2e * (part[e] + part[128 + e] + part[256 + e] + part[384 + e]);
@@ -1200,17 +1207,6 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
                 alpha = 0.f;
             }
             float off = nkr + R;
-            float lmax = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < NC; ++i) lmax = fmaxf(lmax, pv[i] - off);
-            if (group_or(ok && lmax > kShift + kSlack, kEpi)) {
-                // a key beyond the reference (rare): move the reference to it
-                const float top = grp_max(ok ? lmax : -INFINITY, red, ew);
-                const float Rn = R + (top - kShift);
-                alpha *= ex2(R - Rn);
-                R = Rn;
-                off = nkr + R;
-            }
 #pragma unroll
             for (int b = 0; b < NC / 8; ++b) {
                 float v[8];
@@ -1220,6 +1216,26 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
                     mf = fmaxf(mf, v[i]);
                 }
                 kb_store8(kb, row, NC * j + 8 * b, v);
+            }
+            // a feature beyond e^(shift + slack) means a key above the reference
+            // (rare): move the reference to that key and redo the features
+            if (group_or(mf > kMaxFeature, kEpi)) {
+                const float top = grp_max(ok ? log2f(mf) : -INFINITY, red, ew);
+                const float Rn = R + (top - kShift);
+                alpha *= ex2(R - Rn);
+                R = Rn;
+                off = nkr + R;
+                mf = 0.f;
+#pragma unroll
+                for (int b = 0; b < NC / 8; ++b) {
+                    float v[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        v[i] = ok ? ex2(pv[8 * b + i] - off) : 0.f;
+                        mf = fmaxf(mf, v[i]);
+                    }
+                    kb_store8(kb, row, NC * j + 8 * b, v);
+                }
             }
         } else if (g.map == FAVOR_MAP_TRIG) {
             // projection p -> features 128 (p / 64) + p % 64 (sin) and that + 64
@@ -1360,7 +1376,7 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
         alive &= ewait(bar_v, ph, abortp);
         {
             float am;
-            convert_tile_512(xv, 1, e, am);
+            convert_tile_512<false, true>(xv, 1, e, am);
             // one reduction: max |v| of this chunk and the key mass of its phi_K
             // (sum over keys of the largest feature), the bound on the next z
             float vm, ms;
@@ -1376,16 +1392,23 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
         alive &= ewait(bar_a, ph, abortp);
         tc_fence_after();
         float av[32];
-        tmem_ld32(tm_addr(tmem, q, kColBig + 32 * j), av);
-        tmem_ld_wait();
-        const int limit = min(row, valid - 1) - 32 * j;
+        const int limit = min(row, valid - 1) - 32 * j;   // keys j' <= limit (local index)
         float rs = 0.f, rm = 0.f;
+        if (limit < 0) {                 // this quarter lies entirely above the diagonal
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const float x = i <= limit ? av[i] : 0.f;
-            av[i] = x;
-            rs += x;
-            rm = fmaxf(rm, fabsf(x));
+            for (int i = 0; i < 32; ++i) av[i] = 0.f;
+        } else {
+            tmem_ld32(tm_addr(tmem, q, kColBig + 32 * j), av);
+            tmem_ld_wait();
+            if (limit < 31) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) av[i] = i <= limit ? av[i] : 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                rs += av[i];
+                rm = fmaxf(rm, fabsf(av[i]));
+            }
         }
         part[j * 128 + row] = rs;
         part2[j * 128 + row] = rm;
