@@ -273,6 +273,9 @@ def run_ours(args):
         evs[i][1].record(stream)
     torch.cuda.synchronize()
     t1 = time.time()
+    st = fv.favor_get_device_status(stream)
+    if st != fv.FAVOR_OK:
+        raise fv.FavorError(st, "device status after the timed steps")
     if dist:
         dist.barrier()
     stats = fv.favor_stats_read()
@@ -314,6 +317,9 @@ def run_ours(args):
     for _ in range(e2e_steps):
         check(ecall())
     te = (time.perf_counter() - te0) / e2e_steps
+    st = fv.favor_get_device_status(stream)
+    if st != fv.FAVOR_OK:
+        raise fv.FavorError(st, "device status after the end-to-end steps")
     if dist:
         t = torch.tensor([te], dtype=torch.float64, device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)

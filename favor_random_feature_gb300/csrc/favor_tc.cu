@@ -37,12 +37,12 @@ namespace {
 using namespace tc;
 
 constexpr int kC = 128;                 // tokens per chunk (= MMA M)
-constexpr int kThreads = 256;           // 8 warps: two per TMEM lane quarter
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kShift = 8.0f * 1.4426950408889634f;   // e^8 headroom (log2 units)
-constexpr float kSlack = 2.0f * 1.4426950408889634f;   // tolerated excess before re-referencing
 constexpr float kSigmaTarget = 16384.f;  // bound for |sigma * S| in the fp16 state operand
-constexpr float kMaxFeature = 22026.4658f;  // e^10 = 2^(kShift + kSlack): largest key feature kept
+// largest key feature kept, e^10: a chunk may exceed the reference by e^2
+// before the reference moves
+constexpr float kMaxFeature = 22026.4658f;
 constexpr long long kWaitLimit = 1ll << 32;             // ~2 s of clock cycles
 constexpr uint32_t kBlk = 16384;        // one [128][64] fp16 block (128B swizzle)
 
@@ -96,35 +96,6 @@ __device__ __forceinline__ void set_status(int *status, int code) {
     if (status) atomicExch(status, code);
 }
 
-// In-place bf16 -> fp16 conversion of a [128][64*nblk] tile (128B-swizzled
-// blocks of 16 KB).  Thread (row = tid % 128, half = tid / 128) converts four
-// 16-byte chunks of its row per block, rotating the chunk index with the row
-// so that eight consecutive rows hit distinct banks.  Returns this thread's
-// partial sum of squares and max |x| over its chunks.
-__device__ __forceinline__ void convert_tile(uint8_t *tile, int nblk, float &sumsq, float &amax) {
-    const int row = threadIdx.x & 127, half = threadIdx.x >> 7;
-    sumsq = 0.f;
-    amax = 0.f;
-    for (int b = 0; b < nblk; ++b) {
-        uint8_t *rp = tile + b * kBlk + row * 128;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            int p = (half * 4 + c + row) & 7;
-            uint4 *ptr = reinterpret_cast<uint4 *>(rp + p * 16);
-            uint4 u = *ptr;
-            uint32_t w[4] = {u.x, u.y, u.z, u.w}, o[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
-                sumsq = fmaf(lo, lo, fmaf(hi, hi, sumsq));
-                amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
-                o[i] = pack_half2(lo, hi);
-            }
-            *ptr = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-    }
-}
-
 // Store 32 features (fp16) of one row into a 128B-swizzled [128][64] block at
 // columns [c0, c0 + 32).
 __device__ __forceinline__ void store_row32(uint8_t *blk, int row, int c0, const float (&v)[32]) {
@@ -133,23 +104,6 @@ __device__ __forceinline__ void store_row32(uint8_t *blk, int row, int c0, const
         uint4 u = make_uint4(pack_half2(v[8 * c + 0], v[8 * c + 1]), pack_half2(v[8 * c + 2], v[8 * c + 3]),
                              pack_half2(v[8 * c + 4], v[8 * c + 5]), pack_half2(v[8 * c + 6], v[8 * c + 7]));
         *reinterpret_cast<uint4 *>(blk + sw128_offset(row, c0 + 8 * c)) = u;
-    }
-}
-
-__device__ __forceinline__ float half_lo(uint32_t u) { return __half2float(__ushort_as_half((unsigned short)(u & 0xffff))); }
-__device__ __forceinline__ float half_hi(uint32_t u) { return __half2float(__ushort_as_half((unsigned short)(u >> 16))); }
-
-// Reload 32 fp16 features of a row (as stored by store_row32) into floats.
-__device__ __forceinline__ void load_row32(const uint8_t *blk, int row, int c0, float (&v)[32]) {
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        uint4 u = *reinterpret_cast<const uint4 *>(blk + sw128_offset(row, c0 + 8 * c));
-        uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            v[8 * c + 2 * i] = half_lo(w[i]);
-            v[8 * c + 2 * i + 1] = half_hi(w[i]);
-        }
     }
 }
 
@@ -190,29 +144,6 @@ __global__ void tc_prep_omega(const float *__restrict__ omega, uint8_t *__restri
 }
 
 // ---------------------------------------------------------------------------
-// MMA issue helpers (one thread)
-// ---------------------------------------------------------------------------
-// P[:, 128 t .. ] = X W_tile^T for feature tiles [t0, t0 + nt); X K-major
-// [128][d] in nd blocks; W image K-major [nproj][64] per d block.
-// W image in smem: MN-major atoms [d][64] of 64 projections, the first one
-// holding projection 0 of the image.
-__device__ __forceinline__ void issue_projection(const Geo &g, uint32_t tmem, uint32_t x_s,
-                                                 uint32_t w_s, int w_rows, int t0, int nt, int col0) {
-    (void)w_rows;
-    const uint32_t idesc = idesc_f16(128, g.np_tile, 0, 1);
-    const int nk = g.d / 16;
-    for (int t = 0; t < nt; ++t) {
-        const int p0 = (t0 + t) * g.np_tile;
-        for (int kk = 0; kk < nk; ++kk) {
-            uint64_t a = smem_desc(x_s + (kk >> 2) * kBlk + (kk & 3) * 32, 16, 1024);
-            uint64_t b = smem_desc(w_s + (p0 / 64) * (uint32_t)g.d * 128 + kk * 2048,
-                                   (uint32_t)g.d * 128, 1024);
-            mma_f16(tmem + col0 + 128 * t, a, b, idesc, kk > 0);
-        }
-    }
-}
-
-// ---------------------------------------------------------------------------
 // tc_state: per (feature tile, segment, head) the segment state
 //   S[f][c] = sum_t phi(k_t)_f v_t[c],  z[f] = sum_t phi(k_t)_f
 // at the key reference R, written as fp32 [f][dv + 1] plus (R, max z, max|v|,
@@ -238,6 +169,7 @@ struct StateArgs {
 
 // in-place bf16 -> fp16 conversion of a [128][64 nblk] tile by 256 threads
 // (thread e: row e % 128, four 16-byte chunks of it per block)
+template <bool SQ, bool AMAX>
 __device__ __forceinline__ void convert_tile_256(uint8_t *tile, int nblk, int e, float &sumsq,
                                                  float &amax) {
     const int row = e & 127, half = e >> 7;
@@ -254,8 +186,8 @@ __device__ __forceinline__ void convert_tile_256(uint8_t *tile, int nblk, int e,
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
-                sumsq = fmaf(lo, lo, fmaf(hi, hi, sumsq));
-                amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
+                if (SQ) sumsq = fmaf(lo, lo, fmaf(hi, hi, sumsq));
+                if (AMAX) amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
                 o[i] = pack_half2(lo, hi);
             }
             *ptr = make_uint4(o[0], o[1], o[2], o[3]);
@@ -306,7 +238,8 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     float *red = small + 512;       // [8]
     uint64_t *bars = reinterpret_cast<uint64_t *>(small + 528);
     uint64_t *bar_w = &bars[0], *bar_k = &bars[1] /*[2]*/, *bar_v = &bars[3] /*[2]*/,
-             *bar_pk = &bars[5] /*[2]*/, *bar_s = &bars[7] /*[2]*/, *e_x = &bars[9], *e_k = &bars[10];
+             *bar_pk = &bars[5] /*[2]*/, *bar_s = &bars[7] /*[2]*/, *e_x = &bars[9] /*[2]*/,
+             *e_k = &bars[11] /*[2]*/;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(small + 560);
     volatile int *abortp = reinterpret_cast<volatile int *>(small + 562);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -314,7 +247,7 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < 9; ++i) mbar_init(&bars[i], 1);
-        for (int i = 9; i < 11; ++i) mbar_init(&bars[i], kStEpi);
+        for (int i = 9; i < 13; ++i) mbar_init(&bars[i], kStEpi);
         fence_mbar_init();
         *abortp = 0;
     }
@@ -364,14 +297,17 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                 load_k(1);
                 if (NSV == 2) load_v(1);
             }
-            alive = st_wait(bar_w, 0, abortp) && st_wait(e_x, 0, abortp);
+            // e_x and e_k alternate between two barriers per chunk parity: the
+            // epilogue may finish converting K(0) and K(1) before this thread
+            // looks, and one barrier would then have moved two phases on
+            alive = st_wait(bar_w, 0, abortp) && st_wait(&e_x[0], 0, abortp);
             if (alive) {
                 tc_fence_after();
                 issue_proj(0);
             }
             for (int c = 0; c < nchunk && alive; ++c) {
                 if (c + 1 < nchunk) {
-                    if (!(alive = st_wait(e_x, (c + 1) & 1, abortp))) break;
+                    if (!(alive = st_wait(&e_x[(c + 1) & 1], ((c + 1) >> 1) & 1, abortp))) break;
                     tc_fence_after();
                     issue_proj(c + 1);
                 }
@@ -381,7 +317,7 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                     if (!(alive = st_wait(&bar_pk[c & 1], (c >> 1) & 1, abortp))) break;
                     load_k(c + 2);
                 }
-                if (!(alive = st_wait(e_k, c & 1, abortp))) break;
+                if (!(alive = st_wait(&e_k[c & 1], (c >> 1) & 1, abortp))) break;
                 tc_fence_after();
                 {
                     const uint32_t idesc = idesc_f16(128, g.dv + 16, 1, 1);
@@ -417,12 +353,12 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         auto convert_k = [&](int c) -> bool {
             bool ok = st_wait(&bar_k[c & 1], (c >> 1) & 1, abortp);
             float ss, am;
-            convert_tile_256(xk + (size_t)(c & 1) * xkb, nd, e, ss, am);
+            convert_tile_256<true, false>(xk + (size_t)(c & 1) * xkb, nd, e, ss, am);
             part[(e >> 7) * 128 + (e & 127)] = ss;
             group_sync(kStEpi);
             if (e < 128) nk[(c & 1) * 128 + e] = 0.5f * kLog2e * (part[e] + part[128 + e]);
             fence_async_smem();
-            mbar_arrive(e_x);
+            mbar_arrive(&e_x[c & 1]);
             return ok;
         };
         if (nchunk > 0) alive = convert_k(0);
@@ -457,16 +393,25 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                     R = st_grp_max(ok ? mx - nkr : -INFINITY, red, ew) - kShift;
                 }
                 float off = nkr + R;
-                float lmax = -INFINITY;
+                float mf = 0.f;
 #pragma unroll
-                for (int i = 0; i < 64; ++i) lmax = fmaxf(lmax, pv[i] - off);
-                if (group_or(ok && lmax > kShift + kSlack, kStEpi)) {
-                    const float top = st_grp_max(ok ? lmax : -INFINITY, red, ew);
+                for (int b = 0; b < 2; ++b) {
+                    float v[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        v[i] = ok ? ex2(pv[32 * b + i] - off) : 0.f;
+                        mf = fmaxf(mf, v[i]);
+                    }
+                    store_row32(phb + (size_t)h * kBlk, row, 32 * b, v);
+                }
+                if (group_or(mf > kMaxFeature, kStEpi)) {
+                    // a key above the reference (rare): move it, rescale the
+                    // running state, redo the features
+                    const float top = st_grp_max(ok ? log2f(mf) : -INFINITY, red, ew);
                     const float Rn = R + (top - kShift);
                     alpha = ex2(R - Rn);
                     R = Rn;
                     off = nkr + R;
-                    // rescale the running state: wait for the last state update
                     if (c >= 1) alive &= st_wait(&bar_s[(c - 1) & 1], ((c - 1) >> 1) & 1, abortp);
                     tc_fence_after();
                     for (int cc = 32 * h; cc < g.dv + 16; cc += 64) {
@@ -478,13 +423,13 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                         tmem_st32(tm_addr(tmem, q, col_s + cc), v);
                     }
                     tmem_st_wait();
-                }
 #pragma unroll
-                for (int b = 0; b < 2; ++b) {
-                    float v[32];
+                    for (int b = 0; b < 2; ++b) {
+                        float v[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = ok ? ex2(pv[32 * b + i] - off) : 0.f;
-                    store_row32(phb + (size_t)h * kBlk, row, 32 * b, v);
+                        for (int i = 0; i < 32; ++i) v[i] = ok ? ex2(pv[32 * b + i] - off) : 0.f;
+                        store_row32(phb + (size_t)h * kBlk, row, 32 * b, v);
+                    }
                 }
             } else if (g.map == FAVOR_MAP_TRIG) {
                 float v[32], s[32], co[32];
@@ -511,12 +456,12 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             alive &= st_wait(&bar_v[c % NSV], NSV == 2 ? ((c >> 1) & 1) : (c & 1), abortp);
             {
                 float ss, am;
-                convert_tile_256(xv + (size_t)(c % NSV) * a.xv_stride, nvb, e, ss, am);
+                convert_tile_256<false, true>(xv + (size_t)(c % NSV) * a.xv_stride, nvb, e, ss, am);
                 vmax = fmaxf(vmax, am);
             }
             fence_async_smem();
             tc_fence_before();
-            mbar_arrive(e_k);
+            mbar_arrive(&e_k[c & 1]);
         }
         // the last state update, then S, z -> global with the tile's max |S| and max z
         if (nchunk > 0) alive &= st_wait(&bar_s[(nchunk - 1) & 1], ((nchunk - 1) >> 1) & 1, abortp);
@@ -567,8 +512,9 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
 // tc_combine: fixed-order combination of segment states, rescaled to one key
 // reference R* (the largest of the segments'), grid (heads, outputs, slices):
 //  non-causal: KV = sum_g S_g 2^(R_g - R*), z likewise; sigma is a power of
-//    two with sigma * (bound on max |KV|) <= 16384; writes the fp16 state
-//    operand image [nvb][r][64] (128B-swizzled MN-major), z (fp32), sigma.
+//    two with sigma * (bound on max |KV| and max z) <= 16384; writes the fp16
+//    operand image of [sigma KV | sigma z]: nvb atoms [r][64] of KV and one
+//    z atom (128B-swizzled MN-major).
 //  causal (output s for segment s + 1): S_in = sum_{g <= s} ..., fp32
 //    [r][dv+1], with (R*, bound on max z, max |v|).
 // The bounds come from each segment tile's max z and max |S|.
@@ -579,9 +525,7 @@ struct CombineArgs {
     int causal;
     int slice;             // elements per block
     const float *state, *meta;
-    uint8_t *sop;          // non-causal: [BH][nvb][r][64] fp16 image
-    float *zout;           // non-causal: [BH][r]
-    float *sig;            // non-causal: [BH]
+    uint8_t *sop;          // non-causal: [BH][nvb + 1][r][64] fp16 image
     float *s_in;           // causal: [BH][nseg+1][r][dv+1]
     float *meta_in;        // causal: [BH][nseg+1][4]
 };
@@ -642,241 +586,26 @@ __global__ void tc_combine(const CombineArgs a) {
         }
         return;
     }
-    const float sb = sh[2];
+    const float sb = fmaxf(sh[2], sh[1]);
     const float sigma = sb > 0.f ? exp2f(floorf(log2f(kSigmaTarget / sb))) : 1.f;
-    if (blockIdx.z == 0 && threadIdx.x == 0) a.sig[bh] = sigma;
     const int nvb = g.dv / 64;
-    uint8_t *img = a.sop + (size_t)bh * nvb * g.r * 128;
+    uint8_t *img = a.sop + (size_t)bh * (nvb + 1) * g.r * 128;
     for (size_t e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
         const int f = (int)(e / W), c = (int)(e % W);
         const int ftile = f / 128;
         float sum = 0.f;
         for (int gi = 0; gi < upto; ++gi) sum += st[gi * per + e] * scale[gi * g.n_ft + ftile];
-        if (c == g.dv)
-            a.zout[(size_t)bh * g.r + f] = sum;
-        else
+        if (c == g.dv) {
+            // z atom: column 0 holds sigma z, columns 1..15 (the rest of the
+            // N = 80 operand) zero
+            uint8_t *za = img + (size_t)nvb * g.r * 128;
+            const uint32_t lo = __half_as_ushort(__float2half_rn(sum * sigma));
+            *reinterpret_cast<uint4 *>(za + sw128_offset(f, 0)) = make_uint4(lo, 0u, 0u, 0u);
+            *reinterpret_cast<uint4 *>(za + sw128_offset(f, 8)) = make_uint4(0u, 0u, 0u, 0u);
+        } else
             *reinterpret_cast<__half *>(img + (size_t)(c / 64) * g.r * 128 + sw128_offset(f, c % 64)) =
                 __float2half_rn(sum * sigma);
     }
-}
-
-// ---------------------------------------------------------------------------
-// Query feature epilogue (tc_output, tc_causal).  P for all n_ft tiles is in
-// TMEM [0, 128 n_ft).  Writes fp16 query features to phq (blocks of 64) and
-// returns this thread's partial phi(q) . z over its columns (z fp32 in smem).
-// ---------------------------------------------------------------------------
-__device__ float query_features(const Geo &g, uint32_t tmem, uint8_t *phq, const float *zs,
-                                float *part) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int q = warp & 3, h = warp >> 2;
-    const int row = q * 32 + lane;
-    float den = 0.f;
-    if (g.map == FAVOR_MAP_POSITIVE) {
-        float mx = -INFINITY;
-        for (int t = 0; t < g.n_ft; ++t)
-            for (int c = 0; c < 2; ++c) {
-                float v[32];
-                tmem_ld32(tm_addr(tmem, q, 128 * t + 64 * h + 32 * c), v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, v[i]);
-            }
-        part[h * 128 + row] = mx;
-        __syncthreads();
-        const float off = fmaxf(part[row], part[128 + row]) - kShift;
-        for (int t = 0; t < g.n_ft; ++t) {
-            uint8_t *blk = phq + (size_t)(2 * t + h) * kBlk;
-            for (int c = 0; c < 2; ++c) {
-                float v[32];
-                tmem_ld32(tm_addr(tmem, q, 128 * t + 64 * h + 32 * c), v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = ex2(v[i] - off);
-                store_row32(blk, row, 32 * c, v);
-                float r[32];
-                load_row32(blk, row, 32 * c, r);   // the rounded values the MMA sees
-                const float *z = zs + 128 * t + 64 * h + 32 * c;
-#pragma unroll
-                for (int i = 0; i < 32; ++i) den = fmaf(r[i], z[i], den);
-            }
-        }
-    } else if (g.map == FAVOR_MAP_TRIG) {
-        for (int t = 0; t < g.n_ft; ++t) {
-            float v[32], s[32], co[32];
-            tmem_ld32(tm_addr(tmem, q, 128 * t + 32 * h), v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) sincos_reduced(v[i], s[i], co[i]);
-            uint8_t *bs = phq + (size_t)(2 * t) * kBlk, *bc = phq + (size_t)(2 * t + 1) * kBlk;
-            store_row32(bs, row, 32 * h, s);
-            store_row32(bc, row, 32 * h, co);
-            float rs[32], rc[32];
-            load_row32(bs, row, 32 * h, rs);
-            load_row32(bc, row, 32 * h, rc);
-            const float *zsn = zs + 128 * t + 32 * h, *zco = zs + 128 * t + 64 + 32 * h;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) den = fmaf(rs[i], zsn[i], fmaf(rc[i], zco[i], den));
-        }
-    } else {
-        for (int t = 0; t < g.n_ft; ++t) {
-            uint8_t *blk = phq + (size_t)(2 * t + h) * kBlk;
-            for (int c = 0; c < 2; ++c) {
-                float v[32];
-                tmem_ld32(tm_addr(tmem, q, 128 * t + 64 * h + 32 * c), v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = elu1(v[i]);
-                store_row32(blk, row, 32 * c, v);
-                float r[32];
-                load_row32(blk, row, 32 * c, r);
-                const float *z = zs + 128 * t + 64 * h + 32 * c;
-#pragma unroll
-                for (int i = 0; i < 32; ++i) den = fmaf(r[i], z[i], den);
-            }
-        }
-    }
-    return den;
-}
-
-// D (M = 128 queries, N = 64) = phi_Q S_op over K = r features.
-__device__ __forceinline__ void issue_inter(const Geo &g, uint32_t tmem_d, uint32_t phq_s,
-                                            uint32_t sop_s, int accumulate_first) {
-    const uint32_t idesc = idesc_f16(128, 64, 0, 1);
-    for (int kk = 0; kk < g.r / 16; ++kk) {
-        uint64_t a = smem_desc(phq_s + (kk >> 2) * kBlk + (kk & 3) * 32, 16, 1024);
-        uint64_t b = smem_desc(sop_s + kk * 2048, kBlk, 1024);
-        mma_f16(tmem_d, a, b, idesc, (kk > 0) || accumulate_first);
-    }
-}
-
-// Write a [128][64] fp32 output tile (values given per thread: row, 32
-// columns at 32 h) into the staging area as two 128B-swizzled [128][32]
-// halves for the TMA store.
-__device__ __forceinline__ void stage_out(uint8_t *stage, int row, int h, const float (&o)[32]) {
-    uint8_t *half = stage + h * kBlk;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        int p = (c ^ (row & 7));
-        *reinterpret_cast<float4 *>(half + row * 128 + p * 16) =
-            make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
-    }
-}
-
-// ---------------------------------------------------------------------------
-// tc_output: non-causal rows.  Grid (row groups, dv tiles, heads).
-// ---------------------------------------------------------------------------
-struct OutputArgs {
-    Geo g;
-    int H, L, chunks_per_cta;
-    const uint8_t *omg, *sop;
-    const float *z, *sig;
-    int *status;
-    uint32_t o_w, o_xq, o_sop, o_phq, o_stage, o_small, tmem_cols;
-};
-
-__global__ void __launch_bounds__(kThreads, 1)
-tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_out,
-          const OutputArgs a) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const Geo &g = a.g;
-    const int dvt = blockIdx.y, bh = blockIdx.z, head = bh % a.H;
-    const int nchunk_total = (a.L + kC - 1) / kC;
-    const int c_begin = blockIdx.x * a.chunks_per_cta;
-    const int c_end = min(nchunk_total, c_begin + a.chunks_per_cta);
-    const int nd = g.d / 64;
-    uint8_t *w = sm + a.o_w, *xq = sm + a.o_xq, *sop = sm + a.o_sop, *phq = sm + a.o_phq,
-            *stage = sm + a.o_stage;
-    float *small = reinterpret_cast<float *>(sm + a.o_small);
-    float *zs = small, *part = small + 256, *dpart = small + 512;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(small + 776);   // 0: w+sop, 1: q, 2: mma
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(small + 784);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = warp & 3, h = warp >> 2;
-    const int row = q * 32 + lane;
-
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
-        fence_mbar_init();
-    }
-    if (warp == 0) tmem_alloc(tslot, a.tmem_cols);
-    for (int f = threadIdx.x; f < g.r; f += kThreads) zs[f] = a.z[(size_t)bh * g.r + f];
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tslot;
-    const int col_d = 256;
-    const float inv_sigma = 1.f / a.sig[bh];
-    if (threadIdx.x == 0 && c_begin < c_end) {
-        const uint32_t wbytes = (uint32_t)g.nproj * g.d * 2, sbytes = (uint32_t)g.r * 128;
-        mbar_arrive_expect_tx(&bars[0], wbytes + sbytes);
-        bulk_load(w, a.omg + (size_t)head * wbytes, wbytes, &bars[0]);
-        bulk_load(sop, a.sop + ((size_t)bh * (g.dv / 64) + dvt) * sbytes, sbytes, &bars[0]);
-        mbar_arrive_expect_tx(&bars[1], kBlk * nd);
-        for (int b = 0; b < nd; ++b) tma_load_3d(xq + b * kBlk, &tm_q, &bars[1], 64 * b, c_begin * kC, bh);
-    }
-    bool alive = mbar_wait(&bars[0], 0, kWaitLimit);
-    uint32_t ph_q = 0, ph_m = 0;
-    const uint32_t w_s = smem_u32(w), xq_s = smem_u32(xq), sop_s = smem_u32(sop), phq_s = smem_u32(phq);
-    for (int c = c_begin; c < c_end; ++c) {
-        alive = alive && mbar_wait(&bars[1], ph_q, kWaitLimit);
-        ph_q ^= 1;
-        if (__syncthreads_or(!alive)) break;
-        float ss, am;
-        convert_tile(xq, nd, ss, am);
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        if (threadIdx.x == 0) {
-            issue_projection(g, tmem, xq_s, w_s, g.nproj, 0, g.n_ft, 0);
-            mma_commit(&bars[2]);
-        }
-        alive = mbar_wait(&bars[2], ph_m, kWaitLimit);
-        ph_m ^= 1;
-        if (__syncthreads_or(!alive)) break;
-        tc_fence_after();
-        if (threadIdx.x == 0 && c + 1 < c_end) {
-            mbar_arrive_expect_tx(&bars[1], kBlk * nd);
-            for (int b = 0; b < nd; ++b) tma_load_3d(xq + b * kBlk, &tm_q, &bars[1], 64 * b, (c + 1) * kC, bh);
-        }
-        float den = query_features(g, tmem, phq, zs, part);
-        dpart[h * 128 + row] = den;
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        if (threadIdx.x == 0) {
-            issue_inter(g, tmem + col_d, phq_s, sop_s, 0);
-            mma_commit(&bars[2]);
-        }
-        alive = mbar_wait(&bars[2], ph_m, kWaitLimit);
-        ph_m ^= 1;
-        if (__syncthreads_or(!alive)) break;
-        tc_fence_after();
-        const float dn = dpart[row] + dpart[128 + row];
-        float o[32];
-        tmem_ld32(tm_addr(tmem, q, col_d + 32 * h), o);
-        tmem_ld_wait();
-        const float scale = inv_sigma / dn;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] *= scale;
-        if (threadIdx.x == 0) bulk_wait_read0();
-        __syncthreads();
-        stage_out(stage, row, h, o);
-        fence_async_smem();
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            tma_store_3d(&tm_out, stage, 64 * dvt, c * kC, bh);
-            tma_store_3d(&tm_out, stage + kBlk, 64 * dvt + 32, c * kC, bh);
-            bulk_commit();
-        }
-    }
-    if (threadIdx.x == 0) bulk_wait0();
-    if (!alive) set_status(a.status, FAVOR_ERR_TIMEOUT);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, a.tmem_cols);
 }
 
 // ---------------------------------------------------------------------------
@@ -1503,6 +1232,247 @@ tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
 }
 
 // ---------------------------------------------------------------------------
+// tc_output: non-causal rows, warp-specialised like tc_causal.  The grid is a
+// flat list of (head, dv tile, 128-row chunk) units split evenly over about
+// one CTA per SM; a CTA reloads W and the state operand when its units move to
+// another head.  Per unit: P_Q = Q W^T (N = all projections) -> phi(Q) packed
+// into TMEM -> D = phi(Q) [sigma KV | sigma z] (N = 64 + 16, B MN-major) ->
+// out = D[:, :64] / D[:, 64] (sigma cancels).
+// ---------------------------------------------------------------------------
+struct OutputArgs {
+    Geo g;
+    int H, L, total_units, nq;     // nq: Q tile slots (1 or 2)
+    const uint8_t *omg, *sop;      // W images; state images [BH][nvb + 1][r][64]
+    int *status;
+    uint32_t o_w, o_s, o_x, o_stage, o_small, tmem_cols;
+};
+
+constexpr int kOutThreads = 32 + kEpi;
+
+template <int NC>
+__device__ void output_body(const OutputArgs &a, uint8_t *sm, uint32_t tmem,
+                            const CUtensorMap *tm_q, const CUtensorMap *tm_out) {
+    const Geo &g = a.g;
+    const int nvb = g.dv / 64, nchunk = (a.L + kC - 1) / kC;
+    // units [u0, u1): an even split, CTAs differ by at most one unit
+    const int u0 = (int)((long long)blockIdx.x * a.total_units / gridDim.x);
+    const int u1 = (int)((long long)(blockIdx.x + 1) * a.total_units / gridDim.x);
+    const int n = u1 - u0, nq = a.nq;
+    const int nd = g.d / 64;
+    const uint32_t xb = (uint32_t)kC * g.d * 2;
+    uint8_t *w = sm + a.o_w, *sbuf = sm + a.o_s, *xs = sm + a.o_x, *stage = sm + a.o_stage;
+    float *small = reinterpret_cast<float *>(sm + a.o_small);
+    float *part = small;            // [4][128]
+    float *red = small + 512;       // [32]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(small + 544);
+    uint64_t *bar_w = &bars[0], *bar_x = &bars[1] /*[2]*/, *bar_pq = &bars[3], *bar_d = &bars[4],
+             *e_x = &bars[5], *e_q = &bars[6];
+    volatile int *abortp = reinterpret_cast<volatile int *>(small + 570);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int kColD = 256;
+    auto unit_bh = [&](int u) { return u / (nvb * nchunk); };
+    auto unit_dvt = [&](int u) { return (u / nchunk) % nvb; };
+    auto unit_c = [&](int u) { return u % nchunk; };
+    bool alive = true;
+
+    if (warp == 0) {
+        if (lane == 0 && n > 0) {
+            const uint32_t w_s = smem_u32(w), s_s = smem_u32(sbuf), xs_s = smem_u32(xs);
+            const uint32_t wbytes = (uint32_t)g.nproj * g.d * 2, atom = (uint32_t)g.r * 128;
+            int wphase = 0, cur = -1;
+            auto load_operands = [&](int u) {
+                const int bh = unit_bh(u), dvt = unit_dvt(u);
+                mbar_arrive_expect_tx(bar_w, wbytes + 2 * atom);
+                bulk_load(w, a.omg + (size_t)(bh % a.H) * wbytes, wbytes, bar_w);
+                const uint8_t *img = a.sop + (size_t)bh * (nvb + 1) * atom;
+                bulk_load(sbuf, img + (size_t)dvt * atom, atom, bar_w);
+                bulk_load(sbuf + atom, img + (size_t)nvb * atom, atom, bar_w);
+            };
+            auto load_q = [&](int i) {
+                const int u = u0 + i, s = i % nq;
+                mbar_arrive_expect_tx(&bar_x[s], xb);
+                for (int b = 0; b < nd; ++b)
+                    tma_load_3d(xs + (size_t)s * xb + b * kBlk, tm_q, &bar_x[s], 64 * b, unit_c(u) * kC, unit_bh(u));
+            };
+            for (int i = 0; i < min(n, nq); ++i) load_q(i);
+            for (int i = 0; i < n && alive; ++i) {
+                const int u = u0 + i;
+                const int key = unit_bh(u) * nvb + unit_dvt(u);
+                if (key != cur) {
+                    // new head / dv tile: every MMA on the old operands has completed
+                    load_operands(u);
+                    if (!(alive = ewait(bar_w, wphase & 1, abortp))) break;
+                    ++wphase;
+                    cur = key;
+                }
+                if (!(alive = ewait(e_x, i & 1, abortp))) break;
+                tc_fence_after();
+                {
+                    const uint32_t x_s = xs_s + (uint32_t)(i % nq) * xb;
+                    const uint32_t idesc = idesc_f16(128, g.nproj, 0, 1);
+                    for (int kk = 0; kk < g.d / 16; ++kk)
+                        mma_f16(tmem, smem_desc(x_s + (kk >> 2) * kBlk + (kk & 3) * 32, 16, 1024),
+                                smem_desc(w_s + kk * 2048, (uint32_t)g.d * 128, 1024), idesc, kk > 0);
+                    mma_commit(bar_pq);
+                }
+                if (!(alive = ewait(bar_pq, i & 1, abortp))) break;
+                if (i + nq < n) load_q(i + nq);
+                if (!(alive = ewait(e_q, i & 1, abortp))) break;
+                tc_fence_after();
+                {
+                    const uint32_t idesc = idesc_f16(128, 80, 0, 1);
+                    for (int kk = 0; kk < g.r / 16; ++kk)
+                        mma_f16_ts(tmem + kColD, tmem + 8 * kk, smem_desc(s_s + kk * 2048, atom, 1024), idesc, kk > 0);
+                    mma_commit(bar_d);
+                }
+                if (!(alive = ewait(bar_d, i & 1, abortp))) break;
+            }
+            if (!alive) set_status(a.status, FAVOR_ERR_TIMEOUT);
+        }
+        return;
+    }
+    const int e = threadIdx.x - 32, ew = e >> 5;
+    const int q = (ew + 1) & 3, j = ew >> 2;
+    const int row = q * 32 + lane;
+    auto convert_x = [&](int i) -> bool {
+        const bool ok = ewait(&bar_x[i % nq], (i / nq) & 1, abortp);
+        float am;
+        convert_tile_512<false, false>(xs + (size_t)(i % nq) * xb, nd, e, am);
+        tc_fence_before();
+        fence_async_smem();
+        mbar_arrive(e_x);
+        return ok;
+    };
+    if (n > 0) alive = convert_x(0);
+    for (int i = 0; i < n; ++i) {
+        const int u = u0 + i;
+        // ---- query features -> phi_Q packed in TMEM [0, r/2) ----
+        alive &= ewait(bar_pq, i & 1, abortp);
+        tc_fence_after();
+        float pv[NC];
+#pragma unroll
+        for (int b = 0; b < NC / 16; ++b) {
+            float t16[16];
+            tmem_ld16(tm_addr(tmem, q, NC * j + 16 * b), t16);
+#pragma unroll
+            for (int k2 = 0; k2 < 16; ++k2) pv[16 * b + k2] = t16[k2];
+        }
+        tmem_ld_wait();
+        if (g.map == FAVOR_MAP_POSITIVE) {
+            float mx = -INFINITY;
+#pragma unroll
+            for (int k2 = 0; k2 < NC; ++k2) mx = fmaxf(mx, pv[k2]);
+            part[j * 128 + row] = mx;
+        }
+        tc_fence_before();
+        group_sync(kEpi);   // every projection column read: phi_Q may overwrite them
+        tc_fence_after();
+        if (g.map == FAVOR_MAP_POSITIVE) {
+            const float qoff = fmaxf(fmaxf(part[row], part[128 + row]), fmaxf(part[256 + row], part[384 + row])) - kShift;
+#pragma unroll
+            for (int b = 0; b < NC / 32; ++b) {
+                uint32_t o[16];
+#pragma unroll
+                for (int k2 = 0; k2 < 16; ++k2)
+                    o[k2] = pack_half2(ex2(pv[32 * b + 2 * k2] - qoff), ex2(pv[32 * b + 2 * k2 + 1] - qoff));
+                tmem_st16(tm_addr(tmem, q, (NC * j + 32 * b) / 2), o);
+            }
+        } else if (g.map == FAVOR_MAP_TRIG) {
+            const int fs = 128 * ((NC * j) / 64) + (NC * j) % 64;
+#pragma unroll
+            for (int b = 0; b < NC / 16; ++b) {
+                uint32_t os[8], oc[8];
+#pragma unroll
+                for (int k2 = 0; k2 < 8; ++k2) {
+                    float s0, c0, s1, c1;
+                    sincos_reduced(pv[16 * b + 2 * k2], s0, c0);
+                    sincos_reduced(pv[16 * b + 2 * k2 + 1], s1, c1);
+                    os[k2] = pack_half2(s0, s1);
+                    oc[k2] = pack_half2(c0, c1);
+                }
+                tmem_st8(tm_addr(tmem, q, (fs + 16 * b) / 2), os);
+                tmem_st8(tm_addr(tmem, q, (fs + 64 + 16 * b) / 2), oc);
+            }
+        } else {
+#pragma unroll
+            for (int b = 0; b < NC / 32; ++b) {
+                uint32_t o[16];
+#pragma unroll
+                for (int k2 = 0; k2 < 16; ++k2)
+                    o[k2] = pack_half2(elu1(pv[32 * b + 2 * k2]), elu1(pv[32 * b + 2 * k2 + 1]));
+                tmem_st16(tm_addr(tmem, q, (NC * j + 32 * b) / 2), o);
+            }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(e_q);
+        // ---- next unit's Q tile (while the MMA runs) ----
+        if (i + 1 < n) alive &= convert_x(i + 1);
+        // ---- output ----
+        alive &= ewait(bar_d, i & 1, abortp);
+        tc_fence_after();
+        float dn[16], dd[16];
+        tmem_ld16(tm_addr(tmem, q, kColD + 16 * j), dn);
+        tmem_ld16(tm_addr(tmem, q, kColD + 64), dd);
+        tmem_ld_wait();
+        if (e == 0) bulk_wait_read0();   // the previous unit's staging has been read
+        group_sync(kEpi);
+        {
+            const float id = 1.f / dd[0];
+            uint8_t *halfp = stage + (size_t)((16 * j) >> 5) * kBlk;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const int col = (16 * j + 4 * cc) & 31;
+                const int p = (col >> 2) ^ (row & 7);
+                *reinterpret_cast<float4 *>(halfp + row * 128 + p * 16) =
+                    make_float4(dn[4 * cc] * id, dn[4 * cc + 1] * id, dn[4 * cc + 2] * id, dn[4 * cc + 3] * id);
+            }
+        }
+        fence_async_smem();
+        group_sync(kEpi);
+        if (e == 0 && !*abortp) {
+            tma_store_3d(tm_out, stage, 64 * unit_dvt(u), unit_c(u) * kC, unit_bh(u));
+            tma_store_3d(tm_out, stage + kBlk, 64 * unit_dvt(u) + 32, unit_c(u) * kC, unit_bh(u));
+            bulk_commit();
+        }
+    }
+    if (e == 0) bulk_wait0();
+    if (!alive) set_status(a.status, FAVOR_ERR_TIMEOUT);
+}
+
+__global__ void __launch_bounds__(kOutThreads, 1)
+tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_out,
+          const OutputArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float *small = reinterpret_cast<float *>(sm + a.o_small);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(small + 544);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(small + 568);
+    volatile int *abortp = reinterpret_cast<volatile int *>(small + 570);
+    const int warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 5; ++i) mbar_init(&bars[i], 1);
+        for (int i = 5; i < 7; ++i) mbar_init(&bars[i], kEpi);
+        fence_mbar_init();
+        *abortp = 0;
+    }
+    if (warp == 0) tmem_alloc(tslot, a.tmem_cols);
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const int nc = a.g.nproj / 4;
+    if (nc == 64) output_body<64>(a, sm, tmem, &tm_q, &tm_out);
+    else if (nc == 32) output_body<32>(a, sm, tmem, &tm_q, &tm_out);
+    else output_body<16>(a, sm, tmem, &tm_q, &tm_out);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, a.tmem_cols);
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 constexpr uint32_t kSmemMax = 232448;   // 227 KB opt-in per block
@@ -1559,18 +1529,22 @@ StateLayout state_layout(const Geo &g) {
 }
 
 struct OutputLayout {
-    uint32_t o_w, o_xq, o_sop, o_phq, o_stage, o_small, bytes;
+    uint32_t o_w, o_s, o_x, o_stage, o_small, bytes;
+    int nq;
 };
 OutputLayout output_layout(const Geo &g) {
     OutputLayout l;
-    uint32_t o = 0;
-    l.o_w = o; o = align1k(o + (uint32_t)g.nproj * g.d * 2);
-    l.o_xq = o; o = align1k(o + (uint32_t)kC * g.d * 2);
-    l.o_sop = o; o = align1k(o + (uint32_t)g.r * 128);
-    l.o_phq = o; o = align1k(o + (uint32_t)kC * g.r * 2);
-    l.o_stage = o; o = align1k(o + 2 * kBlk);
-    l.o_small = o; o = align1k(o + 800 * 4);
-    l.bytes = o + 1024;
+    for (int nq = 2; nq >= 1; --nq) {
+        uint32_t o = 0;
+        l.o_w = o; o = align1k(o + (uint32_t)g.nproj * g.d * 2);
+        l.o_s = o; o = align1k(o + 2u * g.r * 128);             // state atom + z atom
+        l.o_x = o; o = align1k(o + (uint32_t)nq * kC * g.d * 2);
+        l.o_stage = o; o = align1k(o + 2 * kBlk);
+        l.o_small = o; o = align1k(o + 576 * 4);
+        l.bytes = o + 1024;
+        l.nq = nq;
+        if (l.bytes <= kSmemMax) break;
+    }
     return l;
 }
 
@@ -1638,8 +1612,7 @@ Plan make_plan(const Problem &p) {
         bytes += carve_bytes<float>((size_t)p.BH * pl.G * pl.per_state) +
                  carve_bytes<float>((size_t)p.BH * pl.G * 4);
     else
-        bytes += carve_bytes<uint8_t>((size_t)p.BH * pl.nvb * p.r * 128) +
-                 carve_bytes<float>((size_t)p.BH * p.r) + carve_bytes<float>(p.BH);
+        bytes += carve_bytes<uint8_t>((size_t)p.BH * (pl.nvb + 1) * p.r * 128);
     pl.bytes = bytes;
     return pl;
 }
@@ -1696,12 +1669,10 @@ int tc_run(const void *q, const void *k, const void *v, const float *omega, floa
     }
 
     if (!p.causal) {
-        uint8_t *sop = cv.take<uint8_t>((size_t)p.BH * nvb * p.r * 128);
-        float *z = cv.take<float>((size_t)p.BH * p.r);
-        float *sig = cv.take<float>(p.BH);
+        uint8_t *sop = cv.take<uint8_t>((size_t)p.BH * (nvb + 1) * p.r * 128);
         CombineArgs ca{};
         ca.g = g; ca.nseg = nstate; ca.causal = 0; ca.state = state; ca.meta = meta;
-        ca.sop = sop; ca.zout = z; ca.sig = sig;
+        ca.sop = sop;
         ca.slice = 2048;
         const int nsl = (int)((per_state + ca.slice - 1) / ca.slice);
         tc_combine<<<dim3(p.BH, 1, nsl), 256, 0, st>>>(ca);
@@ -1709,17 +1680,17 @@ int tc_run(const void *q, const void *k, const void *v, const float *omega, floa
         OutputLayout ol = output_layout(g);
         OutputArgs oa;
         oa.g = g; oa.H = p.H; oa.L = p.L;
-        const int want_ctas = 2 * sms;
-        int per = std::max(1, (int)((long long)nchunk * p.BH * nvb / want_ctas));
-        oa.chunks_per_cta = per;
-        oa.omg = img; oa.sop = sop; oa.z = z; oa.sig = sig; oa.status = dstat;
-        oa.o_w = ol.o_w; oa.o_xq = ol.o_xq; oa.o_sop = ol.o_sop; oa.o_phq = ol.o_phq;
+        oa.total_units = nchunk * p.BH * nvb;
+        oa.nq = ol.nq;
+        oa.omg = img; oa.sop = sop; oa.status = dstat;
+        oa.o_w = ol.o_w; oa.o_s = ol.o_s; oa.o_x = ol.o_x;
         oa.o_stage = ol.o_stage; oa.o_small = ol.o_small; oa.tmem_cols = 512;
         if (cudaFuncSetAttribute(tc_output, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ol.bytes) != cudaSuccess)
             return FAVOR_ERR_CUDA;
-        dim3 grid((nchunk + per - 1) / per, nvb, p.BH);
+        // one persistent CTA per SM, each on a contiguous run of (head, dv tile, chunk) units
+        const int grid = std::min(oa.total_units, sms);
         stats_begin(st, "tc_output");
-        tc_output<<<grid, kThreads, ol.bytes, st>>>(mq, mo, oa);
+        tc_output<<<grid, kOutThreads, ol.bytes, st>>>(mq, mo, oa);
         stats_end(st);
         FAVOR_LAUNCH_CHECK();
         return FAVOR_OK;

@@ -244,3 +244,26 @@ def test_tensor_core_path_taken(w, causal, kernel):
         fv.favor_stats_enable(False)
     assert st.dominant_kernel.decode() == kernel
     assert st.dominant_launches == 1 and st.kernel_launches >= 3
+
+
+# ---------------------------------------------------------------------------
+# many calls queued back to back on one stream, no host synchronisation in
+# between: every bounded wait must still be met (a wait that runs out sets
+# the device status) and the result must not change from call to call
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("w,causal", [(NC4096, False), (CAUSAL8K, True)], ids=["noncausal", "causal"])
+def test_back_to_back_calls(w, causal):
+    import torch
+    import favor_random_feature_gb300 as fv
+    inp = make_inputs(w)
+    q, k, v, om = to_device(inp)
+    stream = torch.cuda.current_stream()
+    outs = [torch.empty((w.B, w.H, w.L, w.dv), dtype=torch.float32, device="cuda") for _ in range(2)]
+    for i in range(24):
+        rc = fv.favor_attn_forward(q, k, v, om, outs[i % 2], w.B, w.H, w.L, w.d, w.dv, w.m,
+                                   int(causal), MAP_POSITIVE, stream)
+        assert rc == fv.FAVOR_OK, fv.strerror(rc)
+    torch.cuda.synchronize()
+    st = fv.favor_get_device_status(stream)
+    assert st == fv.FAVOR_OK, fv.strerror(st)
+    assert torch.equal(outs[0], outs[1])
