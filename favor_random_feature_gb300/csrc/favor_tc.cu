@@ -92,6 +92,19 @@ __device__ __forceinline__ uint32_t tm_addr(uint32_t base, int quarter, int col)
     return base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)col;
 }
 
+// 2^-floor(log2 x) for a positive normal x: the exponent field, negated
+__device__ __forceinline__ float pow2_inv_floor(float x) {
+    return __int_as_float(0x7F000000 - (__float_as_int(x) & 0x7F800000));
+}
+
+// the largest power of two s with s * b <= 2^14 (b > 0 normal): 2^(14 - ceil(log2 b))
+__device__ __forceinline__ float pow2_scale_14(float b) {
+    const int bits = __float_as_int(b);
+    const int e = ((bits >> 23) & 0xFF) - 127 + ((bits & 0x7FFFFF) ? 1 : 0);
+    const int se = min(max(14 - e, -126), 127);
+    return __int_as_float((se + 127) << 23);
+}
+
 __device__ __forceinline__ void set_status(int *status, int code) {
     if (status) atomicExch(status, code);
 }
@@ -144,42 +157,53 @@ __global__ void tc_prep_omega(const float *__restrict__ omega, uint8_t *__restri
 }
 
 // ---------------------------------------------------------------------------
-// tc_state: per (feature tile, segment, head) the segment state
-//   S[f][c] = sum_t phi(k_t)_f v_t[c],  z[f] = sum_t phi(k_t)_f
-// at the key reference R, written as fp32 [f][dv + 1] plus (R, max z, max|v|,
-// max|S|) of the tile.
-// Warp 0 lane 0 issues every TMA copy and MMA; warps 1..8 (256 threads,
-// named barrier 1) convert tiles and compute features.  Projections P[2]
-// alternate in TMEM; K, V and phi_K are double-buffered in shared memory, so
-// the projection of chunk c+1 and the state update of chunk c run while the
-// epilogue works on the features of the next chunk.
+// Epilogue group helpers (tc_state, tc_causal, tc_output): warps 1..16 of a
+// CTA, 512 threads synchronised on named barrier 1.
 // ---------------------------------------------------------------------------
-constexpr int kStEpi = 256;
-constexpr int kStateThreads = 32 + kStEpi;
+constexpr int kEpi = 512;
 
-struct StateArgs {
-    Geo g;
-    int H, L, seg_len, nseg, nvs;      // nvs: V buffers (1 or 2)
-    const uint8_t *omg;                // MN-major W images
-    float *state;                      // [BH][nseg][r][dv+1]
-    float *meta;                       // [BH][nseg][n_ft][4]: R, max z, max|v|, max|S|
-    int *status;
-    uint32_t o_w, o_xk, o_xv, o_phk, o_small, xv_stride, tmem_cols;
-};
+__device__ __forceinline__ float grp_max(float v, float *red, int ew) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    group_sync(kEpi);
+    if ((threadIdx.x & 31) == 0) red[ew] = v;
+    group_sync(kEpi);
+    float r = red[0];
+#pragma unroll
+    for (int i = 1; i < kEpi / 32; ++i) r = fmaxf(r, red[i]);
+    return r;
+}
 
-// in-place bf16 -> fp16 conversion of a [128][64 nblk] tile by 256 threads
-// (thread e: row e % 128, four 16-byte chunks of it per block)
+// Bounded mbarrier wait that also gives up at once when another thread of
+// the CTA has already timed out (*abort set), so that every thread keeps
+// running the same sequence of group barriers and the kernel still ends.
+__device__ __forceinline__ bool ewait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort) return false;
+        if (clock64() - t0 > kWaitLimit) {
+            *abort = 1;
+            return false;
+        }
+    }
+    return true;
+}
+
+// In-place bf16 -> fp16 conversion of a [128][64 nblk] tile by 512 threads:
+// thread e converts two 16-byte chunks of row e % 128 per block (chunk index
+// rotated with the row).  SQ / AMAX select the statistics it also returns:
+// the partial sum of squares (key norms) and max |x| (values).
 template <bool SQ, bool AMAX>
-__device__ __forceinline__ void convert_tile_256(uint8_t *tile, int nblk, int e, float &sumsq,
-                                                 float &amax) {
-    const int row = e & 127, half = e >> 7;
-    sumsq = 0.f;
+__device__ __forceinline__ float convert_tile_512(uint8_t *tile, int nblk, int e, float &amax) {
+    const int row = e & 127, part = e >> 7;
+    float sumsq = 0.f;
     amax = 0.f;
     for (int b = 0; b < nblk; ++b) {
         uint8_t *rp = tile + b * kBlk + row * 128;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const int p = (half * 4 + c + row) & 7;
+        for (int c = 0; c < 2; ++c) {
+            const int p = (part * 2 + c + row) & 7;
             uint4 *ptr = reinterpret_cast<uint4 *>(rp + p * 16);
             uint4 u = *ptr;
             uint32_t w[4] = {u.x, u.y, u.z, u.w}, o[4];
@@ -193,32 +217,32 @@ __device__ __forceinline__ void convert_tile_256(uint8_t *tile, int nblk, int e,
             *ptr = make_uint4(o[0], o[1], o[2], o[3]);
         }
     }
+    return sumsq;
 }
 
-__device__ __forceinline__ float st_grp_max(float v, float *red, int ew) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    group_sync(kStEpi);
-    if ((threadIdx.x & 31) == 0) red[ew] = v;
-    group_sync(kStEpi);
-    float r = red[0];
-#pragma unroll
-    for (int i = 1; i < kStEpi / 32; ++i) r = fmaxf(r, red[i]);
-    return r;
-}
+// ---------------------------------------------------------------------------
+// tc_state: per (feature tile, segment, head) the segment state
+//   S[f][c] = sum_t phi(k_t)_f v_t[c],  z[f] = sum_t phi(k_t)_f
+// at the key reference R, written as fp32 [f][dv + 1] plus (R, max z, max|v|,
+// max|S|) of the tile.
+// Warp 0 lane 0 issues every TMA copy and MMA; warps 1..16 (the epilogue
+// group) convert tiles and compute features, warp w on TMEM lane quarter
+// w % 4 and feature quarter (w - 1) / 4.  Projections P[2] alternate in TMEM;
+// K, V and phi_K are double-buffered in shared memory, so the projection of
+// chunk c+1 and the state update of chunk c run while the epilogue works on
+// the features of the next chunk.
+// ---------------------------------------------------------------------------
+constexpr int kStateThreads = 32 + kEpi;
 
-__device__ __forceinline__ bool st_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
-        if (*abort) return false;
-        if (clock64() - t0 > kWaitLimit) {
-            *abort = 1;
-            return false;
-        }
-    }
-    return true;
-}
+struct StateArgs {
+    Geo g;
+    int H, L, seg_len, nseg, nvs;      // nvs: V buffers (1 or 2)
+    const uint8_t *omg;                // MN-major W images
+    float *state;                      // [BH][nseg][r][dv+1]
+    float *meta;                       // [BH][nseg][n_ft][4]: R, max z, max|v|, max|S|
+    int *status;
+    uint32_t o_w, o_xk, o_xv, o_phk, o_small, xv_stride, tmem_cols;
+};
 
 __global__ void __launch_bounds__(kStateThreads, 1)
 tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -234,20 +258,20 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     uint8_t *w = sm + a.o_w, *xk = sm + a.o_xk, *xv = sm + a.o_xv, *phk = sm + a.o_phk;
     float *small = reinterpret_cast<float *>(sm + a.o_small);
     float *nk = small;              // [2][128]
-    float *part = small + 256;      // [2][128]
-    float *red = small + 512;       // [8]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(small + 528);
+    float *part = small + 256;      // [4][128]
+    float *red = small + 768;       // [32]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(small + 800);
     uint64_t *bar_w = &bars[0], *bar_k = &bars[1] /*[2]*/, *bar_v = &bars[3] /*[2]*/,
              *bar_pk = &bars[5] /*[2]*/, *bar_s = &bars[7] /*[2]*/, *e_x = &bars[9] /*[2]*/,
              *e_k = &bars[11] /*[2]*/;
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(small + 560);
-    volatile int *abortp = reinterpret_cast<volatile int *>(small + 562);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(small + 830);
+    volatile int *abortp = reinterpret_cast<volatile int *>(small + 832);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int col_s = 256;          // state tile: dv values, then 16 copies of z
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < 9; ++i) mbar_init(&bars[i], 1);
-        for (int i = 9; i < 13; ++i) mbar_init(&bars[i], kStEpi);
+        for (int i = 9; i < 13; ++i) mbar_init(&bars[i], kEpi);
         fence_mbar_init();
         *abortp = 0;
     }
@@ -300,24 +324,24 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             // e_x and e_k alternate between two barriers per chunk parity: the
             // epilogue may finish converting K(0) and K(1) before this thread
             // looks, and one barrier would then have moved two phases on
-            alive = st_wait(bar_w, 0, abortp) && st_wait(&e_x[0], 0, abortp);
+            alive = ewait(bar_w, 0, abortp) && ewait(&e_x[0], 0, abortp);
             if (alive) {
                 tc_fence_after();
                 issue_proj(0);
             }
             for (int c = 0; c < nchunk && alive; ++c) {
                 if (c + 1 < nchunk) {
-                    if (!(alive = st_wait(&e_x[(c + 1) & 1], ((c + 1) >> 1) & 1, abortp))) break;
+                    if (!(alive = ewait(&e_x[(c + 1) & 1], ((c + 1) >> 1) & 1, abortp))) break;
                     tc_fence_after();
                     issue_proj(c + 1);
                 }
                 if (c + 2 < nchunk) {
                     // K buffer c % 2 is free once P_K(c) is done: refill it early,
                     // a whole chunk of epilogue work ahead of its use
-                    if (!(alive = st_wait(&bar_pk[c & 1], (c >> 1) & 1, abortp))) break;
+                    if (!(alive = ewait(&bar_pk[c & 1], (c >> 1) & 1, abortp))) break;
                     load_k(c + 2);
                 }
-                if (!(alive = st_wait(&e_k[c & 1], (c >> 1) & 1, abortp))) break;
+                if (!(alive = ewait(&e_k[c & 1], (c >> 1) & 1, abortp))) break;
                 tc_fence_after();
                 {
                     const uint32_t idesc = idesc_f16(128, g.dv + 16, 1, 1);
@@ -330,7 +354,7 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                 }
                 const int nextv = c + NSV;
                 if (nextv < nchunk) {
-                    if (!(alive = st_wait(&bar_s[c & 1], (c >> 1) & 1, abortp))) break;
+                    if (!(alive = ewait(&bar_s[c & 1], (c >> 1) & 1, abortp))) break;
                     load_v(nextv);
                 }
             }
@@ -338,25 +362,26 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         }
     } else {
         const int e = threadIdx.x - 32, ew = e >> 5;
-        const int q = (ew + 1) & 3, h = ew >> 2;
+        const int q = (ew + 1) & 3, j = ew >> 2;
         const int row = q * 32 + lane;
         float R = g.map == FAVOR_MAP_POSITIVE ? -INFINITY : 0.f;
         float vmax = 0.f;
         // zero state and z
         {
-            float zero[32];
+            uint32_t zero[16];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) zero[i] = 0.f;
-            for (int cc = 32 * h; cc < g.dv + 16; cc += 64) tmem_st32(tm_addr(tmem, q, col_s + cc), zero);
+            for (int i = 0; i < 16; ++i) zero[i] = 0u;
+            for (int cc = 16 * j; cc < g.dv + 16; cc += 64) tmem_st16(tm_addr(tmem, q, col_s + cc), zero);
             tmem_st_wait();
         }
         auto convert_k = [&](int c) -> bool {
-            bool ok = st_wait(&bar_k[c & 1], (c >> 1) & 1, abortp);
-            float ss, am;
-            convert_tile_256<true, false>(xk + (size_t)(c & 1) * xkb, nd, e, ss, am);
+            bool ok = ewait(&bar_k[c & 1], (c >> 1) & 1, abortp);
+            float am;
+            const float ss = convert_tile_512<true, false>(xk + (size_t)(c & 1) * xkb, nd, e, am);
             part[(e >> 7) * 128 + (e & 127)] = ss;
-            group_sync(kStEpi);
-            if (e < 128) nk[(c & 1) * 128 + e] = 0.5f * kLog2e * (part[e] + part[128 + e]);
+            group_sync(kEpi);
+            if (e < 128)
+                nk[(c & 1) * 128 + e] = 0.5f * kLog2e * ((part[e] + part[128 + e]) + (part[256 + e] + part[384 + e]));
             fence_async_smem();
             mbar_arrive(&e_x[c & 1]);
             return ok;
@@ -368,95 +393,96 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             const bool ok = row < valid;
             if (c + 1 < nchunk) alive &= convert_k(c + 1);
             // P_K(c) ready; phi_K buffer c % 2 free once the state update of c - 2 is done
-            alive &= st_wait(&bar_pk[c & 1], (c >> 1) & 1, abortp);
-            if (c >= 2) alive &= st_wait(&bar_s[c & 1], ((c - 2) >> 1) & 1, abortp);
+            alive &= ewait(&bar_pk[c & 1], (c >> 1) & 1, abortp);
+            if (c >= 2) alive &= ewait(&bar_s[c & 1], ((c - 2) >> 1) & 1, abortp);
             tc_fence_after();
-            group_sync(kStEpi);   // norms of this chunk visible
+            group_sync(kEpi);   // norms of this chunk visible
             uint8_t *phb = phk + (size_t)(c & 1) * 2 * kBlk;
             const int pcol = 128 * (c & 1);
             if (g.map == FAVOR_MAP_POSITIVE) {
-                float pv[64];
-                {
-                    float t0[32], t1[32];
-                    tmem_ld32(tm_addr(tmem, q, pcol + 64 * h), t0);
-                    tmem_ld32(tm_addr(tmem, q, pcol + 64 * h + 32), t1);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) { pv[i] = t0[i]; pv[32 + i] = t1[i]; }
-                }
+                // feature columns 32 j .. 32 j + 31 of the tile
+                float pv[32];
+                tmem_ld32(tm_addr(tmem, q, pcol + 32 * j), pv);
+                tmem_ld_wait();
                 const float nkr = nk[(c & 1) * 128 + row];
-                float alpha = 1.f;
                 if (R == -INFINITY) {
                     float mx = -INFINITY;
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) mx = fmaxf(mx, pv[i]);
-                    R = st_grp_max(ok ? mx - nkr : -INFINITY, red, ew) - kShift;
+                    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, pv[i]);
+                    R = grp_max(ok ? mx - nkr : -INFINITY, red, ew) - kShift;
                 }
-                float off = nkr + R;
+                // rows past the end take an infinite offset: their features are 0
+                float off = ok ? nkr + R : INFINITY;
                 float mf = 0.f;
-#pragma unroll
-                for (int b = 0; b < 2; ++b) {
+                uint8_t *blk = phb + (size_t)(j >> 1) * kBlk;
+                const int c0 = 32 * (j & 1);
+                {
                     float v[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        v[i] = ok ? ex2(pv[32 * b + i] - off) : 0.f;
+                        v[i] = ex2(pv[i] - off);
                         mf = fmaxf(mf, v[i]);
                     }
-                    store_row32(phb + (size_t)h * kBlk, row, 32 * b, v);
+                    store_row32(blk, row, c0, v);
                 }
-                if (group_or(mf > kMaxFeature, kStEpi)) {
+                if (group_or(mf > kMaxFeature, kEpi)) {
                     // a key above the reference (rare): move it, rescale the
                     // running state, redo the features
-                    const float top = st_grp_max(ok ? log2f(mf) : -INFINITY, red, ew);
+                    const float top = grp_max(ok ? log2f(mf) : -INFINITY, red, ew);
                     const float Rn = R + (top - kShift);
-                    alpha = ex2(R - Rn);
+                    const float alpha = ex2(R - Rn);
                     R = Rn;
-                    off = nkr + R;
-                    if (c >= 1) alive &= st_wait(&bar_s[(c - 1) & 1], ((c - 1) >> 1) & 1, abortp);
+                    off = ok ? nkr + R : INFINITY;
+                    if (c >= 1) alive &= ewait(&bar_s[(c - 1) & 1], ((c - 1) >> 1) & 1, abortp);
                     tc_fence_after();
-                    for (int cc = 32 * h; cc < g.dv + 16; cc += 64) {
-                        float v[32];
-                        tmem_ld32(tm_addr(tmem, q, col_s + cc), v);
+                    for (int cc = 16 * j; cc < g.dv + 16; cc += 64) {
+                        float v[16];
+                        tmem_ld16(tm_addr(tmem, q, col_s + cc), v);
                         tmem_ld_wait();
+                        uint32_t u[16];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] *= alpha;
-                        tmem_st32(tm_addr(tmem, q, col_s + cc), v);
+                        for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(v[i] * alpha);
+                        tmem_st16(tm_addr(tmem, q, col_s + cc), u);
                     }
                     tmem_st_wait();
+                    float v[32];
 #pragma unroll
-                    for (int b = 0; b < 2; ++b) {
-                        float v[32];
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = ok ? ex2(pv[32 * b + i] - off) : 0.f;
-                        store_row32(phb + (size_t)h * kBlk, row, 32 * b, v);
-                    }
+                    for (int i = 0; i < 32; ++i) v[i] = ex2(pv[i] - off);
+                    store_row32(blk, row, c0, v);
                 }
             } else if (g.map == FAVOR_MAP_TRIG) {
-                float v[32], s[32], co[32];
-                tmem_ld32(tm_addr(tmem, q, pcol + 32 * h), v);
+                // 64 projections per tile: thread j takes 16 of them; the tile
+                // holds their sin in columns 0..63 and cos in 64..127
+                float v[16], s[16], co[16];
+                tmem_ld16(tm_addr(tmem, q, pcol + 16 * j), v);
                 tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
+                for (int i = 0; i < 16; ++i) {
                     if (ok) sincos_reduced(v[i], s[i], co[i]);
                     else s[i] = co[i] = 0.f;
                 }
-                store_row32(phb, row, 32 * h, s);
-                store_row32(phb + kBlk, row, 32 * h, co);
-            } else {
-                for (int b = 0; b < 2; ++b) {
-                    float v[32];
-                    tmem_ld32(tm_addr(tmem, q, pcol + 64 * h + 32 * b), v);
-                    tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = ok ? elu1(v[i]) : 0.f;
-                    store_row32(phb + (size_t)h * kBlk, row, 32 * b, v);
+                for (int c8 = 0; c8 < 2; ++c8) {
+                    uint4 us = make_uint4(pack_half2(s[8 * c8 + 0], s[8 * c8 + 1]), pack_half2(s[8 * c8 + 2], s[8 * c8 + 3]),
+                                          pack_half2(s[8 * c8 + 4], s[8 * c8 + 5]), pack_half2(s[8 * c8 + 6], s[8 * c8 + 7]));
+                    uint4 uc = make_uint4(pack_half2(co[8 * c8 + 0], co[8 * c8 + 1]), pack_half2(co[8 * c8 + 2], co[8 * c8 + 3]),
+                                          pack_half2(co[8 * c8 + 4], co[8 * c8 + 5]), pack_half2(co[8 * c8 + 6], co[8 * c8 + 7]));
+                    *reinterpret_cast<uint4 *>(phb + sw128_offset(row, 16 * j + 8 * c8)) = us;
+                    *reinterpret_cast<uint4 *>(phb + kBlk + sw128_offset(row, 16 * j + 8 * c8)) = uc;
                 }
+            } else {
+                float v[32];
+                tmem_ld32(tm_addr(tmem, q, pcol + 32 * j), v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = ok ? elu1(v[i]) : 0.f;
+                store_row32(phb + (size_t)(j >> 1) * kBlk, row, 32 * (j & 1), v);
             }
             // V(c) -> fp16
-            alive &= st_wait(&bar_v[c % NSV], NSV == 2 ? ((c >> 1) & 1) : (c & 1), abortp);
+            alive &= ewait(&bar_v[c % NSV], NSV == 2 ? ((c >> 1) & 1) : (c & 1), abortp);
             {
-                float ss, am;
-                convert_tile_256<false, true>(xv + (size_t)(c % NSV) * a.xv_stride, nvb, e, ss, am);
+                float am;
+                convert_tile_512<false, true>(xv + (size_t)(c % NSV) * a.xv_stride, nvb, e, am);
                 vmax = fmaxf(vmax, am);
             }
             fence_async_smem();
@@ -464,32 +490,32 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             mbar_arrive(&e_k[c & 1]);
         }
         // the last state update, then S, z -> global with the tile's max |S| and max z
-        if (nchunk > 0) alive &= st_wait(&bar_s[(nchunk - 1) & 1], ((nchunk - 1) >> 1) & 1, abortp);
+        if (nchunk > 0) alive &= ewait(&bar_s[(nchunk - 1) & 1], ((nchunk - 1) >> 1) & 1, abortp);
         tc_fence_after();
         const int f = ft * 128 + row;
         float *dst = a.state + (((size_t)bh * a.nseg + seg) * g.r + f) * (g.dv + 1);
         const bool write = alive && !*abortp;
         float smax = 0.f, zval = 0.f;
-        for (int cc = 32 * h; cc < g.dv; cc += 64) {
-            float v[32];
-            tmem_ld32(tm_addr(tmem, q, col_s + cc), v);
+        for (int cc = 16 * j; cc < g.dv; cc += 64) {
+            float v[16];
+            tmem_ld16(tm_addr(tmem, q, col_s + cc), v);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int i = 0; i < 16; ++i) {
                 smax = fmaxf(smax, fabsf(v[i]));
                 if (write) dst[cc + i] = v[i];
             }
         }
-        {
+        if (j == 0) {
             float v[16];
             tmem_ld16(tm_addr(tmem, q, col_s + g.dv), v);
             tmem_ld_wait();
             zval = fabsf(v[0]);
-            if (write && h == 0) dst[g.dv] = v[0];
+            if (write) dst[g.dv] = v[0];
         }
-        const float vm = st_grp_max(vmax, red, ew);
-        const float sm_all = st_grp_max(smax, red, ew);
-        const float zm = st_grp_max(zval, red, ew);
+        const float vm = grp_max(vmax, red, ew);
+        const float sm_all = grp_max(smax, red, ew);
+        const float zm = grp_max(zval, red, ew);
         if (write) {
             if (e == 0) {
                 float *m = a.meta + (((size_t)bh * a.nseg + seg) * g.n_ft + ft) * 4;
@@ -617,17 +643,22 @@ __global__ void tc_combine(const CombineArgs a) {
 //                      w serves TMEM lane quarter w % 4 and column quarter
 //                      (w - 1) / 4.
 // Per chunk the tensor core runs: P_K = K W^T and P_Q = Q W^T (N = all
-// projections); one N = 144 MMA with A = phi(Q) from TMEM against the rows
-// [phi(K); sigma z^T] -> [A | phi_Q z]; phi_Q (sigma S) (N = 64, the state
-// operand MN-major); A V with the row-scaled masked A from TMEM; and
-// S += phi(K)^T [V | 1] (N = 80) per 128 features.  The epilogue turns projections into features, the state into
-// its fp16 operand rows, A into its masked, row-scaled fp16 form, and the
-// accumulators into out.
+// projections); one N = 208 MMA with A = phi(Q) from TMEM against the rows
+// KB = [phi(K); sigma S^T; sigma z^T] -> [A | phi_Q sigma S | phi_Q sigma z];
+// S += phi(K)^T [V | 1] (N = 80) per 128 features; and [A_m V | A_m 1]
+// (N = 80), A_m the masked, row-scaled A from TMEM.  The epilogue turns
+// projections into features, the state into its fp16 rows of KB, A into A_m
+// and the accumulators into out, staged for a TMA store.  P_Q is
+// issued as soon as the epilogue holds P_K in registers, so the tensor core
+// computes it while the key features are formed; the state rows of the next
+// chunk are written while the tensor core computes its P_K.
 // ---------------------------------------------------------------------------
-constexpr int kEpi = 512;
 constexpr int kCausalThreads = 32 + kEpi;
-constexpr int kKbRows = 144;                     // phi_K keys 128 | z 1 | pad 15
+constexpr int kKbRows = 208;                     // phi_K 128 | sigma S^T 64 | sigma z 1 | pad 15
 constexpr uint32_t kKbBlk = kKbRows * 128;       // one 64-feature block of the KB operand
+constexpr int kKbS = 128, kKbZ = 192;            // first rows of sigma S^T and sigma z
+// small-area float offsets of the barriers, TMEM slot, abort flag; total size
+constexpr int kCausalBars = 1696, kCausalTslot = 1728, kCausalAbort = 1730, kCausalSmall = 1736;
 
 struct CausalArgs {
     Geo g;
@@ -635,106 +666,30 @@ struct CausalArgs {
     const uint8_t *omg;            // MN-major W images
     const float *s_in, *meta_in;   // [BH][nseg][r][dv+1], [BH][nseg][4] (segment 0 unused)
     int *status;
-    uint32_t o_w, o_x, o_v, o_kb, o_sop, o_small, tmem_cols;
+    uint32_t o_w, o_x, o_v, o_kb, o_small, tmem_cols;
 };
 
-// TMEM columns: P [0, 256) | phi_Q packed [0, r/2) | B [0, 64) | D_I [64, 128) |
-// A [128, 256) | phi_Q z [256, 272) | phi_Q S [272, 336) | state tiles
-constexpr int kColP = 0, kColB = 0, kColDI = 64, kColBig = 128, kColDD = 256, kColDX = 272,
-              kColS = 336, kSStride = 80;
-
-__device__ __forceinline__ float grp_max(float v, float *red, int ew) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    group_sync(kEpi);
-    if ((threadIdx.x & 31) == 0) red[ew] = v;
-    group_sync(kEpi);
-    float r = red[0];
-#pragma unroll
-    for (int i = 1; i < kEpi / 32; ++i) r = fmaxf(r, red[i]);
-    return r;
-}
-
-// Bounded mbarrier wait that also gives up at once when another thread of
-// the CTA has already timed out (*abort set), so that every thread keeps
-// running the same sequence of group barriers and the kernel still ends.
-__device__ __forceinline__ bool ewait(uint64_t *bar, uint32_t parity, volatile int *abort) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
-        if (*abort) return false;
-        if (clock64() - t0 > kWaitLimit) {
-            *abort = 1;
-            return false;
-        }
-    }
-    return true;
-}
-
-// (max of a, sum of b) over the epilogue group; red holds 32 floats
-__device__ __forceinline__ void grp_maxsum(float a, float b, float *red, int ew, float &mx, float &sm) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-        b += __shfl_xor_sync(0xffffffffu, b, o);
-    }
-    group_sync(kEpi);
-    if ((threadIdx.x & 31) == 0) {
-        red[ew] = a;
-        red[16 + ew] = b;
-    }
-    group_sync(kEpi);
-    mx = red[0];
-    sm = 0.f;
-#pragma unroll
-    for (int i = 0; i < kEpi / 32; ++i) {
-        mx = fmaxf(mx, red[i]);
-        sm += red[16 + i];
-    }
-}
-
-// In-place bf16 -> fp16 conversion of a [128][64 nblk] tile by 512 threads:
-// thread e converts two 16-byte chunks of row e % 128 per block (chunk index
-// rotated with the row).  SQ / AMAX select the statistics it also returns:
-// the partial sum of squares (key norms) and max |x| (values).
-template <bool SQ, bool AMAX>
-__device__ __forceinline__ float convert_tile_512(uint8_t *tile, int nblk, int e, float &amax) {
-    const int row = e & 127, part = e >> 7;
-    float sumsq = 0.f;
-    amax = 0.f;
-    for (int b = 0; b < nblk; ++b) {
-        uint8_t *rp = tile + b * kBlk + row * 128;
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            const int p = (part * 2 + c + row) & 7;
-            uint4 *ptr = reinterpret_cast<uint4 *>(rp + p * 16);
-            uint4 u = *ptr;
-            uint32_t w[4] = {u.x, u.y, u.z, u.w}, o[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
-                if (SQ) sumsq = fmaf(lo, lo, fmaf(hi, hi, sumsq));
-                if (AMAX) amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
-                o[i] = pack_half2(lo, hi);
-            }
-            *ptr = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-    }
-    return sumsq;
-}
-
-template <int N>
-__device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[N]) {
-    static_assert(N == 16 || N == 32, "");
-    if constexpr (N == 32) tmem_ld32(taddr, v);
-    else tmem_ld16(taddr, v);
-}
+// TMEM columns: P [0, 256) | phi_Q packed [0, r/2) | A_m packed [0, 64) |
+// [A_m V | A_m 1] [64, 144) | [A | phi_Q S | phi_Q z] [128, 336) | state
+// tiles [352, 512), 80 columns each (dv values, then z)
+constexpr int kColP = 0, kColB = 0, kColDI = 64, kColBig = 128, kColDX = 256, kColDD = 320,
+              kColS = 352, kSStride = 80;
 
 // 8 fp16 features (one 16-byte chunk) of a key row into the KB operand
 __device__ __forceinline__ void kb_store8(uint8_t *kb, int row, int f, const float *v) {
     uint4 u = make_uint4(pack_half2(v[0], v[1]), pack_half2(v[2], v[3]), pack_half2(v[4], v[5]),
                          pack_half2(v[6], v[7]));
     *reinterpret_cast<uint4 *>(kb + (size_t)(f >> 6) * kKbBlk + sw128_offset(row, f & 63)) = u;
+}
+
+// sigma x 16 state values of feature f (value columns c0 .. c0 + 15) into KB
+// rows kKbS + c0 .. (the K-major rows of sigma S^T), one fp16 each
+__device__ __forceinline__ void kb_state16(uint8_t *kb, int f, int c0, const float (&v)[16], float sc) {
+    uint8_t *base = kb + (size_t)(f >> 6) * kKbBlk + (size_t)(kKbS + c0) * 128 + ((f & 7) << 1);
+    const uint32_t c3 = (uint32_t)(f & 63) >> 3;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        *reinterpret_cast<__half *>(base + i * 128 + ((c3 ^ (uint32_t)(i & 7)) << 4)) = __float2half_rn(v[i] * sc);
 }
 
 // NC = projection columns per epilogue thread (a quarter of the projections)
@@ -748,28 +703,27 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
     const int nchunk = (t_end - t_begin + kC - 1) / kC;
     const int nd = g.d / 64, nft = g.n_ft;
     const uint32_t xb = (uint32_t)kC * g.d * 2;
-    uint8_t *w = sm + a.o_w, *xq = sm + a.o_x, *xk = xq + xb, *xv = sm + a.o_v, *kb = sm + a.o_kb,
-            *sop = sm + a.o_sop;
-    uint8_t *stage = sop;  // output staging aliases the state operand (dead after phi_Q S)
+    uint8_t *w = sm + a.o_w, *xq = sm + a.o_x, *xk = xq + xb, *xv = sm + a.o_v, *kb = sm + a.o_kb;
     float *small = reinterpret_cast<float *>(sm + a.o_small);
-    float *nk = small;             // [128]
-    float *part = small + 128;     // [4][128]
-    float *part2 = small + 640;    // [4][128]
-    float *red = small + 1152;     // [32]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(small + 1184);
+    float *nk = small;             // [128] half key norms (log2 units)
+    float *part = small + 128;     // [4][128] query row max
+    float *part2 = small + 640;    // [4][128] intra-chunk row max
+    float *part3 = small + 1152;   // [4][128] key sums of squares
+    float *red = small + 1664;     // [32]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(small + kCausalBars);
     uint64_t *bar_w = &bars[0], *bar_x = &bars[1], *bar_v = &bars[2], *bar_pk = &bars[3],
-             *bar_pq = &bars[4], *bar_a = &bars[5], *bar_av = &bars[6];   // bars[7] unused
-    uint64_t *e_x = &bars[8], *e_k = &bars[9], *e_sop = &bars[10], *e_q = &bars[11],
-             *e_v = &bars[12], *e_b = &bars[13], *e_out = &bars[14];
+             *bar_pq = &bars[4], *bar_a = &bars[5], *bar_av = &bars[6], *bar_st = &bars[13];
+    uint64_t *e_x = &bars[7], *e_pk = &bars[8], *e_q = &bars[9], *e_v = &bars[10],
+             *e_b = &bars[11], *e_out = &bars[12];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    volatile int *abortp = reinterpret_cast<volatile int *>(small + 1224);
+    volatile int *abortp = reinterpret_cast<volatile int *>(small + kCausalAbort);
     bool alive = true;
 
     if (warp == 0) {
         // ======================= control thread =======================
         if (lane == 0) {
             const uint32_t w_s = smem_u32(w), xq_s = smem_u32(xq), xk_s = smem_u32(xk),
-                           v_s = smem_u32(xv), kb_s = smem_u32(kb), sop_s = smem_u32(sop);
+                           v_s = smem_u32(xv), kb_s = smem_u32(kb);
             const uint32_t wbytes = (uint32_t)g.nproj * g.d * 2;
             auto load_x = [&](int c) {
                 mbar_arrive_expect_tx(bar_x, 2 * xb);
@@ -804,14 +758,15 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
                     issue_proj(xk_s);
                     mma_commit(bar_pk);
                 }
-                if (!(alive = ewait(e_k, ph, abortp))) break;
+                // P_Q as soon as the epilogue holds P_K in registers
+                if (!(alive = ewait(e_pk, ph, abortp))) break;
                 tc_fence_after();
                 issue_proj(xq_s);
                 mma_commit(bar_pq);
                 if (!(alive = ewait(bar_pq, ph, abortp))) break;
                 if (c + 1 < nchunk) load_x(c + 1);
-                // [A | phi_Q z] = phi_Q [phi_K ; z]^T and phi_Q (sigma S)
-                if (!(alive = ewait(e_sop, ph, abortp))) break;
+                // [A | phi_Q sigma S | phi_Q sigma z] = phi_Q KB^T once phi_Q,
+                // phi_K and the state rows are in place
                 if (!(alive = ewait(e_q, ph, abortp))) break;
                 tc_fence_after();
                 {
@@ -819,9 +774,6 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
                     for (int kk = 0; kk < g.r / 16; ++kk)
                         mma_f16_ts(tmem + kColBig, tmem + 8 * kk,
                                    smem_desc(kb_s + (kk >> 2) * kKbBlk + (kk & 3) * 32, 16, 1024), idesc, kk > 0);
-                    const uint32_t idx = idesc_f16(128, 64, 0, 1);
-                    for (int kk = 0; kk < g.r / 16; ++kk)
-                        mma_f16_ts(tmem + kColDX, tmem + 8 * kk, smem_desc(sop_s + kk * 2048, kBlk, 1024), idx, kk > 0);
                 }
                 mma_commit(bar_a);
                 // S += phi_K^T [V | 1] as soon as V is converted: it runs while
@@ -836,26 +788,35 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
                                     smem_desc(kb_s + (2 * t) * kKbBlk + kk * 2048, kKbBlk, 1024),
                                     smem_desc(v_s + kk * 2048, kBlk, 1024), ids, 1);
                 }
-                // A V
+                // [A_m V | A_m 1]
                 if (!(alive = ewait(e_b, ph, abortp))) break;
                 tc_fence_after();
                 {
-                    const uint32_t idv = idesc_f16(128, 64, 0, 1);
+                    const uint32_t idv = idesc_f16(128, 80, 0, 1);
                     for (int kk = 0; kk < kC / 16; ++kk)
                         mma_f16_ts(tmem + kColDI, tmem + kColB + 8 * kk, smem_desc(v_s + kk * 2048, kBlk, 1024), idv, kk > 0);
                     mma_commit(bar_av);   // covers the state update issued before it
                 }
+                // the epilogue has staged out (fp32, two [128][32] halves in KB
+                // rows 0..127 of blocks 0 and 1): store it, and once the store
+                // has read the staging, the next chunk's key projection
+                if (!(alive = ewait(e_out, ph, abortp))) break;
+                tma_store_3d(tm_out, kb, 64 * dvt, t_begin + c * kC, bh);
+                tma_store_3d(tm_out, kb + kKbBlk, 64 * dvt + 32, t_begin + c * kC, bh);
+                bulk_commit();
                 if (c + 1 < nchunk) {
-                    // next chunk's key projection once D_I has been read
                     if (!(alive = ewait(e_x, (c + 1) & 1, abortp))) break;
-                    if (!(alive = ewait(e_out, ph, abortp))) break;
                     tc_fence_after();
                     issue_proj(xk_s);
                     mma_commit(bar_pk);
                     if (!(alive = ewait(bar_av, ph, abortp))) break;
                     load_v(c + 1);
+                    // the staging rows are phi_K rows again once the store has read them
+                    bulk_wait_read0();
+                    mbar_arrive(bar_st);
                 }
             }
+            bulk_wait0();
             if (!alive) set_status(a.status, FAVOR_ERR_TIMEOUT);
         }
         return;
@@ -880,32 +841,55 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(src ? src[64 * dvt + 16 * j + i] : 0.f);
         tmem_st16(tm_addr(tmem, q, kColS + t * kSStride + 16 * j), v);
-        if (j == 0) {
-            const float zval = src ? src[g.dv] : 0.f;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(zval);
-            tmem_st16(tm_addr(tmem, q, kColS + t * kSStride + 64), v);
-        }
+        if (j == 0) tmem_st1(tm_addr(tmem, q, kColS + t * kSStride + 64), src ? src[g.dv] : 0.f);
     }
     tmem_st_wait();
-    // pad rows 129..143 of every KB block start at zero (later chunks' output
-    // staging may overwrite them; they only feed accumulator columns never read)
+    // pad rows of every KB block: they feed accumulator columns never read
     for (int i = e; i < (g.r / 64) * 15 * 8; i += kEpi) {
-        const int blk = i / 120, rr = 129 + (i % 120) / 8, ch = i % 8;
+        const int blk = i / 120, rr = kKbZ + 1 + (i % 120) / 8, ch = i % 8;
         *reinterpret_cast<uint4 *>(kb + (size_t)blk * kKbBlk + rr * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
     }
+    // sigma S^T and sigma z -> KB rows kKbS.. and kKbZ, sigma a power of two
+    // with sigma * (bound on max |S| and max z) <= kSigmaTarget.  alpha != 1
+    // first rescales the state in TMEM (the key reference has moved).
+    float sigma = 1.f;
+    auto state_rows = [&](float alpha) {
+        const float bound = zmax * fmaxf(vmax, 1.f);
+        sigma = bound > 0.f ? pow2_scale_14(bound) : 1.f;
+        for (int t = 0; t < nft; ++t) {
+            const uint32_t col = kColS + t * kSStride;
+            float s0[16], z0 = 0.f;
+            tmem_ld16(tm_addr(tmem, q, col + 16 * j), s0);
+            if (j == 0) tmem_ld1(tm_addr(tmem, q, col + 64), z0);
+            tmem_ld_wait();
+            if (alpha != 1.f) {
+                uint32_t u[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(s0[i] *= alpha);
+                tmem_st16(tm_addr(tmem, q, col + 16 * j), u);
+                if (j == 0) tmem_st1(tm_addr(tmem, q, col + 64), z0 *= alpha);
+                tmem_st_wait();
+            }
+            const int f = t * 128 + row;
+            kb_state16(kb, f, 16 * j, s0, sigma);
+            if (j == 0)
+                *reinterpret_cast<__half *>(kb + (size_t)(f >> 6) * kKbBlk + sw128_offset(kKbZ, f & 63)) =
+                    __float2half_rn(z0 * sigma);
+        }
+    };
     auto convert_x = [&](int c) -> bool {
         const bool ok_x = ewait(bar_x, c & 1, abortp);
         float am;
         convert_tile_512<false, false>(xq, nd, e, am);
         const float ss = convert_tile_512<true, false>(xk, nd, e, am);
-        part[(e >> 7) * 128 + (e & 127)] = ss;
+        part3[(e >> 7) * 128 + (e & 127)] = ss;
         group_sync(kEpi);
-        if (e < 128) nk[e] = 0.5f * kLog2e * (part[e] + part[128 + e] + part[256 + e] + part[384 + e]);
+        if (e < 128) nk[e] = 0.5f * kLog2e * ((part3[e] + part3[128 + e]) + (part3[256 + e] + part3[384 + e]));
         fence_async_smem();
         mbar_arrive(e_x);
         return ok_x;
     };
+    state_rows(1.f);
     if (nchunk > 0) alive = convert_x(0);
     for (int c = 0; c < nchunk; ++c) {
         const uint32_t ph = c & 1;
@@ -925,42 +909,46 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
         }
         tmem_ld_wait();
         tc_fence_before();
+        mbar_arrive(e_pk);   // P_K is in registers: P_Q may overwrite it
+        // KB rows 0..127 held the previous chunk's output staging
+        if (c > 0) alive &= ewait(bar_st, (c - 1) & 1, abortp);
         const float nkr = nk[row];
-        float alpha = 1.f, mf = 0.f;
+        float mf = 0.f, moved = 1.f;   // moved: state rescale when the key reference moves
         if (g.map == FAVOR_MAP_POSITIVE) {
             if (R == -INFINITY) {
                 float mx = -INFINITY;
 #pragma unroll
                 for (int i = 0; i < NC; ++i) mx = fmaxf(mx, pv[i]);
                 R = grp_max(ok ? mx - nkr : -INFINITY, red, ew) - kShift;
-                alpha = 0.f;
             }
-            float off = nkr + R;
+            // rows past the end take an infinite offset: their features are 0
+            float off = ok ? nkr + R : INFINITY;
 #pragma unroll
             for (int b = 0; b < NC / 8; ++b) {
                 float v[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    v[i] = ok ? ex2(pv[8 * b + i] - off) : 0.f;
+                    v[i] = ex2(pv[8 * b + i] - off);
                     mf = fmaxf(mf, v[i]);
                 }
                 kb_store8(kb, row, NC * j + 8 * b, v);
             }
             // a feature beyond e^(shift + slack) means a key above the reference
-            // (rare): move the reference to that key and redo the features
+            // (rare): move the reference to that key, rescale the state and
+            // redo the features
             if (group_or(mf > kMaxFeature, kEpi)) {
                 const float top = grp_max(ok ? log2f(mf) : -INFINITY, red, ew);
                 const float Rn = R + (top - kShift);
-                alpha *= ex2(R - Rn);
+                moved = ex2(R - Rn);
                 R = Rn;
-                off = nkr + R;
+                off = ok ? nkr + R : INFINITY;
                 mf = 0.f;
 #pragma unroll
                 for (int b = 0; b < NC / 8; ++b) {
                     float v[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        v[i] = ok ? ex2(pv[8 * b + i] - off) : 0.f;
+                        v[i] = ex2(pv[8 * b + i] - off);
                         mf = fmaxf(mf, v[i]);
                     }
                     kb_store8(kb, row, NC * j + 8 * b, v);
@@ -994,51 +982,11 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
                 kb_store8(kb, row, NC * j + 8 * b, v);
             }
         }
-        fence_async_smem();
-        mbar_arrive(e_k);
-        // ---------------- state -> fp16 operand (MN-major), z -> KB row 128 ----------------
-        if (e == 0) bulk_wait_read0();   // the previous chunk's output staging has been read
-        group_sync(kEpi);
-        const float zb = zmax * alpha;
-        const float bound = zb * fmaxf(vmax, 1.f);
-        const float sigma = bound > 0.f ? exp2f(floorf(log2f(kSigmaTarget / bound))) : 1.f;
-        for (int t = 0; t < nft; ++t) {
-            const int f = t * 128 + row;
-            float v[16];
-            tmem_ld16(tm_addr(tmem, q, kColS + t * kSStride + 16 * j), v);
-            tmem_ld_wait();
-            if (alpha != 1.f) {
-                uint32_t u[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(v[i] * alpha);
-                tmem_st16(tm_addr(tmem, q, kColS + t * kSStride + 16 * j), u);
-            }
-            const float sc = alpha * sigma;
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh)
-                *reinterpret_cast<uint4 *>(sop + sw128_offset(f, 16 * j + 8 * hh)) =
-                    make_uint4(pack_half2(v[8 * hh + 0] * sc, v[8 * hh + 1] * sc), pack_half2(v[8 * hh + 2] * sc, v[8 * hh + 3] * sc),
-                               pack_half2(v[8 * hh + 4] * sc, v[8 * hh + 5] * sc), pack_half2(v[8 * hh + 6] * sc, v[8 * hh + 7] * sc));
-            if (j == 0) {
-                float zv[16];
-                tmem_ld16(tm_addr(tmem, q, kColS + t * kSStride + 64), zv);
-                tmem_ld_wait();
-                const float zval = zv[0] * alpha;
-                if (alpha != 1.f) {
-                    uint32_t u[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(zval);
-                    tmem_st16(tm_addr(tmem, q, kColS + t * kSStride + 64), u);
-                }
-                *reinterpret_cast<__half *>(kb + (size_t)(f >> 6) * kKbBlk + sw128_offset(128, f & 63)) =
-                    __float2half_rn(zval * sigma);
-            }
+        if (moved != 1.f) {
+            // the state so far and its rows in KB move to the new reference
+            zmax *= moved;
+            state_rows(moved);
         }
-        tmem_st_wait();
-        zmax = zb;
-        fence_async_smem();
-        tc_fence_before();
-        mbar_arrive(e_sop);
         // ---------------- query features -> phi_Q in TMEM [0, r/2) ----------------
         alive &= ewait(bar_pq, ph, abortp);
         tc_fence_after();
@@ -1060,6 +1008,7 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
         tc_fence_before();
         group_sync(kEpi);   // every projection column read: phi_Q may now overwrite them
         tc_fence_after();
+
         if (g.map == FAVOR_MAP_POSITIVE) {
             qoff = fmaxf(fmaxf(part[row], part[128 + row]), fmaxf(part[256 + row], part[384 + row])) - kShift;
 #pragma unroll
@@ -1099,6 +1048,7 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
             }
         }
         tmem_st_wait();
+        fence_async_smem();   // KB rows (features, state) for the tensor core
         tc_fence_before();
         mbar_arrive(e_q);
         // ---------------- V -> fp16, running max |v| ----------------
@@ -1106,23 +1056,28 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
         {
             float am;
             convert_tile_512<false, true>(xv, 1, e, am);
-            // one reduction: max |v| of this chunk and the key mass of its phi_K
-            // (sum over keys of the largest feature), the bound on the next z
-            float vm, ms;
-            grp_maxsum(am, mf, red, ew, vm, ms);
-            vmax = fmaxf(vmax, vm);
-            zmax += ms;
+            fence_async_smem();
+            mbar_arrive(e_v);
+            // warp partials of max |v| and of the key mass (sum over keys of the
+            // largest feature, the bound on the growth of z); the group combines
+            // them after the barrier of the next Q, K conversion
+            float ms = mf;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+                ms += __shfl_xor_sync(0xffffffffu, ms, o);
+            }
+            if (lane == 0) {
+                red[ew] = am;
+                red[16 + ew] = ms;
+            }
         }
-        fence_async_smem();
-        mbar_arrive(e_v);
-        // ---------------- next chunk's Q, K ----------------
-        if (c + 1 < nchunk) alive &= convert_x(c + 1);
         // ---------------- intra-chunk matrix -> masked, row-scaled, TMEM ----------------
         alive &= ewait(bar_a, ph, abortp);
         tc_fence_after();
         float av[32];
         const int limit = min(row, valid - 1) - 32 * j;   // keys j' <= limit (local index)
-        float rs = 0.f, rm = 0.f;
+        float rm = 0.f;
         if (limit < 0) {                 // this quarter lies entirely above the diagonal
 #pragma unroll
             for (int i = 0; i < 32; ++i) av[i] = 0.f;
@@ -1134,17 +1089,12 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
                 for (int i = 0; i < 32; ++i) av[i] = i <= limit ? av[i] : 0.f;
             }
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                rs += av[i];
-                rm = fmaxf(rm, fabsf(av[i]));
-            }
+            for (int i = 0; i < 32; ++i) rm = fmaxf(rm, fabsf(av[i]));
         }
-        part[j * 128 + row] = rs;
         part2[j * 128 + row] = rm;
         group_sync(kEpi);
-        const float den_intra = (part[row] + part[128 + row]) + (part[256 + row] + part[384 + row]);
         const float rmax = fmaxf(fmaxf(part2[row], part2[128 + row]), fmaxf(part2[256 + row], part2[384 + row]));
-        const float rho = rmax > 0.f ? exp2f(-floorf(log2f(rmax))) : 1.f;
+        const float rho = rmax > 0.f ? pow2_inv_floor(rmax) : 1.f;
         {
             uint32_t o[16];
 #pragma unroll
@@ -1154,43 +1104,51 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(e_b);
+        // ---------------- next chunk's Q, K (while the tensor core runs A_m V) ----------------
+        if (c + 1 < nchunk) {
+            alive &= convert_x(c + 1);   // its group barrier publishes red
+            float vm = red[0], ms = 0.f;
+#pragma unroll
+            for (int i = 0; i < kEpi / 32; ++i) {
+                vm = fmaxf(vm, red[i]);
+                ms += red[16 + i];
+            }
+            vmax = fmaxf(vmax, vm);
+            zmax += ms;
+        }
         // ---------------- output ----------------
         alive &= ewait(bar_av, ph, abortp);
         tc_fence_after();
         {
-            float di[16], dx[16], dd[16];
+            float di[16], dx[16], ddi, ddx;
             tmem_ld16(tm_addr(tmem, q, kColDI + 16 * j), di);
             tmem_ld16(tm_addr(tmem, q, kColDX + 16 * j), dx);
-            tmem_ld16(tm_addr(tmem, q, kColDD), dd);
+            tmem_ld1(tm_addr(tmem, q, kColDI + 64), ddi);
+            tmem_ld1(tm_addr(tmem, q, kColDD), ddx);
             tmem_ld_wait();
             tc_fence_before();
-            mbar_arrive(e_out);
-            const float inv_sigma = 1.f / sigma;
-            const float id = 1.f / (den_intra + dd[0] * inv_sigma);
-            const float ir = 1.f / rho;
-            // output columns 16 j .. 16 j + 15 -> staging half (16 j) / 32, chunks of 4
-            uint8_t *half = stage + (size_t)((16 * j) >> 5) * kBlk;
+            const float is = pow2_inv_floor(sigma), ir = pow2_inv_floor(rho);   // exact: powers of two
+            const float id = __fdividef(1.f, fmaf(ddi, ir, ddx * is));
+            // output columns 16 j .. 16 j + 15 -> staging half (16 j) / 32 (the
+            // phi_K rows of KB block 0 or 1, free since the state update), 128B
+            // swizzle in chunks of 4 floats
+            uint8_t *half = kb + (size_t)((16 * j) >> 5) * kKbBlk;
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 const int col = (16 * j + 4 * cc) & 31;
                 const int p = (col >> 2) ^ (row & 7);
-                float4 o4;
-                o4.x = fmaf(di[4 * cc + 0], ir, dx[4 * cc + 0] * inv_sigma) * id;
-                o4.y = fmaf(di[4 * cc + 1], ir, dx[4 * cc + 1] * inv_sigma) * id;
-                o4.z = fmaf(di[4 * cc + 2], ir, dx[4 * cc + 2] * inv_sigma) * id;
-                o4.w = fmaf(di[4 * cc + 3], ir, dx[4 * cc + 3] * inv_sigma) * id;
-                *reinterpret_cast<float4 *>(half + row * 128 + p * 16) = o4;
+                *reinterpret_cast<float4 *>(half + row * 128 + p * 16) =
+                    make_float4(fmaf(di[4 * cc + 0], ir, dx[4 * cc + 0] * is) * id,
+                                fmaf(di[4 * cc + 1], ir, dx[4 * cc + 1] * is) * id,
+                                fmaf(di[4 * cc + 2], ir, dx[4 * cc + 2] * is) * id,
+                                fmaf(di[4 * cc + 3], ir, dx[4 * cc + 3] * is) * id);
             }
+            fence_async_smem();
+            mbar_arrive(e_out);
         }
-        fence_async_smem();
-        group_sync(kEpi);
-        if (e == 0 && !*abortp) {
-            tma_store_3d(tm_out, stage, 64 * dvt, tc0, bh);
-            tma_store_3d(tm_out, stage + kBlk, 64 * dvt + 32, tc0, bh);
-            bulk_commit();
-        }
+        // ---------------- state rows of the next chunk (during its P_K) ----------------
+        if (c + 1 < nchunk) state_rows(1.f);
     }
-    if (e == 0) bulk_wait0();
     if (!alive) set_status(a.status, FAVOR_ERR_TIMEOUT);
 }
 
@@ -1201,17 +1159,19 @@ tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *small = reinterpret_cast<float *>(sm + a.o_small);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(small + 1184);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(small + 1220);
-    volatile int *abortp = reinterpret_cast<volatile int *>(small + 1224);
-    if (threadIdx.x == 0) *abortp = 0;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(small + kCausalBars);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(small + kCausalTslot);
+    volatile int *abortp = reinterpret_cast<volatile int *>(small + kCausalAbort);
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 8; ++i) mbar_init(&bars[i], 1);
-        for (int i = 8; i < 15; ++i) mbar_init(&bars[i], kEpi);
+        *abortp = 0;
+        for (int i = 0; i < 7; ++i) mbar_init(&bars[i], 1);
+        for (int i = 7; i < 13; ++i) mbar_init(&bars[i], kEpi);
+        mbar_init(&bars[13], 1);
         fence_mbar_init();
     }
-    // ones atom after the V tile: the z column of S += phi_K^T [V | 1]
+    // ones atom after the V tile: the z column of S += phi_K^T [V | 1] and
+    // the row sums of [A_m V | A_m 1]
     uint8_t *ones = sm + a.o_v + kBlk;
     for (int i = threadIdx.x; i < (int)(kBlk / 16); i += kCausalThreads)
         reinterpret_cast<uint4 *>(ones)[i] = make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
@@ -1263,7 +1223,6 @@ __device__ void output_body(const OutputArgs &a, uint8_t *sm, uint32_t tmem,
     uint8_t *w = sm + a.o_w, *sbuf = sm + a.o_s, *xs = sm + a.o_x, *stage = sm + a.o_stage;
     float *small = reinterpret_cast<float *>(sm + a.o_small);
     float *part = small;            // [4][128]
-    float *red = small + 512;       // [32]
     uint64_t *bars = reinterpret_cast<uint64_t *>(small + 544);
     uint64_t *bar_w = &bars[0], *bar_x = &bars[1] /*[2]*/, *bar_pq = &bars[3], *bar_d = &bars[4],
              *e_x = &bars[5], *e_q = &bars[6];
@@ -1492,7 +1451,7 @@ Geo make_geo(const Problem &p) {
 }
 
 struct CausalLayout {
-    uint32_t o_w, o_x, o_v, o_kb, o_sop, o_small, bytes;
+    uint32_t o_w, o_x, o_v, o_kb, o_small, bytes;
 };
 CausalLayout causal_layout(const Geo &g) {
     CausalLayout l;
@@ -1501,8 +1460,7 @@ CausalLayout causal_layout(const Geo &g) {
     l.o_x = o; o = align1k(o + 2u * kC * g.d * 2);
     l.o_v = o; o = align1k(o + 2 * kBlk);                   // V tile + ones atom
     l.o_kb = o; o = align1k(o + (uint32_t)(g.r / 64) * kKbBlk);
-    l.o_sop = o; o = align1k(o + std::max<uint32_t>((uint32_t)g.r * 128, 2 * kBlk));
-    l.o_small = o; o = align1k(o + 1232 * 4);
+    l.o_small = o; o = align1k(o + kCausalSmall * 4);
     l.bytes = o + 1024;
     return l;
 }
@@ -1520,7 +1478,7 @@ StateLayout state_layout(const Geo &g) {
         l.xv_stride = (uint32_t)(g.dv / 64 + 1) * kBlk;       // V blocks + ones atom
         l.o_xv = o; o = align1k(o + (uint32_t)nvs * l.xv_stride);
         l.o_phk = o; o = align1k(o + 4 * kBlk);
-        l.o_small = o; o = align1k(o + 576 * 4);
+        l.o_small = o; o = align1k(o + 840 * 4);
         l.bytes = o + 1024;
         l.nvs = nvs;
         if (l.bytes <= 232448) break;
@@ -1712,7 +1670,7 @@ int tc_run(const void *q, const void *k, const void *v, const float *omega, floa
     a.g = g;
     a.H = p.H; a.L = p.L; a.seg_len = seg_len; a.nseg = G;
     a.omg = img; a.s_in = s_in; a.meta_in = meta_in; a.status = dstat;
-    a.o_w = cl.o_w; a.o_x = cl.o_x; a.o_v = cl.o_v; a.o_kb = cl.o_kb; a.o_sop = cl.o_sop; a.o_small = cl.o_small;
+    a.o_w = cl.o_w; a.o_x = cl.o_x; a.o_v = cl.o_v; a.o_kb = cl.o_kb; a.o_small = cl.o_small;
     a.tmem_cols = 512;
     if (cudaFuncSetAttribute(tc_causal, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cl.bytes) != cudaSuccess)
         return FAVOR_ERR_CUDA;

@@ -129,6 +129,22 @@ def test_head_dims(d, dv, m, causal):
     check_bf16(e, f"d={d} dv={dv} m={m}")
 
 
+# many heads: one segment per head (or two), so each CTA scans several chunks
+# and carries its state from chunk to chunk (the launch shape of the full-size
+# workloads, at a length the oracle finishes quickly)
+@pytest.mark.parametrize("B,H,dv,heads", [(1, 160, 64, [0, 77, 159]), (4, 19, 64, [0, 40, 75]),
+                                          (2, 80, 128, [1, 100, 159])],
+                         ids=["one_segment", "two_segments", "dv128"])
+def test_causal_many_chunks_per_cta(B, H, dv, heads):
+    w = CAUSAL8K.with_(dv=dv)
+    inp = make_inputs(w, L=1000, B=B, H=H)
+    out = run_gpu(inp, True, MAP_POSITIVE)
+    ref = oracle_ref(inp, True, MAP_POSITIVE, heads=heads)
+    BH = B * H
+    e = row_errors(out.reshape(BH, 1000, dv)[heads], ref.reshape(BH, 1000, dv)[heads])
+    check_bf16(e, f"B={B} H={H} dv={dv}")
+
+
 def test_causal_first_row_is_v0_and_last_row_matches_noncausal():
     inp = make_inputs(CAUSAL8K, L=300, B=1, H=2)
     oc = run_gpu(inp, True, MAP_POSITIVE)
