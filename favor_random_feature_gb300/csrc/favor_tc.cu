@@ -236,7 +236,7 @@ constexpr int kStateThreads = 32 + kEpi;
 
 struct StateArgs {
     Geo g;
-    int H, L, seg_len, nseg, nvs;      // nvs: V buffers (1 or 2)
+    int H, L, seg_len, nseg, nvs, nks; // V buffers (1 or 2), K buffers (2 or 3)
     const uint8_t *omg;                // MN-major W images
     float *state;                      // [BH][nseg][r][dv+1]
     float *meta;                       // [BH][nseg][n_ft][4]: R, max z, max|v|, max|S|
@@ -253,7 +253,7 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     const int ft = blockIdx.x, seg = blockIdx.y, bh = blockIdx.z, head = bh % a.H;
     const int t_begin = seg * a.seg_len, t_end = min(a.L, t_begin + a.seg_len);
     const int nchunk = (t_end - t_begin + kC - 1) / kC;
-    const int nd = g.d / 64, nvb = g.dv / 64, NSV = a.nvs;
+    const int nd = g.d / 64, nvb = g.dv / 64, NSV = a.nvs, NSK = a.nks;
     const uint32_t xkb = (uint32_t)kC * g.d * 2;
     uint8_t *w = sm + a.o_w, *xk = sm + a.o_xk, *xv = sm + a.o_xv, *phk = sm + a.o_phk;
     float *small = reinterpret_cast<float *>(sm + a.o_small);
@@ -261,17 +261,18 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     float *part = small + 256;      // [4][128]
     float *red = small + 768;       // [32]
     uint64_t *bars = reinterpret_cast<uint64_t *>(small + 800);
-    uint64_t *bar_w = &bars[0], *bar_k = &bars[1] /*[2]*/, *bar_v = &bars[3] /*[2]*/,
+    uint64_t *bar_w = &bars[0], *bar_k = &bars[13] /*[3]*/, *bar_v = &bars[3] /*[2]*/,
              *bar_pk = &bars[5] /*[2]*/, *bar_s = &bars[7] /*[2]*/, *e_x = &bars[9] /*[2]*/,
              *e_k = &bars[11] /*[2]*/;
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(small + 830);
-    volatile int *abortp = reinterpret_cast<volatile int *>(small + 832);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(small + 834);
+    volatile int *abortp = reinterpret_cast<volatile int *>(small + 836);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int col_s = 256;          // state tile: dv values, then 16 copies of z
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < 9; ++i) mbar_init(&bars[i], 1);
         for (int i = 9; i < 13; ++i) mbar_init(&bars[i], kEpi);
+        for (int i = 13; i < 16; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
         *abortp = 0;
     }
@@ -293,11 +294,12 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         if (lane == 0 && nchunk > 0) {
             const uint32_t w_s = smem_u32(w), xk_s = smem_u32(xk), xv_s = smem_u32(xv), phk_s = smem_u32(phk);
             const uint32_t wbytes = (uint32_t)g.np_tile * g.d * 2;
+            // K in NSK buffers: K(c + NSK) loads as soon as P_K(c) is done
             auto load_k = [&](int c) {
-                uint64_t *bar = &bar_k[c & 1];
+                uint64_t *bar = &bar_k[c % NSK];
                 mbar_arrive_expect_tx(bar, xkb);
                 for (int b = 0; b < nd; ++b)
-                    tma_load_3d(xk + (size_t)(c & 1) * xkb + b * kBlk, &tm_k, bar, 64 * b, t_begin + c * kC, bh);
+                    tma_load_3d(xk + (size_t)(c % NSK) * xkb + b * kBlk, &tm_k, bar, 64 * b, t_begin + c * kC, bh);
             };
             auto load_v = [&](int c) {
                 const int s = c % NSV;
@@ -307,7 +309,7 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             };
             auto issue_proj = [&](int c) {
                 const uint32_t idesc = idesc_f16(128, g.np_tile, 0, 1);
-                const uint32_t x_s = xk_s + (uint32_t)(c & 1) * xkb;
+                const uint32_t x_s = xk_s + (uint32_t)(c % NSK) * xkb;
                 for (int kk = 0; kk < g.d / 16; ++kk)
                     mma_f16(tmem + 128 * (c & 1), smem_desc(x_s + (kk >> 2) * kBlk + (kk & 3) * 32, 16, 1024),
                             smem_desc(w_s + kk * 2048, (uint32_t)g.d * 128, 1024), idesc, kk > 0);
@@ -321,6 +323,7 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                 load_k(1);
                 if (NSV == 2) load_v(1);
             }
+            if (nchunk > 2 && NSK == 3) load_k(2);
             // e_x and e_k alternate between two barriers per chunk parity: the
             // epilogue may finish converting K(0) and K(1) before this thread
             // looks, and one barrier would then have moved two phases on
@@ -335,11 +338,11 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                     tc_fence_after();
                     issue_proj(c + 1);
                 }
-                if (c + 2 < nchunk) {
-                    // K buffer c % 2 is free once P_K(c) is done: refill it early,
-                    // a whole chunk of epilogue work ahead of its use
+                if (c + NSK < nchunk) {
+                    // K buffer c % NSK is free once P_K(c) is done: refill it
+                    // ahead of its use
                     if (!(alive = ewait(&bar_pk[c & 1], (c >> 1) & 1, abortp))) break;
-                    load_k(c + 2);
+                    load_k(c + NSK);
                 }
                 if (!(alive = ewait(&e_k[c & 1], (c >> 1) & 1, abortp))) break;
                 tc_fence_after();
@@ -375,9 +378,9 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             tmem_st_wait();
         }
         auto convert_k = [&](int c) -> bool {
-            bool ok = ewait(&bar_k[c & 1], (c >> 1) & 1, abortp);
+            bool ok = ewait(&bar_k[c % NSK], (c / NSK) & 1, abortp);
             float am;
-            const float ss = convert_tile_512<true, false>(xk + (size_t)(c & 1) * xkb, nd, e, am);
+            const float ss = convert_tile_512<true, false>(xk + (size_t)(c % NSK) * xkb, nd, e, am);
             part[(e >> 7) * 128 + (e & 127)] = ss;
             group_sync(kEpi);
             if (e < 128)
@@ -1467,21 +1470,24 @@ CausalLayout causal_layout(const Geo &g) {
 
 struct StateLayout {
     uint32_t o_w, o_xk, o_xv, o_phk, o_small, xv_stride, bytes;
-    int nvs;
+    int nvs, nks;
 };
 StateLayout state_layout(const Geo &g) {
     StateLayout l;
-    for (int nvs = 2; nvs >= 1; --nvs) {
+    // most buffering that fits: three K and two V buffers first
+    const int opts[4][2] = {{3, 2}, {2, 2}, {3, 1}, {2, 1}};
+    for (const auto &op : opts) {
         uint32_t o = 0;
         l.o_w = o; o = align1k(o + (uint32_t)g.np_tile * g.d * 2);
-        l.o_xk = o; o = align1k(o + 2u * kC * g.d * 2);
+        l.o_xk = o; o = align1k(o + (uint32_t)op[0] * kC * g.d * 2);
         l.xv_stride = (uint32_t)(g.dv / 64 + 1) * kBlk;       // V blocks + ones atom
-        l.o_xv = o; o = align1k(o + (uint32_t)nvs * l.xv_stride);
+        l.o_xv = o; o = align1k(o + (uint32_t)op[1] * l.xv_stride);
         l.o_phk = o; o = align1k(o + 4 * kBlk);
         l.o_small = o; o = align1k(o + 840 * 4);
         l.bytes = o + 1024;
-        l.nvs = nvs;
-        if (l.bytes <= 232448) break;
+        l.nks = op[0];
+        l.nvs = op[1];
+        if (l.bytes <= kSmemMax) break;
     }
     return l;
 }
@@ -1617,6 +1623,7 @@ int tc_run(const void *q, const void *k, const void *v, const float *omega, floa
         StateLayout sl = state_layout(g);
         StateArgs sa;
         sa.g = g; sa.H = p.H; sa.L = p.L; sa.seg_len = seg_len; sa.nseg = nstate; sa.nvs = sl.nvs;
+        sa.nks = sl.nks;
         sa.omg = img; sa.state = state; sa.meta = meta; sa.status = dstat;
         sa.o_w = sl.o_w; sa.o_xk = sl.o_xk; sa.o_xv = sl.o_xv; sa.o_phk = sl.o_phk;
         sa.o_small = sl.o_small; sa.xv_stride = sl.xv_stride; sa.tmem_cols = 512;
