@@ -143,6 +143,7 @@ __device__ __forceinline__ float elu1(float p) { return p > 0.f ? p + 1.f : ex2(
 // ---------------------------------------------------------------------------
 __global__ void tc_prep_omega(const float *__restrict__ omega, uint8_t *__restrict__ img, int H,
                               int nproj, int d, int map) {
+    grid_dep_launch();
     const int h = blockIdx.y;
     const size_t per = (size_t)nproj * d;
     for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < per;
@@ -289,8 +290,10 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     tc_fence_after();
     const uint32_t tmem = *tslot;
     bool alive = true;
+    grid_dep_launch();
 
     if (warp == 0) {
+        if (lane == 0 && nchunk == 0) grid_dep_wait();
         if (lane == 0 && nchunk > 0) {
             const uint32_t w_s = smem_u32(w), xk_s = smem_u32(xk), xv_s = smem_u32(xv), phk_s = smem_u32(phk);
             const uint32_t wbytes = (uint32_t)g.np_tile * g.d * 2;
@@ -315,8 +318,6 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                             smem_desc(w_s + kk * 2048, (uint32_t)g.d * 128, 1024), idesc, kk > 0);
                 mma_commit(&bar_pk[c & 1]);
             };
-            mbar_arrive_expect_tx(bar_w, wbytes);
-            bulk_load(w, a.omg + (size_t)head * g.nproj * g.d * 2 + (size_t)ft * wbytes, wbytes, bar_w);
             load_k(0);
             load_v(0);
             if (nchunk > 1) {
@@ -324,6 +325,10 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                 if (NSV == 2) load_v(1);
             }
             if (nchunk > 2 && NSK == 3) load_k(2);
+            // the W image comes from the kernel before this one
+            grid_dep_wait();
+            mbar_arrive_expect_tx(bar_w, wbytes);
+            bulk_load(w, a.omg + (size_t)head * g.nproj * g.d * 2 + (size_t)ft * wbytes, wbytes, bar_w);
             // e_x and e_k alternate between two barriers per chunk parity: the
             // epilogue may finish converting K(0) and K(1) before this thread
             // looks, and one barrier would then have moved two phases on
@@ -560,6 +565,8 @@ struct CombineArgs {
 };
 
 __global__ void tc_combine(const CombineArgs a) {
+    grid_dep_launch();
+    grid_dep_wait();
     const Geo &g = a.g;
     const int bh = blockIdx.x;
     const int upto = a.causal ? blockIdx.y + 1 : a.nseg;   // segments [0, upto)
@@ -668,6 +675,8 @@ struct CausalArgs {
     int H, L, seg_len, nseg;
     const uint8_t *omg;            // MN-major W images
     const float *s_in, *meta_in;   // [BH][nseg][r][dv+1], [BH][nseg][4] (segment 0 unused)
+    const float *state, *meta;     // segment states [BH][nstate][r][dv+1], [BH][nstate][n_ft][4]
+    int nstate, direct;            // direct: combine the earlier segments' states here
     int *status;
     uint32_t o_w, o_x, o_v, o_kb, o_small, tmem_cols;
 };
@@ -747,10 +756,15 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
                             smem_desc(w_s + kk * 2048, (uint32_t)g.d * 128, 1024), idesc, kk > 0);
             };
             if (nchunk > 0) {
-                mbar_arrive_expect_tx(bar_w, wbytes);
-                bulk_load(w, a.omg + (size_t)head * wbytes, wbytes, bar_w);
                 load_x(0);
                 load_v(0);
+            }
+            // the W image (and the state of the earlier segments) come from
+            // the kernels before this one
+            grid_dep_wait();
+            if (nchunk > 0) {
+                mbar_arrive_expect_tx(bar_w, wbytes);
+                bulk_load(w, a.omg + (size_t)head * wbytes, wbytes, bar_w);
                 alive = ewait(bar_w, 0, abortp);
             }
             for (int c = 0; c < nchunk && alive; ++c) {
@@ -828,30 +842,15 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
     const int e = threadIdx.x - 32, ew = e >> 5;
     const int q = (ew + 1) & 3, j = ew >> 2;
     const int row = q * 32 + lane;
-    float R, zmax, vmax;
-    {
-        const float *m = a.meta_in + ((size_t)bh * a.nseg + seg) * 4;
-        const bool has_in = seg > 0;
-        R = has_in ? m[0] : (g.map == FAVOR_MAP_POSITIVE ? -INFINITY : 0.f);
-        zmax = has_in ? m[1] : 0.f;
-        vmax = has_in ? m[2] : 0.f;
-    }
-    // initial state (S_in or zero): tile t, lanes = features, 16 value columns per thread
-    for (int t = 0; t < nft; ++t) {
-        const int f = t * 128 + row;
-        const float *src = (seg > 0) ? a.s_in + (((size_t)bh * a.nseg + seg) * g.r + f) * (g.dv + 1) : nullptr;
-        uint32_t v[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(src ? src[64 * dvt + 16 * j + i] : 0.f);
-        tmem_st16(tm_addr(tmem, q, kColS + t * kSStride + 16 * j), v);
-        if (j == 0) tmem_st1(tm_addr(tmem, q, kColS + t * kSStride + 64), src ? src[g.dv] : 0.f);
-    }
-    tmem_st_wait();
     // pad rows of every KB block: they feed accumulator columns never read
     for (int i = e; i < (g.r / 64) * 15 * 8; i += kEpi) {
         const int blk = i / 120, rr = kKbZ + 1 + (i % 120) / 8, ch = i % 8;
         *reinterpret_cast<uint4 *>(kb + (size_t)blk * kKbBlk + rr * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
     }
+    float R = g.map == FAVOR_MAP_POSITIVE ? -INFINITY : 0.f, zmax = 0.f, vmax = 0.f;
+    float s0[16], s1[16], z0 = 0.f, z1 = 0.f;   // this thread's part of the initial state
+#pragma unroll
+    for (int i = 0; i < 16; ++i) s0[i] = s1[i] = 0.f;
     // sigma S^T and sigma z -> KB rows kKbS.. and kKbZ, sigma a power of two
     // with sigma * (bound on max |S| and max z) <= kSigmaTarget.  alpha != 1
     // first rescales the state in TMEM (the key reference has moved).
@@ -892,8 +891,81 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
         mbar_arrive(e_x);
         return ok_x;
     };
-    state_rows(1.f);
+    // X(0) is the caller's data: convert it while the kernels before this
+    // one finish; the state of the earlier segments is theirs
     if (nchunk > 0) alive = convert_x(0);
+    grid_dep_wait();
+    if (seg > 0 && a.direct) {
+        // the state after segments 0 .. seg-1, combined here at the largest of
+        // their key references (few segments: no separate combine pass)
+        const float *meta = a.meta + (size_t)bh * a.nstate * nft * 4;   // [g][tile][R, max z, max|v|, max|S|]
+        float Rs = -INFINITY;
+        for (int gi = 0; gi < seg; ++gi)
+            for (int t = 0; t < nft; ++t) {
+                Rs = fmaxf(Rs, meta[(gi * nft + t) * 4]);
+                vmax = fmaxf(vmax, meta[(gi * nft + t) * 4 + 2]);
+            }
+        auto scale = [&](int gi, int t) -> float {
+            if (g.map != FAVOR_MAP_POSITIVE) return 1.f;
+            const float Rg = meta[(gi * nft + t) * 4];
+            return (Rg == -INFINITY || Rs == -INFINITY) ? 0.f : ex2(Rg - Rs);
+        };
+        for (int gi = 0; gi < seg; ++gi) {
+            float zt = 0.f;
+            for (int t = 0; t < nft; ++t) zt = fmaxf(zt, meta[(gi * nft + t) * 4 + 1] * scale(gi, t));
+            zmax += zt;
+        }
+        if (g.map == FAVOR_MAP_POSITIVE) R = Rs;
+        const size_t per = (size_t)g.r * (g.dv + 1);
+        for (int gi = 0; gi < seg; ++gi) {
+            const float *st = a.state + ((size_t)bh * a.nstate + gi) * per;
+            const float sc0 = scale(gi, 0), sc1 = nft == 2 ? scale(gi, 1) : 0.f;
+            const float *r0 = st + (size_t)row * (g.dv + 1), *r1 = st + (size_t)(128 + row) * (g.dv + 1);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) s0[i] += r0[64 * dvt + 16 * j + i] * sc0;
+            if (nft == 2) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) s1[i] += r1[64 * dvt + 16 * j + i] * sc1;
+            }
+            if (j == 0) {
+                z0 += r0[g.dv] * sc0;
+                if (nft == 2) z1 += r1[g.dv] * sc1;
+            }
+        }
+    } else if (seg > 0) {
+        const float *m = a.meta_in + ((size_t)bh * a.nseg + seg) * 4;
+        R = m[0];
+        zmax = m[1];
+        vmax = m[2];
+        const float *src = a.s_in + (((size_t)bh * a.nseg + seg) * g.r) * (g.dv + 1);
+        const float *r0 = src + (size_t)row * (g.dv + 1), *r1 = src + (size_t)(128 + row) * (g.dv + 1);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) s0[i] = r0[64 * dvt + 16 * j + i];
+        if (nft == 2) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) s1[i] = r1[64 * dvt + 16 * j + i];
+        }
+        if (j == 0) {
+            z0 = r0[g.dv];
+            if (nft == 2) z1 = r1[g.dv];
+        }
+    }
+    // initial state into TMEM: tile t, lanes = features, 16 value columns per thread
+    {
+        uint32_t u[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(s0[i]);
+        tmem_st16(tm_addr(tmem, q, kColS + 16 * j), u);
+        if (j == 0) tmem_st1(tm_addr(tmem, q, kColS + 64), z0);
+        if (nft == 2) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(s1[i]);
+            tmem_st16(tm_addr(tmem, q, kColS + kSStride + 16 * j), u);
+            if (j == 0) tmem_st1(tm_addr(tmem, q, kColS + kSStride + 64), z1);
+        }
+        tmem_st_wait();
+    }
+    state_rows(1.f);
     for (int c = 0; c < nchunk; ++c) {
         const uint32_t ph = c & 1;
         const int tc0 = t_begin + c * kC;
@@ -1185,6 +1257,7 @@ tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const int nc = a.g.nproj / 4;
+    grid_dep_launch();
     if (nc == 64) causal_body<64>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
     else if (nc == 32) causal_body<32>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
     else causal_body<16>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
@@ -1238,6 +1311,7 @@ __device__ void output_body(const OutputArgs &a, uint8_t *sm, uint32_t tmem,
     bool alive = true;
 
     if (warp == 0) {
+        if (lane == 0 && n == 0) grid_dep_wait();
         if (lane == 0 && n > 0) {
             const uint32_t w_s = smem_u32(w), s_s = smem_u32(sbuf), xs_s = smem_u32(xs);
             const uint32_t wbytes = (uint32_t)g.nproj * g.d * 2, atom = (uint32_t)g.r * 128;
@@ -1257,6 +1331,7 @@ __device__ void output_body(const OutputArgs &a, uint8_t *sm, uint32_t tmem,
                     tma_load_3d(xs + (size_t)s * xb + b * kBlk, tm_q, &bar_x[s], 64 * b, unit_c(u) * kC, unit_bh(u));
             };
             for (int i = 0; i < min(n, nq); ++i) load_q(i);
+            grid_dep_wait();   // the W and state images come from the kernels before this one
             for (int i = 0; i < n && alive; ++i) {
                 const int u = u0 + i;
                 const int key = unit_bh(u) * nvb + unit_dvt(u);
@@ -1424,6 +1499,7 @@ tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    grid_dep_launch();
     const int nc = a.g.nproj / 4;
     if (nc == 64) output_body<64>(a, sm, tmem, &tm_q, &tm_out);
     else if (nc == 32) output_body<32>(a, sm, tmem, &tm_q, &tm_out);
@@ -1510,6 +1586,29 @@ OutputLayout output_layout(const Geo &g) {
         if (l.bytes <= kSmemMax) break;
     }
     return l;
+}
+
+// Launch with programmatic stream serialisation: the kernel may start while
+// the previous kernel on the stream is still running and waits for it with
+// griddepcontrol.wait before touching that kernel's results.
+template <typename... KArgs, typename... Args>
+int launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                     Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...) != cudaSuccess) {
+        cudaGetLastError();
+        return FAVOR_ERR_CUDA;
+    }
+    return FAVOR_OK;
 }
 
 int num_sms() {
@@ -1629,7 +1728,9 @@ int tc_run(const void *q, const void *k, const void *v, const float *omega, floa
         sa.o_small = sl.o_small; sa.xv_stride = sl.xv_stride; sa.tmem_cols = 512;
         if (cudaFuncSetAttribute(tc_state, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sl.bytes) != cudaSuccess)
             return FAVOR_ERR_CUDA;
-        tc_state<<<dim3(g.n_ft, nstate, p.BH), kStateThreads, sl.bytes, st>>>(mk, mv, sa);
+        if ((rc = launch_dependent(tc_state, dim3(g.n_ft, nstate, p.BH), dim3(kStateThreads), sl.bytes, st,
+                                   mk, mv, sa)))
+            return rc;
         FAVOR_LAUNCH_CHECK();
     }
 
@@ -1640,7 +1741,7 @@ int tc_run(const void *q, const void *k, const void *v, const float *omega, floa
         ca.sop = sop;
         ca.slice = 2048;
         const int nsl = (int)((per_state + ca.slice - 1) / ca.slice);
-        tc_combine<<<dim3(p.BH, 1, nsl), 256, 0, st>>>(ca);
+        if ((rc = launch_dependent(tc_combine, dim3(p.BH, 1, nsl), dim3(256), 0, st, ca))) return rc;
         FAVOR_LAUNCH_CHECK();
         OutputLayout ol = output_layout(g);
         OutputArgs oa;
@@ -1655,7 +1756,10 @@ int tc_run(const void *q, const void *k, const void *v, const float *omega, floa
         // one persistent CTA per SM, each on a contiguous run of (head, dv tile, chunk) units
         const int grid = std::min(oa.total_units, sms);
         stats_begin(st, "tc_output");
-        tc_output<<<grid, kOutThreads, ol.bytes, st>>>(mq, mo, oa);
+        if ((rc = launch_dependent(tc_output, dim3(grid), dim3(kOutThreads), ol.bytes, st, mq, mo, oa))) {
+            stats_end(st);
+            return rc;
+        }
         stats_end(st);
         FAVOR_LAUNCH_CHECK();
         return FAVOR_OK;
@@ -1663,13 +1767,15 @@ int tc_run(const void *q, const void *k, const void *v, const float *omega, floa
 
     float *s_in = cv.take<float>((size_t)p.BH * G * per_state);
     float *meta_in = cv.take<float>((size_t)p.BH * G * 4);
-    if (G > 1) {
+    // up to four segments the scan kernel combines the earlier states itself
+    const bool direct = G <= 4;
+    if (G > 1 && !direct) {
         CombineArgs ca{};
         ca.g = g; ca.nseg = nstate; ca.causal = 1; ca.state = state; ca.meta = meta;
         ca.s_in = s_in; ca.meta_in = meta_in;
         ca.slice = 2048;
         const int nsl = (int)((per_state + ca.slice - 1) / ca.slice);
-        tc_combine<<<dim3(p.BH, G - 1, nsl), 256, 0, st>>>(ca);
+        if ((rc = launch_dependent(tc_combine, dim3(p.BH, G - 1, nsl), dim3(256), 0, st, ca))) return rc;
         FAVOR_LAUNCH_CHECK();
     }
     CausalLayout cl = causal_layout(g);
@@ -1677,12 +1783,17 @@ int tc_run(const void *q, const void *k, const void *v, const float *omega, floa
     a.g = g;
     a.H = p.H; a.L = p.L; a.seg_len = seg_len; a.nseg = G;
     a.omg = img; a.s_in = s_in; a.meta_in = meta_in; a.status = dstat;
+    a.state = state; a.meta = meta; a.nstate = nstate; a.direct = direct ? 1 : 0;
     a.o_w = cl.o_w; a.o_x = cl.o_x; a.o_v = cl.o_v; a.o_kb = cl.o_kb; a.o_small = cl.o_small;
     a.tmem_cols = 512;
     if (cudaFuncSetAttribute(tc_causal, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cl.bytes) != cudaSuccess)
         return FAVOR_ERR_CUDA;
     stats_begin(st, "tc_causal");
-    tc_causal<<<dim3(G, nvb, p.BH), kCausalThreads, cl.bytes, st>>>(mq, mk, mv, mo, a);
+    if ((rc = launch_dependent(tc_causal, dim3(G, nvb, p.BH), dim3(kCausalThreads), cl.bytes, st, mq, mk, mv,
+                               mo, a))) {
+        stats_end(st);
+        return rc;
+    }
     stats_end(st);
     FAVOR_LAUNCH_CHECK();
     return FAVOR_OK;

@@ -259,6 +259,16 @@ __device__ __forceinline__ void tmem_st_wait() {
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start while the kernel before it is still running;
+// grid_dep_wait() blocks the calling thread until that kernel (and so every
+// kernel before it on the stream) has completed and its writes are visible,
+// grid_dep_launch() lets the next kernel start launching.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // per-warpgroup register budgets (every warp of the warpgroup executes these)
 // ---------------------------------------------------------------------------
 template <uint32_t N>

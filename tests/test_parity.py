@@ -133,8 +133,8 @@ def test_head_dims(d, dv, m, causal):
 # and carries its state from chunk to chunk (the launch shape of the full-size
 # workloads, at a length the oracle finishes quickly)
 @pytest.mark.parametrize("B,H,dv,heads", [(1, 160, 64, [0, 77, 159]), (4, 19, 64, [0, 40, 75]),
-                                          (2, 80, 128, [1, 100, 159])],
-                         ids=["one_segment", "two_segments", "dv128"])
+                                          (2, 20, 64, [0, 21, 39]), (2, 80, 128, [1, 100, 159])],
+                         ids=["one_segment", "two_segments", "four_segments", "dv128"])
 def test_causal_many_chunks_per_cta(B, H, dv, heads):
     w = CAUSAL8K.with_(dv=dv)
     inp = make_inputs(w, L=1000, B=B, H=H)
