@@ -38,7 +38,9 @@ TRAFFIC = {
     ("tc_causal", "causal8k"): (305.94e6, "a7852c27acac0a5d"),
 }
 KERNEL_SECTIONS = {
-    "tc_causal": ("// tc_causal: the chunked causal scan, warp-specialised.", "// host side"),
+    "tc_causal": ("// tc_causal: the chunked causal scan, warp-specialised.", "// tc_output: non-causal rows"),
+    "tc_output": ("// tc_output: non-causal rows", "// host side"),
+    "tc_state": ("// tc_state: per (feature tile, segment, head) the segment state", "// tc_combine:"),
 }
 
 

@@ -43,6 +43,7 @@ constexpr float kSigmaTarget = 16384.f;  // bound for |sigma * S| in the fp16 st
 // largest key feature kept, e^10: a chunk may exceed the reference by e^2
 // before the reference moves
 constexpr float kMaxFeature = 22026.4658f;
+constexpr float kLog2MaxFeature = 14.4269504f;          // log2(e^10)
 constexpr long long kWaitLimit = 1ll << 32;             // ~2 s of clock cycles
 constexpr uint32_t kBlk = 16384;        // one [128][64] fp16 block (128B swizzle)
 
@@ -704,8 +705,9 @@ __device__ __forceinline__ void kb_state16(uint8_t *kb, int f, int c0, const flo
         *reinterpret_cast<__half *>(base + i * 128 + ((c3 ^ (uint32_t)(i & 7)) << 4)) = __float2half_rn(v[i] * sc);
 }
 
-// NC = projection columns per epilogue thread (a quarter of the projections)
-template <int NC>
+// NC = projection columns per epilogue thread (a quarter of the projections),
+// MAP the feature map
+template <int NC, int MAP>
 __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
                             const CUtensorMap *tm_q, const CUtensorMap *tm_k,
                             const CUtensorMap *tm_v, const CUtensorMap *tm_out) {
@@ -847,7 +849,7 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
         const int blk = i / 120, rr = kKbZ + 1 + (i % 120) / 8, ch = i % 8;
         *reinterpret_cast<uint4 *>(kb + (size_t)blk * kKbBlk + rr * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
     }
-    float R = g.map == FAVOR_MAP_POSITIVE ? -INFINITY : 0.f, zmax = 0.f, vmax = 0.f;
+    float R = MAP == FAVOR_MAP_POSITIVE ? -INFINITY : 0.f, zmax = 0.f, vmax = 0.f;
     float s0[16], s1[16], z0 = 0.f, z1 = 0.f;   // this thread's part of the initial state
 #pragma unroll
     for (int i = 0; i < 16; ++i) s0[i] = s1[i] = 0.f;
@@ -906,7 +908,7 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
                 vmax = fmaxf(vmax, meta[(gi * nft + t) * 4 + 2]);
             }
         auto scale = [&](int gi, int t) -> float {
-            if (g.map != FAVOR_MAP_POSITIVE) return 1.f;
+            if (MAP != FAVOR_MAP_POSITIVE) return 1.f;
             const float Rg = meta[(gi * nft + t) * 4];
             return (Rg == -INFINITY || Rs == -INFINITY) ? 0.f : ex2(Rg - Rs);
         };
@@ -915,7 +917,7 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
             for (int t = 0; t < nft; ++t) zt = fmaxf(zt, meta[(gi * nft + t) * 4 + 1] * scale(gi, t));
             zmax += zt;
         }
-        if (g.map == FAVOR_MAP_POSITIVE) R = Rs;
+        if (MAP == FAVOR_MAP_POSITIVE) R = Rs;
         const size_t per = (size_t)g.r * (g.dv + 1);
         for (int gi = 0; gi < seg; ++gi) {
             const float *st = a.state + ((size_t)bh * a.nstate + gi) * per;
@@ -974,11 +976,12 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
         // ---------------- key features -> KB rows 0..127 ----------------
         alive &= ewait(bar_pk, ph, abortp);
         tc_fence_after();
+        const uint32_t pcol = tm_addr(tmem, q, kColP + NC * j);
         float pv[NC];
 #pragma unroll
         for (int b = 0; b < NC / 16; ++b) {
             float t16[16];
-            tmem_ld16(tm_addr(tmem, q, kColP + NC * j + 16 * b), t16);
+            tmem_ld16(pcol + 16 * b, t16);
 #pragma unroll
             for (int i = 0; i < 16; ++i) pv[16 * b + i] = t16[i];
         }
@@ -989,47 +992,29 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
         if (c > 0) alive &= ewait(bar_st, (c - 1) & 1, abortp);
         const float nkr = nk[row];
         float mf = 0.f, moved = 1.f;   // moved: state rescale when the key reference moves
-        if (g.map == FAVOR_MAP_POSITIVE) {
-            if (R == -INFINITY) {
-                float mx = -INFINITY;
+        if constexpr (MAP == FAVOR_MAP_POSITIVE) {
+            float mx = -INFINITY;
 #pragma unroll
-                for (int i = 0; i < NC; ++i) mx = fmaxf(mx, pv[i]);
-                R = grp_max(ok ? mx - nkr : -INFINITY, red, ew) - kShift;
+            for (int i = 0; i < NC; ++i) mx = fmaxf(mx, pv[i]);
+            // a key whose largest feature would pass e^(shift + slack) at the
+            // current reference (always so before the first key) moves the
+            // reference to it; the state so far is rescaled below
+            if (group_or(ok && mx - nkr - R > kLog2MaxFeature, kEpi)) {
+                const float Rn = grp_max(ok ? mx - nkr : -INFINITY, red, ew) - kShift;
+                if (R != -INFINITY) moved = ex2(R - Rn);
+                R = Rn;
             }
             // rows past the end take an infinite offset: their features are 0
-            float off = ok ? nkr + R : INFINITY;
+            const float off = ok ? nkr + R : INFINITY;
+            mf = ex2(mx - off);
 #pragma unroll
             for (int b = 0; b < NC / 8; ++b) {
                 float v[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    v[i] = ex2(pv[8 * b + i] - off);
-                    mf = fmaxf(mf, v[i]);
-                }
+                for (int i = 0; i < 8; ++i) v[i] = ex2(pv[8 * b + i] - off);
                 kb_store8(kb, row, NC * j + 8 * b, v);
             }
-            // a feature beyond e^(shift + slack) means a key above the reference
-            // (rare): move the reference to that key, rescale the state and
-            // redo the features
-            if (group_or(mf > kMaxFeature, kEpi)) {
-                const float top = grp_max(ok ? log2f(mf) : -INFINITY, red, ew);
-                const float Rn = R + (top - kShift);
-                moved = ex2(R - Rn);
-                R = Rn;
-                off = ok ? nkr + R : INFINITY;
-                mf = 0.f;
-#pragma unroll
-                for (int b = 0; b < NC / 8; ++b) {
-                    float v[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        v[i] = ex2(pv[8 * b + i] - off);
-                        mf = fmaxf(mf, v[i]);
-                    }
-                    kb_store8(kb, row, NC * j + 8 * b, v);
-                }
-            }
-        } else if (g.map == FAVOR_MAP_TRIG) {
+        } else if constexpr (MAP == FAVOR_MAP_TRIG) {
             // projection p -> features 128 (p / 64) + p % 64 (sin) and that + 64
             // (cos): each 128-feature tile holds the sin and cos of 64 projections
             const int fs = 128 * ((NC * j) / 64) + (NC * j) % 64;
@@ -1068,13 +1053,13 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
 #pragma unroll
         for (int b = 0; b < NC / 16; ++b) {
             float t16[16];
-            tmem_ld16(tm_addr(tmem, q, kColP + NC * j + 16 * b), t16);
+            tmem_ld16(pcol + 16 * b, t16);
 #pragma unroll
             for (int i = 0; i < 16; ++i) pv[16 * b + i] = t16[i];
         }
         tmem_ld_wait();
         float qoff = 0.f;
-        if (g.map == FAVOR_MAP_POSITIVE) {
+        if constexpr (MAP == FAVOR_MAP_POSITIVE) {
             float mx = -INFINITY;
 #pragma unroll
             for (int i = 0; i < NC; ++i) mx = fmaxf(mx, pv[i]);
@@ -1084,7 +1069,7 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
         group_sync(kEpi);   // every projection column read: phi_Q may now overwrite them
         tc_fence_after();
 
-        if (g.map == FAVOR_MAP_POSITIVE) {
+        if constexpr (MAP == FAVOR_MAP_POSITIVE) {
             qoff = fmaxf(fmaxf(part[row], part[128 + row]), fmaxf(part[256 + row], part[384 + row])) - kShift;
 #pragma unroll
             for (int b = 0; b < NC / 32; ++b) {
@@ -1094,7 +1079,7 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
                     o[i] = pack_half2(ex2(pv[32 * b + 2 * i] - qoff), ex2(pv[32 * b + 2 * i + 1] - qoff));
                 tmem_st16(tm_addr(tmem, q, (NC * j + 32 * b) / 2), o);
             }
-        } else if (g.map == FAVOR_MAP_TRIG) {
+        } else if constexpr (MAP == FAVOR_MAP_TRIG) {
             // same feature order as the keys; 16 projections give 8 packed
             // columns of sin and 8 of cos
             const int fs = 128 * ((NC * j) / 64) + (NC * j) % 64;
@@ -1258,9 +1243,15 @@ tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     const uint32_t tmem = *tslot;
     const int nc = a.g.nproj / 4;
     grid_dep_launch();
-    if (nc == 64) causal_body<64>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
-    else if (nc == 32) causal_body<32>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
-    else causal_body<16>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
+    if (a.g.map == FAVOR_MAP_POSITIVE) {
+        if (nc == 64) causal_body<64, FAVOR_MAP_POSITIVE>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
+        else causal_body<32, FAVOR_MAP_POSITIVE>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
+    } else if (a.g.map == FAVOR_MAP_TRIG) {
+        if (nc == 32) causal_body<32, FAVOR_MAP_TRIG>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
+        else causal_body<16, FAVOR_MAP_TRIG>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
+    } else {
+        causal_body<32, FAVOR_MAP_ELU1>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1285,7 +1276,7 @@ struct OutputArgs {
 
 constexpr int kOutThreads = 32 + kEpi;
 
-template <int NC>
+template <int NC, int MAP>
 __device__ void output_body(const OutputArgs &a, uint8_t *sm, uint32_t tmem,
                             const CUtensorMap *tm_q, const CUtensorMap *tm_out) {
     const Geo &g = a.g;
@@ -1304,7 +1295,9 @@ __device__ void output_body(const OutputArgs &a, uint8_t *sm, uint32_t tmem,
              *e_x = &bars[5], *e_q = &bars[6];
     volatile int *abortp = reinterpret_cast<volatile int *>(small + 570);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    constexpr int kColD = 256;
+    // TMEM: projections [0, nproj) | D = [phi_Q sigma KV | phi_Q sigma z] [256, 336) |
+    // phi_Q packed [336, 336 + r/2)
+    constexpr int kColD = 256, kColPhi = 336;
     auto unit_bh = [&](int u) { return u / (nvb * nchunk); };
     auto unit_dvt = [&](int u) { return (u / nchunk) % nvb; };
     auto unit_c = [&](int u) { return u % nchunk; };
@@ -1315,7 +1308,7 @@ __device__ void output_body(const OutputArgs &a, uint8_t *sm, uint32_t tmem,
         if (lane == 0 && n > 0) {
             const uint32_t w_s = smem_u32(w), s_s = smem_u32(sbuf), xs_s = smem_u32(xs);
             const uint32_t wbytes = (uint32_t)g.nproj * g.d * 2, atom = (uint32_t)g.r * 128;
-            int wphase = 0, cur = -1;
+            int wphase = 0;
             auto load_operands = [&](int u) {
                 const int bh = unit_bh(u), dvt = unit_dvt(u);
                 mbar_arrive_expect_tx(bar_w, wbytes + 2 * atom);
@@ -1330,39 +1323,51 @@ __device__ void output_body(const OutputArgs &a, uint8_t *sm, uint32_t tmem,
                 for (int b = 0; b < nd; ++b)
                     tma_load_3d(xs + (size_t)s * xb + b * kBlk, tm_q, &bar_x[s], 64 * b, unit_c(u) * kC, unit_bh(u));
             };
+            auto issue_pq = [&](int i) {
+                const uint32_t x_s = xs_s + (uint32_t)(i % nq) * xb;
+                const uint32_t idesc = idesc_f16(128, g.nproj, 0, 1);
+                for (int kk = 0; kk < g.d / 16; ++kk)
+                    mma_f16(tmem, smem_desc(x_s + (kk >> 2) * kBlk + (kk & 3) * 32, 16, 1024),
+                            smem_desc(w_s + kk * 2048, (uint32_t)g.d * 128, 1024), idesc, kk > 0);
+                mma_commit(bar_pq);
+            };
+            auto key_of = [&](int u) { return unit_bh(u) * nvb + unit_dvt(u); };
             for (int i = 0; i < min(n, nq); ++i) load_q(i);
             grid_dep_wait();   // the W and state images come from the kernels before this one
-            for (int i = 0; i < n && alive; ++i) {
-                const int u = u0 + i;
-                const int key = unit_bh(u) * nvb + unit_dvt(u);
-                if (key != cur) {
-                    // new head / dv tile: every MMA on the old operands has completed
-                    load_operands(u);
-                    if (!(alive = ewait(bar_w, wphase & 1, abortp))) break;
-                    ++wphase;
-                    cur = key;
-                }
-                if (!(alive = ewait(e_x, i & 1, abortp))) break;
+            load_operands(u0);
+            alive = ewait(bar_w, wphase & 1, abortp) && ewait(e_x, 0, abortp);
+            ++wphase;
+            if (alive) {
                 tc_fence_after();
-                {
-                    const uint32_t x_s = xs_s + (uint32_t)(i % nq) * xb;
-                    const uint32_t idesc = idesc_f16(128, g.nproj, 0, 1);
-                    for (int kk = 0; kk < g.d / 16; ++kk)
-                        mma_f16(tmem, smem_desc(x_s + (kk >> 2) * kBlk + (kk & 3) * 32, 16, 1024),
-                                smem_desc(w_s + kk * 2048, (uint32_t)g.d * 128, 1024), idesc, kk > 0);
-                    mma_commit(bar_pq);
-                }
+                issue_pq(0);
+            }
+            for (int i = 0; i < n && alive; ++i) {
+                // P_Q(i) done: its Q slot takes unit i + nq
                 if (!(alive = ewait(bar_pq, i & 1, abortp))) break;
                 if (i + nq < n) load_q(i + nq);
                 if (!(alive = ewait(e_q, i & 1, abortp))) break;
                 tc_fence_after();
                 {
+                    // D = phi_Q [sigma KV | sigma z] (B MN-major: the state atom, then the z atom)
                     const uint32_t idesc = idesc_f16(128, 80, 0, 1);
                     for (int kk = 0; kk < g.r / 16; ++kk)
-                        mma_f16_ts(tmem + kColD, tmem + 8 * kk, smem_desc(s_s + kk * 2048, atom, 1024), idesc, kk > 0);
+                        mma_f16_ts(tmem + kColD, tmem + kColPhi + 8 * kk, smem_desc(s_s + kk * 2048, atom, 1024),
+                                   idesc, kk > 0);
                     mma_commit(bar_d);
                 }
-                if (!(alive = ewait(bar_d, i & 1, abortp))) break;
+                if (i + 1 < n) {
+                    if (key_of(u0 + i + 1) != key_of(u0 + i)) {
+                        // new head / dv tile: every MMA on the old operands completes first
+                        if (!(alive = ewait(bar_d, i & 1, abortp))) break;
+                        load_operands(u0 + i + 1);
+                        if (!(alive = ewait(bar_w, wphase & 1, abortp))) break;
+                        ++wphase;
+                    }
+                    // P_Q(i + 1) while the epilogue turns D(i) into the output
+                    if (!(alive = ewait(e_x, (i + 1) & 1, abortp))) break;
+                    tc_fence_after();
+                    issue_pq(i + 1);
+                }
             }
             if (!alive) set_status(a.status, FAVOR_ERR_TIMEOUT);
         }
@@ -1381,81 +1386,82 @@ __device__ void output_body(const OutputArgs &a, uint8_t *sm, uint32_t tmem,
         return ok;
     };
     if (n > 0) alive = convert_x(0);
+    const uint32_t pcol = tm_addr(tmem, q, NC * j);
     for (int i = 0; i < n; ++i) {
         const int u = u0 + i;
-        // ---- query features -> phi_Q packed in TMEM [0, r/2) ----
+        // ---- query features -> phi_Q packed in TMEM [kColPhi, kColPhi + r/2) ----
         alive &= ewait(bar_pq, i & 1, abortp);
         tc_fence_after();
-        float pv[NC];
-#pragma unroll
-        for (int b = 0; b < NC / 16; ++b) {
-            float t16[16];
-            tmem_ld16(tm_addr(tmem, q, NC * j + 16 * b), t16);
-#pragma unroll
-            for (int k2 = 0; k2 < 16; ++k2) pv[16 * b + k2] = t16[k2];
-        }
-        tmem_ld_wait();
-        if (g.map == FAVOR_MAP_POSITIVE) {
+        if constexpr (MAP == FAVOR_MAP_POSITIVE) {
             float mx = -INFINITY;
 #pragma unroll
-            for (int k2 = 0; k2 < NC; ++k2) mx = fmaxf(mx, pv[k2]);
+            for (int b = 0; b < NC / 32; ++b) {
+                float t32[32];
+                tmem_ld32(pcol + 32 * b, t32);
+                tmem_ld_wait();
+#pragma unroll
+                for (int k2 = 0; k2 < 32; ++k2) mx = fmaxf(mx, t32[k2]);
+            }
             part[j * 128 + row] = mx;
-        }
-        tc_fence_before();
-        group_sync(kEpi);   // every projection column read: phi_Q may overwrite them
-        tc_fence_after();
-        if (g.map == FAVOR_MAP_POSITIVE) {
+            group_sync(kEpi);
             const float qoff = fmaxf(fmaxf(part[row], part[128 + row]), fmaxf(part[256 + row], part[384 + row])) - kShift;
 #pragma unroll
-            for (int b = 0; b < NC / 32; ++b) {
-                uint32_t o[16];
+            for (int b = 0; b < NC / 16; ++b) {
+                float t16[16];
+                tmem_ld16(pcol + 16 * b, t16);
+                tmem_ld_wait();
+                uint32_t o[8];
 #pragma unroll
-                for (int k2 = 0; k2 < 16; ++k2)
-                    o[k2] = pack_half2(ex2(pv[32 * b + 2 * k2] - qoff), ex2(pv[32 * b + 2 * k2 + 1] - qoff));
-                tmem_st16(tm_addr(tmem, q, (NC * j + 32 * b) / 2), o);
+                for (int k2 = 0; k2 < 8; ++k2) o[k2] = pack_half2(ex2(t16[2 * k2] - qoff), ex2(t16[2 * k2 + 1] - qoff));
+                tmem_st8(tm_addr(tmem, q, kColPhi + (NC * j + 16 * b) / 2), o);
             }
-        } else if (g.map == FAVOR_MAP_TRIG) {
+        } else if constexpr (MAP == FAVOR_MAP_TRIG) {
             const int fs = 128 * ((NC * j) / 64) + (NC * j) % 64;
 #pragma unroll
             for (int b = 0; b < NC / 16; ++b) {
+                float t16[16];
+                tmem_ld16(pcol + 16 * b, t16);
+                tmem_ld_wait();
                 uint32_t os[8], oc[8];
 #pragma unroll
                 for (int k2 = 0; k2 < 8; ++k2) {
                     float s0, c0, s1, c1;
-                    sincos_reduced(pv[16 * b + 2 * k2], s0, c0);
-                    sincos_reduced(pv[16 * b + 2 * k2 + 1], s1, c1);
+                    sincos_reduced(t16[2 * k2], s0, c0);
+                    sincos_reduced(t16[2 * k2 + 1], s1, c1);
                     os[k2] = pack_half2(s0, s1);
                     oc[k2] = pack_half2(c0, c1);
                 }
-                tmem_st8(tm_addr(tmem, q, (fs + 16 * b) / 2), os);
-                tmem_st8(tm_addr(tmem, q, (fs + 64 + 16 * b) / 2), oc);
+                tmem_st8(tm_addr(tmem, q, kColPhi + (fs + 16 * b) / 2), os);
+                tmem_st8(tm_addr(tmem, q, kColPhi + (fs + 64 + 16 * b) / 2), oc);
             }
         } else {
 #pragma unroll
-            for (int b = 0; b < NC / 32; ++b) {
-                uint32_t o[16];
+            for (int b = 0; b < NC / 16; ++b) {
+                float t16[16];
+                tmem_ld16(pcol + 16 * b, t16);
+                tmem_ld_wait();
+                uint32_t o[8];
 #pragma unroll
-                for (int k2 = 0; k2 < 16; ++k2)
-                    o[k2] = pack_half2(elu1(pv[32 * b + 2 * k2]), elu1(pv[32 * b + 2 * k2 + 1]));
-                tmem_st16(tm_addr(tmem, q, (NC * j + 32 * b) / 2), o);
+                for (int k2 = 0; k2 < 8; ++k2) o[k2] = pack_half2(elu1(t16[2 * k2]), elu1(t16[2 * k2 + 1]));
+                tmem_st8(tm_addr(tmem, q, kColPhi + (NC * j + 16 * b) / 2), o);
             }
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(e_q);
-        // ---- next unit's Q tile (while the MMA runs) ----
+        mbar_arrive(e_q);   // also: the projections have been read
+        // ---- next unit's Q tile (while the tensor core computes D and P_Q) ----
         if (i + 1 < n) alive &= convert_x(i + 1);
         // ---- output ----
         alive &= ewait(bar_d, i & 1, abortp);
         tc_fence_after();
-        float dn[16], dd[16];
+        float dn[16], dd;
         tmem_ld16(tm_addr(tmem, q, kColD + 16 * j), dn);
-        tmem_ld16(tm_addr(tmem, q, kColD + 64), dd);
+        tmem_ld1(tm_addr(tmem, q, kColD + 64), dd);
         tmem_ld_wait();
         if (e == 0) bulk_wait_read0();   // the previous unit's staging has been read
         group_sync(kEpi);
         {
-            const float id = 1.f / dd[0];
+            const float id = __fdividef(1.f, dd);
             uint8_t *halfp = stage + (size_t)((16 * j) >> 5) * kBlk;
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
@@ -1501,9 +1507,15 @@ tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     const uint32_t tmem = *tslot;
     grid_dep_launch();
     const int nc = a.g.nproj / 4;
-    if (nc == 64) output_body<64>(a, sm, tmem, &tm_q, &tm_out);
-    else if (nc == 32) output_body<32>(a, sm, tmem, &tm_q, &tm_out);
-    else output_body<16>(a, sm, tmem, &tm_q, &tm_out);
+    if (a.g.map == FAVOR_MAP_POSITIVE) {
+        if (nc == 64) output_body<64, FAVOR_MAP_POSITIVE>(a, sm, tmem, &tm_q, &tm_out);
+        else output_body<32, FAVOR_MAP_POSITIVE>(a, sm, tmem, &tm_q, &tm_out);
+    } else if (a.g.map == FAVOR_MAP_TRIG) {
+        if (nc == 32) output_body<32, FAVOR_MAP_TRIG>(a, sm, tmem, &tm_q, &tm_out);
+        else output_body<16, FAVOR_MAP_TRIG>(a, sm, tmem, &tm_q, &tm_out);
+    } else {
+        output_body<32, FAVOR_MAP_ELU1>(a, sm, tmem, &tm_q, &tm_out);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
