@@ -222,6 +222,22 @@ __device__ __forceinline__ float convert_tile_512(uint8_t *tile, int nblk, int e
     return sumsq;
 }
 
+// One 16-byte chunk (8 values) of a bf16 tile -> fp16 in place; returns the
+// chunk's sum of squares.
+__device__ __forceinline__ float cvt_chunk16_sq(uint8_t *p) {
+    uint4 u = *reinterpret_cast<uint4 *>(p);
+    uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
+        ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+        w[i] = pack_half2(lo, hi);
+    }
+    *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+    return ss;
+}
+
 // ---------------------------------------------------------------------------
 // tc_state: per (feature tile, segment, head) the segment state
 //   S[f][c] = sum_t phi(k_t)_f v_t[c],  z[f] = sum_t phi(k_t)_f
@@ -259,8 +275,7 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     const uint32_t xkb = (uint32_t)kC * g.d * 2;
     uint8_t *w = sm + a.o_w, *xk = sm + a.o_xk, *xv = sm + a.o_xv, *phk = sm + a.o_phk;
     float *small = reinterpret_cast<float *>(sm + a.o_small);
-    float *nk = small;              // [2][128]
-    float *part = small + 256;      // [4][128]
+    float *nk = small;              // [3][128] half key norms, by chunk % 3
     float *red = small + 768;       // [32]
     uint64_t *bars = reinterpret_cast<uint64_t *>(small + 800);
     uint64_t *bar_w = &bars[0], *bar_k = &bars[13] /*[3]*/, *bar_v = &bars[3] /*[2]*/,
@@ -383,14 +398,22 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             for (int cc = 16 * j; cc < g.dv + 16; cc += 64) tmem_st16(tm_addr(tmem, q, col_s + cc), zero);
             tmem_st_wait();
         }
+        // K(c) -> fp16 and the half key norms: thread e takes row e / 4, chunks
+        // 2 (e % 4) and 2 (e % 4) + 1 of each 64-column block, the row's four
+        // threads being neighbouring lanes.  The norms of chunk c go to buffer
+        // c % 3, last read two chunks (and two group barriers) earlier.
         auto convert_k = [&](int c) -> bool {
             bool ok = ewait(&bar_k[c % NSK], (c / NSK) & 1, abortp);
-            float am;
-            const float ss = convert_tile_512<true, false>(xk + (size_t)(c % NSK) * xkb, nd, e, am);
-            part[(e >> 7) * 128 + (e & 127)] = ss;
-            group_sync(kEpi);
-            if (e < 128)
-                nk[(c & 1) * 128 + e] = 0.5f * kLog2e * ((part[e] + part[128 + e]) + (part[256 + e] + part[384 + e]));
+            uint8_t *tile = xk + (size_t)(c % NSK) * xkb;
+            const int r = e >> 2, pp = e & 3;
+            float ss = 0.f;
+            for (int b = 0; b < nd; ++b)
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    ss += cvt_chunk16_sq(tile + b * kBlk + r * 128 + (((2 * pp + h) ^ (r & 7)) << 4));
+            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+            ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+            if (pp == 0) nk[(c % 3) * 128 + r] = 0.5f * kLog2e * ss;
             fence_async_smem();
             mbar_arrive(&e_x[c & 1]);
             return ok;
@@ -413,51 +436,39 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                 float pv[32];
                 tmem_ld32(tm_addr(tmem, q, pcol + 32 * j), pv);
                 tmem_ld_wait();
-                const float nkr = nk[(c & 1) * 128 + row];
-                if (R == -INFINITY) {
-                    float mx = -INFINITY;
+                const float nkr = nk[(c % 3) * 128 + row];
+                float mx = -INFINITY;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, pv[i]);
-                    R = grp_max(ok ? mx - nkr : -INFINITY, red, ew) - kShift;
+                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, pv[i]);
+                // a key whose largest feature would pass e^(shift + slack) at the
+                // current reference (always so before the first key) moves the
+                // reference to it; the running state is rescaled to match
+                if (group_or(ok && mx - nkr - R > kLog2MaxFeature, kEpi)) {
+                    const float Rn = grp_max(ok ? mx - nkr : -INFINITY, red, ew) - kShift;
+                    if (R != -INFINITY) {
+                        const float alpha = ex2(R - Rn);
+                        if (c >= 1) alive &= ewait(&bar_s[(c - 1) & 1], ((c - 1) >> 1) & 1, abortp);
+                        tc_fence_after();
+                        for (int cc = 16 * j; cc < g.dv + 16; cc += 64) {
+                            float v[16];
+                            tmem_ld16(tm_addr(tmem, q, col_s + cc), v);
+                            tmem_ld_wait();
+                            uint32_t u[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(v[i] * alpha);
+                            tmem_st16(tm_addr(tmem, q, col_s + cc), u);
+                        }
+                        tmem_st_wait();
+                    }
+                    R = Rn;
                 }
                 // rows past the end take an infinite offset: their features are 0
-                float off = ok ? nkr + R : INFINITY;
-                float mf = 0.f;
-                uint8_t *blk = phb + (size_t)(j >> 1) * kBlk;
-                const int c0 = 32 * (j & 1);
+                const float off = ok ? nkr + R : INFINITY;
                 {
                     float v[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        v[i] = ex2(pv[i] - off);
-                        mf = fmaxf(mf, v[i]);
-                    }
-                    store_row32(blk, row, c0, v);
-                }
-                if (group_or(mf > kMaxFeature, kEpi)) {
-                    // a key above the reference (rare): move it, rescale the
-                    // running state, redo the features
-                    const float top = grp_max(ok ? log2f(mf) : -INFINITY, red, ew);
-                    const float Rn = R + (top - kShift);
-                    const float alpha = ex2(R - Rn);
-                    R = Rn;
-                    off = ok ? nkr + R : INFINITY;
-                    if (c >= 1) alive &= ewait(&bar_s[(c - 1) & 1], ((c - 1) >> 1) & 1, abortp);
-                    tc_fence_after();
-                    for (int cc = 16 * j; cc < g.dv + 16; cc += 64) {
-                        float v[16];
-                        tmem_ld16(tm_addr(tmem, q, col_s + cc), v);
-                        tmem_ld_wait();
-                        uint32_t u[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(v[i] * alpha);
-                        tmem_st16(tm_addr(tmem, q, col_s + cc), u);
-                    }
-                    tmem_st_wait();
-                    float v[32];
-#pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = ex2(pv[i] - off);
-                    store_row32(blk, row, c0, v);
+                    store_row32(phb + (size_t)(j >> 1) * kBlk, row, 32 * (j & 1), v);
                 }
             } else if (g.map == FAVOR_MAP_TRIG) {
                 // 64 projections per tile: thread j takes 16 of them; the tile
