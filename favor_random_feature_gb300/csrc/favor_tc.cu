@@ -443,23 +443,10 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                 // a key whose largest feature would pass e^(shift + slack) at the
                 // current reference (always so before the first key) moves the
                 // reference to it; the running state is rescaled to match
+                float alpha = 1.f;
                 if (group_or(ok && mx - nkr - R > kLog2MaxFeature, kEpi)) {
                     const float Rn = grp_max(ok ? mx - nkr : -INFINITY, red, ew) - kShift;
-                    if (R != -INFINITY) {
-                        const float alpha = ex2(R - Rn);
-                        if (c >= 1) alive &= ewait(&bar_s[(c - 1) & 1], ((c - 1) >> 1) & 1, abortp);
-                        tc_fence_after();
-                        for (int cc = 16 * j; cc < g.dv + 16; cc += 64) {
-                            float v[16];
-                            tmem_ld16(tm_addr(tmem, q, col_s + cc), v);
-                            tmem_ld_wait();
-                            uint32_t u[16];
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(v[i] * alpha);
-                            tmem_st16(tm_addr(tmem, q, col_s + cc), u);
-                        }
-                        tmem_st_wait();
-                    }
+                    if (R != -INFINITY) alpha = ex2(R - Rn);
                     R = Rn;
                 }
                 // rows past the end take an infinite offset: their features are 0
@@ -469,6 +456,22 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = ex2(pv[i] - off);
                     store_row32(phb + (size_t)(j >> 1) * kBlk, row, 32 * (j & 1), v);
+                }
+                if (alpha != 1.f) {
+                    // the running state moves to the new reference (once the
+                    // previous chunk's update is in it)
+                    if (c >= 1) alive &= ewait(&bar_s[(c - 1) & 1], ((c - 1) >> 1) & 1, abortp);
+                    tc_fence_after();
+                    for (int cc = 16 * j; cc < g.dv + 16; cc += 64) {
+                        float v[16];
+                        tmem_ld16(tm_addr(tmem, q, col_s + cc), v);
+                        tmem_ld_wait();
+                        uint32_t u[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(v[i] * alpha);
+                        tmem_st16(tm_addr(tmem, q, col_s + cc), u);
+                    }
+                    tmem_st_wait();
                 }
             } else if (g.map == FAVOR_MAP_TRIG) {
                 // 64 projections per tile: thread j takes 16 of them; the tile
