@@ -35,7 +35,9 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM traffic (read + write bytes per launch) of a kernel from one ncu capture
 # (profiles/), valid while the kernel's source section is unchanged.
 TRAFFIC = {
-    ("tc_causal", "causal8k"): (305.94e6, "a7852c27acac0a5d"),
+    ("tc_causal", "causal8k"): (303.83e6, "23a98b06ba6794c3"),
+    ("tc_output", "nc4096"): (103.58e6, "0999d582224720a0"),
+    ("tc_state", "causal8k"): (68.87e6, "dd7629c5daf0e3da"),
 }
 KERNEL_SECTIONS = {
     "tc_causal": ("// tc_causal: the chunked causal scan, warp-specialised.", "// tc_output: non-causal rows"),
