@@ -437,9 +437,7 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                 tmem_ld32(tm_addr(tmem, q, pcol + 32 * j), pv);
                 tmem_ld_wait();
                 const float nkr = nk[(c % 3) * 128 + row];
-                float mx = -INFINITY;
-#pragma unroll
-                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, pv[i]);
+                const float mx = max_of(pv);
                 // a key whose largest feature would pass e^(shift + slack) at the
                 // current reference (always so before the first key) moves the
                 // reference to it; the running state is rescaled to match
@@ -1007,9 +1005,7 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
         const float nkr = nk[row];
         float mf = 0.f, moved = 1.f;   // moved: state rescale when the key reference moves
         if constexpr (MAP == FAVOR_MAP_POSITIVE) {
-            float mx = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < NC; ++i) mx = fmaxf(mx, pv[i]);
+            const float mx = max_of(pv);
             // a key whose largest feature would pass e^(shift + slack) at the
             // current reference (always so before the first key) moves the
             // reference to it; the state so far is rescaled below
@@ -1073,12 +1069,7 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
         }
         tmem_ld_wait();
         float qoff = 0.f;
-        if constexpr (MAP == FAVOR_MAP_POSITIVE) {
-            float mx = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < NC; ++i) mx = fmaxf(mx, pv[i]);
-            part[j * 128 + row] = mx;
-        }
+        if constexpr (MAP == FAVOR_MAP_POSITIVE) part[j * 128 + row] = max_of(pv);
         tc_fence_before();
         group_sync(kEpi);   // every projection column read: phi_Q may now overwrite them
         tc_fence_after();
@@ -1162,8 +1153,12 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
 #pragma unroll
                 for (int i = 0; i < 32; ++i) av[i] = i <= limit ? av[i] : 0.f;
             }
+            {
+                float aa[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) rm = fmaxf(rm, fabsf(av[i]));
+                for (int i = 0; i < 32; ++i) aa[i] = fabsf(av[i]);
+                rm = max_of(aa);
+            }
         }
         part2[j * 128 + row] = rm;
         group_sync(kEpi);
@@ -1413,8 +1408,7 @@ __device__ void output_body(const OutputArgs &a, uint8_t *sm, uint32_t tmem,
                 float t32[32];
                 tmem_ld32(pcol + 32 * b, t32);
                 tmem_ld_wait();
-#pragma unroll
-                for (int k2 = 0; k2 < 32; ++k2) mx = fmaxf(mx, t32[k2]);
+                mx = fmaxf(mx, max_of(t32));
             }
             part[j * 128 + row] = mx;
             group_sync(kEpi);

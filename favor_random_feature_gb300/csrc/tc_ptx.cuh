@@ -370,6 +370,26 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     return r;
 }
 
+// max of three (one instruction on sm_100 and later)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// max of N values (N even), two running maxima for instruction-level parallelism
+template <int N>
+__device__ __forceinline__ float max_of(const float (&v)[N]) {
+    static_assert(N % 4 == 0, "");
+    float m0 = fmaxf(v[0], v[1]), m1 = fmaxf(v[2], v[3]);
+#pragma unroll
+    for (int i = 4; i < N; i += 4) {
+        m0 = fmax3(m0, v[i], v[i + 1]);
+        m1 = fmax3(m1, v[i + 2], v[i + 3]);
+    }
+    return fmaxf(m0, m1);
+}
+
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
