@@ -326,3 +326,46 @@ def test_block_orthogonal_omega():
     # iid draws are N(0,1) entries
     iid = omega_iid(rng, 4, 64, d).ravel()
     assert stats.kstest(iid, "norm").pvalue > 1e-3
+
+
+# ---------------------------------------------------------------------------
+# C5 (i): a positive factor per query row and one per head on the keys leave
+# the output unchanged (what the GPU stabilisers rely on).  Brute force with
+# the query norm term and 1/m dropped and the keys scaled by 7.3 must equal
+# the oracle.
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("causal", [False, True])
+def test_row_and_head_scaling_invariance(causal):
+    rs = np.random.default_rng(11)
+    L, d, m = 40, 16, 64
+    q = rs.standard_normal((L, d)) * 0.4
+    k = rs.standard_normal((L, d)) * 0.4
+    v = rs.standard_normal((L, 8))
+    om = omega_iid(np.random.default_rng(12), 1, m, d)[0]
+    fq = np.exp(q @ om.T)                                   # no -|q|^2/2, no 1/sqrt(m)
+    fk = 7.3 * np.exp(k @ om.T - 0.5 * np.sum(k * k, axis=1, keepdims=True))
+    want = brute_attention(fq @ fk.T, v, causal)
+    got = oracle.forward(q[None, None], k[None, None], v[None, None], om[None], causal=causal,
+                         feature_map=MAP_POSITIVE)[0, 0]
+    assert np.allclose(got, want, rtol=1e-11, atol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# C5 (v): with positive features every output is a convex combination of the
+# value rows it attends to, so each column lies within their range
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("fmap", [MAP_POSITIVE, MAP_ELU1])
+def test_outputs_within_value_range(causal, fmap):
+    rs = np.random.default_rng(13)
+    L, d = 50, 16
+    m = d if fmap == MAP_ELU1 else 48
+    q = rs.standard_normal((1, 1, L, d)) * 0.5
+    k = rs.standard_normal((1, 1, L, d)) * 0.5
+    v = rs.standard_normal((1, 1, L, 6))
+    om = None if fmap == MAP_ELU1 else omega_iid(np.random.default_rng(14), 1, m, d)
+    out = oracle.forward(q, k, v, om, causal=causal, feature_map=fmap)[0, 0]
+    vv = v[0, 0]
+    for i in range(L):
+        seen = vv[: i + 1] if causal else vv
+        assert np.all(out[i] >= seen.min(axis=0) - 1e-12) and np.all(out[i] <= seen.max(axis=0) + 1e-12)
