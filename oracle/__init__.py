@@ -60,6 +60,10 @@ def _load():
             ctypes.POINTER(ctypes.c_int), ctypes.c_int]
         lib.oracle_forward.restype = ctypes.c_int
         lib.oracle_feature_dim.argtypes = [ctypes.c_int] * 3
+        lib.oracle_state.argtypes = [P] * 5 + [ctypes.c_int] * 7
+        lib.oracle_state.restype = ctypes.c_int
+        lib.oracle_decode_step.argtypes = [P] * 7 + [ctypes.c_int] * 6
+        lib.oracle_decode_step.restype = ctypes.c_int
         lib.oracle_feature_dim.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -125,6 +129,59 @@ def forward(q, k, v, omega, causal: bool, feature_map: int = MAP_POSITIVE,
     if rc:
         raise FloatingPointError(f"oracle_forward failed ({rc})")
     return (out, den) if return_den else out
+
+
+def _omega_arg(omega, feature_map, H, d):
+    if feature_map == MAP_ELU1:
+        return None, d
+    om = np.ascontiguousarray(omega, dtype=np.float64)
+    assert om.shape[0] == H and om.shape[2] == d
+    return om, om.shape[1]
+
+
+def state(k, v, omega, feature_map: int = MAP_POSITIVE):
+    """Carried state after all L keys of each head (float64):
+    S [B][H][r][dv] = sum_j phi(k_j) v_j^T and z [B][H][r] = sum_j phi(k_j).
+    k: [B][H][L][d]; v: [B][H][L][dv]; omega: [H][m][d] (None for elu1)."""
+    lib = _load()
+    k = np.ascontiguousarray(k, dtype=np.float64)
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    B, H, L, d = k.shape
+    dv = v.shape[-1]
+    assert v.shape[:3] == k.shape[:3]
+    om, m = _omega_arg(omega, feature_map, H, d)
+    r = lib.oracle_feature_dim(feature_map, d, m)
+    S = np.empty((B, H, r, dv), dtype=np.float64)
+    z = np.empty((B, H, r), dtype=np.float64)
+    rc = lib.oracle_state(_dp(k), _dp(v), _dp(om), _dp(S), _dp(z), B, H, L, d, dv, m, feature_map)
+    if rc:
+        raise FloatingPointError(f"oracle_state failed ({rc})")
+    return S, z
+
+
+def decode_step(q, k, v, omega, S, z, feature_map: int = MAP_POSITIVE):
+    """One decode step for every head: returns (out [B][H][dv], S', z') with
+    S' = S + phi(k) v^T, z' = z + phi(k), out = phi(q)^T S' / phi(q)^T z'.
+    q, k: [B][H][d]; v: [B][H][dv]; S, z as returned by ``state`` (not
+    modified)."""
+    lib = _load()
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    k = np.ascontiguousarray(k, dtype=np.float64)
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    B, H, d = q.shape
+    dv = v.shape[-1]
+    assert k.shape == q.shape and v.shape[:2] == q.shape[:2]
+    om, m = _omega_arg(omega, feature_map, H, d)
+    S2 = np.array(S, dtype=np.float64, order="C", copy=True)
+    z2 = np.array(z, dtype=np.float64, order="C", copy=True)
+    r = lib.oracle_feature_dim(feature_map, d, m)
+    assert S2.shape == (B, H, r, dv) and z2.shape == (B, H, r)
+    out = np.empty((B, H, dv), dtype=np.float64)
+    rc = lib.oracle_decode_step(_dp(q), _dp(k), _dp(v), _dp(om), _dp(S2), _dp(z2), _dp(out),
+                                B, H, d, dv, m, feature_map)
+    if rc:
+        raise FloatingPointError(f"oracle_decode_step failed ({rc})")
+    return out, S2, z2
 
 
 def threads_used() -> int:

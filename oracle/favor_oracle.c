@@ -26,6 +26,12 @@
  *      out_i = phi(q_i)^T S_i / phi(q_i)^T z_i   (diagonal j = i included)
  *          -- Performer study notes, "Case 2: the causal version" (prefix sum),
  *             with the denominator of "Core points" step 5.
+ *  - carried state and one decode step (the same recurrence, one token at
+ *    a time): state(K, V) = (S_L, z_L) after L keys; a step takes (S, z) and
+ *    one (q, k, v), forms S + phi(k) v^T, z + phi(k), and returns them with
+ *    out = phi(q)^T S' / phi(q)^T z'
+ *          -- Performer study notes, "Case 2" (S_i, z_i are running sums;
+ *             each step costs O(r d)).
  *
  * No stabiliser, no blocking, no reordering: every value is the definition
  * evaluated in float64.  Exponents are checked against |t| < 700.
@@ -172,4 +178,73 @@ int oracle_forward(const double *q, const double *k, const double *v,
         }
     }
     return status;
+}
+
+/* Carried state after the L keys of every head: S[B][H][r][dv] = sum_j
+ * phi(k_j) v_j^T, z[B][H][r] = sum_j phi(k_j) (Performer study notes,
+ * "Case 2": the prefix sums at i = L).  Returns 0 or the first head status. */
+int oracle_state(const double *k, const double *v, const double *omega, double *S, double *z,
+                 int B, int H, int L, int d, int dv, int m, int map)
+{
+    int r = oracle_feature_dim(map, d, m);
+    int status = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int bh = 0; bh < B * H; ++bh) {
+        const double *om = omega ? omega + (size_t)(bh % H) * m * d : NULL;
+        double *Sh = S + (size_t)bh * r * dv, *zh = z + (size_t)bh * r;
+        double *phik = (double *)malloc(sizeof(double) * (size_t)r);
+        int rc = phik ? 0 : -3;
+        for (size_t i = 0; i < (size_t)r * dv; ++i) Sh[i] = 0.0;
+        for (int f = 0; f < r; ++f) zh[f] = 0.0;
+        for (int j = 0; j < L && !rc; ++j) {
+            rc = oracle_features(k + ((size_t)bh * L + j) * d, om, 1, d, m, map, phik);
+            if (rc) break;
+            const double *vj = v + ((size_t)bh * L + j) * dv;
+            for (int f = 0; f < r; ++f) {
+                for (int c = 0; c < dv; ++c) Sh[(size_t)f * dv + c] += phik[f] * vj[c];
+                zh[f] += phik[f];
+            }
+        }
+        free(phik);
+        if (rc) {
+#pragma omp critical
+            { if (!status) status = rc; }
+        }
+    }
+    return status;
+}
+
+/* One decode step for every head, in place: S += phi(k) v^T, z += phi(k),
+ * then out = phi(q)^T S / phi(q)^T z with the updated state (the diagonal
+ * term included, as in the causal recurrence).  q, k [B][H][d], v, out
+ * [B][H][dv], S [B][H][r][dv], z [B][H][r]. */
+int oracle_decode_step(const double *q, const double *k, const double *v, const double *omega,
+                       double *S, double *z, double *out, int B, int H, int d, int dv, int m, int map)
+{
+    int r = oracle_feature_dim(map, d, m);
+    double *phik = (double *)malloc(sizeof(double) * (size_t)r);
+    double *phiq = (double *)malloc(sizeof(double) * (size_t)r);
+    int rc = (phik && phiq) ? 0 : -3;
+    for (int bh = 0; bh < B * H && !rc; ++bh) {
+        const double *om = omega ? omega + (size_t)(bh % H) * m * d : NULL;
+        double *Sh = S + (size_t)bh * r * dv, *zh = z + (size_t)bh * r;
+        const double *vh = v + (size_t)bh * dv;
+        double *oh = out + (size_t)bh * dv;
+        rc = oracle_features(k + (size_t)bh * d, om, 1, d, m, map, phik);
+        if (!rc) rc = oracle_features(q + (size_t)bh * d, om, 1, d, m, map, phiq);
+        if (rc) break;
+        for (int f = 0; f < r; ++f) {
+            for (int c = 0; c < dv; ++c) Sh[(size_t)f * dv + c] += phik[f] * vh[c];
+            zh[f] += phik[f];
+        }
+        double den = 0.0;
+        for (int f = 0; f < r; ++f) den += phiq[f] * zh[f];
+        for (int c = 0; c < dv; ++c) {
+            double num = 0.0;
+            for (int f = 0; f < r; ++f) num += phiq[f] * Sh[(size_t)f * dv + c];
+            oh[c] = num / den;
+        }
+    }
+    free(phik); free(phiq);
+    return rc;
 }

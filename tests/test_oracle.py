@@ -369,3 +369,84 @@ def test_outputs_within_value_range(causal, fmap):
     for i in range(L):
         seen = vv[: i + 1] if causal else vv
         assert np.all(out[i] >= seen.min(axis=0) - 1e-12) and np.all(out[i] <= seen.max(axis=0) + 1e-12)
+
+
+# ---------------------------------------------------------------------------
+# carried state and the one-token decode step (study notes, "Case 2": the
+# running sums S_i, z_i)
+# ---------------------------------------------------------------------------
+def _features_numpy(x, om, fmap):
+    """Closed-form features written out in numpy: positive exp(w.x - |x|^2/2)/sqrt(m),
+    trig (sin, cos) pairs interleaved per projection over sqrt(m), elu1 elementwise."""
+    if fmap == MAP_ELU1:
+        return np.where(x > 0, x + 1.0, np.exp(np.minimum(x, 0.0)))
+    m = om.shape[0]
+    p = x @ om.T
+    if fmap == MAP_POSITIVE:
+        return np.exp(p - 0.5 * np.sum(x * x, axis=1, keepdims=True)) / math.sqrt(m)
+    out = np.empty((x.shape[0], 2 * m))
+    out[:, 0::2], out[:, 1::2] = np.sin(p), np.cos(p)
+    return out / math.sqrt(m)
+
+
+def _kernel_matrix(q, k, om, fmap):
+    """A_ij = phi(q_i).phi(k_j) by the single-sum closed forms (positive, trig)
+    or the elementwise product (elu1) -- no feature vectors formed."""
+    if fmap == MAP_POSITIVE:
+        return np.array([[kernel_positive_closed(a, b, om) for b in k] for a in q])
+    if fmap == MAP_TRIG:
+        return np.array([[kernel_trig_closed(a, b, om) for b in k] for a in q])
+    e = lambda x: np.where(x > 0, x + 1.0, np.exp(np.minimum(x, 0.0)))
+    return e(q) @ e(k).T
+
+
+def _small_head(seed, L, d, dv, m, fmap, scale=0.4):
+    rs = np.random.default_rng(seed)
+    q = rs.standard_normal((1, 2, L, d)) * scale
+    k = rs.standard_normal((1, 2, L, d)) * scale
+    v = rs.standard_normal((1, 2, L, dv))
+    om = None if fmap == MAP_ELU1 else omega_iid(np.random.default_rng(seed + 1), 2, m, d)
+    return q, k, v, om
+
+
+@pytest.mark.parametrize("fmap", [MAP_POSITIVE, MAP_TRIG, MAP_ELU1])
+def test_state_matches_closed_form_features(fmap):
+    q, k, v, om = _small_head(21, 30, 16, 8, 24, fmap)
+    S, z = oracle.state(k, v, om, feature_map=fmap)
+    for h in range(2):
+        phi = _features_numpy(k[0, h], None if om is None else om[h], fmap)
+        assert np.allclose(S[0, h], phi.T @ v[0, h], rtol=1e-12, atol=1e-14)
+        assert np.allclose(z[0, h], phi.sum(axis=0), rtol=1e-12, atol=1e-14)
+
+
+@pytest.mark.parametrize("fmap", [MAP_POSITIVE, MAP_TRIG, MAP_ELU1])
+def test_decode_steps_from_empty_state_are_brute_causal(fmap):
+    L, d, dv, m = 12, 8, 5, 16
+    q, k, v, om = _small_head(23, L, d, dv, m, fmap)
+    r = oracle.feature_dim(fmap, d, m)
+    S, z = np.zeros((1, 2, r, dv)), np.zeros((1, 2, r))
+    outs = []
+    for t in range(L):
+        o, S, z = oracle.decode_step(q[:, :, t], k[:, :, t], v[:, :, t], om, S, z, feature_map=fmap)
+        outs.append(o)
+    got = np.stack(outs, axis=2)
+    for h in range(2):
+        A = _kernel_matrix(q[0, h], k[0, h], None if om is None else om[h], fmap)
+        want = brute_attention(A, v[0, h], causal=True)
+        assert np.allclose(got[0, h], want, rtol=1e-9, atol=1e-11)
+
+
+def test_state_is_additive_and_decode_continues_a_prefix():
+    L, a = 40, 27
+    q, k, v, om = _small_head(25, L, 16, 8, 32, MAP_POSITIVE)
+    S, z = oracle.state(k, v, om)
+    S1, z1 = oracle.state(k[:, :, :a], v[:, :, :a], om)
+    S2, z2 = oracle.state(k[:, :, a:], v[:, :, a:], om)
+    assert np.allclose(S1 + S2, S, rtol=1e-12, atol=1e-14) and np.allclose(z1 + z2, z, rtol=1e-12)
+    # decoding tokens a.. from the state of the first a keys gives the causal rows a..
+    full = oracle.forward(q, k, v, om, causal=True)
+    St, zt = S1, z1
+    for t in range(a, L):
+        o, St, zt = oracle.decode_step(q[:, :, t], k[:, :, t], v[:, :, t], om, St, zt)
+        assert np.allclose(o, full[:, :, t], rtol=1e-11, atol=1e-13)
+    assert np.allclose(St, S, rtol=1e-11) and np.allclose(zt, z, rtol=1e-11)
