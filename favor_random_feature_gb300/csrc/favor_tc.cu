@@ -239,57 +239,89 @@ __device__ __forceinline__ float cvt_chunk16_sq(uint8_t *p) {
 }
 
 // ---------------------------------------------------------------------------
-// tc_state: per (feature tile, segment, head) the segment state
+// tc_state: per (feature group, piece, head) the state of a run of keys
 //   S[f][c] = sum_t phi(k_t)_f v_t[c],  z[f] = sum_t phi(k_t)_f
-// at the key reference R, written as fp32 [f][dv + 1] plus (R, max z, max|v|,
-// max|S|) of the tile.
+// at the key reference R, written as fp32 [f][dv + 1] plus (R, max z,
+// max|v|, max|S|) per 128-feature tile.  A CTA covers FT = 1 or 2 feature
+// tiles (all of a head's features where TMEM holds them), so each K and V
+// tile is converted once for all of them.
 // Warp 0 lane 0 issues every TMA copy and MMA; warps 1..16 (the epilogue
 // group) convert tiles and compute features, warp w on TMEM lane quarter
-// w % 4 and feature quarter (w - 1) / 4.  Projections P[2] alternate in TMEM;
-// K, V and phi_K are double-buffered in shared memory, so the projection of
-// chunk c+1 and the state update of chunk c run while the epilogue works on
-// the features of the next chunk.
+// w % 4 and projection quarter (w - 1) / 4.  The epilogue reads the
+// projections of chunk c into registers and hands TMEM back at once, so the
+// tensor core projects chunk c + 1 while the features of c are formed, and
+// the state update of c runs while the epilogue starts on c + 1.
 // ---------------------------------------------------------------------------
 constexpr int kStateThreads = 32 + kEpi;
 
 struct StateArgs {
     Geo g;
-    int H, L, seg_len, nseg, nvs, nks; // V buffers (1 or 2), K buffers (2 or 3)
+    int H, L, FT, piece_len, npieces, nvs, nks; // piece p: tokens [p piece_len, (p+1) piece_len) within L
     const uint8_t *omg;                // MN-major W images
-    float *state;                      // [BH][nseg][r][dv+1]
-    float *meta;                       // [BH][nseg][n_ft][4]: R, max z, max|v|, max|S|
+    float *state;                      // [BH][npieces][r][dv+1]
+    float *meta;                       // [BH][npieces][n_ft][4]: R, max z, max|v|, max|S|
     int *status;
     uint32_t o_w, o_xk, o_xv, o_phk, o_small, xv_stride, tmem_cols;
 };
 
-__global__ void __launch_bounds__(kStateThreads, 1)
-tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-         const StateArgs a) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+// N fp16 values (packed pairs) of one row into 128B-swizzled [128][64]
+// blocks at columns [c0, c0 + N)
+template <int N>
+__device__ __forceinline__ void store_row_packed(uint8_t *blk, int row, int c0, const uint32_t *h) {
+#pragma unroll
+    for (int c = 0; c < N / 8; ++c)
+        *reinterpret_cast<uint4 *>(blk + sw128_offset(row, c0 + 8 * c)) =
+            make_uint4(h[4 * c + 0], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
+}
+
+// NC consecutive TMEM columns of the thread's lane into registers
+template <int NC>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&pv)[NC]) {
+    if constexpr (NC % 32 == 0) {
+#pragma unroll
+        for (int b = 0; b < NC / 32; ++b) {
+            float t[32];
+            tmem_ld32(taddr + 32 * b, t);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) pv[32 * b + i] = t[i];
+        }
+    } else {
+        static_assert(NC == 16, "16, 32 or 64 columns");
+        float t[16];
+        tmem_ld16(taddr, t);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pv[i] = t[i];
+    }
+}
+
+// NC = projection columns per epilogue thread (a quarter of the group's
+// projections), MAP the feature map
+template <int NC, int MAP>
+__device__ __forceinline__ void state_body(const CUtensorMap *tm_k, const CUtensorMap *tm_v, const StateArgs &a,
+                                           uint8_t *sm) {
     const Geo &g = a.g;
-    const int ft = blockIdx.x, seg = blockIdx.y, bh = blockIdx.z, head = bh % a.H;
-    const int t_begin = seg * a.seg_len, t_end = min(a.L, t_begin + a.seg_len);
-    const int nchunk = (t_end - t_begin + kC - 1) / kC;
+    const int FT = a.FT, fg = blockIdx.x, piece = blockIdx.y, bh = blockIdx.z, head = bh % a.H;
+    const int t_begin = piece * a.piece_len, t_end = min(a.L, t_begin + a.piece_len);
+    const int nchunk = max(0, (t_end - t_begin + kC - 1) / kC);
     const int nd = g.d / 64, nvb = g.dv / 64, NSV = a.nvs, NSK = a.nks;
+    const int npg = FT * g.np_tile;                  // projections of the group
     const uint32_t xkb = (uint32_t)kC * g.d * 2;
     uint8_t *w = sm + a.o_w, *xk = sm + a.o_xk, *xv = sm + a.o_xv, *phk = sm + a.o_phk;
     float *small = reinterpret_cast<float *>(sm + a.o_small);
     float *nk = small;              // [3][128] half key norms, by chunk % 3
     float *red = small + 768;       // [32]
     uint64_t *bars = reinterpret_cast<uint64_t *>(small + 800);
-    uint64_t *bar_w = &bars[0], *bar_k = &bars[13] /*[3]*/, *bar_v = &bars[3] /*[2]*/,
-             *bar_pk = &bars[5] /*[2]*/, *bar_s = &bars[7] /*[2]*/, *e_x = &bars[9] /*[2]*/,
-             *e_k = &bars[11] /*[2]*/;
+    uint64_t *bar_w = &bars[0], *bar_pk = &bars[1], *bar_s = &bars[2], *bar_v = &bars[3] /*[2]*/,
+             *bar_k = &bars[5] /*[3]*/, *e_x = &bars[8] /*[2]*/, *e_pk = &bars[10], *e_k = &bars[11];
     uint32_t *tslot = reinterpret_cast<uint32_t *>(small + 834);
     volatile int *abortp = reinterpret_cast<volatile int *>(small + 836);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int col_s = 256;          // state tile: dv values, then 16 copies of z
+    const int col_s = 256;          // state tile t at col_s + t (dv + 16): dv values, then 16 copies of z
+    const int sw = g.dv + 16;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 9; ++i) mbar_init(&bars[i], 1);
-        for (int i = 9; i < 13; ++i) mbar_init(&bars[i], kEpi);
-        for (int i = 13; i < 16; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < 8; ++i) mbar_init(&bars[i], 1);
+        for (int i = 8; i < 12; ++i) mbar_init(&bars[i], kEpi);
         fence_mbar_init();
         *abortp = 0;
     }
@@ -312,42 +344,36 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         if (lane == 0 && nchunk == 0) grid_dep_wait();
         if (lane == 0 && nchunk > 0) {
             const uint32_t w_s = smem_u32(w), xk_s = smem_u32(xk), xv_s = smem_u32(xv), phk_s = smem_u32(phk);
-            const uint32_t wbytes = (uint32_t)g.np_tile * g.d * 2;
-            // K in NSK buffers: K(c + NSK) loads as soon as P_K(c) is done
+            const uint32_t wbytes = (uint32_t)npg * g.d * 2;
             auto load_k = [&](int c) {
                 uint64_t *bar = &bar_k[c % NSK];
                 mbar_arrive_expect_tx(bar, xkb);
                 for (int b = 0; b < nd; ++b)
-                    tma_load_3d(xk + (size_t)(c % NSK) * xkb + b * kBlk, &tm_k, bar, 64 * b, t_begin + c * kC, bh);
+                    tma_load_3d(xk + (size_t)(c % NSK) * xkb + b * kBlk, tm_k, bar, 64 * b, t_begin + c * kC, bh);
             };
             auto load_v = [&](int c) {
                 const int s = c % NSV;
                 mbar_arrive_expect_tx(&bar_v[s], (uint32_t)nvb * kBlk);
                 for (int b = 0; b < nvb; ++b)
-                    tma_load_3d(xv + (size_t)s * a.xv_stride + b * kBlk, &tm_v, &bar_v[s], 64 * b, t_begin + c * kC, bh);
+                    tma_load_3d(xv + (size_t)s * a.xv_stride + b * kBlk, tm_v, &bar_v[s], 64 * b, t_begin + c * kC, bh);
             };
             auto issue_proj = [&](int c) {
-                const uint32_t idesc = idesc_f16(128, g.np_tile, 0, 1);
+                const uint32_t idesc = idesc_f16(128, npg, 0, 1);
                 const uint32_t x_s = xk_s + (uint32_t)(c % NSK) * xkb;
                 for (int kk = 0; kk < g.d / 16; ++kk)
-                    mma_f16(tmem + 128 * (c & 1), smem_desc(x_s + (kk >> 2) * kBlk + (kk & 3) * 32, 16, 1024),
+                    mma_f16(tmem, smem_desc(x_s + (kk >> 2) * kBlk + (kk & 3) * 32, 16, 1024),
                             smem_desc(w_s + kk * 2048, (uint32_t)g.d * 128, 1024), idesc, kk > 0);
-                mma_commit(&bar_pk[c & 1]);
+                mma_commit(bar_pk);
             };
-            load_k(0);
-            load_v(0);
-            if (nchunk > 1) {
-                load_k(1);
-                if (NSV == 2) load_v(1);
-            }
-            if (nchunk > 2 && NSK == 3) load_k(2);
+            for (int c = 0; c < min(NSK, nchunk); ++c) load_k(c);
+            for (int c = 0; c < min(NSV, nchunk); ++c) load_v(c);
             // the W image comes from the kernel before this one
             grid_dep_wait();
             mbar_arrive_expect_tx(bar_w, wbytes);
-            bulk_load(w, a.omg + (size_t)head * g.nproj * g.d * 2 + (size_t)ft * wbytes, wbytes, bar_w);
-            // e_x and e_k alternate between two barriers per chunk parity: the
-            // epilogue may finish converting K(0) and K(1) before this thread
-            // looks, and one barrier would then have moved two phases on
+            bulk_load(w, a.omg + (size_t)head * g.nproj * g.d * 2 + (size_t)fg * wbytes, wbytes, bar_w);
+            // e_x alternates between two barriers by chunk parity: with three K
+            // buffers the epilogue may convert K(c + 2) before this thread
+            // looks at K(c + 1), and one barrier would then have moved on twice
             alive = ewait(bar_w, 0, abortp) && ewait(&e_x[0], 0, abortp);
             if (alive) {
                 tc_fence_after();
@@ -355,31 +381,31 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             }
             for (int c = 0; c < nchunk && alive; ++c) {
                 if (c + 1 < nchunk) {
-                    if (!(alive = ewait(&e_x[(c + 1) & 1], ((c + 1) >> 1) & 1, abortp))) break;
+                    // the epilogue holds P(c) in registers (so P(c) is done and
+                    // K buffer c % NSK is free) and has converted K(c + 1)
+                    if (!(alive = ewait(e_pk, c & 1, abortp) &&
+                                  ewait(&e_x[(c + 1) & 1], ((c + 1) >> 1) & 1, abortp)))
+                        break;
                     tc_fence_after();
                     issue_proj(c + 1);
+                    if (c + NSK < nchunk) load_k(c + NSK);
                 }
-                if (c + NSK < nchunk) {
-                    // K buffer c % NSK is free once P_K(c) is done: refill it
-                    // ahead of its use
-                    if (!(alive = ewait(&bar_pk[c & 1], (c >> 1) & 1, abortp))) break;
-                    load_k(c + NSK);
-                }
-                if (!(alive = ewait(&e_k[c & 1], (c >> 1) & 1, abortp))) break;
+                if (!(alive = ewait(e_k, c & 1, abortp))) break;
                 tc_fence_after();
                 {
-                    const uint32_t idesc = idesc_f16(128, g.dv + 16, 1, 1);
-                    const uint32_t a_s = phk_s + (uint32_t)(c & 1) * 2 * kBlk;
+                    const uint32_t idesc = idesc_f16(128, sw, 1, 1);
                     const uint32_t b_s = xv_s + (uint32_t)(c % NSV) * a.xv_stride;
-                    for (int kk = 0; kk < kC / 16; ++kk)
-                        mma_f16(tmem + col_s, smem_desc(a_s + kk * 2048, kBlk, 1024),
-                                smem_desc(b_s + kk * 2048, kBlk, 1024), idesc, 1);
-                    mma_commit(&bar_s[c & 1]);
+                    for (int t = 0; t < FT; ++t) {
+                        const uint32_t a_s = phk_s + (uint32_t)t * 2 * kBlk;
+                        for (int kk = 0; kk < kC / 16; ++kk)
+                            mma_f16(tmem + col_s + t * sw, smem_desc(a_s + kk * 2048, kBlk, 1024),
+                                    smem_desc(b_s + kk * 2048, kBlk, 1024), idesc, 1);
+                    }
+                    mma_commit(bar_s);
                 }
-                const int nextv = c + NSV;
-                if (nextv < nchunk) {
-                    if (!(alive = ewait(&bar_s[c & 1], (c >> 1) & 1, abortp))) break;
-                    load_v(nextv);
+                if (c + NSV < nchunk) {
+                    if (!(alive = ewait(bar_s, c & 1, abortp))) break;
+                    load_v(c + NSV);
                 }
             }
             if (!alive) set_status(a.status, FAVOR_ERR_TIMEOUT);
@@ -388,20 +414,23 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         const int e = threadIdx.x - 32, ew = e >> 5;
         const int q = (ew + 1) & 3, j = ew >> 2;
         const int row = q * 32 + lane;
-        float R = g.map == FAVOR_MAP_POSITIVE ? -INFINITY : 0.f;
+        float R = MAP == FAVOR_MAP_POSITIVE ? -INFINITY : 0.f;
         float vmax = 0.f;
         // zero state and z
         {
             uint32_t zero[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) zero[i] = 0u;
-            for (int cc = 16 * j; cc < g.dv + 16; cc += 64) tmem_st16(tm_addr(tmem, q, col_s + cc), zero);
+            for (int t = 0; t < FT; ++t)
+                for (int cc = 16 * j; cc < sw; cc += 64) tmem_st16(tm_addr(tmem, q, col_s + t * sw + cc), zero);
             tmem_st_wait();
         }
         // K(c) -> fp16 and the half key norms: thread e takes row e / 4, chunks
         // 2 (e % 4) and 2 (e % 4) + 1 of each 64-column block, the row's four
         // threads being neighbouring lanes.  The norms of chunk c go to buffer
-        // c % 3, last read two chunks (and two group barriers) earlier.
+        // c % 3, written at the start of iteration c - 1 and read in iteration
+        // c, with the vote's group barrier between (only the positive map
+        // reads them).
         auto convert_k = [&](int c) -> bool {
             bool ok = ewait(&bar_k[c % NSK], (c / NSK) & 1, abortp);
             uint8_t *tile = xk + (size_t)(c % NSK) * xkb;
@@ -419,29 +448,42 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             return ok;
         };
         if (nchunk > 0) alive = convert_k(0);
+        group_sync(kEpi);   // norms of chunk 0 visible
         for (int c = 0; c < nchunk; ++c) {
             const int tc0 = t_begin + c * kC;
             const int valid = min(kC, t_end - tc0);
             const bool ok = row < valid;
+            // K(c + 1) first: the tensor core is still on P(c)
             if (c + 1 < nchunk) alive &= convert_k(c + 1);
-            // P_K(c) ready; phi_K buffer c % 2 free once the state update of c - 2 is done
-            alive &= ewait(&bar_pk[c & 1], (c >> 1) & 1, abortp);
-            if (c >= 2) alive &= ewait(&bar_s[c & 1], ((c - 2) >> 1) & 1, abortp);
+            // P(c) -> registers (for the positive map after a first pass that
+            // only takes the row maximum, so that the vote below holds no
+            // projections); TMEM then goes back to the tensor core for P(c + 1)
+            float pv[NC];
+            alive &= ewait(bar_pk, c & 1, abortp);
             tc_fence_after();
-            group_sync(kEpi);   // norms of this chunk visible
-            uint8_t *phb = phk + (size_t)(c & 1) * 2 * kBlk;
-            const int pcol = 128 * (c & 1);
-            if (g.map == FAVOR_MAP_POSITIVE) {
-                // feature columns 32 j .. 32 j + 31 of the tile
-                float pv[32];
-                tmem_ld32(tm_addr(tmem, q, pcol + 32 * j), pv);
+            auto take_p = [&]() {
+                tmem_ld_cols<NC>(tm_addr(tmem, q, NC * j), pv);
                 tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(e_pk);
+            };
+            float mx = -INFINITY;
+            if (MAP == FAVOR_MAP_POSITIVE) {
+                tmem_ld_cols<NC>(tm_addr(tmem, q, NC * j), pv);
+                tmem_ld_wait();
+                mx = max_of<NC>(pv);
+            } else {
+                take_p();
+            }
+            // features of chunk c, packed fp16 pairs
+            constexpr int NH = MAP == FAVOR_MAP_TRIG ? NC : NC / 2;
+            uint32_t hp[NH];
+            float alpha = 1.f;
+            if (MAP == FAVOR_MAP_POSITIVE) {
                 const float nkr = nk[(c % 3) * 128 + row];
-                const float mx = max_of(pv);
                 // a key whose largest feature would pass e^(shift + slack) at the
                 // current reference (always so before the first key) moves the
                 // reference to it; the running state is rescaled to match
-                float alpha = 1.f;
                 if (group_or(ok && mx - nkr - R > kLog2MaxFeature, kEpi)) {
                     const float Rn = grp_max(ok ? mx - nkr : -INFINITY, red, ew) - kShift;
                     if (R != -INFINITY) alpha = ex2(R - Rn);
@@ -449,58 +491,59 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
                 }
                 // rows past the end take an infinite offset: their features are 0
                 const float off = ok ? nkr + R : INFINITY;
-                {
-                    float v[32];
+                take_p();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = ex2(pv[i] - off);
-                    store_row32(phb + (size_t)(j >> 1) * kBlk, row, 32 * (j & 1), v);
+                for (int i = 0; i < NC / 2; ++i) hp[i] = pack_half2(ex2(pv[2 * i] - off), ex2(pv[2 * i + 1] - off));
+            } else if (MAP == FAVOR_MAP_TRIG) {
+                // NC projections: sines in hp[0, NC/2), cosines in hp[NC/2, NC)
+#pragma unroll
+                for (int i = 0; i < NC / 2; ++i) {
+                    float s0, c0, s1, c1;
+                    sincos_reduced(pv[2 * i], s0, c0);
+                    sincos_reduced(pv[2 * i + 1], s1, c1);
+                    if (!ok) s0 = c0 = s1 = c1 = 0.f;
+                    hp[i] = pack_half2(s0, s1);
+                    hp[NC / 2 + i] = pack_half2(c0, c1);
                 }
-                if (alpha != 1.f) {
-                    // the running state moves to the new reference (once the
-                    // previous chunk's update is in it)
-                    if (c >= 1) alive &= ewait(&bar_s[(c - 1) & 1], ((c - 1) >> 1) & 1, abortp);
-                    tc_fence_after();
-                    for (int cc = 16 * j; cc < g.dv + 16; cc += 64) {
+            } else {
+#pragma unroll
+                for (int i = 0; i < NC / 2; ++i)
+                    hp[i] = ok ? pack_half2(elu1(pv[2 * i]), elu1(pv[2 * i + 1])) : 0u;
+            }
+            // phi_K and the state are free once the update of chunk c - 1 is done
+            if (c >= 1) alive &= ewait(bar_s, (c - 1) & 1, abortp);
+            tc_fence_after();
+            // the running state moves to the new reference
+            if (MAP == FAVOR_MAP_POSITIVE && alpha != 1.f) {
+                for (int t = 0; t < FT; ++t)
+                    for (int cc = 16 * j; cc < sw; cc += 64) {
                         float v[16];
-                        tmem_ld16(tm_addr(tmem, q, col_s + cc), v);
+                        tmem_ld16(tm_addr(tmem, q, col_s + t * sw + cc), v);
                         tmem_ld_wait();
                         uint32_t u[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(v[i] * alpha);
-                        tmem_st16(tm_addr(tmem, q, col_s + cc), u);
+                        tmem_st16(tm_addr(tmem, q, col_s + t * sw + cc), u);
                     }
-                    tmem_st_wait();
-                }
-            } else if (g.map == FAVOR_MAP_TRIG) {
-                // 64 projections per tile: thread j takes 16 of them; the tile
-                // holds their sin in columns 0..63 and cos in 64..127
-                float v[16], s[16], co[16];
-                tmem_ld16(tm_addr(tmem, q, pcol + 16 * j), v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    if (ok) sincos_reduced(v[i], s[i], co[i]);
-                    else s[i] = co[i] = 0.f;
-                }
-#pragma unroll
-                for (int c8 = 0; c8 < 2; ++c8) {
-                    uint4 us = make_uint4(pack_half2(s[8 * c8 + 0], s[8 * c8 + 1]), pack_half2(s[8 * c8 + 2], s[8 * c8 + 3]),
-                                          pack_half2(s[8 * c8 + 4], s[8 * c8 + 5]), pack_half2(s[8 * c8 + 6], s[8 * c8 + 7]));
-                    uint4 uc = make_uint4(pack_half2(co[8 * c8 + 0], co[8 * c8 + 1]), pack_half2(co[8 * c8 + 2], co[8 * c8 + 3]),
-                                          pack_half2(co[8 * c8 + 4], co[8 * c8 + 5]), pack_half2(co[8 * c8 + 6], co[8 * c8 + 7]));
-                    *reinterpret_cast<uint4 *>(phb + sw128_offset(row, 16 * j + 8 * c8)) = us;
-                    *reinterpret_cast<uint4 *>(phb + kBlk + sw128_offset(row, 16 * j + 8 * c8)) = uc;
-                }
+                tmem_st_wait();
+            }
+            if (MAP == FAVOR_MAP_TRIG) {
+                // projection p of the group: tile p / 64, sine in block 2 (p / 64),
+                // cosine in block 2 (p / 64) + 1, column p % 64
+                const int p0 = NC * j;
+                uint8_t *blk = phk + (size_t)(2 * (p0 / 64)) * kBlk;
+                store_row_packed<NC>(blk, row, p0 % 64, hp);
+                store_row_packed<NC>(blk + kBlk, row, p0 % 64, hp + NC / 2);
             } else {
-                float v[32];
-                tmem_ld32(tm_addr(tmem, q, pcol + 32 * j), v);
-                tmem_ld_wait();
+                // feature f of the group in block f / 64, column f % 64
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = ok ? elu1(v[i]) : 0.f;
-                store_row32(phb + (size_t)(j >> 1) * kBlk, row, 32 * (j & 1), v);
+                for (int g32 = 0; g32 < NC / 32; ++g32) {
+                    const int f0 = NC * j + 32 * g32;
+                    store_row_packed<32>(phk + (size_t)(f0 / 64) * kBlk, row, f0 % 64, hp + 16 * g32);
+                }
             }
             // V(c) -> fp16
-            alive &= ewait(&bar_v[c % NSV], NSV == 2 ? ((c >> 1) & 1) : (c & 1), abortp);
+            alive &= ewait(&bar_v[c % NSV], (c / NSV) & 1, abortp);
             {
                 float am;
                 convert_tile_512<false, true>(xv + (size_t)(c % NSV) * a.xv_stride, nvb, e, am);
@@ -508,46 +551,46 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
             }
             fence_async_smem();
             tc_fence_before();
-            mbar_arrive(&e_k[c & 1]);
+            mbar_arrive(e_k);
         }
-        // the last state update, then S, z -> global with the tile's max |S| and max z
-        if (nchunk > 0) alive &= ewait(&bar_s[(nchunk - 1) & 1], ((nchunk - 1) >> 1) & 1, abortp);
+        // the last state update, then S, z -> global with each tile's max |S| and max z
+        if (nchunk > 0) alive &= ewait(bar_s, (nchunk - 1) & 1, abortp);
         tc_fence_after();
-        const int f = ft * 128 + row;
-        float *dst = a.state + (((size_t)bh * a.nseg + seg) * g.r + f) * (g.dv + 1);
         const bool write = alive && !*abortp;
-        float smax = 0.f, zval = 0.f;
-        for (int cc = 16 * j; cc < g.dv; cc += 64) {
-            float v[16];
-            tmem_ld16(tm_addr(tmem, q, col_s + cc), v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                smax = fmaxf(smax, fabsf(v[i]));
-                if (write) dst[cc + i] = v[i];
-            }
-        }
-        if (j == 0) {
-            float v[16];
-            tmem_ld16(tm_addr(tmem, q, col_s + g.dv), v);
-            tmem_ld_wait();
-            zval = fabsf(v[0]);
-            if (write) dst[g.dv] = v[0];
-        }
         const float vm = grp_max(vmax, red, ew);
-        const float sm_all = grp_max(smax, red, ew);
-        const float zm = grp_max(zval, red, ew);
-        if (write) {
-            if (e == 0) {
-                float *m = a.meta + (((size_t)bh * a.nseg + seg) * g.n_ft + ft) * 4;
+        for (int t = 0; t < FT; ++t) {
+            const int ft = fg * FT + t;
+            const int f = ft * 128 + row;
+            float *dst = a.state + (((size_t)bh * a.npieces + piece) * g.r + f) * (g.dv + 1);
+            float smax = 0.f, zval = 0.f;
+            for (int cc = 16 * j; cc < g.dv; cc += 64) {
+                float v[16];
+                tmem_ld16(tm_addr(tmem, q, col_s + t * sw + cc), v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    smax = fmaxf(smax, fabsf(v[i]));
+                    if (write) dst[cc + i] = v[i];
+                }
+            }
+            if (j == 0) {
+                float v[16];
+                tmem_ld16(tm_addr(tmem, q, col_s + t * sw + g.dv), v);
+                tmem_ld_wait();
+                zval = fabsf(v[0]);
+                if (write) dst[g.dv] = v[0];
+            }
+            const float sm_all = grp_max(smax, red, ew);
+            const float zm = grp_max(zval, red, ew);
+            if (write && e == 0) {
+                float *m = a.meta + (((size_t)bh * a.npieces + piece) * g.n_ft + ft) * 4;
                 m[0] = R;
                 m[1] = zm;
                 m[2] = vm;
                 m[3] = sm_all;
             }
-        } else {
-            set_status(a.status, FAVOR_ERR_TIMEOUT);
         }
+        if (!write) set_status(a.status, FAVOR_ERR_TIMEOUT);
     }
     tc_fence_before();
     __syncthreads();
@@ -555,9 +598,26 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     if (warp == 0) tmem_dealloc(tmem, a.tmem_cols);
 }
 
+__global__ void __launch_bounds__(kStateThreads, 1)
+tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+         const StateArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int nc = a.FT * a.g.np_tile / 4;
+    if (a.g.map == FAVOR_MAP_POSITIVE) {
+        if (nc == 64) state_body<64, FAVOR_MAP_POSITIVE>(&tm_k, &tm_v, a, sm);
+        else state_body<32, FAVOR_MAP_POSITIVE>(&tm_k, &tm_v, a, sm);
+    } else if (a.g.map == FAVOR_MAP_TRIG) {
+        if (nc == 32) state_body<32, FAVOR_MAP_TRIG>(&tm_k, &tm_v, a, sm);
+        else state_body<16, FAVOR_MAP_TRIG>(&tm_k, &tm_v, a, sm);
+    } else {
+        state_body<32, FAVOR_MAP_ELU1>(&tm_k, &tm_v, a, sm);
+    }
+}
+
 // ---------------------------------------------------------------------------
-// tc_combine: fixed-order combination of segment states, rescaled to one key
-// reference R* (the largest of the segments'), grid (heads, outputs, slices):
+// tc_combine: fixed-order combination of piece states, rescaled to one key
+// reference R* (the largest of the pieces'), grid (heads, outputs, slices):
 //  non-causal: KV = sum_g S_g 2^(R_g - R*), z likewise; sigma is a power of
 //    two with sigma * (bound on max |KV| and max z) <= 16384; writes the fp16
 //    operand image of [sigma KV | sigma z]: nvb atoms [r][64] of KV and one
@@ -568,13 +628,15 @@ tc_state(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
 // ---------------------------------------------------------------------------
 struct CombineArgs {
     Geo g;
-    int nseg;              // segment states available
+    int nseg;              // piece states available
+    int pps;               // causal: pieces per scan segment
     int causal;
     int slice;             // elements per block
     const float *state, *meta;
     uint8_t *sop;          // non-causal: [BH][nvb + 1][r][64] fp16 image
-    float *s_in;           // causal: [BH][nseg+1][r][dv+1]
-    float *meta_in;        // causal: [BH][nseg+1][4]
+    float *s_in;           // causal: [BH][nout][r][dv+1]
+    float *meta_in;        // causal: [BH][nout][4]
+    int nout;              // causal: scan segments
 };
 
 __global__ void tc_combine(const CombineArgs a) {
@@ -582,12 +644,19 @@ __global__ void tc_combine(const CombineArgs a) {
     grid_dep_wait();
     const Geo &g = a.g;
     const int bh = blockIdx.x;
-    const int upto = a.causal ? blockIdx.y + 1 : a.nseg;   // segments [0, upto)
+    const int upto = a.causal ? (blockIdx.y + 1) * a.pps : a.nseg;   // pieces [0, upto)
     constexpr int kMaxScale = 256;
     __shared__ float scale[kMaxScale];
     __shared__ float sh[4];   // R*, z bound, |S| bound, vmax
-    const float *meta = a.meta + (size_t)bh * a.nseg * g.n_ft * 4;
+    __shared__ float msh[kMaxScale * 4];
     const int nsc = upto * g.n_ft;
+    {
+        // the segment tiles' (R, max z, max|v|, max|S|), loaded by all threads at once
+        const float *mg = a.meta + (size_t)bh * a.nseg * g.n_ft * 4;
+        for (int i = threadIdx.x; i < min(nsc, kMaxScale) * 4; i += blockDim.x) msh[i] = mg[i];
+        __syncthreads();
+    }
+    const float *meta = msh;
     if (threadIdx.x == 0) {
         float R = -INFINITY, vmax = 0.f;
         for (int i = 0; i < nsc; ++i) {
@@ -619,7 +688,7 @@ __global__ void tc_combine(const CombineArgs a) {
     const float *st = a.state + (size_t)bh * a.nseg * per;
     const size_t e0 = (size_t)blockIdx.z * a.slice, e1 = min(per, e0 + a.slice);
     if (a.causal) {
-        float *dst = a.s_in + ((size_t)bh * (a.nseg + 1) + upto) * per;
+        float *dst = a.s_in + ((size_t)bh * a.nout + blockIdx.y + 1) * per;
         for (size_t e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
             const int ftile = (int)(e / W) / 128;
             float sum = 0.f;
@@ -627,7 +696,7 @@ __global__ void tc_combine(const CombineArgs a) {
             dst[e] = sum;
         }
         if (blockIdx.z == 0 && threadIdx.x == 0) {
-            float *m = a.meta_in + ((size_t)bh * (a.nseg + 1) + upto) * 4;
+            float *m = a.meta_in + ((size_t)bh * a.nout + blockIdx.y + 1) * 4;
             m[0] = sh[0];
             m[1] = sh[1];
             m[2] = sh[3];
@@ -688,8 +757,8 @@ struct CausalArgs {
     int H, L, seg_len, nseg;
     const uint8_t *omg;            // MN-major W images
     const float *s_in, *meta_in;   // [BH][nseg][r][dv+1], [BH][nseg][4] (segment 0 unused)
-    const float *state, *meta;     // segment states [BH][nstate][r][dv+1], [BH][nstate][n_ft][4]
-    int nstate, direct;            // direct: combine the earlier segments' states here
+    const float *state, *meta;     // piece states [BH][nstate][r][dv+1], [BH][nstate][n_ft][4]
+    int nstate, pps, direct;       // pps pieces per segment; direct: combine the earlier pieces here
     int *status;
     uint32_t o_w, o_x, o_v, o_kb, o_small, tmem_cols;
 };
@@ -910,11 +979,13 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
     if (nchunk > 0) alive = convert_x(0);
     grid_dep_wait();
     if (seg > 0 && a.direct) {
-        // the state after segments 0 .. seg-1, combined here at the largest of
-        // their key references (few segments: no separate combine pass)
+        // the state after segments 0 .. seg-1 (pieces 0 .. seg pps - 1),
+        // combined here at the largest of their key references (few segments:
+        // no separate combine pass)
+        const int npin = seg * a.pps;
         const float *meta = a.meta + (size_t)bh * a.nstate * nft * 4;   // [g][tile][R, max z, max|v|, max|S|]
         float Rs = -INFINITY;
-        for (int gi = 0; gi < seg; ++gi)
+        for (int gi = 0; gi < npin; ++gi)
             for (int t = 0; t < nft; ++t) {
                 Rs = fmaxf(Rs, meta[(gi * nft + t) * 4]);
                 vmax = fmaxf(vmax, meta[(gi * nft + t) * 4 + 2]);
@@ -924,14 +995,14 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
             const float Rg = meta[(gi * nft + t) * 4];
             return (Rg == -INFINITY || Rs == -INFINITY) ? 0.f : ex2(Rg - Rs);
         };
-        for (int gi = 0; gi < seg; ++gi) {
+        for (int gi = 0; gi < npin; ++gi) {
             float zt = 0.f;
             for (int t = 0; t < nft; ++t) zt = fmaxf(zt, meta[(gi * nft + t) * 4 + 1] * scale(gi, t));
             zmax += zt;
         }
         if (MAP == FAVOR_MAP_POSITIVE) R = Rs;
         const size_t per = (size_t)g.r * (g.dv + 1);
-        for (int gi = 0; gi < seg; ++gi) {
+        for (int gi = 0; gi < npin; ++gi) {
             const float *st = a.state + ((size_t)bh * a.nstate + gi) * per;
             const float sc0 = scale(gi, 0), sc1 = nft == 2 ? scale(gi, 1) : 0.f;
             const float *r0 = st + (size_t)row * (g.dv + 1), *r1 = st + (size_t)(128 + row) * (g.dv + 1);
@@ -1566,24 +1637,29 @@ CausalLayout causal_layout(const Geo &g) {
 
 struct StateLayout {
     uint32_t o_w, o_xk, o_xv, o_phk, o_small, xv_stride, bytes;
-    int nvs, nks;
+    int nvs, nks, FT;
 };
+// Feature tiles per CTA: two where TMEM holds their two state tiles beside
+// the projections; then the most buffering that fits, three K and two V
+// buffers first.
 StateLayout state_layout(const Geo &g) {
-    StateLayout l;
-    // most buffering that fits: three K and two V buffers first
+    StateLayout l{};
     const int opts[4][2] = {{3, 2}, {2, 2}, {3, 1}, {2, 1}};
-    for (const auto &op : opts) {
-        uint32_t o = 0;
-        l.o_w = o; o = align1k(o + (uint32_t)g.np_tile * g.d * 2);
-        l.o_xk = o; o = align1k(o + (uint32_t)op[0] * kC * g.d * 2);
-        l.xv_stride = (uint32_t)(g.dv / 64 + 1) * kBlk;       // V blocks + ones atom
-        l.o_xv = o; o = align1k(o + (uint32_t)op[1] * l.xv_stride);
-        l.o_phk = o; o = align1k(o + 4 * kBlk);
-        l.o_small = o; o = align1k(o + 840 * 4);
-        l.bytes = o + 1024;
-        l.nks = op[0];
-        l.nvs = op[1];
-        if (l.bytes <= kSmemMax) break;
+    for (int FT = (g.n_ft % 2 == 0 && 256 + 2 * (g.dv + 16) <= 512) ? 2 : 1; FT >= 1; --FT) {
+        for (const auto &op : opts) {
+            uint32_t o = 0;
+            l.o_w = o; o = align1k(o + (uint32_t)FT * g.np_tile * g.d * 2);
+            l.o_xk = o; o = align1k(o + (uint32_t)op[0] * kC * g.d * 2);
+            l.xv_stride = (uint32_t)(g.dv / 64 + 1) * kBlk;       // V blocks + ones atom
+            l.o_xv = o; o = align1k(o + (uint32_t)op[1] * l.xv_stride);
+            l.o_phk = o; o = align1k(o + (uint32_t)FT * 2 * kBlk);
+            l.o_small = o; o = align1k(o + 840 * 4);
+            l.bytes = o + 1024;
+            l.nks = op[0];
+            l.nvs = op[1];
+            l.FT = FT;
+            if (l.bytes <= kSmemMax) return l;
+        }
     }
     return l;
 }
@@ -1663,29 +1739,67 @@ bool tc_supported(const Problem &p) {
 
 namespace {
 struct Plan {
-    int G, seg_len, nstate, nvb, nchunk;
+    int G, seg_len, nstate, pps, piece_len, nfg, nvb, nchunk;
     size_t img_bytes, per_state, bytes;
 };
+
+// Relative time of the state kernel: CTA waves x (chunks per CTA + about two
+// chunks of fixed cost per CTA).
+double state_cost(long ctas, int chunks, int sms) {
+    return (double)((ctas + sms - 1) / sms) * (chunks + 2);
+}
 
 Plan make_plan(const Problem &p) {
     const Geo g = make_geo(p);
     Plan pl;
     pl.nvb = p.dv / 64;
     pl.nchunk = (p.L + kC - 1) / kC;
+    pl.nfg = g.n_ft / state_layout(g).FT;
     const int sms = num_sms();
-    // segments: whole 128-token chunks, about one CTA per SM in the scan
-    int G;
     if (p.causal) {
-        G = (int)std::lround((double)sms / (p.BH * pl.nvb));
+        // scan segments: whole 128-token chunks, about one CTA per SM
+        int G = (int)std::lround((double)sms / (p.BH * pl.nvb));
+        // at most 64 segments: the combine keeps one scale per (piece, feature tile)
+        G = std::max(1, std::min(std::min(G, pl.nchunk), 64));
+        const int seg_chunks = (pl.nchunk + G - 1) / G;
+        pl.G = (pl.nchunk + seg_chunks - 1) / seg_chunks;
+        pl.seg_len = seg_chunks * kC;
+        // the states of segments 0 .. G-2 come in pieces: a divisor of the
+        // segment's chunks that fills the SMs in whole waves
+        int best = 1;
+        double bc = 1e300;
+        for (int pps = 1; pl.G > 1 && pps <= std::min(8, seg_chunks) && (pl.G - 1) * pps <= 64; ++pps) {
+            if (seg_chunks % pps) continue;
+            const double c = state_cost((long)p.BH * (pl.G - 1) * pps * pl.nfg, seg_chunks / pps, sms);
+            if (c < bc - 1e-9) {
+                bc = c;
+                best = pps;
+            }
+        }
+        pl.pps = best;
+        pl.piece_len = seg_chunks / best * kC;
+        pl.nstate = (pl.G - 1) * best;
     } else {
-        G = (int)std::lround(2.0 * sms / (p.BH * g.n_ft));
+        // the state of all keys, in pieces of whole chunks that fill the SMs
+        // in whole waves (the output kernel is persistent and takes no segments)
+        int best = 1, best_pc = pl.nchunk;
+        double bc = 1e300;
+        for (int np = 1; np <= std::min(64, pl.nchunk); ++np) {
+            const int pc = (pl.nchunk + np - 1) / np;
+            const int npe = (pl.nchunk + pc - 1) / pc;
+            const double c = state_cost((long)p.BH * npe * pl.nfg, pc, sms);
+            if (c < bc - 1e-9) {
+                bc = c;
+                best = npe;
+                best_pc = pc;
+            }
+        }
+        pl.G = best;
+        pl.seg_len = best_pc * kC;
+        pl.pps = 1;
+        pl.piece_len = pl.seg_len;
+        pl.nstate = best;
     }
-    // at most 64 segments: the combine keeps one scale per (segment, feature tile)
-    G = std::max(1, std::min(std::min(G, pl.nchunk), 64));
-    const int seg_chunks = (pl.nchunk + G - 1) / G;
-    pl.G = (pl.nchunk + seg_chunks - 1) / seg_chunks;
-    pl.seg_len = seg_chunks * kC;
-    pl.nstate = p.causal ? pl.G - 1 : pl.G;
     pl.img_bytes = (size_t)p.H * p.nproj * p.d * 2;
     pl.per_state = (size_t)p.r * (p.dv + 1);
     size_t bytes = carve_bytes<uint8_t>(pl.img_bytes) +
@@ -1741,14 +1855,14 @@ int tc_run(const void *q, const void *k, const void *v, const float *omega, floa
     if (nstate > 0) {
         StateLayout sl = state_layout(g);
         StateArgs sa;
-        sa.g = g; sa.H = p.H; sa.L = p.L; sa.seg_len = seg_len; sa.nseg = nstate; sa.nvs = sl.nvs;
-        sa.nks = sl.nks;
+        sa.g = g; sa.H = p.H; sa.L = p.L; sa.FT = sl.FT; sa.piece_len = pl.piece_len; sa.npieces = nstate;
+        sa.nvs = sl.nvs; sa.nks = sl.nks;
         sa.omg = img; sa.state = state; sa.meta = meta; sa.status = dstat;
         sa.o_w = sl.o_w; sa.o_xk = sl.o_xk; sa.o_xv = sl.o_xv; sa.o_phk = sl.o_phk;
         sa.o_small = sl.o_small; sa.xv_stride = sl.xv_stride; sa.tmem_cols = 512;
         if (cudaFuncSetAttribute(tc_state, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sl.bytes) != cudaSuccess)
             return FAVOR_ERR_CUDA;
-        if ((rc = launch_dependent(tc_state, dim3(g.n_ft, nstate, p.BH), dim3(kStateThreads), sl.bytes, st,
+        if ((rc = launch_dependent(tc_state, dim3(pl.nfg, nstate, p.BH), dim3(kStateThreads), sl.bytes, st,
                                    mk, mv, sa)))
             return rc;
         FAVOR_LAUNCH_CHECK();
@@ -1757,7 +1871,7 @@ int tc_run(const void *q, const void *k, const void *v, const float *omega, floa
     if (!p.causal) {
         uint8_t *sop = cv.take<uint8_t>((size_t)p.BH * (nvb + 1) * p.r * 128);
         CombineArgs ca{};
-        ca.g = g; ca.nseg = nstate; ca.causal = 0; ca.state = state; ca.meta = meta;
+        ca.g = g; ca.nseg = nstate; ca.pps = 1; ca.causal = 0; ca.state = state; ca.meta = meta;
         ca.sop = sop;
         ca.slice = 2048;
         const int nsl = (int)((per_state + ca.slice - 1) / ca.slice);
@@ -1791,8 +1905,8 @@ int tc_run(const void *q, const void *k, const void *v, const float *omega, floa
     const bool direct = G <= 4;
     if (G > 1 && !direct) {
         CombineArgs ca{};
-        ca.g = g; ca.nseg = nstate; ca.causal = 1; ca.state = state; ca.meta = meta;
-        ca.s_in = s_in; ca.meta_in = meta_in;
+        ca.g = g; ca.nseg = nstate; ca.pps = pl.pps; ca.causal = 1; ca.state = state; ca.meta = meta;
+        ca.s_in = s_in; ca.meta_in = meta_in; ca.nout = G;
         ca.slice = 2048;
         const int nsl = (int)((per_state + ca.slice - 1) / ca.slice);
         if ((rc = launch_dependent(tc_combine, dim3(p.BH, G - 1, nsl), dim3(256), 0, st, ca))) return rc;
@@ -1803,7 +1917,7 @@ int tc_run(const void *q, const void *k, const void *v, const float *omega, floa
     a.g = g;
     a.H = p.H; a.L = p.L; a.seg_len = seg_len; a.nseg = G;
     a.omg = img; a.s_in = s_in; a.meta_in = meta_in; a.status = dstat;
-    a.state = state; a.meta = meta; a.nstate = nstate; a.direct = direct ? 1 : 0;
+    a.state = state; a.meta = meta; a.nstate = nstate; a.pps = pl.pps; a.direct = direct ? 1 : 0;
     a.o_w = cl.o_w; a.o_x = cl.o_x; a.o_v = cl.o_v; a.o_kb = cl.o_kb; a.o_small = cl.o_small;
     a.tmem_cols = 512;
     if (cudaFuncSetAttribute(tc_causal, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cl.bytes) != cudaSuccess)
