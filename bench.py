@@ -42,7 +42,7 @@ TRAFFIC = {
 KERNEL_SECTIONS = {
     "tc_causal": ("// tc_causal: the chunked causal scan, warp-specialised.", "// tc_output: non-causal rows"),
     "tc_output": ("// tc_output: non-causal rows", "// host side"),
-    "tc_state": ("// tc_state: per (feature tile, segment, head) the segment state", "// tc_combine:"),
+    "tc_state": ("// tc_state: per (feature group, piece, head) the state of a run of keys", "// tc_combine:"),
 }
 
 
@@ -309,9 +309,14 @@ def run_ours(args):
     hbm_gbs, tflops, src = peaks()
     kname = stats.dominant_kernel.decode() if stats.dominant_kernel else ""
     # algorithmic HBM bytes of the dominant kernel per token: the causal scan
-    # reads q, k, v and writes out; the non-causal output kernel reads q and
-    # writes out (k, v are read by the state kernel)
-    kbytes_tok = (2 * w.d + 4 * w.dv) if kname == "tc_output" else bytes_tok
+    # reads q, k, v and writes out; the non-causal state kernel reads k and v
+    # (the output kernel then reads q and writes out)
+    if kname == "tc_state":
+        kbytes_tok = 2 * (w.d + w.dv)
+    elif kname == "tc_output":
+        kbytes_tok = 2 * w.d + 4 * w.dv
+    else:
+        kbytes_tok = bytes_tok
     achieved = kbytes_tok * tokens / (dom_ms / 1000.0) / 1e9
     roof_ms = max(flops_tok * tokens / (tflops * 1e12), bytes_tok * tokens / (hbm_gbs * 1e9)) * 1e3
 
@@ -370,6 +375,196 @@ def run_ours(args):
     return 0
 
 
+# decode workloads: (shape of the forward workload, batch, prefix length).
+# The state of a prefix is built once; each step decodes one token per head
+# and updates the state in place.  The large batch takes a short prefix: the
+# state's size, and so the step's work, does not depend on its length.
+DECODE_METRIC = "FAVOR+ decode tokens/sec (one token per head per step, B*H/s); % of HBM roofline"
+DECODE = {"decode8k": ("causal8k", 4, 8192), "decode_b256": ("causal8k", 256, 128)}
+
+
+def decode_bytes_per_head(w):
+    """Algorithmic HBM bytes of one decode step of one head: the state read and
+    written (r (dv + 2) fp32 each way), q, k, v (bf16) and out (fp32)."""
+    return 8 * w.m * (w.dv + 2) + 2 * (2 * w.d + w.dv) + 4 * w.dv
+
+
+def decode_cpu_baseline(w, n_heads, steps):
+    """The float64 oracle's decode step on n heads (state of a 16-key prefix)."""
+    import numpy as np
+    import oracle
+    from favor_inputs import make_inputs
+    inp = make_inputs(w.with_(B=1, H=n_heads), L=16 + steps)
+    om = inp.omega
+    S, z = oracle.state(inp.k32[:, :, :16], inp.v32[:, :, :16], om)
+    t0 = time.perf_counter()
+    for t in range(16, 16 + steps):
+        _, S, z = oracle.decode_step(inp.q32[:, :, t], inp.k32[:, :, t], inp.v32[:, :, t], om, S, z)
+    dt = time.perf_counter() - t0
+    return {"value": n_heads * steps / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n_heads} heads x {steps} decode steps (float64 C oracle, one thread)",
+            "seconds": dt}
+
+
+def run_decode_reference(args):
+    if int(os.environ.get("RANK", "0")) != 0:
+        return 0
+    base, B, L0 = DECODE[args.workload]
+    w = workload(base)[0].with_(B=B)
+    for _ in range(args.warmup):
+        decode_cpu_baseline(w, 64, 50)
+    times = [decode_cpu_baseline(w, 64, 50)["seconds"] for _ in range(args.steps)]
+    ms = 1000 * statistics.mean(times) / 50
+    value = 64 / (ms / 1000)
+    print(json.dumps({
+        "impl": "reference", "metric": DECODE_METRIC, "value": value, "unit": "tokens/s", "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: the oracle's decode step on 64 of {w.B * w.H} heads"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": "64 heads x 50 decode steps per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+    return 0
+
+
+def run_decode(args):
+    import numpy as np
+    import torch
+    from favor_random_feature_gb300 import build as fbuild
+    fbuild.build()
+    import favor_random_feature_gb300 as fv
+    from favor_inputs import make_inputs
+
+    if int(os.environ.get("WORLD_SIZE", "1")) != 1 or args.gpus != 1:
+        raise SystemExit("decode workloads run on one GPU (replicas only)")
+    base, B, L0 = DECODE[args.workload]
+    w = workload(base)[0].with_(B=B)
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(
+        torch.bfloat16).cuda()
+    prefix = make_inputs(w, L=L0)
+    om = torch.from_numpy(np.ascontiguousarray(prefix.omega)).cuda()
+    stream = torch.cuda.current_stream()
+    per = fv.favor_state_floats(w.d, w.dv, w.m, 0)
+    state = torch.empty((w.B, w.H, per), dtype=torch.float32, device="cuda")
+
+    def check(rc, what):
+        if rc != fv.FAVOR_OK:
+            raise fv.FavorError(rc, what)
+
+    check(fv.favor_attn_state(dev(prefix.k), dev(prefix.v), om, state, w.B, w.H, L0, w.d, w.dv, w.m, 0,
+                              stream), "favor_attn_state")
+    del prefix
+    # a pool of new tokens, [T][B][H][.] on the device, used in turn
+    T = 64
+    tok = make_inputs(w.with_(seed=w.seed + 77), L=T)
+    tq = dev(np.moveaxis(tok.q, 2, 0))
+    tk = dev(np.moveaxis(tok.k, 2, 0))
+    tv = dev(np.moveaxis(tok.v, 2, 0))
+    out = torch.empty((w.B, w.H, w.dv), dtype=torch.float32, device="cuda")
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device="cuda")
+    step = [0]
+
+    def call():
+        t = step[0] % T
+        step[0] += 1
+        return fv.favor_attn_decode(tq[t], tk[t], tv[t], om, state, out, w.B, w.H, w.d, w.dv, w.m, 0,
+                                    stream)
+
+    for _ in range(max(3, args.warmup)):
+        check(call(), "favor_attn_decode")
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                           else os.environ["CUDA_VISIBLE_DEVICES"].split(",")[0])
+    t_soak = time.time()
+    while time.time() - t_soak < 1.0:
+        flush.zero_()
+        check(call(), "favor_attn_decode")
+        torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        check(call(), "favor_attn_decode")
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    sampler.stop()
+    st = fv.favor_get_device_status(stream)
+    if st != fv.FAVOR_OK:
+        raise fv.FavorError(st, "device status after the timed steps")
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    # the kernel's own time and the launch count, from separate steps
+    stat_steps = max(3, min(args.steps, 10))
+    fv.favor_stats_enable(True)
+    for _ in range(stat_steps):
+        flush.zero_()
+        check(call(), "favor_attn_decode")
+    torch.cuda.synchronize()
+    stats = fv.favor_stats_read()
+    fv.favor_stats_enable(False)
+    dom_ms = stats.dominant_ms / max(1, stats.dominant_launches)
+    launches_per_step = stats.kernel_launches / stat_steps
+    heads = w.B * w.H
+    kbytes = heads * decode_bytes_per_head(w)
+    hbm_gbs, _, src = peaks()
+    achieved = kbytes / (dom_ms / 1000.0) / 1e9
+
+    # end to end: each step copies its token's q, k, v from pinned host memory,
+    # decodes, and reads out back
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(
+        torch.bfloat16).pin_memory()
+    hq, hk, hv = pin(np.moveaxis(tok.q, 2, 0)), pin(np.moveaxis(tok.k, 2, 0)), pin(np.moveaxis(tok.v, 2, 0))
+    hout = torch.empty((w.B, w.H, w.dv), dtype=torch.float32).pin_memory()
+    dq, dk, dvv = torch.empty_like(tq[0]), torch.empty_like(tk[0]), torch.empty_like(tv[0])
+    e2e_steps = max(3, min(args.steps, 50))
+    torch.cuda.synchronize()
+    te0 = time.perf_counter()
+    for i in range(e2e_steps):
+        t = i % T
+        dq.copy_(hq[t], non_blocking=True)
+        dk.copy_(hk[t], non_blocking=True)
+        dvv.copy_(hv[t], non_blocking=True)
+        check(fv.favor_attn_decode(dq, dk, dvv, om, state, out, w.B, w.H, w.d, w.dv, w.m, 0, stream),
+              "favor_attn_decode")
+        hout.copy_(out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    te = (time.perf_counter() - te0) / e2e_steps
+    h2d = (dq.numel() + dk.numel() + dvv.numel()) * 2
+    line = {
+        "metric": DECODE_METRIC, "value": heads / (ms / 1000.0), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {
+            "workload": f"{args.workload}: B={w.B} H={w.H} d={w.d} dv={w.dv} m={w.m} positive-features, "
+                        f"state of a {L0}-token prefix, one new token per head per step",
+            "B": w.B, "H": w.H, "d": w.d, "dv": w.dv, "m": w.m, "prefix": L0,
+            "inputs": "bf16 q,k,v; fp32 omega, state and out",
+            "l2": "flushed between steps (256 MiB write, outside the timed events)",
+        },
+        "roofline": {
+            "bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+            "frac": achieved / hbm_gbs, "traffic": measured_traffic("decode_step", args.workload),
+            "kernel": stats.dominant_kernel.decode() if stats.dominant_kernel else None,
+            "kernel_ms": dom_ms, "peak_source": src, "algorithmic_bytes_per_launch": kbytes,
+        },
+        "e2e": {"value": heads / te, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": hout.numel() * 4},
+        "gpu_launches": int(round(launches_per_step * args.steps)),
+        "clocks": sampler.summary(t0, t1),
+    }
+    if not args.no_cpu_baseline:
+        cb = decode_cpu_baseline(w, 64, 200)
+        cb.pop("seconds", None)
+        line["cpu_baseline"] = cb
+    print(json.dumps(line))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -377,11 +572,16 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="causal8k",
-                    choices=["causal8k", "nc4096", "long64k", "long64k_nc", "sweep16k"])
+                    choices=["causal8k", "nc4096", "long64k", "long64k_nc", "sweep16k", "decode8k",
+                             "decode_b256"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.workload in DECODE:
+        if args.impl == "reference":
+            return run_decode_reference(args)
+        return run_decode(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -39,6 +39,11 @@ EXPORTS = (
     "favor_feature_dim",
     "favor_stats_enable",
     "favor_stats_read",
+    "favor_state_floats",
+    "favor_attn_state",
+    "favor_attn_state_f32",
+    "favor_attn_decode",
+    "favor_attn_decode_f32",
 )
 
 _lib = None
@@ -84,6 +89,14 @@ def lib() -> ctypes.CDLL:
         L.favor_stats_enable.restype = i
         L.favor_stats_read.argtypes = [ctypes.POINTER(FavorStats)]
         L.favor_stats_read.restype = i
+        L.favor_state_floats.argtypes = [i, i, i, i]
+        L.favor_state_floats.restype = i
+        for name in ("favor_attn_state", "favor_attn_state_f32"):
+            getattr(L, name).argtypes = [vp, vp, fp, fp] + [i] * 7 + [vp]
+            getattr(L, name).restype = i
+        for name in ("favor_attn_decode", "favor_attn_decode_f32"):
+            getattr(L, name).argtypes = [vp, vp, vp, fp, fp, fp] + [i] * 6 + [vp]
+            getattr(L, name).restype = i
         _lib = L
     return _lib
 
@@ -167,6 +180,30 @@ def favor_stats_read() -> FavorStats:
     if rc != FAVOR_OK:
         raise FavorError(rc, "favor_stats_read")
     return st
+
+
+def favor_state_floats(d, dv, m, feature_map) -> int:
+    return lib().favor_state_floats(int(d), int(dv), int(m), int(feature_map))
+
+
+def favor_attn_state(k, v, omega, state, B, H, L, d, dv, m, feature_map, stream=None):
+    return lib().favor_attn_state(_ptr(k), _ptr(v), _ptr(omega), _ptr(state), B, H, L, d, dv, m,
+                                  int(feature_map), _stream(stream))
+
+
+def favor_attn_state_f32(k, v, omega, state, B, H, L, d, dv, m, feature_map, stream=None):
+    return lib().favor_attn_state_f32(_ptr(k), _ptr(v), _ptr(omega), _ptr(state), B, H, L, d, dv, m,
+                                      int(feature_map), _stream(stream))
+
+
+def favor_attn_decode(q, k, v, omega, state, out, B, H, d, dv, m, feature_map, stream=None):
+    return lib().favor_attn_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(omega), _ptr(state), _ptr(out),
+                                   B, H, d, dv, m, int(feature_map), _stream(stream))
+
+
+def favor_attn_decode_f32(q, k, v, omega, state, out, B, H, d, dv, m, feature_map, stream=None):
+    return lib().favor_attn_decode_f32(_ptr(q), _ptr(k), _ptr(v), _ptr(omega), _ptr(state), _ptr(out),
+                                       B, H, d, dv, m, int(feature_map), _stream(stream))
 
 
 def attention(q, k, v, omega, causal: bool, feature_map: int = FAVOR_MAP_POSITIVE,

@@ -58,6 +58,18 @@ int tc_forward(const void *q, const void *k, const void *v, const float *omega, 
 size_t tc_scratch_bytes(const Problem &p);
 int tc_run(const void *q, const void *k, const void *v, const float *omega, float *out,
            const Problem &p, cudaStream_t stream, void *ws, size_t ws_bytes);
+// The state of all L keys of each head (non-causal state pass, no output):
+// piece states [BH][npieces][r][dv+1] and their (R, max z, max|v|, max|S|)
+// per 128-feature tile [BH][npieces][r/128][4], in the workspace.  Features
+// are 2^(log2(e)(w.k - |k|^2/2) - R) (positive; trig sin, cos and elu1 at
+// R = 0), trig features in 128-column tiles [sin 64 | cos 64].
+int tc_key_state(const void *k, const void *v, const float *omega, const Problem &p, cudaStream_t st,
+                 const float **state, const float **meta, int *npieces);
+// The same on the SIMT path: S [BH][r][dv+1] at the per-head reference
+// e^hmax[bh] (natural log), features with the 1/sqrt(m) factor, trig
+// features interleaved (sin, cos) per projection.
+int simt_key_state(const void *k, const void *v, bool bf16_in, const float *omega, const Problem &p,
+                   cudaStream_t st, const float **S, const float **hmax);
 // Host argument checks shared by the forward entry points (esize = bytes per
 // q/k/v element).
 int validate_args(const void *q, const void *k, const void *v, const float *omega,

@@ -322,6 +322,49 @@ int simt_forward(const void *q, const void *k, const void *v, bool bf16_in, cons
                             static_cast<const float *>(v), omega, out, p, stream);
 }
 
+namespace {
+template <typename T>
+int key_state_t(const T *k, const T *v, const float *omega, const Problem &p, cudaStream_t st,
+                const float **S_out, const float **hmax_out) {
+    const size_t rows = (size_t)p.BH * p.L;
+    const size_t per = (size_t)p.r * (p.dv + 1);
+    size_t bytes = carve_bytes<float>(rows * p.nproj) + carve_bytes<float>(rows * p.r) +
+                   carve_bytes<float>(rows) + carve_bytes<float>(p.BH) + carve_bytes<float>((size_t)p.BH * per);
+    int status = FAVOR_OK;
+    void *ws = workspace(bytes, &status);
+    if (!ws) return status;
+    Carve cv{static_cast<char *>(ws), 0};
+    float *P = cv.take<float>(rows * p.nproj);
+    float *phik = cv.take<float>(rows * p.r);
+    float *lsk = cv.take<float>(rows);
+    float *hmax = cv.take<float>(p.BH);
+    float *S = cv.take<float>((size_t)p.BH * per);
+    int rc = features_into<T>(k, omega, P, phik, lsk, p, st);
+    if (rc) return rc;
+    simt_head_max<<<p.BH, 256, 0, st>>>(lsk, hmax, p.L);
+    FAVOR_LAUNCH_CHECK();
+    const size_t total = rows * p.r;
+    const unsigned sg = (unsigned)std::min<size_t>((total + 255) / 256, 152 * 64);
+    simt_key_scale<<<sg, 256, 0, st>>>(phik, lsk, hmax, p.L, p.r, total);
+    FAVOR_LAUNCH_CHECK();
+    dim3 sgrid((p.r + 31) / 32, p.dv + 1, p.BH);
+    simt_state<T><<<sgrid, 32, 0, st>>>(phik, v, S, p.L, p.r, p.dv, p.L, 1);
+    FAVOR_LAUNCH_CHECK();
+    *S_out = S;
+    *hmax_out = hmax;
+    return FAVOR_OK;
+}
+}  // namespace
+
+int simt_key_state(const void *k, const void *v, bool bf16_in, const float *omega, const Problem &p,
+                   cudaStream_t st, const float **S, const float **hmax) {
+    if (bf16_in)
+        return key_state_t<uint16_t>(static_cast<const uint16_t *>(k), static_cast<const uint16_t *>(v),
+                                     omega, p, st, S, hmax);
+    return key_state_t<float>(static_cast<const float *>(k), static_cast<const float *>(v), omega, p, st,
+                              S, hmax);
+}
+
 int simt_feature_map(const void *x, bool bf16_in, const float *omega, float *phi,
                      float *log_scale, const Problem &p, cudaStream_t stream) {
     const size_t rows = (size_t)p.BH * p.L;

@@ -42,7 +42,6 @@ constexpr float kShift = 8.0f * 1.4426950408889634f;   // e^8 headroom (log2 uni
 constexpr float kSigmaTarget = 16384.f;  // bound for |sigma * S| in the fp16 state operand
 // largest key feature kept, e^10: a chunk may exceed the reference by e^2
 // before the reference moves
-constexpr float kMaxFeature = 22026.4658f;
 constexpr float kLog2MaxFeature = 14.4269504f;          // log2(e^10)
 constexpr long long kWaitLimit = 1ll << 32;             // ~2 s of clock cycles
 constexpr uint32_t kBlk = 16384;        // one [128][64] fp16 block (128B swizzle)
@@ -108,17 +107,6 @@ __device__ __forceinline__ float pow2_scale_14(float b) {
 
 __device__ __forceinline__ void set_status(int *status, int code) {
     if (status) atomicExch(status, code);
-}
-
-// Store 32 features (fp16) of one row into a 128B-swizzled [128][64] block at
-// columns [c0, c0 + 32).
-__device__ __forceinline__ void store_row32(uint8_t *blk, int row, int c0, const float (&v)[32]) {
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        uint4 u = make_uint4(pack_half2(v[8 * c + 0], v[8 * c + 1]), pack_half2(v[8 * c + 2], v[8 * c + 3]),
-                             pack_half2(v[8 * c + 4], v[8 * c + 5]), pack_half2(v[8 * c + 6], v[8 * c + 7]));
-        *reinterpret_cast<uint4 *>(blk + sw128_offset(row, c0 + 8 * c)) = u;
-    }
 }
 
 // sin/cos with the argument first reduced to [-pi, pi] (Cody-Waite, 2pi split
@@ -1813,9 +1801,57 @@ Plan make_plan(const Problem &p) {
     pl.bytes = bytes;
     return pl;
 }
+
+// The state pass over the plan's pieces (W image already written by
+// tc_prep_omega on the same stream).
+int launch_state(const Problem &p, const Geo &g, const Plan &pl, const uint8_t *img, float *state,
+                 float *meta, const CUtensorMap &mk, const CUtensorMap &mv, cudaStream_t st, bool timed) {
+    StateLayout sl = state_layout(g);
+    StateArgs sa;
+    sa.g = g; sa.H = p.H; sa.L = p.L; sa.FT = sl.FT; sa.piece_len = pl.piece_len; sa.npieces = pl.nstate;
+    sa.nvs = sl.nvs; sa.nks = sl.nks;
+    sa.omg = img; sa.state = state; sa.meta = meta; sa.status = device_status_ptr();
+    sa.o_w = sl.o_w; sa.o_xk = sl.o_xk; sa.o_xv = sl.o_xv; sa.o_phk = sl.o_phk;
+    sa.o_small = sl.o_small; sa.xv_stride = sl.xv_stride; sa.tmem_cols = 512;
+    if (cudaFuncSetAttribute(tc_state, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sl.bytes) != cudaSuccess)
+        return FAVOR_ERR_CUDA;
+    if (timed) stats_begin(st, "tc_state");
+    int rc = launch_dependent(tc_state, dim3(pl.nfg, pl.nstate, p.BH), dim3(kStateThreads), sl.bytes, st, mk, mv, sa);
+    if (timed) stats_end(st);
+    if (rc) return rc;
+    FAVOR_LAUNCH_CHECK();
+    return FAVOR_OK;
+}
 }  // namespace
 
 size_t tc_scratch_bytes(const Problem &p) { return make_plan(p).bytes; }
+
+int tc_key_state(const void *k, const void *v, const float *omega, const Problem &p0, cudaStream_t st,
+                 const float **state_out, const float **meta_out, int *npieces) {
+    Problem p = p0;
+    p.causal = 0;
+    const Geo g = make_geo(p);
+    const Plan pl = make_plan(p);
+    int status = FAVOR_OK;
+    void *ws = workspace(pl.bytes, &status);
+    if (!ws) return status;
+    Carve cv{static_cast<char *>(ws), 0};
+    uint8_t *img = cv.take<uint8_t>(pl.img_bytes);
+    float *state = cv.take<float>((size_t)p.BH * pl.nstate * pl.per_state);
+    float *meta = cv.take<float>((size_t)p.BH * pl.nstate * g.n_ft * 4);
+    CUtensorMap mk, mv;
+    int rc;
+    if ((rc = make_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.BH, p.L, p.d, 64)) ||
+        (rc = make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.BH, p.L, p.dv, 64)))
+        return rc;
+    tc_prep_omega<<<dim3(32, p.H), 256, 0, st>>>(omega, img, p.H, p.nproj, p.d, p.map);
+    FAVOR_LAUNCH_CHECK();
+    if ((rc = launch_state(p, g, pl, img, state, meta, mk, mv, st, false))) return rc;
+    *state_out = state;
+    *meta_out = meta;
+    *npieces = pl.nstate;
+    return FAVOR_OK;
+}
 
 int tc_forward(const void *q, const void *k, const void *v, const float *omega, float *out,
                const Problem &p, cudaStream_t st) {
@@ -1853,19 +1889,8 @@ int tc_run(const void *q, const void *k, const void *v, const float *omega, floa
     FAVOR_LAUNCH_CHECK();
 
     if (nstate > 0) {
-        StateLayout sl = state_layout(g);
-        StateArgs sa;
-        sa.g = g; sa.H = p.H; sa.L = p.L; sa.FT = sl.FT; sa.piece_len = pl.piece_len; sa.npieces = nstate;
-        sa.nvs = sl.nvs; sa.nks = sl.nks;
-        sa.omg = img; sa.state = state; sa.meta = meta; sa.status = dstat;
-        sa.o_w = sl.o_w; sa.o_xk = sl.o_xk; sa.o_xv = sl.o_xv; sa.o_phk = sl.o_phk;
-        sa.o_small = sl.o_small; sa.xv_stride = sl.xv_stride; sa.tmem_cols = 512;
-        if (cudaFuncSetAttribute(tc_state, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sl.bytes) != cudaSuccess)
-            return FAVOR_ERR_CUDA;
-        if ((rc = launch_dependent(tc_state, dim3(pl.nfg, nstate, p.BH), dim3(kStateThreads), sl.bytes, st,
-                                   mk, mv, sa)))
-            return rc;
-        FAVOR_LAUNCH_CHECK();
+        // the state pass is the largest kernel of the non-causal path
+        if ((rc = launch_state(p, g, pl, img, state, meta, mk, mv, st, !p.causal))) return rc;
     }
 
     if (!p.causal) {
@@ -1889,12 +1914,7 @@ int tc_run(const void *q, const void *k, const void *v, const float *omega, floa
             return FAVOR_ERR_CUDA;
         // one persistent CTA per SM, each on a contiguous run of (head, dv tile, chunk) units
         const int grid = std::min(oa.total_units, sms);
-        stats_begin(st, "tc_output");
-        if ((rc = launch_dependent(tc_output, dim3(grid), dim3(kOutThreads), ol.bytes, st, mq, mo, oa))) {
-            stats_end(st);
-            return rc;
-        }
-        stats_end(st);
+        if ((rc = launch_dependent(tc_output, dim3(grid), dim3(kOutThreads), ol.bytes, st, mq, mo, oa))) return rc;
         FAVOR_LAUNCH_CHECK();
         return FAVOR_OK;
     }

@@ -138,6 +138,53 @@ void favor_release_workspace(void);
 /* Number of feature columns r for a map, or -1 if the arguments are invalid. */
 int favor_feature_dim(int feature_map, int d, int m);
 
+/* ---- carried state and the one-token decode step --------------------------
+ * The causal form keeps running sums (Performer study notes, "Case 2"):
+ *   S_i = S_{i-1} + phi(k_i) v_i^T,  z_i = z_{i-1} + phi(k_i),
+ *   out_i = phi(q_i)^T S_i / phi(q_i)^T z_i,
+ * so generation continues a prefix one token at a time at O(r d) per head.
+ *
+ * Decode state of one head (b, h): favor_state_floats() = r (dv + 2) fp32
+ * values laid out as  S^ [r][dv] | z^ [r] | rho [r],  state buffer
+ * [B][H][r (dv + 2)], 16-byte aligned, owned by the caller.  The carried sums
+ * are S_f = S^_f 2^rho_f and z_f = z^_f 2^rho_f with phi the map above
+ * (1/sqrt(m) included; trig features interleaved (sin, cos) per projection);
+ * rho_f is a per-feature log2 reference that keeps every stored value in
+ * fp32 range.  The empty state (no tokens) is S^ = z^ = 0, rho = -inf. */
+
+/* Values per head of the decode state, r (dv + 2), or -1 if the arguments are
+ * invalid. */
+int favor_state_floats(int d, int dv, int m, int feature_map);
+
+/* The decode state after the L keys of each head: k [B][H][L][d] and
+ * v [B][H][L][dv] bf16 bits, omega as for the forward pass -> state.
+ * L = 0 writes the empty state (k, v may then be NULL).  bf16 inputs run the
+ * tensor-core state pass (fp16 features, fp32 sums) where the shape allows,
+ * else fp32 SIMT kernels.  state must not overlap k, v or omega.
+ * Asynchronous on `stream`; returns favor_status_t. */
+int favor_attn_state(const void *k, const void *v, const float *omega, float *state, int B, int H,
+                     int L, int d, int dv, int m, int feature_map, cudaStream_t stream);
+
+/* Same with fp32 k/v, computed in fp32 SIMT kernels. */
+int favor_attn_state_f32(const float *k, const float *v, const float *omega, float *state, int B,
+                         int H, int L, int d, int dv, int m, int feature_map, cudaStream_t stream);
+
+/* One decode step for every head: q, k [B][H][d] and v [B][H][dv] (bf16
+ * bits) of the new token; state is read and updated in place (S += phi(k)
+ * v^T, z += phi(k)), then out [B][H][dv] fp32 = phi(q)^T S / phi(q)^T z on
+ * the updated state (the new token attends to itself, as in the causal
+ * forward pass).  Supports r <= 1024.  out and state must not overlap each
+ * other or an input.  fp32 SIMT arithmetic throughout (one thread-block
+ * cluster per head).  Asynchronous on `stream`; returns favor_status_t. */
+int favor_attn_decode(const void *q, const void *k, const void *v, const float *omega, float *state,
+                      float *out, int B, int H, int d, int dv, int m, int feature_map,
+                      cudaStream_t stream);
+
+/* Same with fp32 q/k/v. */
+int favor_attn_decode_f32(const float *q, const float *k, const float *v, const float *omega,
+                          float *state, float *out, int B, int H, int d, int dv, int m,
+                          int feature_map, cudaStream_t stream);
+
 /* Measurement hook (no counterpart on the pages): while enabled, every
  * forward call records a CUDA event pair on its stream around its dominant
  * kernel (the causal scan, or the non-causal output kernel), and every

@@ -246,7 +246,7 @@ def test_full_size_sweep_sampled(m):
 # the bf16 entry point runs the tensor-core kernels for the benchmark shapes
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("w,causal,kernel", [(CAUSAL8K, True, "tc_causal"),
-                                             (NC4096, False, "tc_output"),
+                                             (NC4096, False, "tc_state"),
                                              (SWEEP16K.with_(m=128), True, "tc_causal")],
                          ids=["causal", "noncausal", "d128"])
 def test_tensor_core_path_taken(w, causal, kernel):
