@@ -170,7 +170,9 @@ __device__ __forceinline__ float grp_max(float v, float *red, int ew) {
 __device__ __forceinline__ bool ewait(uint64_t *bar, uint32_t parity, volatile int *abort) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
+    // later polls suspend in hardware until the phase completes (at most
+    // 100 us each), so a waiting warp leaves the issue slots to the others
+    while (!mbar_try_wait_hint(bar, parity, 100000u)) {
         if (*abort) return false;
         if (clock64() - t0 > kWaitLimit) {
             *abort = 1;
