@@ -64,6 +64,13 @@ def _load():
         lib.oracle_state.restype = ctypes.c_int
         lib.oracle_decode_step.argtypes = [P] * 7 + [ctypes.c_int] * 6
         lib.oracle_decode_step.restype = ctypes.c_int
+        U64 = ctypes.c_uint64
+        lib.oracle_philox4x64.argtypes = [ctypes.POINTER(U64), ctypes.POINTER(U64), ctypes.POINTER(U64)]
+        lib.oracle_philox4x64.restype = None
+        lib.oracle_normal.argtypes = [U64, U64, U64]
+        lib.oracle_normal.restype = ctypes.c_double
+        lib.oracle_draw_omega.argtypes = [P] + [ctypes.c_int] * 4 + [U64]
+        lib.oracle_draw_omega.restype = ctypes.c_int
         lib.oracle_feature_dim.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -182,6 +189,31 @@ def decode_step(q, k, v, omega, S, z, feature_map: int = MAP_POSITIVE):
     if rc:
         raise FloatingPointError(f"oracle_decode_step failed ({rc})")
     return out, S2, z2
+
+
+def philox4x64(counter, key):
+    """One Philox4x64-10 block: 4 counter words, 2 key words -> 4 uint64 words."""
+    lib = _load()
+    c = (ctypes.c_uint64 * 4)(*[int(x) for x in counter])
+    k = (ctypes.c_uint64 * 2)(*[int(x) for x in key])
+    o = (ctypes.c_uint64 * 4)()
+    lib.oracle_philox4x64(c, k, o)
+    return [int(x) for x in o]
+
+
+def normal(seed: int, stream: int, e: int) -> float:
+    """Normal number e of stream `stream` under `seed` (Philox4x64-10 + Box-Muller)."""
+    return _load().oracle_normal(int(seed), int(stream), int(e))
+
+
+def draw_omega(H: int, m: int, d: int, kind: int, seed: int):
+    """omega [H][m][d] float64: kind 0 iid N(0, I) rows, 1 block-orthogonal."""
+    lib = _load()
+    out = np.empty((H, m, d), dtype=np.float64)
+    rc = lib.oracle_draw_omega(_dp(out), H, m, d, kind, int(seed))
+    if rc:
+        raise ValueError(f"oracle_draw_omega failed ({rc})")
+    return out
 
 
 def threads_used() -> int:

@@ -32,11 +32,25 @@
  *    out = phi(q)^T S' / phi(q)^T z'
  *          -- Performer study notes, "Case 2" (S_i, z_i are running sums;
  *             each step costs O(r d)).
+ *  - random projections drawn from a counter-based generator (the draw the
+ *    library also makes on the device; the pages leave the generator open):
+ *      Philox4x64-10 -- Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers:
+ *        As Easy as 1, 2, 3" (SC 2011): ten rounds of two 64x64->128-bit
+ *        products with the counter words crossed and the key xored in, the
+ *        key bumped by the Weyl constants between rounds;
+ *      Box-Muller normals from pairs of 53-bit uniforms in (0, 1);
+ *      iid rows w_i ~ N(0, I_d) ("Performer: Unbiased Softmax Approximation",
+ *        the w ~ N(0, I) draw), or block-orthogonal rows: per head ceil(m/d)
+ *        Gaussian d x d blocks, rows orthonormalised by modified Gram-Schmidt
+ *        and scaled by the norm of an independent N(0, I_d) vector, the last
+ *        block truncated (the orthogonal random features the Performer study
+ *        notes name, read as in the block construction).
  *
  * No stabiliser, no blocking, no reordering: every value is the definition
  * evaluated in float64.  Exponents are checked against |t| < 700.
  */
 #include <math.h>
+#include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -247,4 +261,85 @@ int oracle_decode_step(const double *q, const double *k, const double *v, const 
     }
     free(phik); free(phiq);
     return rc;
+}
+
+/* ---- random projections ------------------------------------------------ */
+
+/* one Philox4x64-10 block: out = f_key(ctr) */
+void oracle_philox4x64(const uint64_t ctr[4], const uint64_t key[2], uint64_t out[4])
+{
+    const uint64_t M0 = 0xD2E7470EE14C6C93ULL, M1 = 0xCA5A826395121157ULL;
+    const uint64_t W0 = 0x9E3779B97F4A7C15ULL, W1 = 0xBB67AE8584CAA73BULL;
+    uint64_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+    uint64_t k0 = key[0], k1 = key[1];
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) { k0 += W0; k1 += W1; }
+        unsigned __int128 p0 = (unsigned __int128)M0 * c0;
+        unsigned __int128 p1 = (unsigned __int128)M1 * c2;
+        uint64_t hi0 = (uint64_t)(p0 >> 64), lo0 = (uint64_t)p0;
+        uint64_t hi1 = (uint64_t)(p1 >> 64), lo1 = (uint64_t)p1;
+        uint64_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* normal number e of stream s: block (e / 4, s, 0, 0) under key (seed, 0);
+ * words (x0, x1) give normals 0, 1 and (x2, x3) normals 2, 3 by Box-Muller
+ * with u = (x / 2^11 + 1/2) 2^-53 */
+double oracle_normal(uint64_t seed, uint64_t stream, uint64_t e)
+{
+    const uint64_t ctr[4] = {e >> 2, stream, 0, 0}, key[2] = {seed, 0};
+    uint64_t x[4];
+    oracle_philox4x64(ctr, key, x);
+    const int pair = (int)((e >> 1) & 1), which = (int)(e & 1);
+    const double u1 = ((double)(x[2 * pair] >> 11) + 0.5) * 0x1p-53;
+    const double u2 = ((double)(x[2 * pair + 1] >> 11) + 0.5) * 0x1p-53;
+    const double rad = sqrt(-2.0 * log(u1)), ang = 2.0 * 3.14159265358979323846 * u2;
+    return which ? rad * sin(ang) : rad * cos(ang);
+}
+
+/* omega [H][m][d] in float64: kind 0 iid, kind 1 block-orthogonal.
+ * Returns 0, -1 for bad arguments, -3 on allocation failure. */
+int oracle_draw_omega(double *omega, int H, int m, int d, int kind, uint64_t seed)
+{
+    if (H < 1 || m < 1 || d < 1 || (kind != 0 && kind != 1)) return -1;
+    if (kind == 0) {
+        for (uint64_t e = 0; e < (uint64_t)H * m * d; ++e) omega[e] = oracle_normal(seed, 0, e);
+        return 0;
+    }
+    const int nb = (m + d - 1) / d;
+    double *G = (double *)malloc(sizeof(double) * (size_t)d * d);
+    if (!G) return -3;
+    for (int h = 0; h < H; ++h)
+        for (int b = 0; b < nb; ++b) {
+            const uint64_t base = ((uint64_t)h * nb + b) * d * d;
+            for (int i = 0; i < d * d; ++i) G[i] = oracle_normal(seed, 0, base + i);
+            /* modified Gram-Schmidt on the rows, in row order */
+            for (int i = 0; i < d; ++i) {
+                double *v = G + (size_t)i * d;
+                for (int j = 0; j < i; ++j) {
+                    const double *qj = G + (size_t)j * d;
+                    double dot = 0.0;
+                    for (int t = 0; t < d; ++t) dot += v[t] * qj[t];
+                    for (int t = 0; t < d; ++t) v[t] -= dot * qj[t];
+                }
+                double nrm = 0.0;
+                for (int t = 0; t < d; ++t) nrm += v[t] * v[t];
+                nrm = sqrt(nrm);
+                for (int t = 0; t < d; ++t) v[t] /= nrm;
+            }
+            for (int i = 0; i < d && b * d + i < m; ++i) {
+                double ss = 0.0;
+                for (int t = 0; t < d; ++t) {
+                    const double g = oracle_normal(seed, 1, base + (uint64_t)i * d + t);
+                    ss += g * g;
+                }
+                const double chi = sqrt(ss);
+                double *dst = omega + ((size_t)h * m + (size_t)b * d + i) * d;
+                for (int t = 0; t < d; ++t) dst[t] = G[(size_t)i * d + t] * chi;
+            }
+        }
+    free(G);
+    return 0;
 }

@@ -450,3 +450,79 @@ def test_state_is_additive_and_decode_continues_a_prefix():
         o, St, zt = oracle.decode_step(q[:, :, t], k[:, :, t], v[:, :, t], om, St, zt)
         assert np.allclose(o, full[:, :, t], rtol=1e-11, atol=1e-13)
     assert np.allclose(St, S, rtol=1e-11) and np.allclose(zt, z, rtol=1e-11)
+
+
+# ---------------------------------------------------------------------------
+# random projections drawn by a counter-based generator: Philox4x64-10
+# (Salmon et al., SC 2011) against numpy's implementation of the same
+# generator, Box-Muller normals by their distribution, and the
+# block-orthogonal rows against a QR factorisation and the chi law of norms
+# ---------------------------------------------------------------------------
+def _numpy_philox_block(counter, key):
+    """numpy advances its counter before a block: start it one below."""
+    c = sum(int(x) << (64 * i) for i, x in enumerate(counter))
+    c = (c - 1) % (1 << 256)
+    words = np.array([(c >> (64 * i)) & ((1 << 64) - 1) for i in range(4)], dtype=np.uint64)
+    g = np.random.Philox(key=np.array(key, dtype=np.uint64), counter=words)
+    return [int(x) for x in g.random_raw(4)]
+
+
+@pytest.mark.parametrize("counter,key", [
+    ([0, 0, 0, 0], [0, 0]),
+    ([1, 0, 0, 0], [5, 7]),
+    ([0, 1, 0, 0], [2**64 - 1, 3]),                        # a carry into the second word
+    ([2**64 - 1, 2**64 - 1, 0, 9], [123456789, 987654321]),
+    ([12345, 0, 1, 0], [2024, 0]),                         # the stream word of the draws
+])
+def test_philox_matches_numpy(counter, key):
+    assert oracle.philox4x64(counter, key) == _numpy_philox_block(counter, key)
+
+
+def test_normals_are_standard_and_streams_independent():
+    from scipy import stats
+    n = 100_000
+    z0 = np.array([oracle.normal(7, 0, e) for e in range(n)])
+    z1 = np.array([oracle.normal(7, 1, e) for e in range(n)])
+    for z in (z0, z1):
+        assert stats.kstest(z, "norm").pvalue > 1e-3
+        assert abs(z.mean()) < 5 / np.sqrt(n) and abs(z.var() - 1) < 5 * np.sqrt(2 / n)
+    assert abs(np.corrcoef(z0, z1)[0, 1]) < 5 / np.sqrt(n)
+    assert abs(np.corrcoef(z0[:-1], z0[1:])[0, 1]) < 5 / np.sqrt(n)
+    assert oracle.normal(8, 0, 0) != oracle.normal(7, 0, 0)
+
+
+def test_draw_omega_iid_is_the_normal_stream():
+    from scipy import stats
+    w = oracle.draw_omega(3, 40, 32, 0, 99)
+    flat = w.reshape(-1)
+    assert all(flat[e] == oracle.normal(99, 0, e) for e in range(0, flat.size, 97))
+    assert stats.kstest(flat, "norm").pvalue > 1e-3
+
+
+@pytest.mark.parametrize("m,d", [(64, 32), (100, 32), (256, 64)])
+def test_draw_omega_block_orthogonal(m, d):
+    """Each block's rows are the orthonormal factor of its Gaussian block (QR
+    of the transpose with a positive diagonal) scaled by chi(d) norms drawn
+    from the second stream; the last block is truncated to m rows."""
+    from scipy import stats
+    H, seed = 2, 31
+    w = oracle.draw_omega(H, m, d, 1, seed)
+    nb = -(-m // d)
+    norms = []
+    for h in range(H):
+        for b in range(nb):
+            base = (h * nb + b) * d * d
+            G = np.array([oracle.normal(seed, 0, base + i) for i in range(d * d)]).reshape(d, d)
+            Q, R = np.linalg.qr(G.T)
+            Q = Q * np.sign(np.diag(R))
+            rows = min(d, m - b * d)
+            chi = np.array([np.linalg.norm([oracle.normal(seed, 1, base + i * d + t) for t in range(d)])
+                            for i in range(rows)])
+            want = Q.T[:rows] * chi[:, None]
+            got = w[h, b * d: b * d + rows]
+            assert np.allclose(got, want, rtol=1e-10, atol=1e-10)
+            gram = got @ got.T
+            assert np.allclose(gram - np.diag(np.diag(gram)), 0, atol=1e-10 * d)
+            norms.extend(np.linalg.norm(got, axis=1))
+    if len(norms) >= 100:
+        assert stats.kstest(norms, stats.chi(d).cdf).pvalue > 1e-3
