@@ -44,6 +44,7 @@ EXPORTS = (
     "favor_attn_state_f32",
     "favor_attn_decode",
     "favor_attn_decode_f32",
+    "favor_draw_omega",
 )
 
 _lib = None
@@ -94,6 +95,8 @@ def lib() -> ctypes.CDLL:
         for name in ("favor_attn_state", "favor_attn_state_f32"):
             getattr(L, name).argtypes = [vp, vp, fp, fp] + [i] * 7 + [vp]
             getattr(L, name).restype = i
+        L.favor_draw_omega.argtypes = [fp, i, i, i, i, ctypes.c_ulonglong, vp]
+        L.favor_draw_omega.restype = i
         for name in ("favor_attn_decode", "favor_attn_decode_f32"):
             getattr(L, name).argtypes = [vp, vp, vp, fp, fp, fp] + [i] * 6 + [vp]
             getattr(L, name).restype = i
@@ -204,6 +207,11 @@ def favor_attn_decode(q, k, v, omega, state, out, B, H, d, dv, m, feature_map, s
 def favor_attn_decode_f32(q, k, v, omega, state, out, B, H, d, dv, m, feature_map, stream=None):
     return lib().favor_attn_decode_f32(_ptr(q), _ptr(k), _ptr(v), _ptr(omega), _ptr(state), _ptr(out),
                                        B, H, d, dv, m, int(feature_map), _stream(stream))
+
+
+def favor_draw_omega(omega, H, m, d, kind, seed, stream=None):
+    return lib().favor_draw_omega(_ptr(omega), int(H), int(m), int(d), int(kind), int(seed),
+                                  _stream(stream))
 
 
 def attention(q, k, v, omega, causal: bool, feature_map: int = FAVOR_MAP_POSITIVE,

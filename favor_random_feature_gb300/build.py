@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libfavor.so")
 INCLUDE = os.path.join(ROOT, "include")
-SOURCES = ["favor_abi.cu", "favor_simt.cu", "favor_tc.cu", "favor_noalloc.cu", "favor_decode.cu"]
+SOURCES = ["favor_abi.cu", "favor_simt.cu", "favor_tc.cu", "favor_noalloc.cu", "favor_decode.cu", "favor_omega.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 

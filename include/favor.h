@@ -185,6 +185,27 @@ int favor_attn_decode_f32(const float *q, const float *k, const float *v, const 
                           float *state, float *out, int B, int H, int d, int dv, int m,
                           int feature_map, cudaStream_t stream);
 
+/* ---- random projections drawn on the device --------------------------------
+ * omega [H][m][d] fp32 for the forward pass, drawn without a host round trip
+ * (a redraw per step or per layer).  The pages draw w ~ N(0, I_d) ("Performer:
+ * Unbiased Softmax Approximation") and name orthogonal random features as the
+ * lower-variance variant (Performer study notes); the generator is fixed here
+ * so that the draw is reproducible anywhere:
+ *   Philox4x64-10 (Salmon et al., "Parallel Random Numbers: As Easy as 1, 2,
+ *   3", SC 2011) under key (seed, 0); normal number e of stream s comes from
+ *   the block at counter (e / 4, s, 0, 0) by Box-Muller on word pairs
+ *   (x0, x1) and (x2, x3), u = (x / 2^11 + 1/2) 2^-53.
+ *   kind 0 (iid):        omega[h][i][j] = normal (h m + i) d + j of stream 0.
+ *   kind 1 (orthogonal): per head ceil(m/d) blocks; block b holds normals
+ *     ((h nb + b) d + i) d + j of stream 0, its rows are orthonormalised by
+ *     modified Gram-Schmidt in row order and row i is scaled by the norm of
+ *     normals ((h nb + b) d + i) d + t, t < d, of stream 1; the last block is
+ *     truncated.
+ * Computed in fp64, rounded to fp32 once.  d in {32, 64, 128}, m >= 1,
+ * H >= 1.  Asynchronous on `stream`; returns favor_status_t. */
+int favor_draw_omega(float *omega, int H, int m, int d, int kind, unsigned long long seed,
+                     cudaStream_t stream);
+
 /* Measurement hook (no counterpart on the pages): while enabled, every
  * forward call records a CUDA event pair on its stream around its dominant
  * kernel (the causal scan, or the non-causal output kernel), and every
