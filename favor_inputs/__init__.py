@@ -35,7 +35,10 @@ import numpy as np
 MAP_POSITIVE = 0
 MAP_TRIG = 1
 MAP_ELU1 = 2
-MAP_NAMES = {MAP_POSITIVE: "positive", MAP_TRIG: "trig", MAP_ELU1: "elu1"}
+MAP_RELU = 3
+MAP_TRIG_SOFTMAX = 4
+MAP_NAMES = {MAP_POSITIVE: "positive", MAP_TRIG: "trig", MAP_ELU1: "elu1", MAP_RELU: "relu",
+             MAP_TRIG_SOFTMAX: "trig_softmax"}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -55,10 +58,10 @@ class Workload:
 
     @property
     def r(self) -> int:
-        """Feature dimension: m (positive), 2m (trig), d (elu+1)."""
-        if self.feature_map == MAP_TRIG:
+        """Feature dimension: m (positive), 2m (trig, softmax-scaled trig), d (elu+1, relu)."""
+        if self.feature_map in (MAP_TRIG, MAP_TRIG_SOFTMAX):
             return 2 * self.m
-        if self.feature_map == MAP_ELU1:
+        if self.feature_map in (MAP_ELU1, MAP_RELU):
             return self.d
         return self.m
 
@@ -183,14 +186,14 @@ def make_inputs(w: Workload, L: int | None = None, B: int | None = None, H: int 
         v = rs.randn(L, w.dv).astype(np.float32).reshape(1, 1, L, w.dv)
         if B != 1 or H != 1:
             raise ValueError("the page's demo draw is a single head")
-        om = omega_page(w.m, w.d) if w.feature_map != MAP_ELU1 else None
+        om = omega_page(w.m, w.d) if w.feature_map not in (MAP_ELU1, MAP_RELU) else None
     else:
         rng = np.random.default_rng(w.seed)
         s = w.d ** -0.25
         q = rng.standard_normal((B, H, L, w.d), dtype=np.float32) * np.float32(s)
         k = rng.standard_normal((B, H, L, w.d), dtype=np.float32) * np.float32(s)
         v = rng.standard_normal((B, H, L, w.dv), dtype=np.float32)
-        if w.feature_map == MAP_ELU1:
+        if w.feature_map in (MAP_ELU1, MAP_RELU):
             om = None
         elif w.omega == "block_orth":
             om = omega_block_orthogonal(rng, H, w.m, w.d)

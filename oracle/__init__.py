@@ -25,7 +25,8 @@ _SRC = os.path.join(_HERE, "favor_oracle.c")
 _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 
-MAP_POSITIVE, MAP_TRIG, MAP_ELU1 = 0, 1, 2
+MAP_POSITIVE, MAP_TRIG, MAP_ELU1, MAP_RELU, MAP_TRIG_SOFTMAX = 0, 1, 2, 3, 4
+NO_OMEGA = (MAP_ELU1, MAP_RELU)   # elementwise maps: r = d, no projection
 
 _lib = None
 
@@ -89,7 +90,7 @@ def features(x, omega, feature_map: int = MAP_POSITIVE):
     lib = _load()
     x = np.ascontiguousarray(x, dtype=np.float64)
     n, d = x.shape
-    if feature_map == MAP_ELU1:
+    if feature_map in NO_OMEGA:
         om, m = None, d
     else:
         om = np.ascontiguousarray(omega, dtype=np.float64)
@@ -118,7 +119,7 @@ def forward(q, k, v, omega, causal: bool, feature_map: int = MAP_POSITIVE,
     B, H, L, d = q.shape
     dv = v.shape[-1]
     assert k.shape == q.shape and v.shape[:3] == q.shape[:3]
-    if feature_map == MAP_ELU1:
+    if feature_map in NO_OMEGA:
         om, m = None, d
     else:
         om = np.ascontiguousarray(omega, dtype=np.float64)
@@ -139,7 +140,7 @@ def forward(q, k, v, omega, causal: bool, feature_map: int = MAP_POSITIVE,
 
 
 def _omega_arg(omega, feature_map, H, d):
-    if feature_map == MAP_ELU1:
+    if feature_map in NO_OMEGA:
         return None, d
     om = np.ascontiguousarray(omega, dtype=np.float64)
     assert om.shape[0] == H and om.shape[2] == d

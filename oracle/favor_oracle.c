@@ -15,6 +15,13 @@
  *          -- "Kernel Feature Maps", section 3 "Random Fourier Features".
  *      elu1: phi(x)_j = x_j + 1 if x_j > 0, exp(x_j) otherwise  (r = d, no w)
  *          -- "Kernel Feature Maps", section 1 "ELU + 1".
+ *      relu: phi(x)_j = max(0, x_j)  (r = d, no w)
+ *          -- "Kernel Feature Maps", section 2 "ReLU".
+ *      softmax-scaled trig: exp(|x|^2/2) times the trig map, so that
+ *          E[phi(q).phi(k)] = exp(|q|^2/2 + |k|^2/2 - |q-k|^2/2) = exp(q.k)
+ *          -- "Kernel Feature Maps", section 3 (the remark that with an
+ *             additional scaling the Fourier features approximate the
+ *             softmax kernel; the scaling read as the Gaussian identity).
  *  - non-causal contraction (eps = 0):
  *      KV = phi(K)^T V,  z = sum_j phi(k_j),  out_i = phi(q_i)^T KV / phi(q_i)^T z
  *          -- "Performer: Unbiased Softmax Approximation", In[25] (the
@@ -57,12 +64,14 @@
 #define ORACLE_MAP_POSITIVE 0
 #define ORACLE_MAP_TRIG 1
 #define ORACLE_MAP_ELU1 2
+#define ORACLE_MAP_RELU 3
+#define ORACLE_MAP_TRIG_SOFTMAX 4
 
 /* feature count r for a map */
 int oracle_feature_dim(int map, int d, int m)
 {
-    if (map == ORACLE_MAP_TRIG) return 2 * m;
-    if (map == ORACLE_MAP_ELU1) return d;
+    if (map == ORACLE_MAP_TRIG || map == ORACLE_MAP_TRIG_SOFTMAX) return 2 * m;
+    if (map == ORACLE_MAP_ELU1 || map == ORACLE_MAP_RELU) return d;
     return m;
 }
 
@@ -83,6 +92,10 @@ int oracle_features(const double *x, const double *omega, int n, int d, int m,
             }
             continue;
         }
+        if (map == ORACLE_MAP_RELU) {
+            for (int j = 0; j < d; ++j) pt[j] = xt[j] > 0.0 ? xt[j] : 0.0;
+            continue;
+        }
         double norm2 = 0.0;
         for (int j = 0; j < d; ++j) norm2 += xt[j] * xt[j];
         double scale = 1.0 / sqrt((double)m);
@@ -97,6 +110,11 @@ int oracle_features(const double *x, const double *omega, int n, int d, int m,
             } else if (map == ORACLE_MAP_TRIG) {
                 pt[2 * i] = scale * sin(proj);
                 pt[2 * i + 1] = scale * cos(proj);
+            } else if (map == ORACLE_MAP_TRIG_SOFTMAX) {
+                if (norm2 / 2.0 >= 700.0) return -2;
+                const double g = exp(norm2 / 2.0) * scale;
+                pt[2 * i] = g * sin(proj);
+                pt[2 * i + 1] = g * cos(proj);
             } else {
                 return -1;
             }

@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 
 import oracle
-from favor_inputs import (CAUSAL8K, DEMO64, MAP_ELU1, MAP_POSITIVE, MAP_TRIG,
+from favor_inputs import (CAUSAL8K, DEMO64, MAP_ELU1, MAP_POSITIVE, MAP_RELU, MAP_TRIG, MAP_TRIG_SOFTMAX,
                           bf16_bits, bf16_to_f32, make_inputs,
                           omega_block_orthogonal, omega_iid)
 
@@ -118,18 +118,18 @@ def test_elu1_features_piecewise():
 # C2 / C7: brute-force O(L^2) attention with the explicit kernel matrix
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("fmap", [MAP_POSITIVE, MAP_TRIG, MAP_ELU1])
+@pytest.mark.parametrize("fmap", [MAP_POSITIVE, MAP_TRIG, MAP_ELU1, MAP_RELU, MAP_TRIG_SOFTMAX])
 def test_bruteforce_kernel_attention(causal, fmap):
     rng = np.random.default_rng(11 + fmap)
     H, L, d, dv, m = 2, 40, 16, 8, 32
     q = rng.standard_normal((1, H, L, d)) * d ** -0.25
     k = rng.standard_normal((1, H, L, d)) * d ** -0.25
     v = rng.standard_normal((1, H, L, dv))
-    if fmap == MAP_TRIG:
+    if fmap in (MAP_TRIG, MAP_TRIG_SOFTMAX):
         # small inputs keep the trig denominators well away from zero
         q *= 0.3
         k *= 0.3
-    om = rng.standard_normal((H, m, d)) if fmap != MAP_ELU1 else None
+    om = rng.standard_normal((H, m, d)) if fmap not in (MAP_ELU1, MAP_RELU) else None
     out = oracle.forward(q, k, v, om, causal=causal, feature_map=fmap)
     for h in range(H):
         A = np.empty((L, L))
@@ -139,6 +139,11 @@ def test_bruteforce_kernel_attention(causal, fmap):
                     A[i, j] = kernel_positive_closed(q[0, h, i], k[0, h, j], om[h])
                 elif fmap == MAP_TRIG:
                     A[i, j] = kernel_trig_closed(q[0, h, i], k[0, h, j], om[h])
+                elif fmap == MAP_TRIG_SOFTMAX:
+                    qi, kj = q[0, h, i], k[0, h, j]
+                    A[i, j] = math.exp((qi @ qi + kj @ kj) / 2) * kernel_trig_closed(qi, kj, om[h])
+                elif fmap == MAP_RELU:
+                    A[i, j] = np.maximum(q[0, h, i], 0) @ np.maximum(k[0, h, j], 0)
                 else:
                     fq = np.where(q[0, h, i] > 0, q[0, h, i] + 1.0, np.exp(q[0, h, i]))
                     fk = np.where(k[0, h, j] > 0, k[0, h, j] + 1.0, np.exp(k[0, h, j]))
@@ -526,3 +531,38 @@ def test_draw_omega_block_orthogonal(m, d):
             norms.extend(np.linalg.norm(got, axis=1))
     if len(norms) >= 100:
         assert stats.kstest(norms, stats.chi(d).cdf).pvalue > 1e-3
+
+
+# ---------------------------------------------------------------------------
+# ReLU ("Kernel Feature Maps" section 2) and the softmax-scaled Fourier map
+# (section 3's additional scaling)
+# ---------------------------------------------------------------------------
+def test_relu_features_and_homogeneity():
+    x = np.array([[-1.5, 0.0, 0.25, 3.0]])
+    assert np.array_equal(oracle.features(x, None, MAP_RELU), [[0.0, 0.0, 0.25, 3.0]])
+    # phi(c x) = c phi(x) for c > 0: scaling queries or keys leaves the output unchanged
+    rng = np.random.default_rng(41)
+    q, k = rng.standard_normal((1, 1, 30, 16)), rng.standard_normal((1, 1, 30, 16))
+    v = rng.standard_normal((1, 1, 30, 4))
+    for causal in (False, True):
+        a = oracle.forward(q, k, v, None, causal=causal, feature_map=MAP_RELU)
+        b = oracle.forward(2.5 * q, 0.5 * k, v, None, causal=causal, feature_map=MAP_RELU)
+        assert np.allclose(a, b, rtol=1e-12, atol=1e-14)
+
+
+def test_trig_softmax_closed_form_and_monte_carlo_softmax_kernel():
+    d, m = 8, 16
+    q, k = _qk_pair(d, 13, 0.25)
+    om = np.random.default_rng(14).standard_normal((m, d))
+    phi = oracle.features(np.stack([q, k]), om, MAP_TRIG_SOFTMAX)
+    closed = math.exp((q @ q + k @ k) / 2) * kernel_trig_closed(q, k, om)
+    assert abs(phi[0] @ phi[1] - closed) <= 1e-13 * abs(closed)
+    # unbiased for the softmax kernel exp(q.k): E = exp(|q|^2/2 + |k|^2/2) exp(-|q-k|^2/2);
+    # one feature pair's variance is that of the Gaussian-kernel estimate times exp(|q|^2+|k|^2)
+    T = 4000
+    est = _mc_estimates(q, k, m, T, 15, fmap=MAP_TRIG_SOFTMAX)
+    dl = (q - k) @ (q - k)
+    var1 = math.exp(q @ q + k @ k) * ((1 + math.exp(-2 * dl)) / 2 - math.exp(-dl))
+    se = math.sqrt(var1 / m / T)
+    assert abs(est.mean() - math.exp(q @ k)) <= 5 * se, (est.mean(), math.exp(q @ k), se)
+    assert abs(est.var(ddof=1) / (var1 / m) - 1.0) < 0.2
