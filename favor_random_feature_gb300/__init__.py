@@ -26,6 +26,8 @@ FAVOR_ERR_NOMEM = -5
 FAVOR_MAP_POSITIVE = 0
 FAVOR_MAP_TRIG = 1
 FAVOR_MAP_ELU1 = 2
+FAVOR_MAP_RELU = 3
+FAVOR_MAP_TRIG_SOFTMAX = 4
 
 EXPORTS = (
     "favor_attn_forward",
@@ -218,11 +220,11 @@ def attention(q, k, v, omega, causal: bool, feature_map: int = FAVOR_MAP_POSITIV
               out=None, stream=None):
     """Convenience wrapper on torch CUDA tensors: q, k [B,H,L,d] and v
     [B,H,L,dv] (bfloat16 or float32, the same dtype), omega [H,m,d] float32
-    (None for elu1).  Returns out [B,H,L,dv] float32."""
+    (None for elu1 and relu).  Returns out [B,H,L,dv] float32."""
     import torch
     B, H, L, d = q.shape
     dv = v.shape[-1]
-    m = d if feature_map == FAVOR_MAP_ELU1 else omega.shape[1]
+    m = d if feature_map in (FAVOR_MAP_ELU1, FAVOR_MAP_RELU) else omega.shape[1]
     if out is None:
         out = torch.empty((B, H, L, dv), dtype=torch.float32, device=q.device)
     if stream is None:

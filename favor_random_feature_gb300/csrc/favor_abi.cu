@@ -127,10 +127,10 @@ void stats_count_launch() {
 int make_problem(int B, int H, int L, int d, int dv, int m, int causal, int map, Problem *p) {
     if (B < 1 || H < 1 || L < 1) return FAVOR_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return FAVOR_ERR_INVALID_ARG;
-    if (map < FAVOR_MAP_POSITIVE || map > FAVOR_MAP_ELU1) return FAVOR_ERR_INVALID_ARG;
+    if (map < FAVOR_MAP_POSITIVE || map > FAVOR_MAP_TRIG_SOFTMAX) return FAVOR_ERR_INVALID_ARG;
     if (d != 32 && d != 64 && d != 128) return FAVOR_ERR_UNSUPPORTED;
     if (dv != 32 && dv != 64 && dv != 128) return FAVOR_ERR_UNSUPPORTED;
-    if (map == FAVOR_MAP_ELU1) {
+    if (map_is_elementwise(map)) {
         if (m != d) return FAVOR_ERR_INVALID_ARG;
     } else {
         if (m < 1) return FAVOR_ERR_INVALID_ARG;
@@ -143,8 +143,8 @@ int make_problem(int B, int H, int L, int d, int dv, int m, int causal, int map,
     p->causal = causal;
     p->map = map;
     p->BH = B * H;
-    p->nproj = map == FAVOR_MAP_ELU1 ? d : m;
-    p->r = map == FAVOR_MAP_TRIG ? 2 * m : (map == FAVOR_MAP_ELU1 ? d : m);
+    p->nproj = map_is_elementwise(map) ? d : m;
+    p->r = map_is_trig(map) ? 2 * m : (map_is_elementwise(map) ? d : m);
     return FAVOR_OK;
 }
 
@@ -159,7 +159,7 @@ int validate_args(const void *q, const void *k, const void *v, const float *omeg
     if ((rc = check_ptr(q, false)) || (rc = check_ptr(k, false)) || (rc = check_ptr(v, false)) ||
         (rc = check_ptr(out, false)))
         return rc;
-    if ((rc = check_ptr(omega, p.map == FAVOR_MAP_ELU1))) return rc;
+    if ((rc = check_ptr(omega, map_is_elementwise(p.map)))) return rc;
     size_t rows = (size_t)p.BH * p.L;
     size_t out_bytes = rows * p.dv * sizeof(float);
     if (overlaps(out, out_bytes, q, rows * p.d * esize) ||
@@ -176,8 +176,8 @@ using namespace favor;
 
 extern "C" int favor_feature_dim(int feature_map, int d, int m) {
     if (feature_map == FAVOR_MAP_POSITIVE) return m >= 1 ? m : -1;
-    if (feature_map == FAVOR_MAP_TRIG) return m >= 1 ? 2 * m : -1;
-    if (feature_map == FAVOR_MAP_ELU1) return (d >= 1 && m == d) ? d : -1;
+    if (map_is_trig(feature_map)) return m >= 1 ? 2 * m : -1;
+    if (map_is_elementwise(feature_map)) return (d >= 1 && m == d) ? d : -1;
     return -1;
 }
 
@@ -210,7 +210,7 @@ extern "C" int favor_attn_forward_host(const void *q, const void *k, const void 
     Problem p;
     int rc = make_problem(B, H, L, d, dv, m, causal, feature_map, &p);
     if (rc) return rc;
-    if (!q || !k || !v || !out || (!omega && feature_map != FAVOR_MAP_ELU1))
+    if (!q || !k || !v || !out || (!omega && !map_is_elementwise(feature_map)))
         return FAVOR_ERR_INVALID_ARG;
     const size_t rows = (size_t)p.BH * p.L;
     const size_t qb = rows * p.d * 2, vb = rows * p.dv * 2, ob = rows * p.dv * 4;
@@ -250,7 +250,7 @@ extern "C" int favor_feature_map(const void *x, const float *omega, float *phi, 
     if (rc) return rc;
     if ((rc = check_ptr(x, false)) || (rc = check_ptr(phi, false)) ||
         (rc = check_ptr(log_scale, false)) ||
-        (rc = check_ptr(omega, feature_map == FAVOR_MAP_ELU1)))
+        (rc = check_ptr(omega, map_is_elementwise(feature_map))))
         return rc;
     return simt_feature_map(x, true, omega, phi, log_scale, p, stream);
 }

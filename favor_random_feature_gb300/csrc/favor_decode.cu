@@ -212,8 +212,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_step(const DecodeArgs a) {
     // this thread's quarter of the projection row of tile n's feature
     auto load_w = [&](int n, float4 (&w)[NW4]) {
         const int f = tile_of(n) * kDecFt + fl;
-        if (a.map == FAVOR_MAP_ELU1 || f >= r) return;
-        const int p = a.map == FAVOR_MAP_TRIG ? f >> 1 : f;
+        if (map_is_elementwise(a.map) || f >= r) return;
+        const int p = map_is_trig(a.map) ? f >> 1 : f;
         const float4 *w4 =
             reinterpret_cast<const float4 *>(a.omega + ((size_t)(head_of(n) % a.H) * a.m + p) * D + s * DD);
 #pragma unroll
@@ -254,14 +254,14 @@ __global__ void __launch_bounds__(kDecThreads) decode_step(const DecodeArgs a) {
         const bool valid = ok && f < r;
         float dq = 0.f, dk = 0.f, ss = 0.f;
         if (ok) {
-            if (a.map == FAVOR_MAP_POSITIVE) {
+            if (a.map == FAVOR_MAP_POSITIVE || a.map == FAVOR_MAP_TRIG_SOFTMAX) {
 #pragma unroll
                 for (int i = 0; i < DD; ++i) {
                     const float x = load_in(xk, s * DD + i);
                     ss = fmaf(x, x, ss);
                 }
             }
-            if (a.map != FAVOR_MAP_ELU1 && valid) {
+            if (!map_is_elementwise(a.map) && valid) {
 #pragma unroll
                 for (int i = 0; i < NW4; ++i) {
                     const float4 w = wv[i];
@@ -285,17 +285,23 @@ __global__ void __launch_bounds__(kDecThreads) decode_step(const DecodeArgs a) {
         if (a.map == FAVOR_MAP_POSITIVE) {
             ek = kLog2e * (dk - 0.5f * ss) - half_log2m;
             eq = kLog2e * dq;
-        } else if (a.map == FAVOR_MAP_TRIG) {
+        } else if (map_is_trig(a.map)) {
             float sn, cs;
             sincosf(dk, &sn, &cs);
             pk = (f & 1) ? cs : sn;
             sincosf(dq, &sn, &cs);
             pq = (f & 1) ? cs : sn;
-            ek = -half_log2m;
+            // the softmax-scaled map carries exp(|k|^2/2) in the key's scale
+            ek = (a.map == FAVOR_MAP_TRIG_SOFTMAX ? 0.5f * kLog2e * ss : 0.f) - half_log2m;
         } else if (valid) {
             const float x = load_in(xk, f), y = load_in(xq, f);
-            pk = x > 0.f ? x + 1.f : expf(x);
-            pq = y > 0.f ? y + 1.f : expf(y);
+            if (a.map == FAVOR_MAP_RELU) {
+                pk = fmaxf(x, 0.f);
+                pq = fmaxf(y, 0.f);
+            } else {
+                pk = x > 0.f ? x + 1.f : expf(x);
+                pq = y > 0.f ? y + 1.f : expf(y);
+            }
         }
         float sq = -INFINITY, zn = 0.f;
         if (valid) {
@@ -518,7 +524,7 @@ int decode_state(const void *k, const void *v, bool bf16_in, const float *omega,
     }
     const size_t esize = bf16_in ? 2 : 4;
     if ((rc = check_ptr(k, false)) || (rc = check_ptr(v, false)) ||
-        (rc = check_ptr(omega, map == FAVOR_MAP_ELU1)))
+        (rc = check_ptr(omega, map_is_elementwise(map))))
         return rc;
     const size_t rows = (size_t)p.BH * p.L;
     if (overlaps(state, state_bytes, k, rows * p.d * esize) || overlaps(state, state_bytes, v, rows * p.dv * esize) ||
@@ -541,7 +547,7 @@ int decode_state(const void *k, const void *v, bool bf16_in, const float *omega,
         ea.nrt = (p.r + 127) / 128;
         ea.rstride = 4;
         ea.ref_scale = 1.f;
-        ea.rho_add = map == FAVOR_MAP_ELU1 ? 0.f : -0.5f * log2f((float)p.m);
+        ea.rho_add = map_is_elementwise(map) ? 0.f : -0.5f * log2f((float)p.m);
         ea.trig_tiles = map == FAVOR_MAP_TRIG;
     } else {
         const float *S, *hmax;
@@ -568,12 +574,12 @@ int decode_step_run(const void *q, const void *k, const void *v, bool bf16_in, c
     if (p.r > 1024) return FAVOR_ERR_UNSUPPORTED;
     if ((rc = check_ptr(q, false)) || (rc = check_ptr(k, false)) || (rc = check_ptr(v, false)) ||
         (rc = check_ptr(state, false)) || (rc = check_ptr(out, false)) ||
-        (rc = check_ptr(omega, map == FAVOR_MAP_ELU1)))
+        (rc = check_ptr(omega, map_is_elementwise(map))))
         return rc;
     const size_t esize = bf16_in ? 2 : 4;
     const size_t sb = (size_t)p.BH * p.r * (p.dv + 2) * sizeof(float), ob = (size_t)p.BH * p.dv * sizeof(float);
     const size_t xb = (size_t)p.BH * p.d * esize, vb = (size_t)p.BH * p.dv * esize;
-    const size_t wb = map == FAVOR_MAP_ELU1 ? 0 : (size_t)p.H * p.m * p.d * sizeof(float);
+    const size_t wb = map_is_elementwise(map) ? 0 : (size_t)p.H * p.m * p.d * sizeof(float);
     const void *ins[4] = {q, k, v, omega};
     const size_t inb[4] = {xb, xb, vb, wb};
     for (int i = 0; i < 4; ++i)

@@ -19,6 +19,11 @@ struct Problem {
     int BH;       // B * H
 };
 
+// elu1, relu: r = d features straight from x (no projection); trig and its
+// softmax-scaled form: 2m features, (sin, cos) per projection
+__host__ __device__ inline bool map_is_elementwise(int map) { return map == FAVOR_MAP_ELU1 || map == FAVOR_MAP_RELU; }
+__host__ __device__ inline bool map_is_trig(int map) { return map == FAVOR_MAP_TRIG || map == FAVOR_MAP_TRIG_SOFTMAX; }
+
 int make_problem(int B, int H, int L, int d, int dv, int m, int causal, int map, Problem *p);
 int check_ptr(const void *p, bool allow_null);
 

@@ -85,22 +85,33 @@ __global__ void simt_features(const T *__restrict__ x, const float *__restrict__
     const size_t row = (size_t)warp;
     const float *pr = P + row * nproj;
     float *fr = phi + row * r;
-    if (map == FAVOR_MAP_ELU1) {
+    if (map_is_elementwise(map)) {
         for (int n = lane; n < nproj; n += 32) {
             float t = pr[n];
-            fr[n] = t > 0.f ? t + 1.f : expf(t);
+            fr[n] = map == FAVOR_MAP_RELU ? fmaxf(t, 0.f) : (t > 0.f ? t + 1.f : expf(t));
         }
         if (lane == 0) logscale[row] = 0.f;
         return;
     }
-    if (map == FAVOR_MAP_TRIG) {
+    if (map_is_trig(map)) {
         for (int n = lane; n < nproj; n += 32) {
             float s, c;
             sincosf(pr[n], &s, &c);
             fr[2 * n] = s;
             fr[2 * n + 1] = c;
         }
-        if (lane == 0) logscale[row] = -0.5f * logf((float)m);
+        // the softmax-scaled map: exp(|x|^2/2) in the row's log-scale
+        float nrm = 0.f;
+        if (map == FAVOR_MAP_TRIG_SOFTMAX) {
+            const T *xr = x + row * d;
+            for (int j = lane; j < d; j += 32) {
+                float t = load_in(xr, j);
+                nrm = fmaf(t, t, nrm);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) nrm += __shfl_xor_sync(0xffffffffu, nrm, o);
+        }
+        if (lane == 0) logscale[row] = 0.5f * nrm - 0.5f * logf((float)m);
         return;
     }
     float mx = -INFINITY;
@@ -247,7 +258,7 @@ int features_into(const T *x, const float *omega, float *P, float *phi, float *l
                   const Problem &p, cudaStream_t st) {
     dim3 pg((p.L + 31) / 32, (p.nproj + 31) / 32, p.BH);
     simt_project<T><<<pg, 256, 0, st>>>(x, omega, P, p.H, p.L, p.d, p.nproj,
-                                        p.map == FAVOR_MAP_ELU1);
+                                        map_is_elementwise(p.map));
     FAVOR_LAUNCH_CHECK();
     long long rows = (long long)p.BH * p.L;
     simt_features<T><<<(unsigned)((rows * 32 + 255) / 256), 256, 0, st>>>(

@@ -1713,6 +1713,8 @@ int num_sms() {
 }  // namespace
 
 bool tc_supported(const Problem &p) {
+    // ReLU and the softmax-scaled Fourier map run on the SIMT kernels
+    if (p.map == FAVOR_MAP_RELU || p.map == FAVOR_MAP_TRIG_SOFTMAX) return false;
     if (p.d != 64 && p.d != 128) return false;
     if (p.dv != 64 && p.dv != 128) return false;
     if (p.r != 128 && p.r != 256) return false;

@@ -13,6 +13,16 @@
  *   ELU + 1
  *     phi(x)_j = x_j + 1 (x_j > 0), exp(x_j) (x_j <= 0), no projection     (r = d, m must equal d)
  *       -- "Kernel Feature Maps", section 1.
+ *   ReLU
+ *     phi(x)_j = max(0, x_j), no projection                                 (r = d, m must equal d)
+ *       -- "Kernel Feature Maps", section 2.  A query whose features meet no
+ *          key mass has a zero denominator: its row is 0/0 (NaN).
+ *   softmax-scaled random Fourier features
+ *     phi(x) = exp(|x|^2/2) x the sin/cos map above, so that
+ *     E[phi(q).phi(k)] = exp(q.k)                                             (r = 2m)
+ *       -- "Kernel Feature Maps", section 3 (the additional scaling that turns
+ *          the Gaussian-kernel estimate into a softmax-kernel estimate).
+ *   ReLU and the softmax-scaled map run on the fp32 SIMT kernels.
  *
  *   non-causal:  out_i = phi(q_i)^T (sum_j phi(k_j) v_j^T) / phi(q_i)^T (sum_j phi(k_j))
  *       -- Performer page In[25] (performer_attention, with eps = 0) and the
@@ -32,7 +42,8 @@
  *       v      [B][H][L][dv]
  *       omega  [H][m][d]  fp32, one random projection per head, shared by the
  *              batch (rows w_i; drawn by the caller, iid N(0,I) or
- *              block-orthogonal).  Ignored (may be NULL) for FAVOR_MAP_ELU1.
+ *              block-orthogonal).  Ignored (may be NULL) for FAVOR_MAP_ELU1 and
+ *              FAVOR_MAP_RELU.
  *       out    [B][H][L][dv] fp32.
  *   - Device pointers must be 16-byte aligned; out must not alias an input.
  *   - The caller owns every buffer and the stream.  The library owns a
@@ -45,7 +56,7 @@
  *     bounded number of polls and record FAVOR_ERR_TIMEOUT in a device status
  *     word that favor_get_device_status() reads.
  *   - Supported: B, H, L >= 1; d, dv in {32, 64, 128}; m >= 1 and m % 16 == 0
- *     (positive, trig); m == d (elu1).  B*H*L*max(d,dv) must fit in int32
+ *     (positive, trig, softmax-scaled trig); m == d (elu1, relu).  B*H*L*max(d,dv) must fit in int32
  *     element offsets per tensor (checked).
  */
 #ifndef FAVOR_H
@@ -67,9 +78,12 @@ typedef enum {
 } favor_status_t;
 
 typedef enum {
-    FAVOR_MAP_POSITIVE = 0, /* FAVOR+ positive random features, r = m  */
-    FAVOR_MAP_TRIG = 1,     /* sin/cos random Fourier features, r = 2m */
-    FAVOR_MAP_ELU1 = 2      /* elu(x) + 1, r = d (m must equal d)      */
+    FAVOR_MAP_POSITIVE = 0,     /* FAVOR+ positive random features, r = m            */
+    FAVOR_MAP_TRIG = 1,         /* sin/cos random Fourier features, r = 2m           */
+    FAVOR_MAP_ELU1 = 2,         /* elu(x) + 1, r = d (m must equal d)                */
+    FAVOR_MAP_RELU = 3,         /* max(0, x), r = d (m must equal d)                 */
+    FAVOR_MAP_TRIG_SOFTMAX = 4  /* exp(|x|^2/2) x the sin/cos map, r = 2m: unbiased
+                                   for the softmax kernel exp(q.k)                   */
 } favor_feature_map_t;
 
 /* FAVOR attention forward, bf16 q/k/v (raw bf16 bit patterns), fp32 omega

@@ -4,7 +4,9 @@ against the float64 oracle."""
 import numpy as np
 
 import favor_random_feature_gb300 as fv
-from favor_inputs import MAP_ELU1, MAP_TRIG
+from favor_inputs import MAP_ELU1, MAP_RELU, MAP_TRIG, MAP_TRIG_SOFTMAX
+
+NO_OMEGA = (MAP_ELU1, MAP_RELU)
 
 
 def to_device(inp):
@@ -16,7 +18,7 @@ def to_device(inp):
     else:
         conv = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
     om = None
-    if inp.omega is not None and w.feature_map != MAP_ELU1:
+    if inp.omega is not None and w.feature_map not in NO_OMEGA:
         om = torch.from_numpy(np.ascontiguousarray(inp.omega, dtype=np.float32)).cuda()
     return conv(inp.q), conv(inp.k), conv(inp.v), om
 
@@ -27,7 +29,7 @@ def run_gpu(inp, causal, feature_map, entry=None):
     w = inp.w
     q, k, v, om = to_device(inp)
     out = torch.full((w.B, w.H, w.L, w.dv), float("nan"), dtype=torch.float32, device="cuda")
-    m = w.d if feature_map == MAP_ELU1 else w.m
+    m = w.d if feature_map in NO_OMEGA else w.m
     if entry is None:
         entry = fv.favor_attn_forward if w.dtype == "bf16" else fv.favor_attn_forward_f32
     stream = torch.cuda.current_stream()
@@ -40,7 +42,7 @@ def run_gpu(inp, causal, feature_map, entry=None):
 
 def oracle_ref(inp, causal, feature_map, heads=None, return_den=False):
     import oracle
-    om = None if feature_map == MAP_ELU1 else inp.omega
+    om = None if feature_map in NO_OMEGA else inp.omega
     return oracle.forward(inp.q32, inp.k32, inp.v32, om, causal=causal,
                           feature_map=feature_map, heads=heads, return_den=return_den)
 
@@ -55,7 +57,7 @@ def row_errors(out, ref):
     return np.linalg.norm(out - ref, axis=1) / np.linalg.norm(ref, axis=1)
 
 
-def trig_condition(inp, heads=None):
+def trig_condition(inp, heads=None, fmap=MAP_TRIG):
     """kappa_i = (|phi(q_i)|^T sum_j |phi(k_j)|) / |phi(q_i)^T z| for the trig map
     (non-causal sums), used to select well-conditioned rows."""
     import oracle
@@ -66,13 +68,13 @@ def trig_condition(inp, heads=None):
     kap = np.full((BH, w.L), np.inf)
     for bh in (range(BH) if heads is None else heads):
         om = inp.omega[bh % w.H]
-        pq = oracle.features(q[bh], om, MAP_TRIG)
-        pk = oracle.features(k[bh], om, MAP_TRIG)
+        pq = oracle.features(q[bh], om, fmap)
+        pk = oracle.features(k[bh], om, fmap)
         kap[bh] = (np.abs(pq) @ np.abs(pk).sum(0)) / np.abs(pq @ pk.sum(0))
     return kap.reshape(w.B, w.H, w.L)
 
 
-def causal_trig_condition(inp, heads=None):
+def causal_trig_condition(inp, heads=None, fmap=MAP_TRIG):
     import oracle
     w = inp.w
     BH = w.B * w.H
@@ -81,8 +83,8 @@ def causal_trig_condition(inp, heads=None):
     kap = np.full((BH, w.L), np.inf)
     for bh in (range(BH) if heads is None else heads):
         om = inp.omega[bh % w.H]
-        pq = oracle.features(q[bh], om, MAP_TRIG)
-        pk = oracle.features(k[bh], om, MAP_TRIG)
+        pq = oracle.features(q[bh], om, fmap)
+        pk = oracle.features(k[bh], om, fmap)
         zabs = np.cumsum(np.abs(pk), axis=0)
         z = np.cumsum(pk, axis=0)
         kap[bh] = np.sum(np.abs(pq) * zabs, axis=1) / np.abs(np.sum(pq * z, axis=1))

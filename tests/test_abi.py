@@ -46,6 +46,10 @@ def test_feature_dim(lib):
     assert fv.favor_feature_dim(fv.FAVOR_MAP_ELU1, 64, 64) == 64
     assert fv.favor_feature_dim(fv.FAVOR_MAP_ELU1, 64, 32) == -1
     assert fv.favor_feature_dim(7, 64, 64) == -1
+    assert fv.favor_feature_dim(fv.FAVOR_MAP_RELU, 64, 64) == 64
+    assert fv.favor_feature_dim(fv.FAVOR_MAP_RELU, 64, 128) == -1
+    assert fv.favor_feature_dim(fv.FAVOR_MAP_TRIG_SOFTMAX, 64, 256) == 512
+    assert fv.favor_feature_dim(5, 64, 64) == -1
 
 
 # Fake, 16-byte aligned addresses: validation must reject these calls before

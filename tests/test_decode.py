@@ -12,7 +12,10 @@ import numpy as np
 import pytest
 
 import favor_random_feature_gb300 as fv
-from favor_inputs import CAUSAL8K, DEMO64, LONG64K, MAP_ELU1, MAP_POSITIVE, MAP_TRIG, make_inputs
+from favor_inputs import (CAUSAL8K, DEMO64, LONG64K, MAP_ELU1, MAP_POSITIVE, MAP_RELU, MAP_TRIG,
+                          MAP_TRIG_SOFTMAX, make_inputs)
+
+NO_OMEGA = (MAP_ELU1, MAP_RELU)
 from parity_util import row_errors
 
 F32_MAX = 1e-4
@@ -105,10 +108,10 @@ def _run(inp, L0, T, fmap, use_f32=False):
     w = inp.w
     bf16 = w.dtype == "bf16" and not use_f32
     src_q, src_k, src_v = (inp.q, inp.k, inp.v) if bf16 else (inp.q32, inp.k32, inp.v32)
-    m = w.d if fmap == MAP_ELU1 else w.m
+    m = w.d if fmap in NO_OMEGA else w.m
     r = fv.favor_feature_dim(fmap, w.d, m)
     per = fv.favor_state_floats(w.d, w.dv, m, fmap)
-    om = None if fmap == MAP_ELU1 else torch.from_numpy(
+    om = None if fmap in NO_OMEGA else torch.from_numpy(
         np.ascontiguousarray(inp.omega, dtype=np.float32)).cuda()
     stream = torch.cuda.current_stream()
     state = torch.full((w.B, w.H, per), float("nan"), dtype=torch.float32, device="cuda")
@@ -139,7 +142,7 @@ def _run(inp, L0, T, fmap, use_f32=False):
 
 def _oracle_state(inp, L0, fmap):
     import oracle
-    om = None if fmap == MAP_ELU1 else inp.omega
+    om = None if fmap in NO_OMEGA else inp.omega
     return oracle.state(inp.k32[:, :, :L0], inp.v32[:, :, :L0], om, feature_map=fmap)
 
 
@@ -154,7 +157,7 @@ def _state_err(got, ref):
 
 def _decode_ref(inp, L, fmap, heads=None):
     import oracle
-    om = None if fmap == MAP_ELU1 else inp.omega
+    om = None if fmap in NO_OMEGA else inp.omega
     return oracle.forward(inp.q32[:, :, :L], inp.k32[:, :, :L], inp.v32[:, :, :L], om, causal=True,
                           feature_map=fmap, heads=heads)
 
@@ -166,29 +169,32 @@ CASES = [   # (workload, feature map, m or None, L0, T)
     (CAUSAL8K.with_(d=128, dv=32), MAP_ELU1, None, 200, 4),
     (LONG64K, MAP_POSITIVE, 768, 130, 3),        # r > 512: 128-feature tiles
     (CAUSAL8K, MAP_TRIG, 256, 129, 3),           # r = 512: a cluster of 8
+    (CAUSAL8K, MAP_RELU, None, 200, 4),
+    (CAUSAL8K.with_(omega="iid"), MAP_TRIG_SOFTMAX, 64, 150, 3),
 ]
 
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("w,fmap,m,L0,T", CASES,
-                         ids=["pos", "pos_dv128", "trig_r256", "elu_d128", "pos_r768", "trig_r512"])
+                         ids=["pos", "pos_dv128", "trig_r256", "elu_d128", "pos_r768", "trig_r512", "relu",
+                              "trig_softmax"])
 @pytest.mark.parametrize("f32", [False, True], ids=["bf16", "f32"])
 def test_state_then_decode(w, fmap, m, L0, T, f32):
     w = w.with_(feature_map=fmap, **({"m": m} if m else {}))
-    if fmap == MAP_ELU1:
-        w = w.with_(m=w.d)
+    if fmap in NO_OMEGA:
+        w = w.with_(m=w.d, omega="iid")
     inp = make_inputs(w, L=L0 + T, B=2, H=3)
     got_state, got = _run(inp, L0, T, fmap, use_f32=f32)
     es = _state_err(got_state, _oracle_state(inp, L0, fmap))
     assert es.max() <= (STATE_F32 if f32 else STATE_BF16), es.max()
     assert np.isfinite(got_state[2]).all()
     ref = _decode_ref(inp, L0 + T, fmap)[:, :, L0:]
-    if fmap == MAP_TRIG:
+    if fmap in (MAP_TRIG, MAP_TRIG_SOFTMAX):
         # trig denominators are not bounded away from zero (after a few
         # hundred keys every row is ill conditioned): the error of each row
         # is taken relative to its condition number, as for the forward pass
         from parity_util import causal_trig_condition, conditioned_errors
-        kappa = causal_trig_condition(inp)[:, :, L0:]
+        kappa = causal_trig_condition(inp, fmap=fmap)[:, :, L0:]
         e = conditioned_errors(got, ref, kappa, inp.v32)
     else:
         e = row_errors(got, ref)

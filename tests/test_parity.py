@@ -13,7 +13,8 @@ parity_util.conditioned_errors).
 import numpy as np
 import pytest
 
-from favor_inputs import (CAUSAL8K, DEMO64, LONG64K, MAP_ELU1, MAP_POSITIVE, MAP_TRIG, NC4096,
+from favor_inputs import (CAUSAL8K, DEMO64, LONG64K, MAP_ELU1, MAP_POSITIVE, MAP_RELU, MAP_TRIG,
+                          MAP_TRIG_SOFTMAX, NC4096,
                           SWEEP16K, make_inputs, sweep_variants)
 from parity_util import (causal_trig_condition, conditioned_errors, oracle_ref, row_errors,
                          run_gpu, scaled_inputs, to_device, trig_condition)
@@ -283,3 +284,25 @@ def test_back_to_back_calls(w, causal):
     st = fv.favor_get_device_status(stream)
     assert st == fv.FAVOR_OK, fv.strerror(st)
     assert torch.equal(outs[0], outs[1])
+
+
+# ---------------------------------------------------------------------------
+# ReLU and the softmax-scaled Fourier map (fp32 SIMT kernels for both entry
+# points): fp32 arithmetic on the inputs' values, so the fp32 bar applies to
+# both; the softmax-scaled map's denominators are not bounded away from zero,
+# so its error is taken relative to each row's condition number
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("fmap", [MAP_RELU, MAP_TRIG_SOFTMAX], ids=["relu", "trig_softmax"])
+def test_relu_and_softmax_scaled_trig(fmap, causal, dtype):
+    w = NC4096.with_(feature_map=fmap, omega="iid", dtype=dtype, m=64 if fmap == MAP_RELU else 128)
+    inp = make_inputs(w, L=333, B=2, H=3)
+    out = run_gpu(inp, causal, fmap)
+    ref = oracle_ref(inp, causal, fmap)
+    if fmap == MAP_TRIG_SOFTMAX:
+        cond = causal_trig_condition if causal else trig_condition
+        e = conditioned_errors(out, ref, cond(inp, fmap=fmap), inp.v32)
+    else:
+        e = row_errors(out, ref)
+    assert e.max() <= F32_MAX, e.max()
