@@ -35,14 +35,19 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM traffic (read + write bytes per launch) of a kernel from one ncu capture
 # (profiles/), valid while the kernel's source section is unchanged.
 TRAFFIC = {
-    ("tc_causal", "causal8k"): (303.83e6, "23a98b06ba6794c3"),
-    ("tc_output", "nc4096"): (103.58e6, "0999d582224720a0"),
-    ("tc_state", "causal8k"): (68.87e6, "dd7629c5daf0e3da"),
+    ("tc_causal", "causal8k"): (308.40e6, "736dfb285b43d884"),
+    ("tc_state", "causal8k"): (69.16e6, "be3b5bfdadbd00d1"),
+    ("tc_state", "nc4096"): (105.01e6, "be3b5bfdadbd00d1"),
+    ("tc_output", "nc4096"): (103.15e6, "0d1f15dd5f60a63d"),
+    ("decode_step", "decode_b256"): (496.87e6, "74c42f3d2b49b28e"),
 }
-KERNEL_SECTIONS = {
-    "tc_causal": ("// tc_causal: the chunked causal scan, warp-specialised.", "// tc_output: non-causal rows"),
-    "tc_output": ("// tc_output: non-causal rows", "// host side"),
-    "tc_state": ("// tc_state: per (feature group, piece, head) the state of a run of keys", "// tc_combine:"),
+KERNEL_SECTIONS = {   # kernel: (source file, first line of its section, first line after it)
+    "tc_causal": ("favor_tc.cu", "// tc_causal: the chunked causal scan, warp-specialised.",
+                  "// tc_output: non-causal rows"),
+    "tc_output": ("favor_tc.cu", "// tc_output: non-causal rows", "// host side"),
+    "tc_state": ("favor_tc.cu", "// tc_state: per (feature group, piece, head) the state of a run of keys",
+                 "// tc_combine:"),
+    "decode_step": ("favor_decode.cu", "// decode_step: persistent CTAs", "bool overlaps("),
 }
 
 
@@ -50,8 +55,8 @@ def kernel_source_hash(kernel):
     import hashlib
     if kernel not in KERNEL_SECTIONS:
         return None
-    a, b = KERNEL_SECTIONS[kernel]
-    path = os.path.join(ROOT, "favor_random_feature_gb300", "csrc", "favor_tc.cu")
+    f, a, b = KERNEL_SECTIONS[kernel]
+    path = os.path.join(ROOT, "favor_random_feature_gb300", "csrc", f)
     try:
         s = open(path).read()
         return hashlib.sha256(s[s.index(a):s.index(b)].encode()).hexdigest()[:16]
