@@ -72,6 +72,8 @@ def _load():
         lib.oracle_normal.restype = ctypes.c_double
         lib.oracle_draw_omega.argtypes = [P] + [ctypes.c_int] * 4 + [U64]
         lib.oracle_draw_omega.restype = ctypes.c_int
+        lib.oracle_backward.argtypes = [P] * 9 + [ctypes.c_int] * 8
+        lib.oracle_backward.restype = ctypes.c_int
         lib.oracle_feature_dim.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -215,6 +217,30 @@ def draw_omega(H: int, m: int, d: int, kind: int, seed: int):
     if rc:
         raise ValueError(f"oracle_draw_omega failed ({rc})")
     return out
+
+
+def backward(q, k, v, omega, g, causal: bool, feature_map: int = MAP_POSITIVE):
+    """Gradients of a loss with dloss/dout = g through the forward pass:
+    returns (dq, dk, dv, dw) float64; dw [H][m][d] is summed over the batch
+    (None for the elementwise maps)."""
+    lib = _load()
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    k = np.ascontiguousarray(k, dtype=np.float64)
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    g = np.ascontiguousarray(g, dtype=np.float64)
+    B, H, L, d = q.shape
+    dv_ = v.shape[-1]
+    assert k.shape == q.shape and v.shape[:3] == q.shape[:3] and g.shape == v.shape
+    om, m = _omega_arg(omega, feature_map, H, d)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    dw = None if om is None else np.zeros((H, m, d), dtype=np.float64)
+    rc = lib.oracle_backward(_dp(q), _dp(k), _dp(v), _dp(om), _dp(g), _dp(dq), _dp(dk), _dp(dv), _dp(dw),
+                             B, H, L, d, dv_, m, int(bool(causal)), feature_map)
+    if rc:
+        raise FloatingPointError(f"oracle_backward failed ({rc})")
+    return dq, dk, dv, dw
 
 
 def threads_used() -> int:

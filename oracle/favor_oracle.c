@@ -52,6 +52,15 @@
  *        and scaled by the norm of an independent N(0, I_d) vector, the last
  *        block truncated (the orthogonal random features the Performer study
  *        notes name, read as in the block construction).
+ *  - the backward pass of the forward above (gradients of a loss given
+ *    g = dloss/dout), the reverse sweep of the prefix sums the Performer study
+ *    notes ask for ("Case 2"; the prefix sums accumulated in reverse):
+ *      dnum_i = g_i / den_i,  dden_i = -(g_i . out_i) / den_i
+ *      dphi(q_i) = S_i dnum_i + z_i dden_i             (S_i, z_i as above)
+ *      R_j = sum_{i >= j} phi(q_i) dnum_i^T,  rho_j = sum_{i >= j} phi(q_i) dden_i
+ *      dphi(k_j) = R_j v_j + rho_j,  dv_j = R_j^T phi(k_j)
+ *    (non-causal: S, z, R, rho over all rows), then through each feature
+ *    map's derivative to dq, dk and dw (w shared by the batch: summed).
  *
  * No stabiliser, no blocking, no reordering: every value is the definition
  * evaluated in float64.  Exponents are checked against |t| < 700.
@@ -360,4 +369,179 @@ int oracle_draw_omega(double *omega, int H, int m, int d, int kind, uint64_t see
         }
     free(G);
     return 0;
+}
+
+/* ---- backward ------------------------------------------------------------ */
+
+/* dphi (r values) -> dx (d values) for one vector x; dw [m][d] += the
+ * projection rows' gradient.  Feature derivatives:
+ *   positive:  dphi_i/dx = phi_i (w_i - x),  dphi_i/dw_i = phi_i x
+ *   trig:      phi_{2i} = sin(a)/sqrt(m), phi_{2i+1} = cos(a)/sqrt(m), a = w_i.x
+ *   softmax-scaled trig: exp(|x|^2/2) times trig: adds x (sum_f dphi_f phi_f)
+ *   elu1:      1 (x > 0), exp(x);   relu: 1 (x > 0), 0 */
+static int feature_backward(const double *x, const double *omega, const double *dphi, double *dx,
+                            double *dw, int d, int m, int map)
+{
+    int r = oracle_feature_dim(map, d, m);
+    double *phi = (double *)malloc(sizeof(double) * (size_t)r);
+    if (!phi) return -3;
+    int rc = oracle_features(x, omega, 1, d, m, map, phi);
+    if (rc) { free(phi); return rc; }
+    for (int j = 0; j < d; ++j) dx[j] = 0.0;
+    if (map == ORACLE_MAP_ELU1 || map == ORACLE_MAP_RELU) {
+        for (int j = 0; j < d; ++j) {
+            double der = x[j] > 0.0 ? 1.0 : (map == ORACLE_MAP_ELU1 ? exp(x[j]) : 0.0);
+            dx[j] = dphi[j] * der;
+        }
+        free(phi);
+        return 0;
+    }
+    if (map == ORACLE_MAP_POSITIVE) {
+        double tot = 0.0;
+        for (int i = 0; i < m; ++i) {
+            double c = dphi[i] * phi[i];
+            tot += c;
+            const double *wi = omega + (size_t)i * d;
+            for (int j = 0; j < d; ++j) {
+                dx[j] += c * wi[j];
+                dw[(size_t)i * d + j] += c * x[j];
+            }
+        }
+        for (int j = 0; j < d; ++j) dx[j] -= tot * x[j];
+        free(phi);
+        return 0;
+    }
+    /* trig and its softmax-scaled form: phi = s [sin a_i, cos a_i] with
+     * s = 1/sqrt(m) (times exp(|x|^2/2) when scaled) */
+    double norm2 = 0.0;
+    for (int j = 0; j < d; ++j) norm2 += x[j] * x[j];
+    double s = 1.0 / sqrt((double)m);
+    if (map == ORACLE_MAP_TRIG_SOFTMAX) s *= exp(norm2 / 2.0);
+    double tot = 0.0;
+    for (int i = 0; i < m; ++i) {
+        const double *wi = omega + (size_t)i * d;
+        double a = 0.0;
+        for (int j = 0; j < d; ++j) a += wi[j] * x[j];
+        double c = s * (dphi[2 * i] * cos(a) - dphi[2 * i + 1] * sin(a));
+        tot += dphi[2 * i] * phi[2 * i] + dphi[2 * i + 1] * phi[2 * i + 1];
+        for (int j = 0; j < d; ++j) {
+            dx[j] += c * wi[j];
+            dw[(size_t)i * d + j] += c * x[j];
+        }
+    }
+    if (map == ORACLE_MAP_TRIG_SOFTMAX)
+        for (int j = 0; j < d; ++j) dx[j] += tot * x[j];
+    free(phi);
+    return 0;
+}
+
+/* One head: gradients dq, dk [L][d], dv [L][dv] and dw [m][d] (accumulated). */
+static int oracle_head_backward(const double *q, const double *k, const double *v, const double *omega,
+                                const double *g, double *dq, double *dk, double *dv, double *dw,
+                                int L, int d, int dvd, int m, int causal, int map)
+{
+    int r = oracle_feature_dim(map, d, m);
+    double *pk = (double *)malloc(sizeof(double) * (size_t)L * r);
+    double *pq = (double *)malloc(sizeof(double) * (size_t)L * r);
+    double *S = (double *)calloc((size_t)r * dvd, sizeof(double));
+    double *z = (double *)calloc((size_t)r, sizeof(double));
+    double *dnum = (double *)malloc(sizeof(double) * (size_t)L * dvd);
+    double *dden = (double *)malloc(sizeof(double) * (size_t)L);
+    double *dphi = (double *)malloc(sizeof(double) * (size_t)r);
+    double *R = (double *)calloc((size_t)r * dvd, sizeof(double));
+    double *rho = (double *)calloc((size_t)r, sizeof(double));
+    int rc = 0;
+    if (!pk || !pq || !S || !z || !dnum || !dden || !dphi || !R || !rho) { rc = -3; goto done; }
+    if ((rc = oracle_features(k, omega, L, d, m, map, pk))) goto done;
+    if ((rc = oracle_features(q, omega, L, d, m, map, pq))) goto done;
+    if (!causal)
+        for (int j = 0; j < L; ++j)
+            for (int f = 0; f < r; ++f) {
+                for (int c = 0; c < dvd; ++c) S[(size_t)f * dvd + c] += pk[(size_t)j * r + f] * v[(size_t)j * dvd + c];
+                z[f] += pk[(size_t)j * r + f];
+            }
+    /* forward sweep: out_i, dnum_i, dden_i and dphi(q_i) */
+    for (int i = 0; i < L; ++i) {
+        if (causal)
+            for (int f = 0; f < r; ++f) {
+                for (int c = 0; c < dvd; ++c) S[(size_t)f * dvd + c] += pk[(size_t)i * r + f] * v[(size_t)i * dvd + c];
+                z[f] += pk[(size_t)i * r + f];
+            }
+        const double *ph = pq + (size_t)i * r;
+        double den = 0.0;
+        for (int f = 0; f < r; ++f) den += ph[f] * z[f];
+        double gdo = 0.0;
+        for (int c = 0; c < dvd; ++c) {
+            double num = 0.0;
+            for (int f = 0; f < r; ++f) num += ph[f] * S[(size_t)f * dvd + c];
+            gdo += g[(size_t)i * dvd + c] * (num / den);
+            dnum[(size_t)i * dvd + c] = g[(size_t)i * dvd + c] / den;
+        }
+        dden[i] = -gdo / den;
+        for (int f = 0; f < r; ++f) {
+            double acc = z[f] * dden[i];
+            for (int c = 0; c < dvd; ++c) acc += S[(size_t)f * dvd + c] * dnum[(size_t)i * dvd + c];
+            dphi[f] = acc;
+        }
+        if ((rc = feature_backward(q + (size_t)i * d, omega, dphi, dq + (size_t)i * d, dw, d, m, map))) goto done;
+    }
+    /* reverse sweep: R_j, rho_j; dphi(k_j) and dv_j */
+    if (!causal)
+        for (int i = 0; i < L; ++i)
+            for (int f = 0; f < r; ++f) {
+                for (int c = 0; c < dvd; ++c) R[(size_t)f * dvd + c] += pq[(size_t)i * r + f] * dnum[(size_t)i * dvd + c];
+                rho[f] += pq[(size_t)i * r + f] * dden[i];
+            }
+    for (int j = L - 1; j >= 0; --j) {
+        if (causal)
+            for (int f = 0; f < r; ++f) {
+                for (int c = 0; c < dvd; ++c) R[(size_t)f * dvd + c] += pq[(size_t)j * r + f] * dnum[(size_t)j * dvd + c];
+                rho[f] += pq[(size_t)j * r + f] * dden[j];
+            }
+        for (int f = 0; f < r; ++f) {
+            double acc = rho[f];
+            for (int c = 0; c < dvd; ++c) acc += R[(size_t)f * dvd + c] * v[(size_t)j * dvd + c];
+            dphi[f] = acc;
+        }
+        for (int c = 0; c < dvd; ++c) {
+            double acc = 0.0;
+            for (int f = 0; f < r; ++f) acc += R[(size_t)f * dvd + c] * pk[(size_t)j * r + f];
+            dv[(size_t)j * dvd + c] = acc;
+        }
+        if ((rc = feature_backward(k + (size_t)j * d, omega, dphi, dk + (size_t)j * d, dw, d, m, map))) goto done;
+    }
+done:
+    free(pk); free(pq); free(S); free(z); free(dnum); free(dden); free(dphi); free(R); free(rho);
+    return rc;
+}
+
+/* Backward over B*H heads: g [B][H][L][dv] -> dq, dk [B][H][L][d],
+ * dv [B][H][L][dv], dw [H][m][d] (summed over the batch; may be NULL for the
+ * elementwise maps). */
+int oracle_backward(const double *q, const double *k, const double *v, const double *omega,
+                    const double *g, double *dq, double *dk, double *dv, double *dw,
+                    int B, int H, int L, int d, int dvd, int m, int causal, int map)
+{
+    int status = 0;
+    const int has_w = !(map == ORACLE_MAP_ELU1 || map == ORACLE_MAP_RELU);
+    if (has_w) memset(dw, 0, sizeof(double) * (size_t)H * m * d);
+    /* heads of one h share dw: parallel over h, sequential over b */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int h = 0; h < H; ++h) {
+        double *dwh = has_w ? dw + (size_t)h * m * d : NULL;
+        double *scratch = has_w ? NULL : (double *)calloc((size_t)m * d, sizeof(double));
+        for (int b = 0; b < B; ++b) {
+            size_t bh = (size_t)b * H + h;
+            size_t xo = bh * L * d, vo = bh * L * dvd;
+            const double *om = has_w ? omega + (size_t)h * m * d : NULL;
+            int rc = oracle_head_backward(q + xo, k + xo, v + vo, om, g + vo, dq + xo, dk + xo, dv + vo,
+                                          has_w ? dwh : scratch, L, d, dvd, m, causal, map);
+            if (rc) {
+#pragma omp critical
+                { if (!status) status = rc; }
+            }
+        }
+        free(scratch);
+    }
+    return status;
 }

@@ -566,3 +566,55 @@ def test_trig_softmax_closed_form_and_monte_carlo_softmax_kernel():
     se = math.sqrt(var1 / m / T)
     assert abs(est.mean() - math.exp(q @ k)) <= 5 * se, (est.mean(), math.exp(q @ k), se)
     assert abs(est.var(ddof=1) / (var1 / m) - 1.0) < 0.2
+
+
+# ---------------------------------------------------------------------------
+# backward pass: central finite differences of the forward pass (float64) on
+# sampled entries of every input, for every map, causal and not
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("fmap", [MAP_POSITIVE, MAP_TRIG, MAP_ELU1, MAP_RELU, MAP_TRIG_SOFTMAX])
+def test_backward_matches_finite_differences(causal, fmap):
+    rs = np.random.default_rng(51 + fmap)
+    B, H, L, d, dv, m = 2, 2, 9, 8, 5, 12
+    scale = 0.3 if fmap in (MAP_TRIG, MAP_TRIG_SOFTMAX) else 0.5
+    q = rs.standard_normal((B, H, L, d)) * scale
+    k = rs.standard_normal((B, H, L, d)) * scale
+    if fmap == MAP_RELU:
+        # keep every query's features in touch with some key mass, and away
+        # from the kink at 0 where the derivative jumps
+        q, k = np.abs(q) + 0.05, np.abs(k) + 0.05
+        q[..., ::3] *= -1
+    v = rs.standard_normal((B, H, L, dv))
+    g = rs.standard_normal((B, H, L, dv))
+    om = None if fmap in (MAP_ELU1, MAP_RELU) else rs.standard_normal((H, m, d))
+    dq, dk, dv_, dw = oracle.backward(q, k, v, om, g, causal, fmap)
+
+    def loss(q_, k_, v_, om_):
+        return float(np.sum(oracle.forward(q_, k_, v_, om_, causal=causal, feature_map=fmap) * g))
+
+    h = 1e-6
+    tensors = [("q", q, dq), ("k", k, dk), ("v", v, dv_)] + ([("w", om, dw)] if om is not None else [])
+    for name, arr, grad in tensors:
+        for _ in range(6):
+            idx = tuple(int(rs.integers(0, n)) for n in arr.shape)
+            a, b = arr.copy(), arr.copy()
+            a[idx] += h
+            b[idx] -= h
+            sub = {"q": 0, "k": 1, "v": 2, "w": 3}[name]
+            args_a, args_b = [q, k, v, om], [q, k, v, om]
+            args_a[sub], args_b[sub] = a, b
+            fd = (loss(*args_a) - loss(*args_b)) / (2 * h)
+            assert abs(fd - grad[idx]) <= 1e-6 * (abs(grad[idx]) + np.abs(grad).max()), (name, idx, fd, grad[idx])
+
+
+def test_backward_single_token_passes_the_gradient_to_v():
+    """L = 1: out = v exactly, so dv = g and dq = dk = dw = 0."""
+    rs = np.random.default_rng(61)
+    q, k = rs.standard_normal((1, 2, 1, 8)), rs.standard_normal((1, 2, 1, 8))
+    v, g = rs.standard_normal((1, 2, 1, 4)), rs.standard_normal((1, 2, 1, 4))
+    om = rs.standard_normal((2, 16, 8))
+    for causal in (False, True):
+        dq, dk, dv, dw = oracle.backward(q, k, v, om, g, causal)
+        assert np.allclose(dv, g, rtol=1e-13, atol=1e-15)
+        assert np.abs(dq).max() < 1e-12 and np.abs(dk).max() < 1e-12 and np.abs(dw).max() < 1e-12
