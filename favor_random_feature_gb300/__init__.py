@@ -47,6 +47,8 @@ EXPORTS = (
     "favor_attn_decode",
     "favor_attn_decode_f32",
     "favor_draw_omega",
+    "favor_attn_backward",
+    "favor_attn_backward_f32",
 )
 
 _lib = None
@@ -96,6 +98,9 @@ def lib() -> ctypes.CDLL:
         L.favor_state_floats.restype = i
         for name in ("favor_attn_state", "favor_attn_state_f32"):
             getattr(L, name).argtypes = [vp, vp, fp, fp] + [i] * 7 + [vp]
+            getattr(L, name).restype = i
+        for name in ("favor_attn_backward", "favor_attn_backward_f32"):
+            getattr(L, name).argtypes = [vp, vp, vp, fp, fp, fp, fp, fp, fp] + [i] * 8 + [vp]
             getattr(L, name).restype = i
         L.favor_draw_omega.argtypes = [fp, i, i, i, i, ctypes.c_ulonglong, vp]
         L.favor_draw_omega.restype = i
@@ -209,6 +214,20 @@ def favor_attn_decode(q, k, v, omega, state, out, B, H, d, dv, m, feature_map, s
 def favor_attn_decode_f32(q, k, v, omega, state, out, B, H, d, dv, m, feature_map, stream=None):
     return lib().favor_attn_decode_f32(_ptr(q), _ptr(k), _ptr(v), _ptr(omega), _ptr(state), _ptr(out),
                                        B, H, d, dv, m, int(feature_map), _stream(stream))
+
+
+def favor_attn_backward(q, k, v, omega, dout, dq, dk, dv, domega, B, H, L, d, dv_, m, causal, feature_map,
+                        stream=None):
+    return lib().favor_attn_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(omega), _ptr(dout), _ptr(dq), _ptr(dk),
+                                     _ptr(dv), _ptr(domega), B, H, L, d, dv_, m, int(causal), int(feature_map),
+                                     _stream(stream))
+
+
+def favor_attn_backward_f32(q, k, v, omega, dout, dq, dk, dv, domega, B, H, L, d, dv_, m, causal, feature_map,
+                            stream=None):
+    return lib().favor_attn_backward_f32(_ptr(q), _ptr(k), _ptr(v), _ptr(omega), _ptr(dout), _ptr(dq), _ptr(dk),
+                                         _ptr(dv), _ptr(domega), B, H, L, d, dv_, m, int(causal),
+                                         int(feature_map), _stream(stream))
 
 
 def favor_draw_omega(omega, H, m, d, kind, seed, stream=None):

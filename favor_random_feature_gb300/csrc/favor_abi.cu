@@ -203,6 +203,51 @@ extern "C" int favor_attn_forward_f32(const float *q, const float *k, const floa
     return simt_forward(q, k, v, false, omega, out, p, stream);
 }
 
+namespace {
+int backward_entry(const void *q, const void *k, const void *v, const float *omega, const float *dout, float *dq,
+                   float *dk, float *dv, float *domega, bool bf16_in, int B, int H, int L, int d, int dv_, int m,
+                   int causal, int feature_map, cudaStream_t stream) {
+    Problem p;
+    int rc = make_problem(B, H, L, d, dv_, m, causal, feature_map, &p);
+    if (rc) return rc;
+    const size_t esize = bf16_in ? 2 : 4;
+    if ((rc = validate_args(q, k, v, omega, dq, esize, p))) return rc;
+    if ((rc = check_ptr(dout, false)) || (rc = check_ptr(dk, false)) || (rc = check_ptr(dv, false)) ||
+        (rc = check_ptr(domega, true)))
+        return rc;
+    const size_t rows = (size_t)p.BH * p.L;
+    const void *ins[5] = {q, k, v, omega, dout};
+    const size_t inb[5] = {rows * p.d * esize, rows * p.d * esize, rows * p.dv * esize,
+                           omega ? (size_t)p.H * p.nproj * p.d * sizeof(float) : 0, rows * p.dv * sizeof(float)};
+    const void *outs[4] = {dq, dk, dv, domega};
+    const size_t outb[4] = {rows * p.d * 4, rows * p.d * 4, rows * p.dv * 4,
+                            domega ? (size_t)p.H * p.nproj * p.d * sizeof(float) : 0};
+    for (int i = 0; i < 4; ++i) {
+        if (!outs[i]) continue;
+        for (int j = 0; j < 5; ++j)
+            if (ins[j] && overlaps(outs[i], outb[i], ins[j], inb[j])) return FAVOR_ERR_INVALID_ARG;
+        for (int j = i + 1; j < 4; ++j)
+            if (outs[j] && overlaps(outs[i], outb[i], outs[j], outb[j])) return FAVOR_ERR_INVALID_ARG;
+    }
+    return simt_backward(q, k, v, bf16_in, omega, dout, dq, dk, dv, domega, p, stream);
+}
+}  // namespace
+
+extern "C" int favor_attn_backward(const void *q, const void *k, const void *v, const float *omega,
+                                   const float *dout, float *dq, float *dk, float *dv, float *domega, int B, int H,
+                                   int L, int d, int dv_, int m, int causal, int feature_map, cudaStream_t stream) {
+    return backward_entry(q, k, v, omega, dout, dq, dk, dv, domega, true, B, H, L, d, dv_, m, causal, feature_map,
+                          stream);
+}
+
+extern "C" int favor_attn_backward_f32(const float *q, const float *k, const float *v, const float *omega,
+                                       const float *dout, float *dq, float *dk, float *dv, float *domega, int B,
+                                       int H, int L, int d, int dv_, int m, int causal, int feature_map,
+                                       cudaStream_t stream) {
+    return backward_entry(q, k, v, omega, dout, dq, dk, dv, domega, false, B, H, L, d, dv_, m, causal, feature_map,
+                          stream);
+}
+
 extern "C" int favor_attn_forward_host(const void *q, const void *k, const void *v,
                                        const float *omega, float *out, int B, int H, int L, int d,
                                        int dv, int m, int causal, int feature_map,

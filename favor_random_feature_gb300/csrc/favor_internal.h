@@ -50,6 +50,11 @@ template <typename T> size_t carve_bytes(size_t count) {
 // SIMT path (fp32 arithmetic; input element type float or bf16 bits).
 int simt_forward(const void *q, const void *k, const void *v, bool bf16_in, const float *omega,
                  float *out, const Problem &p, cudaStream_t stream);
+// Backward pass on the SIMT path: g = dloss/dout [B][H][L][dv] fp32 ->
+// dq, dk [B][H][L][d], dv [B][H][L][dv] and dw [H][m][d] (summed over the
+// batch; skipped if null or for the elementwise maps), all fp32.
+int simt_backward(const void *q, const void *k, const void *v, bool bf16_in, const float *omega, const float *g,
+                  float *dq, float *dk, float *dv, float *dw, const Problem &p, cudaStream_t stream);
 int simt_feature_map(const void *x, bool bf16_in, const float *omega, float *phi,
                      float *log_scale, const Problem &p, cudaStream_t stream);
 

@@ -388,4 +388,327 @@ int simt_feature_map(const void *x, bool bf16_in, const float *omega, float *phi
     return features_into<float>(static_cast<const float *>(x), omega, P, phi, log_scale, p, stream);
 }
 
+// ---------------------------------------------------------------------------
+// Backward pass (fp32 SIMT): the gradients of a loss given g = dloss/dout,
+//   dnum_i = g_i / den_i,  dden_i = -(g_i . out_i) / den_i
+//   dphi(q_i) = S_i dnum_i + z_i dden_i
+//   dphi(k_j) = R_j v_j + rho_j,  dv_j = R_j^T phi(k_j),
+//   R_j = sum_{i >= j} phi(q_i) dnum_i^T,  rho_j = sum_{i >= j} phi(q_i) dden_i
+// (non-causal: S, z, R, rho over all rows), then the feature maps'
+// derivatives to dq, dk and dw -- the prefix sums of the Performer study
+// notes ("Case 2") accumulated in reverse.  In chunks of 64 rows: the states
+// entering (S) and leaving (R) a chunk plus the masked products inside it,
+//   A_ij = phi(q_i).phi(k_j),  B_ij = dnum_i.v_j + dden_i   (j <= i).
+// The stabilised features of the forward pass serve as the features (out
+// does not change under them); the map derivatives use the products
+// dphi_f phi_f (positive map) or the scale applied to the raw sin, cos (trig
+// maps), which are the same for the stabilised and the exact features.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kBwdRows = 64;    // rows per chunk (= kChunk)
+
+// per row: out from the entering state (+ the masked chunk sum), then dnum
+// and dden into Y [rows][dv + 1].  block per (chunk, head), 256 threads.
+template <typename T>
+__global__ void bwd_rows(const float *__restrict__ phiq, const float *__restrict__ phik, const T *__restrict__ v,
+                         const float *__restrict__ Sin, const float *__restrict__ g, float *__restrict__ Y, int L,
+                         int r, int dv, int nst, int causal) {
+    __shared__ float A[kBwdRows][kBwdRows + 1];
+    __shared__ float den_s[kBwdRows];
+    const int ch = blockIdx.x, bh = blockIdx.y, t0 = ch * kBwdRows, n = min(kBwdRows, L - t0);
+    const float *pq = phiq + ((size_t)bh * L + t0) * r;
+    const float *pk = phik + ((size_t)bh * L + t0) * r;
+    const T *vb = v + ((size_t)bh * L + t0) * dv;
+    const float *S = Sin + ((size_t)bh * nst + (causal ? ch : 0)) * r * (dv + 1);
+    if (causal) {
+        for (int e = threadIdx.x; e < kBwdRows * kBwdRows; e += blockDim.x) {
+            const int i = e / kBwdRows, j = e % kBwdRows;
+            float acc = 0.f;
+            if (i < n && j <= i)
+                for (int f = 0; f < r; ++f) acc = fmaf(pq[(size_t)i * r + f], pk[(size_t)j * r + f], acc);
+            A[i][j] = acc;
+        }
+        __syncthreads();
+    }
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        float den = 0.f;
+        for (int f = 0; f < r; ++f) den = fmaf(pq[(size_t)i * r + f], S[(size_t)f * (dv + 1) + dv], den);
+        if (causal)
+            for (int j = 0; j <= i; ++j) den += A[i][j];
+        den_s[i] = den;
+    }
+    __syncthreads();
+    // warp per row: lanes over value columns
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    for (int i = warp; i < n; i += nw) {
+        const float den = den_s[i];
+        float gdo = 0.f;
+        for (int c = lane; c < dv; c += 32) {
+            float num = 0.f;
+            for (int f = 0; f < r; ++f) num = fmaf(pq[(size_t)i * r + f], S[(size_t)f * (dv + 1) + c], num);
+            if (causal)
+                for (int j = 0; j <= i; ++j) num = fmaf(A[i][j], load_in(vb, (size_t)j * dv + c), num);
+            const float gi = g[((size_t)bh * L + t0 + i) * dv + c];
+            gdo = fmaf(gi, num / den, gdo);
+            Y[((size_t)bh * L + t0 + i) * (dv + 1) + c] = gi / den;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) gdo += __shfl_xor_sync(0xffffffffu, gdo, o);
+        if (lane == 0) Y[((size_t)bh * L + t0 + i) * (dv + 1) + dv] = -gdo / den;
+    }
+}
+
+// per segment: R[f][c] = sum_{rows} phi_q[row][f] Y[row][c], c <= dv.
+// grid (ceil(r/32), dv+1, BH*nseg), 32 threads.
+__global__ void bwd_state(const float *__restrict__ phiq, const float *__restrict__ Y, float *__restrict__ R, int L,
+                          int r, int dv, int seg, int nseg) {
+    const int f = blockIdx.x * 32 + threadIdx.x, c = blockIdx.y;
+    const int bh = blockIdx.z / nseg, s = blockIdx.z % nseg;
+    if (f >= r) return;
+    const int t0 = s * seg, t1 = min(L, t0 + seg);
+    float acc = 0.f;
+    for (int t = t0; t < t1; ++t)
+        acc = fmaf(phiq[((size_t)bh * L + t) * r + f], Y[((size_t)bh * L + t) * (dv + 1) + c], acc);
+    R[(((size_t)bh * nseg + s) * r + f) * (dv + 1) + c] = acc;
+}
+
+// exclusive suffix over segments, in place: R_s <- sum_{s' > s} R_s'
+__global__ void bwd_state_suffix(float *__restrict__ R, int nseg, size_t per_seg, int BH) {
+    const size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+    if (e >= per_seg * BH) return;
+    const int bh = (int)(e / per_seg);
+    const size_t within = e % per_seg;
+    float run = 0.f;
+    for (int s = nseg - 1; s >= 0; --s) {
+        float *p = R + ((size_t)bh * nseg + s) * per_seg + within;
+        const float t = *p;
+        *p = run;
+        run += t;
+    }
+}
+
+// dphi_q, dphi_k [rows][r] and dv [rows][dv] of a chunk from the entering
+// state S, the leaving state R and (causal) the masked A, B inside it.
+// block per (chunk, head), 256 threads.
+template <typename T>
+__global__ void bwd_chunk(const float *__restrict__ phiq, const float *__restrict__ phik, const T *__restrict__ v,
+                          const float *__restrict__ Sin, const float *__restrict__ Rout, const float *__restrict__ Y,
+                          float *__restrict__ dphiq, float *__restrict__ dphik, float *__restrict__ dV, int L, int r,
+                          int dv, int nst, int causal) {
+    __shared__ float A[kBwdRows][kBwdRows + 1];
+    __shared__ float Bm[kBwdRows][kBwdRows + 1];
+    const int ch = blockIdx.x, bh = blockIdx.y, t0 = ch * kBwdRows, n = min(kBwdRows, L - t0);
+    const size_t row0 = (size_t)bh * L + t0;
+    const float *pq = phiq + row0 * r, *pk = phik + row0 * r, *y = Y + row0 * (dv + 1);
+    const T *vb = v + row0 * dv;
+    const size_t st = ((size_t)bh * nst + (causal ? ch : 0)) * r * (dv + 1);
+    const float *S = Sin + st, *R = Rout + st;
+    if (causal) {
+        for (int e = threadIdx.x; e < kBwdRows * kBwdRows; e += blockDim.x) {
+            const int i = e / kBwdRows, j = e % kBwdRows;
+            float a = 0.f, b = 0.f;
+            if (i < n && j <= i) {
+                for (int f = 0; f < r; ++f) a = fmaf(pq[(size_t)i * r + f], pk[(size_t)j * r + f], a);
+                b = y[(size_t)i * (dv + 1) + dv];
+                for (int c = 0; c < dv; ++c) b = fmaf(y[(size_t)i * (dv + 1) + c], load_in(vb, (size_t)j * dv + c), b);
+            }
+            A[i][j] = a;
+            Bm[i][j] = b;
+        }
+        __syncthreads();
+    }
+    for (int e = threadIdx.x; e < n * r; e += blockDim.x) {
+        const int i = e / r, f = e % r;
+        // dphi_q[i][f] = S_f . dnum_i + z_f dden_i + sum_{j <= i} B_ij phi_k[j][f]
+        float aq = S[(size_t)f * (dv + 1) + dv] * y[(size_t)i * (dv + 1) + dv];
+        for (int c = 0; c < dv; ++c) aq = fmaf(S[(size_t)f * (dv + 1) + c], y[(size_t)i * (dv + 1) + c], aq);
+        // dphi_k[i][f] = R_f . v_i + rho_f + sum_{i' >= i} B_i'i phi_q[i'][f]
+        float ak = R[(size_t)f * (dv + 1) + dv];
+        for (int c = 0; c < dv; ++c) ak = fmaf(R[(size_t)f * (dv + 1) + c], load_in(vb, (size_t)i * dv + c), ak);
+        if (causal) {
+            for (int j = 0; j <= i; ++j) aq = fmaf(Bm[i][j], pk[(size_t)j * r + f], aq);
+            for (int j = i; j < n; ++j) ak = fmaf(Bm[j][i], pq[(size_t)j * r + f], ak);
+        }
+        dphiq[(row0 + i) * r + f] = aq;
+        dphik[(row0 + i) * r + f] = ak;
+    }
+    for (int e = threadIdx.x; e < n * dv; e += blockDim.x) {
+        const int j = e / dv, c = e % dv;
+        // dv[j][c] = R[:, c] . phi_k[j] + sum_{i >= j} A_ij dnum_i[c]
+        float acc = 0.f;
+        for (int f = 0; f < r; ++f) acc = fmaf(R[(size_t)f * (dv + 1) + c], pk[(size_t)j * r + f], acc);
+        if (causal)
+            for (int i = j; i < n; ++i) acc = fmaf(A[i][j], y[(size_t)i * (dv + 1) + c], acc);
+        dV[(row0 + j) * dv + c] = acc;
+    }
+}
+
+// per (row, projection p): the coefficient c of the map derivative, in place
+// of the projection P[row][p]:
+//   positive: c = dphi_p phi_p              (dx = sum_p c w_p - x sum_p c)
+//   trig:     c = s (dphi_2p cos P - dphi_2p+1 sin P), s the scale on the raw
+//             sin, cos of that row           (dx = sum_p c w_p [+ x tot])
+//   elu1, relu: c = dphi_p phi'(x_p)        (dx = c)
+__global__ void bwd_coeff(float *__restrict__ P, const float *__restrict__ dphi, const float *__restrict__ phi,
+                          const float *__restrict__ logscale, const float *__restrict__ hmax, size_t rows, int L,
+                          int nproj, int r, int map, int is_key) {
+    const size_t total = rows * nproj;
+    for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < total; e += (size_t)gridDim.x * blockDim.x) {
+        const size_t row = e / nproj;
+        const int p = (int)(e % nproj);
+        const float a = P[e];
+        float c;
+        if (map == FAVOR_MAP_POSITIVE) {
+            c = dphi[row * r + p] * phi[row * r + p];
+        } else if (map_is_trig(map)) {
+            // keys carry exp(logscale - head max) on the raw sin, cos; queries 1
+            const float s = is_key ? expf(logscale[row] - hmax[row / L]) : 1.f;
+            float sn, cs;
+            sincosf(a, &sn, &cs);
+            c = s * (dphi[row * r + 2 * p] * cs - dphi[row * r + 2 * p + 1] * sn);
+        } else {
+            const float der = a > 0.f ? 1.f : (map == FAVOR_MAP_ELU1 ? expf(a) : 0.f);
+            c = dphi[row * r + p] * der;
+        }
+        P[e] = c;
+    }
+}
+
+// dx [rows][d] from the coefficients: warp per row, lanes over d
+template <typename T>
+__global__ void bwd_dx(const float *__restrict__ C, const float *__restrict__ dphi, const float *__restrict__ phi,
+                       const T *__restrict__ x, const float *__restrict__ omega, float *__restrict__ dx, size_t rows,
+                       int L, int H, int d, int nproj, int r, int map) {
+    const size_t row = (blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const float *c = C + row * nproj;
+    if (map_is_elementwise(map)) {
+        for (int j = lane; j < d; j += 32) dx[row * d + j] = c[j];
+        return;
+    }
+    const int h = (int)((row / L) % H);
+    const float *w = omega + (size_t)h * nproj * d;
+    float tot = 0.f;
+    if (map == FAVOR_MAP_POSITIVE) {
+        for (int p = lane; p < nproj; p += 32) tot += c[p];
+    } else if (map == FAVOR_MAP_TRIG_SOFTMAX) {
+        for (int f = lane; f < r; f += 32) tot = fmaf(dphi[row * r + f], phi[row * r + f], tot);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    for (int j = lane; j < d; j += 32) {
+        float acc = 0.f;
+        for (int p = 0; p < nproj; ++p) acc = fmaf(c[p], w[(size_t)p * d + j], acc);
+        const float xj = load_in(x, row * d + j);
+        if (map == FAVOR_MAP_POSITIVE) acc = fmaf(-tot, xj, acc);
+        else if (map == FAVOR_MAP_TRIG_SOFTMAX) acc = fmaf(tot, xj, acc);
+        dx[row * d + j] = acc;
+    }
+}
+
+// dw[h][p][j] += sum over a slice of the head's rows (all batches, queries
+// and keys) of c[row][p] x[row][j]; grid (ceil(nproj d / 256), H, slices)
+template <typename T>
+__global__ void bwd_dw(const float *__restrict__ Cq, const float *__restrict__ Ck, const T *__restrict__ q,
+                       const T *__restrict__ k, float *__restrict__ dw, int B, int H, int L, int d, int nproj,
+                       int slice) {
+    const int e = blockIdx.x * blockDim.x + threadIdx.x, h = blockIdx.y;
+    if (e >= nproj * d) return;
+    const int p = e / d, j = e % d;
+    const int r0 = blockIdx.z * slice, r1 = min(B * L, r0 + slice);
+    float acc = 0.f;
+    for (int t = r0; t < r1; ++t) {
+        const int b = t / L, i = t % L;
+        const size_t row = ((size_t)b * H + h) * L + i;
+        acc = fmaf(Cq[row * nproj + p], load_in(q, row * d + j), acc);
+        acc = fmaf(Ck[row * nproj + p], load_in(k, row * d + j), acc);
+    }
+    atomicAdd(&dw[((size_t)h * nproj + p) * d + j], acc);
+}
+
+template <typename T>
+int backward_t(const T *q, const T *k, const T *v, const float *omega, const float *g, float *dq, float *dk,
+               float *dv, float *dw, const Problem &p, cudaStream_t st) {
+    const size_t rows = (size_t)p.BH * p.L;
+    const int nch = p.causal ? (p.L + kBwdRows - 1) / kBwdRows : 1;
+    const int seg = p.causal ? kBwdRows : p.L;
+    const size_t per = (size_t)p.r * (p.dv + 1);
+    size_t bytes = 2 * carve_bytes<float>(rows * p.nproj) + 4 * carve_bytes<float>(rows * p.r) +
+                   2 * carve_bytes<float>(rows) + carve_bytes<float>(p.BH) +
+                   2 * carve_bytes<float>((size_t)p.BH * nch * per) + carve_bytes<float>(rows * (p.dv + 1));
+    int status = FAVOR_OK;
+    void *ws = workspace(bytes, &status);
+    if (!ws) return status;
+    Carve cv{static_cast<char *>(ws), 0};
+    float *Pq = cv.take<float>(rows * p.nproj), *Pk = cv.take<float>(rows * p.nproj);
+    float *phiq = cv.take<float>(rows * p.r), *phik = cv.take<float>(rows * p.r);
+    float *dphiq = cv.take<float>(rows * p.r), *dphik = cv.take<float>(rows * p.r);
+    float *lsq = cv.take<float>(rows), *lsk = cv.take<float>(rows);
+    float *hmax = cv.take<float>(p.BH);
+    float *S = cv.take<float>((size_t)p.BH * nch * per), *R = cv.take<float>((size_t)p.BH * nch * per);
+    float *Y = cv.take<float>(rows * (p.dv + 1));
+
+    int rc;
+    if ((rc = features_into<T>(q, omega, Pq, phiq, lsq, p, st)) || (rc = features_into<T>(k, omega, Pk, phik, lsk, p, st)))
+        return rc;
+    simt_head_max<<<p.BH, 256, 0, st>>>(lsk, hmax, p.L);
+    FAVOR_LAUNCH_CHECK();
+    const size_t total = rows * p.r;
+    const unsigned sg = (unsigned)std::min<size_t>((total + 255) / 256, 152 * 64);
+    simt_key_scale<<<sg, 256, 0, st>>>(phik, lsk, hmax, p.L, p.r, total);
+    FAVOR_LAUNCH_CHECK();
+    // the forward states entering each chunk (causal) or the total
+    simt_state<T><<<dim3((p.r + 31) / 32, p.dv + 1, p.BH * nch), 32, 0, st>>>(phik, v, S, p.L, p.r, p.dv, seg, nch);
+    FAVOR_LAUNCH_CHECK();
+    if (p.causal) {
+        simt_state_prefix<<<(unsigned)((per * p.BH + 255) / 256), 256, 0, st>>>(S, nch, per, p.BH);
+        FAVOR_LAUNCH_CHECK();
+    }
+    const dim3 cg((p.L + kBwdRows - 1) / kBwdRows, p.BH);
+    bwd_rows<T><<<cg, 256, 0, st>>>(phiq, phik, v, S, g, Y, p.L, p.r, p.dv, nch, p.causal);
+    FAVOR_LAUNCH_CHECK();
+    // the states leaving each chunk: exclusive suffix (causal) or the total
+    bwd_state<<<dim3((p.r + 31) / 32, p.dv + 1, p.BH * nch), 32, 0, st>>>(phiq, Y, R, p.L, p.r, p.dv, seg, nch);
+    FAVOR_LAUNCH_CHECK();
+    if (p.causal) {
+        bwd_state_suffix<<<(unsigned)((per * p.BH + 255) / 256), 256, 0, st>>>(R, nch, per, p.BH);
+        FAVOR_LAUNCH_CHECK();
+    }
+    stats_begin(st, "bwd_chunk");
+    bwd_chunk<T><<<cg, 256, 0, st>>>(phiq, phik, v, S, R, Y, dphiq, dphik, dv, p.L, p.r, p.dv, nch, p.causal);
+    stats_end(st);
+    FAVOR_LAUNCH_CHECK();
+    const unsigned cgr = (unsigned)std::min<size_t>((rows * p.nproj + 255) / 256, 152 * 64);
+    bwd_coeff<<<cgr, 256, 0, st>>>(Pq, dphiq, phiq, lsq, hmax, rows, p.L, p.nproj, p.r, p.map, 0);
+    FAVOR_LAUNCH_CHECK();
+    bwd_coeff<<<cgr, 256, 0, st>>>(Pk, dphik, phik, lsk, hmax, rows, p.L, p.nproj, p.r, p.map, 1);
+    FAVOR_LAUNCH_CHECK();
+    const unsigned xg = (unsigned)((rows * 32 + 255) / 256);
+    bwd_dx<T><<<xg, 256, 0, st>>>(Pq, dphiq, phiq, q, omega, dq, rows, p.L, p.H, p.d, p.nproj, p.r, p.map);
+    FAVOR_LAUNCH_CHECK();
+    bwd_dx<T><<<xg, 256, 0, st>>>(Pk, dphik, phik, k, omega, dk, rows, p.L, p.H, p.d, p.nproj, p.r, p.map);
+    FAVOR_LAUNCH_CHECK();
+    if (dw && !map_is_elementwise(p.map)) {
+        if (cudaMemsetAsync(dw, 0, (size_t)p.H * p.nproj * p.d * sizeof(float), st) != cudaSuccess) return FAVOR_ERR_CUDA;
+        const int brows = p.B * p.L, slices = std::max(1, std::min(64, brows / 256));
+        const int slice = (brows + slices - 1) / slices;
+        bwd_dw<T><<<dim3((p.nproj * p.d + 255) / 256, p.H, slices), 256, 0, st>>>(Pq, Pk, q, k, dw, p.B, p.H, p.L,
+                                                                                  p.d, p.nproj, slice);
+        FAVOR_LAUNCH_CHECK();
+    }
+    return FAVOR_OK;
+}
+}  // namespace
+
+int simt_backward(const void *q, const void *k, const void *v, bool bf16_in, const float *omega, const float *g,
+                  float *dq, float *dk, float *dv, float *dw, const Problem &p, cudaStream_t stream) {
+    if (bf16_in)
+        return backward_t<uint16_t>(static_cast<const uint16_t *>(q), static_cast<const uint16_t *>(k),
+                                    static_cast<const uint16_t *>(v), omega, g, dq, dk, dv, dw, p, stream);
+    return backward_t<float>(static_cast<const float *>(q), static_cast<const float *>(k),
+                             static_cast<const float *>(v), omega, g, dq, dk, dv, dw, p, stream);
+}
+
 }  // namespace favor

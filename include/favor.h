@@ -152,6 +152,30 @@ void favor_release_workspace(void);
 /* Number of feature columns r for a map, or -1 if the arguments are invalid. */
 int favor_feature_dim(int feature_map, int d, int m);
 
+/* ---- backward pass ----------------------------------------------------------
+ * Gradients of a loss through the forward pass, given dout = dloss/dout
+ * [B][H][L][dv] fp32 (the prefix sums of the Performer study notes, "Case 2",
+ * accumulated in reverse for the keys and values):
+ *   dnum_i = dout_i / den_i,  dden_i = -(dout_i . out_i) / den_i
+ *   dphi(q_i) = S_i dnum_i + z_i dden_i
+ *   dphi(k_j) = R_j v_j + rho_j,  dv_j = R_j^T phi(k_j),
+ *   R_j = sum_{i >= j} phi(q_i) dnum_i^T,  rho_j = sum_{i >= j} phi(q_i) dden_i
+ * (non-causal: all rows), then each feature map's derivative to dq and dk,
+ * and to domega [H][m][d] summed over the batch.  Outputs dq, dk
+ * [B][H][L][d], dv [B][H][L][dv] fp32; domega may be NULL (not computed; it
+ * is never written for elu1 and relu).  No output may overlap an input or
+ * another output.  fp32 SIMT kernels (out is recomputed, not passed in).
+ * Asynchronous on `stream`; returns favor_status_t. */
+int favor_attn_backward(const void *q, const void *k, const void *v, const float *omega,
+                        const float *dout, float *dq, float *dk, float *dv, float *domega, int B, int H,
+                        int L, int d, int dv_, int m, int causal, int feature_map, cudaStream_t stream);
+
+/* Same with fp32 q/k/v. */
+int favor_attn_backward_f32(const float *q, const float *k, const float *v, const float *omega,
+                            const float *dout, float *dq, float *dk, float *dv, float *domega, int B,
+                            int H, int L, int d, int dv_, int m, int causal, int feature_map,
+                            cudaStream_t stream);
+
 /* ---- carried state and the one-token decode step --------------------------
  * The causal form keeps running sums (Performer study notes, "Case 2"):
  *   S_i = S_{i-1} + phi(k_i) v_i^T,  z_i = z_{i-1} + phi(k_i),
