@@ -411,6 +411,150 @@ def decode_cpu_baseline(w, n_heads, steps):
             "seconds": dt}
 
 
+# backward workloads: the forward workload's shape; a step is one backward
+# call (gradients of q, k, v and omega for a seeded dloss/dout)
+BWD_METRIC = "FAVOR+ backward tokens/sec (B*H*L/s); % of the fp32 ALU roofline"
+BACKWARD = {"causal8k_bwd": "causal8k", "nc4096_bwd": "nc4096"}
+BWD_ROWS = 64   # rows per chunk of the backward kernels
+
+
+def bwd_chunk_flops_per_token(w, causal):
+    """Executed FLOPs per token of the backward chunk kernel: the masked chunk
+    products A and B (causal), dphi_q and dphi_k from the carried states plus
+    the chunk sums, and dv."""
+    r, dv, C = w.r, w.dv, BWD_ROWS
+    intra = C / 2 if causal else 0
+    ab = (C / 2) * (r + dv + 1) * 2 if causal else 0
+    dphi = 2 * r * (dv + 1 + intra) * 2
+    dvv = dv * (r + intra) * 2
+    return ab + dphi + dvv
+
+
+def run_backward(args):
+    import numpy as np
+    import torch
+    from favor_random_feature_gb300 import build as fbuild
+    fbuild.build()
+    import favor_random_feature_gb300 as fv
+    from favor_inputs import make_inputs
+
+    if int(os.environ.get("WORLD_SIZE", "1")) != 1 or args.gpus != 1:
+        raise SystemExit("backward workloads run on one GPU (replicas only)")
+    w, causal = workload(BACKWARD[args.workload])
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    inp = make_inputs(w)
+    dev16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+    q, k, v = dev16(inp.q), dev16(inp.k), dev16(inp.v)
+    om = torch.from_numpy(np.ascontiguousarray(inp.omega)).cuda()
+    g_host = np.random.default_rng(w.seed + 500).standard_normal((w.B, w.H, w.L, w.dv)).astype(np.float32)
+    g = torch.from_numpy(g_host).cuda()
+    dq = torch.empty((w.B, w.H, w.L, w.d), dtype=torch.float32, device="cuda")
+    dk, dv = torch.empty_like(dq), torch.empty((w.B, w.H, w.L, w.dv), dtype=torch.float32, device="cuda")
+    dw = torch.empty((w.H, w.m, w.d), dtype=torch.float32, device="cuda")
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def call(qq=q, kk=k, vv=v, gg=g):
+        rc = fv.favor_attn_backward(qq, kk, vv, om, gg, dq, dk, dv, dw, w.B, w.H, w.L, w.d, w.dv, w.m,
+                                    int(causal), 0, stream)
+        if rc != fv.FAVOR_OK:
+            raise fv.FavorError(rc, "favor_attn_backward")
+
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                           else os.environ["CUDA_VISIBLE_DEVICES"].split(",")[0])
+    t_soak = time.time()
+    while time.time() - t_soak < 1.0:
+        call()
+        torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        call()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    sampler.stop()
+    st = fv.favor_get_device_status(stream)
+    if st != fv.FAVOR_OK:
+        raise fv.FavorError(st, "device status after the timed steps")
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    stat_steps = max(3, min(args.steps, 5))
+    fv.favor_stats_enable(True)
+    for _ in range(stat_steps):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    stats = fv.favor_stats_read()
+    fv.favor_stats_enable(False)
+    dom_ms = stats.dominant_ms / max(1, stats.dominant_launches)
+    tokens = w.B * w.H * w.L
+    clocks = sampler.summary(t0, t1)
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    mhz = clocks.get("sm_max_mhz") or 2070.0
+    peak = props.multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12   # fp32 FMA lanes x 2 flops x clock
+    achieved = bwd_chunk_flops_per_token(w, causal) * tokens / (dom_ms / 1000.0) / 1e12
+
+    # end to end: q, k, v and dloss/dout from pinned host memory, the
+    # gradients back to it, every step
+    pin16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).pin_memory()
+    hq, hk, hv = pin16(inp.q), pin16(inp.k), pin16(inp.v)
+    hg = torch.from_numpy(g_host).pin_memory()
+    hdq, hdk, hdv = (torch.empty(t.shape, dtype=torch.float32).pin_memory() for t in (dq, dk, dv))
+    hdw = torch.empty(dw.shape, dtype=torch.float32).pin_memory()
+    dq_in, dk_in, dv_in, dg_in = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(g)
+    e2e_steps = max(3, min(args.steps, 10))
+    torch.cuda.synchronize()
+    te0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        dq_in.copy_(hq, non_blocking=True)
+        dk_in.copy_(hk, non_blocking=True)
+        dv_in.copy_(hv, non_blocking=True)
+        dg_in.copy_(hg, non_blocking=True)
+        call(dq_in, dk_in, dv_in, dg_in)
+        for h_, d_ in ((hdq, dq), (hdk, dk), (hdv, dv), (hdw, dw)):
+            h_.copy_(d_, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    te = (time.perf_counter() - te0) / e2e_steps
+    h2d = (q.numel() + k.numel() + v.numel()) * 2 + g.numel() * 4
+    d2h = (dq.numel() + dk.numel() + dv.numel() + dw.numel()) * 4
+    line = {
+        "metric": BWD_METRIC, "value": tokens / (ms / 1000.0), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": dict(describe(w, causal), workload=f"{args.workload}: backward of " + describe(w, causal)["workload"],
+                       inputs="bf16 q,k,v; fp32 omega, dloss/dout and gradients"),
+        "roofline": {
+            "bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "traffic": None, "kernel": stats.dominant_kernel.decode() if stats.dominant_kernel else None,
+            "kernel_ms": dom_ms, "peak_source": "derived: SMs x 128 fp32 lanes x 2 flops x max SM clock",
+            "executed_flops_per_token": bwd_chunk_flops_per_token(w, causal),
+        },
+        "e2e": {"value": tokens / te, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(round(stats.kernel_launches / stat_steps * args.steps)),
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        n = min(w.B * w.H, 2 * oracle.threads_used())
+        Lc = 1024
+        sel = lambda a: a.reshape(w.B * w.H, w.L, a.shape[-1])[:n, :Lc][None]
+        t_c = time.perf_counter()
+        oracle.backward(sel(inp.q32), sel(inp.k32), sel(inp.v32), inp.omega[[h % w.H for h in range(n)]],
+                        sel(g_host).astype(np.float64), causal, 0)
+        dt = time.perf_counter() - t_c
+        line["cpu_baseline"] = {"value": n * Lc / dt, "unit": "tokens/s", "cores": oracle.threads_used(),
+                                "kind": "oracle",
+                                "sample": f"{n} heads x the first {Lc} tokens (float64 C oracle backward)"}
+    print(json.dumps(line))
+    return 0
+
+
 def run_decode_reference(args):
     if int(os.environ.get("RANK", "0")) != 0:
         return 0
@@ -428,6 +572,36 @@ def run_decode_reference(args):
         "config": {"workload": f"{args.workload}: the oracle's decode step on 64 of {w.B * w.H} heads"},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                          "sample": "64 heads x 50 decode steps per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+    return 0
+
+
+def run_backward_reference(args):
+    if int(os.environ.get("RANK", "0")) != 0:
+        return 0
+    import numpy as np
+    import oracle
+    from favor_inputs import make_inputs
+    w, causal = workload(BACKWARD[args.workload])
+    n, Lc = min(w.B * w.H, oracle.threads_used()), 1024
+    inp = make_inputs(w.with_(B=1, H=n, L=Lc))
+    g = np.random.default_rng(1).standard_normal((1, n, Lc, w.dv))
+    times = []
+    for i in range(args.warmup + args.steps):
+        t_c = time.perf_counter()
+        oracle.backward(inp.q32, inp.k32, inp.v32, inp.omega, g, causal, 0)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t_c)
+    ms = 1000 * statistics.mean(times)
+    value = n * Lc / (ms / 1000)
+    print(json.dumps({
+        "impl": "reference", "metric": BWD_METRIC, "value": value, "unit": "tokens/s", "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: the oracle's backward on {n} heads x {Lc} tokens per step"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.threads_used(), "kind": "oracle",
+                         "sample": f"{n} heads x {Lc} tokens per step"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
     return 0
@@ -578,11 +752,15 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="causal8k",
                     choices=["causal8k", "nc4096", "long64k", "long64k_nc", "sweep16k", "decode8k",
-                             "decode_b256"])
+                             "decode_b256", "causal8k_bwd", "nc4096_bwd"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.workload in BACKWARD:
+        if args.impl == "reference":
+            return run_backward_reference(args)
+        return run_backward(args)
     if args.workload in DECODE:
         if args.impl == "reference":
             return run_decode_reference(args)
