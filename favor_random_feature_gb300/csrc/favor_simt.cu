@@ -408,71 +408,6 @@ namespace {
 
 constexpr int kBwdRows = 64;    // rows per chunk (= kChunk)
 
-// per row: out from the entering state (+ the masked chunk sum), then dnum
-// and dden into Y [rows][dv + 1].  block per (chunk, head), 256 threads.
-template <typename T>
-__global__ void bwd_rows(const float *__restrict__ phiq, const float *__restrict__ phik, const T *__restrict__ v,
-                         const float *__restrict__ Sin, const float *__restrict__ g, float *__restrict__ Y, int L,
-                         int r, int dv, int nst, int causal) {
-    __shared__ float A[kBwdRows][kBwdRows + 1];
-    __shared__ float den_s[kBwdRows];
-    const int ch = blockIdx.x, bh = blockIdx.y, t0 = ch * kBwdRows, n = min(kBwdRows, L - t0);
-    const float *pq = phiq + ((size_t)bh * L + t0) * r;
-    const float *pk = phik + ((size_t)bh * L + t0) * r;
-    const T *vb = v + ((size_t)bh * L + t0) * dv;
-    const float *S = Sin + ((size_t)bh * nst + (causal ? ch : 0)) * r * (dv + 1);
-    if (causal) {
-        for (int e = threadIdx.x; e < kBwdRows * kBwdRows; e += blockDim.x) {
-            const int i = e / kBwdRows, j = e % kBwdRows;
-            float acc = 0.f;
-            if (i < n && j <= i)
-                for (int f = 0; f < r; ++f) acc = fmaf(pq[(size_t)i * r + f], pk[(size_t)j * r + f], acc);
-            A[i][j] = acc;
-        }
-        __syncthreads();
-    }
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-        float den = 0.f;
-        for (int f = 0; f < r; ++f) den = fmaf(pq[(size_t)i * r + f], S[(size_t)f * (dv + 1) + dv], den);
-        if (causal)
-            for (int j = 0; j <= i; ++j) den += A[i][j];
-        den_s[i] = den;
-    }
-    __syncthreads();
-    // warp per row: lanes over value columns
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-    for (int i = warp; i < n; i += nw) {
-        const float den = den_s[i];
-        float gdo = 0.f;
-        for (int c = lane; c < dv; c += 32) {
-            float num = 0.f;
-            for (int f = 0; f < r; ++f) num = fmaf(pq[(size_t)i * r + f], S[(size_t)f * (dv + 1) + c], num);
-            if (causal)
-                for (int j = 0; j <= i; ++j) num = fmaf(A[i][j], load_in(vb, (size_t)j * dv + c), num);
-            const float gi = g[((size_t)bh * L + t0 + i) * dv + c];
-            gdo = fmaf(gi, num / den, gdo);
-            Y[((size_t)bh * L + t0 + i) * (dv + 1) + c] = gi / den;
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) gdo += __shfl_xor_sync(0xffffffffu, gdo, o);
-        if (lane == 0) Y[((size_t)bh * L + t0 + i) * (dv + 1) + dv] = -gdo / den;
-    }
-}
-
-// per segment: R[f][c] = sum_{rows} phi_q[row][f] Y[row][c], c <= dv.
-// grid (ceil(r/32), dv+1, BH*nseg), 32 threads.
-__global__ void bwd_state(const float *__restrict__ phiq, const float *__restrict__ Y, float *__restrict__ R, int L,
-                          int r, int dv, int seg, int nseg) {
-    const int f = blockIdx.x * 32 + threadIdx.x, c = blockIdx.y;
-    const int bh = blockIdx.z / nseg, s = blockIdx.z % nseg;
-    if (f >= r) return;
-    const int t0 = s * seg, t1 = min(L, t0 + seg);
-    float acc = 0.f;
-    for (int t = t0; t < t1; ++t)
-        acc = fmaf(phiq[((size_t)bh * L + t) * r + f], Y[((size_t)bh * L + t) * (dv + 1) + c], acc);
-    R[(((size_t)bh * nseg + s) * r + f) * (dv + 1) + c] = acc;
-}
-
 // exclusive suffix over segments, in place: R_s <- sum_{s' > s} R_s'
 __global__ void bwd_state_suffix(float *__restrict__ R, int nseg, size_t per_seg, int BH) {
     const size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
@@ -489,59 +424,190 @@ __global__ void bwd_state_suffix(float *__restrict__ R, int nseg, size_t per_seg
 }
 
 // dphi_q, dphi_k [rows][r] and dv [rows][dv] of a chunk from the entering
-// state S, the leaving state R and (causal) the masked A, B inside it.
-// block per (chunk, head), 256 threads.
-template <typename T>
-__global__ void bwd_chunk(const float *__restrict__ phiq, const float *__restrict__ phik, const T *__restrict__ v,
-                          const float *__restrict__ Sin, const float *__restrict__ Rout, const float *__restrict__ Y,
-                          float *__restrict__ dphiq, float *__restrict__ dphik, float *__restrict__ dV, int L, int r,
-                          int dv, int nst, int causal) {
-    __shared__ float A[kBwdRows][kBwdRows + 1];
-    __shared__ float Bm[kBwdRows][kBwdRows + 1];
-    const int ch = blockIdx.x, bh = blockIdx.y, t0 = ch * kBwdRows, n = min(kBwdRows, L - t0);
+// state S, the leaving state R and (causal) the masked A, B inside it, in
+// shared-memory tiles: block per (chunk, head), 256 threads; thread t owns
+// rows 4 (t / 16) .. + 3 of every output tile.
+//   pass 1 (32-feature tiles): A += phi_q phi_k^T,  dv += phi_k R[:, :dv]
+//   then B = Y [V | 1]^T, A and B masked to j <= i, dv += A^T dnum
+//   pass 2 (32-feature tiles): dphi_q = Y S^T + B phi_k, dphi_k = [V | 1] R^T + B^T phi_q
+template <typename T, int DV>
+__global__ void __launch_bounds__(256) bwd_chunk(const float *__restrict__ phiq, const float *__restrict__ phik,
+                                                 const T *__restrict__ v, const float *__restrict__ Sin,
+                                                 const float *__restrict__ Rout, const float *__restrict__ Y,
+                                                 float *__restrict__ dphiq, float *__restrict__ dphik,
+                                                 float *__restrict__ dV, int L, int r, int nst, int causal) {
+    constexpr int C = kBwdRows, FT = 32, W = DV + 1, WP = DV + 1;   // row widths (odd: no bank conflicts)
+    constexpr int CV = DV / 16;                                      // dv columns per thread
+    extern __shared__ float sm[];
+    float *Ys = sm;                      // [C][WP]: dnum | dden
+    float *Vs = Ys + C * WP;             // [C][WP]: v | 1
+    float *As = Vs + C * WP;             // [C][C + 1]
+    float *Bs = As + C * (C + 1);        // [C][C + 1]
+    float *Qt = Bs + C * (C + 1);        // [C][FT + 1]
+    float *Kt = Qt + C * (FT + 1);       // [C][FT + 1]
+    float *St = Kt + C * (FT + 1);       // [FT][WP]
+    float *Rt = St + FT * WP;            // [FT][WP]
+    const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
+    const int ch = blockIdx.x, bh = blockIdx.y, t0 = ch * C, n = min(C, L - t0);
     const size_t row0 = (size_t)bh * L + t0;
-    const float *pq = phiq + row0 * r, *pk = phik + row0 * r, *y = Y + row0 * (dv + 1);
-    const T *vb = v + row0 * dv;
-    const size_t st = ((size_t)bh * nst + (causal ? ch : 0)) * r * (dv + 1);
+    const size_t st = ((size_t)bh * nst + (causal ? ch : 0)) * r * W;
     const float *S = Sin + st, *R = Rout + st;
-    if (causal) {
-        for (int e = threadIdx.x; e < kBwdRows * kBwdRows; e += blockDim.x) {
-            const int i = e / kBwdRows, j = e % kBwdRows;
-            float a = 0.f, b = 0.f;
-            if (i < n && j <= i) {
-                for (int f = 0; f < r; ++f) a = fmaf(pq[(size_t)i * r + f], pk[(size_t)j * r + f], a);
-                b = y[(size_t)i * (dv + 1) + dv];
-                for (int c = 0; c < dv; ++c) b = fmaf(y[(size_t)i * (dv + 1) + c], load_in(vb, (size_t)j * dv + c), b);
-            }
-            A[i][j] = a;
-            Bm[i][j] = b;
+    for (int e = tid; e < C * W; e += 256) {
+        const int i = e / W, c = e % W;
+        Ys[i * WP + c] = i < n ? Y[(row0 + i) * W + c] : 0.f;
+        Vs[i * WP + c] = i < n ? (c < DV ? load_in(v, (row0 + i) * DV + c) : 1.f) : 0.f;
+    }
+    auto load_tiles = [&](int f0, bool states) {
+        for (int e = tid; e < C * FT; e += 256) {
+            const int i = e / FT, f = e % FT;
+            const bool ok = i < n && f0 + f < r;
+            Qt[i * (FT + 1) + f] = ok ? phiq[(row0 + i) * r + f0 + f] : 0.f;
+            Kt[i * (FT + 1) + f] = ok ? phik[(row0 + i) * r + f0 + f] : 0.f;
         }
+        for (int e = tid; e < FT * W; e += 256) {
+            const int f = e / W, c = e % W;
+            const bool ok = f0 + f < r;
+            Rt[f * WP + c] = ok ? R[(size_t)(f0 + f) * W + c] : 0.f;
+            if (states) St[f * WP + c] = ok ? S[(size_t)(f0 + f) * W + c] : 0.f;
+        }
+    };
+    // ---- pass 1
+    float a[4][4] = {}, dvr[4][CV] = {};
+    for (int f0 = 0; f0 < r; f0 += FT) {
         __syncthreads();
-    }
-    for (int e = threadIdx.x; e < n * r; e += blockDim.x) {
-        const int i = e / r, f = e % r;
-        // dphi_q[i][f] = S_f . dnum_i + z_f dden_i + sum_{j <= i} B_ij phi_k[j][f]
-        float aq = S[(size_t)f * (dv + 1) + dv] * y[(size_t)i * (dv + 1) + dv];
-        for (int c = 0; c < dv; ++c) aq = fmaf(S[(size_t)f * (dv + 1) + c], y[(size_t)i * (dv + 1) + c], aq);
-        // dphi_k[i][f] = R_f . v_i + rho_f + sum_{i' >= i} B_i'i phi_q[i'][f]
-        float ak = R[(size_t)f * (dv + 1) + dv];
-        for (int c = 0; c < dv; ++c) ak = fmaf(R[(size_t)f * (dv + 1) + c], load_in(vb, (size_t)i * dv + c), ak);
-        if (causal) {
-            for (int j = 0; j <= i; ++j) aq = fmaf(Bm[i][j], pk[(size_t)j * r + f], aq);
-            for (int j = i; j < n; ++j) ak = fmaf(Bm[j][i], pq[(size_t)j * r + f], ak);
+        load_tiles(f0, false);
+        __syncthreads();
+#pragma unroll 4
+        for (int f = 0; f < FT; ++f) {
+            float qv[4], kv[4], rv[CV];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                qv[u] = Qt[(4 * ty + u) * (FT + 1) + f];
+                kv[u] = Kt[(4 * tx + u) * (FT + 1) + f];
+            }
+#pragma unroll
+            for (int w = 0; w < CV; ++w) rv[w] = Rt[f * WP + tx * CV + w];
+            if (causal) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) a[u][w] = fmaf(qv[u], kv[w], a[u][w]);
+            }
+            // dv rows 4 ty .. + 3 take phi_k of those rows
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float kr = Kt[(4 * ty + u) * (FT + 1) + f];
+#pragma unroll
+                for (int w = 0; w < CV; ++w) dvr[u][w] = fmaf(kr, rv[w], dvr[u][w]);
+            }
         }
-        dphiq[(row0 + i) * r + f] = aq;
-        dphik[(row0 + i) * r + f] = ak;
     }
-    for (int e = threadIdx.x; e < n * dv; e += blockDim.x) {
-        const int j = e / dv, c = e % dv;
-        // dv[j][c] = R[:, c] . phi_k[j] + sum_{i >= j} A_ij dnum_i[c]
-        float acc = 0.f;
-        for (int f = 0; f < r; ++f) acc = fmaf(R[(size_t)f * (dv + 1) + c], pk[(size_t)j * r + f], acc);
-        if (causal)
-            for (int i = j; i < n; ++i) acc = fmaf(A[i][j], y[(size_t)i * (dv + 1) + c], acc);
-        dV[(row0 + j) * dv + c] = acc;
+    if (causal) {
+        // A and B, masked to j <= i
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const int i = 4 * ty + u, j = 4 * tx + w;
+                As[i * (C + 1) + j] = j <= i ? a[u][w] : 0.f;
+            }
+        float b[4][4] = {};
+        for (int c = 0; c < W; ++c) {
+            float yv[4], vv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                yv[u] = Ys[(4 * ty + u) * WP + c];
+                vv[u] = Vs[(4 * tx + u) * WP + c];
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int w = 0; w < 4; ++w) b[u][w] = fmaf(yv[u], vv[w], b[u][w]);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const int i = 4 * ty + u, j = 4 * tx + w;
+                Bs[i * (C + 1) + j] = j <= i ? b[u][w] : 0.f;
+            }
+        __syncthreads();
+        // dv[j][c] += sum_{i >= j} A_ij dnum_i[c]
+        for (int i = 0; i < C; ++i) {
+            float yr[CV];
+#pragma unroll
+            for (int w = 0; w < CV; ++w) yr[w] = Ys[i * WP + tx * CV + w];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float av = As[i * (C + 1) + 4 * ty + u];
+#pragma unroll
+                for (int w = 0; w < CV; ++w) dvr[u][w] = fmaf(av, yr[w], dvr[u][w]);
+            }
+        }
     }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+        if (4 * ty + u < n)
+#pragma unroll
+            for (int w = 0; w < CV; ++w) dV[(row0 + 4 * ty + u) * DV + tx * CV + w] = dvr[u][w];
+    // ---- pass 2: thread (ty, tx) owns rows 4 ty .. + 3, features 2 tx, 2 tx + 1 of each tile
+    for (int f0 = 0; f0 < r; f0 += FT) {
+        __syncthreads();
+        load_tiles(f0, true);
+        __syncthreads();
+        float dq[4][2] = {}, dk[4][2] = {};
+        for (int c = 0; c < W; ++c) {
+            float yv[4], vv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                yv[u] = Ys[(4 * ty + u) * WP + c];
+                vv[u] = Vs[(4 * ty + u) * WP + c];
+            }
+            const float s0 = St[(2 * tx) * WP + c], s1 = St[(2 * tx + 1) * WP + c];
+            const float r0 = Rt[(2 * tx) * WP + c], r1 = Rt[(2 * tx + 1) * WP + c];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                dq[u][0] = fmaf(yv[u], s0, dq[u][0]);
+                dq[u][1] = fmaf(yv[u], s1, dq[u][1]);
+                dk[u][0] = fmaf(vv[u], r0, dk[u][0]);
+                dk[u][1] = fmaf(vv[u], r1, dk[u][1]);
+            }
+        }
+        if (causal) {
+            for (int j = 0; j < C; ++j) {
+                const float k0 = Kt[j * (FT + 1) + 2 * tx], k1 = Kt[j * (FT + 1) + 2 * tx + 1];
+                const float q0 = Qt[j * (FT + 1) + 2 * tx], q1 = Qt[j * (FT + 1) + 2 * tx + 1];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float bij = Bs[(4 * ty + u) * (C + 1) + j];   // B_ij, i = my row
+                    const float bji = Bs[j * (C + 1) + 4 * ty + u];     // B_ji: row j attends my row
+                    dq[u][0] = fmaf(bij, k0, dq[u][0]);
+                    dq[u][1] = fmaf(bij, k1, dq[u][1]);
+                    dk[u][0] = fmaf(bji, q0, dk[u][0]);
+                    dk[u][1] = fmaf(bji, q1, dk[u][1]);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = 4 * ty + u;
+            if (i >= n) continue;
+#pragma unroll
+            for (int w = 0; w < 2; ++w) {
+                const int f = f0 + 2 * tx + w;
+                if (f < r) {
+                    dphiq[(row0 + i) * r + f] = dq[u][w];
+                    dphik[(row0 + i) * r + f] = dk[u][w];
+                }
+            }
+        }
+    }
+}
+
+template <typename T, int DV>
+constexpr size_t bwd_chunk_smem() {
+    return sizeof(float) * (2 * kBwdRows * (DV + 1) + 2 * kBwdRows * (kBwdRows + 1) + 2 * kBwdRows * 33 +
+                            2 * 32 * (DV + 1));
 }
 
 // per (row, projection p): the coefficient c of the map derivative, in place
@@ -608,36 +674,243 @@ __global__ void bwd_dx(const float *__restrict__ C, const float *__restrict__ dp
     }
 }
 
-// dw[h][p][j] += sum over a slice of the head's rows (all batches, queries
-// and keys) of c[row][p] x[row][j]; grid (ceil(nproj d / 256), H, slices)
-template <typename T>
-__global__ void bwd_dw(const float *__restrict__ Cq, const float *__restrict__ Ck, const T *__restrict__ q,
-                       const T *__restrict__ k, float *__restrict__ dw, int B, int H, int L, int d, int nproj,
-                       int slice) {
-    const int e = blockIdx.x * blockDim.x + threadIdx.x, h = blockIdx.y;
-    if (e >= nproj * d) return;
-    const int p = e / d, j = e % d;
-    const int r0 = blockIdx.z * slice, r1 = min(B * L, r0 + slice);
-    float acc = 0.f;
-    for (int t = r0; t < r1; ++t) {
-        const int b = t / L, i = t % L;
-        const size_t row = ((size_t)b * H + h) * L + i;
-        acc = fmaf(Cq[row * nproj + p], load_in(q, row * d + j), acc);
-        acc = fmaf(Ck[row * nproj + p], load_in(k, row * d + j), acc);
+// per chunk of 64 rows: St[f][c] = sum_rows phi[row][f] Yc[row][c], c <= dv, where
+// Yc = [v | 1] (forward state) or the rows' [dnum | dden] (backward state);
+// block per (chunk, head), 256 threads, 32-feature tiles in shared memory;
+// thread (ty, tx) owns features 2 ty, 2 ty + 1 and columns tx, tx + 16, ...
+template <typename T, int DV>
+__global__ void __launch_bounds__(256) state_tile(const float *__restrict__ phi, const T *__restrict__ v,
+                                                  const float *__restrict__ Y, float *__restrict__ S, int L, int r,
+                                                  int nch) {
+    constexpr int C = kBwdRows, FT = 32, W = DV + 1, CW = (W + 15) / 16;
+    __shared__ float Ps[C][FT + 1];
+    __shared__ float Ys[C][W];
+    const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
+    const int ch = blockIdx.x, bh = blockIdx.y, t0 = ch * C, n = min(C, L - t0);
+    const size_t row0 = (size_t)bh * L + t0;
+    for (int e = tid; e < C * W; e += 256) {
+        const int i = e / W, c = e % W;
+        float y = 0.f;
+        if (i < n) y = Y ? Y[(row0 + i) * W + c] : (c < DV ? load_in(v, (row0 + i) * DV + c) : 1.f);
+        Ys[i][c] = y;
     }
-    atomicAdd(&dw[((size_t)h * nproj + p) * d + j], acc);
+    float *dst = S + ((size_t)bh * nch + ch) * r * W;
+    for (int f0 = 0; f0 < r; f0 += FT) {
+        __syncthreads();
+        for (int e = tid; e < C * FT; e += 256) {
+            const int i = e / FT, f = e % FT;
+            Ps[i][f] = (i < n && f0 + f < r) ? phi[(row0 + i) * r + f0 + f] : 0.f;
+        }
+        __syncthreads();
+        float acc[2][CW] = {};
+        for (int i = 0; i < C; ++i) {
+            float pv[2], yv[CW];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) pv[u] = Ps[i][2 * ty + u];
+#pragma unroll
+            for (int w = 0; w < CW; ++w) yv[w] = (tx + 16 * w < W) ? Ys[i][tx + 16 * w] : 0.f;
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int w = 0; w < CW; ++w) acc[u][w] = fmaf(pv[u], yv[w], acc[u][w]);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int f = f0 + 2 * ty + u;
+            if (f >= r) continue;
+#pragma unroll
+            for (int w = 0; w < CW; ++w)
+                if (tx + 16 * w < W) dst[(size_t)f * W + tx + 16 * w] = acc[u][w];
+        }
+    }
 }
 
-template <typename T>
-int backward_t(const T *q, const T *k, const T *v, const float *omega, const float *g, float *dq, float *dk,
-               float *dv, float *dw, const Problem &p, cudaStream_t st) {
+// non-causal: the chunk states summed into chunk slot 0 (fixed order)
+__global__ void state_total(float *__restrict__ S, int nch, size_t per, int BH) {
+    const size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+    if (e >= per * BH) return;
+    const int bh = (int)(e / per);
+    const size_t within = e % per;
+    float *base = S + (size_t)bh * nch * per + within;
+    float sum = 0.f;
+    for (int s = 0; s < nch; ++s) sum += base[(size_t)s * per];
+    base[0] = sum;
+}
+
+// per row of a chunk: num, den from the entering state (+ the masked chunk
+// sum), out = num / den, then dnum = g / den and dden = -(g . out) / den into
+// Y [rows][dv + 1].  Block per (chunk, head), 256 threads, tiles as bwd_chunk.
+template <typename T, int DV>
+__global__ void __launch_bounds__(256) bwd_rows(const float *__restrict__ phiq, const float *__restrict__ phik,
+                                                const T *__restrict__ v, const float *__restrict__ Sin,
+                                                const float *__restrict__ g, float *__restrict__ Y, int L, int r,
+                                                int nst, int causal) {
+    constexpr int C = kBwdRows, FT = 32, W = DV + 1, CW = (W + 15) / 16;
+    extern __shared__ float sm[];
+    float(*Qt)[FT + 1] = reinterpret_cast<float(*)[FT + 1]>(sm);
+    float(*Kt)[FT + 1] = reinterpret_cast<float(*)[FT + 1]>(sm + C * (FT + 1));
+    float(*St)[W] = reinterpret_cast<float(*)[W]>(sm + 2 * C * (FT + 1));
+    float(*Vs)[W] = reinterpret_cast<float(*)[W]>(sm + 2 * C * (FT + 1) + FT * W);
+    float(*As)[C + 1] = reinterpret_cast<float(*)[C + 1]>(sm + 2 * C * (FT + 1) + FT * W + C * W);
+    float(*NUM)[W] = Vs;   // the chunk's [num | den] once V is no longer read
+    const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
+    const int ch = blockIdx.x, bh = blockIdx.y, t0 = ch * C, n = min(C, L - t0);
+    const size_t row0 = (size_t)bh * L + t0;
+    const float *S = Sin + ((size_t)bh * nst + (causal ? ch : 0)) * r * W;
+    for (int e = tid; e < C * W; e += 256) {
+        const int i = e / W, c = e % W;
+        Vs[i][c] = i < n ? (c < DV ? load_in(v, (row0 + i) * DV + c) : 1.f) : 0.f;
+    }
+    float a[4][4] = {}, num[4][CW] = {};
+    for (int f0 = 0; f0 < r; f0 += FT) {
+        __syncthreads();
+        for (int e = tid; e < C * FT; e += 256) {
+            const int i = e / FT, f = e % FT;
+            const bool ok = i < n && f0 + f < r;
+            Qt[i][f] = ok ? phiq[(row0 + i) * r + f0 + f] : 0.f;
+            Kt[i][f] = ok ? phik[(row0 + i) * r + f0 + f] : 0.f;
+        }
+        for (int e = tid; e < FT * W; e += 256) {
+            const int f = e / W, c = e % W;
+            St[f][c] = f0 + f < r ? S[(size_t)(f0 + f) * W + c] : 0.f;
+        }
+        __syncthreads();
+        for (int f = 0; f < FT; ++f) {
+            float qv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) qv[u] = Qt[4 * ty + u][f];
+            if (causal) {
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const float kv = Kt[4 * tx + w][f];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) a[u][w] = fmaf(qv[u], kv, a[u][w]);
+                }
+            }
+#pragma unroll
+            for (int w = 0; w < CW; ++w) {
+                const float sv = (tx + 16 * w < W) ? St[f][tx + 16 * w] : 0.f;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) num[u][w] = fmaf(qv[u], sv, num[u][w]);
+            }
+        }
+    }
+    if (causal) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int w = 0; w < 4; ++w) As[4 * ty + u][4 * tx + w] = (4 * tx + w <= 4 * ty + u) ? a[u][w] : 0.f;
+        __syncthreads();
+        for (int j = 0; j < C; ++j) {
+            float vv[CW];
+#pragma unroll
+            for (int w = 0; w < CW; ++w) vv[w] = (tx + 16 * w < W) ? Vs[j][tx + 16 * w] : 0.f;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float av = As[4 * ty + u][j];
+#pragma unroll
+                for (int w = 0; w < CW; ++w) num[u][w] = fmaf(av, vv[w], num[u][w]);
+            }
+        }
+    }
+    // [num | den] of the chunk's rows -> shared (over V), then row-wise dnum, dden
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int w = 0; w < CW; ++w)
+            if (tx + 16 * w < W) NUM[4 * ty + u][tx + 16 * w] = num[u][w];
+    __syncthreads();
+    const int warp = tid >> 5, lane = tid & 31;
+    for (int i = warp; i < n; i += 8) {
+        const float den = NUM[i][DV];
+        float gdo = 0.f;
+        for (int c = lane; c < DV; c += 32) {
+            const float gi = g[(row0 + i) * DV + c];
+            gdo = fmaf(gi, NUM[i][c] / den, gdo);
+            Y[(row0 + i) * W + c] = gi / den;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) gdo += __shfl_xor_sync(0xffffffffu, gdo, o);
+        if (lane == 0) Y[(row0 + i) * W + DV] = -gdo / den;
+    }
+}
+
+// dw[h][p][j] += over a slice of 512 of the head's rows (all batches; queries
+// and keys): sum_rows c[row][p] x[row][j].  Block per (64-projection tile,
+// slice, head), 256 threads, 32 rows at a time in shared memory: thread
+// (ty, tx) owns projections 4 ty .. + 3 and columns tx, tx + 16, ...; one
+// atomic add per output and block.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) bwd_dw(const float *__restrict__ Cq, const float *__restrict__ Ck,
+                                              const T *__restrict__ q, const T *__restrict__ k,
+                                              float *__restrict__ dw, int B, int H, int L, int nproj) {
+    constexpr int RS = 32, PT = 64, CD = D / 16, SUB = 16;   // 16 sub-slices of 32 rows per block
+    __shared__ float Cs[RS][PT + 1];
+    __shared__ float Xs[RS][D + 1];
+    const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
+    const int p0 = blockIdx.x * PT, h = blockIdx.z;
+    float acc[4][CD] = {};
+    for (int sub = 0; sub < SUB; ++sub)
+    for (int side = 0; side < 2; ++side) {
+        const int r0 = (blockIdx.y * SUB + sub) * RS;      // 32 of the B L rows of head h
+        const float *Cm = side ? Ck : Cq;
+        const T *X = side ? k : q;
+        __syncthreads();
+        for (int e = tid; e < RS * PT; e += 256) {
+            const int i = e / PT, p = e % PT, t = r0 + i;
+            float cv = 0.f;
+            if (t < B * L && p0 + p < nproj) {
+                const size_t row = ((size_t)(t / L) * H + h) * L + t % L;
+                cv = Cm[row * nproj + p0 + p];
+            }
+            Cs[i][p] = cv;
+        }
+        for (int e = tid; e < RS * D; e += 256) {
+            const int i = e / D, j = e % D, t = r0 + i;
+            float xv = 0.f;
+            if (t < B * L) {
+                const size_t row = ((size_t)(t / L) * H + h) * L + t % L;
+                xv = load_in(X, row * D + j);
+            }
+            Xs[i][j] = xv;
+        }
+        __syncthreads();
+        for (int i = 0; i < RS; ++i) {
+            float cv[4], xv[CD];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) cv[u] = Cs[i][4 * ty + u];
+#pragma unroll
+            for (int w = 0; w < CD; ++w) xv[w] = Xs[i][tx + 16 * w];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int w = 0; w < CD; ++w) acc[u][w] = fmaf(cv[u], xv[w], acc[u][w]);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int p = p0 + 4 * ty + u;
+        if (p >= nproj) continue;
+#pragma unroll
+        for (int w = 0; w < CD; ++w) atomicAdd(&dw[((size_t)h * nproj + p) * D + tx + 16 * w], acc[u][w]);
+    }
+}
+
+template <int DV>
+constexpr size_t bwd_rows_smem() {
+    return sizeof(float) * (2 * kBwdRows * 33 + 32 * (DV + 1) + kBwdRows * (DV + 1) + kBwdRows * (kBwdRows + 1));
+}
+
+template <typename T, int DV>
+int backward_dv(const T *q, const T *k, const T *v, const float *omega, const float *g, float *dq, float *dk,
+                float *dv, float *dw, const Problem &p, cudaStream_t st) {
     const size_t rows = (size_t)p.BH * p.L;
-    const int nch = p.causal ? (p.L + kBwdRows - 1) / kBwdRows : 1;
-    const int seg = p.causal ? kBwdRows : p.L;
-    const size_t per = (size_t)p.r * (p.dv + 1);
+    const int nch = (p.L + kBwdRows - 1) / kBwdRows;     // chunks of 64 rows, both modes
+    const size_t per = (size_t)p.r * (DV + 1);
     size_t bytes = 2 * carve_bytes<float>(rows * p.nproj) + 4 * carve_bytes<float>(rows * p.r) +
                    2 * carve_bytes<float>(rows) + carve_bytes<float>(p.BH) +
-                   2 * carve_bytes<float>((size_t)p.BH * nch * per) + carve_bytes<float>(rows * (p.dv + 1));
+                   2 * carve_bytes<float>((size_t)p.BH * nch * per) + carve_bytes<float>(rows * (DV + 1));
     int status = FAVOR_OK;
     void *ws = workspace(bytes, &status);
     if (!ws) return status;
@@ -648,7 +921,7 @@ int backward_t(const T *q, const T *k, const T *v, const float *omega, const flo
     float *lsq = cv.take<float>(rows), *lsk = cv.take<float>(rows);
     float *hmax = cv.take<float>(p.BH);
     float *S = cv.take<float>((size_t)p.BH * nch * per), *R = cv.take<float>((size_t)p.BH * nch * per);
-    float *Y = cv.take<float>(rows * (p.dv + 1));
+    float *Y = cv.take<float>(rows * (DV + 1));
 
     int rc;
     if ((rc = features_into<T>(q, omega, Pq, phiq, lsq, p, st)) || (rc = features_into<T>(k, omega, Pk, phik, lsk, p, st)))
@@ -659,27 +932,42 @@ int backward_t(const T *q, const T *k, const T *v, const float *omega, const flo
     const unsigned sg = (unsigned)std::min<size_t>((total + 255) / 256, 152 * 64);
     simt_key_scale<<<sg, 256, 0, st>>>(phik, lsk, hmax, p.L, p.r, total);
     FAVOR_LAUNCH_CHECK();
-    // the forward states entering each chunk (causal) or the total
-    simt_state<T><<<dim3((p.r + 31) / 32, p.dv + 1, p.BH * nch), 32, 0, st>>>(phik, v, S, p.L, p.r, p.dv, seg, nch);
+    const dim3 cg(nch, p.BH);
+    const unsigned sb = (unsigned)((per * p.BH + 255) / 256);
+    // the forward states entering each chunk (causal: exclusive prefix) or the total (chunk slot 0)
+    state_tile<T, DV><<<cg, 256, 0, st>>>(phik, v, nullptr, S, p.L, p.r, nch);
     FAVOR_LAUNCH_CHECK();
-    if (p.causal) {
-        simt_state_prefix<<<(unsigned)((per * p.BH + 255) / 256), 256, 0, st>>>(S, nch, per, p.BH);
+    if (p.causal) simt_state_prefix<<<sb, 256, 0, st>>>(S, nch, per, p.BH);
+    else state_total<<<sb, 256, 0, st>>>(S, nch, per, p.BH);
+    FAVOR_LAUNCH_CHECK();
+    {
+        const size_t smem = bwd_rows_smem<DV>();
+        if (cudaFuncSetAttribute(bwd_rows<T, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return FAVOR_ERR_CUDA;
+        }
+        bwd_rows<T, DV><<<cg, 256, smem, st>>>(phiq, phik, v, S, g, Y, p.L, p.r, nch, p.causal);
         FAVOR_LAUNCH_CHECK();
     }
-    const dim3 cg((p.L + kBwdRows - 1) / kBwdRows, p.BH);
-    bwd_rows<T><<<cg, 256, 0, st>>>(phiq, phik, v, S, g, Y, p.L, p.r, p.dv, nch, p.causal);
+    // the states leaving each chunk (causal: exclusive suffix) or the total
+    state_tile<T, DV><<<cg, 256, 0, st>>>(phiq, v, Y, R, p.L, p.r, nch);
     FAVOR_LAUNCH_CHECK();
-    // the states leaving each chunk: exclusive suffix (causal) or the total
-    bwd_state<<<dim3((p.r + 31) / 32, p.dv + 1, p.BH * nch), 32, 0, st>>>(phiq, Y, R, p.L, p.r, p.dv, seg, nch);
+    if (p.causal) bwd_state_suffix<<<sb, 256, 0, st>>>(R, nch, per, p.BH);
+    else state_total<<<sb, 256, 0, st>>>(R, nch, per, p.BH);
     FAVOR_LAUNCH_CHECK();
-    if (p.causal) {
-        bwd_state_suffix<<<(unsigned)((per * p.BH + 255) / 256), 256, 0, st>>>(R, nch, per, p.BH);
+    {
+        const size_t smem = bwd_chunk_smem<T, DV>();
+        if (cudaFuncSetAttribute(bwd_chunk<T, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return FAVOR_ERR_CUDA;
+        }
+        stats_begin(st, "bwd_chunk");
+        bwd_chunk<T, DV><<<cg, 256, smem, st>>>(phiq, phik, v, S, R, Y, dphiq, dphik, dv, p.L, p.r, nch, p.causal);
+        stats_end(st);
         FAVOR_LAUNCH_CHECK();
     }
-    stats_begin(st, "bwd_chunk");
-    bwd_chunk<T><<<cg, 256, 0, st>>>(phiq, phik, v, S, R, Y, dphiq, dphik, dv, p.L, p.r, p.dv, nch, p.causal);
-    stats_end(st);
-    FAVOR_LAUNCH_CHECK();
     const unsigned cgr = (unsigned)std::min<size_t>((rows * p.nproj + 255) / 256, 152 * 64);
     bwd_coeff<<<cgr, 256, 0, st>>>(Pq, dphiq, phiq, lsq, hmax, rows, p.L, p.nproj, p.r, p.map, 0);
     FAVOR_LAUNCH_CHECK();
@@ -692,13 +980,21 @@ int backward_t(const T *q, const T *k, const T *v, const float *omega, const flo
     FAVOR_LAUNCH_CHECK();
     if (dw && !map_is_elementwise(p.map)) {
         if (cudaMemsetAsync(dw, 0, (size_t)p.H * p.nproj * p.d * sizeof(float), st) != cudaSuccess) return FAVOR_ERR_CUDA;
-        const int brows = p.B * p.L, slices = std::max(1, std::min(64, brows / 256));
-        const int slice = (brows + slices - 1) / slices;
-        bwd_dw<T><<<dim3((p.nproj * p.d + 255) / 256, p.H, slices), 256, 0, st>>>(Pq, Pk, q, k, dw, p.B, p.H, p.L,
-                                                                                  p.d, p.nproj, slice);
+        const dim3 wg((p.nproj + 63) / 64, (p.B * p.L + 511) / 512, p.H);
+        if (p.d == 32) bwd_dw<T, 32><<<wg, 256, 0, st>>>(Pq, Pk, q, k, dw, p.B, p.H, p.L, p.nproj);
+        else if (p.d == 64) bwd_dw<T, 64><<<wg, 256, 0, st>>>(Pq, Pk, q, k, dw, p.B, p.H, p.L, p.nproj);
+        else bwd_dw<T, 128><<<wg, 256, 0, st>>>(Pq, Pk, q, k, dw, p.B, p.H, p.L, p.nproj);
         FAVOR_LAUNCH_CHECK();
     }
     return FAVOR_OK;
+}
+
+template <typename T>
+int backward_t(const T *q, const T *k, const T *v, const float *omega, const float *g, float *dq, float *dk,
+               float *dv, float *dw, const Problem &p, cudaStream_t st) {
+    if (p.dv == 32) return backward_dv<T, 32>(q, k, v, omega, g, dq, dk, dv, dw, p, st);
+    if (p.dv == 64) return backward_dv<T, 64>(q, k, v, omega, g, dq, dk, dv, dw, p, st);
+    return backward_dv<T, 128>(q, k, v, omega, g, dq, dk, dv, dw, p, st);
 }
 }  // namespace
 
