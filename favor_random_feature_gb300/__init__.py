@@ -32,6 +32,7 @@ FAVOR_MAP_TRIG_SOFTMAX = 4
 EXPORTS = (
     "favor_attn_forward",
     "favor_attn_forward_noalloc",
+    "favor_attn_forward_bf16out",
     "favor_attn_forward_f32",
     "favor_attn_forward_host",
     "favor_feature_map",
@@ -77,7 +78,7 @@ def lib() -> ctypes.CDLL:
         vp, i, fp = ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p
         fwd = [vp, vp, vp, fp, fp] + [i] * 8 + [vp]
         for name in ("favor_attn_forward", "favor_attn_forward_f32", "favor_attn_forward_host",
-                     "favor_attn_forward_noalloc"):
+                     "favor_attn_forward_noalloc", "favor_attn_forward_bf16out"):
             getattr(L, name).argtypes = fwd
             getattr(L, name).restype = i
         L.favor_feature_map.argtypes = [vp, fp, fp, fp] + [i] * 7 + [vp]
@@ -144,6 +145,12 @@ def favor_attn_forward(q, k, v, omega, out, B, H, L, d, dv, m, causal, feature_m
 def favor_attn_forward_noalloc(q, k, v, omega, out, B, H, L, d, dv, m, causal, feature_map,
                                stream=None):
     return lib().favor_attn_forward_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(omega), _ptr(out),
+                                            B, H, L, d, dv, m, int(causal), int(feature_map),
+                                            _stream(stream))
+
+
+def favor_attn_forward_bf16out(q, k, v, omega, out, B, H, L, d, dv, m, causal, feature_map, stream=None):
+    return lib().favor_attn_forward_bf16out(_ptr(q), _ptr(k), _ptr(v), _ptr(omega), _ptr(out),
                                             B, H, L, d, dv, m, int(causal), int(feature_map),
                                             _stream(stream))
 

@@ -161,7 +161,7 @@ int validate_args(const void *q, const void *k, const void *v, const float *omeg
         return rc;
     if ((rc = check_ptr(omega, map_is_elementwise(p.map)))) return rc;
     size_t rows = (size_t)p.BH * p.L;
-    size_t out_bytes = rows * p.dv * sizeof(float);
+    size_t out_bytes = rows * p.dv * (p.out_bf16 ? 2 : sizeof(float));
     if (overlaps(out, out_bytes, q, rows * p.d * esize) ||
         overlaps(out, out_bytes, k, rows * p.d * esize) ||
         overlaps(out, out_bytes, v, rows * p.dv * esize) ||
@@ -190,6 +190,19 @@ extern "C" int favor_attn_forward(const void *q, const void *k, const void *v, c
     if ((rc = validate_args(q, k, v, omega, out, 2, p))) return rc;
     if (tc_supported(p)) return tc_forward(q, k, v, omega, out, p, stream);
     return simt_forward(q, k, v, true, omega, out, p, stream);
+}
+
+extern "C" int favor_attn_forward_bf16out(const void *q, const void *k, const void *v, const float *omega,
+                                          void *out, int B, int H, int L, int d, int dv, int m, int causal,
+                                          int feature_map, cudaStream_t stream) {
+    Problem p;
+    int rc = make_problem(B, H, L, d, dv, m, causal, feature_map, &p);
+    if (rc) return rc;
+    p.out_bf16 = 1;
+    float *o = static_cast<float *>(out);   // bf16 storage; the kernels take the element type from p
+    if ((rc = validate_args(q, k, v, omega, o, 2, p))) return rc;
+    if (tc_supported(p)) return tc_forward(q, k, v, omega, o, p, stream);
+    return simt_forward(q, k, v, true, omega, o, p, stream);
 }
 
 extern "C" int favor_attn_forward_f32(const float *q, const float *k, const float *v,

@@ -17,6 +17,7 @@ struct Problem {
     int nproj;    // projections per token: m (positive, trig) or d (elu1)
     int r;        // feature columns: m, 2m or d
     int BH;       // B * H
+    int out_bf16 = 0;   // out stored as bf16 (else fp32)
 };
 
 // elu1, relu: r = d features straight from x (no projection); trig and its

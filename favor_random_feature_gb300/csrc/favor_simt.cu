@@ -20,6 +20,8 @@
 //      -- study notes "Case 2" (prefix sum), diagonal included.
 #include <cmath>
 
+#include <cuda_bf16.h>
+
 #include "favor_internal.h"
 
 namespace favor {
@@ -31,6 +33,8 @@ __device__ __forceinline__ float load_in(const float *p, size_t i) { return p[i]
 __device__ __forceinline__ float load_in(const uint16_t *p, size_t i) {
     return __uint_as_float(static_cast<uint32_t>(p[i]) << 16);
 }
+__device__ __forceinline__ void store_out(float *p, size_t i, float v) { p[i] = v; }
+__device__ __forceinline__ void store_out(__nv_bfloat16 *p, size_t i, float v) { p[i] = __float2bfloat16_rn(v); }
 
 // 1. projections: block = 32 tokens x 32 projections, x and omega tiles in smem.
 template <typename T>
@@ -197,8 +201,9 @@ __global__ void simt_state_prefix(float *__restrict__ S, int nseg, size_t per_se
 }
 
 // 4a. non-causal output: thread per (row, c).
+template <typename O>
 __global__ void simt_out_noncausal(const float *__restrict__ phiq, const float *__restrict__ S,
-                                   float *__restrict__ out, int L, int r, int dv) {
+                                   O *__restrict__ out, int L, int r, int dv) {
     const int c = threadIdx.x;
     const int row = blockIdx.x * blockDim.y + threadIdx.y;
     const int bh = blockIdx.y;
@@ -211,14 +216,14 @@ __global__ void simt_out_noncausal(const float *__restrict__ phiq, const float *
         num = fmaf(a, Sb[(size_t)f * (dv + 1) + c], num);
         den = fmaf(a, Sb[(size_t)f * (dv + 1) + dv], den);
     }
-    out[((size_t)bh * L + row) * dv + c] = num / den;
+    store_out(out, ((size_t)bh * L + row) * dv + c, num / den);
 }
 
 // 4b. causal output: block per (chunk, head), 256 threads.
-template <typename T>
+template <typename T, typename O>
 __global__ void simt_out_causal(const float *__restrict__ phiq, const float *__restrict__ phik,
                                 const T *__restrict__ v, const float *__restrict__ Sin,
-                                float *__restrict__ out, int L, int r, int dv, int nch) {
+                                O *__restrict__ out, int L, int r, int dv, int nch) {
     __shared__ float A[kChunk][kChunk + 1];
     __shared__ float den_s[kChunk];
     const int ch = blockIdx.x, bh = blockIdx.y;
@@ -249,7 +254,7 @@ __global__ void simt_out_causal(const float *__restrict__ phiq, const float *__r
         float num = 0.f;
         for (int f = 0; f < r; ++f) num = fmaf(pq[(size_t)i * r + f], Sb[(size_t)f * (dv + 1) + c], num);
         for (int j = 0; j <= i; ++j) num = fmaf(A[i][j], load_in(vb, (size_t)j * dv + c), num);
-        out[((size_t)bh * L + t0 + i) * dv + c] = num / den_s[i];
+        store_out(out, ((size_t)bh * L + t0 + i) * dv + c, num / den_s[i]);
     }
 }
 
@@ -307,7 +312,10 @@ int forward_t(const T *q, const T *k, const T *v, const float *omega, float *out
         dim3 blk(p.dv, std::max(1, 256 / p.dv));
         dim3 og((p.L + blk.y - 1) / blk.y, p.BH);
         stats_begin(st, "simt_out_noncausal");
-        simt_out_noncausal<<<og, blk, 0, st>>>(phiq, S, out, p.L, p.r, p.dv);
+        if (p.out_bf16)
+            simt_out_noncausal<<<og, blk, 0, st>>>(phiq, S, reinterpret_cast<__nv_bfloat16 *>(out), p.L, p.r, p.dv);
+        else
+            simt_out_noncausal<<<og, blk, 0, st>>>(phiq, S, out, p.L, p.r, p.dv);
         stats_end(st);
         FAVOR_LAUNCH_CHECK();
         return FAVOR_OK;
@@ -316,7 +324,11 @@ int forward_t(const T *q, const T *k, const T *v, const float *omega, float *out
     simt_state_prefix<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(S, nch, per_seg, p.BH);
     FAVOR_LAUNCH_CHECK();
     stats_begin(st, "simt_out_causal");
-    simt_out_causal<T><<<dim3(nch, p.BH), 256, 0, st>>>(phiq, phik, v, S, out, p.L, p.r, p.dv, nch);
+    if (p.out_bf16)
+        simt_out_causal<T, __nv_bfloat16><<<dim3(nch, p.BH), 256, 0, st>>>(
+            phiq, phik, v, S, reinterpret_cast<__nv_bfloat16 *>(out), p.L, p.r, p.dv, nch);
+    else
+        simt_out_causal<T, float><<<dim3(nch, p.BH), 256, 0, st>>>(phiq, phik, v, S, out, p.L, p.r, p.dv, nch);
     stats_end(st);
     FAVOR_LAUNCH_CHECK();
     return FAVOR_OK;

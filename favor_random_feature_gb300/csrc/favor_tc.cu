@@ -25,6 +25,7 @@
 // tc_combine (fixed-order sums / exclusive prefixes of the segment states),
 // tc_output (non-causal rows), tc_causal (the chunked causal scan).
 #include <cmath>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
@@ -742,6 +743,21 @@ constexpr int kKbS = 128, kKbZ = 192;            // first rows of sigma S^T and 
 // small-area float offsets of the barriers, TMEM slot, abort flag; total size
 constexpr int kCausalBars = 1696, kCausalTslot = 1728, kCausalAbort = 1730, kCausalSmall = 1736;
 
+// 16 output values of one row (columns c0 .. c0 + 15) into a 128B-swizzled
+// [128][64] bf16 staging block
+__device__ __forceinline__ void stage_bf16_16(uint8_t *blk, int row, int c0, const float (&o)[16]) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat162 b = __floats2bfloat162_rn(o[8 * h + 2 * i], o[8 * h + 2 * i + 1]);
+            w[i] = *reinterpret_cast<const uint32_t *>(&b);
+        }
+        *reinterpret_cast<uint4 *>(blk + sw128_offset(row, c0 + 8 * h)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
 struct CausalArgs {
     Geo g;
     int H, L, seg_len, nseg;
@@ -749,6 +765,7 @@ struct CausalArgs {
     const float *s_in, *meta_in;   // [BH][nseg][r][dv+1], [BH][nseg][4] (segment 0 unused)
     const float *state, *meta;     // piece states [BH][nstate][r][dv+1], [BH][nstate][n_ft][4]
     int nstate, pps, direct;       // pps pieces per segment; direct: combine the earlier pieces here
+    int out_bf16;                  // out in bf16 (one [128][64] staging block) instead of fp32
     int *status;
     uint32_t o_w, o_x, o_v, o_kb, o_small, tmem_cols;
 };
@@ -777,8 +794,8 @@ __device__ __forceinline__ void kb_state16(uint8_t *kb, int f, int c0, const flo
 }
 
 // NC = projection columns per epilogue thread (a quarter of the projections),
-// MAP the feature map
-template <int NC, int MAP>
+// MAP the feature map, OB16 out stored as bf16
+template <int NC, int MAP, bool OB16>
 __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
                             const CUtensorMap *tm_q, const CUtensorMap *tm_k,
                             const CUtensorMap *tm_v, const CUtensorMap *tm_out) {
@@ -892,7 +909,7 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
                 // has read the staging, the next chunk's key projection
                 if (!(alive = ewait(e_out, ph, abortp))) break;
                 tma_store_3d(tm_out, kb, 64 * dvt, t_begin + c * kC, bh);
-                tma_store_3d(tm_out, kb + kKbBlk, 64 * dvt + 32, t_begin + c * kC, bh);
+                if (!OB16) tma_store_3d(tm_out, kb + kKbBlk, 64 * dvt + 32, t_begin + c * kC, bh);
                 bulk_commit();
                 if (c + 1 < nchunk) {
                     if (!(alive = ewait(e_x, (c + 1) & 1, abortp))) break;
@@ -1259,19 +1276,28 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
             tc_fence_before();
             const float is = pow2_inv_floor(sigma), ir = pow2_inv_floor(rho);   // exact: powers of two
             const float id = __fdividef(1.f, fmaf(ddi, ir, ddx * is));
-            // output columns 16 j .. 16 j + 15 -> staging half (16 j) / 32 (the
-            // phi_K rows of KB block 0 or 1, free since the state update), 128B
-            // swizzle in chunks of 4 floats
-            uint8_t *half = kb + (size_t)((16 * j) >> 5) * kKbBlk;
+            if constexpr (OB16) {
+                // output columns 16 j .. 16 j + 15 -> the bf16 staging block
+                // (phi_K rows of KB block 0, free since the state update)
+                float o[16];
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                const int col = (16 * j + 4 * cc) & 31;
-                const int p = (col >> 2) ^ (row & 7);
-                *reinterpret_cast<float4 *>(half + row * 128 + p * 16) =
-                    make_float4(fmaf(di[4 * cc + 0], ir, dx[4 * cc + 0] * is) * id,
-                                fmaf(di[4 * cc + 1], ir, dx[4 * cc + 1] * is) * id,
-                                fmaf(di[4 * cc + 2], ir, dx[4 * cc + 2] * is) * id,
-                                fmaf(di[4 * cc + 3], ir, dx[4 * cc + 3] * is) * id);
+                for (int i = 0; i < 16; ++i) o[i] = fmaf(di[i], ir, dx[i] * is) * id;
+                stage_bf16_16(kb, row, 16 * j, o);
+            } else {
+                // output columns 16 j .. 16 j + 15 -> staging half (16 j) / 32 (the
+                // phi_K rows of KB block 0 or 1, free since the state update), 128B
+                // swizzle in chunks of 4 floats
+                uint8_t *half = kb + (size_t)((16 * j) >> 5) * kKbBlk;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const int col = (16 * j + 4 * cc) & 31;
+                    const int p = (col >> 2) ^ (row & 7);
+                    *reinterpret_cast<float4 *>(half + row * 128 + p * 16) =
+                        make_float4(fmaf(di[4 * cc + 0], ir, dx[4 * cc + 0] * is) * id,
+                                    fmaf(di[4 * cc + 1], ir, dx[4 * cc + 1] * is) * id,
+                                    fmaf(di[4 * cc + 2], ir, dx[4 * cc + 2] * is) * id,
+                                    fmaf(di[4 * cc + 3], ir, dx[4 * cc + 3] * is) * id);
+                }
             }
             fence_async_smem();
             mbar_arrive(e_out);
@@ -1282,6 +1308,9 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
     if (!alive) set_status(a.status, FAVOR_ERR_TIMEOUT);
 }
 
+// OB16: out stored as bf16 (a kernel of its own, so that the fp32 kernel's
+// registers are allocated for the fp32 epilogue alone)
+template <bool OB16>
 __global__ void __launch_bounds__(kCausalThreads, 1)
 tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_out,
@@ -1314,13 +1343,13 @@ tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     const int nc = a.g.nproj / 4;
     grid_dep_launch();
     if (a.g.map == FAVOR_MAP_POSITIVE) {
-        if (nc == 64) causal_body<64, FAVOR_MAP_POSITIVE>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
-        else causal_body<32, FAVOR_MAP_POSITIVE>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
+        if (nc == 64) causal_body<64, FAVOR_MAP_POSITIVE, OB16>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
+        else causal_body<32, FAVOR_MAP_POSITIVE, OB16>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
     } else if (a.g.map == FAVOR_MAP_TRIG) {
-        if (nc == 32) causal_body<32, FAVOR_MAP_TRIG>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
-        else causal_body<16, FAVOR_MAP_TRIG>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
+        if (nc == 32) causal_body<32, FAVOR_MAP_TRIG, OB16>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
+        else causal_body<16, FAVOR_MAP_TRIG, OB16>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
     } else {
-        causal_body<32, FAVOR_MAP_ELU1>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
+        causal_body<32, FAVOR_MAP_ELU1, OB16>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
     }
     tc_fence_before();
     __syncthreads();
@@ -1340,6 +1369,7 @@ struct OutputArgs {
     Geo g;
     int H, L, total_units, nq;     // nq: Q tile slots (1 or 2)
     const uint8_t *omg, *sop;      // W images; state images [BH][nvb + 1][r][64]
+    int out_bf16;                  // out in bf16 (one [128][64] staging block) instead of fp32
     int *status;
     uint32_t o_w, o_s, o_x, o_stage, o_small, tmem_cols;
 };
@@ -1531,20 +1561,28 @@ __device__ void output_body(const OutputArgs &a, uint8_t *sm, uint32_t tmem,
         group_sync(kEpi);
         {
             const float id = __fdividef(1.f, dd);
-            uint8_t *halfp = stage + (size_t)((16 * j) >> 5) * kBlk;
+            if (a.out_bf16) {
+                float o[16];
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                const int col = (16 * j + 4 * cc) & 31;
-                const int p = (col >> 2) ^ (row & 7);
-                *reinterpret_cast<float4 *>(halfp + row * 128 + p * 16) =
-                    make_float4(dn[4 * cc] * id, dn[4 * cc + 1] * id, dn[4 * cc + 2] * id, dn[4 * cc + 3] * id);
+                for (int i = 0; i < 16; ++i) o[i] = dn[i] * id;
+                stage_bf16_16(stage, row, 16 * j, o);
+            } else {
+                uint8_t *halfp = stage + (size_t)((16 * j) >> 5) * kBlk;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const int col = (16 * j + 4 * cc) & 31;
+                    const int p = (col >> 2) ^ (row & 7);
+                    *reinterpret_cast<float4 *>(halfp + row * 128 + p * 16) =
+                        make_float4(dn[4 * cc] * id, dn[4 * cc + 1] * id, dn[4 * cc + 2] * id, dn[4 * cc + 3] * id);
+                }
             }
         }
         fence_async_smem();
         group_sync(kEpi);
         if (e == 0 && !*abortp) {
             tma_store_3d(tm_out, stage, 64 * unit_dvt(u), unit_c(u) * kC, unit_bh(u));
-            tma_store_3d(tm_out, stage + kBlk, 64 * unit_dvt(u) + 32, unit_c(u) * kC, unit_bh(u));
+            if (!a.out_bf16)
+                tma_store_3d(tm_out, stage + kBlk, 64 * unit_dvt(u) + 32, unit_c(u) * kC, unit_bh(u));
             bulk_commit();
         }
     }
@@ -1886,7 +1924,8 @@ int tc_run(const void *q, const void *k, const void *v, const float *omega, floa
     if ((rc = make_map(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.BH, p.L, p.d, 64)) ||
         (rc = make_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.BH, p.L, p.d, 64)) ||
         (rc = make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.BH, p.L, p.dv, 64)) ||
-        (rc = make_map(&mo, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.BH, p.L, p.dv, 32)))
+        (rc = p.out_bf16 ? make_map(&mo, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.BH, p.L, p.dv, 64)
+                         : make_map(&mo, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.BH, p.L, p.dv, 32)))
         return rc;
 
     tc_prep_omega<<<dim3(32, p.H), 256, 0, st>>>(omega, img, p.H, p.nproj, p.d, p.map);
@@ -1911,7 +1950,7 @@ int tc_run(const void *q, const void *k, const void *v, const float *omega, floa
         oa.g = g; oa.H = p.H; oa.L = p.L;
         oa.total_units = nchunk * p.BH * nvb;
         oa.nq = ol.nq;
-        oa.omg = img; oa.sop = sop; oa.status = dstat;
+        oa.omg = img; oa.sop = sop; oa.status = dstat; oa.out_bf16 = p.out_bf16;
         oa.o_w = ol.o_w; oa.o_s = ol.o_s; oa.o_x = ol.o_x;
         oa.o_stage = ol.o_stage; oa.o_small = ol.o_small; oa.tmem_cols = 512;
         if (cudaFuncSetAttribute(tc_output, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ol.bytes) != cudaSuccess)
@@ -1942,12 +1981,14 @@ int tc_run(const void *q, const void *k, const void *v, const float *omega, floa
     a.H = p.H; a.L = p.L; a.seg_len = seg_len; a.nseg = G;
     a.omg = img; a.s_in = s_in; a.meta_in = meta_in; a.status = dstat;
     a.state = state; a.meta = meta; a.nstate = nstate; a.pps = pl.pps; a.direct = direct ? 1 : 0;
+    a.out_bf16 = p.out_bf16;
     a.o_w = cl.o_w; a.o_x = cl.o_x; a.o_v = cl.o_v; a.o_kb = cl.o_kb; a.o_small = cl.o_small;
     a.tmem_cols = 512;
-    if (cudaFuncSetAttribute(tc_causal, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cl.bytes) != cudaSuccess)
+    auto kern = p.out_bf16 ? tc_causal<true> : tc_causal<false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cl.bytes) != cudaSuccess)
         return FAVOR_ERR_CUDA;
     stats_begin(st, "tc_causal");
-    if ((rc = launch_dependent(tc_causal, dim3(G, nvb, p.BH), dim3(kCausalThreads), cl.bytes, st, mq, mk, mv,
+    if ((rc = launch_dependent(kern, dim3(G, nvb, p.BH), dim3(kCausalThreads), cl.bytes, st, mq, mk, mv,
                                mo, a))) {
         stats_end(st);
         return rc;

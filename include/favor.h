@@ -113,6 +113,14 @@ int favor_attn_forward_noalloc(const void *q, const void *k, const void *v, cons
                                float *out, int B, int H, int L, int d, int dv, int m, int causal,
                                int feature_map, cudaStream_t stream);
 
+/* favor_attn_forward with out stored as bf16 bits [B][H][L][dv] (round to
+ * nearest even from the fp32 result): half the output traffic.  No
+ * counterpart on the pages (they do not state an output type; the default
+ * entry keeps fp32).  Same inputs, conventions and result codes. */
+int favor_attn_forward_bf16out(const void *q, const void *k, const void *v, const float *omega,
+                               void *out, int B, int H, int L, int d, int dv, int m, int causal,
+                               int feature_map, cudaStream_t stream);
+
 /* Same operation and parameters with fp32 q/k/v: computed entirely in fp32
  * (FFMA, accurate expf/sincosf) by SIMT kernels.  Returns favor_status_t. */
 int favor_attn_forward_f32(const float *q, const float *k, const float *v, const float *omega,

@@ -306,3 +306,37 @@ def test_relu_and_softmax_scaled_trig(fmap, causal, dtype):
     else:
         e = row_errors(out, ref)
     assert e.max() <= F32_MAX, e.max()
+
+
+# ---------------------------------------------------------------------------
+# bf16 output (favor_attn_forward_bf16out): the same computation as the fp32
+# entry point with one final rounding, so the result is the fp32 output
+# rounded to nearest even, bit for bit; against the oracle the bar grows by
+# that rounding (2^-8 relative per row at most)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("w,causal,fmap,L", [
+    (CAUSAL8K, True, MAP_POSITIVE, 1000),     # tensor-core scan
+    (NC4096, False, MAP_POSITIVE, 1000),      # tensor-core state + output
+    (CAUSAL8K, True, MAP_TRIG, 700),
+    (NC4096.with_(omega="iid"), True, MAP_RELU, 333),   # SIMT kernels
+    (NC4096.with_(omega="iid"), False, MAP_TRIG_SOFTMAX, 333),
+], ids=["causal", "noncausal", "trig_causal", "relu_simt", "trig_softmax_simt"])
+def test_bf16_output(w, causal, fmap, L):
+    import torch
+    import favor_random_feature_gb300 as fv
+    w = w.with_(feature_map=fmap, m=w.d if fmap == MAP_RELU else w.m)
+    inp = make_inputs(w, L=L, B=1, H=3)
+    q, k, v, om = to_device(inp)
+    m = w.d if fmap == MAP_RELU else w.m
+    out32 = torch.empty((1, 3, L, w.dv), dtype=torch.float32, device="cuda")
+    out16 = torch.empty((1, 3, L, w.dv), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    assert fv.favor_attn_forward(q, k, v, om, out32, 1, 3, L, w.d, w.dv, m, int(causal), fmap, stream) == 0
+    assert fv.favor_attn_forward_bf16out(q, k, v, om, out16, 1, 3, L, w.d, w.dv, m, int(causal), fmap,
+                                         stream) == 0
+    assert fv.favor_get_device_status(stream) == fv.FAVOR_OK
+    assert torch.equal(out16, out32.to(torch.bfloat16))
+    if fmap == MAP_POSITIVE:
+        ref = oracle_ref(inp, causal, fmap)
+        e = row_errors(out16.float().cpu().numpy().astype(np.float64), ref)
+        assert e.max() <= BF16_MAX + 2 ** -8 and e.mean() <= BF16_MEAN + 2 ** -8, (e.max(), e.mean())
