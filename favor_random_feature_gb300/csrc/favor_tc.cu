@@ -622,7 +622,7 @@ struct CombineArgs {
     int nseg;              // piece states available
     int pps;               // causal: pieces per scan segment
     int causal;
-    int slice;             // elements per block
+    int slice;             // per block: state elements (causal) or (feature, 8-column) units (non-causal)
     const float *state, *meta;
     uint8_t *sop;          // non-causal: [BH][nvb + 1][r][64] fp16 image
     float *s_in;           // causal: [BH][nout][r][dv+1]
@@ -699,21 +699,36 @@ __global__ void tc_combine(const CombineArgs a) {
     const float sigma = sb > 0.f ? exp2f(floorf(log2f(kSigmaTarget / sb))) : 1.f;
     const int nvb = g.dv / 64;
     uint8_t *img = a.sop + (size_t)bh * (nvb + 1) * g.r * 128;
-    for (size_t e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
-        const int f = (int)(e / W), c = (int)(e % W);
+    // unit u = (feature f, group cg of 8 value columns; cg = dv / 8 is the z
+    // column): the pieces' sum, scaled, rounded and stored as one 16-byte chunk
+    const int ng = g.dv / 8 + 1;
+    const size_t u0 = (size_t)blockIdx.z * a.slice, u1 = min((size_t)g.r * ng, u0 + a.slice);
+    for (size_t u = u0 + threadIdx.x; u < u1; u += blockDim.x) {
+        const int f = (int)(u / ng), cg = (int)(u % ng);
         const int ftile = f / 128;
-        float sum = 0.f;
-        for (int gi = 0; gi < upto; ++gi) sum += st[gi * per + e] * scale[gi * g.n_ft + ftile];
-        if (c == g.dv) {
+        const size_t e = (size_t)f * W + 8 * cg;
+        if (cg * 8 == g.dv) {
             // z atom: column 0 holds sigma z, columns 1..15 (the rest of the
             // N = 80 operand) zero
+            float sum = 0.f;
+            for (int gi = 0; gi < upto; ++gi) sum += st[gi * per + e] * scale[gi * g.n_ft + ftile];
             uint8_t *za = img + (size_t)nvb * g.r * 128;
             const uint32_t lo = __half_as_ushort(__float2half_rn(sum * sigma));
             *reinterpret_cast<uint4 *>(za + sw128_offset(f, 0)) = make_uint4(lo, 0u, 0u, 0u);
             *reinterpret_cast<uint4 *>(za + sw128_offset(f, 8)) = make_uint4(0u, 0u, 0u, 0u);
-        } else
-            *reinterpret_cast<__half *>(img + (size_t)(c / 64) * g.r * 128 + sw128_offset(f, c % 64)) =
-                __float2half_rn(sum * sigma);
+            continue;
+        }
+        float sum[8] = {};
+        for (int gi = 0; gi < upto; ++gi) {
+            const float sc = scale[gi * g.n_ft + ftile];
+            const float *src = st + gi * per + e;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) sum[i] = fmaf(src[i], sc, sum[i]);
+        }
+        const int c0 = 8 * cg;
+        *reinterpret_cast<uint4 *>(img + (size_t)(c0 / 64) * g.r * 128 + sw128_offset(f, c0 % 64)) =
+            make_uint4(pack_half2(sum[0] * sigma, sum[1] * sigma), pack_half2(sum[2] * sigma, sum[3] * sigma),
+                       pack_half2(sum[4] * sigma, sum[5] * sigma), pack_half2(sum[6] * sigma, sum[7] * sigma));
     }
 }
 
@@ -1941,8 +1956,8 @@ int tc_run(const void *q, const void *k, const void *v, const float *omega, floa
         CombineArgs ca{};
         ca.g = g; ca.nseg = nstate; ca.pps = 1; ca.causal = 0; ca.state = state; ca.meta = meta;
         ca.sop = sop;
-        ca.slice = 2048;
-        const int nsl = (int)((per_state + ca.slice - 1) / ca.slice);
+        ca.slice = 256;   // units of (feature, 8 value columns)
+        const int nsl = (int)(((size_t)p.r * (p.dv / 8 + 1) + ca.slice - 1) / ca.slice);
         if ((rc = launch_dependent(tc_combine, dim3(p.BH, 1, nsl), dim3(256), 0, st, ca))) return rc;
         FAVOR_LAUNCH_CHECK();
         OutputLayout ol = output_layout(g);
