@@ -36,44 +36,57 @@ __device__ __forceinline__ float load_in(const uint16_t *p, size_t i) {
 __device__ __forceinline__ void store_out(float *p, size_t i, float v) { p[i] = v; }
 __device__ __forceinline__ void store_out(__nv_bfloat16 *p, size_t i, float v) { p[i] = __float2bfloat16_rn(v); }
 
-// 1. projections: block = 32 tokens x 32 projections, x and omega tiles in smem.
+// 1. projections P[t][n] = w_n . x_t: block = 64 tokens x 64 projections of
+// one head, 256 threads with 4 x 4 register tiles, x and omega in 32-wide
+// slices of d in shared memory.
 template <typename T>
-__global__ void simt_project(const T *__restrict__ x, const float *__restrict__ omega,
-                             float *__restrict__ P, int H, int L, int d, int nproj, int identity) {
-    __shared__ float xs[32][129];
-    __shared__ float ws[32][129];
+__global__ void __launch_bounds__(256) simt_project(const T *__restrict__ x, const float *__restrict__ omega,
+                                                    float *__restrict__ P, int H, int L, int d, int nproj,
+                                                    int identity) {
+    constexpr int TT = 64, NT = 64, KT = 32;
+    __shared__ float xs[TT][KT + 1];
+    __shared__ float ws[NT][KT + 1];
     const int bh = blockIdx.z, h = bh % H;
-    const int t0 = blockIdx.x * 32, n0 = blockIdx.y * 32;
+    const int t0 = blockIdx.x * TT, n0 = blockIdx.y * NT;
+    const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
     const T *xb = x + (size_t)bh * L * d;
-    for (int e = threadIdx.x; e < 32 * d; e += blockDim.x) {
-        int t = e / d, j = e % d;
-        xs[t][j] = (t0 + t < L) ? load_in(xb, (size_t)(t0 + t) * d + j) : 0.f;
-    }
-    for (int e = threadIdx.x; e < 32 * d; e += blockDim.x) {
-        int n = e / d, j = e % d;
-        float w = 0.f;
-        if (n0 + n < nproj) {
-            w = identity ? (n0 + n == j ? 1.f : 0.f)
-                         : omega[((size_t)h * nproj + n0 + n) * d + j];
+    float acc[4][4] = {};
+    for (int k0 = 0; k0 < d; k0 += KT) {
+        __syncthreads();
+        for (int e = tid; e < TT * KT; e += 256) {
+            const int t = e / KT, j = e % KT;
+            xs[t][j] = (t0 + t < L && k0 + j < d) ? load_in(xb, (size_t)(t0 + t) * d + k0 + j) : 0.f;
         }
-        ws[n][j] = w;
+        for (int e = tid; e < NT * KT; e += 256) {
+            const int n = e / KT, j = e % KT;
+            float w = 0.f;
+            if (n0 + n < nproj && k0 + j < d)
+                w = identity ? (n0 + n == k0 + j ? 1.f : 0.f) : omega[((size_t)h * nproj + n0 + n) * d + k0 + j];
+            ws[n][j] = w;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int j = 0; j < KT; ++j) {
+            float xv[4], wv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                xv[u] = xs[4 * ty + u][j];
+                wv[u] = ws[4 * tx + u][j];
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int w = 0; w < 4; ++w) acc[u][w] = fmaf(xv[u], wv[w], acc[u][w]);
+        }
     }
-    __syncthreads();
-    // 256 threads: thread -> (n = tid % 32, token group tid / 32 -> 4 tokens)
-    const int n = threadIdx.x % 32, tg = threadIdx.x / 32;
-    float acc[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) acc[i] = 0.f;
-    for (int j = 0; j < d; ++j) {
-        float w = ws[n][j];
+    for (int u = 0; u < 4; ++u) {
+        const int t = t0 + 4 * ty + u;
+        if (t >= L) continue;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) acc[i] = fmaf(w, xs[tg * 4 + i][j], acc[i]);
-    }
-    if (n0 + n < nproj) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            int t = t0 + tg * 4 + i;
-            if (t < L) P[((size_t)bh * L + t) * nproj + n0 + n] = acc[i];
+        for (int w = 0; w < 4; ++w) {
+            const int n = n0 + 4 * tx + w;
+            if (n < nproj) P[((size_t)bh * L + t) * nproj + n] = acc[u][w];
         }
     }
 }
@@ -186,17 +199,24 @@ __global__ void simt_state(const float *__restrict__ phik, const T *__restrict__
 }
 
 // 4b. exclusive prefix over chunks, in place.
+// (eight segments' values are loaded before any is stored, so that the
+// loads are in flight together)
 __global__ void simt_state_prefix(float *__restrict__ S, int nseg, size_t per_seg, int BH) {
     size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
     if (e >= per_seg * BH) return;
     int bh = (int)(e / per_seg);
     size_t within = e % per_seg;
+    float *base = S + (size_t)bh * nseg * per_seg + within;
     float run = 0.f;
-    for (int s = 0; s < nseg; ++s) {
-        float *p = S + ((size_t)bh * nseg + s) * per_seg + within;
-        float t = *p;
-        *p = run;
-        run += t;
+    for (int s0 = 0; s0 < nseg; s0 += 8) {
+        float t[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) t[i] = s0 + i < nseg ? base[(size_t)(s0 + i) * per_seg] : 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (s0 + i < nseg) base[(size_t)(s0 + i) * per_seg] = run;
+            run += t[i];
+        }
     }
 }
 
@@ -261,7 +281,7 @@ __global__ void simt_out_causal(const float *__restrict__ phiq, const float *__r
 template <typename T>
 int features_into(const T *x, const float *omega, float *P, float *phi, float *logscale,
                   const Problem &p, cudaStream_t st) {
-    dim3 pg((p.L + 31) / 32, (p.nproj + 31) / 32, p.BH);
+    dim3 pg((p.L + 63) / 64, (p.nproj + 63) / 64, p.BH);
     simt_project<T><<<pg, 256, 0, st>>>(x, omega, P, p.H, p.L, p.d, p.nproj,
                                         map_is_elementwise(p.map));
     FAVOR_LAUNCH_CHECK();
@@ -426,12 +446,17 @@ __global__ void bwd_state_suffix(float *__restrict__ R, int nseg, size_t per_seg
     if (e >= per_seg * BH) return;
     const int bh = (int)(e / per_seg);
     const size_t within = e % per_seg;
+    float *base = R + (size_t)bh * nseg * per_seg + within;
     float run = 0.f;
-    for (int s = nseg - 1; s >= 0; --s) {
-        float *p = R + ((size_t)bh * nseg + s) * per_seg + within;
-        const float t = *p;
-        *p = run;
-        run += t;
+    for (int s0 = nseg - 1; s0 >= 0; s0 -= 8) {
+        float t[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) t[i] = s0 - i >= 0 ? base[(size_t)(s0 - i) * per_seg] : 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (s0 - i >= 0) base[(size_t)(s0 - i) * per_seg] = run;
+            run += t[i];
+        }
     }
 }
 
@@ -653,36 +678,79 @@ __global__ void bwd_coeff(float *__restrict__ P, const float *__restrict__ dphi,
     }
 }
 
-// dx [rows][d] from the coefficients: warp per row, lanes over d
-template <typename T>
-__global__ void bwd_dx(const float *__restrict__ C, const float *__restrict__ dphi, const float *__restrict__ phi,
-                       const T *__restrict__ x, const float *__restrict__ omega, float *__restrict__ dx, size_t rows,
-                       int L, int H, int d, int nproj, int r, int map) {
-    const size_t row = (blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (row >= rows) return;
-    const float *c = C + row * nproj;
+// dx [rows][d] from the coefficients, 64 rows of one head per block (256
+// threads): dx = C w_h (C [rows][nproj] in 32-projection tiles, w_h
+// [nproj][d] likewise), then the map's row term: positive - x sum_p C[p];
+// softmax-scaled trig + x sum_f dphi_f phi_f; elementwise maps dx = C.
+// Thread (ty, tx) owns rows 4 ty .. + 3 and columns tx, tx + 16, ...
+template <typename T, int D>
+__global__ void __launch_bounds__(256) bwd_dx(const float *__restrict__ C, const float *__restrict__ dphi,
+                                              const float *__restrict__ phi, const T *__restrict__ x,
+                                              const float *__restrict__ omega, float *__restrict__ dx, int L, int H,
+                                              int nproj, int r, int map) {
+    constexpr int RB = 64, PT = 32, CD = D / 16;
+    __shared__ float Cs[RB][PT + 1];
+    __shared__ float Ws[PT][D + 1];
+    __shared__ float tot[RB];
+    const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
+    const int t0 = blockIdx.x * RB, bh = blockIdx.y, h = bh % H, n = min(RB, L - t0);
+    const size_t row0 = (size_t)bh * L + t0;
     if (map_is_elementwise(map)) {
-        for (int j = lane; j < d; j += 32) dx[row * d + j] = c[j];
+        for (int e = tid; e < n * D; e += 256) dx[row0 * D + e] = C[row0 * nproj + e];
         return;
     }
-    const int h = (int)((row / L) % H);
-    const float *w = omega + (size_t)h * nproj * d;
-    float tot = 0.f;
-    if (map == FAVOR_MAP_POSITIVE) {
-        for (int p = lane; p < nproj; p += 32) tot += c[p];
-    } else if (map == FAVOR_MAP_TRIG_SOFTMAX) {
-        for (int f = lane; f < r; f += 32) tot = fmaf(dphi[row * r + f], phi[row * r + f], tot);
-    }
+    // the row terms
+    {
+        const int warp = tid >> 5, lane = tid & 31;
+        for (int i = warp; i < RB; i += 8) {
+            float s = 0.f;
+            if (i < n) {
+                if (map == FAVOR_MAP_POSITIVE)
+                    for (int p = lane; p < nproj; p += 32) s += C[(row0 + i) * nproj + p];
+                else if (map == FAVOR_MAP_TRIG_SOFTMAX)
+                    for (int f = lane; f < r; f += 32) s = fmaf(dphi[(row0 + i) * r + f], phi[(row0 + i) * r + f], s);
+            }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-    for (int j = lane; j < d; j += 32) {
-        float acc = 0.f;
-        for (int p = 0; p < nproj; ++p) acc = fmaf(c[p], w[(size_t)p * d + j], acc);
-        const float xj = load_in(x, row * d + j);
-        if (map == FAVOR_MAP_POSITIVE) acc = fmaf(-tot, xj, acc);
-        else if (map == FAVOR_MAP_TRIG_SOFTMAX) acc = fmaf(tot, xj, acc);
-        dx[row * d + j] = acc;
+            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+            if (lane == 0) tot[i] = s;
+        }
+    }
+    const float *w = omega + (size_t)h * nproj * D;
+    float acc[4][CD] = {};
+    for (int p0 = 0; p0 < nproj; p0 += PT) {
+        __syncthreads();
+        for (int e = tid; e < RB * PT; e += 256) {
+            const int i = e / PT, p = e % PT;
+            Cs[i][p] = (i < n && p0 + p < nproj) ? C[(row0 + i) * nproj + p0 + p] : 0.f;
+        }
+        for (int e = tid; e < PT * D; e += 256) {
+            const int p = e / D, j = e % D;
+            Ws[p][j] = p0 + p < nproj ? w[(size_t)(p0 + p) * D + j] : 0.f;
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int p = 0; p < PT; ++p) {
+            float cv[4], wv[CD];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) cv[u] = Cs[4 * ty + u][p];
+#pragma unroll
+            for (int c = 0; c < CD; ++c) wv[c] = Ws[p][tx + 16 * c];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int c = 0; c < CD; ++c) acc[u][c] = fmaf(cv[u], wv[c], acc[u][c]);
+        }
+    }
+    const float sgn = map == FAVOR_MAP_POSITIVE ? -1.f : (map == FAVOR_MAP_TRIG_SOFTMAX ? 1.f : 0.f);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int i = 4 * ty + u;
+        if (i >= n) continue;
+#pragma unroll
+        for (int c = 0; c < CD; ++c) {
+            const int j = tx + 16 * c;
+            dx[(row0 + i) * D + j] = fmaf(sgn * tot[i], load_in(x, (row0 + i) * D + j), acc[u][c]);
+        }
     }
 }
 
@@ -985,11 +1053,17 @@ int backward_dv(const T *q, const T *k, const T *v, const float *omega, const fl
     FAVOR_LAUNCH_CHECK();
     bwd_coeff<<<cgr, 256, 0, st>>>(Pk, dphik, phik, lsk, hmax, rows, p.L, p.nproj, p.r, p.map, 1);
     FAVOR_LAUNCH_CHECK();
-    const unsigned xg = (unsigned)((rows * 32 + 255) / 256);
-    bwd_dx<T><<<xg, 256, 0, st>>>(Pq, dphiq, phiq, q, omega, dq, rows, p.L, p.H, p.d, p.nproj, p.r, p.map);
-    FAVOR_LAUNCH_CHECK();
-    bwd_dx<T><<<xg, 256, 0, st>>>(Pk, dphik, phik, k, omega, dk, rows, p.L, p.H, p.d, p.nproj, p.r, p.map);
-    FAVOR_LAUNCH_CHECK();
+    {
+        const dim3 xg((p.L + 63) / 64, p.BH);
+        auto dx_launch = [&](auto kern) {
+            kern<<<xg, 256, 0, st>>>(Pq, dphiq, phiq, q, omega, dq, p.L, p.H, p.nproj, p.r, p.map);
+            kern<<<xg, 256, 0, st>>>(Pk, dphik, phik, k, omega, dk, p.L, p.H, p.nproj, p.r, p.map);
+        };
+        if (p.d == 32) dx_launch(bwd_dx<T, 32>);
+        else if (p.d == 64) dx_launch(bwd_dx<T, 64>);
+        else dx_launch(bwd_dx<T, 128>);
+        FAVOR_LAUNCH_CHECK();
+    }
     if (dw && !map_is_elementwise(p.map)) {
         if (cudaMemsetAsync(dw, 0, (size_t)p.H * p.nproj * p.d * sizeof(float), st) != cudaSuccess) return FAVOR_ERR_CUDA;
         const dim3 wg((p.nproj + 63) / 64, (p.B * p.L + 511) / 512, p.H);
