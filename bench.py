@@ -35,10 +35,10 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM traffic (read + write bytes per launch) of a kernel from one ncu capture
 # (profiles/), valid while the kernel's source section is unchanged.
 TRAFFIC = {
-    ("tc_causal", "causal8k"): (308.40e6, "736dfb285b43d884"),
+    ("tc_causal", "causal8k"): (308.35e6, "0605ad87d79db580"),
     ("tc_state", "causal8k"): (69.16e6, "be3b5bfdadbd00d1"),
     ("tc_state", "nc4096"): (105.01e6, "be3b5bfdadbd00d1"),
-    ("tc_output", "nc4096"): (103.15e6, "0d1f15dd5f60a63d"),
+    ("tc_output", "nc4096"): (103.19e6, "3912a4eb0b80c731"),
     ("decode_step", "decode_b256"): (496.87e6, "74c42f3d2b49b28e"),
 }
 KERNEL_SECTIONS = {   # kernel: (source file, first line of its section, first line after it)
