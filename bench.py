@@ -181,6 +181,27 @@ def cpu_baseline(inp, causal, heads_per_sample=None):
             "seconds": dt}
 
 
+def max_over_ranks(values, dist, device):
+    """The per-rank timings reduced to their maximum over the ranks (the job
+    takes as long as its slowest replica); unchanged on one process."""
+    if not dist:
+        return list(values)
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_throughput(tokens_per_rank, world, ms):
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank / (ms / 1000.0)
+
+
+def rank_inputs_seed(seed, rank):
+    """Each replica draws its own inputs (rank 0 the workload's seed)."""
+    return seed + 1000 * rank
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -238,7 +259,7 @@ def run_ours(args):
     w, causal = workload(args.workload)
     if args.workload == "long64k_nc":
         causal = False
-    inp = make_inputs(w.with_(seed=w.seed + 1000 * rank)) if rank else make_inputs(w)
+    inp = make_inputs(w.with_(seed=rank_inputs_seed(w.seed, rank)))
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(
         torch.bfloat16).cuda()
     q, k, v = dev(inp.q), dev(inp.k), dev(inp.v)
@@ -303,12 +324,9 @@ def run_ours(args):
     fv.favor_stats_enable(False)
     dom_ms = stats.dominant_ms / max(1, stats.dominant_launches)
     launches_per_step = stats.kernel_launches / stat_steps
-    if dist:
-        t = torch.tensor([ms, dom_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, dom_ms = t.tolist()
+    ms, dom_ms = max_over_ranks([ms, dom_ms], dist, "cuda")
     tokens = w.B * w.H * w.L
-    value = world * tokens / (ms / 1000.0)
+    value = job_throughput(tokens, world, ms)
 
     flops_tok, bytes_tok, exps_tok = per_token(w)
     hbm_gbs, tflops, src = peaks()
@@ -344,10 +362,7 @@ def run_ours(args):
     st = fv.favor_get_device_status(stream)
     if st != fv.FAVOR_OK:
         raise fv.FavorError(st, "device status after the end-to-end steps")
-    if dist:
-        t = torch.tensor([te], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        te = t.item()
+    (te,) = max_over_ranks([te], dist, "cuda")
     h2d = inp.q.nbytes + inp.k.nbytes + inp.v.nbytes + hom.nbytes
     d2h = hout.nbytes
 
