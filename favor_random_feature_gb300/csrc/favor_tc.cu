@@ -1230,6 +1230,18 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
                 red[16 + ew] = ms;
             }
         }
+        // ---------------- next chunk's Q, K (while the tensor core runs the merged MMA) ----------------
+        if (c + 1 < nchunk) {
+            alive &= convert_x(c + 1);   // its group barrier publishes red
+            float vm = red[0], ms = 0.f;
+#pragma unroll
+            for (int i = 0; i < kEpi / 32; ++i) {
+                vm = fmaxf(vm, red[i]);
+                ms += red[16 + i];
+            }
+            vmax = fmaxf(vmax, vm);
+            zmax += ms;
+        }
         // ---------------- intra-chunk matrix -> masked, row-scaled, TMEM ----------------
         alive &= ewait(bar_a, ph, abortp);
         tc_fence_after();
@@ -1266,18 +1278,6 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(e_b);
-        // ---------------- next chunk's Q, K (while the tensor core runs A_m V) ----------------
-        if (c + 1 < nchunk) {
-            alive &= convert_x(c + 1);   // its group barrier publishes red
-            float vm = red[0], ms = 0.f;
-#pragma unroll
-            for (int i = 0; i < kEpi / 32; ++i) {
-                vm = fmaxf(vm, red[i]);
-                ms += red[16 + i];
-            }
-            vmax = fmaxf(vmax, vm);
-            zmax += ms;
-        }
         // ---------------- output ----------------
         alive &= ewait(bar_av, ph, abortp);
         tc_fence_after();
