@@ -798,16 +798,6 @@ __device__ __forceinline__ void kb_store8(uint8_t *kb, int row, int f, const flo
     *reinterpret_cast<uint4 *>(kb + (size_t)(f >> 6) * kKbBlk + sw128_offset(row, f & 63)) = u;
 }
 
-// sigma x 16 state values of feature f (value columns c0 .. c0 + 15) into KB
-// rows kKbS + c0 .. (the K-major rows of sigma S^T), one fp16 each
-__device__ __forceinline__ void kb_state16(uint8_t *kb, int f, int c0, const float (&v)[16], float sc) {
-    uint8_t *base = kb + (size_t)(f >> 6) * kKbBlk + (size_t)(kKbS + c0) * 128 + ((f & 7) << 1);
-    const uint32_t c3 = (uint32_t)(f & 63) >> 3;
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-        *reinterpret_cast<__half *>(base + i * 128 + ((c3 ^ (uint32_t)(i & 7)) << 4)) = __float2half_rn(v[i] * sc);
-}
-
 // NC = projection columns per epilogue thread (a quarter of the projections),
 // MAP the feature map, OB16 out stored as bf16
 template <int NC, int MAP, bool OB16>
@@ -963,25 +953,48 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
     auto state_rows = [&](float alpha) {
         const float bound = zmax * fmaxf(vmax, 1.f);
         sigma = bound > 0.f ? pow2_scale_14(bound) : 1.f;
+        const uint32_t kb_s = smem_u32(kb);
         for (int t = 0; t < nft; ++t) {
             const uint32_t col = kColS + t * kSStride;
-            float s0[16], z0 = 0.f;
-            tmem_ld16(tm_addr(tmem, q, col + 16 * j), s0);
-            if (j == 0) tmem_ld1(tm_addr(tmem, q, col + 64), z0);
-            tmem_ld_wait();
             if (alpha != 1.f) {
+                float s0[16], z0 = 0.f;
+                tmem_ld16(tm_addr(tmem, q, col + 16 * j), s0);
+                if (j == 0) tmem_ld1(tm_addr(tmem, q, col + 64), z0);
+                tmem_ld_wait();
                 uint32_t u[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(s0[i] *= alpha);
+                for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(s0[i] * alpha);
                 tmem_st16(tm_addr(tmem, q, col + 16 * j), u);
-                if (j == 0) tmem_st1(tm_addr(tmem, q, col + 64), z0 *= alpha);
+                if (j == 0) tmem_st1(tm_addr(tmem, q, col + 64), z0 * alpha);
                 tmem_st_wait();
             }
-            const int f = t * 128 + row;
-            kb_state16(kb, f, 16 * j, s0, sigma);
-            if (j == 0)
+            // this warp's 32 features x 16 value columns as four 16-lane x
+            // 8-column fragments [h][g], stored transposed (rows = value
+            // columns, 8 features per 16-byte chunk) by two stmatrix
+            float a4[4][4], z0 = 0.f;
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int g = 0; g < 2; ++g)
+                    tmem_ld_16x256b(tm_addr(tmem, q, col + 16 * j + 8 * g) + ((uint32_t)(16 * h) << 16), a4[2 * h + g]);
+            if (j == 0) tmem_ld1(tm_addr(tmem, q, col + 64), z0);
+            tmem_ld_wait();
+            const int mi = lane >> 3;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int f = t * 128 + 32 * q + 16 * h + 8 * (mi & 1);
+                const int rr = kKbS + 16 * j + 8 * (mi >> 1) + (lane & 7);
+                const uint32_t addr = kb_s + (uint32_t)(f >> 6) * kKbBlk + (uint32_t)rr * 128u +
+                                      ((((uint32_t)(f & 63) >> 3) ^ ((uint32_t)rr & 7u)) << 4);
+                const float(&lo)[4] = a4[2 * h], (&hi)[4] = a4[2 * h + 1];
+                stmatrix_x4_trans(addr, pack_half2(lo[0] * sigma, lo[1] * sigma), pack_half2(lo[2] * sigma, lo[3] * sigma),
+                                  pack_half2(hi[0] * sigma, hi[1] * sigma), pack_half2(hi[2] * sigma, hi[3] * sigma));
+            }
+            if (j == 0) {
+                const int f = t * 128 + row;
                 *reinterpret_cast<__half *>(kb + (size_t)(f >> 6) * kKbBlk + sw128_offset(kKbZ, f & 63)) =
                     __float2half_rn(z0 * sigma);
+            }
         }
     };
     auto convert_x = [&](int c) -> bool {

@@ -223,6 +223,18 @@ __device__ __forceinline__ void tmem_ld1(uint32_t taddr, float &v) {
     v = __uint_as_float(r);
 }
 
+// 16 lanes x 256 bits: thread t receives lane t/4 (columns 2 (t % 4), +1) in
+// v[0], v[1] and lane t/4 + 8 (the same columns) in v[2], v[3] -- the
+// fragment layout stmatrix takes
+__device__ __forceinline__ void tmem_ld_16x256b(uint32_t taddr, float (&v)[4]) {
+    uint32_t r[4];
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -382,6 +394,17 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.f16x2.f32 %0, %2, %1;" : "=r"(r) : "f"(lo), "f"(hi));
     return r;
+}
+
+// four 8x8 fp16 matrices, transposed on the way: register i of thread t holds
+// row t/4, columns 2 (t % 4), +1 of matrix i; threads 8i .. 8i + 7 give the
+// shared-memory addresses of the eight stored rows of matrix i (row j = column
+// j of the held matrix, 16 bytes each)
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t saddr, uint32_t r0, uint32_t r1, uint32_t r2,
+                                                  uint32_t r3) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(saddr), "r"(r0),
+                 "r"(r1), "r"(r2), "r"(r3)
+                 : "memory");
 }
 
 // max of three (one instruction on sm_100 and later)
