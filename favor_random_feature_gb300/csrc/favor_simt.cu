@@ -439,6 +439,7 @@ int simt_feature_map(const void *x, bool bf16_in, const float *omega, float *phi
 namespace {
 
 constexpr int kBwdRows = 64;    // rows per chunk (= kChunk)
+constexpr int kBwdThreads = 256;   // threads of a bwd_chunk block
 
 // exclusive suffix over segments, in place: R_s <- sum_{s' > s} R_s'
 __global__ void bwd_state_suffix(float *__restrict__ R, int nseg, size_t per_seg, int BH) {
@@ -460,182 +461,225 @@ __global__ void bwd_state_suffix(float *__restrict__ R, int nseg, size_t per_seg
     }
 }
 
-// dphi_q, dphi_k [rows][r] and dv [rows][dv] of a chunk from the entering
-// state S, the leaving state R and (causal) the masked A, B inside it, in
-// shared-memory tiles: block per (chunk, head), 256 threads; thread t owns
-// rows 4 (t / 16) .. + 3 of every output tile.
-//   pass 1 (32-feature tiles): A += phi_q phi_k^T,  dv += phi_k R[:, :dv]
-//   then B = Y [V | 1]^T, A and B masked to j <= i, dv += A^T dnum
-//   pass 2 (32-feature tiles): dphi_q = Y S^T + B phi_k, dphi_k = [V | 1] R^T + B^T phi_q
+// Register-tiled products of shared-memory tiles for 16 RS threads, ty = tid / 16,
+// tx = tid % 16.  A thread owns rows ty + RS u (u < RU, RS RU = 64) of the result
+// and the columns 4 tx + w (mm_nn) or tx + 16 w (mm_nt), w < 4; the operands are
+// read 4 values of the contraction at a time (16-byte loads: RU + 4 loads per
+// 16 RU FMAs).
+// Row pitches are multiples of 4 floats; the B rows that 16 threads read at once
+// (mm_nt) have an odd pitch in 16-byte units, so those loads do not conflict.
+//   mm_nn: acc[u][w] += sum_k A[ty + RS u][k] B[k][4 tx + w]
+//   mm_nt: acc[u][w] += sum_k A[ty + RS u][k] B[tx + 16 w][k]
+template <int RU = 4, int RS = 16>
+__device__ __forceinline__ void mm_nn(float (&acc)[RU][4], const float *A, int lda, const float *B, int ldb, int K,
+                                      int ty, int tx) {
+#pragma unroll 2
+    for (int k = 0; k < K; k += 4) {
+        float4 a[RU], b[4];
+#pragma unroll
+        for (int u = 0; u < RU; ++u) a[u] = *reinterpret_cast<const float4 *>(A + (ty + RS * u) * lda + k);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) b[kk] = *reinterpret_cast<const float4 *>(B + (k + kk) * ldb + 4 * tx);
+#pragma unroll
+        for (int u = 0; u < RU; ++u) {
+            const float av[4] = {a[u].x, a[u].y, a[u].z, a[u].w};
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                acc[u][0] = fmaf(av[kk], b[kk].x, acc[u][0]);
+                acc[u][1] = fmaf(av[kk], b[kk].y, acc[u][1]);
+                acc[u][2] = fmaf(av[kk], b[kk].z, acc[u][2]);
+                acc[u][3] = fmaf(av[kk], b[kk].w, acc[u][3]);
+            }
+        }
+    }
+}
+
+template <int RU = 4, int RS = 16>
+__device__ __forceinline__ void mm_nt(float (&acc)[RU][4], const float *A, int lda, const float *B, int ldb, int K,
+                                      int ty, int tx) {
+#pragma unroll 2
+    for (int k = 0; k < K; k += 4) {
+        float4 a[RU], b[4];
+#pragma unroll
+        for (int u = 0; u < RU; ++u) a[u] = *reinterpret_cast<const float4 *>(A + (ty + RS * u) * lda + k);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) b[w] = *reinterpret_cast<const float4 *>(B + (tx + 16 * w) * ldb + k);
+#pragma unroll
+        for (int u = 0; u < RU; ++u)
+#pragma unroll
+            for (int w = 0; w < 4; ++w)
+                acc[u][w] = fmaf(a[u].x, b[w].x,
+                                 fmaf(a[u].y, b[w].y, fmaf(a[u].z, b[w].z, fmaf(a[u].w, b[w].w, acc[u][w]))));
+    }
+}
+
+// dphi_q, dphi_k [rows][r] and dv [rows][dv] of a chunk of C = 64 rows from the
+// entering state S, the leaving state R and (causal) the masked A, B inside
+// it; block per (chunk, head), kBwdThreads threads, 64-feature tiles:
+//   B = Y [V | 1]^T, masked to j <= i (and its transpose)
+//   pass 1: A += phi_q phi_k^T,  dv += phi_k R[:, :dv]; then dv += A^T dnum
+//   pass 2: dphi_q = Y S^T + B phi_k,  dphi_k = [V | 1] R^T + B^T phi_q
 template <typename T, int DV>
-__global__ void __launch_bounds__(256) bwd_chunk(const float *__restrict__ phiq, const float *__restrict__ phik,
+__global__ void __launch_bounds__(kBwdThreads) bwd_chunk(const float *__restrict__ phiq, const float *__restrict__ phik,
                                                  const T *__restrict__ v, const float *__restrict__ Sin,
                                                  const float *__restrict__ Rout, const float *__restrict__ Y,
                                                  float *__restrict__ dphiq, float *__restrict__ dphik,
                                                  float *__restrict__ dV, int L, int r, int nst, int causal) {
-    constexpr int C = kBwdRows, FT = 32, W = DV + 1, WP = DV + 1;   // row widths (odd: no bank conflicts)
-    constexpr int CV = DV / 16;                                      // dv columns per thread
-    extern __shared__ float sm[];
-    float *Ys = sm;                      // [C][WP]: dnum | dden
-    float *Vs = Ys + C * WP;             // [C][WP]: v | 1
-    float *As = Vs + C * WP;             // [C][C + 1]
-    float *Bs = As + C * (C + 1);        // [C][C + 1]
-    float *Qt = Bs + C * (C + 1);        // [C][FT + 1]
-    float *Kt = Qt + C * (FT + 1);       // [C][FT + 1]
-    float *St = Kt + C * (FT + 1);       // [FT][WP]
-    float *Rt = St + FT * WP;            // [FT][WP]
+    constexpr int C = kBwdRows, FT = 64, P = FT + 4, W = DV + 1, WP = DV + 4, NG = (DV + 63) / 64;
+    constexpr int NT = kBwdThreads, RS = NT / 16, RU = 64 / RS;
+    extern __shared__ float4 sm4[];
+    float *Ys = reinterpret_cast<float *>(sm4);   // [C][WP]  dnum | dden | 0
+    float *Vs = Ys + C * WP;                      // [C][WP]  v | 1 | 0
+    float *Bs = Vs + C * WP;                      // [C][P]   B
+    float *Bt = Bs + C * P;                       // [C][P]   B^T
+    float *Qt = Bt + C * P;                       // [C][P]   phi_q tile (rows x features); A^T after pass 1
+    float *Kt = Qt + C * P;                       // [C][P]   phi_k tile
+    float *Ss = Kt + C * P;                       // [WP][P]  S^T tile (pass 2); R tile [FT][WP] (pass 1)
+    float *Rs = Ss + WP * P;                      // [WP][P]  R^T tile (pass 2)
     const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
     const int ch = blockIdx.x, bh = blockIdx.y, t0 = ch * C, n = min(C, L - t0);
     const size_t row0 = (size_t)bh * L + t0;
     const size_t st = ((size_t)bh * nst + (causal ? ch : 0)) * r * W;
     const float *S = Sin + st, *R = Rout + st;
-    for (int e = tid; e < C * W; e += 256) {
-        const int i = e / W, c = e % W;
-        Ys[i * WP + c] = i < n ? Y[(row0 + i) * W + c] : 0.f;
-        Vs[i * WP + c] = i < n ? (c < DV ? load_in(v, (row0 + i) * DV + c) : 1.f) : 0.f;
+#pragma unroll 4
+    for (int e = tid; e < C * WP; e += NT) {
+        const int i = e / WP, c = e % WP;
+        const bool ok = i < n && c < W;
+        Ys[e] = ok ? Y[(row0 + i) * W + c] : 0.f;
+        Vs[e] = ok ? (c < DV ? load_in(v, (row0 + i) * DV + c) : 1.f) : 0.f;
     }
-    auto load_tiles = [&](int f0, bool states) {
-        for (int e = tid; e < C * FT; e += 256) {
-            const int i = e / FT, f = e % FT;
-            const bool ok = i < n && f0 + f < r;
-            Qt[i * (FT + 1) + f] = ok ? phiq[(row0 + i) * r + f0 + f] : 0.f;
-            Kt[i * (FT + 1) + f] = ok ? phik[(row0 + i) * r + f0 + f] : 0.f;
-        }
-        for (int e = tid; e < FT * W; e += 256) {
-            const int f = e / W, c = e % W;
-            const bool ok = f0 + f < r;
-            Rt[f * WP + c] = ok ? R[(size_t)(f0 + f) * W + c] : 0.f;
-            if (states) St[f * WP + c] = ok ? S[(size_t)(f0 + f) * W + c] : 0.f;
+    // the next feature tile is read into registers while the current one is
+    // used: phi_q, phi_k (NX float4 each) and the state rows (NS values each)
+    constexpr int NX = C * FT / 4 / NT, NS = (FT * W + NT - 1) / NT;
+    float4 xq[NX], xk[NX];
+    float xs[NS], xr[NS];
+    auto fetch_x = [&](int f0) {
+#pragma unroll
+        for (int k = 0; k < NX; ++k) {
+            const int e = tid + NT * k, i = e / (FT / 4), f = 4 * (e % (FT / 4));
+            const bool ok = i < n && f0 + f < r;   // r % 4 == 0
+            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+            xq[k] = ok ? *reinterpret_cast<const float4 *>(phiq + (row0 + i) * r + f0 + f) : z;
+            xk[k] = ok ? *reinterpret_cast<const float4 *>(phik + (row0 + i) * r + f0 + f) : z;
         }
     };
-    // ---- pass 1
-    float a[4][4] = {}, dvr[4][CV] = {};
-    for (int f0 = 0; f0 < r; f0 += FT) {
-        __syncthreads();
-        load_tiles(f0, false);
-        __syncthreads();
-#pragma unroll 4
-        for (int f = 0; f < FT; ++f) {
-            float qv[4], kv[4], rv[CV];
+    auto put_x = [&]() {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                qv[u] = Qt[(4 * ty + u) * (FT + 1) + f];
-                kv[u] = Kt[(4 * tx + u) * (FT + 1) + f];
-            }
-#pragma unroll
-            for (int w = 0; w < CV; ++w) rv[w] = Rt[f * WP + tx * CV + w];
-            if (causal) {
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-#pragma unroll
-                    for (int w = 0; w < 4; ++w) a[u][w] = fmaf(qv[u], kv[w], a[u][w]);
-            }
-            // dv rows 4 ty .. + 3 take phi_k of those rows
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float kr = Kt[(4 * ty + u) * (FT + 1) + f];
-#pragma unroll
-                for (int w = 0; w < CV; ++w) dvr[u][w] = fmaf(kr, rv[w], dvr[u][w]);
-            }
+        for (int k = 0; k < NX; ++k) {
+            const int e = tid + NT * k, i = e / (FT / 4), f = 4 * (e % (FT / 4));
+            *reinterpret_cast<float4 *>(Qt + i * P + f) = xq[k];
+            *reinterpret_cast<float4 *>(Kt + i * P + f) = xk[k];
         }
-    }
+    };
+    auto fetch_s = [&](const float *src, float(&dst)[NS], int f0) {   // rows f0 .. f0 + FT - 1, all W columns
+#pragma unroll
+        for (int k = 0; k < NS; ++k) {
+            const int e = tid + NT * k, f = e / W, c = e % W;
+            dst[k] = (e < FT * W && f0 + f < r) ? src[(size_t)(f0 + f) * W + c] : 0.f;
+        }
+    };
+    __syncthreads();
     if (causal) {
-        // A and B, masked to j <= i
+        float b[RU][4] = {};
+        mm_nt<RU, RS>(b, Ys, WP, Vs, WP, WP, ty, tx);
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                const int i = 4 * ty + u, j = 4 * tx + w;
-                As[i * (C + 1) + j] = j <= i ? a[u][w] : 0.f;
-            }
-        float b[4][4] = {};
-        for (int c = 0; c < W; ++c) {
-            float yv[4], vv[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                yv[u] = Ys[(4 * ty + u) * WP + c];
-                vv[u] = Vs[(4 * tx + u) * WP + c];
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-#pragma unroll
-                for (int w = 0; w < 4; ++w) b[u][w] = fmaf(yv[u], vv[w], b[u][w]);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
+        for (int u = 0; u < RU; ++u)
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
-                const int i = 4 * ty + u, j = 4 * tx + w;
-                Bs[i * (C + 1) + j] = j <= i ? b[u][w] : 0.f;
+                const int i = ty + RS * u, j = tx + 16 * w;
+                const float x = j <= i ? b[u][w] : 0.f;
+                Bs[i * P + j] = x;
+                Bt[j * P + i] = x;
             }
-        __syncthreads();
-        // dv[j][c] += sum_{i >= j} A_ij dnum_i[c]
-        for (int i = 0; i < C; ++i) {
-            float yr[CV];
-#pragma unroll
-            for (int w = 0; w < CV; ++w) yr[w] = Ys[i * WP + tx * CV + w];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float av = As[i * (C + 1) + 4 * ty + u];
-#pragma unroll
-                for (int w = 0; w < CV; ++w) dvr[u][w] = fmaf(av, yr[w], dvr[u][w]);
-            }
-        }
     }
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-        if (4 * ty + u < n)
-#pragma unroll
-            for (int w = 0; w < CV; ++w) dV[(row0 + 4 * ty + u) * DV + tx * CV + w] = dvr[u][w];
-    // ---- pass 2: thread (ty, tx) owns rows 4 ty .. + 3, features 2 tx, 2 tx + 1 of each tile
+    // ---- pass 1 (R tile row-major [f][WP] in Ss; its pad columns are never read)
+    float a[RU][4] = {}, dvr[NG][RU][4] = {};
+    fetch_x(0);
+    fetch_s(R, xr, 0);
     for (int f0 = 0; f0 < r; f0 += FT) {
         __syncthreads();
-        load_tiles(f0, true);
+        put_x();
+#pragma unroll
+        for (int k = 0; k < NS; ++k) {
+            const int e = tid + NT * k;
+            if (e < FT * W) Ss[(e / W) * WP + e % W] = xr[k];
+        }
         __syncthreads();
-        float dq[4][2] = {}, dk[4][2] = {};
-        for (int c = 0; c < W; ++c) {
-            float yv[4], vv[4];
+        if (f0 + FT < r) {
+            fetch_x(f0 + FT);
+            fetch_s(R, xr, f0 + FT);
+        }
+        if (causal) mm_nt<RU, RS>(a, Qt, P, Kt, P, FT, ty, tx);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                yv[u] = Ys[(4 * ty + u) * WP + c];
-                vv[u] = Vs[(4 * ty + u) * WP + c];
+        for (int g = 0; g < NG; ++g)
+            if (64 * g + 4 * tx < DV) mm_nn<RU, RS>(dvr[g], Kt, P, Ss + 64 * g, WP, FT, ty, tx);
+    }
+    // the first tile of pass 2 is read while A^T dnum is formed
+    fetch_x(0);
+    fetch_s(S, xs, 0);
+    fetch_s(R, xr, 0);
+    __syncthreads();
+    if (causal) {
+#pragma unroll
+        for (int u = 0; u < RU; ++u)
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const int i = ty + RS * u, j = tx + 16 * w;
+                Qt[j * P + i] = j <= i ? a[u][w] : 0.f;   // A^T
             }
-            const float s0 = St[(2 * tx) * WP + c], s1 = St[(2 * tx + 1) * WP + c];
-            const float r0 = Rt[(2 * tx) * WP + c], r1 = Rt[(2 * tx + 1) * WP + c];
+    }
+    // pad rows W .. WP - 1 of the transposed state tiles stay zero through pass 2
+    for (int e = tid; e < (WP - W) * P; e += NT) {
+        Ss[W * P + e] = 0.f;
+        Rs[W * P + e] = 0.f;
+    }
+    __syncthreads();
+    if (causal) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                dq[u][0] = fmaf(yv[u], s0, dq[u][0]);
-                dq[u][1] = fmaf(yv[u], s1, dq[u][1]);
-                dk[u][0] = fmaf(vv[u], r0, dk[u][0]);
-                dk[u][1] = fmaf(vv[u], r1, dk[u][1]);
+        for (int g = 0; g < NG; ++g)
+            if (64 * g + 4 * tx < DV) mm_nn<RU, RS>(dvr[g], Qt, P, Ys + 64 * g, WP, C, ty, tx);
+    }
+#pragma unroll
+    for (int g = 0; g < NG; ++g)
+#pragma unroll
+        for (int u = 0; u < RU; ++u) {
+            const int j = ty + RS * u, c = 64 * g + 4 * tx;
+            if (j < n && c < DV)
+                *reinterpret_cast<float4 *>(dV + (row0 + j) * DV + c) =
+                    make_float4(dvr[g][u][0], dvr[g][u][1], dvr[g][u][2], dvr[g][u][3]);
+        }
+    // ---- pass 2 (S^T, R^T tiles [c][P])
+    for (int f0 = 0; f0 < r; f0 += FT) {
+        __syncthreads();
+        put_x();
+#pragma unroll
+        for (int k = 0; k < NS; ++k) {
+            const int e = tid + NT * k;
+            if (e < FT * W) {
+                const int f = e / W, c = e % W;
+                Ss[c * P + f] = xs[k];
+                Rs[c * P + f] = xr[k];
             }
         }
+        __syncthreads();
+        if (f0 + FT < r) {
+            fetch_x(f0 + FT);
+            fetch_s(S, xs, f0 + FT);
+            fetch_s(R, xr, f0 + FT);
+        }
+        float dq[RU][4] = {}, dk[RU][4] = {};
+        mm_nn<RU, RS>(dq, Ys, WP, Ss, P, WP, ty, tx);
+        mm_nn<RU, RS>(dk, Vs, WP, Rs, P, WP, ty, tx);
         if (causal) {
-            for (int j = 0; j < C; ++j) {
-                const float k0 = Kt[j * (FT + 1) + 2 * tx], k1 = Kt[j * (FT + 1) + 2 * tx + 1];
-                const float q0 = Qt[j * (FT + 1) + 2 * tx], q1 = Qt[j * (FT + 1) + 2 * tx + 1];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float bij = Bs[(4 * ty + u) * (C + 1) + j];   // B_ij, i = my row
-                    const float bji = Bs[j * (C + 1) + 4 * ty + u];     // B_ji: row j attends my row
-                    dq[u][0] = fmaf(bij, k0, dq[u][0]);
-                    dq[u][1] = fmaf(bij, k1, dq[u][1]);
-                    dk[u][0] = fmaf(bji, q0, dk[u][0]);
-                    dk[u][1] = fmaf(bji, q1, dk[u][1]);
-                }
-            }
+            mm_nn<RU, RS>(dq, Bs, P, Kt, P, C, ty, tx);
+            mm_nn<RU, RS>(dk, Bt, P, Qt, P, C, ty, tx);
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int i = 4 * ty + u;
-            if (i >= n) continue;
-#pragma unroll
-            for (int w = 0; w < 2; ++w) {
-                const int f = f0 + 2 * tx + w;
-                if (f < r) {
-                    dphiq[(row0 + i) * r + f] = dq[u][w];
-                    dphik[(row0 + i) * r + f] = dk[u][w];
-                }
+        for (int u = 0; u < RU; ++u) {
+            const int i = ty + RS * u, f = f0 + 4 * tx;
+            if (i < n && f < r) {
+                *reinterpret_cast<float4 *>(dphiq + (row0 + i) * r + f) = make_float4(dq[u][0], dq[u][1], dq[u][2], dq[u][3]);
+                *reinterpret_cast<float4 *>(dphik + (row0 + i) * r + f) = make_float4(dk[u][0], dk[u][1], dk[u][2], dk[u][3]);
             }
         }
     }
@@ -643,8 +687,7 @@ __global__ void __launch_bounds__(256) bwd_chunk(const float *__restrict__ phiq,
 
 template <typename T, int DV>
 constexpr size_t bwd_chunk_smem() {
-    return sizeof(float) * (2 * kBwdRows * (DV + 1) + 2 * kBwdRows * (kBwdRows + 1) + 2 * kBwdRows * 33 +
-                            2 * 32 * (DV + 1));
+    return sizeof(float) * (2 * kBwdRows * (DV + 4) + 4 * kBwdRows * 68 + 2 * (DV + 4) * 68);
 }
 
 // per (row, projection p): the coefficient c of the map derivative, in place
@@ -1044,7 +1087,7 @@ int backward_dv(const T *q, const T *k, const T *v, const float *omega, const fl
             return FAVOR_ERR_CUDA;
         }
         stats_begin(st, "bwd_chunk");
-        bwd_chunk<T, DV><<<cg, 256, smem, st>>>(phiq, phik, v, S, R, Y, dphiq, dphik, dv, p.L, p.r, nch, p.causal);
+        bwd_chunk<T, DV><<<cg, kBwdThreads, smem, st>>>(phiq, phik, v, S, R, Y, dphiq, dphik, dv, p.L, p.r, nch, p.causal);
         stats_end(st);
         FAVOR_LAUNCH_CHECK();
     }
