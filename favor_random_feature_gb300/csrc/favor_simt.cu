@@ -513,6 +513,27 @@ __device__ __forceinline__ void mm_nt(float (&acc)[RU][4], const float *A, int l
     }
 }
 
+// acc[u][w] += sum_k A[k][ty + 16 u] B[k][4 tx + w]: both operands row-major
+// with the contraction along their rows (4 broadcast scalar loads and one
+// 16-byte load per 16 FMAs)
+__device__ __forceinline__ void mm_tn(float (&acc)[4][4], const float *A, int lda, const float *B, int ldb, int K,
+                                      int ty, int tx) {
+#pragma unroll 4
+    for (int k = 0; k < K; ++k) {
+        float a[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) a[u] = A[k * lda + ty + 16 * u];
+        const float4 b = *reinterpret_cast<const float4 *>(B + k * ldb + 4 * tx);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            acc[u][0] = fmaf(a[u], b.x, acc[u][0]);
+            acc[u][1] = fmaf(a[u], b.y, acc[u][1]);
+            acc[u][2] = fmaf(a[u], b.z, acc[u][2]);
+            acc[u][3] = fmaf(a[u], b.w, acc[u][3]);
+        }
+    }
+}
+
 // dphi_q, dphi_k [rows][r] and dv [rows][dv] of a chunk of C = 64 rows from the
 // entering state S, the leaving state R and (causal) the masked A, B inside
 // it; block per (chunk, head), kBwdThreads threads, 64-feature tiles:
@@ -799,51 +820,77 @@ __global__ void __launch_bounds__(256) bwd_dx(const float *__restrict__ C, const
 
 // per chunk of 64 rows: St[f][c] = sum_rows phi[row][f] Yc[row][c], c <= dv, where
 // Yc = [v | 1] (forward state) or the rows' [dnum | dden] (backward state);
-// block per (chunk, head), 256 threads, 32-feature tiles in shared memory;
-// thread (ty, tx) owns features 2 ty, 2 ty + 1 and columns tx, tx + 16, ...
+// block per (chunk, head), 256 threads, 64-feature tiles of phi read a tile
+// ahead into registers; thread (ty, tx) owns features ty + 16 u and value
+// columns 4 tx + w (+ 64 per group); the last column (sum of phi, or of
+// phi dden) from per-thread row partials summed over tx.
 template <typename T, int DV>
 __global__ void __launch_bounds__(256) state_tile(const float *__restrict__ phi, const T *__restrict__ v,
                                                   const float *__restrict__ Y, float *__restrict__ S, int L, int r,
                                                   int nch) {
-    constexpr int C = kBwdRows, FT = 32, W = DV + 1, CW = (W + 15) / 16;
-    __shared__ float Ps[C][FT + 1];
-    __shared__ float Ys[C][W];
+    constexpr int C = kBwdRows, FT = 64, P = FT + 4, W = DV + 1, WP = DV + 4, NG = (DV + 63) / 64, NT = 256;
+    constexpr int NX = C * FT / 4 / NT;
+    extern __shared__ float4 sm4[];
+    float *Ps = reinterpret_cast<float *>(sm4);   // [C][P]  phi tile (rows x features)
+    float *Ys = Ps + C * P;                       // [C][WP] Yc | 0
     const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
     const int ch = blockIdx.x, bh = blockIdx.y, t0 = ch * C, n = min(C, L - t0);
     const size_t row0 = (size_t)bh * L + t0;
-    for (int e = tid; e < C * W; e += 256) {
-        const int i = e / W, c = e % W;
+#pragma unroll 4
+    for (int e = tid; e < C * WP; e += NT) {
+        const int i = e / WP, c = e % WP;
         float y = 0.f;
-        if (i < n) y = Y ? Y[(row0 + i) * W + c] : (c < DV ? load_in(v, (row0 + i) * DV + c) : 1.f);
-        Ys[i][c] = y;
+        if (i < n && c < W) y = Y ? Y[(row0 + i) * W + c] : (c < DV ? load_in(v, (row0 + i) * DV + c) : 1.f);
+        Ys[e] = y;
     }
+    float4 xp[NX];
+    auto fetch = [&](int f0) {
+#pragma unroll
+        for (int k = 0; k < NX; ++k) {
+            const int e = tid + NT * k, i = e / (FT / 4), f = 4 * (e % (FT / 4));
+            xp[k] = (i < n && f0 + f < r) ? *reinterpret_cast<const float4 *>(phi + (row0 + i) * r + f0 + f)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    };
     float *dst = S + ((size_t)bh * nch + ch) * r * W;
+    fetch(0);
     for (int f0 = 0; f0 < r; f0 += FT) {
         __syncthreads();
-        for (int e = tid; e < C * FT; e += 256) {
-            const int i = e / FT, f = e % FT;
-            Ps[i][f] = (i < n && f0 + f < r) ? phi[(row0 + i) * r + f0 + f] : 0.f;
+#pragma unroll
+        for (int k = 0; k < NX; ++k) {
+            const int e = tid + NT * k, i = e / (FT / 4), f = 4 * (e % (FT / 4));
+            *reinterpret_cast<float4 *>(Ps + i * P + f) = xp[k];
         }
         __syncthreads();
-        float acc[2][CW] = {};
-        for (int i = 0; i < C; ++i) {
-            float pv[2], yv[CW];
+        if (f0 + FT < r) fetch(f0 + FT);
+        float acc[NG][4][4] = {}, zc[4] = {};
 #pragma unroll
-            for (int u = 0; u < 2; ++u) pv[u] = Ps[i][2 * ty + u];
+        for (int gi = 0; gi < NG; ++gi)
+            if (64 * gi + 4 * tx < DV) mm_tn(acc[gi], Ps, P, Ys + 64 * gi, WP, C, ty, tx);
+        // column DV: rows tx, tx + 16, ... of this thread, summed over tx
 #pragma unroll
-            for (int w = 0; w < CW; ++w) yv[w] = (tx + 16 * w < W) ? Ys[i][tx + 16 * w] : 0.f;
+        for (int u = 0; u < 4; ++u) {
 #pragma unroll
-            for (int u = 0; u < 2; ++u)
+            for (int ii = 0; ii < C / 16; ++ii) {
+                const int i = tx + 16 * ii;
+                zc[u] = fmaf(Ps[i * P + ty + 16 * u], Ys[i * WP + DV], zc[u]);
+            }
 #pragma unroll
-                for (int w = 0; w < CW; ++w) acc[u][w] = fmaf(pv[u], yv[w], acc[u][w]);
+            for (int o = 8; o > 0; o >>= 1) zc[u] += __shfl_xor_sync(0xffffffffu, zc[u], o);
         }
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int f = f0 + 2 * ty + u;
+        for (int u = 0; u < 4; ++u) {
+            const int f = f0 + ty + 16 * u;
             if (f >= r) continue;
 #pragma unroll
-            for (int w = 0; w < CW; ++w)
-                if (tx + 16 * w < W) dst[(size_t)f * W + tx + 16 * w] = acc[u][w];
+            for (int gi = 0; gi < NG; ++gi) {
+                const int c = 64 * gi + 4 * tx;
+                if (c < DV) {
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) dst[(size_t)f * W + c + w] = acc[gi][u][w];
+                }
+            }
+            if (tx == 0) dst[(size_t)f * W + DV] = zc[u];
         }
     }
 }
@@ -862,167 +909,212 @@ __global__ void state_total(float *__restrict__ S, int nch, size_t per, int BH) 
 
 // per row of a chunk: num, den from the entering state (+ the masked chunk
 // sum), out = num / den, then dnum = g / den and dden = -(g . out) / den into
-// Y [rows][dv + 1].  Block per (chunk, head), 256 threads, tiles as bwd_chunk.
+// Y [rows][dv + 1].  Block per (chunk, head), 256 threads, 64-feature tiles
+// read a tile ahead into registers (as bwd_chunk):
+//   num = phi_q S[:, :dv] (+ A_m V),  den = phi_q z (+ A_m 1),  A_m = (phi_q phi_k^T) masked to j <= i
 template <typename T, int DV>
 __global__ void __launch_bounds__(256) bwd_rows(const float *__restrict__ phiq, const float *__restrict__ phik,
                                                 const T *__restrict__ v, const float *__restrict__ Sin,
                                                 const float *__restrict__ g, float *__restrict__ Y, int L, int r,
                                                 int nst, int causal) {
-    constexpr int C = kBwdRows, FT = 32, W = DV + 1, CW = (W + 15) / 16;
-    extern __shared__ float sm[];
-    float(*Qt)[FT + 1] = reinterpret_cast<float(*)[FT + 1]>(sm);
-    float(*Kt)[FT + 1] = reinterpret_cast<float(*)[FT + 1]>(sm + C * (FT + 1));
-    float(*St)[W] = reinterpret_cast<float(*)[W]>(sm + 2 * C * (FT + 1));
-    float(*Vs)[W] = reinterpret_cast<float(*)[W]>(sm + 2 * C * (FT + 1) + FT * W);
-    float(*As)[C + 1] = reinterpret_cast<float(*)[C + 1]>(sm + 2 * C * (FT + 1) + FT * W + C * W);
-    float(*NUM)[W] = Vs;   // the chunk's [num | den] once V is no longer read
+    constexpr int C = kBwdRows, FT = 64, P = FT + 4, W = DV + 1, WP = DV + 4, NG = (DV + 63) / 64, NT = 256;
+    extern __shared__ float4 sm4[];
+    float *Qt = reinterpret_cast<float *>(sm4);   // [C][P]   phi_q tile
+    float *Kt = Qt + C * P;                       // [C][P]   phi_k tile; A_m after the feature loop
+    float *Ss = Kt + C * P;                       // [FT][WP] state rows (values | z); [num | den] at the end
+    float *Vs = Ss + FT * WP;                     // [C][WP]  v | 1 | 0
     const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
     const int ch = blockIdx.x, bh = blockIdx.y, t0 = ch * C, n = min(C, L - t0);
     const size_t row0 = (size_t)bh * L + t0;
     const float *S = Sin + ((size_t)bh * nst + (causal ? ch : 0)) * r * W;
-    for (int e = tid; e < C * W; e += 256) {
-        const int i = e / W, c = e % W;
-        Vs[i][c] = i < n ? (c < DV ? load_in(v, (row0 + i) * DV + c) : 1.f) : 0.f;
+#pragma unroll 4
+    for (int e = tid; e < C * WP; e += NT) {
+        const int i = e / WP, c = e % WP;
+        Vs[e] = (i < n && c < W) ? (c < DV ? load_in(v, (row0 + i) * DV + c) : 1.f) : 0.f;
     }
-    float a[4][4] = {}, num[4][CW] = {};
+    constexpr int NX = C * FT / 4 / NT, NS = (FT * W + NT - 1) / NT;
+    float4 xq[NX], xk[NX];
+    float xs[NS];
+    auto fetch = [&](int f0) {
+#pragma unroll
+        for (int k = 0; k < NX; ++k) {
+            const int e = tid + NT * k, i = e / (FT / 4), f = 4 * (e % (FT / 4));
+            const bool ok = i < n && f0 + f < r;   // r % 4 == 0
+            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+            xq[k] = ok ? *reinterpret_cast<const float4 *>(phiq + (row0 + i) * r + f0 + f) : z;
+            xk[k] = (ok && causal) ? *reinterpret_cast<const float4 *>(phik + (row0 + i) * r + f0 + f) : z;
+        }
+#pragma unroll
+        for (int k = 0; k < NS; ++k) {
+            const int e = tid + NT * k, f = e / W, c = e % W;
+            xs[k] = (e < FT * W && f0 + f < r) ? S[(size_t)(f0 + f) * W + c] : 0.f;
+        }
+    };
+    float a[4][4] = {}, num[NG][4][4] = {}, den[4] = {};
+    fetch(0);
     for (int f0 = 0; f0 < r; f0 += FT) {
         __syncthreads();
-        for (int e = tid; e < C * FT; e += 256) {
-            const int i = e / FT, f = e % FT;
-            const bool ok = i < n && f0 + f < r;
-            Qt[i][f] = ok ? phiq[(row0 + i) * r + f0 + f] : 0.f;
-            Kt[i][f] = ok ? phik[(row0 + i) * r + f0 + f] : 0.f;
+#pragma unroll
+        for (int k = 0; k < NX; ++k) {
+            const int e = tid + NT * k, i = e / (FT / 4), f = 4 * (e % (FT / 4));
+            *reinterpret_cast<float4 *>(Qt + i * P + f) = xq[k];
+            *reinterpret_cast<float4 *>(Kt + i * P + f) = xk[k];
         }
-        for (int e = tid; e < FT * W; e += 256) {
-            const int f = e / W, c = e % W;
-            St[f][c] = f0 + f < r ? S[(size_t)(f0 + f) * W + c] : 0.f;
+#pragma unroll
+        for (int k = 0; k < NS; ++k) {
+            const int e = tid + NT * k;
+            if (e < FT * W) Ss[(e / W) * WP + e % W] = xs[k];
         }
         __syncthreads();
-        for (int f = 0; f < FT; ++f) {
-            float qv[4];
+        if (f0 + FT < r) fetch(f0 + FT);
+        if (causal) mm_nt(a, Qt, P, Kt, P, FT, ty, tx);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) qv[u] = Qt[4 * ty + u][f];
-            if (causal) {
+        for (int gi = 0; gi < NG; ++gi)
+            if (64 * gi + 4 * tx < DV) mm_nn(num[gi], Qt, P, Ss + 64 * gi, WP, FT, ty, tx);
+        // den partial over features 4 tx .. 4 tx + 3 of the tile (summed over tx below)
+        const float z0 = Ss[(4 * tx) * WP + DV], z1 = Ss[(4 * tx + 1) * WP + DV], z2 = Ss[(4 * tx + 2) * WP + DV],
+                    z3 = Ss[(4 * tx + 3) * WP + DV];
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const float kv = Kt[4 * tx + w][f];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) a[u][w] = fmaf(qv[u], kv, a[u][w]);
-                }
-            }
-#pragma unroll
-            for (int w = 0; w < CW; ++w) {
-                const float sv = (tx + 16 * w < W) ? St[f][tx + 16 * w] : 0.f;
-#pragma unroll
-                for (int u = 0; u < 4; ++u) num[u][w] = fmaf(qv[u], sv, num[u][w]);
-            }
+        for (int u = 0; u < 4; ++u) {
+            const float4 qv = *reinterpret_cast<const float4 *>(Qt + (ty + 16 * u) * P + 4 * tx);
+            den[u] = fmaf(qv.x, z0, fmaf(qv.y, z1, fmaf(qv.z, z2, fmaf(qv.w, z3, den[u]))));
         }
     }
     if (causal) {
+        __syncthreads();
 #pragma unroll
         for (int u = 0; u < 4; ++u)
 #pragma unroll
-            for (int w = 0; w < 4; ++w) As[4 * ty + u][4 * tx + w] = (4 * tx + w <= 4 * ty + u) ? a[u][w] : 0.f;
-        __syncthreads();
-        for (int j = 0; j < C; ++j) {
-            float vv[CW];
-#pragma unroll
-            for (int w = 0; w < CW; ++w) vv[w] = (tx + 16 * w < W) ? Vs[j][tx + 16 * w] : 0.f;
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float av = As[4 * ty + u][j];
-#pragma unroll
-                for (int w = 0; w < CW; ++w) num[u][w] = fmaf(av, vv[w], num[u][w]);
+            for (int w = 0; w < 4; ++w) {
+                const int i = ty + 16 * u, j = tx + 16 * w;
+                const float x = j <= i ? a[u][w] : 0.f;
+                Kt[i * P + j] = x;
+                den[u] += x;
             }
-        }
+        __syncthreads();
+#pragma unroll
+        for (int gi = 0; gi < NG; ++gi)
+            if (64 * gi + 4 * tx < DV) mm_nn(num[gi], Kt, P, Vs + 64 * gi, WP, C, ty, tx);
     }
-    // [num | den] of the chunk's rows -> shared (over V), then row-wise dnum, dden
-    __syncthreads();
 #pragma unroll
     for (int u = 0; u < 4; ++u)
 #pragma unroll
-        for (int w = 0; w < CW; ++w)
-            if (tx + 16 * w < W) NUM[4 * ty + u][tx + 16 * w] = num[u][w];
+        for (int o = 8; o > 0; o >>= 1) den[u] += __shfl_xor_sync(0xffffffffu, den[u], o);
+    // [num | den] of the chunk's rows -> shared (over the state tile), then row-wise dnum, dden
+    __syncthreads();
+    float *NUM = Ss;   // [C][WP]
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int i = ty + 16 * u;
+#pragma unroll
+        for (int gi = 0; gi < NG; ++gi)
+            if (64 * gi + 4 * tx < DV)
+                *reinterpret_cast<float4 *>(NUM + i * WP + 64 * gi + 4 * tx) =
+                    make_float4(num[gi][u][0], num[gi][u][1], num[gi][u][2], num[gi][u][3]);
+        if (tx == 0) NUM[i * WP + DV] = den[u];
+    }
     __syncthreads();
     const int warp = tid >> 5, lane = tid & 31;
-    for (int i = warp; i < n; i += 8) {
-        const float den = NUM[i][DV];
+    for (int i = warp; i < n; i += NT / 32) {
+        const float dn = NUM[i * WP + DV];
         float gdo = 0.f;
         for (int c = lane; c < DV; c += 32) {
             const float gi = g[(row0 + i) * DV + c];
-            gdo = fmaf(gi, NUM[i][c] / den, gdo);
-            Y[(row0 + i) * W + c] = gi / den;
+            gdo = fmaf(gi, NUM[i * WP + c] / dn, gdo);
+            Y[(row0 + i) * W + c] = gi / dn;
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) gdo += __shfl_xor_sync(0xffffffffu, gdo, o);
-        if (lane == 0) Y[(row0 + i) * W + DV] = -gdo / den;
+        if (lane == 0) Y[(row0 + i) * W + DV] = -gdo / dn;
     }
 }
 
 // dw[h][p][j] += over a slice of 512 of the head's rows (all batches; queries
 // and keys): sum_rows c[row][p] x[row][j].  Block per (64-projection tile,
-// slice, head), 256 threads, 32 rows at a time in shared memory: thread
-// (ty, tx) owns projections 4 ty .. + 3 and columns tx, tx + 16, ...; one
-// atomic add per output and block.
+// slice, head), 256 threads, 64 rows at a time in shared memory, read a
+// sub-slice ahead into registers: thread (ty, tx) owns projections ty + 16 u
+// and columns 4 tx + w (+ 64 per group); one atomic add per output and block.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) bwd_dw(const float *__restrict__ Cq, const float *__restrict__ Ck,
                                               const T *__restrict__ q, const T *__restrict__ k,
                                               float *__restrict__ dw, int B, int H, int L, int nproj) {
-    constexpr int RS = 32, PT = 64, CD = D / 16, SUB = 16;   // 16 sub-slices of 32 rows per block
-    __shared__ float Cs[RS][PT + 1];
-    __shared__ float Xs[RS][D + 1];
+    constexpr int RS = 64, PT = 64, P = PT + 4, DP = D + 4, NG = (D + 63) / 64, NT = 256, SUB = 8;
+    constexpr int NC = RS * PT / 4 / NT, NXD = (RS * D / 4 + NT - 1) / NT;
+    extern __shared__ float4 sm4[];
+    float *Cs = reinterpret_cast<float *>(sm4);   // [RS][P]  coefficient rows
+    float *Xs = Cs + RS * P;                      // [RS][DP] input rows
     const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
     const int p0 = blockIdx.x * PT, h = blockIdx.z;
-    float acc[4][CD] = {};
-    for (int sub = 0; sub < SUB; ++sub)
-    for (int side = 0; side < 2; ++side) {
-        const int r0 = (blockIdx.y * SUB + sub) * RS;      // 32 of the B L rows of head h
+    float4 rc[NC], rx[NXD];
+    auto fetch = [&](int it) {   // sub-slice it / 2 of side it % 2
+        const int side = it & 1, r0 = (blockIdx.y * SUB + (it >> 1)) * RS;
         const float *Cm = side ? Ck : Cq;
         const T *X = side ? k : q;
-        __syncthreads();
-        for (int e = tid; e < RS * PT; e += 256) {
-            const int i = e / PT, p = e % PT, t = r0 + i;
-            float cv = 0.f;
-            if (t < B * L && p0 + p < nproj) {
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int kk = 0; kk < NC; ++kk) {
+            const int e = tid + NT * kk, i = e / (PT / 4), pp = 4 * (e % (PT / 4)), t = r0 + i;
+            rc[kk] = z;
+            if (t < B * L && p0 + pp < nproj) {   // nproj % 4 == 0
                 const size_t row = ((size_t)(t / L) * H + h) * L + t % L;
-                cv = Cm[row * nproj + p0 + p];
+                rc[kk] = *reinterpret_cast<const float4 *>(Cm + row * nproj + p0 + pp);
             }
-            Cs[i][p] = cv;
         }
-        for (int e = tid; e < RS * D; e += 256) {
-            const int i = e / D, j = e % D, t = r0 + i;
-            float xv = 0.f;
-            if (t < B * L) {
+#pragma unroll
+        for (int kk = 0; kk < NXD; ++kk) {
+            const int e = tid + NT * kk, i = e / (D / 4), j = 4 * (e % (D / 4)), t = r0 + i;
+            rx[kk] = z;
+            if (e < RS * D / 4 && t < B * L) {
                 const size_t row = ((size_t)(t / L) * H + h) * L + t % L;
-                xv = load_in(X, row * D + j);
+                rx[kk] = make_float4(load_in(X, row * D + j), load_in(X, row * D + j + 1), load_in(X, row * D + j + 2),
+                                     load_in(X, row * D + j + 3));
             }
-            Xs[i][j] = xv;
+        }
+    };
+    float acc[NG][4][4] = {};
+    fetch(0);
+    for (int it = 0; it < 2 * SUB; ++it) {
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < NC; ++kk) {
+            const int e = tid + NT * kk, i = e / (PT / 4), pp = 4 * (e % (PT / 4));
+            *reinterpret_cast<float4 *>(Cs + i * P + pp) = rc[kk];
+        }
+#pragma unroll
+        for (int kk = 0; kk < NXD; ++kk) {
+            const int e = tid + NT * kk, i = e / (D / 4), j = 4 * (e % (D / 4));
+            if (e < RS * D / 4) *reinterpret_cast<float4 *>(Xs + i * DP + j) = rx[kk];
         }
         __syncthreads();
-        for (int i = 0; i < RS; ++i) {
-            float cv[4], xv[CD];
+        if (it + 1 < 2 * SUB) fetch(it + 1);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) cv[u] = Cs[i][4 * ty + u];
-#pragma unroll
-            for (int w = 0; w < CD; ++w) xv[w] = Xs[i][tx + 16 * w];
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-#pragma unroll
-                for (int w = 0; w < CD; ++w) acc[u][w] = fmaf(cv[u], xv[w], acc[u][w]);
-        }
+        for (int gi = 0; gi < NG; ++gi)
+            if (64 * gi + 4 * tx < D) mm_tn(acc[gi], Cs, P, Xs + 64 * gi, DP, RS, ty, tx);
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-        const int p = p0 + 4 * ty + u;
+        const int p = p0 + ty + 16 * u;
         if (p >= nproj) continue;
 #pragma unroll
-        for (int w = 0; w < CD; ++w) atomicAdd(&dw[((size_t)h * nproj + p) * D + tx + 16 * w], acc[u][w]);
+        for (int gi = 0; gi < NG; ++gi) {
+            const int j = 64 * gi + 4 * tx;
+            if (j < D) {
+#pragma unroll
+                for (int w = 0; w < 4; ++w) atomicAdd(&dw[((size_t)h * nproj + p) * D + j + w], acc[gi][u][w]);
+            }
+        }
     }
+}
+
+// dynamic shared memory of state_tile (DV value columns) and bwd_dw (D input columns)
+template <int DV>
+constexpr size_t state_tile_smem() {
+    return sizeof(float) * (kBwdRows * 68 + kBwdRows * (DV + 4));
 }
 
 template <int DV>
 constexpr size_t bwd_rows_smem() {
-    return sizeof(float) * (2 * kBwdRows * 33 + 32 * (DV + 1) + kBwdRows * (DV + 1) + kBwdRows * (kBwdRows + 1));
+    return sizeof(float) * (2 * kBwdRows * 68 + 2 * kBwdRows * (DV + 4));
 }
 
 template <typename T, int DV>
@@ -1057,8 +1149,14 @@ int backward_dv(const T *q, const T *k, const T *v, const float *omega, const fl
     FAVOR_LAUNCH_CHECK();
     const dim3 cg(nch, p.BH);
     const unsigned sb = (unsigned)((per * p.BH + 255) / 256);
+    const size_t st_smem = state_tile_smem<DV>();
+    if (cudaFuncSetAttribute(state_tile<T, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st_smem) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return FAVOR_ERR_CUDA;
+    }
     // the forward states entering each chunk (causal: exclusive prefix) or the total (chunk slot 0)
-    state_tile<T, DV><<<cg, 256, 0, st>>>(phik, v, nullptr, S, p.L, p.r, nch);
+    state_tile<T, DV><<<cg, 256, st_smem, st>>>(phik, v, nullptr, S, p.L, p.r, nch);
     FAVOR_LAUNCH_CHECK();
     if (p.causal) simt_state_prefix<<<sb, 256, 0, st>>>(S, nch, per, p.BH);
     else state_total<<<sb, 256, 0, st>>>(S, nch, per, p.BH);
@@ -1074,7 +1172,7 @@ int backward_dv(const T *q, const T *k, const T *v, const float *omega, const fl
         FAVOR_LAUNCH_CHECK();
     }
     // the states leaving each chunk (causal: exclusive suffix) or the total
-    state_tile<T, DV><<<cg, 256, 0, st>>>(phiq, v, Y, R, p.L, p.r, nch);
+    state_tile<T, DV><<<cg, 256, st_smem, st>>>(phiq, v, Y, R, p.L, p.r, nch);
     FAVOR_LAUNCH_CHECK();
     if (p.causal) bwd_state_suffix<<<sb, 256, 0, st>>>(R, nch, per, p.BH);
     else state_total<<<sb, 256, 0, st>>>(R, nch, per, p.BH);
@@ -1110,9 +1208,19 @@ int backward_dv(const T *q, const T *k, const T *v, const float *omega, const fl
     if (dw && !map_is_elementwise(p.map)) {
         if (cudaMemsetAsync(dw, 0, (size_t)p.H * p.nproj * p.d * sizeof(float), st) != cudaSuccess) return FAVOR_ERR_CUDA;
         const dim3 wg((p.nproj + 63) / 64, (p.B * p.L + 511) / 512, p.H);
-        if (p.d == 32) bwd_dw<T, 32><<<wg, 256, 0, st>>>(Pq, Pk, q, k, dw, p.B, p.H, p.L, p.nproj);
-        else if (p.d == 64) bwd_dw<T, 64><<<wg, 256, 0, st>>>(Pq, Pk, q, k, dw, p.B, p.H, p.L, p.nproj);
-        else bwd_dw<T, 128><<<wg, 256, 0, st>>>(Pq, Pk, q, k, dw, p.B, p.H, p.L, p.nproj);
+        auto dw_launch = [&](auto kern, size_t smem) -> int {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+                cudaGetLastError();
+                return FAVOR_ERR_CUDA;
+            }
+            kern<<<wg, 256, smem, st>>>(Pq, Pk, q, k, dw, p.B, p.H, p.L, p.nproj);
+            return FAVOR_OK;
+        };
+        // the input tile has the shape of a state tile with D columns
+        const int rc = p.d == 32   ? dw_launch(bwd_dw<T, 32>, state_tile_smem<32>())
+                       : p.d == 64 ? dw_launch(bwd_dw<T, 64>, state_tile_smem<64>())
+                                   : dw_launch(bwd_dw<T, 128>, state_tile_smem<128>());
+        if (rc != FAVOR_OK) return rc;
         FAVOR_LAUNCH_CHECK();
     }
     return FAVOR_OK;
