@@ -913,7 +913,7 @@ __global__ void state_total(float *__restrict__ S, int nch, size_t per, int BH) 
 // read a tile ahead into registers (as bwd_chunk):
 //   num = phi_q S[:, :dv] (+ A_m V),  den = phi_q z (+ A_m 1),  A_m = (phi_q phi_k^T) masked to j <= i
 template <typename T, int DV>
-__global__ void __launch_bounds__(256) bwd_rows(const float *__restrict__ phiq, const float *__restrict__ phik,
+__global__ void __launch_bounds__(256, 2) bwd_rows(const float *__restrict__ phiq, const float *__restrict__ phik,
                                                 const T *__restrict__ v, const float *__restrict__ Sin,
                                                 const float *__restrict__ g, float *__restrict__ Y, int L, int r,
                                                 int nst, int causal) {
