@@ -36,59 +36,131 @@ __device__ __forceinline__ float load_in(const uint16_t *p, size_t i) {
 __device__ __forceinline__ void store_out(float *p, size_t i, float v) { p[i] = v; }
 __device__ __forceinline__ void store_out(__nv_bfloat16 *p, size_t i, float v) { p[i] = __float2bfloat16_rn(v); }
 
+// Register-tiled products of shared-memory tiles for 16 RS threads, ty = tid / 16,
+// tx = tid % 16.  A thread owns rows ty + RS u (u < RU, RS RU = 64) of the result
+// and the columns 4 tx + w (mm_nn) or tx + 16 w (mm_nt), w < 4; the operands are
+// read 4 values of the contraction at a time (16-byte loads: RU + 4 loads per
+// 16 RU FMAs).
+// Row pitches are multiples of 4 floats; the B rows that 16 threads read at once
+// (mm_nt) have an odd pitch in 16-byte units, so those loads do not conflict.
+//   mm_nn: acc[u][w] += sum_k A[ty + RS u][k] B[k][4 tx + w]
+//   mm_nt: acc[u][w] += sum_k A[ty + RS u][k] B[tx + 16 w][k]
+template <int RU = 4, int RS = 16>
+__device__ __forceinline__ void mm_nn(float (&acc)[RU][4], const float *A, int lda, const float *B, int ldb, int K,
+                                      int ty, int tx) {
+#pragma unroll 2
+    for (int k = 0; k < K; k += 4) {
+        float4 a[RU], b[4];
+#pragma unroll
+        for (int u = 0; u < RU; ++u) a[u] = *reinterpret_cast<const float4 *>(A + (ty + RS * u) * lda + k);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) b[kk] = *reinterpret_cast<const float4 *>(B + (k + kk) * ldb + 4 * tx);
+#pragma unroll
+        for (int u = 0; u < RU; ++u) {
+            const float av[4] = {a[u].x, a[u].y, a[u].z, a[u].w};
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                acc[u][0] = fmaf(av[kk], b[kk].x, acc[u][0]);
+                acc[u][1] = fmaf(av[kk], b[kk].y, acc[u][1]);
+                acc[u][2] = fmaf(av[kk], b[kk].z, acc[u][2]);
+                acc[u][3] = fmaf(av[kk], b[kk].w, acc[u][3]);
+            }
+        }
+    }
+}
+
+template <int RU = 4, int RS = 16>
+__device__ __forceinline__ void mm_nt(float (&acc)[RU][4], const float *A, int lda, const float *B, int ldb, int K,
+                                      int ty, int tx) {
+#pragma unroll 2
+    for (int k = 0; k < K; k += 4) {
+        float4 a[RU], b[4];
+#pragma unroll
+        for (int u = 0; u < RU; ++u) a[u] = *reinterpret_cast<const float4 *>(A + (ty + RS * u) * lda + k);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) b[w] = *reinterpret_cast<const float4 *>(B + (tx + 16 * w) * ldb + k);
+#pragma unroll
+        for (int u = 0; u < RU; ++u)
+#pragma unroll
+            for (int w = 0; w < 4; ++w)
+                acc[u][w] = fmaf(a[u].x, b[w].x,
+                                 fmaf(a[u].y, b[w].y, fmaf(a[u].z, b[w].z, fmaf(a[u].w, b[w].w, acc[u][w]))));
+    }
+}
+
+// acc[u][w] += sum_k A[k][ty + 16 u] B[k][4 tx + w]: both operands row-major
+// with the contraction along their rows (4 broadcast scalar loads and one
+// 16-byte load per 16 FMAs)
+__device__ __forceinline__ void mm_tn(float (&acc)[4][4], const float *A, int lda, const float *B, int ldb, int K,
+                                      int ty, int tx) {
+#pragma unroll 4
+    for (int k = 0; k < K; ++k) {
+        float a[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) a[u] = A[k * lda + ty + 16 * u];
+        const float4 b = *reinterpret_cast<const float4 *>(B + k * ldb + 4 * tx);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            acc[u][0] = fmaf(a[u], b.x, acc[u][0]);
+            acc[u][1] = fmaf(a[u], b.y, acc[u][1]);
+            acc[u][2] = fmaf(a[u], b.z, acc[u][2]);
+            acc[u][3] = fmaf(a[u], b.w, acc[u][3]);
+        }
+    }
+}
+
 // 1. projections P[t][n] = w_n . x_t: block = 64 tokens x 64 projections of
-// one head, 256 threads with 4 x 4 register tiles, x and omega in 32-wide
-// slices of d in shared memory.
-template <typename T>
+// one head, 256 threads with 4 x 4 register tiles (mm_nt), x and omega rows
+// of the whole width D in shared memory.
+template <typename T, int D>
 __global__ void __launch_bounds__(256) simt_project(const T *__restrict__ x, const float *__restrict__ omega,
-                                                    float *__restrict__ P, int H, int L, int d, int nproj,
-                                                    int identity) {
-    constexpr int TT = 64, NT = 64, KT = 32;
-    __shared__ float xs[TT][KT + 1];
-    __shared__ float ws[NT][KT + 1];
+                                                    float *__restrict__ P, int H, int L, int nproj, int identity) {
+    constexpr int TT = 64, NT = 64, DP = D + 4;
+    extern __shared__ float4 sm4[];
+    float *xs = reinterpret_cast<float *>(sm4);   // [TT][DP]
+    float *ws = xs + TT * DP;                     // [NT][DP]
     const int bh = blockIdx.z, h = bh % H;
     const int t0 = blockIdx.x * TT, n0 = blockIdx.y * NT;
     const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
-    const T *xb = x + (size_t)bh * L * d;
-    float acc[4][4] = {};
-    for (int k0 = 0; k0 < d; k0 += KT) {
-        __syncthreads();
-        for (int e = tid; e < TT * KT; e += 256) {
-            const int t = e / KT, j = e % KT;
-            xs[t][j] = (t0 + t < L && k0 + j < d) ? load_in(xb, (size_t)(t0 + t) * d + k0 + j) : 0.f;
-        }
-        for (int e = tid; e < NT * KT; e += 256) {
-            const int n = e / KT, j = e % KT;
-            float w = 0.f;
-            if (n0 + n < nproj && k0 + j < d)
-                w = identity ? (n0 + n == k0 + j ? 1.f : 0.f) : omega[((size_t)h * nproj + n0 + n) * d + k0 + j];
-            ws[n][j] = w;
-        }
-        __syncthreads();
-#pragma unroll 8
-        for (int j = 0; j < KT; ++j) {
-            float xv[4], wv[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                xv[u] = xs[4 * ty + u][j];
-                wv[u] = ws[4 * tx + u][j];
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-#pragma unroll
-                for (int w = 0; w < 4; ++w) acc[u][w] = fmaf(xv[u], wv[w], acc[u][w]);
-        }
+    const T *xb = x + (size_t)bh * L * D;
+#pragma unroll 4
+    for (int e = tid; e < TT * D; e += 256) {
+        const int t = e / D, j = e % D;
+        xs[t * DP + j] = t0 + t < L ? load_in(xb, (size_t)(t0 + t) * D + j) : 0.f;
     }
+#pragma unroll 4
+    for (int e = tid; e < NT * D; e += 256) {
+        const int n = e / D, j = e % D;
+        float w = 0.f;
+        if (n0 + n < nproj) w = identity ? (n0 + n == j ? 1.f : 0.f) : omega[((size_t)h * nproj + n0 + n) * D + j];
+        ws[n * DP + j] = w;
+    }
+    __syncthreads();
+    float acc[4][4] = {};
+    mm_nt(acc, xs, DP, ws, DP, D, ty, tx);
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-        const int t = t0 + 4 * ty + u;
+        const int t = t0 + ty + 16 * u;
         if (t >= L) continue;
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
-            const int n = n0 + 4 * tx + w;
+            const int n = n0 + tx + 16 * w;
             if (n < nproj) P[((size_t)bh * L + t) * nproj + n] = acc[u][w];
         }
     }
+}
+
+template <typename T, int D>
+int project_launch(const T *x, const float *omega, float *P, const Problem &p, cudaStream_t st) {
+    const size_t smem = sizeof(float) * 2 * 64 * (D + 4);
+    if (cudaFuncSetAttribute(simt_project<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return FAVOR_ERR_CUDA;
+    }
+    const dim3 pg((p.L + 63) / 64, (p.nproj + 63) / 64, p.BH);
+    simt_project<T, D><<<pg, 256, smem, st>>>(x, omega, P, p.H, p.L, p.nproj, map_is_elementwise(p.map));
+    return FAVOR_OK;
 }
 
 // 2. features: one warp per token row.
@@ -281,9 +353,10 @@ __global__ void simt_out_causal(const float *__restrict__ phiq, const float *__r
 template <typename T>
 int features_into(const T *x, const float *omega, float *P, float *phi, float *logscale,
                   const Problem &p, cudaStream_t st) {
-    dim3 pg((p.L + 63) / 64, (p.nproj + 63) / 64, p.BH);
-    simt_project<T><<<pg, 256, 0, st>>>(x, omega, P, p.H, p.L, p.d, p.nproj,
-                                        map_is_elementwise(p.map));
+    const int prc = p.d == 32   ? project_launch<T, 32>(x, omega, P, p, st)
+                    : p.d == 64 ? project_launch<T, 64>(x, omega, P, p, st)
+                                : project_launch<T, 128>(x, omega, P, p, st);
+    if (prc != FAVOR_OK) return prc;
     FAVOR_LAUNCH_CHECK();
     long long rows = (long long)p.BH * p.L;
     simt_features<T><<<(unsigned)((rows * 32 + 255) / 256), 256, 0, st>>>(
@@ -457,79 +530,6 @@ __global__ void bwd_state_suffix(float *__restrict__ R, int nseg, size_t per_seg
         for (int i = 0; i < 8; ++i) {
             if (s0 - i >= 0) base[(size_t)(s0 - i) * per_seg] = run;
             run += t[i];
-        }
-    }
-}
-
-// Register-tiled products of shared-memory tiles for 16 RS threads, ty = tid / 16,
-// tx = tid % 16.  A thread owns rows ty + RS u (u < RU, RS RU = 64) of the result
-// and the columns 4 tx + w (mm_nn) or tx + 16 w (mm_nt), w < 4; the operands are
-// read 4 values of the contraction at a time (16-byte loads: RU + 4 loads per
-// 16 RU FMAs).
-// Row pitches are multiples of 4 floats; the B rows that 16 threads read at once
-// (mm_nt) have an odd pitch in 16-byte units, so those loads do not conflict.
-//   mm_nn: acc[u][w] += sum_k A[ty + RS u][k] B[k][4 tx + w]
-//   mm_nt: acc[u][w] += sum_k A[ty + RS u][k] B[tx + 16 w][k]
-template <int RU = 4, int RS = 16>
-__device__ __forceinline__ void mm_nn(float (&acc)[RU][4], const float *A, int lda, const float *B, int ldb, int K,
-                                      int ty, int tx) {
-#pragma unroll 2
-    for (int k = 0; k < K; k += 4) {
-        float4 a[RU], b[4];
-#pragma unroll
-        for (int u = 0; u < RU; ++u) a[u] = *reinterpret_cast<const float4 *>(A + (ty + RS * u) * lda + k);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) b[kk] = *reinterpret_cast<const float4 *>(B + (k + kk) * ldb + 4 * tx);
-#pragma unroll
-        for (int u = 0; u < RU; ++u) {
-            const float av[4] = {a[u].x, a[u].y, a[u].z, a[u].w};
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                acc[u][0] = fmaf(av[kk], b[kk].x, acc[u][0]);
-                acc[u][1] = fmaf(av[kk], b[kk].y, acc[u][1]);
-                acc[u][2] = fmaf(av[kk], b[kk].z, acc[u][2]);
-                acc[u][3] = fmaf(av[kk], b[kk].w, acc[u][3]);
-            }
-        }
-    }
-}
-
-template <int RU = 4, int RS = 16>
-__device__ __forceinline__ void mm_nt(float (&acc)[RU][4], const float *A, int lda, const float *B, int ldb, int K,
-                                      int ty, int tx) {
-#pragma unroll 2
-    for (int k = 0; k < K; k += 4) {
-        float4 a[RU], b[4];
-#pragma unroll
-        for (int u = 0; u < RU; ++u) a[u] = *reinterpret_cast<const float4 *>(A + (ty + RS * u) * lda + k);
-#pragma unroll
-        for (int w = 0; w < 4; ++w) b[w] = *reinterpret_cast<const float4 *>(B + (tx + 16 * w) * ldb + k);
-#pragma unroll
-        for (int u = 0; u < RU; ++u)
-#pragma unroll
-            for (int w = 0; w < 4; ++w)
-                acc[u][w] = fmaf(a[u].x, b[w].x,
-                                 fmaf(a[u].y, b[w].y, fmaf(a[u].z, b[w].z, fmaf(a[u].w, b[w].w, acc[u][w]))));
-    }
-}
-
-// acc[u][w] += sum_k A[k][ty + 16 u] B[k][4 tx + w]: both operands row-major
-// with the contraction along their rows (4 broadcast scalar loads and one
-// 16-byte load per 16 FMAs)
-__device__ __forceinline__ void mm_tn(float (&acc)[4][4], const float *A, int lda, const float *B, int ldb, int K,
-                                      int ty, int tx) {
-#pragma unroll 4
-    for (int k = 0; k < K; ++k) {
-        float a[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) a[u] = A[k * lda + ty + 16 * u];
-        const float4 b = *reinterpret_cast<const float4 *>(B + k * ldb + 4 * tx);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            acc[u][0] = fmaf(a[u], b.x, acc[u][0]);
-            acc[u][1] = fmaf(a[u], b.y, acc[u][1]);
-            acc[u][2] = fmaf(a[u], b.z, acc[u][2]);
-            acc[u][3] = fmaf(a[u], b.w, acc[u][3]);
         }
     }
 }
