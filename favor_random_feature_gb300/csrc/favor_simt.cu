@@ -743,77 +743,114 @@ __global__ void bwd_coeff(float *__restrict__ P, const float *__restrict__ dphi,
 }
 
 // dx [rows][d] from the coefficients, 64 rows of one head per block (256
-// threads): dx = C w_h (C [rows][nproj] in 32-projection tiles, w_h
-// [nproj][d] likewise), then the map's row term: positive - x sum_p C[p];
-// softmax-scaled trig + x sum_f dphi_f phi_f; elementwise maps dx = C.
-// Thread (ty, tx) owns rows 4 ty .. + 3 and columns tx, tx + 16, ...
+// threads): dx = C w_h (C [rows][nproj] and w_h [nproj][d] in 64-projection
+// tiles, register-tiled, read a tile ahead into registers), then the map's row
+// term: positive - x sum_p C[p]; softmax-scaled trig + x sum_f dphi_f phi_f;
+// elementwise maps dx = C.  For the positive map the coefficients
+// C = dphi phi are formed here from the feature gradients and written to C
+// (the omega gradient reads them); the other maps take C from bwd_coeff.
+// Thread (ty, tx) owns rows ty + 16 u and columns 4 tx + w (+ 64 per group).
 template <typename T, int D>
-__global__ void __launch_bounds__(256) bwd_dx(const float *__restrict__ C, const float *__restrict__ dphi,
+__global__ void __launch_bounds__(256) bwd_dx(float *__restrict__ C, const float *__restrict__ dphi,
                                               const float *__restrict__ phi, const T *__restrict__ x,
                                               const float *__restrict__ omega, float *__restrict__ dx, int L, int H,
                                               int nproj, int r, int map) {
-    constexpr int RB = 64, PT = 32, CD = D / 16;
-    __shared__ float Cs[RB][PT + 1];
-    __shared__ float Ws[PT][D + 1];
-    __shared__ float tot[RB];
+    constexpr int RB = 64, PT = 64, P = PT + 4, DP = D + 4, NG = (D + 63) / 64, NT = 256;
+    constexpr int NX = RB * PT / 4 / NT, NW = (PT * D / 4 + NT - 1) / NT;
+    extern __shared__ float4 sm4[];
+    float *Cs = reinterpret_cast<float *>(sm4);   // [RB][P]  coefficients
+    float *Ws = Cs + RB * P;                      // [PT][DP] projections w_p
+    float *tot = Ws + PT * DP;                    // [RB]     row term (softmax-scaled trig)
     const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
     const int t0 = blockIdx.x * RB, bh = blockIdx.y, h = bh % H, n = min(RB, L - t0);
     const size_t row0 = (size_t)bh * L + t0;
     if (map_is_elementwise(map)) {
-        for (int e = tid; e < n * D; e += 256) dx[row0 * D + e] = C[row0 * nproj + e];
+        for (int e = tid; e < n * D; e += NT) dx[row0 * D + e] = C[row0 * nproj + e];
         return;
     }
-    // the row terms
-    {
+    const bool pos = map == FAVOR_MAP_POSITIVE;
+    if (map == FAVOR_MAP_TRIG_SOFTMAX) {
         const int warp = tid >> 5, lane = tid & 31;
-        for (int i = warp; i < RB; i += 8) {
-            float s = 0.f;
-            if (i < n) {
-                if (map == FAVOR_MAP_POSITIVE)
-                    for (int p = lane; p < nproj; p += 32) s += C[(row0 + i) * nproj + p];
-                else if (map == FAVOR_MAP_TRIG_SOFTMAX)
-                    for (int f = lane; f < r; f += 32) s = fmaf(dphi[(row0 + i) * r + f], phi[(row0 + i) * r + f], s);
-            }
+        for (int i = warp; i < RB; i += NT / 32) {
+            float sv = 0.f;
+            if (i < n)
+                for (int f = lane; f < r; f += 32) sv = fmaf(dphi[(row0 + i) * r + f], phi[(row0 + i) * r + f], sv);
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-            if (lane == 0) tot[i] = s;
+            for (int o = 16; o > 0; o >>= 1) sv += __shfl_xor_sync(0xffffffffu, sv, o);
+            if (lane == 0) tot[i] = sv;
         }
     }
     const float *w = omega + (size_t)h * nproj * D;
-    float acc[4][CD] = {};
+    float4 xc[NX], xw[NW];
+    auto fetch = [&](int p0) {
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < NX; ++k) {
+            const int e = tid + NT * k, i = e / (PT / 4), pp = 4 * (e % (PT / 4));
+            xc[k] = z;
+            if (i < n && p0 + pp < nproj) {   // nproj % 4 == 0
+                const size_t o = (row0 + i) * nproj + p0 + pp;
+                if (pos) {   // positive map: r == nproj
+                    const float4 g = *reinterpret_cast<const float4 *>(dphi + o),
+                                 f = *reinterpret_cast<const float4 *>(phi + o);
+                    xc[k] = make_float4(g.x * f.x, g.y * f.y, g.z * f.z, g.w * f.w);
+                    *reinterpret_cast<float4 *>(C + o) = xc[k];
+                } else {
+                    xc[k] = *reinterpret_cast<const float4 *>(C + o);
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < NW; ++k) {
+            const int e = tid + NT * k, pp = e / (D / 4), j = 4 * (e % (D / 4));
+            xw[k] = (e < PT * D / 4 && p0 + pp < nproj) ? *reinterpret_cast<const float4 *>(w + (size_t)(p0 + pp) * D + j)
+                                                       : z;
+        }
+    };
+    float acc[NG][4][4] = {}, rs[4] = {};
+    fetch(0);
     for (int p0 = 0; p0 < nproj; p0 += PT) {
         __syncthreads();
-        for (int e = tid; e < RB * PT; e += 256) {
-            const int i = e / PT, p = e % PT;
-            Cs[i][p] = (i < n && p0 + p < nproj) ? C[(row0 + i) * nproj + p0 + p] : 0.f;
+#pragma unroll
+        for (int k = 0; k < NX; ++k) {
+            const int e = tid + NT * k, i = e / (PT / 4), pp = 4 * (e % (PT / 4));
+            *reinterpret_cast<float4 *>(Cs + i * P + pp) = xc[k];
         }
-        for (int e = tid; e < PT * D; e += 256) {
-            const int p = e / D, j = e % D;
-            Ws[p][j] = p0 + p < nproj ? w[(size_t)(p0 + p) * D + j] : 0.f;
+#pragma unroll
+        for (int k = 0; k < NW; ++k) {
+            const int e = tid + NT * k, pp = e / (D / 4), j = 4 * (e % (D / 4));
+            if (e < PT * D / 4) *reinterpret_cast<float4 *>(Ws + pp * DP + j) = xw[k];
         }
         __syncthreads();
-#pragma unroll 4
-        for (int p = 0; p < PT; ++p) {
-            float cv[4], wv[CD];
+        if (p0 + PT < nproj) fetch(p0 + PT);
+        if (pos) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) cv[u] = Cs[4 * ty + u][p];
-#pragma unroll
-            for (int c = 0; c < CD; ++c) wv[c] = Ws[p][tx + 16 * c];
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-#pragma unroll
-                for (int c = 0; c < CD; ++c) acc[u][c] = fmaf(cv[u], wv[c], acc[u][c]);
+            for (int u = 0; u < 4; ++u) {
+                const float4 cv = *reinterpret_cast<const float4 *>(Cs + (ty + 16 * u) * P + 4 * tx);
+                rs[u] += (cv.x + cv.y) + (cv.z + cv.w);
+            }
         }
+#pragma unroll
+        for (int gi = 0; gi < NG; ++gi)
+            if (64 * gi + 4 * tx < D) mm_nn(acc[gi], Cs, P, Ws + 64 * gi, DP, PT, ty, tx);
     }
-    const float sgn = map == FAVOR_MAP_POSITIVE ? -1.f : (map == FAVOR_MAP_TRIG_SOFTMAX ? 1.f : 0.f);
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) rs[u] += __shfl_xor_sync(0xffffffffu, rs[u], o);
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-        const int i = 4 * ty + u;
+        const int i = ty + 16 * u;
         if (i >= n) continue;
+        const float term = pos ? -rs[u] : (map == FAVOR_MAP_TRIG_SOFTMAX ? tot[i] : 0.f);
 #pragma unroll
-        for (int c = 0; c < CD; ++c) {
-            const int j = tx + 16 * c;
-            dx[(row0 + i) * D + j] = fmaf(sgn * tot[i], load_in(x, (row0 + i) * D + j), acc[u][c]);
+        for (int gi = 0; gi < NG; ++gi) {
+            const int j = 64 * gi + 4 * tx;
+            if (j >= D) continue;
+            const size_t o = (row0 + i) * D + j;
+            *reinterpret_cast<float4 *>(dx + o) =
+                make_float4(fmaf(term, load_in(x, o), acc[gi][u][0]), fmaf(term, load_in(x, o + 1), acc[gi][u][1]),
+                            fmaf(term, load_in(x, o + 2), acc[gi][u][2]), fmaf(term, load_in(x, o + 3), acc[gi][u][3]));
         }
     }
 }
@@ -1189,20 +1226,29 @@ int backward_dv(const T *q, const T *k, const T *v, const float *omega, const fl
         stats_end(st);
         FAVOR_LAUNCH_CHECK();
     }
-    const unsigned cgr = (unsigned)std::min<size_t>((rows * p.nproj + 255) / 256, 152 * 64);
-    bwd_coeff<<<cgr, 256, 0, st>>>(Pq, dphiq, phiq, lsq, hmax, rows, p.L, p.nproj, p.r, p.map, 0);
-    FAVOR_LAUNCH_CHECK();
-    bwd_coeff<<<cgr, 256, 0, st>>>(Pk, dphik, phik, lsk, hmax, rows, p.L, p.nproj, p.r, p.map, 1);
-    FAVOR_LAUNCH_CHECK();
+    if (p.map != FAVOR_MAP_POSITIVE) {   // the positive map's coefficients are formed in bwd_dx
+        const unsigned cgr = (unsigned)std::min<size_t>((rows * p.nproj + 255) / 256, 152 * 64);
+        bwd_coeff<<<cgr, 256, 0, st>>>(Pq, dphiq, phiq, lsq, hmax, rows, p.L, p.nproj, p.r, p.map, 0);
+        FAVOR_LAUNCH_CHECK();
+        bwd_coeff<<<cgr, 256, 0, st>>>(Pk, dphik, phik, lsk, hmax, rows, p.L, p.nproj, p.r, p.map, 1);
+        FAVOR_LAUNCH_CHECK();
+    }
     {
         const dim3 xg((p.L + 63) / 64, p.BH);
-        auto dx_launch = [&](auto kern) {
-            kern<<<xg, 256, 0, st>>>(Pq, dphiq, phiq, q, omega, dq, p.L, p.H, p.nproj, p.r, p.map);
-            kern<<<xg, 256, 0, st>>>(Pk, dphik, phik, k, omega, dk, p.L, p.H, p.nproj, p.r, p.map);
+        auto dx_launch = [&](auto kern, int D) -> int {
+            const size_t smem = sizeof(float) * (64 * 68 + 64 * (D + 4) + 64);
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+                cudaGetLastError();
+                return FAVOR_ERR_CUDA;
+            }
+            kern<<<xg, 256, smem, st>>>(Pq, dphiq, phiq, q, omega, dq, p.L, p.H, p.nproj, p.r, p.map);
+            kern<<<xg, 256, smem, st>>>(Pk, dphik, phik, k, omega, dk, p.L, p.H, p.nproj, p.r, p.map);
+            return FAVOR_OK;
         };
-        if (p.d == 32) dx_launch(bwd_dx<T, 32>);
-        else if (p.d == 64) dx_launch(bwd_dx<T, 64>);
-        else dx_launch(bwd_dx<T, 128>);
+        const int rc = p.d == 32 ? dx_launch(bwd_dx<T, 32>, 32)
+                       : p.d == 64 ? dx_launch(bwd_dx<T, 64>, 64)
+                                   : dx_launch(bwd_dx<T, 128>, 128);
+        if (rc != FAVOR_OK) return rc;
         FAVOR_LAUNCH_CHECK();
     }
     if (dw && !map_is_elementwise(p.map)) {
