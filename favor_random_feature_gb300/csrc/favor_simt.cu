@@ -536,27 +536,27 @@ __global__ void bwd_state_suffix(float *__restrict__ R, int nseg, size_t per_seg
 
 // dphi_q, dphi_k [rows][r] and dv [rows][dv] of a chunk of C = 64 rows from the
 // entering state S, the leaving state R and (causal) the masked A, B inside
-// it; block per (chunk, head), kBwdThreads threads, 64-feature tiles:
-//   B = Y [V | 1]^T, masked to j <= i (and its transpose)
+// it; block per (chunk, head), 256 threads, 64-feature tiles (two blocks per
+// SM at dv = 64):
+//   B = Y [V | 1]^T, masked to j <= i
 //   pass 1: A += phi_q phi_k^T,  dv += phi_k R[:, :dv]; then dv += A^T dnum
-//   pass 2: dphi_q = Y S^T + B phi_k,  dphi_k = [V | 1] R^T + B^T phi_q
+//   pass 2: dphi_q = Y S^T + B phi_k, then dphi_k = [V | 1] R^T + B^T phi_q
 template <typename T, int DV>
-__global__ void __launch_bounds__(kBwdThreads) bwd_chunk(const float *__restrict__ phiq, const float *__restrict__ phik,
+__global__ void __launch_bounds__(kBwdThreads, DV <= 64 ? 2 : 1) bwd_chunk(const float *__restrict__ phiq, const float *__restrict__ phik,
                                                  const T *__restrict__ v, const float *__restrict__ Sin,
                                                  const float *__restrict__ Rout, const float *__restrict__ Y,
                                                  float *__restrict__ dphiq, float *__restrict__ dphik,
                                                  float *__restrict__ dV, int L, int r, int nst, int causal) {
     constexpr int C = kBwdRows, FT = 64, P = FT + 4, W = DV + 1, WP = DV + 4, NG = (DV + 63) / 64;
-    constexpr int NT = kBwdThreads, RS = NT / 16, RU = 64 / RS;
+    constexpr int NT = kBwdThreads;
+    static_assert(NT == 256, "the tiled products assume 256 threads");
     extern __shared__ float4 sm4[];
     float *Ys = reinterpret_cast<float *>(sm4);   // [C][WP]  dnum | dden | 0
     float *Vs = Ys + C * WP;                      // [C][WP]  v | 1 | 0
     float *Bs = Vs + C * WP;                      // [C][P]   B
-    float *Bt = Bs + C * P;                       // [C][P]   B^T
-    float *Qt = Bt + C * P;                       // [C][P]   phi_q tile (rows x features); A^T after pass 1
-    float *Kt = Qt + C * P;                       // [C][P]   phi_k tile
-    float *Ss = Kt + C * P;                       // [WP][P]  S^T tile (pass 2); R tile [FT][WP] (pass 1)
-    float *Rs = Ss + WP * P;                      // [WP][P]  R^T tile (pass 2)
+    float *X1 = Bs + C * P;                       // [C][P]   phi_q (pass 1), A (after it), phi_k (pass 2)
+    float *X2 = X1 + C * P;                       // [C][P]   phi_k (pass 1), phi_q (pass 2)
+    float *Ts = X2 + C * P;                       // R tile [FT][WP] (pass 1); S^T, R^T [WP][P] (pass 2)
     const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
     const int ch = blockIdx.x, bh = blockIdx.y, t0 = ch * C, n = min(C, L - t0);
     const size_t row0 = (size_t)bh * L + t0;
@@ -569,138 +569,133 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_chunk(const float *__restrict
         Ys[e] = ok ? Y[(row0 + i) * W + c] : 0.f;
         Vs[e] = ok ? (c < DV ? load_in(v, (row0 + i) * DV + c) : 1.f) : 0.f;
     }
-    // the next feature tile is read into registers while the current one is
-    // used: phi_q, phi_k (NX float4 each) and the state rows (NS values each)
-    constexpr int NX = C * FT / 4 / NT, NS = (FT * W + NT - 1) / NT;
-    float4 xq[NX], xk[NX];
-    float xs[NS], xr[NS];
-    auto fetch_x = [&](int f0) {
+    // rows x 64 features of phi (phiq or phik) into a [C][P] tile
+    auto load_x = [&](float *dst, const float *src, int f0) {
+        float4 t[C * FT / 4 / NT];
 #pragma unroll
-        for (int k = 0; k < NX; ++k) {
+        for (int k = 0; k < C * FT / 4 / NT; ++k) {
             const int e = tid + NT * k, i = e / (FT / 4), f = 4 * (e % (FT / 4));
-            const bool ok = i < n && f0 + f < r;   // r % 4 == 0
-            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-            xq[k] = ok ? *reinterpret_cast<const float4 *>(phiq + (row0 + i) * r + f0 + f) : z;
-            xk[k] = ok ? *reinterpret_cast<const float4 *>(phik + (row0 + i) * r + f0 + f) : z;
+            t[k] = (i < n && f0 + f < r) ? *reinterpret_cast<const float4 *>(src + (row0 + i) * r + f0 + f)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);   // r % 4 == 0
+        }
+#pragma unroll
+        for (int k = 0; k < C * FT / 4 / NT; ++k) {
+            const int e = tid + NT * k, i = e / (FT / 4), f = 4 * (e % (FT / 4));
+            *reinterpret_cast<float4 *>(dst + i * P + f) = t[k];
         }
     };
-    auto put_x = [&]() {
-#pragma unroll
-        for (int k = 0; k < NX; ++k) {
-            const int e = tid + NT * k, i = e / (FT / 4), f = 4 * (e % (FT / 4));
-            *reinterpret_cast<float4 *>(Qt + i * P + f) = xq[k];
-            *reinterpret_cast<float4 *>(Kt + i * P + f) = xk[k];
-        }
-    };
-    auto fetch_s = [&](const float *src, float(&dst)[NS], int f0) {   // rows f0 .. f0 + FT - 1, all W columns
+    // state rows f0 .. f0 + 63 (all W columns) transposed into [WP][P]
+    auto load_st = [&](const float *src, int f0) {
+        constexpr int NS = (FT * W + NT - 1) / NT;
+        float t[NS];
 #pragma unroll
         for (int k = 0; k < NS; ++k) {
             const int e = tid + NT * k, f = e / W, c = e % W;
-            dst[k] = (e < FT * W && f0 + f < r) ? src[(size_t)(f0 + f) * W + c] : 0.f;
+            t[k] = (e < FT * W && f0 + f < r) ? src[(size_t)(f0 + f) * W + c] : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < NS; ++k) {
+            const int e = tid + NT * k;
+            if (e < FT * W) Ts[(e % W) * P + e / W] = t[k];
         }
     };
     __syncthreads();
     if (causal) {
-        float b[RU][4] = {};
-        mm_nt<RU, RS>(b, Ys, WP, Vs, WP, WP, ty, tx);
+        float b[4][4] = {};
+        mm_nt(b, Ys, WP, Vs, WP, WP, ty, tx);
 #pragma unroll
-        for (int u = 0; u < RU; ++u)
+        for (int u = 0; u < 4; ++u)
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
-                const int i = ty + RS * u, j = tx + 16 * w;
-                const float x = j <= i ? b[u][w] : 0.f;
-                Bs[i * P + j] = x;
-                Bt[j * P + i] = x;
+                const int i = ty + 16 * u, j = tx + 16 * w;
+                Bs[i * P + j] = j <= i ? b[u][w] : 0.f;
             }
     }
-    // ---- pass 1 (R tile row-major [f][WP] in Ss; its pad columns are never read)
-    float a[RU][4] = {}, dvr[NG][RU][4] = {};
-    fetch_x(0);
-    fetch_s(R, xr, 0);
+    // ---- pass 1 (R tile row-major [f][WP]; its pad columns are never read)
+    float a[4][4] = {}, dvr[NG][4][4] = {};
     for (int f0 = 0; f0 < r; f0 += FT) {
         __syncthreads();
-        put_x();
+        load_x(X1, phiq, f0);
+        load_x(X2, phik, f0);
+        {
+            constexpr int NS = (FT * W + NT - 1) / NT;
+            float t[NS];
 #pragma unroll
-        for (int k = 0; k < NS; ++k) {
-            const int e = tid + NT * k;
-            if (e < FT * W) Ss[(e / W) * WP + e % W] = xr[k];
+            for (int k = 0; k < NS; ++k) {
+                const int e = tid + NT * k, f = e / W, c = e % W;
+                t[k] = (e < FT * W && f0 + f < r) ? R[(size_t)(f0 + f) * W + c] : 0.f;
+            }
+#pragma unroll
+            for (int k = 0; k < NS; ++k) {
+                const int e = tid + NT * k;
+                if (e < FT * W) Ts[(e / W) * WP + e % W] = t[k];
+            }
         }
         __syncthreads();
-        if (f0 + FT < r) {
-            fetch_x(f0 + FT);
-            fetch_s(R, xr, f0 + FT);
-        }
-        if (causal) mm_nt<RU, RS>(a, Qt, P, Kt, P, FT, ty, tx);
+        if (causal) mm_nt(a, X1, P, X2, P, FT, ty, tx);
 #pragma unroll
         for (int g = 0; g < NG; ++g)
-            if (64 * g + 4 * tx < DV) mm_nn<RU, RS>(dvr[g], Kt, P, Ss + 64 * g, WP, FT, ty, tx);
+            if (64 * g + 4 * tx < DV) mm_nn(dvr[g], X2, P, Ts + 64 * g, WP, FT, ty, tx);
     }
-    // the first tile of pass 2 is read while A^T dnum is formed
-    fetch_x(0);
-    fetch_s(S, xs, 0);
-    fetch_s(R, xr, 0);
     __syncthreads();
     if (causal) {
 #pragma unroll
-        for (int u = 0; u < RU; ++u)
+        for (int u = 0; u < 4; ++u)
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
-                const int i = ty + RS * u, j = tx + 16 * w;
-                Qt[j * P + i] = j <= i ? a[u][w] : 0.f;   // A^T
+                const int i = ty + 16 * u, j = tx + 16 * w;
+                X1[i * P + j] = j <= i ? a[u][w] : 0.f;   // A
             }
     }
     // pad rows W .. WP - 1 of the transposed state tiles stay zero through pass 2
-    for (int e = tid; e < (WP - W) * P; e += NT) {
-        Ss[W * P + e] = 0.f;
-        Rs[W * P + e] = 0.f;
-    }
+    for (int e = tid; e < (WP - W) * P; e += NT) Ts[W * P + e] = 0.f;
     __syncthreads();
     if (causal) {
 #pragma unroll
         for (int g = 0; g < NG; ++g)
-            if (64 * g + 4 * tx < DV) mm_nn<RU, RS>(dvr[g], Qt, P, Ys + 64 * g, WP, C, ty, tx);
+            if (64 * g + 4 * tx < DV) mm_tn(dvr[g], X1, P, Ys + 64 * g, WP, C, ty, tx);
     }
 #pragma unroll
     for (int g = 0; g < NG; ++g)
 #pragma unroll
-        for (int u = 0; u < RU; ++u) {
-            const int j = ty + RS * u, c = 64 * g + 4 * tx;
+        for (int u = 0; u < 4; ++u) {
+            const int j = ty + 16 * u, c = 64 * g + 4 * tx;
             if (j < n && c < DV)
                 *reinterpret_cast<float4 *>(dV + (row0 + j) * DV + c) =
                     make_float4(dvr[g][u][0], dvr[g][u][1], dvr[g][u][2], dvr[g][u][3]);
         }
-    // ---- pass 2 (S^T, R^T tiles [c][P])
+    // ---- pass 2
     for (int f0 = 0; f0 < r; f0 += FT) {
         __syncthreads();
-        put_x();
+        load_x(X1, phik, f0);
+        load_x(X2, phiq, f0);
+        load_st(S, f0);
+        __syncthreads();
+        {
+            float dq[4][4] = {};
+            mm_nn(dq, Ys, WP, Ts, P, WP, ty, tx);
+            if (causal) mm_nn(dq, Bs, P, X1, P, C, ty, tx);
 #pragma unroll
-        for (int k = 0; k < NS; ++k) {
-            const int e = tid + NT * k;
-            if (e < FT * W) {
-                const int f = e / W, c = e % W;
-                Ss[c * P + f] = xs[k];
-                Rs[c * P + f] = xr[k];
+            for (int u = 0; u < 4; ++u) {
+                const int i = ty + 16 * u, f = f0 + 4 * tx;
+                if (i < n && f < r)
+                    *reinterpret_cast<float4 *>(dphiq + (row0 + i) * r + f) =
+                        make_float4(dq[u][0], dq[u][1], dq[u][2], dq[u][3]);
             }
         }
         __syncthreads();
-        if (f0 + FT < r) {
-            fetch_x(f0 + FT);
-            fetch_s(S, xs, f0 + FT);
-            fetch_s(R, xr, f0 + FT);
-        }
-        float dq[RU][4] = {}, dk[RU][4] = {};
-        mm_nn<RU, RS>(dq, Ys, WP, Ss, P, WP, ty, tx);
-        mm_nn<RU, RS>(dk, Vs, WP, Rs, P, WP, ty, tx);
-        if (causal) {
-            mm_nn<RU, RS>(dq, Bs, P, Kt, P, C, ty, tx);
-            mm_nn<RU, RS>(dk, Bt, P, Qt, P, C, ty, tx);
-        }
+        load_st(R, f0);
+        __syncthreads();
+        {
+            float dk[4][4] = {};
+            mm_nn(dk, Vs, WP, Ts, P, WP, ty, tx);
+            if (causal) mm_tn(dk, Bs, P, X2, P, C, ty, tx);
 #pragma unroll
-        for (int u = 0; u < RU; ++u) {
-            const int i = ty + RS * u, f = f0 + 4 * tx;
-            if (i < n && f < r) {
-                *reinterpret_cast<float4 *>(dphiq + (row0 + i) * r + f) = make_float4(dq[u][0], dq[u][1], dq[u][2], dq[u][3]);
-                *reinterpret_cast<float4 *>(dphik + (row0 + i) * r + f) = make_float4(dk[u][0], dk[u][1], dk[u][2], dk[u][3]);
+            for (int u = 0; u < 4; ++u) {
+                const int i = ty + 16 * u, f = f0 + 4 * tx;
+                if (i < n && f < r)
+                    *reinterpret_cast<float4 *>(dphik + (row0 + i) * r + f) =
+                        make_float4(dk[u][0], dk[u][1], dk[u][2], dk[u][3]);
             }
         }
     }
@@ -708,7 +703,8 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_chunk(const float *__restrict
 
 template <typename T, int DV>
 constexpr size_t bwd_chunk_smem() {
-    return sizeof(float) * (2 * kBwdRows * (DV + 4) + 4 * kBwdRows * 68 + 2 * (DV + 4) * 68);
+    return sizeof(float) * (2 * kBwdRows * (DV + 4) + 3 * kBwdRows * 68 +
+                            ((DV + 4) * 68 > 64 * (DV + 4) ? (DV + 4) * 68 : 64 * (DV + 4)));
 }
 
 // per (row, projection p): the coefficient c of the map derivative, in place
