@@ -514,26 +514,6 @@ namespace {
 constexpr int kBwdRows = 64;    // rows per chunk (= kChunk)
 constexpr int kBwdThreads = 256;   // threads of a bwd_chunk block
 
-// exclusive suffix over segments, in place: R_s <- sum_{s' > s} R_s'
-__global__ void bwd_state_suffix(float *__restrict__ R, int nseg, size_t per_seg, int BH) {
-    const size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
-    if (e >= per_seg * BH) return;
-    const int bh = (int)(e / per_seg);
-    const size_t within = e % per_seg;
-    float *base = R + (size_t)bh * nseg * per_seg + within;
-    float run = 0.f;
-    for (int s0 = nseg - 1; s0 >= 0; s0 -= 8) {
-        float t[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) t[i] = s0 - i >= 0 ? base[(size_t)(s0 - i) * per_seg] : 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            if (s0 - i >= 0) base[(size_t)(s0 - i) * per_seg] = run;
-            run += t[i];
-        }
-    }
-}
-
 // dphi_q, dphi_k [rows][r] and dv [rows][dv] of a chunk of C = 64 rows from the
 // entering state S, the leaving state R and (causal) the masked A, B inside
 // it; block per (chunk, head), 256 threads, 64-feature tiles (two blocks per
@@ -851,68 +831,56 @@ __global__ void __launch_bounds__(256) bwd_dx(float *__restrict__ C, const float
     }
 }
 
-// per chunk of 64 rows: St[f][c] = sum_rows phi[row][f] Yc[row][c], c <= dv, where
-// Yc = [v | 1] (forward state) or the rows' [dnum | dden] (backward state);
-// block per (chunk, head), 256 threads, 64-feature tiles of phi read a tile
-// ahead into registers; thread (ty, tx) owns features ty + 16 u and value
-// columns 4 tx + w (+ 64 per group); the last column (sum of phi, or of
-// phi dden) from per-thread row partials summed over tx.
+// The chunk states of a head in one pass over its chunks: the state of chunk c
+// is St_c[f][col] = sum_{rows of c} phi[row][f] Yc[row][col], col <= dv, with
+// Yc = [v | 1] (forward) or the rows' [dnum | dden] (backward).  Written per
+// chunk: causal, the exclusive prefix (forward: chunks before c; reverse:
+// chunks after c); non-causal, the total of the z-th of gridDim.z ranges of
+// chunks into chunk slot z (state_sum adds them).  Block per (64-feature
+// tile, head, range), 256 threads, the chunks in order (a fixed
+// summation order), the next chunk's rows read into registers while the
+// current one is added; thread (ty, tx) owns features ty + 16 u and columns
+// 4 tx + w (+ 64 per group) of the running state; the last column (sum of
+// phi, or of phi dden) from per-thread row partials summed over tx.
 template <typename T, int DV>
-__global__ void __launch_bounds__(256) state_tile(const float *__restrict__ phi, const T *__restrict__ v,
-                                                  const float *__restrict__ Y, float *__restrict__ S, int L, int r,
-                                                  int nch) {
+__global__ void __launch_bounds__(256, 2) state_scan(const float *__restrict__ phi, const T *__restrict__ v,
+                                                     const float *__restrict__ Y, float *__restrict__ S, int L,
+                                                     int r, int nch, int causal, int reverse) {
     constexpr int C = kBwdRows, FT = 64, P = FT + 4, W = DV + 1, WP = DV + 4, NG = (DV + 63) / 64, NT = 256;
-    constexpr int NX = C * FT / 4 / NT;
+    constexpr int NX = C * FT / 4 / NT, NY = (C * W + NT - 1) / NT;
     extern __shared__ float4 sm4[];
-    float *Ps = reinterpret_cast<float *>(sm4);   // [C][P]  phi tile (rows x features)
+    float *Ps = reinterpret_cast<float *>(sm4);   // [C][P]  phi rows x this block's 64 features
     float *Ys = Ps + C * P;                       // [C][WP] Yc | 0
     const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
-    const int ch = blockIdx.x, bh = blockIdx.y, t0 = ch * C, n = min(C, L - t0);
-    const size_t row0 = (size_t)bh * L + t0;
-#pragma unroll 4
-    for (int e = tid; e < C * WP; e += NT) {
-        const int i = e / WP, c = e % WP;
-        float y = 0.f;
-        if (i < n && c < W) y = Y ? Y[(row0 + i) * W + c] : (c < DV ? load_in(v, (row0 + i) * DV + c) : 1.f);
-        Ys[e] = y;
-    }
+    const int f0 = blockIdx.x * FT, bh = blockIdx.y;
     float4 xp[NX];
-    auto fetch = [&](int f0) {
+    float xy[NY];
+    auto fetch = [&](int ch) {
+        const int t0 = ch * C, n = min(C, L - t0);
+        const size_t row0 = (size_t)bh * L + t0;
 #pragma unroll
         for (int k = 0; k < NX; ++k) {
             const int e = tid + NT * k, i = e / (FT / 4), f = 4 * (e % (FT / 4));
             xp[k] = (i < n && f0 + f < r) ? *reinterpret_cast<const float4 *>(phi + (row0 + i) * r + f0 + f)
-                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);   // r % 4 == 0
+        }
+#pragma unroll
+        for (int k = 0; k < NY; ++k) {
+            const int e = tid + NT * k, i = e / W, c = e % W;
+            float y = 0.f;
+            if (e < C * W && i < n) y = Y ? Y[(row0 + i) * W + c] : (c < DV ? load_in(v, (row0 + i) * DV + c) : 1.f);
+            xy[k] = y;
         }
     };
-    float *dst = S + ((size_t)bh * nch + ch) * r * W;
-    fetch(0);
-    for (int f0 = 0; f0 < r; f0 += FT) {
-        __syncthreads();
-#pragma unroll
-        for (int k = 0; k < NX; ++k) {
-            const int e = tid + NT * k, i = e / (FT / 4), f = 4 * (e % (FT / 4));
-            *reinterpret_cast<float4 *>(Ps + i * P + f) = xp[k];
-        }
-        __syncthreads();
-        if (f0 + FT < r) fetch(f0 + FT);
-        float acc[NG][4][4] = {}, zc[4] = {};
-#pragma unroll
-        for (int gi = 0; gi < NG; ++gi)
-            if (64 * gi + 4 * tx < DV) mm_tn(acc[gi], Ps, P, Ys + 64 * gi, WP, C, ty, tx);
-        // column DV: rows tx, tx + 16, ... of this thread, summed over tx
+    for (int e = tid; e < C * WP; e += NT) Ys[e] = 0.f;   // pad columns stay zero
+    float acc[NG][4][4] = {}, zp[4] = {};
+    auto write_state = [&](int slot) {
+        float *dst = S + ((size_t)bh * nch + slot) * r * W;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
+            float z = zp[u];
 #pragma unroll
-            for (int ii = 0; ii < C / 16; ++ii) {
-                const int i = tx + 16 * ii;
-                zc[u] = fmaf(Ps[i * P + ty + 16 * u], Ys[i * WP + DV], zc[u]);
-            }
-#pragma unroll
-            for (int o = 8; o > 0; o >>= 1) zc[u] += __shfl_xor_sync(0xffffffffu, zc[u], o);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
+            for (int o = 8; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
             const int f = f0 + ty + 16 * u;
             if (f >= r) continue;
 #pragma unroll
@@ -923,20 +891,49 @@ __global__ void __launch_bounds__(256) state_tile(const float *__restrict__ phi,
                     for (int w = 0; w < 4; ++w) dst[(size_t)f * W + c + w] = acc[gi][u][w];
                 }
             }
-            if (tx == 0) dst[(size_t)f * W + DV] = zc[u];
+            if (tx == 0) dst[(size_t)f * W + DV] = z;
         }
+    };
+    // this block's chunks: all (causal) or the z-th range (non-causal)
+    const int per_z = (nch + gridDim.z - 1) / gridDim.z, c_lo = blockIdx.z * per_z, c_n = min(nch, c_lo + per_z) - c_lo;
+    if (c_n > 0) fetch(reverse ? c_lo + c_n - 1 : c_lo);
+    for (int it = 0; it < c_n; ++it) {
+        const int ch = reverse ? c_lo + c_n - 1 - it : c_lo + it;
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < NX; ++k) {
+            const int e = tid + NT * k, i = e / (FT / 4), f = 4 * (e % (FT / 4));
+            *reinterpret_cast<float4 *>(Ps + i * P + f) = xp[k];
+        }
+#pragma unroll
+        for (int k = 0; k < NY; ++k) {
+            const int e = tid + NT * k;
+            if (e < C * W) Ys[(e / W) * WP + e % W] = xy[k];
+        }
+        __syncthreads();
+        if (it + 1 < c_n) fetch(reverse ? ch - 1 : ch + 1);
+        if (causal) write_state(ch);   // exclusive: before this chunk is added
+#pragma unroll
+        for (int gi = 0; gi < NG; ++gi)
+            if (64 * gi + 4 * tx < DV) mm_tn(acc[gi], Ps, P, Ys + 64 * gi, WP, C, ty, tx);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int ii = 0; ii < C / 16; ++ii) {
+                const int i = tx + 16 * ii;
+                zp[u] = fmaf(Ps[i * P + ty + 16 * u], Ys[i * WP + DV], zp[u]);
+            }
     }
+    if (!causal) write_state(blockIdx.z);
 }
 
-// non-causal: the chunk states summed into chunk slot 0 (fixed order)
-__global__ void state_total(float *__restrict__ S, int nch, size_t per, int BH) {
+// non-causal: chunk slots 1 .. nz - 1 added to slot 0 in order
+__global__ void state_sum(float *__restrict__ S, int nch, int nz, size_t per, int BH) {
     const size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
     if (e >= per * BH) return;
-    const int bh = (int)(e / per);
-    const size_t within = e % per;
-    float *base = S + (size_t)bh * nch * per + within;
-    float sum = 0.f;
-    for (int s = 0; s < nch; ++s) sum += base[(size_t)s * per];
+    float *base = S + (e / per) * nch * per + e % per;
+    float sum = base[0];
+    for (int z = 1; z < nz; ++z) sum += base[(size_t)z * per];
     base[0] = sum;
 }
 
@@ -1139,7 +1136,7 @@ __global__ void __launch_bounds__(256) bwd_dw(const float *__restrict__ Cq, cons
     }
 }
 
-// dynamic shared memory of state_tile (DV value columns) and bwd_dw (D input columns)
+// dynamic shared memory of state_scan (DV value columns) and bwd_dw (D input columns)
 template <int DV>
 constexpr size_t state_tile_smem() {
     return sizeof(float) * (kBwdRows * 68 + kBwdRows * (DV + 4));
@@ -1180,19 +1177,19 @@ int backward_dv(const T *q, const T *k, const T *v, const float *omega, const fl
     const unsigned sg = (unsigned)std::min<size_t>((total + 255) / 256, 152 * 64);
     simt_key_scale<<<sg, 256, 0, st>>>(phik, lsk, hmax, p.L, p.r, total);
     FAVOR_LAUNCH_CHECK();
-    const dim3 cg(nch, p.BH);
+    // non-causal: the chunks in up to 8 ranges (more blocks), summed by state_sum
+    const int nz = p.causal ? 1 : std::min(nch, 8);
+    const dim3 cg(nch, p.BH), sg2((p.r + 63) / 64, p.BH, nz);
     const unsigned sb = (unsigned)((per * p.BH + 255) / 256);
     const size_t st_smem = state_tile_smem<DV>();
-    if (cudaFuncSetAttribute(state_tile<T, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st_smem) !=
+    if (cudaFuncSetAttribute(state_scan<T, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st_smem) !=
         cudaSuccess) {
         cudaGetLastError();
         return FAVOR_ERR_CUDA;
     }
     // the forward states entering each chunk (causal: exclusive prefix) or the total (chunk slot 0)
-    state_tile<T, DV><<<cg, 256, st_smem, st>>>(phik, v, nullptr, S, p.L, p.r, nch);
-    FAVOR_LAUNCH_CHECK();
-    if (p.causal) simt_state_prefix<<<sb, 256, 0, st>>>(S, nch, per, p.BH);
-    else state_total<<<sb, 256, 0, st>>>(S, nch, per, p.BH);
+    state_scan<T, DV><<<sg2, 256, st_smem, st>>>(phik, v, nullptr, S, p.L, p.r, nch, p.causal, 0);
+    if (nz > 1) state_sum<<<sb, 256, 0, st>>>(S, nch, nz, per, p.BH);
     FAVOR_LAUNCH_CHECK();
     {
         const size_t smem = bwd_rows_smem<DV>();
@@ -1205,10 +1202,8 @@ int backward_dv(const T *q, const T *k, const T *v, const float *omega, const fl
         FAVOR_LAUNCH_CHECK();
     }
     // the states leaving each chunk (causal: exclusive suffix) or the total
-    state_tile<T, DV><<<cg, 256, st_smem, st>>>(phiq, v, Y, R, p.L, p.r, nch);
-    FAVOR_LAUNCH_CHECK();
-    if (p.causal) bwd_state_suffix<<<sb, 256, 0, st>>>(R, nch, per, p.BH);
-    else state_total<<<sb, 256, 0, st>>>(R, nch, per, p.BH);
+    state_scan<T, DV><<<sg2, 256, st_smem, st>>>(phiq, v, Y, R, p.L, p.r, nch, p.causal, 1);
+    if (nz > 1) state_sum<<<sb, 256, 0, st>>>(R, nch, nz, per, p.BH);
     FAVOR_LAUNCH_CHECK();
     {
         const size_t smem = bwd_chunk_smem<T, DV>();
