@@ -1,6 +1,7 @@
 // favor_abi.cu -- the extern "C" boundary of libfavor: argument validation,
 // the per-device workspace, the device status word and dispatch to the
 // tensor-core path (bf16 inputs) or the fp32 SIMT path.
+#include <algorithm>
 #include <atomic>
 #include <cstdio>
 #include <cstring>
@@ -17,12 +18,17 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
+constexpr int kHostGroups = 4;   // head groups of the host-buffer entry point
+
 struct DeviceState {
     void *ws = nullptr;
     size_t ws_bytes = 0;
     void *stage = nullptr;     // host-API staging buffer
     size_t stage_bytes = 0;
     int *status = nullptr;     // device address of g_device_status
+    // host-API copy streams and their events (created on first use)
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    cudaEvent_t ev_in[kHostGroups] = {}, ev_done[kHostGroups] = {}, ev_out = nullptr;
 };
 
 std::mutex g_mu;
@@ -261,6 +267,51 @@ extern "C" int favor_attn_backward_f32(const float *q, const float *k, const flo
                           stream);
 }
 
+// The host-buffer entry point cuts the heads into up to kHostGroups groups of
+// whole heads (whole batches when B allows, else head ranges of one batch) and
+// pipelines them over three streams: the inputs of group g + 1 are copied in
+// on s_in while group g is computed on the caller's stream and group g - 1 is
+// copied out on s_out.  Each group is an independent forward pass over its
+// heads (its own segment plan).
+namespace {
+struct HostGroup {
+    int b0, nb, h0, nh;
+};
+
+int host_groups(int B, int H, HostGroup *g) {
+    int n = 0;
+    if (B >= kHostGroups) {
+        for (int i = 0; i < kHostGroups; ++i) {
+            const int b0 = (int)((long long)B * i / kHostGroups), b1 = (int)((long long)B * (i + 1) / kHostGroups);
+            if (b1 > b0) g[n++] = {b0, b1 - b0, 0, H};
+        }
+    } else {
+        const int parts = std::min(H, kHostGroups / B);
+        for (int b = 0; b < B; ++b)
+            for (int i = 0; i < parts; ++i) {
+                const int h0 = (int)((long long)H * i / parts), h1 = (int)((long long)H * (i + 1) / parts);
+                if (h1 > h0) g[n++] = {b, 1, h0, h1 - h0};
+            }
+    }
+    return n;
+}
+
+int host_streams(DeviceState &s) {
+    if (s.s_in) return FAVOR_OK;
+    bool ok = cudaStreamCreateWithFlags(&s.s_in, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&s.s_out, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&s.ev_out, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; ok && i < kHostGroups; ++i)
+        ok = cudaEventCreateWithFlags(&s.ev_in[i], cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&s.ev_done[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+        cudaGetLastError();
+        return FAVOR_ERR_CUDA;
+    }
+    return FAVOR_OK;
+}
+}  // namespace
+
 extern "C" int favor_attn_forward_host(const void *q, const void *k, const void *v,
                                        const float *omega, float *out, int B, int H, int L, int d,
                                        int dv, int m, int causal, int feature_map,
@@ -278,23 +329,49 @@ extern "C" int favor_attn_forward_host(const void *q, const void *k, const void 
     int dev;
     if ((rc = current_device(&dev))) return rc;
     char *stage;
+    DeviceState &ds = g_dev[dev];
     {
         std::lock_guard<std::mutex> lk(g_mu);
-        stage = static_cast<char *>(grow(&g_dev[dev].stage, &g_dev[dev].stage_bytes, need, &rc));
+        stage = static_cast<char *>(grow(&ds.stage, &ds.stage_bytes, need, &rc));
+        if (stage) rc = host_streams(ds);
     }
-    if (!stage) return rc;
+    if (!stage || rc) return rc ? rc : FAVOR_ERR_NOMEM;
     Carve cv{stage, 0};
     char *dq = cv.take<char>(qb), *dk = cv.take<char>(qb), *dvp = cv.take<char>(vb);
     float *dw = omega ? reinterpret_cast<float *>(cv.take<char>(wb)) : nullptr;
     float *dout = reinterpret_cast<float *>(cv.take<char>(ob));
-    if (cudaMemcpyAsync(dq, q, qb, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
-        cudaMemcpyAsync(dk, k, qb, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
-        cudaMemcpyAsync(dvp, v, vb, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
-        (dw && cudaMemcpyAsync(dw, omega, wb, cudaMemcpyHostToDevice, stream) != cudaSuccess))
+    HostGroup grp[kHostGroups];
+    const int ng = host_groups(B, H, grp);
+    const char *hq = static_cast<const char *>(q), *hk = static_cast<const char *>(k),
+               *hv = static_cast<const char *>(v);
+    char *hout = reinterpret_cast<char *>(out);
+    // the copy streams start after the work already queued on the caller's stream
+    if (cudaEventRecord(ds.ev_out, stream) != cudaSuccess || cudaStreamWaitEvent(ds.s_in, ds.ev_out, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(ds.s_out, ds.ev_out, 0) != cudaSuccess)
         return FAVOR_ERR_CUDA;
-    rc = favor_attn_forward(dq, dk, dvp, dw, dout, B, H, L, d, dv, m, causal, feature_map, stream);
-    if (rc) return rc;
-    if (cudaMemcpyAsync(out, dout, ob, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    if (dw && cudaMemcpyAsync(dw, omega, wb, cudaMemcpyHostToDevice, ds.s_in) != cudaSuccess) return FAVOR_ERR_CUDA;
+    for (int i = 0; i < ng; ++i) {
+        const HostGroup &g = grp[i];
+        // rows [r0, r0 + nr) of the flattened [B H L] rows
+        const size_t r0 = ((size_t)g.b0 * H + g.h0) * L, nr = (size_t)g.nb * g.nh * L;
+        // whole batches: contiguous; a head range of one batch: contiguous too
+        if (cudaMemcpyAsync(dq + r0 * d * 2, hq + r0 * d * 2, nr * d * 2, cudaMemcpyHostToDevice, ds.s_in) != cudaSuccess ||
+            cudaMemcpyAsync(dk + r0 * d * 2, hk + r0 * d * 2, nr * d * 2, cudaMemcpyHostToDevice, ds.s_in) != cudaSuccess ||
+            cudaMemcpyAsync(dvp + r0 * dv * 2, hv + r0 * dv * 2, nr * dv * 2, cudaMemcpyHostToDevice, ds.s_in) !=
+                cudaSuccess ||
+            cudaEventRecord(ds.ev_in[i], ds.s_in) != cudaSuccess || cudaStreamWaitEvent(stream, ds.ev_in[i], 0) != cudaSuccess)
+            return FAVOR_ERR_CUDA;
+        rc = favor_attn_forward(dq + r0 * d * 2, dk + r0 * d * 2, dvp + r0 * dv * 2,
+                                dw ? dw + (size_t)g.h0 * p.nproj * d : nullptr, dout + r0 * dv, g.nb, g.nh, L, d, dv, m,
+                                causal, feature_map, stream);
+        if (rc) return rc;
+        if (cudaEventRecord(ds.ev_done[i], stream) != cudaSuccess ||
+            cudaStreamWaitEvent(ds.s_out, ds.ev_done[i], 0) != cudaSuccess ||
+            cudaMemcpyAsync(hout + r0 * dv * 4, reinterpret_cast<char *>(dout) + r0 * dv * 4, nr * dv * 4,
+                            cudaMemcpyDeviceToHost, ds.s_out) != cudaSuccess)
+            return FAVOR_ERR_CUDA;
+    }
+    if (cudaEventRecord(ds.ev_out, ds.s_out) != cudaSuccess || cudaStreamWaitEvent(stream, ds.ev_out, 0) != cudaSuccess)
         return FAVOR_ERR_CUDA;
     return cuda_status(cudaStreamSynchronize(stream));
 }
@@ -371,13 +448,24 @@ extern "C" void favor_release_workspace(void) {
     cudaGetDevice(&cur);
     for (int dev = 0; dev < kMaxDevices; ++dev) {
         DeviceState &s = g_dev[dev];
-        if (!s.ws && !s.stage) continue;
+        if (!s.ws && !s.stage && !s.s_in) continue;
         cudaSetDevice(dev);
         cudaDeviceSynchronize();
         if (s.ws) cudaFree(s.ws);
         if (s.stage) cudaFree(s.stage);
         s.ws = s.stage = nullptr;
         s.ws_bytes = s.stage_bytes = 0;
+        if (s.s_in) {
+            cudaStreamDestroy(s.s_in);
+            cudaStreamDestroy(s.s_out);
+            cudaEventDestroy(s.ev_out);
+            for (int i = 0; i < kHostGroups; ++i) {
+                cudaEventDestroy(s.ev_in[i]);
+                cudaEventDestroy(s.ev_done[i]);
+            }
+            s.s_in = s.s_out = nullptr;
+            s.ev_out = nullptr;
+        }
     }
     cudaSetDevice(cur);
 }

@@ -198,17 +198,24 @@ def test_feature_map_entry(fmap):
         assert np.allclose(got[0, h], want, rtol=1e-4, atol=3e-5 * np.abs(want).max())
 
 
-def test_host_entry_matches_device_entry():
+@pytest.mark.parametrize("B,H,L,causal", [(1, 2, 500, True), (4, 3, 300, True), (6, 2, 257, False), (1, 1, 129, True)],
+                         ids=["heads-split", "batch-groups", "uneven-batches", "one-head"])
+def test_host_entry_matches_oracle(B, H, L, causal):
+    """The host-buffer entry point copies in, computes and copies out head
+    groups (whole batches, or head ranges of one batch) on overlapping streams;
+    each group is its own forward pass, so its rows meet the same bar against
+    the oracle as the device entry point's, and every row is written."""
     import favor_random_feature_gb300 as fv
-    inp = make_inputs(CAUSAL8K, L=500, B=1, H=2)
+    inp = make_inputs(CAUSAL8K, L=L, B=B, H=H)
     w = inp.w
-    dev = run_gpu(inp, True, MAP_POSITIVE)
-    out = np.empty((w.B, w.H, w.L, w.dv), dtype=np.float32)
+    out = np.full((w.B, w.H, w.L, w.dv), np.nan, dtype=np.float32)
     om = np.ascontiguousarray(inp.omega, dtype=np.float32)
     rc = fv.favor_attn_forward_host(inp.q, inp.k, inp.v, om, out, w.B, w.H, w.L, w.d, w.dv,
-                                    w.m, 1, MAP_POSITIVE)
+                                    w.m, int(causal), MAP_POSITIVE)
     assert rc == 0, fv.strerror(rc)
-    assert np.array_equal(out.astype(np.float64), dev)
+    ref = oracle_ref(inp, causal, MAP_POSITIVE)
+    check_bf16(row_errors(out.astype(np.float64), ref), "host entry")
+    check_bf16(row_errors(run_gpu(inp, causal, MAP_POSITIVE), ref), "device entry")
 
 
 # ---------------------------------------------------------------------------
