@@ -18,7 +18,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
-constexpr int kHostGroups = 4;   // head groups of the host-buffer entry point
+constexpr int kHostGroups = 8;   // head groups of the host-buffer entry point
 
 struct DeviceState {
     void *ws = nullptr;
