@@ -129,9 +129,15 @@ int favor_attn_forward_f32(const float *q, const float *k, const float *v, const
 
 /* End-to-end variant of favor_attn_forward on HOST buffers (q/k/v bf16 bits,
  * omega and out fp32; pinned memory gives the fastest copies).  Copies the
- * inputs to a library-owned device staging area on `stream`, runs the
- * forward pass, copies out back and synchronises `stream` before returning.
- * Not for use inside a stream capture.  Returns favor_status_t. */
+ * inputs to a library-owned device staging area, runs the forward pass and
+ * copies out back, in up to eight groups of whole heads (whole batches, or
+ * head ranges of one batch) whose copies run on two library-owned streams
+ * while the caller's `stream` computes the neighbouring groups; each group
+ * is a separate forward pass (its rows agree with one device-buffer call to
+ * within the bf16 parity bar, not bit for bit).  Starts after the work queued
+ * on `stream`, synchronises `stream` before returning.  Not for use inside a
+ * stream capture, nor from two threads at once on one device.  Returns
+ * favor_status_t. */
 int favor_attn_forward_host(const void *q, const void *k, const void *v, const float *omega,
                             float *out, int B, int H, int L, int d, int dv, int m, int causal,
                             int feature_map, cudaStream_t stream);
