@@ -45,14 +45,18 @@ __device__ __forceinline__ void store_out(__nv_bfloat16 *p, size_t i, float v) {
 // (mm_nt) have an odd pitch in 16-byte units, so those loads do not conflict.
 //   mm_nn: acc[u][w] += sum_k A[ty + RS u][k] B[k][4 tx + w]
 //   mm_nt: acc[u][w] += sum_k A[ty + RS u][k] B[tx + 16 w][k]
-template <int RU = 4, int RS = 16>
+// With BLK the rows are 4 ty + u instead (the A rows a warp reads are still
+// shared by its 16-thread halves), so that a triangular operand's loop can
+// stop at the diagonal (k0, k1: the contraction range, multiples of 4).
+template <int RU = 4, int RS = 16, bool BLK = false>
 __device__ __forceinline__ void mm_nn(float (&acc)[RU][4], const float *A, int lda, const float *B, int ldb, int K,
-                                      int ty, int tx) {
+                                      int ty, int tx, int k0 = 0) {
 #pragma unroll 2
-    for (int k = 0; k < K; k += 4) {
+    for (int k = k0; k < K; k += 4) {
         float4 a[RU], b[4];
 #pragma unroll
-        for (int u = 0; u < RU; ++u) a[u] = *reinterpret_cast<const float4 *>(A + (ty + RS * u) * lda + k);
+        for (int u = 0; u < RU; ++u)
+            a[u] = *reinterpret_cast<const float4 *>(A + (BLK ? RU * ty + u : ty + RS * u) * lda + k);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) b[kk] = *reinterpret_cast<const float4 *>(B + (k + kk) * ldb + 4 * tx);
 #pragma unroll
@@ -69,14 +73,15 @@ __device__ __forceinline__ void mm_nn(float (&acc)[RU][4], const float *A, int l
     }
 }
 
-template <int RU = 4, int RS = 16>
+template <int RU = 4, int RS = 16, bool BLK = false>
 __device__ __forceinline__ void mm_nt(float (&acc)[RU][4], const float *A, int lda, const float *B, int ldb, int K,
                                       int ty, int tx) {
 #pragma unroll 2
     for (int k = 0; k < K; k += 4) {
         float4 a[RU], b[4];
 #pragma unroll
-        for (int u = 0; u < RU; ++u) a[u] = *reinterpret_cast<const float4 *>(A + (ty + RS * u) * lda + k);
+        for (int u = 0; u < RU; ++u)
+            a[u] = *reinterpret_cast<const float4 *>(A + (BLK ? RU * ty + u : ty + RS * u) * lda + k);
 #pragma unroll
         for (int w = 0; w < 4; ++w) b[w] = *reinterpret_cast<const float4 *>(B + (tx + 16 * w) * ldb + k);
 #pragma unroll
@@ -88,16 +93,23 @@ __device__ __forceinline__ void mm_nt(float (&acc)[RU][4], const float *A, int l
     }
 }
 
-// acc[u][w] += sum_k A[k][ty + 16 u] B[k][4 tx + w]: both operands row-major
-// with the contraction along their rows (4 broadcast scalar loads and one
-// 16-byte load per 16 FMAs)
+// acc[u][w] += sum_k A[k][ty + 16 u] B[k][4 tx + w] (BLK: A[k][4 ty + u]), k
+// in [k0, K): both operands row-major with the contraction along their rows
+// (4 broadcast scalar loads, or one 16-byte load with BLK, and one 16-byte
+// load per 16 FMAs)
+template <bool BLK = false>
 __device__ __forceinline__ void mm_tn(float (&acc)[4][4], const float *A, int lda, const float *B, int ldb, int K,
-                                      int ty, int tx) {
+                                      int ty, int tx, int k0 = 0) {
 #pragma unroll 4
-    for (int k = 0; k < K; ++k) {
+    for (int k = k0; k < K; ++k) {
         float a[4];
+        if (BLK) {
+            const float4 a4 = *reinterpret_cast<const float4 *>(A + k * lda + 4 * ty);
+            a[0] = a4.x, a[1] = a4.y, a[2] = a4.z, a[3] = a4.w;
+        } else {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) a[u] = A[k * lda + ty + 16 * u];
+            for (int u = 0; u < 4; ++u) a[u] = A[k * lda + ty + 16 * u];
+        }
         const float4 b = *reinterpret_cast<const float4 *>(B + k * ldb + 4 * tx);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -521,6 +533,9 @@ constexpr int kBwdThreads = 256;   // threads of a bwd_chunk block
 //   B = Y [V | 1]^T, masked to j <= i
 //   pass 1: A += phi_q phi_k^T,  dv += phi_k R[:, :dv]; then dv += A^T dnum
 //   pass 2: dphi_q = Y S^T + B phi_k, then dphi_k = [V | 1] R^T + B^T phi_q
+// A thread owns rows 4 ty .. 4 ty + 3, so the triangular products (B phi_k,
+// B^T phi_q, A^T dnum) run only over the keys or queries on its side of the
+// diagonal.
 template <typename T, int DV>
 __global__ void __launch_bounds__(kBwdThreads, DV <= 64 ? 2 : 1) bwd_chunk(const float *__restrict__ phiq, const float *__restrict__ phik,
                                                  const T *__restrict__ v, const float *__restrict__ Sin,
@@ -582,12 +597,12 @@ __global__ void __launch_bounds__(kBwdThreads, DV <= 64 ? 2 : 1) bwd_chunk(const
     __syncthreads();
     if (causal) {
         float b[4][4] = {};
-        mm_nt(b, Ys, WP, Vs, WP, WP, ty, tx);
+        mm_nt<4, 16, true>(b, Ys, WP, Vs, WP, WP, ty, tx);
 #pragma unroll
         for (int u = 0; u < 4; ++u)
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
-                const int i = ty + 16 * u, j = tx + 16 * w;
+                const int i = 4 * ty + u, j = tx + 16 * w;
                 Bs[i * P + j] = j <= i ? b[u][w] : 0.f;
             }
     }
@@ -612,10 +627,10 @@ __global__ void __launch_bounds__(kBwdThreads, DV <= 64 ? 2 : 1) bwd_chunk(const
             }
         }
         __syncthreads();
-        if (causal) mm_nt(a, X1, P, X2, P, FT, ty, tx);
+        if (causal) mm_nt<4, 16, true>(a, X1, P, X2, P, FT, ty, tx);
 #pragma unroll
         for (int g = 0; g < NG; ++g)
-            if (64 * g + 4 * tx < DV) mm_nn(dvr[g], X2, P, Ts + 64 * g, WP, FT, ty, tx);
+            if (64 * g + 4 * tx < DV) mm_nn<4, 16, true>(dvr[g], X2, P, Ts + 64 * g, WP, FT, ty, tx);
     }
     __syncthreads();
     if (causal) {
@@ -623,7 +638,7 @@ __global__ void __launch_bounds__(kBwdThreads, DV <= 64 ? 2 : 1) bwd_chunk(const
         for (int u = 0; u < 4; ++u)
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
-                const int i = ty + 16 * u, j = tx + 16 * w;
+                const int i = 4 * ty + u, j = tx + 16 * w;
                 X1[i * P + j] = j <= i ? a[u][w] : 0.f;   // A
             }
     }
@@ -633,13 +648,13 @@ __global__ void __launch_bounds__(kBwdThreads, DV <= 64 ? 2 : 1) bwd_chunk(const
     if (causal) {
 #pragma unroll
         for (int g = 0; g < NG; ++g)
-            if (64 * g + 4 * tx < DV) mm_tn(dvr[g], X1, P, Ys + 64 * g, WP, C, ty, tx);
+            if (64 * g + 4 * tx < DV) mm_tn<true>(dvr[g], X1, P, Ys + 64 * g, WP, C, ty, tx, 4 * ty);   // i >= j
     }
 #pragma unroll
     for (int g = 0; g < NG; ++g)
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            const int j = ty + 16 * u, c = 64 * g + 4 * tx;
+            const int j = 4 * ty + u, c = 64 * g + 4 * tx;
             if (j < n && c < DV)
                 *reinterpret_cast<float4 *>(dV + (row0 + j) * DV + c) =
                     make_float4(dvr[g][u][0], dvr[g][u][1], dvr[g][u][2], dvr[g][u][3]);
@@ -653,11 +668,11 @@ __global__ void __launch_bounds__(kBwdThreads, DV <= 64 ? 2 : 1) bwd_chunk(const
         __syncthreads();
         {
             float dq[4][4] = {};
-            mm_nn(dq, Ys, WP, Ts, P, WP, ty, tx);
-            if (causal) mm_nn(dq, Bs, P, X1, P, C, ty, tx);
+            mm_nn<4, 16, true>(dq, Ys, WP, Ts, P, WP, ty, tx);
+            if (causal) mm_nn<4, 16, true>(dq, Bs, P, X1, P, 4 * ty + 4, ty, tx);   // j <= i
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const int i = ty + 16 * u, f = f0 + 4 * tx;
+                const int i = 4 * ty + u, f = f0 + 4 * tx;
                 if (i < n && f < r)
                     *reinterpret_cast<float4 *>(dphiq + (row0 + i) * r + f) =
                         make_float4(dq[u][0], dq[u][1], dq[u][2], dq[u][3]);
@@ -668,11 +683,11 @@ __global__ void __launch_bounds__(kBwdThreads, DV <= 64 ? 2 : 1) bwd_chunk(const
         __syncthreads();
         {
             float dk[4][4] = {};
-            mm_nn(dk, Vs, WP, Ts, P, WP, ty, tx);
-            if (causal) mm_tn(dk, Bs, P, X2, P, C, ty, tx);
+            mm_nn<4, 16, true>(dk, Vs, WP, Ts, P, WP, ty, tx);
+            if (causal) mm_tn<true>(dk, Bs, P, X2, P, C, ty, tx, 4 * ty);   // j >= i
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const int i = ty + 16 * u, f = f0 + 4 * tx;
+                const int i = 4 * ty + u, f = f0 + 4 * tx;
                 if (i < n && f < r)
                     *reinterpret_cast<float4 *>(dphik + (row0 + i) * r + f) =
                         make_float4(dk[u][0], dk[u][1], dk[u][2], dk[u][3]);
