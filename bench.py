@@ -434,9 +434,11 @@ BWD_ROWS = 64   # rows per chunk of the backward kernels
 
 
 def bwd_chunk_flops_per_token(w, causal):
-    """Executed FLOPs per token of the backward chunk kernel: the masked chunk
-    products A and B (causal), dphi_q and dphi_k from the carried states plus
-    the chunk sums, and dv."""
+    """Algorithmic FLOPs per token of the backward chunk kernel: the masked
+    chunk products A and B (causal, lower triangles), dphi_q and dphi_k from
+    the carried states plus the chunk sums, and dv; the dv + 1 state columns
+    without padding.  The kernel executes about 17 % more at r = 256, dv = 64
+    (full 64 x 64 A and B tiles, columns padded to dv + 4)."""
     r, dv, C = w.r, w.dv, BWD_ROWS
     intra = C / 2 if causal else 0
     ab = (C / 2) * (r + dv + 1) * 2 if causal else 0
@@ -548,7 +550,7 @@ def run_backward(args):
             "bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
             "traffic": None, "kernel": stats.dominant_kernel.decode() if stats.dominant_kernel else None,
             "kernel_ms": dom_ms, "peak_source": "derived: SMs x 128 fp32 lanes x 2 flops x max SM clock",
-            "executed_flops_per_token": bwd_chunk_flops_per_token(w, causal),
+            "algorithmic_flops_per_token": bwd_chunk_flops_per_token(w, causal),
         },
         "e2e": {"value": tokens / te, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": int(round(stats.kernel_launches / stat_steps * args.steps)),
