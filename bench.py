@@ -435,13 +435,13 @@ BWD_ROWS = 64   # rows per chunk of the backward kernels
 
 def bwd_chunk_flops_per_token(w, causal):
     """Algorithmic FLOPs per token of the backward chunk kernel: the masked
-    chunk products A and B (causal, lower triangles), dphi_q and dphi_k from
-    the carried states plus the chunk sums, and dv; the dv + 1 state columns
-    without padding.  The kernel executes about 17 % more at r = 256, dv = 64
-    (full 64 x 64 A and B tiles, columns padded to dv + 4)."""
+    chunk product B (causal, lower triangle; the masked A comes from the row
+    kernel), dphi_q and dphi_k from the carried states plus the chunk sums,
+    and dv; the dv + 1 state columns without padding.  The kernel executes
+    more (a full 64 x 64 B tile, columns padded to dv + 4)."""
     r, dv, C = w.r, w.dv, BWD_ROWS
     intra = C / 2 if causal else 0
-    ab = (C / 2) * (r + dv + 1) * 2 if causal else 0
+    ab = (C / 2) * (dv + 1) * 2 if causal else 0
     dphi = 2 * r * (dv + 1 + intra) * 2
     dvv = dv * (r + intra) * 2
     return ab + dphi + dvv

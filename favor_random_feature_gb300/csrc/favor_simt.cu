@@ -531,7 +531,7 @@ constexpr int kBwdThreads = 256;   // threads of a bwd_chunk block
 // it; block per (chunk, head), 256 threads, 64-feature tiles (two blocks per
 // SM at dv = 64):
 //   B = Y [V | 1]^T, masked to j <= i
-//   pass 1: A += phi_q phi_k^T,  dv += phi_k R[:, :dv]; then dv += A^T dnum
+//   pass 1: dv += phi_k R[:, :dv]; then dv += A^T dnum (A masked, from bwd_rows)
 //   pass 2: dphi_q = Y S^T + B phi_k, then dphi_k = [V | 1] R^T + B^T phi_q
 // A thread owns rows 4 ty .. 4 ty + 3, so the triangular products (B phi_k,
 // B^T phi_q, A^T dnum) run only over the keys or queries on its side of the
@@ -540,8 +540,9 @@ template <typename T, int DV>
 __global__ void __launch_bounds__(kBwdThreads, DV <= 64 ? 2 : 1) bwd_chunk(const float *__restrict__ phiq, const float *__restrict__ phik,
                                                  const T *__restrict__ v, const float *__restrict__ Sin,
                                                  const float *__restrict__ Rout, const float *__restrict__ Y,
-                                                 float *__restrict__ dphiq, float *__restrict__ dphik,
-                                                 float *__restrict__ dV, int L, int r, int nst, int causal) {
+                                                 const float *__restrict__ Am, float *__restrict__ dphiq,
+                                                 float *__restrict__ dphik, float *__restrict__ dV, int L, int r,
+                                                 int nst, int causal) {
     constexpr int C = kBwdRows, FT = 64, P = FT + 4, W = DV + 1, WP = DV + 4, NG = (DV + 63) / 64;
     constexpr int NT = kBwdThreads;
     static_assert(NT == 256, "the tiled products assume 256 threads");
@@ -607,10 +608,9 @@ __global__ void __launch_bounds__(kBwdThreads, DV <= 64 ? 2 : 1) bwd_chunk(const
             }
     }
     // ---- pass 1 (R tile row-major [f][WP]; its pad columns are never read)
-    float a[4][4] = {}, dvr[NG][4][4] = {};
+    float dvr[NG][4][4] = {};
     for (int f0 = 0; f0 < r; f0 += FT) {
         __syncthreads();
-        load_x(X1, phiq, f0);
         load_x(X2, phik, f0);
         {
             constexpr int NS = (FT * W + NT - 1) / NT;
@@ -627,20 +627,18 @@ __global__ void __launch_bounds__(kBwdThreads, DV <= 64 ? 2 : 1) bwd_chunk(const
             }
         }
         __syncthreads();
-        if (causal) mm_nt<4, 16, true>(a, X1, P, X2, P, FT, ty, tx);
 #pragma unroll
         for (int g = 0; g < NG; ++g)
             if (64 * g + 4 * tx < DV) mm_nn<4, 16, true>(dvr[g], X2, P, Ts + 64 * g, WP, FT, ty, tx);
     }
     __syncthreads();
-    if (causal) {
+    if (causal) {   // the masked A of this chunk, row-major
+        const float *src = Am + ((size_t)bh * nst + ch) * C * C;
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                const int i = 4 * ty + u, j = tx + 16 * w;
-                X1[i * P + j] = j <= i ? a[u][w] : 0.f;   // A
-            }
+        for (int k = 0; k < C * C / 4 / NT; ++k) {
+            const int e = tid + NT * k, i = e / (C / 4), j = 4 * (e % (C / 4));
+            *reinterpret_cast<float4 *>(X1 + i * P + j) = *reinterpret_cast<const float4 *>(src + i * C + j);
+        }
     }
     // pad rows W .. WP - 1 of the transposed state tiles stay zero through pass 2
     for (int e = tid; e < (WP - W) * P; e += NT) Ts[W * P + e] = 0.f;
@@ -954,14 +952,15 @@ __global__ void state_sum(float *__restrict__ S, int nch, int nz, size_t per, in
 
 // per row of a chunk: num, den from the entering state (+ the masked chunk
 // sum), out = num / den, then dnum = g / den and dden = -(g . out) / den into
-// Y [rows][dv + 1].  Block per (chunk, head), 256 threads, 64-feature tiles
-// read a tile ahead into registers (as bwd_chunk):
+// Y [rows][dv + 1] (and, causal, the masked A of the chunk into Am
+// [BH][chunks][64][64] for bwd_chunk).  Block per (chunk, head), 256 threads,
+// 64-feature tiles read a tile ahead into registers:
 //   num = phi_q S[:, :dv] (+ A_m V),  den = phi_q z (+ A_m 1),  A_m = (phi_q phi_k^T) masked to j <= i
 template <typename T, int DV>
 __global__ void __launch_bounds__(256, 2) bwd_rows(const float *__restrict__ phiq, const float *__restrict__ phik,
                                                 const T *__restrict__ v, const float *__restrict__ Sin,
-                                                const float *__restrict__ g, float *__restrict__ Y, int L, int r,
-                                                int nst, int causal) {
+                                                const float *__restrict__ g, float *__restrict__ Y,
+                                                float *__restrict__ Am, int L, int r, int nst, int causal) {
     constexpr int C = kBwdRows, FT = 64, P = FT + 4, W = DV + 1, WP = DV + 4, NG = (DV + 63) / 64, NT = 256;
     extern __shared__ float4 sm4[];
     float *Qt = reinterpret_cast<float *>(sm4);   // [C][P]   phi_q tile
@@ -1034,6 +1033,7 @@ __global__ void __launch_bounds__(256, 2) bwd_rows(const float *__restrict__ phi
                 const int i = ty + 16 * u, j = tx + 16 * w;
                 const float x = j <= i ? a[u][w] : 0.f;
                 Kt[i * P + j] = x;
+                Am[(((size_t)bh * nst + ch) * C + i) * C + j] = x;   // for bwd_chunk
                 den[u] += x;
             }
         __syncthreads();
@@ -1170,7 +1170,8 @@ int backward_dv(const T *q, const T *k, const T *v, const float *omega, const fl
     const size_t per = (size_t)p.r * (DV + 1);
     size_t bytes = 2 * carve_bytes<float>(rows * p.nproj) + 4 * carve_bytes<float>(rows * p.r) +
                    2 * carve_bytes<float>(rows) + carve_bytes<float>(p.BH) +
-                   2 * carve_bytes<float>((size_t)p.BH * nch * per) + carve_bytes<float>(rows * (DV + 1));
+                   2 * carve_bytes<float>((size_t)p.BH * nch * per) + carve_bytes<float>(rows * (DV + 1)) +
+                   (p.causal ? carve_bytes<float>((size_t)p.BH * nch * kBwdRows * kBwdRows) : 0);
     int status = FAVOR_OK;
     void *ws = workspace(bytes, &status);
     if (!ws) return status;
@@ -1182,6 +1183,8 @@ int backward_dv(const T *q, const T *k, const T *v, const float *omega, const fl
     float *hmax = cv.take<float>(p.BH);
     float *S = cv.take<float>((size_t)p.BH * nch * per), *R = cv.take<float>((size_t)p.BH * nch * per);
     float *Y = cv.take<float>(rows * (DV + 1));
+    // the masked chunk matrices A (causal), formed by bwd_rows and read by bwd_chunk
+    float *Am = p.causal ? cv.take<float>((size_t)p.BH * nch * kBwdRows * kBwdRows) : nullptr;
 
     int rc;
     if ((rc = features_into<T>(q, omega, Pq, phiq, lsq, p, st)) || (rc = features_into<T>(k, omega, Pk, phik, lsk, p, st)))
@@ -1213,7 +1216,7 @@ int backward_dv(const T *q, const T *k, const T *v, const float *omega, const fl
             cudaGetLastError();
             return FAVOR_ERR_CUDA;
         }
-        bwd_rows<T, DV><<<cg, 256, smem, st>>>(phiq, phik, v, S, g, Y, p.L, p.r, nch, p.causal);
+        bwd_rows<T, DV><<<cg, 256, smem, st>>>(phiq, phik, v, S, g, Y, Am, p.L, p.r, nch, p.causal);
         FAVOR_LAUNCH_CHECK();
     }
     // the states leaving each chunk (causal: exclusive suffix) or the total
@@ -1228,7 +1231,8 @@ int backward_dv(const T *q, const T *k, const T *v, const float *omega, const fl
             return FAVOR_ERR_CUDA;
         }
         stats_begin(st, "bwd_chunk");
-        bwd_chunk<T, DV><<<cg, kBwdThreads, smem, st>>>(phiq, phik, v, S, R, Y, dphiq, dphik, dv, p.L, p.r, nch, p.causal);
+        bwd_chunk<T, DV><<<cg, kBwdThreads, smem, st>>>(phiq, phik, v, S, R, Y, Am, dphiq, dphik, dv, p.L, p.r, nch,
+                                                          p.causal);
         stats_end(st);
         FAVOR_LAUNCH_CHECK();
     }
