@@ -33,6 +33,14 @@ __device__ __forceinline__ float load_in(const float *p, size_t i) { return p[i]
 __device__ __forceinline__ float load_in(const uint16_t *p, size_t i) {
     return __uint_as_float(static_cast<uint32_t>(p[i]) << 16);
 }
+// an input element's bits, converted later (a prefetch that converts at once
+// waits for its load there)
+__device__ __forceinline__ uint32_t load_raw(const float *p, size_t i) { return __float_as_uint(p[i]); }
+__device__ __forceinline__ uint32_t load_raw(const uint16_t *p, size_t i) { return p[i]; }
+template <typename T>
+__device__ __forceinline__ float from_raw(uint32_t b) {
+    return sizeof(T) == 4 ? __uint_as_float(b) : __uint_as_float(b << 16);
+}
 __device__ __forceinline__ void store_out(float *p, size_t i, float v) { p[i] = v; }
 __device__ __forceinline__ void store_out(__nv_bfloat16 *p, size_t i, float v) { p[i] = __float2bfloat16_rn(v); }
 
@@ -770,20 +778,20 @@ __global__ void __launch_bounds__(256) bwd_dx(float *__restrict__ C, const float
         }
     }
     const float *w = omega + (size_t)h * nproj * D;
-    float4 xc[NX], xw[NW];
+    // staged a tile ahead: the coefficients (other maps) or dphi and phi
+    // (positive map, multiplied when the tile is put in shared memory)
+    float4 xc[NX], xf[NX], xw[NW];
     auto fetch = [&](int p0) {
         const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < NX; ++k) {
             const int e = tid + NT * k, i = e / (PT / 4), pp = 4 * (e % (PT / 4));
-            xc[k] = z;
+            xc[k] = xf[k] = z;
             if (i < n && p0 + pp < nproj) {   // nproj % 4 == 0
                 const size_t o = (row0 + i) * nproj + p0 + pp;
                 if (pos) {   // positive map: r == nproj
-                    const float4 g = *reinterpret_cast<const float4 *>(dphi + o),
-                                 f = *reinterpret_cast<const float4 *>(phi + o);
-                    xc[k] = make_float4(g.x * f.x, g.y * f.y, g.z * f.z, g.w * f.w);
-                    *reinterpret_cast<float4 *>(C + o) = xc[k];
+                    xc[k] = *reinterpret_cast<const float4 *>(dphi + o);
+                    xf[k] = *reinterpret_cast<const float4 *>(phi + o);
                 } else {
                     xc[k] = *reinterpret_cast<const float4 *>(C + o);
                 }
@@ -803,7 +811,13 @@ __global__ void __launch_bounds__(256) bwd_dx(float *__restrict__ C, const float
 #pragma unroll
         for (int k = 0; k < NX; ++k) {
             const int e = tid + NT * k, i = e / (PT / 4), pp = 4 * (e % (PT / 4));
-            *reinterpret_cast<float4 *>(Cs + i * P + pp) = xc[k];
+            float4 cv = xc[k];
+            if (pos) {
+                cv = make_float4(cv.x * xf[k].x, cv.y * xf[k].y, cv.z * xf[k].z, cv.w * xf[k].w);
+                if (i < n && p0 + pp < nproj)
+                    *reinterpret_cast<float4 *>(C + (row0 + i) * nproj + p0 + pp) = cv;   // for the omega gradient
+            }
+            *reinterpret_cast<float4 *>(Cs + i * P + pp) = cv;
         }
 #pragma unroll
         for (int k = 0; k < NW; ++k) {
@@ -856,7 +870,7 @@ __global__ void __launch_bounds__(256) bwd_dx(float *__restrict__ C, const float
 // 4 tx + w (+ 64 per group) of the running state; the last column (sum of
 // phi, or of phi dden) from per-thread row partials summed over tx.
 template <typename T, int DV>
-__global__ void __launch_bounds__(256, 2) state_scan(const float *__restrict__ phi, const T *__restrict__ v,
+__global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) state_scan(const float *__restrict__ phi, const T *__restrict__ v,
                                                      const float *__restrict__ Y, float *__restrict__ S, int L,
                                                      int r, int nch, int causal, int reverse) {
     constexpr int C = kBwdRows, FT = 64, P = FT + 4, W = DV + 1, WP = DV + 4, NG = (DV + 63) / 64, NT = 256;
@@ -867,7 +881,7 @@ __global__ void __launch_bounds__(256, 2) state_scan(const float *__restrict__ p
     const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
     const int f0 = blockIdx.x * FT, bh = blockIdx.y;
     float4 xp[NX];
-    float xy[NY];
+    uint32_t xy[NY];   // Yc bits (v converted when put in shared memory)
     auto fetch = [&](int ch) {
         const int t0 = ch * C, n = min(C, L - t0);
         const size_t row0 = (size_t)bh * L + t0;
@@ -880,10 +894,17 @@ __global__ void __launch_bounds__(256, 2) state_scan(const float *__restrict__ p
 #pragma unroll
         for (int k = 0; k < NY; ++k) {
             const int e = tid + NT * k, i = e / W, c = e % W;
-            float y = 0.f;
-            if (e < C * W && i < n) y = Y ? Y[(row0 + i) * W + c] : (c < DV ? load_in(v, (row0 + i) * DV + c) : 1.f);
+            uint32_t y = 0u;   // rows past the end: 0 (and the v | 1 rows' 1 only for valid rows)
+            if (e < C * W && i < n)
+                y = Y ? __float_as_uint(Y[(row0 + i) * W + c]) : (c < DV ? load_raw(v, (row0 + i) * DV + c) : 1u);
             xy[k] = y;
         }
+    };
+    // the staged bits as values: Y as is; v converted, the ones column (bits 1) as 1
+    auto y_of = [&](int e, uint32_t b) -> float {
+        if (Y) return __uint_as_float(b);
+        if (e % W == DV) return b ? 1.f : 0.f;
+        return from_raw<T>(b);
     };
     for (int e = tid; e < C * WP; e += NT) Ys[e] = 0.f;   // pad columns stay zero
     float acc[NG][4][4] = {}, zp[4] = {};
@@ -921,7 +942,7 @@ __global__ void __launch_bounds__(256, 2) state_scan(const float *__restrict__ p
 #pragma unroll
         for (int k = 0; k < NY; ++k) {
             const int e = tid + NT * k;
-            if (e < C * W) Ys[(e / W) * WP + e % W] = xy[k];
+            if (e < C * W) Ys[(e / W) * WP + e % W] = y_of(e, xy[k]);
         }
         __syncthreads();
         if (it + 1 < c_n) fetch(reverse ? ch - 1 : ch + 1);
@@ -957,7 +978,7 @@ __global__ void state_sum(float *__restrict__ S, int nch, int nz, size_t per, in
 // 64-feature tiles read a tile ahead into registers:
 //   num = phi_q S[:, :dv] (+ A_m V),  den = phi_q z (+ A_m 1),  A_m = (phi_q phi_k^T) masked to j <= i
 template <typename T, int DV>
-__global__ void __launch_bounds__(256, 2) bwd_rows(const float *__restrict__ phiq, const float *__restrict__ phik,
+__global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) bwd_rows(const float *__restrict__ phiq, const float *__restrict__ phik,
                                                 const T *__restrict__ v, const float *__restrict__ Sin,
                                                 const float *__restrict__ g, float *__restrict__ Y,
                                                 float *__restrict__ Am, int L, int r, int nst, int causal) {
@@ -1090,7 +1111,8 @@ __global__ void __launch_bounds__(256) bwd_dw(const float *__restrict__ Cq, cons
     float *Xs = Cs + RS * P;                      // [RS][DP] input rows
     const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
     const int p0 = blockIdx.x * PT, h = blockIdx.z;
-    float4 rc[NC], rx[NXD];
+    float4 rc[NC];
+    uint32_t rx[NXD][4];   // input bits, converted when put in shared memory
     auto fetch = [&](int it) {   // sub-slice it / 2 of side it % 2
         const int side = it & 1, r0 = (blockIdx.y * SUB + (it >> 1)) * RS;
         const float *Cm = side ? Ck : Cq;
@@ -1108,11 +1130,12 @@ __global__ void __launch_bounds__(256) bwd_dw(const float *__restrict__ Cq, cons
 #pragma unroll
         for (int kk = 0; kk < NXD; ++kk) {
             const int e = tid + NT * kk, i = e / (D / 4), j = 4 * (e % (D / 4)), t = r0 + i;
-            rx[kk] = z;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) rx[kk][c] = 0u;
             if (e < RS * D / 4 && t < B * L) {
                 const size_t row = ((size_t)(t / L) * H + h) * L + t % L;
-                rx[kk] = make_float4(load_in(X, row * D + j), load_in(X, row * D + j + 1), load_in(X, row * D + j + 2),
-                                     load_in(X, row * D + j + 3));
+#pragma unroll
+                for (int c = 0; c < 4; ++c) rx[kk][c] = load_raw(X, row * D + j + c);
             }
         }
     };
@@ -1128,7 +1151,9 @@ __global__ void __launch_bounds__(256) bwd_dw(const float *__restrict__ Cq, cons
 #pragma unroll
         for (int kk = 0; kk < NXD; ++kk) {
             const int e = tid + NT * kk, i = e / (D / 4), j = 4 * (e % (D / 4));
-            if (e < RS * D / 4) *reinterpret_cast<float4 *>(Xs + i * DP + j) = rx[kk];
+            if (e < RS * D / 4)
+                *reinterpret_cast<float4 *>(Xs + i * DP + j) = make_float4(
+                    from_raw<T>(rx[kk][0]), from_raw<T>(rx[kk][1]), from_raw<T>(rx[kk][2]), from_raw<T>(rx[kk][3]));
         }
         __syncthreads();
         if (it + 1 < 2 * SUB) fetch(it + 1);
