@@ -867,8 +867,8 @@ __global__ void __launch_bounds__(256) bwd_dx(float *__restrict__ C, const float
 // tile, head, range), 256 threads, the chunks in order (a fixed
 // summation order), the next chunk's rows read into registers while the
 // current one is added; thread (ty, tx) owns features ty + 16 u and columns
-// 4 tx + w (+ 64 per group) of the running state; the last column (sum of
-// phi, or of phi dden) from per-thread row partials summed over tx.
+// 4 tx + w (+ 64 per group) of the running state, and every thread the last
+// column (sum of phi, or of phi dden) of its features.
 template <typename T, int DV>
 __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) state_scan(const float *__restrict__ phi, const T *__restrict__ v,
                                                      const float *__restrict__ Y, float *__restrict__ S, int L,
@@ -907,14 +907,12 @@ __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) state_scan(const float 
         return from_raw<T>(b);
     };
     for (int e = tid; e < C * WP; e += NT) Ys[e] = 0.f;   // pad columns stay zero
-    float acc[NG][4][4] = {}, zp[4] = {};
+    float acc[NG][4][4] = {}, zc[4] = {};   // zc: the last column (every tx holds it)
     auto write_state = [&](int slot) {
         float *dst = S + ((size_t)bh * nch + slot) * r * W;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            float z = zp[u];
-#pragma unroll
-            for (int o = 8; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+            const float z = zc[u];
             const int f = f0 + ty + 16 * u;
             if (f >= r) continue;
 #pragma unroll
@@ -947,16 +945,29 @@ __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) state_scan(const float 
         __syncthreads();
         if (it + 1 < c_n) fetch(reverse ? ch - 1 : ch + 1);
         if (causal) write_state(ch);   // exclusive: before this chunk is added
+        // acc[g][u][w] += sum_i phi[i][ty + 16 u] Yc[i][64 g + 4 tx + w] and the last
+        // column in the same pass over the rows (one more broadcast load per row)
+#pragma unroll 4
+        for (int i = 0; i < C; ++i) {
+            float av[4];
 #pragma unroll
-        for (int gi = 0; gi < NG; ++gi)
-            if (64 * gi + 4 * tx < DV) mm_tn(acc[gi], Ps, P, Ys + 64 * gi, WP, C, ty, tx);
+            for (int u = 0; u < 4; ++u) av[u] = Ps[i * P + ty + 16 * u];
+            const float yz = Ys[i * WP + DV];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
+            for (int gi = 0; gi < NG; ++gi) {
+                if (64 * gi + 4 * tx >= DV) continue;
+                const float4 bv = *reinterpret_cast<const float4 *>(Ys + i * WP + 64 * gi + 4 * tx);
 #pragma unroll
-            for (int ii = 0; ii < C / 16; ++ii) {
-                const int i = tx + 16 * ii;
-                zp[u] = fmaf(Ps[i * P + ty + 16 * u], Ys[i * WP + DV], zp[u]);
+                for (int u = 0; u < 4; ++u) {
+                    acc[gi][u][0] = fmaf(av[u], bv.x, acc[gi][u][0]);
+                    acc[gi][u][1] = fmaf(av[u], bv.y, acc[gi][u][1]);
+                    acc[gi][u][2] = fmaf(av[u], bv.z, acc[gi][u][2]);
+                    acc[gi][u][3] = fmaf(av[u], bv.w, acc[gi][u][3]);
+                }
             }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) zc[u] = fmaf(av[u], yz, zc[u]);
+        }
     }
     if (!causal) write_state(blockIdx.z);
 }
