@@ -564,7 +564,7 @@ __global__ void __launch_bounds__(kBwdThreads, DV <= 64 ? 2 : 1) bwd_chunk(const
     const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
     const int ch = blockIdx.x, bh = blockIdx.y, t0 = ch * C, n = min(C, L - t0);
     const size_t row0 = (size_t)bh * L + t0;
-    const size_t st = ((size_t)bh * nst + (causal ? ch : 0)) * r * W;
+    const size_t st = ((size_t)bh * nst + (causal ? ch : 0)) * r * WP;
     const float *S = Sin + st, *R = Rout + st;
 #pragma unroll 4
     for (int e = tid; e < C * WP; e += NT) {
@@ -588,19 +588,28 @@ __global__ void __launch_bounds__(kBwdThreads, DV <= 64 ? 2 : 1) bwd_chunk(const
             *reinterpret_cast<float4 *>(dst + i * P + f) = t[k];
         }
     };
-    // state rows f0 .. f0 + 63 (all W columns) transposed into [WP][P]
-    auto load_st = [&](const float *src, int f0) {
-        constexpr int NS = (FT * W + NT - 1) / NT;
-        float t[NS];
+    // state rows f0 .. f0 + 63 (pitch WP, 16 bytes at a time) transposed into [WP][P]
+    constexpr int NS = (FT * WP / 4 + NT - 1) / NT;
+    auto fetch_st = [&](const float *src, int f0, float4(&t)[NS]) {
 #pragma unroll
         for (int k = 0; k < NS; ++k) {
-            const int e = tid + NT * k, f = e / W, c = e % W;
-            t[k] = (e < FT * W && f0 + f < r) ? src[(size_t)(f0 + f) * W + c] : 0.f;
+            const int e = tid + NT * k, f = e / (WP / 4), c = 4 * (e % (WP / 4));
+            t[k] = (e < FT * WP / 4 && f0 + f < r) ? *reinterpret_cast<const float4 *>(src + (size_t)(f0 + f) * WP + c)
+                                                    : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+    };
+    auto load_st = [&](const float *src, int f0) {
+        float4 t[NS];
+        fetch_st(src, f0, t);
 #pragma unroll
         for (int k = 0; k < NS; ++k) {
-            const int e = tid + NT * k;
-            if (e < FT * W) Ts[(e % W) * P + e / W] = t[k];
+            const int e = tid + NT * k, f = e / (WP / 4), c = 4 * (e % (WP / 4));
+            if (e < FT * WP / 4) {
+                Ts[(c + 0) * P + f] = t[k].x;
+                Ts[(c + 1) * P + f] = t[k].y;
+                Ts[(c + 2) * P + f] = t[k].z;
+                Ts[(c + 3) * P + f] = t[k].w;
+            }
         }
     };
     __syncthreads();
@@ -621,17 +630,12 @@ __global__ void __launch_bounds__(kBwdThreads, DV <= 64 ? 2 : 1) bwd_chunk(const
         __syncthreads();
         load_x(X2, phik, f0);
         {
-            constexpr int NS = (FT * W + NT - 1) / NT;
-            float t[NS];
-#pragma unroll
-            for (int k = 0; k < NS; ++k) {
-                const int e = tid + NT * k, f = e / W, c = e % W;
-                t[k] = (e < FT * W && f0 + f < r) ? R[(size_t)(f0 + f) * W + c] : 0.f;
-            }
+            float4 t[NS];
+            fetch_st(R, f0, t);
 #pragma unroll
             for (int k = 0; k < NS; ++k) {
                 const int e = tid + NT * k;
-                if (e < FT * W) Ts[(e / W) * WP + e % W] = t[k];
+                if (e < FT * WP / 4) *reinterpret_cast<float4 *>(Ts + 4 * e) = t[k];   // [FT][WP], same pitch
             }
         }
         __syncthreads();
@@ -909,7 +913,7 @@ __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) state_scan(const float 
     for (int e = tid; e < C * WP; e += NT) Ys[e] = 0.f;   // pad columns stay zero
     float acc[NG][4][4] = {}, zc[4] = {};   // zc: the last column (every tx holds it)
     auto write_state = [&](int slot) {
-        float *dst = S + ((size_t)bh * nch + slot) * r * W;
+        float *dst = S + ((size_t)bh * nch + slot) * r * WP;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const float z = zc[u];
@@ -918,12 +922,11 @@ __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) state_scan(const float 
 #pragma unroll
             for (int gi = 0; gi < NG; ++gi) {
                 const int c = 64 * gi + 4 * tx;
-                if (c < DV) {
-#pragma unroll
-                    for (int w = 0; w < 4; ++w) dst[(size_t)f * W + c + w] = acc[gi][u][w];
-                }
+                if (c < DV)
+                    *reinterpret_cast<float4 *>(dst + (size_t)f * WP + c) =
+                        make_float4(acc[gi][u][0], acc[gi][u][1], acc[gi][u][2], acc[gi][u][3]);
             }
-            if (tx == 0) dst[(size_t)f * W + DV] = z;
+            if (tx == 0) *reinterpret_cast<float4 *>(dst + (size_t)f * WP + DV) = make_float4(z, 0.f, 0.f, 0.f);
         }
     };
     // this block's chunks: all (causal) or the z-th range (non-causal)
@@ -1002,15 +1005,14 @@ __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) bwd_rows(const float *_
     const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
     const int ch = blockIdx.x, bh = blockIdx.y, t0 = ch * C, n = min(C, L - t0);
     const size_t row0 = (size_t)bh * L + t0;
-    const float *S = Sin + ((size_t)bh * nst + (causal ? ch : 0)) * r * W;
+    const float *S = Sin + ((size_t)bh * nst + (causal ? ch : 0)) * r * WP;
 #pragma unroll 4
     for (int e = tid; e < C * WP; e += NT) {
         const int i = e / WP, c = e % WP;
         Vs[e] = (i < n && c < W) ? (c < DV ? load_in(v, (row0 + i) * DV + c) : 1.f) : 0.f;
     }
-    constexpr int NX = C * FT / 4 / NT, NS = (FT * W + NT - 1) / NT;
-    float4 xq[NX], xk[NX];
-    float xs[NS];
+    constexpr int NX = C * FT / 4 / NT, NS = (FT * WP / 4 + NT - 1) / NT;
+    float4 xq[NX], xk[NX], xs[NS];
     auto fetch = [&](int f0) {
 #pragma unroll
         for (int k = 0; k < NX; ++k) {
@@ -1021,9 +1023,10 @@ __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) bwd_rows(const float *_
             xk[k] = (ok && causal) ? *reinterpret_cast<const float4 *>(phik + (row0 + i) * r + f0 + f) : z;
         }
 #pragma unroll
-        for (int k = 0; k < NS; ++k) {
-            const int e = tid + NT * k, f = e / W, c = e % W;
-            xs[k] = (e < FT * W && f0 + f < r) ? S[(size_t)(f0 + f) * W + c] : 0.f;
+        for (int k = 0; k < NS; ++k) {   // state rows f0 .. f0 + 63, 16 bytes at a time
+            const int e = tid + NT * k, f = e / (WP / 4), c = 4 * (e % (WP / 4));
+            xs[k] = (e < FT * WP / 4 && f0 + f < r) ? *reinterpret_cast<const float4 *>(S + (size_t)(f0 + f) * WP + c)
+                                                     : make_float4(0.f, 0.f, 0.f, 0.f);
         }
     };
     float a[4][4] = {}, num[NG][4][4] = {}, den[4] = {};
@@ -1039,7 +1042,7 @@ __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) bwd_rows(const float *_
 #pragma unroll
         for (int k = 0; k < NS; ++k) {
             const int e = tid + NT * k;
-            if (e < FT * W) Ss[(e / W) * WP + e % W] = xs[k];
+            if (e < FT * WP / 4) *reinterpret_cast<float4 *>(Ss + 4 * e) = xs[k];   // [FT][WP], same pitch
         }
         __syncthreads();
         if (f0 + FT < r) fetch(f0 + FT);
@@ -1203,7 +1206,7 @@ int backward_dv(const T *q, const T *k, const T *v, const float *omega, const fl
                 float *dv, float *dw, const Problem &p, cudaStream_t st) {
     const size_t rows = (size_t)p.BH * p.L;
     const int nch = (p.L + kBwdRows - 1) / kBwdRows;     // chunks of 64 rows, both modes
-    const size_t per = (size_t)p.r * (DV + 1);
+    const size_t per = (size_t)p.r * (DV + 4);   // chunk states [r][dv + 4]: dv values, z, 3 zero columns
     size_t bytes = 2 * carve_bytes<float>(rows * p.nproj) + 4 * carve_bytes<float>(rows * p.r) +
                    2 * carve_bytes<float>(rows) + carve_bytes<float>(p.BH) +
                    2 * carve_bytes<float>((size_t)p.BH * nch * per) + carve_bytes<float>(rows * (DV + 1)) +
