@@ -567,11 +567,15 @@ __global__ void __launch_bounds__(kBwdThreads, DV <= 64 ? 2 : 1) bwd_chunk(const
     const size_t st = ((size_t)bh * nst + (causal ? ch : 0)) * r * WP;
     const float *S = Sin + st, *R = Rout + st;
 #pragma unroll 4
+    for (int e = tid; e < C * WP / 4; e += NT) {   // Y rows have the same pitch (zero pad columns)
+        const int i = e / (WP / 4), c = 4 * (e % (WP / 4));
+        *reinterpret_cast<float4 *>(Ys + 4 * e) =
+            i < n ? *reinterpret_cast<const float4 *>(Y + (row0 + i) * WP + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll 4
     for (int e = tid; e < C * WP; e += NT) {
         const int i = e / WP, c = e % WP;
-        const bool ok = i < n && c < W;
-        Ys[e] = ok ? Y[(row0 + i) * W + c] : 0.f;
-        Vs[e] = ok ? (c < DV ? load_in(v, (row0 + i) * DV + c) : 1.f) : 0.f;
+        Vs[e] = (i < n && c < W) ? (c < DV ? load_in(v, (row0 + i) * DV + c) : 1.f) : 0.f;
     }
     // rows x 64 features of phi (phiq or phik) into a [C][P] tile
     auto load_x = [&](float *dst, const float *src, int f0) {
@@ -873,7 +877,7 @@ __global__ void __launch_bounds__(256) bwd_dx(float *__restrict__ C, const float
 // current one is added; thread (ty, tx) owns features ty + 16 u and columns
 // 4 tx + w (+ 64 per group) of the running state, and every thread the last
 // column (sum of phi, or of phi dden) of its features.
-template <typename T, int DV>
+template <typename T, int DV, bool YIN>
 __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) state_scan(const float *__restrict__ phi, const T *__restrict__ v,
                                                      const float *__restrict__ Y, float *__restrict__ S, int L,
                                                      int r, int nch, int causal, int reverse) {
@@ -884,8 +888,9 @@ __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) state_scan(const float 
     float *Ys = Ps + C * P;                       // [C][WP] Yc | 0
     const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
     const int f0 = blockIdx.x * FT, bh = blockIdx.y;
-    float4 xp[NX];
-    uint32_t xy[NY];   // Yc bits (v converted when put in shared memory)
+    constexpr int NY4 = (C * WP / 4 + NT - 1) / NT;
+    float4 xp[NX], xy4[YIN ? NY4 : 1];   // Y rows (pitch WP), 16 bytes at a time
+    uint32_t xy[YIN ? 1 : NY];           // v bits (converted when put in shared memory)
     auto fetch = [&](int ch) {
         const int t0 = ch * C, n = min(C, L - t0);
         const size_t row0 = (size_t)bh * L + t0;
@@ -895,18 +900,25 @@ __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) state_scan(const float 
             xp[k] = (i < n && f0 + f < r) ? *reinterpret_cast<const float4 *>(phi + (row0 + i) * r + f0 + f)
                                           : make_float4(0.f, 0.f, 0.f, 0.f);   // r % 4 == 0
         }
+        if constexpr (YIN) {
 #pragma unroll
-        for (int k = 0; k < NY; ++k) {
-            const int e = tid + NT * k, i = e / W, c = e % W;
-            uint32_t y = 0u;   // rows past the end: 0 (and the v | 1 rows' 1 only for valid rows)
-            if (e < C * W && i < n)
-                y = Y ? __float_as_uint(Y[(row0 + i) * W + c]) : (c < DV ? load_raw(v, (row0 + i) * DV + c) : 1u);
-            xy[k] = y;
+            for (int k = 0; k < NY4; ++k) {
+                const int e = tid + NT * k, i = e / (WP / 4), c = 4 * (e % (WP / 4));
+                xy4[k] = (e < C * WP / 4 && i < n) ? *reinterpret_cast<const float4 *>(Y + (row0 + i) * WP + c)
+                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < NY; ++k) {
+                const int e = tid + NT * k, i = e / W, c = e % W;
+                uint32_t y = 0u;   // rows past the end: 0 (and the v | 1 rows' 1 only for valid rows)
+                if (e < C * W && i < n) y = c < DV ? load_raw(v, (row0 + i) * DV + c) : 1u;
+                xy[k] = y;
+            }
         }
     };
-    // the staged bits as values: Y as is; v converted, the ones column (bits 1) as 1
+    // the staged v bits as values, the ones column (bits 1) as 1
     auto y_of = [&](int e, uint32_t b) -> float {
-        if (Y) return __uint_as_float(b);
         if (e % W == DV) return b ? 1.f : 0.f;
         return from_raw<T>(b);
     };
@@ -940,10 +952,18 @@ __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) state_scan(const float 
             const int e = tid + NT * k, i = e / (FT / 4), f = 4 * (e % (FT / 4));
             *reinterpret_cast<float4 *>(Ps + i * P + f) = xp[k];
         }
+        if constexpr (YIN) {
 #pragma unroll
-        for (int k = 0; k < NY; ++k) {
-            const int e = tid + NT * k;
-            if (e < C * W) Ys[(e / W) * WP + e % W] = y_of(e, xy[k]);
+            for (int k = 0; k < NY4; ++k) {
+                const int e = tid + NT * k;
+                if (e < C * WP / 4) *reinterpret_cast<float4 *>(Ys + 4 * e) = xy4[k];
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < NY; ++k) {
+                const int e = tid + NT * k;
+                if (e < C * W) Ys[(e / W) * WP + e % W] = y_of(e, xy[k]);
+            }
         }
         __syncthreads();
         if (it + 1 < c_n) fetch(reverse ? ch - 1 : ch + 1);
@@ -987,7 +1007,7 @@ __global__ void state_sum(float *__restrict__ S, int nch, int nz, size_t per, in
 
 // per row of a chunk: num, den from the entering state (+ the masked chunk
 // sum), out = num / den, then dnum = g / den and dden = -(g . out) / den into
-// Y [rows][dv + 1] (and, causal, the masked A of the chunk into Am
+// Y [rows][dv + 4] (3 zero columns; and, causal, the masked A of the chunk into Am
 // [BH][chunks][64][64] for bwd_chunk).  Block per (chunk, head), 256 threads,
 // 64-feature tiles read a tile ahead into registers:
 //   num = phi_q S[:, :dv] (+ A_m V),  den = phi_q z (+ A_m 1),  A_m = (phi_q phi_k^T) masked to j <= i
@@ -1101,11 +1121,11 @@ __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) bwd_rows(const float *_
         for (int c = lane; c < DV; c += 32) {
             const float gi = g[(row0 + i) * DV + c];
             gdo = fmaf(gi, NUM[i * WP + c] / dn, gdo);
-            Y[(row0 + i) * W + c] = gi / dn;
+            Y[(row0 + i) * WP + c] = gi / dn;
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) gdo += __shfl_xor_sync(0xffffffffu, gdo, o);
-        if (lane == 0) Y[(row0 + i) * W + DV] = -gdo / dn;
+        if (lane == 0) *reinterpret_cast<float4 *>(Y + (row0 + i) * WP + DV) = make_float4(-gdo / dn, 0.f, 0.f, 0.f);
     }
 }
 
@@ -1209,7 +1229,7 @@ int backward_dv(const T *q, const T *k, const T *v, const float *omega, const fl
     const size_t per = (size_t)p.r * (DV + 4);   // chunk states [r][dv + 4]: dv values, z, 3 zero columns
     size_t bytes = 2 * carve_bytes<float>(rows * p.nproj) + 4 * carve_bytes<float>(rows * p.r) +
                    2 * carve_bytes<float>(rows) + carve_bytes<float>(p.BH) +
-                   2 * carve_bytes<float>((size_t)p.BH * nch * per) + carve_bytes<float>(rows * (DV + 1)) +
+                   2 * carve_bytes<float>((size_t)p.BH * nch * per) + carve_bytes<float>(rows * (DV + 4)) +
                    (p.causal ? carve_bytes<float>((size_t)p.BH * nch * kBwdRows * kBwdRows) : 0);
     int status = FAVOR_OK;
     void *ws = workspace(bytes, &status);
@@ -1221,7 +1241,7 @@ int backward_dv(const T *q, const T *k, const T *v, const float *omega, const fl
     float *lsq = cv.take<float>(rows), *lsk = cv.take<float>(rows);
     float *hmax = cv.take<float>(p.BH);
     float *S = cv.take<float>((size_t)p.BH * nch * per), *R = cv.take<float>((size_t)p.BH * nch * per);
-    float *Y = cv.take<float>(rows * (DV + 1));
+    float *Y = cv.take<float>(rows * (DV + 4));   // [rows][dv + 4]: dnum | dden | 3 zero columns
     // the masked chunk matrices A (causal), formed by bwd_rows and read by bwd_chunk
     float *Am = p.causal ? cv.take<float>((size_t)p.BH * nch * kBwdRows * kBwdRows) : nullptr;
 
@@ -1239,13 +1259,15 @@ int backward_dv(const T *q, const T *k, const T *v, const float *omega, const fl
     const dim3 cg(nch, p.BH), sg2((p.r + 63) / 64, p.BH, nz);
     const unsigned sb = (unsigned)((per * p.BH + 255) / 256);
     const size_t st_smem = state_tile_smem<DV>();
-    if (cudaFuncSetAttribute(state_scan<T, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st_smem) !=
-        cudaSuccess) {
+    if (cudaFuncSetAttribute(state_scan<T, DV, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st_smem) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(state_scan<T, DV, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st_smem) !=
+            cudaSuccess) {
         cudaGetLastError();
         return FAVOR_ERR_CUDA;
     }
     // the forward states entering each chunk (causal: exclusive prefix) or the total (chunk slot 0)
-    state_scan<T, DV><<<sg2, 256, st_smem, st>>>(phik, v, nullptr, S, p.L, p.r, nch, p.causal, 0);
+    state_scan<T, DV, false><<<sg2, 256, st_smem, st>>>(phik, v, nullptr, S, p.L, p.r, nch, p.causal, 0);
     if (nz > 1) state_sum<<<sb, 256, 0, st>>>(S, nch, nz, per, p.BH);
     FAVOR_LAUNCH_CHECK();
     {
@@ -1259,7 +1281,7 @@ int backward_dv(const T *q, const T *k, const T *v, const float *omega, const fl
         FAVOR_LAUNCH_CHECK();
     }
     // the states leaving each chunk (causal: exclusive suffix) or the total
-    state_scan<T, DV><<<sg2, 256, st_smem, st>>>(phiq, v, Y, R, p.L, p.r, nch, p.causal, 1);
+    state_scan<T, DV, true><<<sg2, 256, st_smem, st>>>(phiq, v, Y, R, p.L, p.r, nch, p.causal, 1);
     if (nz > 1) state_sum<<<sb, 256, 0, st>>>(R, nch, nz, per, p.BH);
     FAVOR_LAUNCH_CHECK();
     {
