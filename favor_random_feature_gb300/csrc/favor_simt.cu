@@ -1210,9 +1210,10 @@ __global__ void __launch_bounds__(256) bwd_dw(const float *__restrict__ Cq, cons
     }
 }
 
-// dynamic shared memory of state_scan (DV value columns) and bwd_dw (D input columns)
+// dynamic shared memory of a [64][68] tile and a [64][DV + 4] tile (state_scan: DV value
+// columns; bwd_dw: DV = D input columns)
 template <int DV>
-constexpr size_t state_tile_smem() {
+constexpr size_t rows64_smem() {
     return sizeof(float) * (kBwdRows * 68 + kBwdRows * (DV + 4));
 }
 
@@ -1258,7 +1259,7 @@ int backward_dv(const T *q, const T *k, const T *v, const float *omega, const fl
     const int nz = p.causal ? 1 : std::min(nch, 8);
     const dim3 cg(nch, p.BH), sg2((p.r + 63) / 64, p.BH, nz);
     const unsigned sb = (unsigned)((per * p.BH + 255) / 256);
-    const size_t st_smem = state_tile_smem<DV>();
+    const size_t st_smem = rows64_smem<DV>();
     if (cudaFuncSetAttribute(state_scan<T, DV, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st_smem) !=
             cudaSuccess ||
         cudaFuncSetAttribute(state_scan<T, DV, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st_smem) !=
@@ -1334,9 +1335,9 @@ int backward_dv(const T *q, const T *k, const T *v, const float *omega, const fl
             return FAVOR_OK;
         };
         // the input tile has the shape of a state tile with D columns
-        const int rc = p.d == 32   ? dw_launch(bwd_dw<T, 32>, state_tile_smem<32>())
-                       : p.d == 64 ? dw_launch(bwd_dw<T, 64>, state_tile_smem<64>())
-                                   : dw_launch(bwd_dw<T, 128>, state_tile_smem<128>());
+        const int rc = p.d == 32   ? dw_launch(bwd_dw<T, 32>, rows64_smem<32>())
+                       : p.d == 64 ? dw_launch(bwd_dw<T, 64>, rows64_smem<64>())
+                                   : dw_launch(bwd_dw<T, 128>, rows64_smem<128>());
         if (rc != FAVOR_OK) return rc;
         FAVOR_LAUNCH_CHECK();
     }
