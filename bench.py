@@ -458,6 +458,8 @@ def run_backward(args):
     if int(os.environ.get("WORLD_SIZE", "1")) != 1 or args.gpus != 1:
         raise SystemExit("backward workloads run on one GPU (replicas only)")
     w, causal = workload(BACKWARD[args.workload])
+    if args.heads:   # a smaller case of the same workload, for ncu captures
+        w = w.with_(B=1, H=min(args.heads, w.H))
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
     inp = make_inputs(w)
     dev16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
@@ -544,7 +546,9 @@ def run_backward(args):
         "metric": BWD_METRIC, "value": tokens / (ms / 1000.0), "unit": "tokens/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": dict(describe(w, causal), workload=f"{args.workload}: backward of " + describe(w, causal)["workload"],
+        "config": dict(describe(w, causal),
+                       workload=(f"PROFILING CASE (first {w.H} heads, not a benchmark value) " if args.heads else "")
+                       + f"{args.workload}: backward of " + describe(w, causal)["workload"],
                        inputs="bf16 q,k,v; fp32 omega, dloss/dout and gradients"),
         "roofline": {
             "bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
@@ -771,6 +775,9 @@ def main():
                     choices=["causal8k", "nc4096", "long64k", "long64k_nc", "sweep16k", "decode8k",
                              "decode_b256", "causal8k_bwd", "nc4096_bwd"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="profiling case: the backward workloads on their first N heads (B = 1); "
+                         "the line is marked and is not a benchmark value")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
