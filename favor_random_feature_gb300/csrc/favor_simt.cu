@@ -874,7 +874,7 @@ __global__ void __launch_bounds__(256) bwd_dx(float *__restrict__ C, const float
 // chunks into chunk slot z (state_sum adds them).  Block per (64-feature
 // tile, head, range), 256 threads, the chunks in order (a fixed
 // summation order), the next chunk's rows read into registers while the
-// current one is added; thread (ty, tx) owns features ty + 16 u and columns
+// current one is added; thread (ty, tx) owns features 4 ty + u and columns
 // 4 tx + w (+ 64 per group) of the running state, and every thread the last
 // column (sum of phi, or of phi dden) of its features.
 template <typename T, int DV, bool YIN>
@@ -929,7 +929,7 @@ __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) state_scan(const float 
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const float z = zc[u];
-            const int f = f0 + ty + 16 * u;
+            const int f = f0 + 4 * ty + u;
             if (f >= r) continue;
 #pragma unroll
             for (int gi = 0; gi < NG; ++gi) {
@@ -968,13 +968,12 @@ __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) state_scan(const float 
         __syncthreads();
         if (it + 1 < c_n) fetch(reverse ? ch - 1 : ch + 1);
         if (causal) write_state(ch);   // exclusive: before this chunk is added
-        // acc[g][u][w] += sum_i phi[i][ty + 16 u] Yc[i][64 g + 4 tx + w] and the last
+        // acc[g][u][w] += sum_i phi[i][4 ty + u] Yc[i][64 g + 4 tx + w] and the last
         // column in the same pass over the rows (one more broadcast load per row)
 #pragma unroll 4
         for (int i = 0; i < C; ++i) {
-            float av[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) av[u] = Ps[i * P + ty + 16 * u];
+            const float4 a4 = *reinterpret_cast<const float4 *>(Ps + i * P + 4 * ty);
+            const float av[4] = {a4.x, a4.y, a4.z, a4.w};
             const float yz = Ys[i * WP + DV];
 #pragma unroll
             for (int gi = 0; gi < NG; ++gi) {
@@ -1132,7 +1131,7 @@ __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) bwd_rows(const float *_
 // dw[h][p][j] += over a slice of 512 of the head's rows (all batches; queries
 // and keys): sum_rows c[row][p] x[row][j].  Block per (64-projection tile,
 // slice, head), 256 threads, 64 rows at a time in shared memory, read a
-// sub-slice ahead into registers: thread (ty, tx) owns projections ty + 16 u
+// sub-slice ahead into registers: thread (ty, tx) owns projections 4 ty + u
 // and columns 4 tx + w (+ 64 per group); one atomic add per output and block.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) bwd_dw(const float *__restrict__ Cq, const float *__restrict__ Ck,
@@ -1193,11 +1192,11 @@ __global__ void __launch_bounds__(256) bwd_dw(const float *__restrict__ Cq, cons
         if (it + 1 < 2 * SUB) fetch(it + 1);
 #pragma unroll
         for (int gi = 0; gi < NG; ++gi)
-            if (64 * gi + 4 * tx < D) mm_tn(acc[gi], Cs, P, Xs + 64 * gi, DP, RS, ty, tx);
+            if (64 * gi + 4 * tx < D) mm_tn<true>(acc[gi], Cs, P, Xs + 64 * gi, DP, RS, ty, tx);
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-        const int p = p0 + ty + 16 * u;
+        const int p = p0 + 4 * ty + u;
         if (p >= nproj) continue;
 #pragma unroll
         for (int gi = 0; gi < NG; ++gi) {
