@@ -341,7 +341,16 @@ def run_ours(args):
     else:
         kbytes_tok = bytes_tok
     achieved = kbytes_tok * tokens / (dom_ms / 1000.0) / 1e9
-    roof_ms = max(flops_tok * tokens / (tflops * 1e12), bytes_tok * tokens / (hbm_gbs * 1e9)) * 1e3
+    # the step's three bounds: tensor (measured bf16 rate; the path's fp16 MMAs run at
+    # the same rate), HBM (measured copy), MUFU (derived: SMs x 32 ex2 per clock x the
+    # sampled maximum SM clock)
+    clocks = sampler.summary(t0, t1)
+    mufu_rate = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count * 32 * \
+        (clocks.get("sm_max_mhz") or 2070.0) * 1e6
+    bounds_ms = {"tensor": flops_tok * tokens / (tflops * 1e12) * 1e3,
+                 "hbm": bytes_tok * tokens / (hbm_gbs * 1e9) * 1e3,
+                 "mufu": exps_tok * tokens / mufu_rate * 1e3}
+    roof_ms = max(bounds_ms.values())
 
     # end to end through the host-buffer entry point (pinned host memory)
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory().numpy()
@@ -378,11 +387,13 @@ def run_ours(args):
             "kernel_ms": dom_ms, "peak_source": src,
             "algorithmic_bytes_per_launch": kbytes_tok * tokens,
             "step_roofline_ms": roof_ms, "step_frac": roof_ms / ms,
+            "step_bounds_ms": bounds_ms,
+            "mufu_peak_source": "derived: SMs x 32 ex2 per clock x max SM clock",
         },
         "e2e": {"value": world * tokens / te, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": int(round(launches_per_step * args.steps)),
-        "clocks": sampler.summary(t0, t1),
+        "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb = cpu_baseline(inp, causal)
