@@ -14,10 +14,13 @@
 //      one per-head constant factor, which cancels in the ratio.
 //   4a. non-causal   KVz = phi_K^T [V | 1]; out = phi~_Q KV / phi~_Q z
 //      -- Performer page In[25]; study notes "Core points" steps 4-5.
-//   4b. causal       chunk states dS_c = phi_K(c)^T [V_c | 1]; exclusive prefix
-//      over chunks; out_i = (phi_q S_in + sum_{j<=i in chunk} A_ij v_j) /
-//      (phi_q z_in + sum_{j<=i} A_ij), A_ij = phi~_q_i . phi_K_j
-//      -- study notes "Case 2" (prefix sum), diagonal included.
+//   4b. causal       per 64-row chunk the state entering it (the sum of the
+//      chunk states phi_K(c)^T [V_c | 1] before it); out_i = (phi_q S_in +
+//      sum_{j<=i in chunk} A_ij v_j) / (phi_q z_in + sum_{j<=i} A_ij),
+//      A_ij = phi~_q_i . phi_K_j -- study notes "Case 2" (prefix sum),
+//      diagonal included.
+//   Steps 4a/4b run on state_scan and chunk_rows, the kernels the backward
+//   pass uses too.
 #include <cmath>
 
 #include <cuda_bf16.h>
@@ -26,8 +29,6 @@
 
 namespace favor {
 namespace {
-
-constexpr int kChunk = 64;   // causal chunk length of the SIMT path
 
 __device__ __forceinline__ float load_in(const float *p, size_t i) { return p[i]; }
 __device__ __forceinline__ float load_in(const uint16_t *p, size_t i) {
@@ -289,87 +290,6 @@ __global__ void simt_state(const float *__restrict__ phik, const T *__restrict__
     }
     S[(((size_t)bh * nseg + s) * r + f) * (dv + 1) + c] = acc;
 }
-
-// 4b. exclusive prefix over chunks, in place.
-// (eight segments' values are loaded before any is stored, so that the
-// loads are in flight together)
-__global__ void simt_state_prefix(float *__restrict__ S, int nseg, size_t per_seg, int BH) {
-    size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
-    if (e >= per_seg * BH) return;
-    int bh = (int)(e / per_seg);
-    size_t within = e % per_seg;
-    float *base = S + (size_t)bh * nseg * per_seg + within;
-    float run = 0.f;
-    for (int s0 = 0; s0 < nseg; s0 += 8) {
-        float t[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) t[i] = s0 + i < nseg ? base[(size_t)(s0 + i) * per_seg] : 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            if (s0 + i < nseg) base[(size_t)(s0 + i) * per_seg] = run;
-            run += t[i];
-        }
-    }
-}
-
-// 4a. non-causal output: thread per (row, c).
-template <typename O>
-__global__ void simt_out_noncausal(const float *__restrict__ phiq, const float *__restrict__ S,
-                                   O *__restrict__ out, int L, int r, int dv) {
-    const int c = threadIdx.x;
-    const int row = blockIdx.x * blockDim.y + threadIdx.y;
-    const int bh = blockIdx.y;
-    if (row >= L || c >= dv) return;
-    const float *pq = phiq + ((size_t)bh * L + row) * r;
-    const float *Sb = S + (size_t)bh * r * (dv + 1);
-    float num = 0.f, den = 0.f;
-    for (int f = 0; f < r; ++f) {
-        float a = pq[f];
-        num = fmaf(a, Sb[(size_t)f * (dv + 1) + c], num);
-        den = fmaf(a, Sb[(size_t)f * (dv + 1) + dv], den);
-    }
-    store_out(out, ((size_t)bh * L + row) * dv + c, num / den);
-}
-
-// 4b. causal output: block per (chunk, head), 256 threads.
-template <typename T, typename O>
-__global__ void simt_out_causal(const float *__restrict__ phiq, const float *__restrict__ phik,
-                                const T *__restrict__ v, const float *__restrict__ Sin,
-                                O *__restrict__ out, int L, int r, int dv, int nch) {
-    __shared__ float A[kChunk][kChunk + 1];
-    __shared__ float den_s[kChunk];
-    const int ch = blockIdx.x, bh = blockIdx.y;
-    const int t0 = ch * kChunk;
-    const int n = min(kChunk, L - t0);
-    const float *pq = phiq + ((size_t)bh * L + t0) * r;
-    const float *pk = phik + ((size_t)bh * L + t0) * r;
-    const T *vb = v + ((size_t)bh * L + t0) * dv;
-    const float *Sb = Sin + ((size_t)bh * nch + ch) * r * (dv + 1);
-    for (int e = threadIdx.x; e < kChunk * kChunk; e += blockDim.x) {
-        int i = e / kChunk, j = e % kChunk;
-        float a = 0.f;
-        if (i < n && j <= i) {
-            for (int f = 0; f < r; ++f) a = fmaf(pq[(size_t)i * r + f], pk[(size_t)j * r + f], a);
-        }
-        A[i][j] = a;
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-        float den = 0.f;
-        for (int f = 0; f < r; ++f) den = fmaf(pq[(size_t)i * r + f], Sb[(size_t)f * (dv + 1) + dv], den);
-        for (int j = 0; j <= i; ++j) den += A[i][j];
-        den_s[i] = den;
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < n * dv; e += blockDim.x) {
-        int i = e / dv, c = e % dv;
-        float num = 0.f;
-        for (int f = 0; f < r; ++f) num = fmaf(pq[(size_t)i * r + f], Sb[(size_t)f * (dv + 1) + c], num);
-        for (int j = 0; j <= i; ++j) num = fmaf(A[i][j], load_in(vb, (size_t)j * dv + c), num);
-        store_out(out, ((size_t)bh * L + t0 + i) * dv + c, num / den_s[i]);
-    }
-}
-
 template <typename T>
 int features_into(const T *x, const float *omega, float *P, float *phi, float *logscale,
                   const Problem &p, cudaStream_t st) {
@@ -385,78 +305,8 @@ int features_into(const T *x, const float *omega, float *P, float *phi, float *l
     return FAVOR_OK;
 }
 
-template <typename T>
-int forward_t(const T *q, const T *k, const T *v, const float *omega, float *out, const Problem &p,
-              cudaStream_t st) {
-    const size_t rows = (size_t)p.BH * p.L;
-    const int nch = p.causal ? (p.L + kChunk - 1) / kChunk : 1;
-    const size_t per_seg = (size_t)p.r * (p.dv + 1);
-    size_t bytes = carve_bytes<float>(rows * p.nproj) + 2 * carve_bytes<float>(rows * p.r) +
-                   2 * carve_bytes<float>(rows) + carve_bytes<float>(p.BH) +
-                   carve_bytes<float>((size_t)p.BH * nch * per_seg);
-    int status = FAVOR_OK;
-    void *ws = workspace(bytes, &status);
-    if (!ws) return status;
-    Carve cv{static_cast<char *>(ws), 0};
-    float *P = cv.take<float>(rows * p.nproj);
-    float *phiq = cv.take<float>(rows * p.r);
-    float *phik = cv.take<float>(rows * p.r);
-    float *lsq = cv.take<float>(rows);
-    float *lsk = cv.take<float>(rows);
-    float *hmax = cv.take<float>(p.BH);
-    float *S = cv.take<float>((size_t)p.BH * nch * per_seg);
-
-    int rc = features_into<T>(q, omega, P, phiq, lsq, p, st);
-    if (rc) return rc;
-    rc = features_into<T>(k, omega, P, phik, lsk, p, st);
-    if (rc) return rc;
-    simt_head_max<<<p.BH, 256, 0, st>>>(lsk, hmax, p.L);
-    FAVOR_LAUNCH_CHECK();
-    size_t total = rows * p.r;
-    unsigned sg = (unsigned)std::min<size_t>((total + 255) / 256, 152 * 64);
-    simt_key_scale<<<sg, 256, 0, st>>>(phik, lsk, hmax, p.L, p.r, total);
-    FAVOR_LAUNCH_CHECK();
-
-    const int seg = p.causal ? kChunk : p.L;
-    dim3 sgrid((p.r + 31) / 32, p.dv + 1, p.BH * nch);
-    simt_state<T><<<sgrid, 32, 0, st>>>(phik, v, S, p.L, p.r, p.dv, seg, nch);
-    FAVOR_LAUNCH_CHECK();
-    if (!p.causal) {
-        dim3 blk(p.dv, std::max(1, 256 / p.dv));
-        dim3 og((p.L + blk.y - 1) / blk.y, p.BH);
-        stats_begin(st, "simt_out_noncausal");
-        if (p.out_bf16)
-            simt_out_noncausal<<<og, blk, 0, st>>>(phiq, S, reinterpret_cast<__nv_bfloat16 *>(out), p.L, p.r, p.dv);
-        else
-            simt_out_noncausal<<<og, blk, 0, st>>>(phiq, S, out, p.L, p.r, p.dv);
-        stats_end(st);
-        FAVOR_LAUNCH_CHECK();
-        return FAVOR_OK;
-    }
-    size_t n = per_seg * p.BH;
-    simt_state_prefix<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(S, nch, per_seg, p.BH);
-    FAVOR_LAUNCH_CHECK();
-    stats_begin(st, "simt_out_causal");
-    if (p.out_bf16)
-        simt_out_causal<T, __nv_bfloat16><<<dim3(nch, p.BH), 256, 0, st>>>(
-            phiq, phik, v, S, reinterpret_cast<__nv_bfloat16 *>(out), p.L, p.r, p.dv, nch);
-    else
-        simt_out_causal<T, float><<<dim3(nch, p.BH), 256, 0, st>>>(phiq, phik, v, S, out, p.L, p.r, p.dv, nch);
-    stats_end(st);
-    FAVOR_LAUNCH_CHECK();
-    return FAVOR_OK;
-}
-
 }  // namespace
 
-int simt_forward(const void *q, const void *k, const void *v, bool bf16_in, const float *omega,
-                 float *out, const Problem &p, cudaStream_t stream) {
-    if (bf16_in)
-        return forward_t<uint16_t>(static_cast<const uint16_t *>(q), static_cast<const uint16_t *>(k),
-                                   static_cast<const uint16_t *>(v), omega, out, p, stream);
-    return forward_t<float>(static_cast<const float *>(q), static_cast<const float *>(k),
-                            static_cast<const float *>(v), omega, out, p, stream);
-}
 
 namespace {
 template <typename T>
@@ -531,7 +381,7 @@ int simt_feature_map(const void *x, bool bf16_in, const float *omega, float *phi
 // ---------------------------------------------------------------------------
 namespace {
 
-constexpr int kBwdRows = 64;    // rows per chunk (= kChunk)
+constexpr int kBwdRows = 64;    // rows per chunk of the SIMT forward and backward passes
 constexpr int kBwdThreads = 256;   // threads of a bwd_chunk block
 
 // dphi_q, dphi_k [rows][r] and dv [rows][dv] of a chunk of C = 64 rows from the
@@ -539,7 +389,7 @@ constexpr int kBwdThreads = 256;   // threads of a bwd_chunk block
 // it; block per (chunk, head), 256 threads, 64-feature tiles (two blocks per
 // SM at dv = 64):
 //   B = Y [V | 1]^T, masked to j <= i
-//   pass 1: dv += phi_k R[:, :dv]; then dv += A^T dnum (A masked, from bwd_rows)
+//   pass 1: dv += phi_k R[:, :dv]; then dv += A^T dnum (A masked, from chunk_rows)
 //   pass 2: dphi_q = Y S^T + B phi_k, then dphi_k = [V | 1] R^T + B^T phi_q
 // A thread owns rows 4 ty .. 4 ty + 3, so the triangular products (B phi_k,
 // B^T phi_q, A^T dnum) run only over the keys or queries on its side of the
@@ -871,7 +721,7 @@ __global__ void __launch_bounds__(256) bwd_dx(float *__restrict__ C, const float
 // Yc = [v | 1] (forward) or the rows' [dnum | dden] (backward).  Written per
 // chunk: causal, the exclusive prefix (forward: chunks before c; reverse:
 // chunks after c); non-causal, the total of the z-th of gridDim.z ranges of
-// chunks into chunk slot z (state_sum adds them).  Block per (64-feature
+// chunks into slot z (state_sum adds them).  S holds nslot slots per head.  Block per (64-feature
 // tile, head, range), 256 threads, the chunks in order (a fixed
 // summation order), the next chunk's rows read into registers while the
 // current one is added; thread (ty, tx) owns features 4 ty + u and columns
@@ -880,7 +730,7 @@ __global__ void __launch_bounds__(256) bwd_dx(float *__restrict__ C, const float
 template <typename T, int DV, bool YIN>
 __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) state_scan(const float *__restrict__ phi, const T *__restrict__ v,
                                                      const float *__restrict__ Y, float *__restrict__ S, int L,
-                                                     int r, int nch, int causal, int reverse) {
+                                                     int r, int nch, int nslot, int causal, int reverse) {
     constexpr int C = kBwdRows, FT = 64, P = FT + 4, W = DV + 1, WP = DV + 4, NG = (DV + 63) / 64, NT = 256;
     constexpr int NX = C * FT / 4 / NT, NY = (C * W + NT - 1) / NT;
     extern __shared__ float4 sm4[];
@@ -925,7 +775,7 @@ __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) state_scan(const float 
     for (int e = tid; e < C * WP; e += NT) Ys[e] = 0.f;   // pad columns stay zero
     float acc[NG][4][4] = {}, zc[4] = {};   // zc: the last column (every tx holds it)
     auto write_state = [&](int slot) {
-        float *dst = S + ((size_t)bh * nch + slot) * r * WP;
+        float *dst = S + ((size_t)bh * nslot + slot) * r * WP;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const float z = zc[u];
@@ -995,26 +845,28 @@ __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) state_scan(const float 
 }
 
 // non-causal: chunk slots 1 .. nz - 1 added to slot 0 in order
-__global__ void state_sum(float *__restrict__ S, int nch, int nz, size_t per, int BH) {
+__global__ void state_sum(float *__restrict__ S, int nslot, int nz, size_t per, int BH) {
     const size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
     if (e >= per * BH) return;
-    float *base = S + (e / per) * nch * per + e % per;
+    float *base = S + (e / per) * nslot * per + e % per;
     float sum = base[0];
     for (int z = 1; z < nz; ++z) sum += base[(size_t)z * per];
     base[0] = sum;
 }
 
 // per row of a chunk: num, den from the entering state (+ the masked chunk
-// sum), out = num / den, then dnum = g / den and dden = -(g . out) / den into
+// sum), out = num / den; the forward pass (FWD) stores out, the backward
+// pass forms dnum = g / den and dden = -(g . out) / den into
 // Y [rows][dv + 4] (3 zero columns; and, causal, the masked A of the chunk into Am
 // [BH][chunks][64][64] for bwd_chunk).  Block per (chunk, head), 256 threads,
 // 64-feature tiles read a tile ahead into registers:
 //   num = phi_q S[:, :dv] (+ A_m V),  den = phi_q z (+ A_m 1),  A_m = (phi_q phi_k^T) masked to j <= i
-template <typename T, int DV>
-__global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) bwd_rows(const float *__restrict__ phiq, const float *__restrict__ phik,
+template <typename T, int DV, bool FWD, typename O>
+__global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) chunk_rows(const float *__restrict__ phiq, const float *__restrict__ phik,
                                                 const T *__restrict__ v, const float *__restrict__ Sin,
                                                 const float *__restrict__ g, float *__restrict__ Y,
-                                                float *__restrict__ Am, int L, int r, int nst, int causal) {
+                                                float *__restrict__ Am, O *__restrict__ out, int L, int r, int nst,
+                                                int causal) {
     constexpr int C = kBwdRows, FT = 64, P = FT + 4, W = DV + 1, WP = DV + 4, NG = (DV + 63) / 64, NT = 256;
     extern __shared__ float4 sm4[];
     float *Qt = reinterpret_cast<float *>(sm4);   // [C][P]   phi_q tile
@@ -1087,7 +939,7 @@ __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) bwd_rows(const float *_
                 const int i = ty + 16 * u, j = tx + 16 * w;
                 const float x = j <= i ? a[u][w] : 0.f;
                 Kt[i * P + j] = x;
-                Am[(((size_t)bh * nst + ch) * C + i) * C + j] = x;   // for bwd_chunk
+                if (!FWD) Am[(((size_t)bh * nst + ch) * C + i) * C + j] = x;   // for bwd_chunk
                 den[u] += x;
             }
         __syncthreads();
@@ -1114,17 +966,24 @@ __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) bwd_rows(const float *_
     }
     __syncthreads();
     const int warp = tid >> 5, lane = tid & 31;
-    for (int i = warp; i < n; i += NT / 32) {
-        const float dn = NUM[i * WP + DV];
-        float gdo = 0.f;
-        for (int c = lane; c < DV; c += 32) {
-            const float gi = g[(row0 + i) * DV + c];
-            gdo = fmaf(gi, NUM[i * WP + c] / dn, gdo);
-            Y[(row0 + i) * WP + c] = gi / dn;
+    if constexpr (FWD) {   // the forward pass: out = num / den
+        for (int e = tid; e < n * DV; e += NT) {
+            const int i = e / DV, c = e % DV;
+            store_out(out, (row0 + i) * DV + c, NUM[i * WP + c] / NUM[i * WP + DV]);
         }
+    } else {
+        for (int i = warp; i < n; i += NT / 32) {
+            const float dn = NUM[i * WP + DV];
+            float gdo = 0.f;
+            for (int c = lane; c < DV; c += 32) {
+                const float gi = g[(row0 + i) * DV + c];
+                gdo = fmaf(gi, NUM[i * WP + c] / dn, gdo);
+                Y[(row0 + i) * WP + c] = gi / dn;
+            }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) gdo += __shfl_xor_sync(0xffffffffu, gdo, o);
-        if (lane == 0) *reinterpret_cast<float4 *>(Y + (row0 + i) * WP + DV) = make_float4(-gdo / dn, 0.f, 0.f, 0.f);
+            for (int o = 16; o > 0; o >>= 1) gdo += __shfl_xor_sync(0xffffffffu, gdo, o);
+            if (lane == 0) *reinterpret_cast<float4 *>(Y + (row0 + i) * WP + DV) = make_float4(-gdo / dn, 0.f, 0.f, 0.f);
+        }
     }
 }
 
@@ -1217,7 +1076,7 @@ constexpr size_t rows64_smem() {
 }
 
 template <int DV>
-constexpr size_t bwd_rows_smem() {
+constexpr size_t chunk_rows_smem() {
     return sizeof(float) * (2 * kBwdRows * 68 + 2 * kBwdRows * (DV + 4));
 }
 
@@ -1242,7 +1101,7 @@ int backward_dv(const T *q, const T *k, const T *v, const float *omega, const fl
     float *hmax = cv.take<float>(p.BH);
     float *S = cv.take<float>((size_t)p.BH * nch * per), *R = cv.take<float>((size_t)p.BH * nch * per);
     float *Y = cv.take<float>(rows * (DV + 4));   // [rows][dv + 4]: dnum | dden | 3 zero columns
-    // the masked chunk matrices A (causal), formed by bwd_rows and read by bwd_chunk
+    // the masked chunk matrices A (causal), formed by chunk_rows and read by bwd_chunk
     float *Am = p.causal ? cv.take<float>((size_t)p.BH * nch * kBwdRows * kBwdRows) : nullptr;
 
     int rc;
@@ -1267,21 +1126,22 @@ int backward_dv(const T *q, const T *k, const T *v, const float *omega, const fl
         return FAVOR_ERR_CUDA;
     }
     // the forward states entering each chunk (causal: exclusive prefix) or the total (chunk slot 0)
-    state_scan<T, DV, false><<<sg2, 256, st_smem, st>>>(phik, v, nullptr, S, p.L, p.r, nch, p.causal, 0);
+    state_scan<T, DV, false><<<sg2, 256, st_smem, st>>>(phik, v, nullptr, S, p.L, p.r, nch, nch, p.causal, 0);
     if (nz > 1) state_sum<<<sb, 256, 0, st>>>(S, nch, nz, per, p.BH);
     FAVOR_LAUNCH_CHECK();
     {
-        const size_t smem = bwd_rows_smem<DV>();
-        if (cudaFuncSetAttribute(bwd_rows<T, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        const size_t smem = chunk_rows_smem<DV>();
+        if (cudaFuncSetAttribute(chunk_rows<T, DV, false, float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess) {
             cudaGetLastError();
             return FAVOR_ERR_CUDA;
         }
-        bwd_rows<T, DV><<<cg, 256, smem, st>>>(phiq, phik, v, S, g, Y, Am, p.L, p.r, nch, p.causal);
+        chunk_rows<T, DV, false, float><<<cg, 256, smem, st>>>(phiq, phik, v, S, g, Y, Am, nullptr, p.L, p.r, nch,
+                                                               p.causal);
         FAVOR_LAUNCH_CHECK();
     }
     // the states leaving each chunk (causal: exclusive suffix) or the total
-    state_scan<T, DV, true><<<sg2, 256, st_smem, st>>>(phiq, v, Y, R, p.L, p.r, nch, p.causal, 1);
+    state_scan<T, DV, true><<<sg2, 256, st_smem, st>>>(phiq, v, Y, R, p.L, p.r, nch, nch, p.causal, 1);
     if (nz > 1) state_sum<<<sb, 256, 0, st>>>(R, nch, nz, per, p.BH);
     FAVOR_LAUNCH_CHECK();
     {
@@ -1350,6 +1210,75 @@ int backward_t(const T *q, const T *k, const T *v, const float *omega, const flo
     if (p.dv == 64) return backward_dv<T, 64>(q, k, v, omega, g, dq, dk, dv, dw, p, st);
     return backward_dv<T, 128>(q, k, v, omega, g, dq, dk, dv, dw, p, st);
 }
+// The SIMT forward pass (fp32 entry point; shapes outside the tensor-core
+// layouts): features of q and k (steps 1-3), then the chunk states of the keys
+// (state_scan: causal, each 64-row chunk's exclusive prefix; non-causal, the
+// total) and per chunk num = phi_q S (+ A_m [V | 1]), out = num / den
+// (chunk_rows in its forward mode) -- the same kernels the backward pass runs.
+template <typename T, int DV>
+int forward_dv(const T *q, const T *k, const T *v, const float *omega, void *out, const Problem &p,
+               cudaStream_t st) {
+    const size_t rows = (size_t)p.BH * p.L;
+    const int nch = (p.L + kBwdRows - 1) / kBwdRows;
+    const int nz = p.causal ? 1 : std::min(nch, 8), nslot = p.causal ? nch : nz;
+    const size_t per = (size_t)p.r * (DV + 4);
+    size_t bytes = carve_bytes<float>(rows * p.nproj) + 2 * carve_bytes<float>(rows * p.r) +
+                   2 * carve_bytes<float>(rows) + carve_bytes<float>(p.BH) +
+                   carve_bytes<float>((size_t)p.BH * nslot * per);
+    int status = FAVOR_OK;
+    void *ws = workspace(bytes, &status);
+    if (!ws) return status;
+    Carve cv{static_cast<char *>(ws), 0};
+    float *P = cv.take<float>(rows * p.nproj);
+    float *phiq = cv.take<float>(rows * p.r), *phik = cv.take<float>(rows * p.r);
+    float *lsq = cv.take<float>(rows), *lsk = cv.take<float>(rows);
+    float *hmax = cv.take<float>(p.BH);
+    float *S = cv.take<float>((size_t)p.BH * nslot * per);
+
+    int rc = features_into<T>(q, omega, P, phiq, lsq, p, st);
+    if (rc) return rc;
+    if ((rc = features_into<T>(k, omega, P, phik, lsk, p, st))) return rc;
+    simt_head_max<<<p.BH, 256, 0, st>>>(lsk, hmax, p.L);
+    FAVOR_LAUNCH_CHECK();
+    const size_t total = rows * p.r;
+    const unsigned sg = (unsigned)std::min<size_t>((total + 255) / 256, 152 * 64);
+    simt_key_scale<<<sg, 256, 0, st>>>(phik, lsk, hmax, p.L, p.r, total);
+    FAVOR_LAUNCH_CHECK();
+
+    const size_t st_smem = rows64_smem<DV>(), rw_smem = chunk_rows_smem<DV>();
+    if (cudaFuncSetAttribute(state_scan<T, DV, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st_smem) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(chunk_rows<T, DV, true, float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)rw_smem) != cudaSuccess ||
+        cudaFuncSetAttribute(chunk_rows<T, DV, true, __nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)rw_smem) != cudaSuccess) {
+        cudaGetLastError();
+        return FAVOR_ERR_CUDA;
+    }
+    state_scan<T, DV, false><<<dim3((p.r + 63) / 64, p.BH, nz), 256, st_smem, st>>>(phik, v, nullptr, S, p.L, p.r,
+                                                                                    nch, nslot, p.causal, 0);
+    if (nz > 1) state_sum<<<(unsigned)((per * p.BH + 255) / 256), 256, 0, st>>>(S, nslot, nz, per, p.BH);
+    FAVOR_LAUNCH_CHECK();
+    const dim3 cg(nch, p.BH);
+    stats_begin(st, "chunk_rows");
+    if (p.out_bf16)
+        chunk_rows<T, DV, true, __nv_bfloat16><<<cg, 256, rw_smem, st>>>(
+            phiq, phik, v, S, nullptr, nullptr, nullptr, static_cast<__nv_bfloat16 *>(out), p.L, p.r, nslot, p.causal);
+    else
+        chunk_rows<T, DV, true, float><<<cg, 256, rw_smem, st>>>(phiq, phik, v, S, nullptr, nullptr, nullptr,
+                                                                 static_cast<float *>(out), p.L, p.r, nslot, p.causal);
+    stats_end(st);
+    FAVOR_LAUNCH_CHECK();
+    return FAVOR_OK;
+}
+
+template <typename T>
+int forward_t(const T *q, const T *k, const T *v, const float *omega, void *out, const Problem &p, cudaStream_t st) {
+    if (p.dv == 32) return forward_dv<T, 32>(q, k, v, omega, out, p, st);
+    if (p.dv == 64) return forward_dv<T, 64>(q, k, v, omega, out, p, st);
+    if (p.dv == 128) return forward_dv<T, 128>(q, k, v, omega, out, p, st);
+    return FAVOR_ERR_UNSUPPORTED;
+}
 }  // namespace
 
 int simt_backward(const void *q, const void *k, const void *v, bool bf16_in, const float *omega, const float *g,
@@ -1359,6 +1288,15 @@ int simt_backward(const void *q, const void *k, const void *v, bool bf16_in, con
                                     static_cast<const uint16_t *>(v), omega, g, dq, dk, dv, dw, p, stream);
     return backward_t<float>(static_cast<const float *>(q), static_cast<const float *>(k),
                              static_cast<const float *>(v), omega, g, dq, dk, dv, dw, p, stream);
+}
+
+int simt_forward(const void *q, const void *k, const void *v, bool bf16_in, const float *omega, float *out,
+                 const Problem &p, cudaStream_t stream) {
+    if (bf16_in)
+        return forward_t<uint16_t>(static_cast<const uint16_t *>(q), static_cast<const uint16_t *>(k),
+                                   static_cast<const uint16_t *>(v), omega, out, p, stream);
+    return forward_t<float>(static_cast<const float *>(q), static_cast<const float *>(k), static_cast<const float *>(v),
+                            omega, out, p, stream);
 }
 
 }  // namespace favor
