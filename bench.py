@@ -341,6 +341,7 @@ def run_ours(args):
     else:
         kbytes_tok = bytes_tok
     achieved = kbytes_tok * tokens / (dom_ms / 1000.0) / 1e9
+    alu = kname == "chunk_rows"   # the fp32 SIMT forward (shapes outside the tensor-core layouts)
     # the step's three bounds: tensor (measured bf16 rate; the path's fp16 MMAs run at
     # the same rate), HBM (measured copy), MUFU (derived: SMs x 32 ex2 per clock x the
     # sampled maximum SM clock)
@@ -380,7 +381,7 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
         "config": describe(w, causal),
-        "roofline": {
+        "roofline": dict({
             "bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
             "frac": achieved / hbm_gbs, "traffic": measured_traffic(kname, args.workload),
             "kernel": kname or None,
@@ -389,7 +390,7 @@ def run_ours(args):
             "step_roofline_ms": roof_ms, "step_frac": roof_ms / ms,
             "step_bounds_ms": bounds_ms,
             "mufu_peak_source": "derived: SMs x 32 ex2 per clock x max SM clock",
-        },
+        }, **(simt_rows_roofline(w, causal, tokens, dom_ms, clocks) if alu else {})),
         "e2e": {"value": world * tokens / te, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": int(round(launches_per_step * args.steps)),
@@ -441,7 +442,22 @@ def decode_cpu_baseline(w, n_heads, steps):
 # call (gradients of q, k, v and omega for a seeded dloss/dout)
 BWD_METRIC = "FAVOR+ backward tokens/sec (B*H*L/s); % of the fp32 ALU roofline"
 BACKWARD = {"causal8k_bwd": "causal8k", "nc4096_bwd": "nc4096"}
-BWD_ROWS = 64   # rows per chunk of the backward kernels
+BWD_ROWS = 64   # rows per chunk of the SIMT forward and backward kernels
+
+
+def simt_rows_roofline(w, causal, tokens, dom_ms, clocks):
+    """The fp32 SIMT forward's dominant kernel (chunk_rows) against the fp32 ALU
+    peak: algorithmic FLOPs per token num = phi_q S (2 r (dv + 1)) and, causal,
+    the masked chunk product A (2 r C / 2) and A_m [V | 1] (2 (C / 2)(dv + 1))."""
+    import torch
+    r, dv, C = w.r, w.dv, BWD_ROWS
+    flops = 2 * r * (dv + 1) + ((r * C + C * (dv + 1)) if causal else 0)
+    mhz = clocks.get("sm_max_mhz") or 2070.0
+    peak = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12
+    achieved = flops * tokens / (dom_ms / 1000.0) / 1e12
+    return {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "traffic": None, "peak_source": "derived: SMs x 128 fp32 lanes x 2 flops x max SM clock",
+            "algorithmic_bytes_per_launch": None, "algorithmic_flops_per_token": flops}
 
 
 def bwd_chunk_flops_per_token(w, causal):
