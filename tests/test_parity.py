@@ -120,6 +120,19 @@ def test_short_and_ragged_lengths(L, causal):
     assert e.max() <= BF16_MAX, e.max()
 
 
+@pytest.mark.parametrize("w,bar", [(SWEEP16K.with_(m=512), "bf16"), (NC4096.with_(dtype="f32"), "f32")],
+                         ids=["d128-r512-bf16", "f32"])
+def test_noncausal_chunk_ranges(w, bar):
+    """The SIMT non-causal state is summed from up to 8 ranges of 64-row chunks:
+    L = 1100 gives 18 chunks in ranges of 3, the last two ranges empty."""
+    inp = make_inputs(w, L=1100, B=1, H=2)
+    e = row_errors(run_gpu(inp, False, MAP_POSITIVE), oracle_ref(inp, False, MAP_POSITIVE))
+    if bar == "f32":
+        assert e.max() <= F32_MAX, e.max()
+    else:
+        check_bf16(e, w.name)
+
+
 @pytest.mark.parametrize("d,dv,m", [(32, 32, 16), (32, 128, 64), (128, 32, 128), (64, 128, 256),
                                     (128, 64, 32)])
 @pytest.mark.parametrize("causal", [False, True])
