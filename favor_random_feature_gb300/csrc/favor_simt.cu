@@ -271,7 +271,8 @@ __global__ void simt_key_scale(float *__restrict__ phi, const float *__restrict_
     }
 }
 
-// 4a/4b. state reduction: dS[f][c] = sum_{t in [t0, t1)} phi_K[t][f] * (c < dv ? v[t][c] : 1)
+// The state of a run of keys (the decode state of a prefix, [r][dv + 1]):
+// dS[f][c] = sum_{t in [t0, t1)} phi_K[t][f] * (c < dv ? v[t][c] : 1);
 // grid (ceil(r/32), dv+1, BH*nseg); segment length seg.
 template <typename T>
 __global__ void simt_state(const float *__restrict__ phik, const T *__restrict__ v,
@@ -721,10 +722,10 @@ __global__ void __launch_bounds__(256) bwd_dx(float *__restrict__ C, const float
 // Yc = [v | 1] (forward) or the rows' [dnum | dden] (backward).  Written per
 // chunk: causal, the exclusive prefix (forward: chunks before c; reverse:
 // chunks after c); non-causal, the total of the z-th of gridDim.z ranges of
-// chunks into slot z (state_sum adds them).  S holds nslot slots per head.  Block per (64-feature
-// tile, head, range), 256 threads, the chunks in order (a fixed
-// summation order), the next chunk's rows read into registers while the
-// current one is added; thread (ty, tx) owns features 4 ty + u and columns
+// chunks into slot z (state_sum adds them).  S holds nslot slots per head.
+// Block per (64-feature tile, head, range), 256 threads, the chunks in order
+// (a fixed summation order), the next chunk's rows read into registers while
+// the current one is added; thread (ty, tx) owns features 4 ty + u and columns
 // 4 tx + w (+ 64 per group) of the running state, and every thread the last
 // column (sum of phi, or of phi dden) of its features.
 template <typename T, int DV, bool YIN>
@@ -857,10 +858,11 @@ __global__ void state_sum(float *__restrict__ S, int nslot, int nz, size_t per, 
 // per row of a chunk: num, den from the entering state (+ the masked chunk
 // sum), out = num / den; the forward pass (FWD) stores out, the backward
 // pass forms dnum = g / den and dden = -(g . out) / den into
-// Y [rows][dv + 4] (3 zero columns; and, causal, the masked A of the chunk into Am
-// [BH][chunks][64][64] for bwd_chunk).  Block per (chunk, head), 256 threads,
-// 64-feature tiles read a tile ahead into registers:
-//   num = phi_q S[:, :dv] (+ A_m V),  den = phi_q z (+ A_m 1),  A_m = (phi_q phi_k^T) masked to j <= i
+// Y [rows][dv + 4] (3 zero columns; and, causal, the masked A of the chunk
+// into Am [BH][chunks][64][64] for bwd_chunk).  Block per (chunk, head), 256
+// threads, 64-feature tiles read a tile ahead into registers:
+//   num = phi_q S[:, :dv] (+ A_m V),  den = phi_q z (+ A_m 1),
+//   A_m = (phi_q phi_k^T) masked to j <= i
 template <typename T, int DV, bool FWD, typename O>
 __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) chunk_rows(const float *__restrict__ phiq, const float *__restrict__ phik,
                                                 const T *__restrict__ v, const float *__restrict__ Sin,
