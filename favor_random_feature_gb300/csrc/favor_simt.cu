@@ -723,6 +723,10 @@ __global__ void __launch_bounds__(256) bwd_dx(float *__restrict__ C, const float
 // chunk: causal, the exclusive prefix (forward: chunks before c; reverse:
 // chunks after c); non-causal, the total of the z-th of gridDim.z ranges of
 // chunks into slot z (state_sum adds them).  S holds nslot slots per head.
+// Causal with gridDim.z > 1 (the forward pass with few heads): each range of
+// chunks starts from zero and writes its total into tot [BH][ranges][r][dv + 4];
+// range_offsets turns the totals into each range's offset, which chunk_rows
+// adds to the states it reads.
 // Block per (64-feature tile, head, range), 256 threads, the chunks in order
 // (a fixed summation order), the next chunk's rows read into registers while
 // the current one is added; thread (ty, tx) owns features 4 ty + u and columns
@@ -730,8 +734,9 @@ __global__ void __launch_bounds__(256) bwd_dx(float *__restrict__ C, const float
 // column (sum of phi, or of phi dden) of its features.
 template <typename T, int DV, bool YIN>
 __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) state_scan(const float *__restrict__ phi, const T *__restrict__ v,
-                                                     const float *__restrict__ Y, float *__restrict__ S, int L,
-                                                     int r, int nch, int nslot, int causal, int reverse) {
+                                                     const float *__restrict__ Y, float *__restrict__ S,
+                                                     float *__restrict__ tot, int L, int r, int nch, int nslot,
+                                                     int causal, int reverse) {
     constexpr int C = kBwdRows, FT = 64, P = FT + 4, W = DV + 1, WP = DV + 4, NG = (DV + 63) / 64, NT = 256;
     constexpr int NX = C * FT / 4 / NT, NY = (C * W + NT - 1) / NT;
     extern __shared__ float4 sm4[];
@@ -775,8 +780,7 @@ __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) state_scan(const float 
     };
     for (int e = tid; e < C * WP; e += NT) Ys[e] = 0.f;   // pad columns stay zero
     float acc[NG][4][4] = {}, zc[4] = {};   // zc: the last column (every tx holds it)
-    auto write_state = [&](int slot) {
-        float *dst = S + ((size_t)bh * nslot + slot) * r * WP;
+    auto write_state = [&](float *dst) {
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const float z = zc[u];
@@ -818,7 +822,7 @@ __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) state_scan(const float 
         }
         __syncthreads();
         if (it + 1 < c_n) fetch(reverse ? ch - 1 : ch + 1);
-        if (causal) write_state(ch);   // exclusive: before this chunk is added
+        if (causal) write_state(S + ((size_t)bh * nslot + ch) * r * WP);   // exclusive: before this chunk is added
         // acc[g][u][w] += sum_i phi[i][4 ty + u] Yc[i][64 g + 4 tx + w] and the last
         // column in the same pass over the rows (one more broadcast load per row)
 #pragma unroll 4
@@ -842,7 +846,21 @@ __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) state_scan(const float 
             for (int u = 0; u < 4; ++u) zc[u] = fmaf(av[u], yz, zc[u]);
         }
     }
-    if (!causal) write_state(blockIdx.z);
+    if (!causal) write_state(S + ((size_t)bh * nslot + blockIdx.z) * r * WP);
+    else if (gridDim.z > 1) write_state(tot + ((size_t)bh * gridDim.z + blockIdx.z) * r * WP);   // the range's total
+}
+
+// causal chunk ranges: tot[bh][z] <- sum of the totals of ranges z' < z (in order)
+__global__ void range_offsets(float *__restrict__ tot, int nz, size_t per, int BH) {
+    const size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+    if (e >= per * BH) return;
+    float *base = tot + (e / per) * nz * per + e % per;
+    float run = 0.f;
+    for (int z = 0; z < nz; ++z) {
+        const float t = base[(size_t)z * per];
+        base[(size_t)z * per] = run;
+        run += t;
+    }
 }
 
 // non-causal: chunk slots 1 .. nz - 1 added to slot 0 in order
@@ -867,7 +885,8 @@ template <typename T, int DV, bool FWD, typename O>
 __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) chunk_rows(const float *__restrict__ phiq, const float *__restrict__ phik,
                                                 const T *__restrict__ v, const float *__restrict__ Sin,
                                                 const float *__restrict__ g, float *__restrict__ Y,
-                                                float *__restrict__ Am, O *__restrict__ out, int L, int r, int nst,
+                                                float *__restrict__ Am, O *__restrict__ out,
+                                                const float *__restrict__ off, int nz, int L, int r, int nst,
                                                 int causal) {
     constexpr int C = kBwdRows, FT = 64, P = FT + 4, W = DV + 1, WP = DV + 4, NG = (DV + 63) / 64, NT = 256;
     extern __shared__ float4 sm4[];
@@ -879,6 +898,9 @@ __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) chunk_rows(const float 
     const int ch = blockIdx.x, bh = blockIdx.y, t0 = ch * C, n = min(C, L - t0);
     const size_t row0 = (size_t)bh * L + t0;
     const float *S = Sin + ((size_t)bh * nst + (causal ? ch : 0)) * r * WP;
+    // causal chunk ranges (forward): the offset of this chunk's range, added to its state
+    const int zr = (FWD && causal && nz > 1) ? ch / ((nst + nz - 1) / nz) : 0;
+    const float *O0 = zr > 0 ? off + ((size_t)bh * nz + zr) * r * WP : nullptr;
 #pragma unroll 4
     for (int e = tid; e < C * WP; e += NT) {
         const int i = e / WP, c = e % WP;
@@ -898,8 +920,12 @@ __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) chunk_rows(const float 
 #pragma unroll
         for (int k = 0; k < NS; ++k) {   // state rows f0 .. f0 + 63, 16 bytes at a time
             const int e = tid + NT * k, f = e / (WP / 4), c = 4 * (e % (WP / 4));
-            xs[k] = (e < FT * WP / 4 && f0 + f < r) ? *reinterpret_cast<const float4 *>(S + (size_t)(f0 + f) * WP + c)
-                                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+            const bool ok = e < FT * WP / 4 && f0 + f < r;
+            xs[k] = ok ? *reinterpret_cast<const float4 *>(S + (size_t)(f0 + f) * WP + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            if (FWD && O0 && ok) {
+                const float4 o = *reinterpret_cast<const float4 *>(O0 + (size_t)(f0 + f) * WP + c);
+                xs[k] = make_float4(xs[k].x + o.x, xs[k].y + o.y, xs[k].z + o.z, xs[k].w + o.w);
+            }
         }
     };
     float a[4][4] = {}, num[NG][4][4] = {}, den[4] = {};
@@ -1128,7 +1154,7 @@ int backward_dv(const T *q, const T *k, const T *v, const float *omega, const fl
         return FAVOR_ERR_CUDA;
     }
     // the forward states entering each chunk (causal: exclusive prefix) or the total (chunk slot 0)
-    state_scan<T, DV, false><<<sg2, 256, st_smem, st>>>(phik, v, nullptr, S, p.L, p.r, nch, nch, p.causal, 0);
+    state_scan<T, DV, false><<<sg2, 256, st_smem, st>>>(phik, v, nullptr, S, nullptr, p.L, p.r, nch, nch, p.causal, 0);
     if (nz > 1) state_sum<<<sb, 256, 0, st>>>(S, nch, nz, per, p.BH);
     FAVOR_LAUNCH_CHECK();
     {
@@ -1138,12 +1164,12 @@ int backward_dv(const T *q, const T *k, const T *v, const float *omega, const fl
             cudaGetLastError();
             return FAVOR_ERR_CUDA;
         }
-        chunk_rows<T, DV, false, float><<<cg, 256, smem, st>>>(phiq, phik, v, S, g, Y, Am, nullptr, p.L, p.r, nch,
-                                                               p.causal);
+        chunk_rows<T, DV, false, float><<<cg, 256, smem, st>>>(phiq, phik, v, S, g, Y, Am, nullptr, nullptr, 1,
+                                                               p.L, p.r, nch, p.causal);
         FAVOR_LAUNCH_CHECK();
     }
     // the states leaving each chunk (causal: exclusive suffix) or the total
-    state_scan<T, DV, true><<<sg2, 256, st_smem, st>>>(phiq, v, Y, R, p.L, p.r, nch, nch, p.causal, 1);
+    state_scan<T, DV, true><<<sg2, 256, st_smem, st>>>(phiq, v, Y, R, nullptr, p.L, p.r, nch, nch, p.causal, 1);
     if (nz > 1) state_sum<<<sb, 256, 0, st>>>(R, nch, nz, per, p.BH);
     FAVOR_LAUNCH_CHECK();
     {
@@ -1222,11 +1248,18 @@ int forward_dv(const T *q, const T *k, const T *v, const float *omega, void *out
                cudaStream_t st) {
     const size_t rows = (size_t)p.BH * p.L;
     const int nch = (p.L + kBwdRows - 1) / kBwdRows;
-    const int nz = p.causal ? 1 : std::min(nch, 8), nslot = p.causal ? nch : nz;
+    // ranges of chunks per head: non-causal, up to 8 (partial totals summed by
+    // state_sum); causal, enough for about one block per SM slot when the heads
+    // alone give fewer (each range's offset added by chunk_rows)
+    const int ntile = (p.r + 63) / 64, slots = 152 * (DV <= 64 ? 2 : 1);
+    const int nz = p.causal ? std::max(1, std::min(std::min(nch, 8), slots / std::max(1, ntile * p.BH)))
+                            : std::min(nch, 8);
+    const int nslot = p.causal ? nch : nz;
     const size_t per = (size_t)p.r * (DV + 4);
     size_t bytes = carve_bytes<float>(rows * p.nproj) + 2 * carve_bytes<float>(rows * p.r) +
                    2 * carve_bytes<float>(rows) + carve_bytes<float>(p.BH) +
-                   carve_bytes<float>((size_t)p.BH * nslot * per);
+                   carve_bytes<float>((size_t)p.BH * nslot * per) +
+                   (p.causal && nz > 1 ? carve_bytes<float>((size_t)p.BH * nz * per) : 0);
     int status = FAVOR_OK;
     void *ws = workspace(bytes, &status);
     if (!ws) return status;
@@ -1236,6 +1269,7 @@ int forward_dv(const T *q, const T *k, const T *v, const float *omega, void *out
     float *lsq = cv.take<float>(rows), *lsk = cv.take<float>(rows);
     float *hmax = cv.take<float>(p.BH);
     float *S = cv.take<float>((size_t)p.BH * nslot * per);
+    float *tot = p.causal && nz > 1 ? cv.take<float>((size_t)p.BH * nz * per) : nullptr;
 
     int rc = features_into<T>(q, omega, P, phiq, lsq, p, st);
     if (rc) return rc;
@@ -1257,18 +1291,24 @@ int forward_dv(const T *q, const T *k, const T *v, const float *omega, void *out
         cudaGetLastError();
         return FAVOR_ERR_CUDA;
     }
-    state_scan<T, DV, false><<<dim3((p.r + 63) / 64, p.BH, nz), 256, st_smem, st>>>(phik, v, nullptr, S, p.L, p.r,
-                                                                                    nch, nslot, p.causal, 0);
-    if (nz > 1) state_sum<<<(unsigned)((per * p.BH + 255) / 256), 256, 0, st>>>(S, nslot, nz, per, p.BH);
+    state_scan<T, DV, false><<<dim3((p.r + 63) / 64, p.BH, nz), 256, st_smem, st>>>(phik, v, nullptr, S, tot, p.L,
+                                                                                    p.r, nch, nslot, p.causal, 0);
+    if (nz > 1) {
+        const unsigned sb = (unsigned)((per * p.BH + 255) / 256);
+        if (p.causal) range_offsets<<<sb, 256, 0, st>>>(tot, nz, per, p.BH);
+        else state_sum<<<sb, 256, 0, st>>>(S, nslot, nz, per, p.BH);
+    }
     FAVOR_LAUNCH_CHECK();
     const dim3 cg(nch, p.BH);
     stats_begin(st, "chunk_rows");
     if (p.out_bf16)
         chunk_rows<T, DV, true, __nv_bfloat16><<<cg, 256, rw_smem, st>>>(
-            phiq, phik, v, S, nullptr, nullptr, nullptr, static_cast<__nv_bfloat16 *>(out), p.L, p.r, nslot, p.causal);
+            phiq, phik, v, S, nullptr, nullptr, nullptr, static_cast<__nv_bfloat16 *>(out), tot, nz, p.L, p.r, nslot,
+            p.causal);
     else
         chunk_rows<T, DV, true, float><<<cg, 256, rw_smem, st>>>(phiq, phik, v, S, nullptr, nullptr, nullptr,
-                                                                 static_cast<float *>(out), p.L, p.r, nslot, p.causal);
+                                                                 static_cast<float *>(out), tot, nz, p.L, p.r, nslot,
+                                                                 p.causal);
     stats_end(st);
     FAVOR_LAUNCH_CHECK();
     return FAVOR_OK;
