@@ -34,6 +34,13 @@ __device__ __forceinline__ float load_in(const float *p, size_t i) { return p[i]
 __device__ __forceinline__ float load_in(const uint16_t *p, size_t i) {
     return __uint_as_float(static_cast<uint32_t>(p[i]) << 16);
 }
+// four consecutive input elements (i % 4 == 0; 16-byte fp32 or 8-byte bf16 loads)
+__device__ __forceinline__ float4 load4_in(const float *p, size_t i) { return *reinterpret_cast<const float4 *>(p + i); }
+__device__ __forceinline__ float4 load4_in(const uint16_t *p, size_t i) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(p + i);
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y << 16),
+                       __uint_as_float(u.y & 0xffff0000u));
+}
 // an input element's bits, converted later (a prefetch that converts at once
 // waits for its load there)
 __device__ __forceinline__ uint32_t load_raw(const float *p, size_t i) { return __float_as_uint(p[i]); }
@@ -144,17 +151,26 @@ __global__ void __launch_bounds__(256) simt_project(const T *__restrict__ x, con
     const int t0 = blockIdx.x * TT, n0 = blockIdx.y * NT;
     const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
     const T *xb = x + (size_t)bh * L * D;
-#pragma unroll 4
-    for (int e = tid; e < TT * D; e += 256) {
-        const int t = e / D, j = e % D;
-        xs[t * DP + j] = t0 + t < L ? load_in(xb, (size_t)(t0 + t) * D + j) : 0.f;
+    // 4 values per load (rows of D values: D % 4 == 0)
+#pragma unroll
+    for (int e = tid; e < TT * D / 4; e += 256) {
+        const int t = e / (D / 4), j = 4 * (e % (D / 4));
+        *reinterpret_cast<float4 *>(xs + t * DP + j) =
+            t0 + t < L ? load4_in(xb, (size_t)(t0 + t) * D + j) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-#pragma unroll 4
-    for (int e = tid; e < NT * D; e += 256) {
-        const int n = e / D, j = e % D;
-        float w = 0.f;
-        if (n0 + n < nproj) w = identity ? (n0 + n == j ? 1.f : 0.f) : omega[((size_t)h * nproj + n0 + n) * D + j];
-        ws[n * DP + j] = w;
+#pragma unroll
+    for (int e = tid; e < NT * D / 4; e += 256) {
+        const int n = e / (D / 4), j = 4 * (e % (D / 4));
+        float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (n0 + n < nproj) {
+            if (identity) {
+                const int c = n0 + n - j;   // the 1 of row n0 + n, if among columns j .. j + 3
+                w = make_float4(c == 0, c == 1, c == 2, c == 3);
+            } else {
+                w = *reinterpret_cast<const float4 *>(omega + ((size_t)h * nproj + n0 + n) * D + j);
+            }
+        }
+        *reinterpret_cast<float4 *>(ws + n * DP + j) = w;
     }
     __syncthreads();
     float acc[4][4] = {};
