@@ -41,13 +41,18 @@ __device__ __forceinline__ float4 load4_in(const uint16_t *p, size_t i) {
     return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y << 16),
                        __uint_as_float(u.y & 0xffff0000u));
 }
-// an input element's bits, converted later (a prefetch that converts at once
-// waits for its load there)
-__device__ __forceinline__ uint32_t load_raw(const float *p, size_t i) { return __float_as_uint(p[i]); }
-__device__ __forceinline__ uint32_t load_raw(const uint16_t *p, size_t i) { return p[i]; }
+// the bits of four consecutive input elements (i % 4 == 0), converted later
+// (a prefetch that converts at once waits for its load there)
+__device__ __forceinline__ uint4 load4_raw(const float *p, size_t i) { return *reinterpret_cast<const uint4 *>(p + i); }
+__device__ __forceinline__ uint4 load4_raw(const uint16_t *p, size_t i) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(p + i);
+    return make_uint4(u.x, u.y, 0u, 0u);
+}
 template <typename T>
-__device__ __forceinline__ float from_raw(uint32_t b) {
-    return sizeof(T) == 4 ? __uint_as_float(b) : __uint_as_float(b << 16);
+__device__ __forceinline__ float4 from_raw4(uint4 b) {
+    if (sizeof(T) == 4) return make_float4(__uint_as_float(b.x), __uint_as_float(b.y), __uint_as_float(b.z), __uint_as_float(b.w));
+    return make_float4(__uint_as_float(b.x << 16), __uint_as_float(b.x & 0xffff0000u), __uint_as_float(b.y << 16),
+                       __uint_as_float(b.y & 0xffff0000u));
 }
 __device__ __forceinline__ void store_out(float *p, size_t i, float v) { p[i] = v; }
 __device__ __forceinline__ void store_out(__nv_bfloat16 *p, size_t i, float v) { p[i] = __float2bfloat16_rn(v); }
@@ -726,9 +731,10 @@ __global__ void __launch_bounds__(256) bwd_dx(float *__restrict__ C, const float
             const int j = 64 * gi + 4 * tx;
             if (j >= D) continue;
             const size_t o = (row0 + i) * D + j;
+            const float4 xv = load4_in(x, o);
             *reinterpret_cast<float4 *>(dx + o) =
-                make_float4(fmaf(term, load_in(x, o), acc[gi][u][0]), fmaf(term, load_in(x, o + 1), acc[gi][u][1]),
-                            fmaf(term, load_in(x, o + 2), acc[gi][u][2]), fmaf(term, load_in(x, o + 3), acc[gi][u][3]));
+                make_float4(fmaf(term, xv.x, acc[gi][u][0]), fmaf(term, xv.y, acc[gi][u][1]),
+                            fmaf(term, xv.z, acc[gi][u][2]), fmaf(term, xv.w, acc[gi][u][3]));
         }
     }
 }
@@ -753,16 +759,17 @@ __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) state_scan(const float 
                                                      const float *__restrict__ Y, float *__restrict__ S,
                                                      float *__restrict__ tot, int L, int r, int nch, int nslot,
                                                      int causal, int reverse) {
-    constexpr int C = kBwdRows, FT = 64, P = FT + 4, W = DV + 1, WP = DV + 4, NG = (DV + 63) / 64, NT = 256;
-    constexpr int NX = C * FT / 4 / NT, NY = (C * W + NT - 1) / NT;
+    constexpr int C = kBwdRows, FT = 64, P = FT + 4, WP = DV + 4, NG = (DV + 63) / 64, NT = 256;
+    constexpr int NX = C * FT / 4 / NT;
     extern __shared__ float4 sm4[];
     float *Ps = reinterpret_cast<float *>(sm4);   // [C][P]  phi rows x this block's 64 features
     float *Ys = Ps + C * P;                       // [C][WP] Yc | 0
     const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
     const int f0 = blockIdx.x * FT, bh = blockIdx.y;
-    constexpr int NY4 = (C * WP / 4 + NT - 1) / NT;
+    constexpr int NY4 = (C * WP / 4 + NT - 1) / NT, NV4 = (C * DV / 4 + NT - 1) / NT;
     float4 xp[NX], xy4[YIN ? NY4 : 1];   // Y rows (pitch WP), 16 bytes at a time
-    uint32_t xy[YIN ? 1 : NY];           // v bits (converted when put in shared memory)
+    uint4 xv[YIN ? 1 : NV4];             // v rows, 4 values a load (bits, converted when put)
+    int nstaged = 0;                     // valid rows of the staged chunk
     auto fetch = [&](int ch) {
         const int t0 = ch * C, n = min(C, L - t0);
         const size_t row0 = (size_t)bh * L + t0;
@@ -781,18 +788,12 @@ __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) state_scan(const float 
             }
         } else {
 #pragma unroll
-            for (int k = 0; k < NY; ++k) {
-                const int e = tid + NT * k, i = e / W, c = e % W;
-                uint32_t y = 0u;   // rows past the end: 0 (and the v | 1 rows' 1 only for valid rows)
-                if (e < C * W && i < n) y = c < DV ? load_raw(v, (row0 + i) * DV + c) : 1u;
-                xy[k] = y;
+            for (int k = 0; k < NV4; ++k) {
+                const int e = tid + NT * k, i = e / (DV / 4), c = 4 * (e % (DV / 4));
+                xv[k] = (e < C * DV / 4 && i < n) ? load4_raw(v, (row0 + i) * DV + c) : make_uint4(0u, 0u, 0u, 0u);
             }
+            nstaged = n;
         }
-    };
-    // the staged v bits as values, the ones column (bits 1) as 1
-    auto y_of = [&](int e, uint32_t b) -> float {
-        if (e % W == DV) return b ? 1.f : 0.f;
-        return from_raw<T>(b);
     };
     for (int e = tid; e < C * WP; e += NT) Ys[e] = 0.f;   // pad columns stay zero
     float acc[NG][4][4] = {}, zc[4] = {};   // zc: the last column (every tx holds it)
@@ -831,10 +832,11 @@ __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) state_scan(const float 
             }
         } else {
 #pragma unroll
-            for (int k = 0; k < NY; ++k) {
-                const int e = tid + NT * k;
-                if (e < C * W) Ys[(e / W) * WP + e % W] = y_of(e, xy[k]);
+            for (int k = 0; k < NV4; ++k) {
+                const int e = tid + NT * k, i = e / (DV / 4), c = 4 * (e % (DV / 4));
+                if (e < C * DV / 4) *reinterpret_cast<float4 *>(Ys + i * WP + c) = from_raw4<T>(xv[k]);
             }
+            if (tid < C) Ys[tid * WP + DV] = tid < nstaged ? 1.f : 0.f;   // the ones column (pads stay 0)
         }
         __syncthreads();
         if (it + 1 < c_n) fetch(reverse ? ch - 1 : ch + 1);
@@ -1048,7 +1050,7 @@ __global__ void __launch_bounds__(256) bwd_dw(const float *__restrict__ Cq, cons
     const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
     const int p0 = blockIdx.x * PT, h = blockIdx.z;
     float4 rc[NC];
-    uint32_t rx[NXD][4];   // input bits, converted when put in shared memory
+    uint4 rx[NXD];   // input bits, converted when put in shared memory
     auto fetch = [&](int it) {   // sub-slice it / 2 of side it % 2
         const int side = it & 1, r0 = (blockIdx.y * SUB + (it >> 1)) * RS;
         const float *Cm = side ? Ck : Cq;
@@ -1066,12 +1068,10 @@ __global__ void __launch_bounds__(256) bwd_dw(const float *__restrict__ Cq, cons
 #pragma unroll
         for (int kk = 0; kk < NXD; ++kk) {
             const int e = tid + NT * kk, i = e / (D / 4), j = 4 * (e % (D / 4)), t = r0 + i;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) rx[kk][c] = 0u;
+            rx[kk] = make_uint4(0u, 0u, 0u, 0u);
             if (e < RS * D / 4 && t < B * L) {
                 const size_t row = ((size_t)(t / L) * H + h) * L + t % L;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) rx[kk][c] = load_raw(X, row * D + j + c);
+                rx[kk] = load4_raw(X, row * D + j);
             }
         }
     };
@@ -1087,9 +1087,7 @@ __global__ void __launch_bounds__(256) bwd_dw(const float *__restrict__ Cq, cons
 #pragma unroll
         for (int kk = 0; kk < NXD; ++kk) {
             const int e = tid + NT * kk, i = e / (D / 4), j = 4 * (e % (D / 4));
-            if (e < RS * D / 4)
-                *reinterpret_cast<float4 *>(Xs + i * DP + j) = make_float4(
-                    from_raw<T>(rx[kk][0]), from_raw<T>(rx[kk][1]), from_raw<T>(rx[kk][2]), from_raw<T>(rx[kk][3]));
+            if (e < RS * D / 4) *reinterpret_cast<float4 *>(Xs + i * DP + j) = from_raw4<T>(rx[kk]);
         }
         __syncthreads();
         if (it + 1 < 2 * SUB) fetch(it + 1);
