@@ -907,8 +907,16 @@ __global__ void state_sum(float *__restrict__ S, int nslot, int nz, size_t per, 
 // threads, 64-feature tiles read a tile ahead into registers:
 //   num = phi_q S[:, :dv] (+ A_m V),  den = phi_q z (+ A_m 1),
 //   A_m = (phi_q phi_k^T) masked to j <= i
+// The forward instance at dv = 128 reads each tile straight into shared memory
+// instead of a tile ahead into registers: without the staged tile it fits 128
+// registers, so two blocks share an SM and hide each other's load latency.
+template <int DV, bool FWD>
+__host__ __device__ constexpr bool chunk_rows_staged() {
+    return !(FWD && DV > 64);
+}
+
 template <typename T, int DV, bool FWD, typename O>
-__global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) chunk_rows(const float *__restrict__ phiq, const float *__restrict__ phik,
+__global__ void __launch_bounds__(256, (DV <= 64 || !chunk_rows_staged<DV, FWD>()) ? 2 : 1) chunk_rows(const float *__restrict__ phiq, const float *__restrict__ phik,
                                                 const T *__restrict__ v, const float *__restrict__ Sin,
                                                 const float *__restrict__ g, float *__restrict__ Y,
                                                 float *__restrict__ Am, O *__restrict__ out,
@@ -933,44 +941,63 @@ __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) chunk_rows(const float 
         Vs[e] = (i < n && c < W) ? (c < DV ? load_in(v, (row0 + i) * DV + c) : 1.f) : 0.f;
     }
     constexpr int NX = C * FT / 4 / NT, NS = (FT * WP / 4 + NT - 1) / NT;
-    float4 xq[NX], xk[NX], xs[NS];
+    constexpr bool STAGED = chunk_rows_staged<DV, FWD>();
+    // the 16-byte pieces of a feature tile f0 that thread tid moves: phi_q and
+    // phi_k rows (k < NX), state rows f0 .. f0 + 63 with the range offset (k < NS)
+    const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    auto q4 = [&](int k, int f0) {
+        const int e = tid + NT * k, i = e / (FT / 4), f = 4 * (e % (FT / 4));
+        return (i < n && f0 + f < r) ? *reinterpret_cast<const float4 *>(phiq + (row0 + i) * r + f0 + f) : zero4;
+    };
+    auto k4 = [&](int k, int f0) {
+        const int e = tid + NT * k, i = e / (FT / 4), f = 4 * (e % (FT / 4));
+        return (causal && i < n && f0 + f < r) ? *reinterpret_cast<const float4 *>(phik + (row0 + i) * r + f0 + f)
+                                                : zero4;   // r % 4 == 0
+    };
+    auto s4 = [&](int k, int f0) {
+        const int e = tid + NT * k, f = e / (WP / 4), c = 4 * (e % (WP / 4));
+        if (e >= FT * WP / 4 || f0 + f >= r) return zero4;
+        float4 x = *reinterpret_cast<const float4 *>(S + (size_t)(f0 + f) * WP + c);
+        if (FWD && O0) {
+            const float4 o = *reinterpret_cast<const float4 *>(O0 + (size_t)(f0 + f) * WP + c);
+            x = make_float4(x.x + o.x, x.y + o.y, x.z + o.z, x.w + o.w);
+        }
+        return x;
+    };
+    float4 xq[STAGED ? NX : 1], xk[STAGED ? NX : 1], xs[STAGED ? NS : 1];
     auto fetch = [&](int f0) {
 #pragma unroll
         for (int k = 0; k < NX; ++k) {
-            const int e = tid + NT * k, i = e / (FT / 4), f = 4 * (e % (FT / 4));
-            const bool ok = i < n && f0 + f < r;   // r % 4 == 0
-            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-            xq[k] = ok ? *reinterpret_cast<const float4 *>(phiq + (row0 + i) * r + f0 + f) : z;
-            xk[k] = (ok && causal) ? *reinterpret_cast<const float4 *>(phik + (row0 + i) * r + f0 + f) : z;
+            xq[k] = q4(k, f0);
+            xk[k] = k4(k, f0);
         }
 #pragma unroll
-        for (int k = 0; k < NS; ++k) {   // state rows f0 .. f0 + 63, 16 bytes at a time
-            const int e = tid + NT * k, f = e / (WP / 4), c = 4 * (e % (WP / 4));
-            const bool ok = e < FT * WP / 4 && f0 + f < r;
-            xs[k] = ok ? *reinterpret_cast<const float4 *>(S + (size_t)(f0 + f) * WP + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-            if (FWD && O0 && ok) {
-                const float4 o = *reinterpret_cast<const float4 *>(O0 + (size_t)(f0 + f) * WP + c);
-                xs[k] = make_float4(xs[k].x + o.x, xs[k].y + o.y, xs[k].z + o.z, xs[k].w + o.w);
-            }
-        }
+        for (int k = 0; k < NS; ++k) xs[k] = s4(k, f0);
     };
     float a[4][4] = {}, num[NG][4][4] = {}, den[4] = {};
-    fetch(0);
+    if constexpr (STAGED) fetch(0);
     for (int f0 = 0; f0 < r; f0 += FT) {
         __syncthreads();
 #pragma unroll
         for (int k = 0; k < NX; ++k) {
             const int e = tid + NT * k, i = e / (FT / 4), f = 4 * (e % (FT / 4));
-            *reinterpret_cast<float4 *>(Qt + i * P + f) = xq[k];
-            *reinterpret_cast<float4 *>(Kt + i * P + f) = xk[k];
+            if constexpr (STAGED) {
+                *reinterpret_cast<float4 *>(Qt + i * P + f) = xq[k];
+                *reinterpret_cast<float4 *>(Kt + i * P + f) = xk[k];
+            } else {
+                *reinterpret_cast<float4 *>(Qt + i * P + f) = q4(k, f0);
+                *reinterpret_cast<float4 *>(Kt + i * P + f) = k4(k, f0);
+            }
         }
 #pragma unroll
         for (int k = 0; k < NS; ++k) {
             const int e = tid + NT * k;
-            if (e < FT * WP / 4) *reinterpret_cast<float4 *>(Ss + 4 * e) = xs[k];   // [FT][WP], same pitch
+            if (e < FT * WP / 4)   // [FT][WP], same pitch
+                *reinterpret_cast<float4 *>(Ss + 4 * e) = STAGED ? xs[k] : s4(k, f0);
         }
         __syncthreads();
-        if (f0 + FT < r) fetch(f0 + FT);
+        if constexpr (STAGED)
+            if (f0 + FT < r) fetch(f0 + FT);
         if (causal) mm_nt(a, Qt, P, Kt, P, FT, ty, tx);
 #pragma unroll
         for (int gi = 0; gi < NG; ++gi)
