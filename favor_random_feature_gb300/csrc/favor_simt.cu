@@ -762,8 +762,16 @@ __global__ void __launch_bounds__(256) bwd_dx(float *__restrict__ C, const float
 // the current one is added; thread (ty, tx) owns features 4 ty + u and columns
 // 4 tx + w (+ 64 per group) of the running state, and every thread the last
 // column (sum of phi, or of phi dden) of its features.
+// The instance that reads v at dv = 128 loads each chunk straight into shared
+// memory instead: without the staged chunk it fits 128 registers, two blocks
+// per SM, and the forward pass gives it twice the chunk ranges.
+template <int DV, bool YIN>
+__host__ __device__ constexpr bool state_scan_staged() {
+    return YIN || DV <= 64;
+}
+
 template <typename T, int DV, bool YIN>
-__global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) state_scan(const float *__restrict__ phi, const T *__restrict__ v,
+__global__ void __launch_bounds__(256, (DV <= 64 || !state_scan_staged<DV, YIN>()) ? 2 : 1) state_scan(const float *__restrict__ phi, const T *__restrict__ v,
                                                      const float *__restrict__ Y, float *__restrict__ S,
                                                      float *__restrict__ tot, int L, int r, int nch, int nslot,
                                                      int causal, int reverse) {
@@ -775,18 +783,25 @@ __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) state_scan(const float 
     const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
     const int f0 = blockIdx.x * FT, bh = blockIdx.y;
     constexpr int NY4 = (C * WP / 4 + NT - 1) / NT, NV4 = (C * DV / 4 + NT - 1) / NT;
-    float4 xp[NX], xy4[YIN ? NY4 : 1];   // Y rows (pitch WP), 16 bytes at a time
-    uint4 xv[YIN ? 1 : NV4];             // v rows, 4 values a load (bits, converted when put)
-    int nstaged = 0;                     // valid rows of the staged chunk
+    constexpr bool STAGED = state_scan_staged<DV, YIN>();
+    // the 16-byte pieces of chunk ch that thread tid moves: phi rows (k < NX), v rows (k < NV4)
+    auto p4 = [&](int k, int ch) {
+        const int t0 = ch * C, n = min(C, L - t0), e = tid + NT * k, i = e / (FT / 4), f = 4 * (e % (FT / 4));
+        return (i < n && f0 + f < r) ? *reinterpret_cast<const float4 *>(phi + ((size_t)bh * L + t0 + i) * r + f0 + f)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);   // r % 4 == 0
+    };
+    auto v4 = [&](int k, int ch) {
+        const int t0 = ch * C, n = min(C, L - t0), e = tid + NT * k, i = e / (DV / 4), c = 4 * (e % (DV / 4));
+        return (e < C * DV / 4 && i < n) ? load4_raw(v, ((size_t)bh * L + t0 + i) * DV + c) : make_uint4(0u, 0u, 0u, 0u);
+    };
+    float4 xp[STAGED ? NX : 1], xy4[YIN ? NY4 : 1];   // Y rows (pitch WP), 16 bytes at a time
+    uint4 xv[(YIN || !STAGED) ? 1 : NV4];             // v rows, 4 values a load (bits, converted when put)
+    int nstaged = 0;                                  // valid rows of the staged chunk
     auto fetch = [&](int ch) {
         const int t0 = ch * C, n = min(C, L - t0);
         const size_t row0 = (size_t)bh * L + t0;
 #pragma unroll
-        for (int k = 0; k < NX; ++k) {
-            const int e = tid + NT * k, i = e / (FT / 4), f = 4 * (e % (FT / 4));
-            xp[k] = (i < n && f0 + f < r) ? *reinterpret_cast<const float4 *>(phi + (row0 + i) * r + f0 + f)
-                                          : make_float4(0.f, 0.f, 0.f, 0.f);   // r % 4 == 0
-        }
+        for (int k = 0; k < NX; ++k) xp[k] = p4(k, ch);
         if constexpr (YIN) {
 #pragma unroll
             for (int k = 0; k < NY4; ++k) {
@@ -796,10 +811,7 @@ __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) state_scan(const float 
             }
         } else {
 #pragma unroll
-            for (int k = 0; k < NV4; ++k) {
-                const int e = tid + NT * k, i = e / (DV / 4), c = 4 * (e % (DV / 4));
-                xv[k] = (e < C * DV / 4 && i < n) ? load4_raw(v, (row0 + i) * DV + c) : make_uint4(0u, 0u, 0u, 0u);
-            }
+            for (int k = 0; k < NV4; ++k) xv[k] = v4(k, ch);
             nstaged = n;
         }
     };
@@ -823,14 +835,15 @@ __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) state_scan(const float 
     };
     // this block's chunks: all (causal) or the z-th range (non-causal)
     const int per_z = (nch + gridDim.z - 1) / gridDim.z, c_lo = blockIdx.z * per_z, c_n = min(nch, c_lo + per_z) - c_lo;
-    if (c_n > 0) fetch(reverse ? c_lo + c_n - 1 : c_lo);
+    if constexpr (STAGED)
+        if (c_n > 0) fetch(reverse ? c_lo + c_n - 1 : c_lo);
     for (int it = 0; it < c_n; ++it) {
         const int ch = reverse ? c_lo + c_n - 1 - it : c_lo + it;
         __syncthreads();
 #pragma unroll
         for (int k = 0; k < NX; ++k) {
             const int e = tid + NT * k, i = e / (FT / 4), f = 4 * (e % (FT / 4));
-            *reinterpret_cast<float4 *>(Ps + i * P + f) = xp[k];
+            *reinterpret_cast<float4 *>(Ps + i * P + f) = STAGED ? xp[k] : p4(k, ch);
         }
         if constexpr (YIN) {
 #pragma unroll
@@ -842,12 +855,14 @@ __global__ void __launch_bounds__(256, DV <= 64 ? 2 : 1) state_scan(const float 
 #pragma unroll
             for (int k = 0; k < NV4; ++k) {
                 const int e = tid + NT * k, i = e / (DV / 4), c = 4 * (e % (DV / 4));
-                if (e < C * DV / 4) *reinterpret_cast<float4 *>(Ys + i * WP + c) = from_raw4<T>(xv[k]);
+                if (e < C * DV / 4) *reinterpret_cast<float4 *>(Ys + i * WP + c) = from_raw4<T>(STAGED ? xv[k] : v4(k, ch));
             }
-            if (tid < C) Ys[tid * WP + DV] = tid < nstaged ? 1.f : 0.f;   // the ones column (pads stay 0)
+            const int nrows = STAGED ? nstaged : min(C, L - ch * C);
+            if (tid < C) Ys[tid * WP + DV] = tid < nrows ? 1.f : 0.f;   // the ones column (pads stay 0)
         }
         __syncthreads();
-        if (it + 1 < c_n) fetch(reverse ? ch - 1 : ch + 1);
+        if constexpr (STAGED)
+            if (it + 1 < c_n) fetch(reverse ? ch - 1 : ch + 1);
         if (causal) write_state(S + ((size_t)bh * nslot + ch) * r * WP);   // exclusive: before this chunk is added
         // acc[g][u][w] += sum_i phi[i][4 ty + u] Yc[i][64 g + 4 tx + w] and the last
         // column in the same pass over the rows (one more broadcast load per row)
@@ -1297,9 +1312,9 @@ int forward_dv(const T *q, const T *k, const T *v, const float *omega, void *out
     const size_t rows = (size_t)p.BH * p.L;
     const int nch = (p.L + kBwdRows - 1) / kBwdRows;
     // ranges of chunks per head: non-causal, up to 8 (partial totals summed by
-    // state_sum); causal, enough for about one block per SM slot when the heads
+    // state_sum); causal, enough for about one state_scan block per SM slot when the heads
     // alone give fewer (each range's offset added by chunk_rows)
-    const int ntile = (p.r + 63) / 64, slots = 152 * (DV <= 64 ? 2 : 1);
+    const int ntile = (p.r + 63) / 64, slots = 152 * 2;   // two state_scan blocks per SM at every dv
     const int nz = p.causal ? std::max(1, std::min(std::min(nch, 8), slots / std::max(1, ntile * p.BH)))
                             : std::min(nch, 8);
     const int nslot = p.causal ? nch : nz;
