@@ -48,7 +48,10 @@
  *   - Device pointers must be 16-byte aligned; out must not alias an input.
  *   - The caller owns every buffer and the stream.  The library owns a
  *     per-device workspace that it grows on demand (cudaMalloc outside any
- *     stream capture) and frees in favor_release_workspace().
+ *     stream capture) and frees in favor_release_workspace().  Every call on
+ *     a device uses that one workspace: calls whose kernels can overlap on
+ *     the GPU (streams with no ordering between them) race on it, so order
+ *     such calls with events or issue them on one stream.
  *   - Calls are asynchronous on `stream` (0 = legacy default stream) unless
  *     stated otherwise.  Argument errors are detected on the host and
  *     returned before anything is launched.  A launch failure returns
