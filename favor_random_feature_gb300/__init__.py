@@ -37,6 +37,7 @@ EXPORTS = (
     "favor_attn_forward_host",
     "favor_feature_map",
     "favor_get_device_status",
+    "favor_wait_expiry_check",
     "favor_strerror",
     "favor_release_workspace",
     "favor_feature_dim",
@@ -85,6 +86,8 @@ def lib() -> ctypes.CDLL:
         L.favor_feature_map.restype = i
         L.favor_get_device_status.argtypes = [vp]
         L.favor_get_device_status.restype = i
+        L.favor_wait_expiry_check.argtypes = [ctypes.c_longlong, vp]
+        L.favor_wait_expiry_check.restype = i
         L.favor_strerror.argtypes = [i]
         L.favor_strerror.restype = ctypes.c_char_p
         L.favor_release_workspace.argtypes = []
@@ -177,6 +180,10 @@ def favor_feature_map(x, omega, phi, log_scale, B, H, L, d, m, feature_map, is_k
 
 def favor_get_device_status(stream=None) -> int:
     return lib().favor_get_device_status(_stream(stream))
+
+
+def favor_wait_expiry_check(limit_cycles: int, stream=None) -> int:
+    return lib().favor_wait_expiry_check(int(limit_cycles), _stream(stream))
 
 
 def favor_release_workspace() -> None:

@@ -401,6 +401,13 @@ extern "C" int favor_get_device_status(cudaStream_t stream) {
     return h;
 }
 
+extern "C" int favor_wait_expiry_check(long long limit_cycles, cudaStream_t stream) {
+    if (limit_cycles < 1 || limit_cycles > (1ll << 31)) return FAVOR_ERR_INVALID_ARG;
+    int *sp = device_status_ptr();
+    if (!sp) return FAVOR_ERR_CUDA;
+    return tc_wait_expiry(limit_cycles, sp, stream);
+}
+
 extern "C" const char *favor_strerror(int status) {
     switch (status) {
         case FAVOR_OK: return "FAVOR_OK";

@@ -67,6 +67,9 @@ int tc_forward(const void *q, const void *k, const void *v, const float *omega, 
 // Scratch bytes the tensor-core path needs for a problem, and the path run on
 // caller-provided scratch (FAVOR_ERR_UNSUPPORTED if ws_bytes is too small).
 size_t tc_scratch_bytes(const Problem &p);
+// One bounded mbarrier wait that nothing completes: it runs out after
+// limit_cycles clock cycles and records FAVOR_ERR_TIMEOUT in *status.
+int tc_wait_expiry(long long limit_cycles, int *status, cudaStream_t st);
 int tc_run(const void *q, const void *k, const void *v, const float *omega, float *out,
            const Problem &p, cudaStream_t stream, void *ws, size_t ws_bytes);
 // The state of all L keys of each head (non-causal state pass, no output):

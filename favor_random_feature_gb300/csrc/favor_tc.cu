@@ -110,6 +110,18 @@ __device__ __forceinline__ void set_status(int *status, int code) {
     if (status) atomicExch(status, code);
 }
 
+// A bounded wait made to run out: one thread waits for the first phase of an
+// mbarrier that nothing arrives on, with the same bounded wait the pipelines
+// use.  It gives up after `limit` clock cycles and records the expiry the way
+// a stalled pipeline does, so the expiry path and the status word can be
+// checked without faulting or hanging anything.
+__global__ void __launch_bounds__(1) wait_expiry_kernel(int *status, long long limit) {
+    __shared__ __align__(8) uint64_t bar;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    if (!mbar_wait(&bar, 0, limit)) set_status(status, FAVOR_ERR_TIMEOUT);
+}
+
 // sin/cos with the argument first reduced to [-pi, pi] (Cody-Waite, 2pi split
 // in three parts) so that the hardware approximations stay accurate for
 // projections of any size met here.
@@ -1895,6 +1907,11 @@ int launch_state(const Problem &p, const Geo &g, const Plan &pl, const uint8_t *
 }  // namespace
 
 size_t tc_scratch_bytes(const Problem &p) { return make_plan(p).bytes; }
+
+int tc_wait_expiry(long long limit_cycles, int *status, cudaStream_t st) {
+    wait_expiry_kernel<<<1, 1, 0, st>>>(status, limit_cycles);
+    return cuda_status(cudaGetLastError());
+}
 
 int tc_key_state(const void *k, const void *v, const float *omega, const Problem &p0, cudaStream_t st,
                  const float **state_out, const float **meta_out, int *npieces) {

@@ -159,6 +159,18 @@ int favor_feature_map(const void *x, const float *omega, float *phi, float *log_
  * (FAVOR_OK or FAVOR_ERR_TIMEOUT), or FAVOR_ERR_CUDA if the sync failed. */
 int favor_get_device_status(cudaStream_t stream);
 
+/* No counterpart on the pages: a check of the library's failure detection.
+ * Launches one thread that waits, with the same bounded mbarrier wait the
+ * pipelines use, for a barrier phase that nothing completes.  After
+ * limit_cycles SM clock cycles (1 .. 2^31; 2^21 is about a millisecond) the
+ * wait gives up and records FAVOR_ERR_TIMEOUT in the device status word, as a
+ * stalled pipeline would; nothing faults, traps or hangs, and the context
+ * stays usable.  favor_get_device_status(stream) then returns (and clears)
+ * FAVOR_ERR_TIMEOUT.  Asynchronous on `stream`.  Returns FAVOR_OK,
+ * FAVOR_ERR_INVALID_ARG for a limit out of range (before any CUDA call), or
+ * FAVOR_ERR_CUDA. */
+int favor_wait_expiry_check(long long limit_cycles, cudaStream_t stream);
+
 /* Human-readable name of a favor_status_t value (static string). */
 const char *favor_strerror(int status);
 
