@@ -13,6 +13,7 @@ import os
 import re
 import subprocess
 import sys
+from concurrent.futures import ThreadPoolExecutor
 
 import pytest
 
@@ -88,21 +89,24 @@ def _mutated(name):
 
 @pytest.fixture(scope="module")
 def runs(tmp_path_factory):
-    """Build and run every mutant (and the control) in parallel child processes."""
+    """Build and run every mutant (and the control) in child processes, as many
+    at a time as the host has cores."""
     env = dict(os.environ, OMP_NUM_THREADS="1")
-    procs = {}
+    jobs = []
     for i, name in enumerate([None] + list(MUTANTS)):
         d = tmp_path_factory.mktemp(f"mutant{i}")
         src = d / "favor_oracle.c"
         src.write_text(_mutated(name))
-        procs[name] = subprocess.Popen(
-            [sys.executable, "-c", _DRIVER, ROOT, str(src), str(d / "_build")], cwd=ROOT, env=env,
-            stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
-    out = {}
-    for name, p in procs.items():
-        text, _ = p.communicate(timeout=900)
-        out[name] = (p.returncode, text)
-    return out
+        jobs.append((name, [sys.executable, "-c", _DRIVER, ROOT, str(src), str(d / "_build")]))
+
+    def run(job):
+        name, cmd = job
+        r = subprocess.run(cmd, cwd=ROOT, env=env, stdout=subprocess.PIPE, stderr=subprocess.STDOUT,
+                           text=True, timeout=900)
+        return name, (r.returncode, r.stdout)
+
+    with ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 1))) as pool:
+        return dict(pool.map(run, jobs))
 
 
 def test_unchanged_copy_passes_every_pin(runs):
