@@ -105,3 +105,23 @@ def test_noncausal_keys_left_out_of_the_state_are_rejected(noncausal, lo, hi):
         pk = oracle.features(inp.k32[0, h], inp.omega[h])[keep]
         out[0, h] = (pq @ (pk.T @ inp.v32[0, h][keep].astype(np.float64))) / (pq @ pk.sum(0))[:, None]
     assert not passes(row_errors(out, ref))
+
+
+def test_fp32_bar_admits_fp32_features_and_rejects_fp16_omega():
+    """The fp32 bar (max 1e-4) on the page's demo head (L = 64, d = 32, m = 256):
+    features rounded to fp32 pass it; omega rounded to fp16 (the tensor-core
+    operand precision) does not."""
+    from favor_inputs import DEMO64
+    inp = make_inputs(DEMO64)
+    q, k, v, om = inp.q32[0, 0], inp.k32[0, 0], inp.v32[0, 0].astype(np.float64), inp.omega[0]
+    ref = oracle.forward(inp.q32, inp.k32, inp.v32, inp.omega, causal=False)[0, 0]
+
+    def out_from(pq, pk):
+        return (pq @ (pk.T @ v)) / (pq @ pk.sum(0))[:, None]
+
+    f32 = lambda a: a.astype(np.float32).astype(np.float64)
+    e32 = row_errors(out_from(f32(oracle.features(q, om)), f32(oracle.features(k, om))), ref)
+    assert e32.max() <= 1e-4
+    om16 = om.astype(np.float16).astype(np.float32)
+    e16 = row_errors(out_from(oracle.features(q, om16), oracle.features(k, om16)), ref)
+    assert e16.max() > 1e-4
