@@ -22,6 +22,7 @@ FAVOR_ERR_UNSUPPORTED = -2
 FAVOR_ERR_CUDA = -3
 FAVOR_ERR_TIMEOUT = -4
 FAVOR_ERR_NOMEM = -5
+FAVOR_ERR_RANGE = -6
 
 FAVOR_MAP_POSITIVE = 0
 FAVOR_MAP_TRIG = 1
@@ -43,6 +44,7 @@ EXPORTS = (
     "favor_feature_dim",
     "favor_stats_enable",
     "favor_stats_read",
+    "favor_probe_ex2_rate",
     "favor_state_floats",
     "favor_attn_state",
     "favor_attn_state_f32",
@@ -98,6 +100,8 @@ def lib() -> ctypes.CDLL:
         L.favor_stats_enable.restype = i
         L.favor_stats_read.argtypes = [ctypes.POINTER(FavorStats)]
         L.favor_stats_read.restype = i
+        L.favor_probe_ex2_rate.argtypes = [ctypes.POINTER(ctypes.c_double), vp]
+        L.favor_probe_ex2_rate.restype = i
         L.favor_state_floats.argtypes = [i, i, i, i]
         L.favor_state_floats.restype = i
         for name in ("favor_attn_state", "favor_attn_state_f32"):
@@ -204,6 +208,15 @@ def favor_stats_read() -> FavorStats:
     if rc != FAVOR_OK:
         raise FavorError(rc, "favor_stats_read")
     return st
+
+
+def favor_probe_ex2_rate(stream=None) -> float:
+    """Exponentials per second of the current device (favor.h)."""
+    rate = ctypes.c_double(0.0)
+    rc = lib().favor_probe_ex2_rate(ctypes.byref(rate), _stream(stream))
+    if rc != FAVOR_OK:
+        raise FavorError(rc, "favor_probe_ex2_rate")
+    return rate.value
 
 
 def favor_state_floats(d, dv, m, feature_map) -> int:

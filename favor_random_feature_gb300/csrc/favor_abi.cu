@@ -416,8 +416,67 @@ extern "C" const char *favor_strerror(int status) {
         case FAVOR_ERR_CUDA: return "FAVOR_ERR_CUDA: CUDA runtime error";
         case FAVOR_ERR_TIMEOUT: return "FAVOR_ERR_TIMEOUT: bounded device wait expired";
         case FAVOR_ERR_NOMEM: return "FAVOR_ERR_NOMEM: workspace allocation failed";
+        case FAVOR_ERR_RANGE: return "FAVOR_ERR_RANGE: an input left the range of the fp16 tensor-core operands";
         default: return "unknown favor status";
     }
+}
+
+namespace favor {
+namespace {
+__device__ float g_ex2_sink;
+
+// eight independent ex2 chains per thread; the feedback (y = -ex2(y)) keeps
+// every operand in [-1, 0) and the chains alive
+__global__ void __launch_bounds__(256) ex2_rate_kernel(int iters) {
+    float a[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = -1.f - 1e-3f * (float)((threadIdx.x + i) & 63);
+    for (int it = 0; it < iters; ++it) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float y;
+            asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(a[i]));
+            a[i] = -y;
+        }
+    }
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s += a[i];
+    if (s > 0.f) g_ex2_sink = s;   // never true (s < 0): keeps the chains
+}
+}  // namespace
+}  // namespace favor
+
+extern "C" int favor_probe_ex2_rate(double *ex2_per_second, cudaStream_t stream) {
+    if (!ex2_per_second) return FAVOR_ERR_INVALID_ARG;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        return FAVOR_ERR_CUDA;
+    const int blocks = sms * 8, iters = 4096;
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
+        if (e0) cudaEventDestroy(e0);
+        return FAVOR_ERR_CUDA;
+    }
+    int rc = FAVOR_OK;
+    float best = 0.f;
+    for (int rep = 0; rep < 4 && rc == FAVOR_OK; ++rep) {   // the first run warms up
+        cudaEventRecord(e0, stream);
+        favor::ex2_rate_kernel<<<blocks, 256, 0, stream>>>(iters);
+        cudaEventRecord(e1, stream);
+        float ms = 0.f;
+        if (cudaGetLastError() != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess ||
+            cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess)
+            rc = FAVOR_ERR_CUDA;
+        else if (rep > 0 && (best == 0.f || ms < best))
+            best = ms;
+    }
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    if (rc) return rc;
+    *ex2_per_second = (double)blocks * 256 * iters * 8 / (best * 1e-3);
+    return FAVOR_OK;
 }
 
 extern "C" int favor_stats_enable(int enable) {

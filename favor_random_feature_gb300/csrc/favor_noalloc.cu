@@ -24,7 +24,7 @@
 namespace favor {
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;   // 16 MiB
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;   // 32 MiB
 constexpr int kMaxDev = 64;
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -64,8 +64,9 @@ extern "C" int favor_attn_forward_noalloc(const void *q, const void *k, const vo
     int rc = make_problem(B, H, L, d, dv, m, causal, feature_map, &p);
     if (rc) return rc;
     if ((rc = validate_args(q, k, v, omega, out, 2, p))) return rc;
-    if (!tc_supported(p)) return FAVOR_ERR_UNSUPPORTED;
+    // the size check first: it needs no device and touches no pointer
     if (tc_scratch_bytes(p) > kNoAllocScratchBytes) return FAVOR_ERR_UNSUPPORTED;
+    if (!tc_supported(p)) return FAVOR_ERR_UNSUPPORTED;
     void *scratch = nullptr;
     if ((rc = scratch_address(&scratch))) return rc;
     return tc_run(q, k, v, omega, out, p, stream, scratch, kNoAllocScratchBytes);

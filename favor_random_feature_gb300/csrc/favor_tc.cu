@@ -110,6 +110,22 @@ __device__ __forceinline__ void set_status(int *status, int code) {
     if (status) atomicExch(status, code);
 }
 
+// FAVOR_ERR_RANGE unless another error is already recorded: an input left
+// the range of the fp16 operands (the call still completes)
+__device__ __forceinline__ void flag_range(int *status) {
+    if (status) atomicCAS(status, FAVOR_OK, FAVOR_ERR_RANGE);
+}
+
+// the largest |x| that bf16 -> fp16 conversion keeps finite: 65280, the
+// largest bf16 value below fp16's 65504 (inf and larger values fail the test)
+constexpr float kMaxOperand = 65280.f;
+// The fp16 floor of a positive-feature denominator: every operand feature
+// carries an absolute rounding error of at most 2^-25 (subnormal spacing
+// 2^-24, halved), so a row whose denominator is below (keys) x (row sum of
+// its query features) x 2^-15 may have lost more than 2^-10 of it to
+// underflow.  For inputs inside the range this ratio stays above 2^-9.
+constexpr float kRangeFloor = 3.0517578125e-05f;   // 2^-15
+
 // A bounded wait made to run out: one thread waits for the first phase of an
 // mbarrier that nothing arrives on, with the same bounded wait the pipelines
 // use.  It gives up after `limit` clock cycles and records the expiry the way
@@ -122,12 +138,14 @@ __global__ void __launch_bounds__(1) wait_expiry_kernel(int *status, long long l
     if (!mbar_wait(&bar, 0, limit)) set_status(status, FAVOR_ERR_TIMEOUT);
 }
 
-// sin/cos with the argument first reduced to [-pi, pi] (Cody-Waite, 2pi split
-// in three parts) so that the hardware approximations stay accurate for
-// projections of any size met here.
+// sin/cos with the argument first reduced to [-pi, pi] (Cody-Waite) so that
+// the hardware approximations stay accurate for projections of any size met
+// here.  2pi = p1 + p2 + p3: p1 = 6.28125 has 8 significant bits, so n p1 is
+// exact for |n| < 2^16; p2 = fl(2pi - p1) and p3 = fl(2pi - p1 - p2), which
+// leaves a representation error of about 3e-19 per period.
 __device__ __forceinline__ void sincos_reduced(float x, float &s, float &c) {
     const float inv2pi = 0.15915494309189535f;
-    const float p1 = 6.28125f, p2 = 1.9353071795864769e-3f, p3 = 0.0f;
+    const float p1 = 6.28125f, p2 = 1.935307169e-3f, p3 = 1.025337627e-11f;
     float n = rintf(x * inv2pi);
     float t = fmaf(-n, p1, x);
     t = fmaf(-n, p2, t);
@@ -226,8 +244,8 @@ __device__ __forceinline__ float convert_tile_512(uint8_t *tile, int nblk, int e
 }
 
 // One 16-byte chunk (8 values) of a bf16 tile -> fp16 in place; returns the
-// chunk's sum of squares.
-__device__ __forceinline__ float cvt_chunk16_sq(uint8_t *p) {
+// chunk's sum of squares and raises amax to the chunk's largest |x|.
+__device__ __forceinline__ float cvt_chunk16_sq(uint8_t *p, float &amax) {
     uint4 u = *reinterpret_cast<uint4 *>(p);
     uint32_t w[4] = {u.x, u.y, u.z, u.w};
     float ss = 0.f;
@@ -235,6 +253,7 @@ __device__ __forceinline__ float cvt_chunk16_sq(uint8_t *p) {
     for (int i = 0; i < 4; ++i) {
         const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
         ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+        amax = fmax3(amax, fabsf(lo), fabsf(hi));
         w[i] = pack_half2(lo, hi);
     }
     *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -438,11 +457,12 @@ __device__ __forceinline__ void state_body(const CUtensorMap *tm_k, const CUtens
             bool ok = ewait(&bar_k[c % NSK], (c / NSK) & 1, abortp);
             uint8_t *tile = xk + (size_t)(c % NSK) * xkb;
             const int r = e >> 2, pp = e & 3;
-            float ss = 0.f;
+            float ss = 0.f, kmax = 0.f;
             for (int b = 0; b < nd; ++b)
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
-                    ss += cvt_chunk16_sq(tile + b * kBlk + r * 128 + (((2 * pp + h) ^ (r & 7)) << 4));
+                    ss += cvt_chunk16_sq(tile + b * kBlk + r * 128 + (((2 * pp + h) ^ (r & 7)) << 4), kmax);
+            if (kmax > kMaxOperand) flag_range(a.status);
             ss += __shfl_xor_sync(0xffffffffu, ss, 1);
             ss += __shfl_xor_sync(0xffffffffu, ss, 2);
             if (pp == 0) nk[(c % 3) * 128 + r] = 0.5f * kLog2e * ss;
@@ -561,6 +581,7 @@ __device__ __forceinline__ void state_body(const CUtensorMap *tm_k, const CUtens
         tc_fence_after();
         const bool write = alive && !*abortp;
         const float vm = grp_max(vmax, red, ew);
+        if (e == 0 && vm > kMaxOperand) flag_range(a.status);
         for (int t = 0; t < FT; ++t) {
             const int ft = fg * FT + t;
             const int f = ft * 128 + row;
@@ -720,12 +741,15 @@ __global__ void tc_combine(const CombineArgs a) {
         const int ftile = f / 128;
         const size_t e = (size_t)f * W + 8 * cg;
         if (cg * 8 == g.dv) {
-            // z atom: column 0 holds sigma z, columns 1..15 (the rest of the
+            // z atom: column 0 holds sigma z, column 1 sigma itself (its
+            // accumulator column is sigma times the row sum of the query
+            // features, for the range check), columns 2..15 (the rest of the
             // N = 80 operand) zero
             float sum = 0.f;
             for (int gi = 0; gi < upto; ++gi) sum += st[gi * per + e] * scale[gi * g.n_ft + ftile];
             uint8_t *za = img + (size_t)nvb * g.r * 128;
-            const uint32_t lo = __half_as_ushort(__float2half_rn(sum * sigma));
+            const uint32_t lo = __half_as_ushort(__float2half_rn(sum * sigma)) |
+                                ((uint32_t)__half_as_ushort(__float2half_rn(sigma)) << 16);
             *reinterpret_cast<uint4 *>(za + sw128_offset(f, 0)) = make_uint4(lo, 0u, 0u, 0u);
             *reinterpret_cast<uint4 *>(za + sw128_offset(f, 8)) = make_uint4(0u, 0u, 0u, 0u);
             continue;
@@ -764,9 +788,9 @@ __global__ void tc_combine(const CombineArgs a) {
 // chunk are written while the tensor core computes its P_K.
 // ---------------------------------------------------------------------------
 constexpr int kCausalThreads = 32 + kEpi;
-constexpr int kKbRows = 208;                     // phi_K 128 | sigma S^T 64 | sigma z 1 | pad 15
+constexpr int kKbRows = 208;                     // phi_K 128 | sigma S^T 64 | sigma z 1 | ones 1 | pad 14
 constexpr uint32_t kKbBlk = kKbRows * 128;       // one 64-feature block of the KB operand
-constexpr int kKbS = 128, kKbZ = 192;            // first rows of sigma S^T and sigma z
+constexpr int kKbS = 128, kKbZ = 192, kKbOne = 193;   // first rows of sigma S^T, sigma z, ones
 // small-area float offsets of the barriers, TMEM slot, abort flag; total size
 constexpr int kCausalBars = 1696, kCausalTslot = 1728, kCausalAbort = 1730, kCausalSmall = 1736;
 
@@ -949,10 +973,13 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
     const int e = threadIdx.x - 32, ew = e >> 5;
     const int q = (ew + 1) & 3, j = ew >> 2;
     const int row = q * 32 + lane;
-    // pad rows of every KB block: they feed accumulator columns never read
+    // the ones row (its accumulator column is the row sum of the query
+    // features, for the range check) and the pad rows after it (they feed
+    // accumulator columns never read)
     for (int i = e; i < (g.r / 64) * 15 * 8; i += kEpi) {
-        const int blk = i / 120, rr = kKbZ + 1 + (i % 120) / 8, ch = i % 8;
-        *reinterpret_cast<uint4 *>(kb + (size_t)blk * kKbBlk + rr * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+        const int blk = i / 120, rr = kKbOne + (i % 120) / 8, ch = i % 8;
+        const uint32_t one = rr == kKbOne ? 0x3C003C00u : 0u;
+        *reinterpret_cast<uint4 *>(kb + (size_t)blk * kKbBlk + rr * 128 + ch * 16) = make_uint4(one, one, one, one);
     }
     float R = MAP == FAVOR_MAP_POSITIVE ? -INFINITY : 0.f, zmax = 0.f, vmax = 0.f;
     float s0[16], s1[16], z0 = 0.f, z1 = 0.f;   // this thread's part of the initial state
@@ -1011,9 +1038,10 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
     };
     auto convert_x = [&](int c) -> bool {
         const bool ok_x = ewait(bar_x, c & 1, abortp);
-        float am;
-        convert_tile_512<false, false>(xq, nd, e, am);
-        const float ss = convert_tile_512<true, false>(xk, nd, e, am);
+        float am, am2;
+        convert_tile_512<false, true>(xq, nd, e, am);
+        const float ss = convert_tile_512<true, true>(xk, nd, e, am2);
+        if (fmaxf(am, am2) > kMaxOperand) flag_range(a.status);
         part3[(e >> 7) * 128 + (e & 127)] = ss;
         group_sync(kEpi);
         if (e < 128) nk[e] = 0.5f * kLog2e * ((part3[e] + part3[128 + e]) + (part3[256 + e] + part3[384 + e]));
@@ -1239,6 +1267,7 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
         {
             float am;
             convert_tile_512<false, true>(xv, 1, e, am);
+            if (am > kMaxOperand) flag_range(a.status);
             fence_async_smem();
             mbar_arrive(e_v);
             // warp partials of max |v| and of the key mass (sum over keys of the
@@ -1307,15 +1336,22 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
         alive &= ewait(bar_av, ph, abortp);
         tc_fence_after();
         {
-            float di[16], dx[16], ddi, ddx;
+            float di[16], dx[16], ddi, ddx, qsum = 0.f;
             tmem_ld16(tm_addr(tmem, q, kColDI + 16 * j), di);
             tmem_ld16(tm_addr(tmem, q, kColDX + 16 * j), dx);
             tmem_ld1(tm_addr(tmem, q, kColDI + 64), ddi);
             tmem_ld1(tm_addr(tmem, q, kColDD), ddx);
+            if (j == 0) tmem_ld1(tm_addr(tmem, q, kColDD + 1), qsum);
             tmem_ld_wait();
             tc_fence_before();
             const float is = pow2_inv_floor(sigma), ir = pow2_inv_floor(rho);   // exact: powers of two
-            const float id = __fdividef(1.f, fmaf(ddi, ir, ddx * is));
+            const float den = fmaf(ddi, ir, ddx * is);
+            const float id = __fdividef(1.f, den);
+            // the range check: the denominator against the features' fp16
+            // floor (keys so far x the row sum of the query features x the
+            // flush level, with a 2^10 margin)
+            if (MAP == FAVOR_MAP_POSITIVE && j == 0 && ok && den < (float)(tc0 + row + 1) * qsum * kRangeFloor)
+                flag_range(a.status);
             if constexpr (OB16) {
                 // output columns 16 j .. 16 j + 15 -> the bf16 staging block
                 // (phi_K rows of KB block 0, free since the state update)
@@ -1519,7 +1555,8 @@ __device__ void output_body(const OutputArgs &a, uint8_t *sm, uint32_t tmem,
     auto convert_x = [&](int i) -> bool {
         const bool ok = ewait(&bar_x[i % nq], (i / nq) & 1, abortp);
         float am;
-        convert_tile_512<false, false>(xs + (size_t)(i % nq) * xb, nd, e, am);
+        convert_tile_512<false, true>(xs + (size_t)(i % nq) * xb, nd, e, am);
+        if (am > kMaxOperand) flag_range(a.status);
         tc_fence_before();
         fence_async_smem();
         mbar_arrive(e_x);
@@ -1593,10 +1630,16 @@ __device__ void output_body(const OutputArgs &a, uint8_t *sm, uint32_t tmem,
         // ---- output ----
         alive &= ewait(bar_d, i & 1, abortp);
         tc_fence_after();
-        float dn[16], dd;
+        float dn[16], dd, qs = 0.f;
         tmem_ld16(tm_addr(tmem, q, kColD + 16 * j), dn);
         tmem_ld1(tm_addr(tmem, q, kColD + 64), dd);
+        if (j == 0) tmem_ld1(tm_addr(tmem, q, kColD + 65), qs);
         tmem_ld_wait();
+        // the range check (sigma cancels: column 65 holds sigma x the row sum
+        // of the query features)
+        if (MAP == FAVOR_MAP_POSITIVE && j == 0 && unit_c(u) * kC + row < a.L &&
+            dd < (float)a.L * qs * kRangeFloor)
+            flag_range(a.status);
         if (e == 0) bulk_wait_read0();   // the previous unit's staging has been read
         group_sync(kEpi);
         {
@@ -1875,7 +1918,9 @@ Plan make_plan(const Problem &p) {
     size_t bytes = carve_bytes<uint8_t>(pl.img_bytes) +
                    carve_bytes<float>((size_t)p.BH * std::max(1, pl.nstate) * pl.per_state) +
                    carve_bytes<float>((size_t)p.BH * std::max(1, pl.nstate) * g.n_ft * 4);
-    if (p.causal)
+    // causal: the combined segment states, only where a combine pass runs
+    // (more than four segments; up to four the scan combines them itself)
+    if (p.causal && pl.G > 4)
         bytes += carve_bytes<float>((size_t)p.BH * pl.G * pl.per_state) +
                  carve_bytes<float>((size_t)p.BH * pl.G * 4);
     else
@@ -2007,10 +2052,10 @@ int tc_run(const void *q, const void *k, const void *v, const float *omega, floa
         return FAVOR_OK;
     }
 
-    float *s_in = cv.take<float>((size_t)p.BH * G * per_state);
-    float *meta_in = cv.take<float>((size_t)p.BH * G * 4);
     // up to four segments the scan kernel combines the earlier states itself
     const bool direct = G <= 4;
+    float *s_in = direct ? nullptr : cv.take<float>((size_t)p.BH * G * per_state);
+    float *meta_in = direct ? nullptr : cv.take<float>((size_t)p.BH * G * 4);
     if (G > 1 && !direct) {
         CombineArgs ca{};
         ca.g = g; ca.nseg = nstate; ca.pps = pl.pps; ca.causal = 1; ca.state = state; ca.meta = meta;

@@ -33,8 +33,24 @@
  *          with the linear denominator of "Core points" step 5.
  *
  * Every kernel stabilises the exponentials (a per-row query maximum and a
- * per-head running key maximum); both cancel exactly in the ratio, so the
- * result is the definition above.
+ * per-head running key maximum); both cancel exactly in the ratio.
+ *
+ * Range of the tensor-core path (favor_attn_forward and its variants; the
+ * fp32 entry points compute every feature in fp32 and have no such limit).
+ * Its MMA operands are fp16, whose finite range is 2^-24 .. 65504:
+ *   - q, k and v values must be finite with |x| <= 65280 (the largest bf16
+ *     value below fp16's 65504);
+ *   - a key's largest feature is scaled to at most e^10 against the head's
+ *     running key maximum; a key whose largest feature would land below
+ *     2^-14 there (about e^-18 or more below the largest key feature of the
+ *     head so far) would lose its features to fp16 underflow.
+ * Isotropic inputs stay far inside both bounds (the largest feature of every
+ * key of N(0,1) d^-1/4 inputs lands within [e^0, e^10]).  The kernels check
+ * both on the device; an input outside them still completes, and the
+ * device status word (favor_get_device_status) then reads FAVOR_ERR_RANGE:
+ * the result is unreliable and favor_attn_forward_f32 on the same values
+ * (bf16 widened to fp32) computes it within the fp32 bound.  Inside the
+ * range the result is the definition above within fp16 operand rounding.
  *
  * Conventions common to all entry points
  *   - All tensors are dense, row-major, contiguous:
@@ -77,7 +93,11 @@ typedef enum {
     FAVOR_ERR_UNSUPPORTED = -2, /* valid but outside the supported shapes       */
     FAVOR_ERR_CUDA = -3,        /* a CUDA runtime call or launch failed          */
     FAVOR_ERR_TIMEOUT = -4,     /* a bounded device-side wait expired            */
-    FAVOR_ERR_NOMEM = -5        /* workspace allocation failed                   */
+    FAVOR_ERR_NOMEM = -5,       /* workspace allocation failed                   */
+    FAVOR_ERR_RANGE = -6        /* device status only: an input left the range
+                                   the fp16 tensor-core operands represent (see
+                                   "Range of the tensor-core path" above); the
+                                   call completed but its result is unreliable */
 } favor_status_t;
 
 typedef enum {
@@ -104,11 +124,14 @@ int favor_attn_forward(const void *q, const void *k, const void *v, const float 
  * fails), or a serving loop that cannot take the device-wide synchronisation
  * of cudaMalloc/cudaFree mid-request.  Same parameters and result as
  * favor_attn_forward; it never calls cudaMalloc, cudaFree or an allocating
- * routine.  Its scratch is a fixed 16 MiB array in the library's device
+ * routine.  Its scratch is a fixed 32 MiB array in the library's device
  * memory, held on every GPU that loads the library until the process exits.
  * Returns FAVOR_ERR_UNSUPPORTED for a shape the tensor-core kernels do not
- * cover or whose scratch (per-head fp16 W image, segment states) exceeds
- * 16 MiB -- e.g. B=4, H=16, L=8192, d=dv=64, m=256 causal fits.  The first
+ * cover or whose scratch (per-head fp16 W image, segment or piece states,
+ * the non-causal state image) exceeds 32 MiB: with d=dv=64, m=256 the
+ * benchmark shapes B=4, H=16, L=8192 causal (about 9 MB) and B=8, H=12,
+ * L=4096 non-causal (about 26 MB) fit; B=1, H=8, L=65536 causal, whose many
+ * segments per head carry many states, does not.  The first
  * call on a device looks the array's device address up (make it before any
  * stream capture).  All calls share the array: calls whose kernels overlap
  * on the GPU race on it.  Nothing in it needs clearing between calls. */
@@ -289,6 +312,16 @@ typedef struct {
 } favor_stats_t;
 int favor_stats_enable(int enable);
 int favor_stats_read(favor_stats_t *out);
+
+/* Measurement hook, no counterpart on the pages: the exponential throughput
+ * of the current device, the MUFU term of the roofline (the positive map
+ * takes 2 m exponentials per token).  Launches one kernel in which every
+ * thread of (SMs x 2048 / 256) blocks of 256 threads runs eight independent
+ * chains of ex2.approx.ftz.f32 (the instruction the feature epilogues use),
+ * times it with CUDA events on `stream`, and stores the rate in
+ * *ex2_per_second (exponentials per second, whole device).  Synchronous:
+ * it waits for the timing to finish.  Returns favor_status_t. */
+int favor_probe_ex2_rate(double *ex2_per_second, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

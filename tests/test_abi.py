@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_strerror(lib):
     assert fv.strerror(0) == "FAVOR_OK"
-    for s in (-1, -2, -3, -4, -5):
+    for s in (-1, -2, -3, -4, -5, -6):
         assert fv.strerror(s).startswith("FAVOR_ERR")
     assert "unknown" in fv.strerror(17)
 
@@ -95,3 +95,13 @@ def test_f32_and_host_entry_validate_too(lib):
     assert fv.favor_attn_forward_host(A, B_, C, None, O, 1, 1, 8, 32, 32, 16, 0, 0) == \
         fv.FAVOR_ERR_INVALID_ARG
     assert fv.favor_feature_map(A, W, O, None, 1, 1, 8, 32, 16, 0, 0) == fv.FAVOR_ERR_INVALID_ARG
+
+
+def test_noalloc_rejects_scratch_beyond_its_maximum(lib):
+    """The no-allocation entry point refuses a shape whose scratch exceeds its
+    fixed array before any device work: B*H = 256 heads of L = 65536 need
+    far more than 32 MiB of segment states.  The fake, far-apart pointers are
+    never touched (on a machine without a GPU the same refusal holds)."""
+    q, k, v, w, o = (i << 40 for i in range(1, 6))
+    rc = fv.favor_attn_forward_noalloc(q, k, v, w, o, 16, 16, 65536, 64, 64, 256, 1, fv.FAVOR_MAP_POSITIVE)
+    assert rc == fv.FAVOR_ERR_UNSUPPORTED

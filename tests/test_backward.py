@@ -1,8 +1,23 @@
 """The backward pass (favor_attn_backward / _f32) against the float64
 oracle's gradients (oracle.backward, pinned to finite differences of the
-forward pass): per head and per tensor, |G - G_ref|_F / |G_ref|_F.  The SIMT
+forward pass), row by row: for every row t of dq, dk, dv (a token) and of
+domega (a projection),
+
+    e_t = |G_t - G_ref_t| / max(|G_ref_t|, 1e-2 rms_t |G_ref_t|),
+
+the normwise per-row error of the forward parity tests, with a floor at
+1e-2 of the tensor's root-mean-square row norm: a row whose exact gradient
+vanishes (dq of the first causal row: out_0 = v_0 whatever q_0) is scored
+against the others' scale instead of against rounding noise (its error
+must still stay below 2e-4 of the rms row).  Bars: max_t
+e_t <= 2e-2 (the forward bf16 bar's) and mean_t e_t <= 2e-5.  The SIMT
 kernels compute in fp32 on the inputs' values (bf16 inputs are exact in
-fp32), so one bound serves both entry points.  CPU: host validation."""
+fp32), so one bar serves both entry points.  Measured on the GB300: mean row
+errors of 1e-7 to 4e-6 (3.3e-6 for dq at the full benchmark shape); single
+rows of dq reach 2e-3 to 7e-3 where the feature terms of a small-gradient
+row cancel (early causal rows, d = 128).  A wrong, missing or misplaced term
+moves a row by 1e-1 or more, so the max bar still catches it, and the mean
+bar sits five times above the worst measured mean.  CPU: host validation."""
 import numpy as np
 import pytest
 
@@ -11,7 +26,8 @@ from favor_inputs import (CAUSAL8K, MAP_ELU1, MAP_POSITIVE, MAP_RELU, MAP_TRIG, 
                           make_inputs)
 
 NO_OMEGA = (MAP_ELU1, MAP_RELU)
-GRAD_TOL = 2e-4
+GRAD_MAX, GRAD_MEAN = 2e-2, 2e-5
+ROW_FLOOR = 1e-2
 
 
 A, K, V, W, G, DQ, DK, DV, DW = (0x10000 * i for i in range(1, 10))
@@ -68,19 +84,24 @@ def _run(inp, g, causal, fmap, f32):
     return to(dq), to(dk), to(dv), to(dw)
 
 
-def _rel(got, ref, axes):
-    return np.linalg.norm(got - ref, axis=axes) / np.linalg.norm(ref, axis=axes)
+def row_errors(got, ref):
+    """Per-row normwise error with a floor at ROW_FLOOR x the rms row norm."""
+    a = got.reshape(-1, got.shape[-1])
+    b = ref.reshape(-1, ref.shape[-1])
+    nb = np.linalg.norm(b, axis=1)
+    floor = ROW_FLOOR * np.sqrt(np.mean(nb ** 2))
+    return np.linalg.norm(a - b, axis=1) / np.maximum(nb, floor)
 
 
-def _check(got, ref, tol):
+def _check(got, ref, bar_max=GRAD_MAX, bar_mean=GRAD_MEAN):
     names = ("dq", "dk", "dv", "dw")
     for name, a, b in zip(names, got, ref):
         if b is None:
             assert a is None
             continue
         assert np.isfinite(a).all(), name
-        e = _rel(a, b, (-2, -1))
-        assert e.max() <= tol, (name, e.max())
+        e = row_errors(a, b)
+        assert e.max() <= bar_max and e.mean() <= bar_mean, (name, e.max(), e.mean())
 
 
 CASES = [
@@ -105,14 +126,34 @@ def test_backward_matches_oracle(fmap, m, causal, f32):
     g = np.random.default_rng(71).standard_normal((2, 3, 200, w.dv))
     got = _run(inp, g, causal, fmap, f32)
     ref = oracle.backward(inp.q32, inp.k32, inp.v32, None if fmap in NO_OMEGA else inp.omega, g, causal, fmap)
-    _check(got, ref, GRAD_TOL)
+    _check(got, ref)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("causal", [False, True], ids=["noncausal", "causal"])
+@pytest.mark.parametrize("fmap", [MAP_POSITIVE, MAP_ELU1], ids=["positive", "elu1"])
+@pytest.mark.parametrize("d,dv,m", [(32, 32, 64), (64, 128, 64), (128, 128, 128)],
+                         ids=["d32", "d64-dv128", "d128"])
+def test_backward_head_dims(d, dv, m, fmap, causal):
+    """The other instances of the templated backward kernels: d = dv = 32,
+    dv = 128 (the 156 KB shared-memory launch shape of the chunk kernel) and
+    d = dv = 128."""
+    import oracle
+    w = NC4096.with_(feature_map=fmap, omega="iid", m=m, dtype="bf16", d=d, dv=dv)
+    if fmap in NO_OMEGA:
+        w = w.with_(m=w.d)
+    inp = make_inputs(w, L=200, B=2, H=3)
+    g = np.random.default_rng(73).standard_normal((2, 3, 200, w.dv))
+    got = _run(inp, g, causal, fmap, False)
+    ref = oracle.backward(inp.q32, inp.k32, inp.v32, None if fmap in NO_OMEGA else inp.omega, g, causal, fmap)
+    _check(got, ref)
 
 
 @pytest.mark.gpu
 def test_backward_full_size_sampled_heads():
     """The benchmark shape (B=4, H=16, L=8192, d=dv=64, m=256, causal): two
     heads (all four batches, so their omega gradients are complete) against
-    the oracle."""
+    the oracle, at the same per-row bars as the reduced shapes."""
     import oracle
     w = CAUSAL8K
     inp = make_inputs(w)
@@ -121,4 +162,4 @@ def test_backward_full_size_sampled_heads():
     hs = [5, 11]
     ref = oracle.backward(inp.q32[:, hs], inp.k32[:, hs], inp.v32[:, hs], inp.omega[hs], g[:, hs].astype(np.float64),
                           True, MAP_POSITIVE)
-    _check((got[0][:, hs], got[1][:, hs], got[2][:, hs], got[3][hs]), ref, 1e-3)
+    _check((got[0][:, hs], got[1][:, hs], got[2][:, hs], got[3][hs]), ref)

@@ -94,11 +94,13 @@ def test_sweep_reduced(w):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("m", [64, 128])
-def test_trig_well_conditioned(causal, m):
-    # q, k scaled by 1/4: |q-k|^2 ~ 1, so the Gaussian kernel the sin/cos
-    # features estimate is O(1) and most denominators are well conditioned
-    w = SWEEP16K.with_(m=m, feature_map=MAP_TRIG, d=64, dv=64)
+@pytest.mark.parametrize("d,m", [(64, 64), (64, 128), (128, 64), (128, 128), (128, 256), (128, 512)])
+def test_trig_well_conditioned(causal, d, m):
+    # q, k scaled by 1/4: |q-k|^2 ~ 1 (d = 64) or 1.4 (d = 128), so the
+    # Gaussian kernel the sin/cos features estimate is O(1) and most
+    # denominators are well conditioned; d = 128 is the sweep's head size,
+    # scored here on the plain per-row metric
+    w = SWEEP16K.with_(m=m, feature_map=MAP_TRIG, d=d, dv=d)
     inp = scaled_inputs(make_inputs(w, L=400, B=1, H=2), 0.25)
     out = run_gpu(inp, causal, MAP_TRIG)
     ref = oracle_ref(inp, causal, MAP_TRIG)

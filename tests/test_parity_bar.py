@@ -125,3 +125,69 @@ def test_fp32_bar_admits_fp32_features_and_rejects_fp16_omega():
     om16 = om.astype(np.float16).astype(np.float32)
     e16 = row_errors(out_from(oracle.features(q, om16), oracle.features(k, om16)), ref)
     assert e16.max() > 1e-4
+
+
+# ---------------------------------------------------------------------------
+# the condition-normalised metric of the sin/cos map at the sweep shape
+# (d = dv = 128, m = 256, causal): |o_i - ref_i| / (kappa_i (max_j |v_j| +
+# |ref_i|)) must still reject a swapped sin/cos and a sign error
+# ---------------------------------------------------------------------------
+LT = 512
+
+
+@pytest.fixture(scope="module")
+def sweep_trig():
+    from favor_inputs import MAP_TRIG, SWEEP16K
+    from parity_util import causal_trig_condition
+    w = SWEEP16K.with_(m=256, feature_map=MAP_TRIG)
+    inp = make_inputs(w, L=LT, B=1, H=2)
+    ref = oracle.forward(inp.q32, inp.k32, inp.v32, inp.omega, causal=True, feature_map=MAP_TRIG)
+    kap = causal_trig_condition(inp)
+    feats = [(oracle.features(inp.q32[0, h], inp.omega[h], MAP_TRIG),
+              oracle.features(inp.k32[0, h], inp.omega[h], MAP_TRIG)) for h in range(H)]
+    return inp, ref, kap, feats
+
+
+def _trig_causal(inp, feats, tq=lambda p: p, tk=lambda p: p):
+    out = np.empty((1, H, LT, inp.w.dv))
+    mask = np.tril(np.ones((LT, LT)))
+    for h, (pq, pk) in enumerate(feats):
+        A = (tq(pq) @ tk(pk).T) * mask
+        out[0, h] = (A @ inp.v32[0, h].astype(np.float64)) / A.sum(1, keepdims=True)
+    return out
+
+
+def _swap_sin_cos(p):
+    s = p.copy()
+    s[:, 0::2], s[:, 1::2] = p[:, 1::2], p[:, 0::2]
+    return s
+
+
+def _negate_sin(p):
+    s = p.copy()
+    s[:, 0::2] = -p[:, 0::2]
+    return s
+
+
+def _conditioned_passes(out, sweep):
+    from parity_util import conditioned_errors
+    inp, ref, kap, _ = sweep
+    return passes(conditioned_errors(out, ref, kap, inp.v32))
+
+
+def test_conditioned_metric_admits_the_exact_features(sweep_trig):
+    inp, _, _, feats = sweep_trig
+    assert _conditioned_passes(_trig_causal(inp, feats), sweep_trig)
+
+
+@pytest.mark.parametrize("bug", ["queries' sin and cos swapped", "keys' sin negated",
+                                 "keys' sin and cos swapped"])
+def test_conditioned_metric_rejects_trig_bugs(sweep_trig, bug):
+    inp, _, _, feats = sweep_trig
+    if bug == "queries' sin and cos swapped":
+        out = _trig_causal(inp, feats, tq=_swap_sin_cos)
+    elif bug == "keys' sin negated":
+        out = _trig_causal(inp, feats, tk=_negate_sin)
+    else:
+        out = _trig_causal(inp, feats, tk=_swap_sin_cos)
+    assert not _conditioned_passes(out, sweep_trig), bug

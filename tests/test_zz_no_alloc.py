@@ -1,15 +1,17 @@
 """favor_attn_forward_noalloc -- the entry point for callers that must not
 allocate device memory on the call path (a framework that has reserved the
 GPU's memory in its own pool, a serving loop that cannot take cudaMalloc's
-synchronisation).  It runs the tensor-core path on a fixed 16 MiB scratch
-array inside the library.  Checked against favor_attn_forward on two calls
-in a row (different inputs and modes, so stale scratch from the first call
-would show in the second).  This file is collected last."""
-import numpy as np
+synchronisation).  It runs the tensor-core path on a fixed 32 MiB scratch
+array inside the library, so on the same inputs it must give exactly the
+bits favor_attn_forward gives (same kernels, same plan).  Checked on two
+calls in a row (different inputs and modes, so stale scratch from the first
+call would show in the second), at reduced sizes and at the full benchmark
+shapes the header says fit.  This file is collected last; its refusal of
+oversized shapes is checked on the CPU (tests/test_abi.py)."""
 import pytest
 
 from favor_inputs import CAUSAL8K, MAP_POSITIVE, NC4096, make_inputs
-from parity_util import row_errors, run_gpu
+from parity_util import run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -23,22 +25,21 @@ def built():
     build.build()
 
 
-def test_noalloc_matches_forward_on_two_calls_in_a_row():
+def _same_bits(cases):
+    import numpy as np
     import favor_random_feature_gb300 as fv
-    cases = [(make_inputs(CAUSAL8K, L=2048, B=1, H=4), True),
-             (make_inputs(NC4096, L=1500, B=2, H=2), False)]
     for inp, causal in cases:
         ref = run_gpu(inp, causal, MAP_POSITIVE)
         got = run_gpu(inp, causal, MAP_POSITIVE, entry=fv.favor_attn_forward_noalloc)
-        e = row_errors(got, ref)
-        assert e.max() <= 2e-2 and e.mean() <= 2e-3, (causal, e.max(), e.mean())
+        assert np.array_equal(got, ref), (inp.w.name, causal, np.abs(got - ref).max())
 
 
-def test_noalloc_rejects_scratch_beyond_its_maximum():
-    import favor_random_feature_gb300 as fv
-    # B*H = 256 heads of L = 65536 need far more than 16 MiB of segment states;
-    # the call must refuse before touching the (fake, far apart) pointers.
-    A, Bp, C, W, O = (i << 40 for i in range(1, 6))
-    rc = fv.favor_attn_forward_noalloc(A, Bp, C, W, O, 16, 16, 65536, 64, 64, 256, 1,
-                                       MAP_POSITIVE)
-    assert rc == fv.FAVOR_ERR_UNSUPPORTED
+def test_noalloc_matches_forward_on_two_calls_in_a_row():
+    _same_bits([(make_inputs(CAUSAL8K, L=2048, B=1, H=4), True),
+                (make_inputs(NC4096, L=1500, B=2, H=2), False)])
+
+
+def test_noalloc_at_the_benchmark_shapes():
+    """B=4, H=16, L=8192 causal and B=8, H=12, L=4096 non-causal (d=dv=64,
+    m=256): both fit the array and return FAVOR_OK with the same bits."""
+    _same_bits([(make_inputs(CAUSAL8K), True), (make_inputs(NC4096), False)])
