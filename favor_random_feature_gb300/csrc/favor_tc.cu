@@ -67,14 +67,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
     return fn;
 }
 
-// 3D map over a [BH][L][cols] tensor, box [1][128][box_cols], 128B swizzle.
+// 3D map over a [BH][L][cols] tensor, box [1][box_rows][box_cols], 128B swizzle.
 int make_map(CUtensorMap *m, const void *base, CUtensorMapDataType type, int esize, int BH, int L,
-             int cols, int box_cols) {
+             int cols, int box_cols, int box_rows = kC) {
     auto enc = encoder();
     if (!enc) return FAVOR_ERR_CUDA;
     cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)L, (cuuint64_t)BH};
     cuuint64_t strides[2] = {(cuuint64_t)cols * esize, (cuuint64_t)L * cols * esize};
-    cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)kC, 1};
+    cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1};
     cuuint32_t es[3] = {1, 1, 1};
     CUresult r = enc(m, type, 3, const_cast<void *>(base), dims, strides, box, es,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -204,6 +204,20 @@ __device__ __forceinline__ bool ewait(uint64_t *bar, uint32_t parity, volatile i
     // later polls suspend in hardware until the phase completes (at most
     // 100 us each), so a waiting warp leaves the issue slots to the others
     while (!mbar_try_wait_hint(bar, parity, 100000u)) {
+        if (*abort) return false;
+        if (clock64() - t0 > kWaitLimit) {
+            *abort = 1;
+            return false;
+        }
+    }
+    return true;
+}
+
+// ewait for an mbarrier that other CTAs of the cluster complete (remote
+// stores, remote arrivals): the wait acquires at cluster scope.
+__device__ __forceinline__ bool cwait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait_cluster(bar, parity)) {
         if (*abort) return false;
         if (clock64() - t0 > kWaitLimit) {
             *abort = 1;
@@ -793,6 +807,9 @@ constexpr uint32_t kKbBlk = kKbRows * 128;       // one 64-feature block of the 
 constexpr int kKbS = 128, kKbZ = 192, kKbOne = 193;   // first rows of sigma S^T, sigma z, ones
 // small-area float offsets of the barriers, TMEM slot, abort flag; total size
 constexpr int kCausalBars = 1696, kCausalTslot = 1728, kCausalAbort = 1730, kCausalSmall = 1736;
+// r split: each row of a CTA's partial result travels as 68 floats (64 num,
+// den, log2 scale, row sum of the query features, pad)
+constexpr int kPartFloats = 68;
 
 // 16 output values of one row (columns c0 .. c0 + 15) into a 128B-swizzled
 // [128][64] bf16 staging block
@@ -810,15 +827,18 @@ __device__ __forceinline__ void stage_bf16_16(uint8_t *blk, int row, int c0, con
 }
 
 struct CausalArgs {
-    Geo g;
+    Geo g;                         // this CTA's features (a 128-feature slice where rs > 1)
     int H, L, seg_len, nseg;
+    int rs;                        // CTAs per cluster splitting the features (1: no split)
+    int nft_full, r_full;          // feature tiles and features of the whole head
+    size_t w_head_bytes;           // bytes of one head's W image
     const uint8_t *omg;            // MN-major W images
     const float *s_in, *meta_in;   // [BH][nseg][r][dv+1], [BH][nseg][4] (segment 0 unused)
     const float *state, *meta;     // piece states [BH][nstate][r][dv+1], [BH][nstate][n_ft][4]
     int nstate, pps, direct;       // pps pieces per segment; direct: combine the earlier pieces here
     int out_bf16;                  // out in bf16 (one [128][64] staging block) instead of fp32
     int *status;
-    uint32_t o_w, o_x, o_v, o_kb, o_small, tmem_cols;
+    uint32_t o_w, o_x, o_v, o_kb, o_small, o_recv, tmem_cols;
 };
 
 // TMEM columns: P [0, 256) | phi_Q packed [0, r/2) | A_m packed [0, 64) |
@@ -841,10 +861,12 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
                             const CUtensorMap *tm_q, const CUtensorMap *tm_k,
                             const CUtensorMap *tm_v, const CUtensorMap *tm_out) {
     const Geo &g = a.g;
-    const int seg = blockIdx.x, dvt = blockIdx.y, bh = blockIdx.z, head = bh % a.H;
+    const int rs = a.rs, seg = blockIdx.x / rs, slice = blockIdx.x % rs;
+    const int dvt = blockIdx.y, bh = blockIdx.z, head = bh % a.H;
     const int t_begin = seg * a.seg_len, t_end = min(a.L, t_begin + a.seg_len);
     const int nchunk = (t_end - t_begin + kC - 1) / kC;
-    const int nd = g.d / 64, nft = g.n_ft;
+    const int nd = g.d / 64, nft = g.n_ft, ft0 = slice * nft, nft_full = a.nft_full;
+    const int rpo = kC / rs;       // output rows each CTA of a split finalises
     const uint32_t xb = (uint32_t)kC * g.d * 2;
     uint8_t *w = sm + a.o_w, *xq = sm + a.o_x, *xk = xq + xb, *xv = sm + a.o_v, *kb = sm + a.o_kb;
     float *small = reinterpret_cast<float *>(sm + a.o_small);
@@ -858,6 +880,11 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
              *bar_pq = &bars[4], *bar_a = &bars[5], *bar_av = &bars[6], *bar_st = &bars[13];
     uint64_t *e_x = &bars[7], *e_pk = &bars[8], *e_q = &bars[9], *e_v = &bars[10],
              *e_b = &bars[11], *e_out = &bars[12];
+    // r split: partial rows received from the other CTAs of the cluster (one
+    // slot: [sender][row][kPartFloats]); bar_recv counts their bytes, bar_free
+    // hears from every owner that it has consumed the slot
+    uint64_t *bar_recv = &bars[14], *bar_free = &bars[15];
+    float *recv = reinterpret_cast<float *>(sm + a.o_recv);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int *abortp = reinterpret_cast<volatile int *>(small + kCausalAbort);
     bool alive = true;
@@ -895,7 +922,7 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
             grid_dep_wait();
             if (nchunk > 0) {
                 mbar_arrive_expect_tx(bar_w, wbytes);
-                bulk_load(w, a.omg + (size_t)head * wbytes, wbytes, bar_w);
+                bulk_load(w, a.omg + (size_t)head * a.w_head_bytes + (size_t)slice * wbytes, wbytes, bar_w);
                 alive = ewait(bar_w, 0, abortp);
             }
             for (int c = 0; c < nchunk && alive; ++c) {
@@ -949,8 +976,11 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
                 // rows 0..127 of blocks 0 and 1): store it, and once the store
                 // has read the staging, the next chunk's key projection
                 if (!(alive = ewait(e_out, ph, abortp))) break;
-                tma_store_3d(tm_out, kb, 64 * dvt, t_begin + c * kC, bh);
-                if (!OB16) tma_store_3d(tm_out, kb + kKbBlk, 64 * dvt + 32, t_begin + c * kC, bh);
+                // (split: this CTA's rows slice rpo .. of the chunk; the map's box is rpo rows)
+                tma_store_3d(tm_out, kb + slice * rpo * 128, 64 * dvt, t_begin + c * kC + slice * rpo, bh);
+                if (!OB16)
+                    tma_store_3d(tm_out, kb + kKbBlk + slice * rpo * 128, 64 * dvt + 32, t_begin + c * kC + slice * rpo,
+                                 bh);
                 bulk_commit();
                 if (c + 1 < nchunk) {
                     if (!(alive = ewait(e_x, (c + 1) & 1, abortp))) break;
@@ -1058,27 +1088,28 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
         // combined here at the largest of their key references (few segments:
         // no separate combine pass)
         const int npin = seg * a.pps;
-        const float *meta = a.meta + (size_t)bh * a.nstate * nft * 4;   // [g][tile][R, max z, max|v|, max|S|]
+        // [g][tile][R, max z, max|v|, max|S|]; this CTA's tiles ft0 .. ft0 + nft - 1
+        const float *meta = a.meta + (size_t)bh * a.nstate * nft_full * 4 + (size_t)ft0 * 4;
         float Rs = -INFINITY;
         for (int gi = 0; gi < npin; ++gi)
             for (int t = 0; t < nft; ++t) {
-                Rs = fmaxf(Rs, meta[(gi * nft + t) * 4]);
-                vmax = fmaxf(vmax, meta[(gi * nft + t) * 4 + 2]);
+                Rs = fmaxf(Rs, meta[(gi * nft_full + t) * 4]);
+                vmax = fmaxf(vmax, meta[(gi * nft_full + t) * 4 + 2]);
             }
         auto scale = [&](int gi, int t) -> float {
             if (MAP != FAVOR_MAP_POSITIVE) return 1.f;
-            const float Rg = meta[(gi * nft + t) * 4];
+            const float Rg = meta[(gi * nft_full + t) * 4];
             return (Rg == -INFINITY || Rs == -INFINITY) ? 0.f : ex2(Rg - Rs);
         };
         for (int gi = 0; gi < npin; ++gi) {
             float zt = 0.f;
-            for (int t = 0; t < nft; ++t) zt = fmaxf(zt, meta[(gi * nft + t) * 4 + 1] * scale(gi, t));
+            for (int t = 0; t < nft; ++t) zt = fmaxf(zt, meta[(gi * nft_full + t) * 4 + 1] * scale(gi, t));
             zmax += zt;
         }
         if (MAP == FAVOR_MAP_POSITIVE) R = Rs;
-        const size_t per = (size_t)g.r * (g.dv + 1);
+        const size_t per = (size_t)a.r_full * (g.dv + 1);
         for (int gi = 0; gi < npin; ++gi) {
-            const float *st = a.state + ((size_t)bh * a.nstate + gi) * per;
+            const float *st = a.state + ((size_t)bh * a.nstate + gi) * per + (size_t)ft0 * 128 * (g.dv + 1);
             const float sc0 = scale(gi, 0), sc1 = nft == 2 ? scale(gi, 1) : 0.f;
             const float *r0 = st + (size_t)row * (g.dv + 1), *r1 = st + (size_t)(128 + row) * (g.dv + 1);
 #pragma unroll
@@ -1097,7 +1128,7 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
         R = m[0];
         zmax = m[1];
         vmax = m[2];
-        const float *src = a.s_in + (((size_t)bh * a.nseg + seg) * g.r) * (g.dv + 1);
+        const float *src = a.s_in + (((size_t)bh * a.nseg + seg) * a.r_full + (size_t)ft0 * 128) * (g.dv + 1);
         const float *r0 = src + (size_t)row * (g.dv + 1), *r1 = src + (size_t)(128 + row) * (g.dv + 1);
 #pragma unroll
         for (int i = 0; i < 16; ++i) s0[i] = r0[64 * dvt + 16 * j + i];
@@ -1345,34 +1376,90 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
             tmem_ld_wait();
             tc_fence_before();
             const float is = pow2_inv_floor(sigma), ir = pow2_inv_floor(rho);   // exact: powers of two
-            const float den = fmaf(ddi, ir, ddx * is);
+            float ov[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) ov[i] = fmaf(di[i], ir, dx[i] * is);
+            float den = fmaf(ddi, ir, ddx * is);
+            bool mine = true;   // this thread finalises its row (every row, unless the features are split)
+            if (rs > 1) {
+                // The CTAs of the cluster hold partial sums over their feature
+                // slices, each at its own scale 2^sc (query row offset + key
+                // reference, log2 units).  Row `row` is finalised by CTA row /
+                // rpo: the others send it their partial (num, den, sc, row sum
+                // of the query features) into its one receive slot, once it
+                // has consumed the previous chunk's.
+                const float sc = MAP == FAVOR_MAP_POSITIVE ? qoff + R : 0.f;
+                const int owner = row / rpo;
+                mine = owner == slice;
+                if (!mine) {
+                    if (c > 0) alive &= cwait(bar_free, (c - 1) & 1, abortp);
+                    const int sidx = slice < owner ? slice : slice - 1;
+                    const uint32_t loc = smem_u32(recv + ((size_t)sidx * rpo + (row - owner * rpo)) * kPartFloats);
+                    const uint32_t rem = mapa_shared(loc, (uint32_t)owner);
+                    const uint32_t rbar = mapa_shared(smem_u32(bar_recv), (uint32_t)owner);
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc)
+                        st_async_v4(rem + (uint32_t)(16 * j + 4 * cc) * 4u, __float_as_uint(ov[4 * cc]),
+                                    __float_as_uint(ov[4 * cc + 1]), __float_as_uint(ov[4 * cc + 2]),
+                                    __float_as_uint(ov[4 * cc + 3]), rbar);
+                    if (j == 0)
+                        st_async_v4(rem + 64u * 4u, __float_as_uint(den), __float_as_uint(sc), __float_as_uint(qsum),
+                                    0u, rbar);
+                } else {
+                    if (row == slice * rpo && j == 0)
+                        mbar_arrive_expect_tx(bar_recv, (uint32_t)((rs - 1) * rpo * kPartFloats * 4));
+                    alive &= cwait(bar_recv, c & 1, abortp);
+                    const float *rp = recv + (size_t)(row - slice * rpo) * kPartFloats;
+                    const size_t sstride = (size_t)rpo * kPartFloats;
+                    float smax = sc;
+                    for (int k2 = 0; k2 < rs - 1; ++k2) smax = fmaxf(smax, rp[k2 * sstride + 65]);
+                    const float wl = ex2(sc - smax);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) ov[i] *= wl;
+                    den *= wl;
+                    qsum *= wl;
+                    for (int k2 = 0; k2 < rs - 1; ++k2) {
+                        const float *pk = rp + k2 * sstride;
+                        const float wk = ex2(pk[65] - smax);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) ov[i] = fmaf(pk[16 * j + i], wk, ov[i]);
+                        den = fmaf(pk[64], wk, den);
+                        qsum = fmaf(pk[66], wk, qsum);
+                    }
+                }
+                // the slot has been read: one arrival per owner warp at every sender
+                __syncwarp();
+                const int first = slice * rpo;
+                if (q * 32 + 31 >= first && q * 32 < first + rpo && lane == (first & 31))
+                    for (int o2 = 0; o2 < rs; ++o2)
+                        if (o2 != slice) mbar_arrive_remote(mapa_shared(smem_u32(bar_free), (uint32_t)o2));
+            }
             const float id = __fdividef(1.f, den);
             // the range check: the denominator against the features' fp16
             // floor (keys so far x the row sum of the query features x the
             // flush level, with a 2^10 margin)
-            if (MAP == FAVOR_MAP_POSITIVE && j == 0 && ok && den < (float)(tc0 + row + 1) * qsum * kRangeFloor)
+            if (MAP == FAVOR_MAP_POSITIVE && mine && j == 0 && ok && den < (float)(tc0 + row + 1) * qsum * kRangeFloor)
                 flag_range(a.status);
-            if constexpr (OB16) {
-                // output columns 16 j .. 16 j + 15 -> the bf16 staging block
-                // (phi_K rows of KB block 0, free since the state update)
-                float o[16];
+            if (mine) {
+                if constexpr (OB16) {
+                    // output columns 16 j .. 16 j + 15 -> the bf16 staging block
+                    // (phi_K rows of KB block 0, free since the state update)
+                    float o[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) o[i] = fmaf(di[i], ir, dx[i] * is) * id;
-                stage_bf16_16(kb, row, 16 * j, o);
-            } else {
-                // output columns 16 j .. 16 j + 15 -> staging half (16 j) / 32 (the
-                // phi_K rows of KB block 0 or 1, free since the state update), 128B
-                // swizzle in chunks of 4 floats
-                uint8_t *half = kb + (size_t)((16 * j) >> 5) * kKbBlk;
+                    for (int i = 0; i < 16; ++i) o[i] = ov[i] * id;
+                    stage_bf16_16(kb, row, 16 * j, o);
+                } else {
+                    // output columns 16 j .. 16 j + 15 -> staging half (16 j) / 32 (the
+                    // phi_K rows of KB block 0 or 1, free since the state update), 128B
+                    // swizzle in chunks of 4 floats
+                    uint8_t *half = kb + (size_t)((16 * j) >> 5) * kKbBlk;
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    const int col = (16 * j + 4 * cc) & 31;
-                    const int p = (col >> 2) ^ (row & 7);
-                    *reinterpret_cast<float4 *>(half + row * 128 + p * 16) =
-                        make_float4(fmaf(di[4 * cc + 0], ir, dx[4 * cc + 0] * is) * id,
-                                    fmaf(di[4 * cc + 1], ir, dx[4 * cc + 1] * is) * id,
-                                    fmaf(di[4 * cc + 2], ir, dx[4 * cc + 2] * is) * id,
-                                    fmaf(di[4 * cc + 3], ir, dx[4 * cc + 3] * is) * id);
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const int col = (16 * j + 4 * cc) & 31;
+                        const int p = (col >> 2) ^ (row & 7);
+                        *reinterpret_cast<float4 *>(half + row * 128 + p * 16) =
+                            make_float4(ov[4 * cc] * id, ov[4 * cc + 1] * id, ov[4 * cc + 2] * id, ov[4 * cc + 3] * id);
+                    }
                 }
             }
             fence_async_smem();
@@ -1403,6 +1490,12 @@ tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         for (int i = 0; i < 7; ++i) mbar_init(&bars[i], 1);
         for (int i = 7; i < 13; ++i) mbar_init(&bars[i], kEpi);
         mbar_init(&bars[13], 1);
+        // split features: the receive slot (one local arrival + the senders'
+        // bytes) and the slot-free barrier (one arrival per owner warp of
+        // every other CTA)
+        mbar_init(&bars[14], 1);
+        const int rpo = kC / a.rs;
+        mbar_init(&bars[15], a.rs > 1 ? (a.rs - 1) * 4 * max(1, rpo / 32) : 1);
         fence_mbar_init();
     }
     // ones atom after the V tile: the z column of S += phi_K^T [V | 1] and
@@ -1415,6 +1508,8 @@ tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // every CTA of a split has initialised its barriers before any remote access
+    if (a.rs > 1) cluster_sync();
     const uint32_t tmem = *tslot;
     const int nc = a.g.nproj / 4;
     grid_dep_launch();
@@ -1430,6 +1525,8 @@ tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // no CTA of a split leaves while another may still store into it
+    if (a.rs > 1) cluster_sync();
     if (warp == 0) tmem_dealloc(tmem, a.tmem_cols);
 }
 
@@ -1732,9 +1829,11 @@ Geo make_geo(const Problem &p) {
 }
 
 struct CausalLayout {
-    uint32_t o_w, o_x, o_v, o_kb, o_small, bytes;
+    uint32_t o_w, o_x, o_v, o_kb, o_small, o_recv, bytes;
 };
-CausalLayout causal_layout(const Geo &g) {
+// rs > 1: g is one 128-feature slice, plus the slot that receives the other
+// CTAs' partial rows ([rs - 1][128 / rs][kPartFloats] fp32)
+CausalLayout causal_layout(const Geo &g, int rs = 1) {
     CausalLayout l;
     uint32_t o = 0;
     l.o_w = o; o = align1k(o + (uint32_t)g.nproj * g.d * 2);
@@ -1742,8 +1841,20 @@ CausalLayout causal_layout(const Geo &g) {
     l.o_v = o; o = align1k(o + 2 * kBlk);                   // V tile + ones atom
     l.o_kb = o; o = align1k(o + (uint32_t)(g.r / 64) * kKbBlk);
     l.o_small = o; o = align1k(o + kCausalSmall * 4);
+    l.o_recv = o; if (rs > 1) o = align1k(o + (uint32_t)(rs - 1) * (kC / rs) * kPartFloats * 4);
     l.bytes = o + 1024;
     return l;
+}
+
+// One 128-feature slice of a head: the per-CTA geometry of a split scan
+// (positive and trig maps; a slice holds 128 features: 128 projections, or
+// the sin and cos of 64)
+Geo slice_geo(const Geo &g) {
+    Geo s = g;
+    s.r = 128;
+    s.n_ft = 1;
+    s.nproj = g.map == FAVOR_MAP_TRIG ? 64 : 128;
+    return s;
 }
 
 struct StateLayout {
@@ -1818,6 +1929,31 @@ int launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
     return FAVOR_OK;
 }
 
+// launch_dependent with clusters of `cluster_x` CTAs along x
+template <typename... KArgs, typename... Args>
+int launch_dependent_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             int cluster_x, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)cluster_x;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    if (cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...) != cudaSuccess) {
+        cudaGetLastError();
+        return FAVOR_ERR_CUDA;
+    }
+    return FAVOR_OK;
+}
+
 int num_sms() {
     static int n = 0;
     if (!n) {
@@ -1833,17 +1969,33 @@ int num_sms() {
 
 }  // namespace
 
+namespace {
+// CTAs per cluster that split a head's features in the causal scan: 1 (one
+// CTA holds all of them) where the whole-head layout fits, else one CTA per
+// 128 features (2, 4 or 8); 0 if neither fits.
+int causal_split(const Problem &p) {
+    const Geo g = make_geo(p);
+    if (causal_layout(g).bytes <= kSmemMax && (p.r == 128 || p.r == 256)) return 1;
+    if (p.map == FAVOR_MAP_ELU1 || p.r % 128 != 0) return 0;
+    const int rs = p.r / 128;
+    if (rs < 2 || rs > 8) return 0;
+    return causal_layout(slice_geo(g), rs).bytes <= kSmemMax ? rs : 0;
+}
+}  // namespace
+
 bool tc_supported(const Problem &p) {
     // ReLU and the softmax-scaled Fourier map run on the SIMT kernels
     if (p.map == FAVOR_MAP_RELU || p.map == FAVOR_MAP_TRIG_SOFTMAX) return false;
     if (p.d != 64 && p.d != 128) return false;
     if (p.dv != 64 && p.dv != 128) return false;
-    if (p.r != 128 && p.r != 256) return false;
     if (p.map == FAVOR_MAP_ELU1 && p.r != 128) return false;
     Geo g = make_geo(p);
     if (p.causal) {
-        if (causal_layout(g).bytes > kSmemMax) return false;
+        // wider feature sets split over the CTAs of a cluster
+        if (p.r != 128 && p.r != 256 && p.r != 512 && p.r != 1024) return false;
+        if (causal_split(p) == 0) return false;
     } else {
+        if (p.r != 128 && p.r != 256) return false;
         if (output_layout(g).bytes > kSmemMax) return false;
     }
     if (state_layout(g).bytes > kSmemMax) return false;
@@ -1853,6 +2005,7 @@ bool tc_supported(const Problem &p) {
 namespace {
 struct Plan {
     int G, seg_len, nstate, pps, piece_len, nfg, nvb, nchunk;
+    int rs = 1;                    // causal: CTAs per cluster splitting the features
     size_t img_bytes, per_state, bytes;
 };
 
@@ -1870,10 +2023,14 @@ Plan make_plan(const Problem &p) {
     pl.nfg = g.n_ft / state_layout(g).FT;
     const int sms = num_sms();
     if (p.causal) {
-        // scan segments: whole 128-token chunks, about one CTA per SM
-        int G = (int)std::lround((double)sms / (p.BH * pl.nvb));
-        // at most 64 segments: the combine keeps one scale per (piece, feature tile)
-        G = std::max(1, std::min(std::min(G, pl.nchunk), 64));
+        // scan segments: whole 128-token chunks, about one CTA per SM (a
+        // split head takes rs CTAs per segment)
+        pl.rs = causal_split(p);
+        const int rs = std::max(1, pl.rs);
+        int G = (int)std::lround((double)sms / ((double)p.BH * pl.nvb * rs));
+        // at most 64 segments: the combine keeps one scale per (piece, feature
+        // tile); a split scan combines the earlier segments itself (at most 4)
+        G = std::max(1, std::min(std::min(G, pl.nchunk), rs > 1 ? 4 : 64));
         const int seg_chunks = (pl.nchunk + G - 1) / G;
         pl.G = (pl.nchunk + seg_chunks - 1) / seg_chunks;
         pl.seg_len = seg_chunks * kC;
@@ -2011,11 +2168,13 @@ int tc_run(const void *q, const void *k, const void *v, const float *omega, floa
 
     CUtensorMap mq, mk, mv, mo;
     int rc;
+    // the output box: a chunk's rows, or the rows one CTA of a split finalises
+    const int out_rows = kC / (p.causal ? std::max(1, pl.rs) : 1);
     if ((rc = make_map(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.BH, p.L, p.d, 64)) ||
         (rc = make_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.BH, p.L, p.d, 64)) ||
         (rc = make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.BH, p.L, p.dv, 64)) ||
-        (rc = p.out_bf16 ? make_map(&mo, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.BH, p.L, p.dv, 64)
-                         : make_map(&mo, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.BH, p.L, p.dv, 32)))
+        (rc = p.out_bf16 ? make_map(&mo, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.BH, p.L, p.dv, 64, out_rows)
+                         : make_map(&mo, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.BH, p.L, p.dv, 32, out_rows)))
         return rc;
 
     tc_prep_omega<<<dim3(32, p.H), 256, 0, st>>>(omega, img, p.H, p.nproj, p.d, p.map);
@@ -2065,21 +2224,28 @@ int tc_run(const void *q, const void *k, const void *v, const float *omega, floa
         if ((rc = launch_dependent(tc_combine, dim3(p.BH, G - 1, nsl), dim3(256), 0, st, ca))) return rc;
         FAVOR_LAUNCH_CHECK();
     }
-    CausalLayout cl = causal_layout(g);
+    const int rs = std::max(1, pl.rs);
+    const Geo gs = rs > 1 ? slice_geo(g) : g;
+    CausalLayout cl = causal_layout(gs, rs);
     CausalArgs a;
-    a.g = g;
+    a.g = gs;
     a.H = p.H; a.L = p.L; a.seg_len = seg_len; a.nseg = G;
+    a.rs = rs; a.nft_full = g.n_ft; a.r_full = g.r;
+    a.w_head_bytes = (size_t)p.nproj * p.d * 2;
     a.omg = img; a.s_in = s_in; a.meta_in = meta_in; a.status = dstat;
     a.state = state; a.meta = meta; a.nstate = nstate; a.pps = pl.pps; a.direct = direct ? 1 : 0;
     a.out_bf16 = p.out_bf16;
     a.o_w = cl.o_w; a.o_x = cl.o_x; a.o_v = cl.o_v; a.o_kb = cl.o_kb; a.o_small = cl.o_small;
+    a.o_recv = cl.o_recv;
     a.tmem_cols = 512;
     auto kern = p.out_bf16 ? tc_causal<true> : tc_causal<false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cl.bytes) != cudaSuccess)
         return FAVOR_ERR_CUDA;
     stats_begin(st, "tc_causal");
-    if ((rc = launch_dependent(kern, dim3(G, nvb, p.BH), dim3(kCausalThreads), cl.bytes, st, mq, mk, mv,
-                               mo, a))) {
+    if ((rc = rs > 1 ? launch_dependent_cluster(kern, dim3(rs * G, nvb, p.BH), dim3(kCausalThreads), cl.bytes, st, rs,
+                                                mq, mk, mv, mo, a)
+                     : launch_dependent(kern, dim3(G, nvb, p.BH), dim3(kCausalThreads), cl.bytes, st, mq, mk, mv,
+                                        mo, a))) {
         stats_end(st);
         return rc;
     }
