@@ -827,7 +827,7 @@ __device__ __forceinline__ void stage_bf16_16(uint8_t *blk, int row, int c0, con
 }
 
 struct CausalArgs {
-    Geo g;                         // this CTA's features (a 128-feature slice where rs > 1)
+    Geo g;                         // this CTA's features (one 128-feature slice in tc_causal_split)
     int H, L, seg_len, nseg;
     int rs;                        // CTAs per cluster splitting the features (1: no split)
     int nft_full, r_full;          // feature tiles and features of the whole head
@@ -838,7 +838,7 @@ struct CausalArgs {
     int nstate, pps, direct;       // pps pieces per segment; direct: combine the earlier pieces here
     int out_bf16;                  // out in bf16 (one [128][64] staging block) instead of fp32
     int *status;
-    uint32_t o_w, o_x, o_v, o_kb, o_small, o_recv, tmem_cols;
+    uint32_t o_w, o_x, o_v, o_kb, o_small, o_recv, o_stage, tmem_cols;
 };
 
 // TMEM columns: P [0, 256) | phi_Q packed [0, r/2) | A_m packed [0, 64) |
@@ -861,12 +861,10 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
                             const CUtensorMap *tm_q, const CUtensorMap *tm_k,
                             const CUtensorMap *tm_v, const CUtensorMap *tm_out) {
     const Geo &g = a.g;
-    const int rs = a.rs, seg = blockIdx.x / rs, slice = blockIdx.x % rs;
-    const int dvt = blockIdx.y, bh = blockIdx.z, head = bh % a.H;
+    const int seg = blockIdx.x, dvt = blockIdx.y, bh = blockIdx.z, head = bh % a.H;
     const int t_begin = seg * a.seg_len, t_end = min(a.L, t_begin + a.seg_len);
     const int nchunk = (t_end - t_begin + kC - 1) / kC;
-    const int nd = g.d / 64, nft = g.n_ft, ft0 = slice * nft, nft_full = a.nft_full;
-    const int rpo = kC / rs;       // output rows each CTA of a split finalises
+    const int nd = g.d / 64, nft = g.n_ft, ft0 = 0, nft_full = a.nft_full;
     const uint32_t xb = (uint32_t)kC * g.d * 2;
     uint8_t *w = sm + a.o_w, *xq = sm + a.o_x, *xk = xq + xb, *xv = sm + a.o_v, *kb = sm + a.o_kb;
     float *small = reinterpret_cast<float *>(sm + a.o_small);
@@ -880,11 +878,6 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
              *bar_pq = &bars[4], *bar_a = &bars[5], *bar_av = &bars[6], *bar_st = &bars[13];
     uint64_t *e_x = &bars[7], *e_pk = &bars[8], *e_q = &bars[9], *e_v = &bars[10],
              *e_b = &bars[11], *e_out = &bars[12];
-    // r split: partial rows received from the other CTAs of the cluster (one
-    // slot: [sender][row][kPartFloats]); bar_recv counts their bytes, bar_free
-    // hears from every owner that it has consumed the slot
-    uint64_t *bar_recv = &bars[14], *bar_free = &bars[15];
-    float *recv = reinterpret_cast<float *>(sm + a.o_recv);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int *abortp = reinterpret_cast<volatile int *>(small + kCausalAbort);
     bool alive = true;
@@ -922,7 +915,7 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
             grid_dep_wait();
             if (nchunk > 0) {
                 mbar_arrive_expect_tx(bar_w, wbytes);
-                bulk_load(w, a.omg + (size_t)head * a.w_head_bytes + (size_t)slice * wbytes, wbytes, bar_w);
+                bulk_load(w, a.omg + (size_t)head * a.w_head_bytes, wbytes, bar_w);
                 alive = ewait(bar_w, 0, abortp);
             }
             for (int c = 0; c < nchunk && alive; ++c) {
@@ -976,11 +969,8 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
                 // rows 0..127 of blocks 0 and 1): store it, and once the store
                 // has read the staging, the next chunk's key projection
                 if (!(alive = ewait(e_out, ph, abortp))) break;
-                // (split: this CTA's rows slice rpo .. of the chunk; the map's box is rpo rows)
-                tma_store_3d(tm_out, kb + slice * rpo * 128, 64 * dvt, t_begin + c * kC + slice * rpo, bh);
-                if (!OB16)
-                    tma_store_3d(tm_out, kb + kKbBlk + slice * rpo * 128, 64 * dvt + 32, t_begin + c * kC + slice * rpo,
-                                 bh);
+                tma_store_3d(tm_out, kb, 64 * dvt, t_begin + c * kC, bh);
+                if (!OB16) tma_store_3d(tm_out, kb + kKbBlk, 64 * dvt + 32, t_begin + c * kC, bh);
                 bulk_commit();
                 if (c + 1 < nchunk) {
                     if (!(alive = ewait(e_x, (c + 1) & 1, abortp))) break;
@@ -1380,67 +1370,13 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
 #pragma unroll
             for (int i = 0; i < 16; ++i) ov[i] = fmaf(di[i], ir, dx[i] * is);
             float den = fmaf(ddi, ir, ddx * is);
-            bool mine = true;   // this thread finalises its row (every row, unless the features are split)
-            if (rs > 1) {
-                // The CTAs of the cluster hold partial sums over their feature
-                // slices, each at its own scale 2^sc (query row offset + key
-                // reference, log2 units).  Row `row` is finalised by CTA row /
-                // rpo: the others send it their partial (num, den, sc, row sum
-                // of the query features) into its one receive slot, once it
-                // has consumed the previous chunk's.
-                const float sc = MAP == FAVOR_MAP_POSITIVE ? qoff + R : 0.f;
-                const int owner = row / rpo;
-                mine = owner == slice;
-                if (!mine) {
-                    if (c > 0) alive &= cwait(bar_free, (c - 1) & 1, abortp);
-                    const int sidx = slice < owner ? slice : slice - 1;
-                    const uint32_t loc = smem_u32(recv + ((size_t)sidx * rpo + (row - owner * rpo)) * kPartFloats);
-                    const uint32_t rem = mapa_shared(loc, (uint32_t)owner);
-                    const uint32_t rbar = mapa_shared(smem_u32(bar_recv), (uint32_t)owner);
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc)
-                        st_async_v4(rem + (uint32_t)(16 * j + 4 * cc) * 4u, __float_as_uint(ov[4 * cc]),
-                                    __float_as_uint(ov[4 * cc + 1]), __float_as_uint(ov[4 * cc + 2]),
-                                    __float_as_uint(ov[4 * cc + 3]), rbar);
-                    if (j == 0)
-                        st_async_v4(rem + 64u * 4u, __float_as_uint(den), __float_as_uint(sc), __float_as_uint(qsum),
-                                    0u, rbar);
-                } else {
-                    if (row == slice * rpo && j == 0)
-                        mbar_arrive_expect_tx(bar_recv, (uint32_t)((rs - 1) * rpo * kPartFloats * 4));
-                    alive &= cwait(bar_recv, c & 1, abortp);
-                    const float *rp = recv + (size_t)(row - slice * rpo) * kPartFloats;
-                    const size_t sstride = (size_t)rpo * kPartFloats;
-                    float smax = sc;
-                    for (int k2 = 0; k2 < rs - 1; ++k2) smax = fmaxf(smax, rp[k2 * sstride + 65]);
-                    const float wl = ex2(sc - smax);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) ov[i] *= wl;
-                    den *= wl;
-                    qsum *= wl;
-                    for (int k2 = 0; k2 < rs - 1; ++k2) {
-                        const float *pk = rp + k2 * sstride;
-                        const float wk = ex2(pk[65] - smax);
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) ov[i] = fmaf(pk[16 * j + i], wk, ov[i]);
-                        den = fmaf(pk[64], wk, den);
-                        qsum = fmaf(pk[66], wk, qsum);
-                    }
-                }
-                // the slot has been read: one arrival per owner warp at every sender
-                __syncwarp();
-                const int first = slice * rpo;
-                if (q * 32 + 31 >= first && q * 32 < first + rpo && lane == (first & 31))
-                    for (int o2 = 0; o2 < rs; ++o2)
-                        if (o2 != slice) mbar_arrive_remote(mapa_shared(smem_u32(bar_free), (uint32_t)o2));
-            }
             const float id = __fdividef(1.f, den);
             // the range check: the denominator against the features' fp16
             // floor (keys so far x the row sum of the query features x the
             // flush level, with a 2^10 margin)
-            if (MAP == FAVOR_MAP_POSITIVE && mine && j == 0 && ok && den < (float)(tc0 + row + 1) * qsum * kRangeFloor)
+            if (MAP == FAVOR_MAP_POSITIVE && j == 0 && ok && den < (float)(tc0 + row + 1) * qsum * kRangeFloor)
                 flag_range(a.status);
-            if (mine) {
+            {
                 if constexpr (OB16) {
                     // output columns 16 j .. 16 j + 15 -> the bf16 staging block
                     // (phi_K rows of KB block 0, free since the state update)
@@ -1490,12 +1426,682 @@ tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         for (int i = 0; i < 7; ++i) mbar_init(&bars[i], 1);
         for (int i = 7; i < 13; ++i) mbar_init(&bars[i], kEpi);
         mbar_init(&bars[13], 1);
+        fence_mbar_init();
+    }
+    // ones atom after the V tile: the z column of S += phi_K^T [V | 1] and
+    // the row sums of [A_m V | A_m 1]
+    uint8_t *ones = sm + a.o_v + kBlk;
+    for (int i = threadIdx.x; i < (int)(kBlk / 16); i += kCausalThreads)
+        reinterpret_cast<uint4 *>(ones)[i] = make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
+    if (warp == 0) tmem_alloc(tslot, a.tmem_cols);
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const int nc = a.g.nproj / 4;
+    grid_dep_launch();
+    if (a.g.map == FAVOR_MAP_POSITIVE) {
+        if (nc == 64) causal_body<64, FAVOR_MAP_POSITIVE, OB16>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
+        else causal_body<32, FAVOR_MAP_POSITIVE, OB16>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
+    } else if (a.g.map == FAVOR_MAP_TRIG) {
+        if (nc == 32) causal_body<32, FAVOR_MAP_TRIG, OB16>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
+        else causal_body<16, FAVOR_MAP_TRIG, OB16>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
+    } else {
+        causal_body<32, FAVOR_MAP_ELU1, OB16>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, a.tmem_cols);
+}
+
+// ---------------------------------------------------------------------------
+// tc_causal_split: the chunked causal scan of a head whose features are
+// split over the rs CTAs of a cluster (rs = r / 128: one 128-feature slice
+// each; rs = 1 would be a whole head of 128).  Each CTA scans its slice at
+// its own key reference and query offsets; per chunk every CTA sends its
+// partial numerators, denominators and log-scales for the rows another CTA
+// finalises through distributed shared memory (st.async completing on the
+// owner's mbarrier), and each owner rescales, sums, normalises and stores its
+// rows.  With 128 features the projections, the query features, the
+// intra-chunk matrix and the state leave TMEM room for a second chunk, so
+// the scan is software-pipelined by one chunk: the tensor core projects
+// chunk c + 1 and the epilogue forms its features while chunk c's masked
+// product A_m [V | 1] runs and its output is reduced and stored.
+//   control thread, per chunk c:  merged MMA (c) | S += phi_K^T [V | 1] (c) |
+//     P_K (c + 1) | A_m [V | 1] (c) | P_Q (c + 1) | loads | output store (c)
+//   epilogue, per chunk c:  masked, row-scaled A (c) | key features and
+//     state rows (c + 1) | query features (c + 1) | output (c) |
+//     phi_Q (c + 1) into TMEM | V (c + 1) | Q, K (c + 2) -> fp16
+// TMEM: P [0, 128) | A_m [V | 1] at [128, 208), phi_Q (packed) there before
+// it (the merged MMA has consumed phi_Q when A_m V overwrites it) | [A |
+// phi_Q sigma S | phi_Q sigma z | query row sum] at [208, 416), A_m packed
+// in place (keys 32 j .. 32 j + 31 in columns 208 + 32 j .. + 15) | the
+// state [416, 496) (64 values, z).
+// Shared memory: W slice, Q and K tiles, V tile + ones atom, KB (phi_K 128
+// rows, sigma S^T 64, sigma z, ones) per 64 features, the output staging of
+// the CTA's rows, the small area, the receive slot of a split.
+// ---------------------------------------------------------------------------
+constexpr int kPcP = 0, kPcAV = 128, kPcA = 208, kPcDX = 336, kPcDD = 400, kPcS = 416;
+// small-area float offsets of the split scan
+constexpr int kSpRedM = 1696, kSpRedV = 1728, kSpBars = 1760, kSpTslot = 1800, kSpAbort = 1802, kSpSmall = 1808;
+constexpr int kSpNumBars = 18;
+
+template <int NC, int MAP, bool OB16>
+__device__ void split_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem, const CUtensorMap *tm_q,
+                           const CUtensorMap *tm_k, const CUtensorMap *tm_v, const CUtensorMap *tm_out) {
+    const Geo &g = a.g;
+    const int rs = a.rs, seg = blockIdx.x / rs, slice = blockIdx.x % rs;
+    const int dvt = blockIdx.y, bh = blockIdx.z, head = bh % a.H;
+    const int t_begin = seg * a.seg_len, t_end = min(a.L, t_begin + a.seg_len);
+    const int nchunk = (t_end - t_begin + kC - 1) / kC;
+    const int nd = g.d / 64, ft0 = slice, nft_full = a.nft_full;
+    const int rpo = kC / rs;
+    const uint32_t xb = (uint32_t)kC * g.d * 2;
+    uint8_t *w = sm + a.o_w, *xq = sm + a.o_x, *xk = xq + xb, *xv = sm + a.o_v, *kb = sm + a.o_kb,
+            *stage = sm + a.o_stage;
+    float *small = reinterpret_cast<float *>(sm + a.o_small);
+    float *nk = small;             // [128] half key norms (log2 units)
+    float *part = small + 128;     // [4][128] query row max
+    float *part2 = small + 640;    // [4][128] intra-chunk row max
+    float *part3 = small + 1152;   // [4][128] key sums of squares
+    float *red = small + 1664;     // [32] the vote
+    float *redm = small + kSpRedM; // [2][16] key mass per warp, by chunk parity
+    float *redv = small + kSpRedV; // [2][16] max |v| per warp, by chunk parity
+    uint64_t *bars = reinterpret_cast<uint64_t *>(small + kSpBars);
+    uint64_t *b_w = &bars[0], *b_x = &bars[1], *b_v = &bars[2], *b_pk = &bars[3], *b_pq = &bars[4],
+             *b_a = &bars[5], *b_s = &bars[6], *b_av = &bars[7], *b_st = &bars[8];
+    uint64_t *e_x = &bars[9], *e_pk = &bars[10], *e_q = &bars[11], *e_v = &bars[12], *e_b = &bars[13],
+             *e_out = &bars[14];
+    uint64_t *bar_recv = &bars[15], *bar_free = &bars[16];
+    float *recv = reinterpret_cast<float *>(sm + a.o_recv);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    volatile int *abortp = reinterpret_cast<volatile int *>(small + kSpAbort);
+    bool alive = true;
+
+    if (warp == 0) {
+        // ======================= control thread =======================
+        if (lane == 0) {
+            const uint32_t w_s = smem_u32(w), xq_s = smem_u32(xq), xk_s = smem_u32(xk), v_s = smem_u32(xv),
+                           kb_s = smem_u32(kb);
+            const uint32_t wbytes = (uint32_t)g.nproj * g.d * 2;
+            auto load_x = [&](int c) {
+                mbar_arrive_expect_tx(b_x, 2 * xb);
+                for (int b = 0; b < nd; ++b) {
+                    tma_load_3d(xq + b * kBlk, tm_q, b_x, 64 * b, t_begin + c * kC, bh);
+                    tma_load_3d(xk + b * kBlk, tm_k, b_x, 64 * b, t_begin + c * kC, bh);
+                }
+            };
+            auto load_v = [&](int c) {
+                mbar_arrive_expect_tx(b_v, kBlk);
+                tma_load_3d(xv, tm_v, b_v, 64 * dvt, t_begin + c * kC, bh);
+            };
+            // P = X W^T (N = the slice's projections)
+            auto proj = [&](uint32_t x_s) {
+                const uint32_t idesc = idesc_f16(128, g.nproj, 0, 1);
+                for (int kk = 0; kk < g.d / 16; ++kk)
+                    mma_f16(tmem + kPcP, smem_desc(x_s + (kk >> 2) * kBlk + (kk & 3) * 32, 16, 1024),
+                            smem_desc(w_s + kk * 2048, (uint32_t)g.d * 128, 1024), idesc, kk > 0);
+            };
+            // this CTA's output rows of chunk c (a box of rpo rows), then the
+            // staging is free again
+            auto store_rows = [&](int c) {
+                tma_store_3d(tm_out, stage, 64 * dvt, t_begin + c * kC + slice * rpo, bh);
+                if (!OB16) tma_store_3d(tm_out, stage + rpo * 128, 64 * dvt + 32, t_begin + c * kC + slice * rpo, bh);
+                bulk_commit();
+                bulk_wait_read0();
+                mbar_arrive(b_st);
+            };
+            if (nchunk > 0) {
+                load_x(0);
+                load_v(0);
+            }
+            // the W image (and the state of the earlier segments) come from
+            // the kernels before this one
+            grid_dep_wait();
+            if (nchunk > 0) {
+                mbar_arrive_expect_tx(b_w, wbytes);
+                bulk_load(w, a.omg + (size_t)head * a.w_head_bytes + (size_t)slice * wbytes, wbytes, b_w);
+                alive = ewait(b_w, 0, abortp) && ewait(e_x, 0, abortp);
+                if (alive) {
+                    tc_fence_after();
+                    proj(xk_s);
+                    mma_commit(b_pk);
+                    alive = ewait(e_pk, 0, abortp);
+                }
+                if (alive) {
+                    tc_fence_after();
+                    proj(xq_s);
+                    mma_commit(b_pq);
+                    alive = ewait(b_pq, 0, abortp);
+                    if (alive && nchunk > 1) load_x(1);
+                }
+            }
+            for (int c = 0; c < nchunk && alive; ++c) {
+                const uint32_t ph = c & 1, ph1 = (c + 1) & 1;
+                const bool more = c + 1 < nchunk;
+                // [A | phi_Q sigma S | phi_Q sigma z | q sum] = phi_Q KB^T
+                if (!(alive = ewait(e_q, ph, abortp))) break;
+                tc_fence_after();
+                {
+                    const uint32_t idesc = idesc_f16(128, kKbRows, 0, 0);
+                    for (int kk = 0; kk < g.r / 16; ++kk)
+                        mma_f16_ts(tmem + kPcA, tmem + kPcAV + 8 * kk,
+                                   smem_desc(kb_s + (kk >> 2) * kKbBlk + (kk & 3) * 32, 16, 1024), idesc, kk > 0);
+                    mma_commit(b_a);
+                }
+                // the next chunk's key projection (P was read for chunk c's queries)
+                if (more) {
+                    if (!(alive = ewait(e_x, ph1, abortp))) break;
+                    tc_fence_after();
+                    proj(xk_s);
+                    mma_commit(b_pk);
+                }
+                // S += phi_K^T [V | 1]
+                if (!(alive = ewait(e_v, ph, abortp))) break;
+                tc_fence_after();
+                {
+                    const uint32_t ids = idesc_f16(128, 80, 1, 1);
+                    for (int kk = 0; kk < kC / 16; ++kk)
+                        mma_f16(tmem + kPcS, smem_desc(kb_s + kk * 2048, kKbBlk, 1024),
+                                smem_desc(v_s + kk * 2048, kBlk, 1024), ids, 1);
+                    mma_commit(b_s);
+                }
+                // [A_m V | A_m 1], A_m packed in place in the A columns
+                if (!(alive = ewait(e_b, ph, abortp))) break;
+                tc_fence_after();
+                {
+                    const uint32_t idv = idesc_f16(128, 80, 0, 1);
+                    for (int kk = 0; kk < kC / 16; ++kk)
+                        mma_f16_ts(tmem + kPcAV, tmem + kPcA + 32 * (kk >> 1) + 8 * (kk & 1),
+                                   smem_desc(v_s + kk * 2048, kBlk, 1024), idv, kk > 0);
+                    mma_commit(b_av);
+                }
+                // chunk c - 1's output rows, staged by the epilogue at the end of
+                // its previous iteration
+                if (c > 0) {
+                    if (!(alive = ewait(e_out, (c - 1) & 1, abortp))) break;
+                    store_rows(c - 1);
+                }
+                // the next chunk's query projection, then its Q, K tiles
+                if (more) {
+                    if (!(alive = ewait(e_pk, ph1, abortp))) break;
+                    tc_fence_after();
+                    proj(xq_s);
+                    mma_commit(b_pq);
+                    if (!(alive = ewait(b_pq, ph1, abortp))) break;
+                    if (c + 2 < nchunk) load_x(c + 2);
+                }
+                // V is free once A_m V (and the state update before it) is done
+                if (!(alive = ewait(b_av, ph, abortp))) break;
+                if (more) load_v(c + 1);
+            }
+            if (alive && nchunk > 0 && (alive = ewait(e_out, (nchunk - 1) & 1, abortp))) store_rows(nchunk - 1);
+            bulk_wait0();
+            if (!alive) set_status(a.status, FAVOR_ERR_TIMEOUT);
+        }
+        return;
+    }
+    // ======================= epilogue group =======================
+    const int e = threadIdx.x - 32, ew = e >> 5;
+    const int q = (ew + 1) & 3, j = ew >> 2;
+    const int row = q * 32 + lane;
+    // the ones row and the pad rows of every KB block
+    for (int i = e; i < (g.r / 64) * 15 * 8; i += kEpi) {
+        const int blk = i / 120, rr = kKbOne + (i % 120) / 8, ch = i % 8;
+        const uint32_t one = rr == kKbOne ? 0x3C003C00u : 0u;
+        *reinterpret_cast<uint4 *>(kb + (size_t)blk * kKbBlk + rr * 128 + ch * 16) = make_uint4(one, one, one, one);
+    }
+    float R = MAP == FAVOR_MAP_POSITIVE ? -INFINITY : 0.f, zmax = 0.f, vmax = 0.f, sigma = 1.f;
+    float qoff_next = 0.f;                  // query row offset of the chunk whose features are held
+    constexpr int NH = MAP == FAVOR_MAP_TRIG ? NC : NC / 2;
+    uint32_t hq[NH];                        // that chunk's query features, packed fp16
+    float s0[16], z0 = 0.f;                 // this thread's part of the initial state
+#pragma unroll
+    for (int i = 0; i < 16; ++i) s0[i] = 0.f;
+
+    // sigma S^T and sigma z -> KB rows kKbS.. and kKbZ (sigma: a power of two
+    // with sigma * (bound on max |S| and max z) <= kSigmaTarget); alpha != 1
+    // first rescales the state in TMEM (the key reference has moved)
+    auto state_rows = [&](float alpha) {
+        const float bound = zmax * fmaxf(vmax, 1.f);
+        sigma = bound > 0.f ? pow2_scale_14(bound) : 1.f;
+        const uint32_t kb_s = smem_u32(kb);
+        if (alpha != 1.f) {
+            float t16[16], zz = 0.f;
+            tmem_ld16(tm_addr(tmem, q, kPcS + 16 * j), t16);
+            if (j == 0) tmem_ld1(tm_addr(tmem, q, kPcS + 64), zz);
+            tmem_ld_wait();
+            uint32_t u[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(t16[i] * alpha);
+            tmem_st16(tm_addr(tmem, q, kPcS + 16 * j), u);
+            if (j == 0) tmem_st1(tm_addr(tmem, q, kPcS + 64), zz * alpha);
+            tmem_st_wait();
+        }
+        float a4[4][4], zz = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int g2 = 0; g2 < 2; ++g2)
+                tmem_ld_16x256b(tm_addr(tmem, q, kPcS + 16 * j + 8 * g2) + ((uint32_t)(16 * h) << 16), a4[2 * h + g2]);
+        if (j == 0) tmem_ld1(tm_addr(tmem, q, kPcS + 64), zz);
+        tmem_ld_wait();
+        const int mi = lane >> 3;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int f = 32 * q + 16 * h + 8 * (mi & 1);
+            const int rr = kKbS + 16 * j + 8 * (mi >> 1) + (lane & 7);
+            const uint32_t addr = kb_s + (uint32_t)(f >> 6) * kKbBlk + (uint32_t)rr * 128u +
+                                  ((((uint32_t)(f & 63) >> 3) ^ ((uint32_t)rr & 7u)) << 4);
+            const float(&lo)[4] = a4[2 * h], (&hi)[4] = a4[2 * h + 1];
+            stmatrix_x4_trans(addr, pack_half2(lo[0] * sigma, lo[1] * sigma), pack_half2(lo[2] * sigma, lo[3] * sigma),
+                              pack_half2(hi[0] * sigma, hi[1] * sigma), pack_half2(hi[2] * sigma, hi[3] * sigma));
+        }
+        if (j == 0)
+            *reinterpret_cast<__half *>(kb + (size_t)(row >> 6) * kKbBlk + sw128_offset(kKbZ, row & 63)) =
+                __float2half_rn(zz * sigma);
+    };
+    auto convert_x = [&](int c) -> bool {
+        const bool ok_x = ewait(b_x, c & 1, abortp);
+        float am, am2;
+        convert_tile_512<false, true>(xq, nd, e, am);
+        const float ss = convert_tile_512<true, true>(xk, nd, e, am2);
+        if (fmaxf(am, am2) > kMaxOperand) flag_range(a.status);
+        part3[(e >> 7) * 128 + (e & 127)] = ss;
+        group_sync(kEpi);
+        if (e < 128) nk[e] = 0.5f * kLog2e * ((part3[e] + part3[128 + e]) + (part3[256 + e] + part3[384 + e]));
+        fence_async_smem();
+        mbar_arrive(e_x);
+        return ok_x;
+    };
+    // key features of chunk c -> KB rows 0..127 (after the vote on the key
+    // reference); returns the factor the state so far moves by
+    auto keys = [&](int c) -> float {
+        const int valid = min(kC, t_end - (t_begin + c * kC));
+        const bool ok = row < valid;
+        alive &= ewait(b_pk, c & 1, abortp);
+        tc_fence_after();
+        float pv[NC];
+        tmem_ld_cols<NC>(tm_addr(tmem, q, kPcP + NC * j), pv);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(e_pk);   // P_K is in registers: P_Q may overwrite it
+        const float nkr = nk[row];
+        float mf = 0.f, moved = 1.f;
+        float off = 0.f;
+        if constexpr (MAP == FAVOR_MAP_POSITIVE) {
+            const float mx = max_of(pv);
+            if (group_or(ok && mx - nkr - R > kLog2MaxFeature, kEpi)) {
+                const float Rn = grp_max(ok ? mx - nkr : -INFINITY, red, ew) - kShift;
+                if (R != -INFINITY) moved = ex2(R - Rn);
+                R = Rn;
+            }
+            off = ok ? nkr + R : INFINITY;
+            mf = ex2(mx - off);
+        }
+        // phi_K rows and the state are free once the update of chunk c - 1 is done
+        if (c > 0) alive &= ewait(b_s, (c - 1) & 1, abortp);
+        tc_fence_after();
+        if constexpr (MAP == FAVOR_MAP_POSITIVE) {
+#pragma unroll
+            for (int b = 0; b < NC / 8; ++b) {
+                float v[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[i] = ex2(pv[8 * b + i] - off);
+                kb_store8(kb, row, NC * j + 8 * b, v);
+            }
+        } else if constexpr (MAP == FAVOR_MAP_TRIG) {
+            // projection p -> feature p (sin) and p + 64 (cos) of the slice
+            const int fs = NC * j;
+#pragma unroll
+            for (int b = 0; b < NC / 8; ++b) {
+                float s8[8], c8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (ok) sincos_reduced(pv[8 * b + i], s8[i], c8[i]);
+                    else s8[i] = c8[i] = 0.f;
+                    mf = fmaxf(mf, fmaxf(fabsf(s8[i]), fabsf(c8[i])));
+                }
+                kb_store8(kb, row, fs + 8 * b, s8);
+                kb_store8(kb, row, fs + 64 + 8 * b, c8);
+            }
+        } else {
+#pragma unroll
+            for (int b = 0; b < NC / 8; ++b) {
+                float v[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    v[i] = ok ? elu1(pv[8 * b + i]) : 0.f;
+                    mf = fmaxf(mf, v[i]);
+                }
+                kb_store8(kb, row, NC * j + 8 * b, v);
+            }
+        }
+        // warp partial of the key mass (sum over keys of the largest feature,
+        // the bound on the growth of z), read after the next group barrier
+        float ms = mf;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ms += __shfl_xor_sync(0xffffffffu, ms, o);
+        if (lane == 0) redm[(c & 1) * 16 + ew] = ms;
+        return moved;
+    };
+    // query features of chunk c -> registers (hq), its row offset -> qoff_next
+    auto queries = [&](int c) {
+        alive &= ewait(b_pq, c & 1, abortp);
+        tc_fence_after();
+        float pv[NC];
+        tmem_ld_cols<NC>(tm_addr(tmem, q, kPcP + NC * j), pv);
+        tmem_ld_wait();
+        tc_fence_before();
+        if constexpr (MAP == FAVOR_MAP_POSITIVE) {
+            part[j * 128 + row] = max_of(pv);
+            group_sync(kEpi);
+            qoff_next = fmaxf(fmaxf(part[row], part[128 + row]), fmaxf(part[256 + row], part[384 + row])) - kShift;
+#pragma unroll
+            for (int i = 0; i < NC / 2; ++i) hq[i] = pack_half2(ex2(pv[2 * i] - qoff_next), ex2(pv[2 * i + 1] - qoff_next));
+        } else if constexpr (MAP == FAVOR_MAP_TRIG) {
+            // sines in hq[0, NC/2), cosines in hq[NC/2, NC)
+#pragma unroll
+            for (int i = 0; i < NC / 2; ++i) {
+                float sa, ca, sb, cb;
+                sincos_reduced(pv[2 * i], sa, ca);
+                sincos_reduced(pv[2 * i + 1], sb, cb);
+                hq[i] = pack_half2(sa, sb);
+                hq[NC / 2 + i] = pack_half2(ca, cb);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < NC / 2; ++i) hq[i] = pack_half2(elu1(pv[2 * i]), elu1(pv[2 * i + 1]));
+        }
+    };
+    // the held query features -> TMEM (the A_m V columns, read by the output
+    // of the previous chunk first); then the merged MMA may start
+    auto store_q = [&]() {
+        group_sync(kEpi);
+        tc_fence_after();
+        if constexpr (MAP == FAVOR_MAP_TRIG) {
+            tmem_st8(tm_addr(tmem, q, kPcAV + (NC * j) / 2), *reinterpret_cast<const uint32_t(*)[8]>(hq));
+            tmem_st8(tm_addr(tmem, q, kPcAV + (NC * j + 64) / 2), *reinterpret_cast<const uint32_t(*)[8]>(hq + NC / 2));
+        } else {
+            tmem_st16(tm_addr(tmem, q, kPcAV + (NC * j) / 2), *reinterpret_cast<const uint32_t(*)[16]>(hq));
+        }
+        tmem_st_wait();
+        fence_async_smem();   // KB rows (key features, state) for the tensor core
+        tc_fence_before();
+        mbar_arrive(e_q);
+    };
+    // V(c) -> fp16 with the warp's max |v| (read after the next Q, K conversion)
+    auto values = [&](int c) {
+        alive &= ewait(b_v, c & 1, abortp);
+        float am;
+        convert_tile_512<false, true>(xv, 1, e, am);
+        if (am > kMaxOperand) flag_range(a.status);
+        fence_async_smem();
+        mbar_arrive(e_v);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+        if (lane == 0) redv[(c & 1) * 16 + ew] = am;
+    };
+    auto take_vmax = [&](int c) {   // after a group barrier that follows values(c)
+        float vm = 0.f;
+#pragma unroll
+        for (int i = 0; i < kEpi / 32; ++i) vm = fmaxf(vm, redv[(c & 1) * 16 + i]);
+        vmax = fmaxf(vmax, vm);
+    };
+
+    // X(0) is the caller's data: convert it while the kernels before this
+    // one finish; the state of the earlier segments is theirs
+    if (nchunk > 0) alive &= convert_x(0);
+    grid_dep_wait();
+    if (seg > 0 && a.direct) {
+        const int npin = seg * a.pps;
+        const float *meta = a.meta + (size_t)bh * a.nstate * nft_full * 4 + (size_t)ft0 * 4;
+        float Rs = -INFINITY;
+        for (int gi = 0; gi < npin; ++gi) {
+            Rs = fmaxf(Rs, meta[gi * nft_full * 4]);
+            vmax = fmaxf(vmax, meta[gi * nft_full * 4 + 2]);
+        }
+        auto scale = [&](int gi) -> float {
+            if (MAP != FAVOR_MAP_POSITIVE) return 1.f;
+            const float Rg = meta[gi * nft_full * 4];
+            return (Rg == -INFINITY || Rs == -INFINITY) ? 0.f : ex2(Rg - Rs);
+        };
+        for (int gi = 0; gi < npin; ++gi) zmax += meta[gi * nft_full * 4 + 1] * scale(gi);
+        if (MAP == FAVOR_MAP_POSITIVE) R = Rs;
+        const size_t per = (size_t)a.r_full * (g.dv + 1);
+        for (int gi = 0; gi < npin; ++gi) {
+            const float *r0 = a.state + ((size_t)bh * a.nstate + gi) * per + (size_t)(ft0 * 128 + row) * (g.dv + 1);
+            const float sc0 = scale(gi);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) s0[i] += r0[64 * dvt + 16 * j + i] * sc0;
+            if (j == 0) z0 += r0[g.dv] * sc0;
+        }
+    } else if (seg > 0) {
+        const float *m = a.meta_in + ((size_t)bh * a.nseg + seg) * 4;
+        R = m[0];
+        zmax = m[1];
+        vmax = m[2];
+        const float *r0 = a.s_in + (((size_t)bh * a.nseg + seg) * a.r_full + (size_t)ft0 * 128 + row) * (g.dv + 1);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) s0[i] = r0[64 * dvt + 16 * j + i];
+        if (j == 0) z0 = r0[g.dv];
+    }
+    {
+        uint32_t u[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(s0[i]);
+        tmem_st16(tm_addr(tmem, q, kPcS + 16 * j), u);
+        if (j == 0) tmem_st1(tm_addr(tmem, q, kPcS + 64), z0);
+        tmem_st_wait();
+    }
+    // prologue: chunk 0's key features, state rows and query features
+    if (nchunk > 0) {
+        const float moved = keys(0);
+        if (moved != 1.f) zmax *= moved;
+        state_rows(moved);
+        queries(0);
+        store_q();
+        values(0);
+        if (nchunk > 1) alive &= convert_x(1);
+    }
+    for (int c = 0; c < nchunk; ++c) {
+        const uint32_t ph = c & 1;
+        const int tc0 = t_begin + c * kC;
+        const int valid = min(kC, t_end - tc0);
+        const bool ok = row < valid;
+        const bool more = c + 1 < nchunk;
+        // ---------------- intra-chunk matrix -> masked, row-scaled, packed in place ----------------
+        alive &= ewait(b_a, ph, abortp);
+        tc_fence_after();
+        float rho;
+        {
+            float av[32];
+            const int limit = min(row, valid - 1) - 32 * j;   // keys j' <= limit (local index)
+            float rm = 0.f;
+            if (limit < 0) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) av[i] = 0.f;
+            } else {
+                tmem_ld32(tm_addr(tmem, q, kPcA + 32 * j), av);
+                tmem_ld_wait();
+                if (limit < 31) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) av[i] = i <= limit ? av[i] : 0.f;
+                }
+                float aa[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) aa[i] = fabsf(av[i]);
+                rm = max_of(aa);
+            }
+            part2[j * 128 + row] = rm;
+            group_sync(kEpi);   // also publishes the key mass of chunk c
+            const float rmax = fmaxf(fmaxf(part2[row], part2[128 + row]), fmaxf(part2[256 + row], part2[384 + row]));
+            rho = rmax > 0.f ? pow2_inv_floor(rmax) : 1.f;
+            uint32_t o[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] = pack_half2(av[2 * i] * rho, av[2 * i + 1] * rho);
+            tmem_st16(tm_addr(tmem, q, kPcA + 32 * j), o);
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(e_b);
+        }
+        {
+            // chunk c's key mass and max |v| (their warp partials are complete
+            // since the barrier above)
+            float ms = 0.f;
+#pragma unroll
+            for (int i = 0; i < kEpi / 32; ++i) ms += redm[(c & 1) * 16 + i];
+            zmax += ms;
+            take_vmax(c);
+        }
+        // chunk c's scales for its output, before the next chunk moves them
+        const float qoff_c = qoff_next, R_c = R, sigma_c = sigma;
+        // ---------------- chunk c + 1: key features, state rows, query features ----------------
+        if (more) {
+            const float moved = keys(c + 1);
+            if (moved != 1.f) zmax *= moved;
+            state_rows(moved);
+            queries(c + 1);
+        }
+        // ---------------- output of chunk c: the partial, sent where another CTA finalises the row ----------------
+        alive &= ewait(b_av, ph, abortp);
+        tc_fence_after();
+        float ov[16], den, qsum = 0.f, sc = 0.f;
+        bool mine = true;
+        {
+            float di[16], dx[16], ddi, ddx;
+            tmem_ld16(tm_addr(tmem, q, kPcAV + 16 * j), di);
+            tmem_ld16(tm_addr(tmem, q, kPcDX + 16 * j), dx);
+            tmem_ld1(tm_addr(tmem, q, kPcAV + 64), ddi);
+            tmem_ld1(tm_addr(tmem, q, kPcDD), ddx);
+            if (j == 0) tmem_ld1(tm_addr(tmem, q, kPcDD + 1), qsum);
+            tmem_ld_wait();
+            tc_fence_before();
+            const float is = pow2_inv_floor(sigma_c), ir = pow2_inv_floor(rho);   // exact: powers of two
+#pragma unroll
+            for (int i = 0; i < 16; ++i) ov[i] = fmaf(di[i], ir, dx[i] * is);
+            den = fmaf(ddi, ir, ddx * is);
+            if (rs > 1) {
+                // each CTA's partial sits at its own scale 2^sc (query row
+                // offset + key reference, log2 units); row `row` is finalised
+                // by CTA row / rpo, the others send it their partial now
+                sc = MAP == FAVOR_MAP_POSITIVE ? qoff_c + R_c : 0.f;
+                const int owner = row / rpo;
+                mine = owner == slice;
+                if (!mine) {
+                    if (c > 0) alive &= cwait(bar_free, (c - 1) & 1, abortp);
+                    const int sidx = slice < owner ? slice : slice - 1;
+                    const uint32_t loc = smem_u32(recv + ((size_t)sidx * rpo + (row - owner * rpo)) * kPartFloats);
+                    const uint32_t rem = mapa_shared(loc, (uint32_t)owner);
+                    const uint32_t rbar = mapa_shared(smem_u32(bar_recv), (uint32_t)owner);
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc)
+                        st_async_v4(rem + (uint32_t)(16 * j + 4 * cc) * 4u, __float_as_uint(ov[4 * cc]),
+                                    __float_as_uint(ov[4 * cc + 1]), __float_as_uint(ov[4 * cc + 2]),
+                                    __float_as_uint(ov[4 * cc + 3]), rbar);
+                    if (j == 0)
+                        st_async_v4(rem + 64u * 4u, __float_as_uint(den), __float_as_uint(sc), __float_as_uint(qsum),
+                                    0u, rbar);
+                } else if (row == slice * rpo && j == 0) {
+                    mbar_arrive_expect_tx(bar_recv, (uint32_t)((rs - 1) * rpo * kPartFloats * 4));
+                }
+            }
+        }
+        // ---------------- chunk c + 1: query features into TMEM; chunk c + 2: Q, K ----------------
+        if (more) {
+            store_q();
+            if (c + 2 < nchunk) alive &= convert_x(c + 2);
+        }
+        // ---------------- output of chunk c: gather, normalise, stage ----------------
+        if (rs > 1) {
+            if (mine) {
+                alive &= cwait(bar_recv, ph, abortp);
+                const float *rp = recv + (size_t)(row - slice * rpo) * kPartFloats;
+                const size_t sstride = (size_t)rpo * kPartFloats;
+                float smax = sc;
+                for (int k2 = 0; k2 < rs - 1; ++k2) smax = fmaxf(smax, rp[k2 * sstride + 65]);
+                const float wl = ex2(sc - smax);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) ov[i] *= wl;
+                den *= wl;
+                qsum *= wl;
+                for (int k2 = 0; k2 < rs - 1; ++k2) {
+                    const float *pk = rp + k2 * sstride;
+                    const float wk = ex2(pk[65] - smax);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) ov[i] = fmaf(pk[16 * j + i], wk, ov[i]);
+                    den = fmaf(pk[64], wk, den);
+                    qsum = fmaf(pk[66], wk, qsum);
+                }
+            }
+            // the slot has been read: one arrival per owner warp at every sender
+            __syncwarp();
+            const int first = slice * rpo;
+            if (q * 32 + 31 >= first && q * 32 < first + rpo && lane == (first & 31))
+                for (int o2 = 0; o2 < rs; ++o2)
+                    if (o2 != slice) mbar_arrive_remote(mapa_shared(smem_u32(bar_free), (uint32_t)o2));
+        }
+        {
+            const float id = __fdividef(1.f, den);
+            // the range check: the denominator against the features' fp16
+            // floor (keys so far x the row sum of the query features x the
+            // flush level, with a 2^10 margin)
+            if (MAP == FAVOR_MAP_POSITIVE && mine && j == 0 && ok && den < (float)(tc0 + row + 1) * qsum * kRangeFloor)
+                flag_range(a.status);
+            // the staging is free once the previous chunk's store has read it
+            if (c > 0) alive &= ewait(b_st, (c - 1) & 1, abortp);
+            if (mine) {
+                const int lr = row - slice * rpo;   // row within this CTA's rows
+                if constexpr (OB16) {
+                    float o[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) o[i] = ov[i] * id;
+                    stage_bf16_16(stage, lr, 16 * j, o);
+                } else {
+                    uint8_t *half = stage + (size_t)((16 * j) >> 5) * rpo * 128;
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const int col = (16 * j + 4 * cc) & 31;
+                        const int p = (col >> 2) ^ (lr & 7);
+                        *reinterpret_cast<float4 *>(half + lr * 128 + p * 16) =
+                            make_float4(ov[4 * cc] * id, ov[4 * cc + 1] * id, ov[4 * cc + 2] * id, ov[4 * cc + 3] * id);
+                    }
+                }
+            }
+            fence_async_smem();
+            mbar_arrive(e_out);
+        }
+        // ---------------- chunk c + 1: V ----------------
+        if (more) values(c + 1);
+    }
+    if (!alive) set_status(a.status, FAVOR_ERR_TIMEOUT);
+}
+
+template <bool OB16>
+__global__ void __launch_bounds__(kCausalThreads, 1)
+tc_causal_split(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_out,
+                const CausalArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float *small = reinterpret_cast<float *>(sm + a.o_small);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(small + kSpBars);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(small + kSpTslot);
+    volatile int *abortp = reinterpret_cast<volatile int *>(small + kSpAbort);
+    const int warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        *abortp = 0;
+        for (int i = 0; i < 9; ++i) mbar_init(&bars[i], 1);
+        for (int i = 9; i < 15; ++i) mbar_init(&bars[i], kEpi);
         // split features: the receive slot (one local arrival + the senders'
         // bytes) and the slot-free barrier (one arrival per owner warp of
         // every other CTA)
-        mbar_init(&bars[14], 1);
+        mbar_init(&bars[15], 1);
         const int rpo = kC / a.rs;
-        mbar_init(&bars[15], a.rs > 1 ? (a.rs - 1) * 4 * max(1, rpo / 32) : 1);
+        mbar_init(&bars[16], a.rs > 1 ? (a.rs - 1) * 4 * max(1, rpo / 32) : 1);
+        mbar_init(&bars[17], 1);
         fence_mbar_init();
     }
     // ones atom after the V tile: the z column of S += phi_K^T [V | 1] and
@@ -1511,17 +2117,10 @@ tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     // every CTA of a split has initialised its barriers before any remote access
     if (a.rs > 1) cluster_sync();
     const uint32_t tmem = *tslot;
-    const int nc = a.g.nproj / 4;
     grid_dep_launch();
-    if (a.g.map == FAVOR_MAP_POSITIVE) {
-        if (nc == 64) causal_body<64, FAVOR_MAP_POSITIVE, OB16>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
-        else causal_body<32, FAVOR_MAP_POSITIVE, OB16>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
-    } else if (a.g.map == FAVOR_MAP_TRIG) {
-        if (nc == 32) causal_body<32, FAVOR_MAP_TRIG, OB16>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
-        else causal_body<16, FAVOR_MAP_TRIG, OB16>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
-    } else {
-        causal_body<32, FAVOR_MAP_ELU1, OB16>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
-    }
+    if (a.g.map == FAVOR_MAP_POSITIVE) split_body<32, FAVOR_MAP_POSITIVE, OB16>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
+    else if (a.g.map == FAVOR_MAP_TRIG) split_body<16, FAVOR_MAP_TRIG, OB16>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
+    else split_body<32, FAVOR_MAP_ELU1, OB16>(a, sm, tmem, &tm_q, &tm_k, &tm_v, &tm_out);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1829,11 +2428,9 @@ Geo make_geo(const Problem &p) {
 }
 
 struct CausalLayout {
-    uint32_t o_w, o_x, o_v, o_kb, o_small, o_recv, bytes;
+    uint32_t o_w, o_x, o_v, o_kb, o_small, o_recv, o_stage, bytes;
 };
-// rs > 1: g is one 128-feature slice, plus the slot that receives the other
-// CTAs' partial rows ([rs - 1][128 / rs][kPartFloats] fp32)
-CausalLayout causal_layout(const Geo &g, int rs = 1) {
+CausalLayout causal_layout(const Geo &g) {
     CausalLayout l;
     uint32_t o = 0;
     l.o_w = o; o = align1k(o + (uint32_t)g.nproj * g.d * 2);
@@ -1841,7 +2438,27 @@ CausalLayout causal_layout(const Geo &g, int rs = 1) {
     l.o_v = o; o = align1k(o + 2 * kBlk);                   // V tile + ones atom
     l.o_kb = o; o = align1k(o + (uint32_t)(g.r / 64) * kKbBlk);
     l.o_small = o; o = align1k(o + kCausalSmall * 4);
-    l.o_recv = o; if (rs > 1) o = align1k(o + (uint32_t)(rs - 1) * (kC / rs) * kPartFloats * 4);
+    l.o_recv = 0;
+    l.o_stage = 0;
+    l.bytes = o + 1024;
+    return l;
+}
+
+// The pipelined scan of 128 features per CTA (tc_causal_split): g is one
+// 128-feature slice; its own output staging (the CTA's 128 / rs rows: two
+// [rows][32] fp32 halves, or one [rows][64] bf16 block) and, for rs > 1, the
+// receive slot
+CausalLayout split_layout(const Geo &g, int rs) {
+    CausalLayout l;
+    const uint32_t rpo = (uint32_t)(kC / rs);
+    uint32_t o = 0;
+    l.o_w = o; o = align1k(o + (uint32_t)g.nproj * g.d * 2);
+    l.o_x = o; o = align1k(o + 2u * kC * g.d * 2);
+    l.o_v = o; o = align1k(o + 2 * kBlk);                   // V tile + ones atom
+    l.o_kb = o; o = align1k(o + 2 * kKbBlk);
+    l.o_small = o; o = align1k(o + kSpSmall * 4);
+    l.o_stage = o; o = align1k(o + 2 * rpo * 128);
+    l.o_recv = o; if (rs > 1) o = align1k(o + (uint32_t)(rs - 1) * rpo * kPartFloats * 4);
     l.bytes = o + 1024;
     return l;
 }
@@ -1975,12 +2592,15 @@ namespace {
 // 128 features (2, 4 or 8); 0 if neither fits.
 int causal_split(const Problem &p) {
     const Geo g = make_geo(p);
-    if (causal_layout(g).bytes <= kSmemMax && (p.r == 128 || p.r == 256)) return 1;
+    if ((p.r == 128 || p.r == 256) && causal_layout(g).bytes <= kSmemMax) return 1;
     if (p.map == FAVOR_MAP_ELU1 || p.r % 128 != 0) return 0;
     const int rs = p.r / 128;
     if (rs < 2 || rs > 8) return 0;
-    return causal_layout(slice_geo(g), rs).bytes <= kSmemMax ? rs : 0;
+    return split_layout(slice_geo(g), rs).bytes <= kSmemMax ? rs : 0;
 }
+
+// a split head: the pipelined scan of 128 features per CTA
+bool causal_pipelined(int rs) { return rs > 1; }
 }  // namespace
 
 bool tc_supported(const Problem &p) {
@@ -2225,8 +2845,9 @@ int tc_run(const void *q, const void *k, const void *v, const float *omega, floa
         FAVOR_LAUNCH_CHECK();
     }
     const int rs = std::max(1, pl.rs);
-    const Geo gs = rs > 1 ? slice_geo(g) : g;
-    CausalLayout cl = causal_layout(gs, rs);
+    const bool piped = causal_pipelined(rs);
+    const Geo gs = piped ? slice_geo(g) : g;
+    CausalLayout cl = piped ? split_layout(gs, rs) : causal_layout(gs);
     CausalArgs a;
     a.g = gs;
     a.H = p.H; a.L = p.L; a.seg_len = seg_len; a.nseg = G;
@@ -2236,9 +2857,10 @@ int tc_run(const void *q, const void *k, const void *v, const float *omega, floa
     a.state = state; a.meta = meta; a.nstate = nstate; a.pps = pl.pps; a.direct = direct ? 1 : 0;
     a.out_bf16 = p.out_bf16;
     a.o_w = cl.o_w; a.o_x = cl.o_x; a.o_v = cl.o_v; a.o_kb = cl.o_kb; a.o_small = cl.o_small;
-    a.o_recv = cl.o_recv;
+    a.o_recv = cl.o_recv; a.o_stage = cl.o_stage;
     a.tmem_cols = 512;
-    auto kern = p.out_bf16 ? tc_causal<true> : tc_causal<false>;
+    auto kern = piped ? (p.out_bf16 ? tc_causal_split<true> : tc_causal_split<false>)
+                      : (p.out_bf16 ? tc_causal<true> : tc_causal<false>);
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cl.bytes) != cudaSuccess)
         return FAVOR_ERR_CUDA;
     stats_begin(st, "tc_causal");
