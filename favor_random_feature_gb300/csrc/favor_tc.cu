@@ -838,6 +838,8 @@ struct CausalArgs {
     int nstate, pps, direct;       // pps pieces per segment; direct: combine the earlier pieces here
     int out_bf16;                  // out in bf16 (one [128][64] staging block) instead of fp32
     int *status;
+    void *out;                     // tc_causal_split: out [BH][L][dv] (fp32 or bf16), stored directly
+    int nslots;                    // tc_causal_split: receive slots (2: no slot-free handshake)
     uint32_t o_w, o_x, o_v, o_kb, o_small, o_recv, o_stage, tmem_cols;
 };
 
@@ -1469,19 +1471,27 @@ tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
 // the scan is software-pipelined by one chunk: the tensor core projects
 // chunk c + 1 and the epilogue forms its features while chunk c's masked
 // product A_m [V | 1] runs and its output is reduced and stored.
-//   control thread, per chunk c:  merged MMA (c) | S += phi_K^T [V | 1] (c) |
-//     P_K (c + 1) | A_m [V | 1] (c) | P_Q (c + 1) | loads | output store (c)
+//   control thread, per chunk c:  merged MMA (c) | P_K (c + 1) |
+//     S += phi_K^T [V | 1] (c) | A_m [V | 1] (c) | P_Q (c + 1) | loads
 //   epilogue, per chunk c:  masked, row-scaled A (c) | key features and
-//     state rows (c + 1) | query features (c + 1) | output (c) |
-//     phi_Q (c + 1) into TMEM | V (c + 1) | Q, K (c + 2) -> fp16
+//     state rows (c + 1) | query features (c + 1) | partial output (c), sent
+//     | phi_Q (c + 1) into TMEM | Q, K (c + 2) -> fp16 | output (c) gathered
+//     and stored | V (c + 1) -> fp16
 // TMEM: P [0, 128) | A_m [V | 1] at [128, 208), phi_Q (packed) there before
 // it (the merged MMA has consumed phi_Q when A_m V overwrites it) | [A |
 // phi_Q sigma S | phi_Q sigma z | query row sum] at [208, 416), A_m packed
 // in place (keys 32 j .. 32 j + 31 in columns 208 + 32 j .. + 15) | the
 // state [416, 496) (64 values, z).
 // Shared memory: W slice, Q and K tiles, V tile + ones atom, KB (phi_K 128
-// rows, sigma S^T 64, sigma z, ones) per 64 features, the output staging of
-// the CTA's rows, the small area, the receive slot of a split.
+// rows, sigma S^T 64, sigma z, ones) per 64 features, the small area, and one
+// or two receive slots: per sender, the numerators [4 column quarters][rows
+// 128 / rs][16] (each owner thread reads 64 contiguous bytes) and then
+// [rows][den, log2 scale, query row sum, pad].  With two slots (by chunk
+// parity) a sender never waits: it writes slot c % 2 only after it has
+// received the owner's partials of chunk c - 1, which the owner sends after it
+// has read slot c % 2 for chunk c - 2.  With one slot every owner warp tells
+// the senders when it has read it.  The owners store their rows straight to
+// global memory (64 contiguous bytes per thread).
 // ---------------------------------------------------------------------------
 constexpr int kPcP = 0, kPcAV = 128, kPcA = 208, kPcDX = 336, kPcDD = 400, kPcS = 416;
 // small-area float offsets of the split scan
@@ -1499,8 +1509,7 @@ __device__ void split_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem, cons
     const int nd = g.d / 64, ft0 = slice, nft_full = a.nft_full;
     const int rpo = kC / rs;
     const uint32_t xb = (uint32_t)kC * g.d * 2;
-    uint8_t *w = sm + a.o_w, *xq = sm + a.o_x, *xk = xq + xb, *xv = sm + a.o_v, *kb = sm + a.o_kb,
-            *stage = sm + a.o_stage;
+    uint8_t *w = sm + a.o_w, *xq = sm + a.o_x, *xk = xq + xb, *xv = sm + a.o_v, *kb = sm + a.o_kb;
     float *small = reinterpret_cast<float *>(sm + a.o_small);
     float *nk = small;             // [128] half key norms (log2 units)
     float *part = small + 128;     // [4][128] query row max
@@ -1511,11 +1520,21 @@ __device__ void split_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem, cons
     float *redv = small + kSpRedV; // [2][16] max |v| per warp, by chunk parity
     uint64_t *bars = reinterpret_cast<uint64_t *>(small + kSpBars);
     uint64_t *b_w = &bars[0], *b_x = &bars[1], *b_v = &bars[2], *b_pk = &bars[3], *b_pq = &bars[4],
-             *b_a = &bars[5], *b_s = &bars[6], *b_av = &bars[7], *b_st = &bars[8];
-    uint64_t *e_x = &bars[9], *e_pk = &bars[10], *e_q = &bars[11], *e_v = &bars[12], *e_b = &bars[13],
-             *e_out = &bars[14];
-    uint64_t *bar_recv = &bars[15], *bar_free = &bars[16];
-    float *recv = reinterpret_cast<float *>(sm + a.o_recv);
+             *b_a = &bars[5], *b_s = &bars[6], *b_av = &bars[7];
+    uint64_t *e_x = &bars[9], *e_pk = &bars[10], *e_q = &bars[11], *e_v = &bars[12], *e_b = &bars[13];
+    uint64_t *bar_free = &bars[16];
+    // receive slot s: its barrier, its numerators and its per-row scalars
+    const int nslots = a.nslots;
+    const size_t slot_floats = (size_t)(rs - 1) * rpo * kPartFloats;
+    auto bar_recv = [&](int slot) { return &bars[slot ? 17 : 15]; };
+    auto recv_num = [&](int slot, int sidx, int quarter, int lr) {
+        return reinterpret_cast<float *>(sm + a.o_recv) + slot * slot_floats +
+               ((size_t)(sidx * 4 + quarter) * rpo + lr) * 16;
+    };
+    auto recv_meta = [&](int slot, int sidx, int lr) {
+        return reinterpret_cast<float *>(sm + a.o_recv) + slot * slot_floats + (size_t)(rs - 1) * rpo * 64 +
+               ((size_t)sidx * rpo + lr) * 4;
+    };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int *abortp = reinterpret_cast<volatile int *>(small + kSpAbort);
     bool alive = true;
@@ -1543,15 +1562,6 @@ __device__ void split_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem, cons
                 for (int kk = 0; kk < g.d / 16; ++kk)
                     mma_f16(tmem + kPcP, smem_desc(x_s + (kk >> 2) * kBlk + (kk & 3) * 32, 16, 1024),
                             smem_desc(w_s + kk * 2048, (uint32_t)g.d * 128, 1024), idesc, kk > 0);
-            };
-            // this CTA's output rows of chunk c (a box of rpo rows), then the
-            // staging is free again
-            auto store_rows = [&](int c) {
-                tma_store_3d(tm_out, stage, 64 * dvt, t_begin + c * kC + slice * rpo, bh);
-                if (!OB16) tma_store_3d(tm_out, stage + rpo * 128, 64 * dvt + 32, t_begin + c * kC + slice * rpo, bh);
-                bulk_commit();
-                bulk_wait_read0();
-                mbar_arrive(b_st);
             };
             if (nchunk > 0) {
                 load_x(0);
@@ -1618,12 +1628,6 @@ __device__ void split_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem, cons
                                    smem_desc(v_s + kk * 2048, kBlk, 1024), idv, kk > 0);
                     mma_commit(b_av);
                 }
-                // chunk c - 1's output rows, staged by the epilogue at the end of
-                // its previous iteration
-                if (c > 0) {
-                    if (!(alive = ewait(e_out, (c - 1) & 1, abortp))) break;
-                    store_rows(c - 1);
-                }
                 // the next chunk's query projection, then its Q, K tiles
                 if (more) {
                     if (!(alive = ewait(e_pk, ph1, abortp))) break;
@@ -1637,8 +1641,7 @@ __device__ void split_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem, cons
                 if (!(alive = ewait(b_av, ph, abortp))) break;
                 if (more) load_v(c + 1);
             }
-            if (alive && nchunk > 0 && (alive = ewait(e_out, (nchunk - 1) & 1, abortp))) store_rows(nchunk - 1);
-            bulk_wait0();
+
             if (!alive) set_status(a.status, FAVOR_ERR_TIMEOUT);
         }
         return;
@@ -1990,22 +1993,21 @@ __device__ void split_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem, cons
                 sc = MAP == FAVOR_MAP_POSITIVE ? qoff_c + R_c : 0.f;
                 const int owner = row / rpo;
                 mine = owner == slice;
+                const int slot = nslots == 2 ? (c & 1) : 0;
                 if (!mine) {
-                    if (c > 0) alive &= cwait(bar_free, (c - 1) & 1, abortp);
-                    const int sidx = slice < owner ? slice : slice - 1;
-                    const uint32_t loc = smem_u32(recv + ((size_t)sidx * rpo + (row - owner * rpo)) * kPartFloats);
-                    const uint32_t rem = mapa_shared(loc, (uint32_t)owner);
-                    const uint32_t rbar = mapa_shared(smem_u32(bar_recv), (uint32_t)owner);
+                    if (nslots == 1 && c > 0) alive &= cwait(bar_free, (c - 1) & 1, abortp);
+                    const int sidx = slice < owner ? slice : slice - 1, lr = row - owner * rpo;
+                    const uint32_t rbar = mapa_shared(smem_u32(bar_recv(slot)), (uint32_t)owner);
+                    const uint32_t rnum = mapa_shared(smem_u32(recv_num(slot, sidx, j, lr)), (uint32_t)owner);
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc)
-                        st_async_v4(rem + (uint32_t)(16 * j + 4 * cc) * 4u, __float_as_uint(ov[4 * cc]),
-                                    __float_as_uint(ov[4 * cc + 1]), __float_as_uint(ov[4 * cc + 2]),
-                                    __float_as_uint(ov[4 * cc + 3]), rbar);
+                        st_async_v4(rnum + 16u * cc, __float_as_uint(ov[4 * cc]), __float_as_uint(ov[4 * cc + 1]),
+                                    __float_as_uint(ov[4 * cc + 2]), __float_as_uint(ov[4 * cc + 3]), rbar);
                     if (j == 0)
-                        st_async_v4(rem + 64u * 4u, __float_as_uint(den), __float_as_uint(sc), __float_as_uint(qsum),
-                                    0u, rbar);
+                        st_async_v4(mapa_shared(smem_u32(recv_meta(slot, sidx, lr)), (uint32_t)owner),
+                                    __float_as_uint(den), __float_as_uint(sc), __float_as_uint(qsum), 0u, rbar);
                 } else if (row == slice * rpo && j == 0) {
-                    mbar_arrive_expect_tx(bar_recv, (uint32_t)((rs - 1) * rpo * kPartFloats * 4));
+                    mbar_arrive_expect_tx(bar_recv(slot), (uint32_t)((rs - 1) * rpo * kPartFloats * 4));
                 }
             }
         }
@@ -2014,64 +2016,73 @@ __device__ void split_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem, cons
             store_q();
             if (c + 2 < nchunk) alive &= convert_x(c + 2);
         }
-        // ---------------- output of chunk c: gather, normalise, stage ----------------
+        // ---------------- output of chunk c: gather, normalise, store ----------------
         if (rs > 1) {
+            const int slot = nslots == 2 ? (c & 1) : 0;
             if (mine) {
-                alive &= cwait(bar_recv, ph, abortp);
-                const float *rp = recv + (size_t)(row - slice * rpo) * kPartFloats;
-                const size_t sstride = (size_t)rpo * kPartFloats;
+                alive &= cwait(bar_recv(slot), nslots == 2 ? (c >> 1) & 1 : ph, abortp);
+                const int lr = row - slice * rpo;
                 float smax = sc;
-                for (int k2 = 0; k2 < rs - 1; ++k2) smax = fmaxf(smax, rp[k2 * sstride + 65]);
+                for (int k2 = 0; k2 < rs - 1; ++k2) smax = fmaxf(smax, recv_meta(slot, k2, lr)[1]);
                 const float wl = ex2(sc - smax);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) ov[i] *= wl;
                 den *= wl;
                 qsum *= wl;
                 for (int k2 = 0; k2 < rs - 1; ++k2) {
-                    const float *pk = rp + k2 * sstride;
-                    const float wk = ex2(pk[65] - smax);
+                    const float4 *pn = reinterpret_cast<const float4 *>(recv_num(slot, k2, j, lr));
+                    const float4 pm = *reinterpret_cast<const float4 *>(recv_meta(slot, k2, lr));
+                    const float wk = ex2(pm.y - smax);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) ov[i] = fmaf(pk[16 * j + i], wk, ov[i]);
-                    den = fmaf(pk[64], wk, den);
-                    qsum = fmaf(pk[66], wk, qsum);
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const float4 v4 = pn[cc];
+                        ov[4 * cc] = fmaf(v4.x, wk, ov[4 * cc]);
+                        ov[4 * cc + 1] = fmaf(v4.y, wk, ov[4 * cc + 1]);
+                        ov[4 * cc + 2] = fmaf(v4.z, wk, ov[4 * cc + 2]);
+                        ov[4 * cc + 3] = fmaf(v4.w, wk, ov[4 * cc + 3]);
+                    }
+                    den = fmaf(pm.x, wk, den);
+                    qsum = fmaf(pm.z, wk, qsum);
                 }
             }
-            // the slot has been read: one arrival per owner warp at every sender
-            __syncwarp();
-            const int first = slice * rpo;
-            if (q * 32 + 31 >= first && q * 32 < first + rpo && lane == (first & 31))
-                for (int o2 = 0; o2 < rs; ++o2)
-                    if (o2 != slice) mbar_arrive_remote(mapa_shared(smem_u32(bar_free), (uint32_t)o2));
+            if (nslots == 1) {
+                // the slot has been read: one arrival per owner warp at every
+                // sender.  Relaxed: every value read from the slot has already
+                // fed the arithmetic above, so the reads are complete when the
+                // arrival is issued.
+                __syncwarp();
+                const int first = slice * rpo;
+                if (q * 32 + 31 >= first && q * 32 < first + rpo && lane == (first & 31))
+                    for (int o2 = 0; o2 < rs; ++o2)
+                        if (o2 != slice) mbar_arrive_remote_relaxed(mapa_shared(smem_u32(bar_free), (uint32_t)o2));
+            }
         }
-        {
+        if (mine) {
             const float id = __fdividef(1.f, den);
             // the range check: the denominator against the features' fp16
             // floor (keys so far x the row sum of the query features x the
             // flush level, with a 2^10 margin)
-            if (MAP == FAVOR_MAP_POSITIVE && mine && j == 0 && ok && den < (float)(tc0 + row + 1) * qsum * kRangeFloor)
+            if (MAP == FAVOR_MAP_POSITIVE && j == 0 && ok && den < (float)(tc0 + row + 1) * qsum * kRangeFloor)
                 flag_range(a.status);
-            // the staging is free once the previous chunk's store has read it
-            if (c > 0) alive &= ewait(b_st, (c - 1) & 1, abortp);
-            if (mine) {
-                const int lr = row - slice * rpo;   // row within this CTA's rows
+            if (ok) {
+                const size_t off = ((size_t)bh * a.L + tc0 + row) * g.dv + 64 * dvt + 16 * j;
                 if constexpr (OB16) {
-                    float o[16];
+                    uint32_t h[8];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) o[i] = ov[i] * id;
-                    stage_bf16_16(stage, lr, 16 * j, o);
-                } else {
-                    uint8_t *half = stage + (size_t)((16 * j) >> 5) * rpo * 128;
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        const int col = (16 * j + 4 * cc) & 31;
-                        const int p = (col >> 2) ^ (lr & 7);
-                        *reinterpret_cast<float4 *>(half + lr * 128 + p * 16) =
-                            make_float4(ov[4 * cc] * id, ov[4 * cc + 1] * id, ov[4 * cc + 2] * id, ov[4 * cc + 3] * id);
+                    for (int i = 0; i < 8; ++i) {
+                        const __nv_bfloat162 t2 = __floats2bfloat162_rn(ov[2 * i] * id, ov[2 * i + 1] * id);
+                        h[i] = *reinterpret_cast<const uint32_t *>(&t2);
                     }
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) + off);
+                    dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
+                    dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
+                } else {
+                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(a.out) + off);
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc)
+                        dst[cc] = make_float4(ov[4 * cc] * id, ov[4 * cc + 1] * id, ov[4 * cc + 2] * id, ov[4 * cc + 3] * id);
                 }
             }
-            fence_async_smem();
-            mbar_arrive(e_out);
         }
         // ---------------- chunk c + 1: V ----------------
         if (more) values(c + 1);
@@ -2095,9 +2106,10 @@ tc_causal_split(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         *abortp = 0;
         for (int i = 0; i < 9; ++i) mbar_init(&bars[i], 1);
         for (int i = 9; i < 15; ++i) mbar_init(&bars[i], kEpi);
-        // split features: the receive slot (one local arrival + the senders'
-        // bytes) and the slot-free barrier (one arrival per owner warp of
-        // every other CTA)
+        // split features: the receive slots (one local arrival + the senders'
+        // bytes; slot 0 in bars[15], slot 1 in bars[17]) and the slot-free
+        // barrier of a single slot (one arrival per owner warp of every
+        // other CTA)
         mbar_init(&bars[15], 1);
         const int rpo = kC / a.rs;
         mbar_init(&bars[16], a.rs > 1 ? (a.rs - 1) * 4 * max(1, rpo / 32) : 1);
@@ -2445,10 +2457,8 @@ CausalLayout causal_layout(const Geo &g) {
 }
 
 // The pipelined scan of 128 features per CTA (tc_causal_split): g is one
-// 128-feature slice; its own output staging (the CTA's 128 / rs rows: two
-// [rows][32] fp32 halves, or one [rows][64] bf16 block) and, for rs > 1, the
-// receive slot
-CausalLayout split_layout(const Geo &g, int rs) {
+// 128-feature slice; `nslots` receive slots for rs > 1
+CausalLayout split_layout(const Geo &g, int rs, int nslots) {
     CausalLayout l;
     const uint32_t rpo = (uint32_t)(kC / rs);
     uint32_t o = 0;
@@ -2457,11 +2467,14 @@ CausalLayout split_layout(const Geo &g, int rs) {
     l.o_v = o; o = align1k(o + 2 * kBlk);                   // V tile + ones atom
     l.o_kb = o; o = align1k(o + 2 * kKbBlk);
     l.o_small = o; o = align1k(o + kSpSmall * 4);
-    l.o_stage = o; o = align1k(o + 2 * rpo * 128);
-    l.o_recv = o; if (rs > 1) o = align1k(o + (uint32_t)(rs - 1) * rpo * kPartFloats * 4);
+    l.o_stage = 0;
+    l.o_recv = o; if (rs > 1) o = align1k(o + (uint32_t)nslots * (rs - 1) * rpo * kPartFloats * 4);
     l.bytes = o + 1024;
     return l;
 }
+
+// two receive slots where they fit
+int split_slots(const Geo &gs, int rs) { return split_layout(gs, rs, 2).bytes <= kSmemMax ? 2 : 1; }
 
 // One 128-feature slice of a head: the per-CTA geometry of a split scan
 // (positive and trig maps; a slice holds 128 features: 128 projections, or
@@ -2596,7 +2609,7 @@ int causal_split(const Problem &p) {
     if (p.map == FAVOR_MAP_ELU1 || p.r % 128 != 0) return 0;
     const int rs = p.r / 128;
     if (rs < 2 || rs > 8) return 0;
-    return split_layout(slice_geo(g), rs).bytes <= kSmemMax ? rs : 0;
+    return split_layout(slice_geo(g), rs, 1).bytes <= kSmemMax ? rs : 0;
 }
 
 // a split head: the pipelined scan of 128 features per CTA
@@ -2847,7 +2860,8 @@ int tc_run(const void *q, const void *k, const void *v, const float *omega, floa
     const int rs = std::max(1, pl.rs);
     const bool piped = causal_pipelined(rs);
     const Geo gs = piped ? slice_geo(g) : g;
-    CausalLayout cl = piped ? split_layout(gs, rs) : causal_layout(gs);
+    const int nslots = piped ? split_slots(gs, rs) : 1;
+    CausalLayout cl = piped ? split_layout(gs, rs, nslots) : causal_layout(gs);
     CausalArgs a;
     a.g = gs;
     a.H = p.H; a.L = p.L; a.seg_len = seg_len; a.nseg = G;
@@ -2858,6 +2872,7 @@ int tc_run(const void *q, const void *k, const void *v, const float *omega, floa
     a.out_bf16 = p.out_bf16;
     a.o_w = cl.o_w; a.o_x = cl.o_x; a.o_v = cl.o_v; a.o_kb = cl.o_kb; a.o_small = cl.o_small;
     a.o_recv = cl.o_recv; a.o_stage = cl.o_stage;
+    a.out = out; a.nslots = nslots;
     a.tmem_cols = 512;
     auto kern = piped ? (p.out_bf16 ? tc_causal_split<true> : tc_causal_split<false>)
                       : (p.out_bf16 ? tc_causal<true> : tc_causal<false>);
