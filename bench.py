@@ -46,15 +46,16 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM traffic (read + write bytes per launch) of a kernel from one ncu capture
 # (profiles/), valid while the kernel's source section is unchanged.
 TRAFFIC = {
-    ("tc_causal", "causal8k"): (309.22e6, "870bbdf81e04a577"),
-    ("tc_state", "causal8k"): (69.16e6, "be3b5bfdadbd00d1"),
-    ("tc_state", "nc4096"): (105.01e6, "be3b5bfdadbd00d1"),
-    ("tc_output", "nc4096"): (103.19e6, "3912a4eb0b80c731"),
+    ("tc_causal", "causal8k"): (309.77e6, "b342a4e72dc8da19"),
+    ("tc_causal", "long64k"): (309.42e6, "b342a4e72dc8da19"),
+    ("tc_causal_split", "sweep16k"): (308.60e6, "4671b0818f53bae7"),
     ("decode_step", "decode_b256"): (496.87e6, "74c42f3d2b49b28e"),
 }
 KERNEL_SECTIONS = {   # kernel: (source file, first line of its section, first line after it)
     "tc_causal": ("favor_tc.cu", "// tc_causal: the chunked causal scan, warp-specialised.",
-                  "// tc_output: non-causal rows"),
+                  "// tc_causal_split: the chunked causal scan of a head whose features are"),
+    "tc_causal_split": ("favor_tc.cu", "// tc_causal_split: the chunked causal scan of a head whose features are",
+                        "// tc_output: non-causal rows"),
     "tc_output": ("favor_tc.cu", "// tc_output: non-causal rows", "// host side"),
     "tc_state": ("favor_tc.cu", "// tc_state: per (feature group, piece, head) the state of a run of keys",
                  "// tc_combine:"),

@@ -2878,7 +2878,7 @@ int tc_run(const void *q, const void *k, const void *v, const float *omega, floa
                       : (p.out_bf16 ? tc_causal<true> : tc_causal<false>);
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cl.bytes) != cudaSuccess)
         return FAVOR_ERR_CUDA;
-    stats_begin(st, "tc_causal");
+    stats_begin(st, piped ? "tc_causal_split" : "tc_causal");
     if ((rc = rs > 1 ? launch_dependent_cluster(kern, dim3(rs * G, nvb, p.BH), dim3(kCausalThreads), cl.bytes, st, rs,
                                                 mq, mk, mv, mo, a)
                      : launch_dependent(kern, dim3(G, nvb, p.BH), dim3(kCausalThreads), cl.bytes, st, mq, mk, mv,
