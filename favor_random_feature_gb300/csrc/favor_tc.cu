@@ -2661,9 +2661,8 @@ Plan make_plan(const Problem &p) {
         pl.rs = causal_split(p);
         const int rs = std::max(1, pl.rs);
         int G = (int)std::lround((double)sms / ((double)p.BH * pl.nvb * rs));
-        // at most 64 segments: the combine keeps one scale per (piece, feature
-        // tile); a split scan combines the earlier segments itself (at most 4)
-        G = std::max(1, std::min(std::min(G, pl.nchunk), rs > 1 ? 4 : 64));
+        // at most 64 segments: the combine keeps one scale per (piece, feature tile)
+        G = std::max(1, std::min(std::min(G, pl.nchunk), 64));
         const int seg_chunks = (pl.nchunk + G - 1) / G;
         pl.G = (pl.nchunk + seg_chunks - 1) / seg_chunks;
         pl.seg_len = seg_chunks * kC;

@@ -161,6 +161,28 @@ def test_causal_many_chunks_per_cta(B, H, dv, heads):
     check_bf16(e, f"B={B} H={H} dv={dv}")
 
 
+@pytest.mark.parametrize("m,fmap", [(256, MAP_POSITIVE), (512, MAP_POSITIVE), (256, MAP_TRIG)],
+                         ids=["pos-r256", "pos-r512", "trig-r512"])
+def test_split_heads_many_segments(m, fmap):
+    """One head of a split feature set (d = dv = 128): its clusters scan many
+    segments, whose prefix states come from the state pass through the
+    combine pass (one key reference for every feature slice)."""
+    w = SWEEP16K.with_(m=m, feature_map=fmap)
+    inp = make_inputs(w, L=3000, B=1, H=1)
+    if fmap == MAP_TRIG:
+        inp = scaled_inputs(inp, 0.25)
+    out = run_gpu(inp, True, fmap)
+    ref = oracle_ref(inp, True, fmap)
+    if fmap == MAP_TRIG:
+        kap = causal_trig_condition(inp)
+        good = kap <= 10
+        assert good.mean() > 0.5
+        e = row_errors(out[good][:, None, None, :], ref[good][:, None, None, :])
+    else:
+        e = row_errors(out, ref)
+    check_bf16(e, f"m={m} map={fmap}")
+
+
 def test_causal_first_row_is_v0_and_last_row_matches_noncausal():
     inp = make_inputs(CAUSAL8K, L=300, B=1, H=2)
     oc = run_gpu(inp, True, MAP_POSITIVE)
