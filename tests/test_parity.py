@@ -364,7 +364,9 @@ def test_relu_and_softmax_scaled_trig(fmap, causal, dtype):
     (CAUSAL8K, True, MAP_TRIG, 700),
     (NC4096.with_(omega="iid"), True, MAP_RELU, 333),   # SIMT kernels
     (NC4096.with_(omega="iid"), False, MAP_TRIG_SOFTMAX, 333),
-], ids=["causal", "noncausal", "trig_causal", "relu_simt", "trig_softmax_simt"])
+    (SWEEP16K, True, MAP_POSITIVE, 700),     # feature-split scan (clusters of 2)
+    (SWEEP16K.with_(m=512), True, MAP_POSITIVE, 700),   # clusters of 4, one receive slot
+], ids=["causal", "noncausal", "trig_causal", "relu_simt", "trig_softmax_simt", "split2", "split4"])
 def test_bf16_output(w, causal, fmap, L):
     import torch
     import favor_random_feature_gb300 as fv
