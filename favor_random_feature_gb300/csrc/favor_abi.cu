@@ -194,7 +194,7 @@ extern "C" int favor_attn_forward(const void *q, const void *k, const void *v, c
     int rc = make_problem(B, H, L, d, dv, m, causal, feature_map, &p);
     if (rc) return rc;
     if ((rc = validate_args(q, k, v, omega, out, 2, p))) return rc;
-    if (tc_supported(p)) return tc_forward(q, k, v, omega, out, p, stream);
+    if (tc_forward_supported(p)) return tc_forward(q, k, v, omega, out, p, stream);
     return simt_forward(q, k, v, true, omega, out, p, stream);
 }
 
@@ -207,7 +207,7 @@ extern "C" int favor_attn_forward_bf16out(const void *q, const void *k, const vo
     p.out_bf16 = 1;
     float *o = static_cast<float *>(out);   // bf16 storage; the kernels take the element type from p
     if ((rc = validate_args(q, k, v, omega, o, 2, p))) return rc;
-    if (tc_supported(p)) return tc_forward(q, k, v, omega, o, p, stream);
+    if (tc_forward_supported(p)) return tc_forward(q, k, v, omega, o, p, stream);
     return simt_forward(q, k, v, true, omega, o, p, stream);
 }
 

@@ -18,6 +18,8 @@ struct Problem {
     int r;        // feature columns: m, 2m or d
     int BH;       // B * H
     int out_bf16 = 0;   // out stored as bf16 (else fp32)
+    int omega_rows = 0; // rows of the caller's omega per head (0: nproj); fewer
+                        // than nproj: the projections repeat them (tc_widen)
 };
 
 // elu1, relu: r = d features straight from x (no projection); trig and its
@@ -62,6 +64,12 @@ int simt_feature_map(const void *x, bool bf16_in, const float *omega, float *phi
 // Tensor-core path (tcgen05, fp16 operands, fp32 accumulation); returns
 // FAVOR_ERR_UNSUPPORTED for shapes it does not cover.
 bool tc_supported(const Problem &p);
+// A head of r = 64 features (positive m = 64, sin/cos m = 32, ELU+1 d = 64) as
+// one of 128 with every projection taken twice: numerator and denominator
+// both double, so the result is the same.  Other problems unchanged.
+Problem tc_widen(const Problem &p);
+// The forward entry points' test: the problem, widened, fits the kernels.
+bool tc_forward_supported(const Problem &p);
 int tc_forward(const void *q, const void *k, const void *v, const float *omega, float *out,
                const Problem &p, cudaStream_t stream);
 // Scratch bytes the tensor-core path needs for a problem, and the path run on

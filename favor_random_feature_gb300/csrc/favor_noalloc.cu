@@ -65,9 +65,10 @@ extern "C" int favor_attn_forward_noalloc(const void *q, const void *k, const vo
     if (rc) return rc;
     if ((rc = validate_args(q, k, v, omega, out, 2, p))) return rc;
     // the size check first: it needs no device and touches no pointer
-    if (tc_scratch_bytes(p) > kNoAllocScratchBytes) return FAVOR_ERR_UNSUPPORTED;
-    if (!tc_supported(p)) return FAVOR_ERR_UNSUPPORTED;
+    const Problem pw = tc_widen(p);
+    if (tc_scratch_bytes(pw) > kNoAllocScratchBytes) return FAVOR_ERR_UNSUPPORTED;
+    if (!tc_supported(pw)) return FAVOR_ERR_UNSUPPORTED;
     void *scratch = nullptr;
     if ((rc = scratch_address(&scratch))) return rc;
-    return tc_run(q, k, v, omega, out, p, stream, scratch, kNoAllocScratchBytes);
+    return tc_run(q, k, v, omega, out, pw, stream, scratch, kNoAllocScratchBytes);
 }

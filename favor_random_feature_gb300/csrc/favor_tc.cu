@@ -161,17 +161,20 @@ __device__ __forceinline__ float elu1(float p) { return p > 0.f ? p + 1.f : ex2(
 // (the B operand of P = X W^T with K = d), scaled by log2(e) for the
 // positive map; the identity for elu1.
 // ---------------------------------------------------------------------------
+// rows: rows of the caller's omega per head; projection p takes row p % rows
+// (rows < nproj: a widened head, every projection twice)
 __global__ void tc_prep_omega(const float *__restrict__ omega, uint8_t *__restrict__ img, int H,
-                              int nproj, int d, int map) {
+                              int nproj, int d, int map, int rows) {
     grid_dep_launch();
     const int h = blockIdx.y;
     const size_t per = (size_t)nproj * d;
     for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < per;
          e += (size_t)gridDim.x * blockDim.x) {
         int p = (int)(e / d), j = (int)(e % d);
+        const int src = p % rows;
         float w;
-        if (map == FAVOR_MAP_ELU1) w = (p == j) ? 1.f : 0.f;
-        else w = omega[(size_t)h * per + e] * (map == FAVOR_MAP_POSITIVE ? kLog2e : 1.f);
+        if (map == FAVOR_MAP_ELU1) w = (src == j) ? 1.f : 0.f;
+        else w = omega[((size_t)h * rows + src) * d + j] * (map == FAVOR_MAP_POSITIVE ? kLog2e : 1.f);
         uint8_t *atom = img + (size_t)h * per * 2 + (size_t)(p / 64) * d * 128;
         *reinterpret_cast<__half *>(atom + sw128_offset(j, p % 64)) = __float2half_rn(w);
     }
@@ -2616,6 +2619,18 @@ int causal_split(const Problem &p) {
 bool causal_pipelined(int rs) { return rs > 1; }
 }  // namespace
 
+Problem tc_widen(const Problem &p) {
+    if (p.r != 64 || p.map == FAVOR_MAP_RELU || p.map == FAVOR_MAP_TRIG_SOFTMAX) return p;
+    Problem w = p;
+    w.omega_rows = p.nproj;
+    w.nproj = 2 * p.nproj;
+    w.r = 128;
+    w.m = 2 * p.m;
+    return w;
+}
+
+bool tc_forward_supported(const Problem &p) { return tc_supported(tc_widen(p)); }
+
 bool tc_supported(const Problem &p) {
     // ReLU and the softmax-scaled Fourier map run on the SIMT kernels
     if (p.map == FAVOR_MAP_RELU || p.map == FAVOR_MAP_TRIG_SOFTMAX) return false;
@@ -2765,7 +2780,8 @@ int tc_key_state(const void *k, const void *v, const float *omega, const Problem
     if ((rc = make_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.BH, p.L, p.d, 64)) ||
         (rc = make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.BH, p.L, p.dv, 64)))
         return rc;
-    tc_prep_omega<<<dim3(32, p.H), 256, 0, st>>>(omega, img, p.H, p.nproj, p.d, p.map);
+    tc_prep_omega<<<dim3(32, p.H), 256, 0, st>>>(omega, img, p.H, p.nproj, p.d, p.map,
+                                                 p.omega_rows ? p.omega_rows : p.nproj);
     FAVOR_LAUNCH_CHECK();
     if ((rc = launch_state(p, g, pl, img, state, meta, mk, mv, st, false))) return rc;
     *state_out = state;
@@ -2775,7 +2791,8 @@ int tc_key_state(const void *k, const void *v, const float *omega, const Problem
 }
 
 int tc_forward(const void *q, const void *k, const void *v, const float *omega, float *out,
-               const Problem &p, cudaStream_t st) {
+               const Problem &p0, cudaStream_t st) {
+    const Problem p = tc_widen(p0);
     int status = FAVOR_OK;
     const size_t bytes = tc_scratch_bytes(p);
     void *ws = workspace(bytes, &status);
@@ -2809,7 +2826,8 @@ int tc_run(const void *q, const void *k, const void *v, const float *omega, floa
                          : make_map(&mo, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.BH, p.L, p.dv, 32, out_rows)))
         return rc;
 
-    tc_prep_omega<<<dim3(32, p.H), 256, 0, st>>>(omega, img, p.H, p.nproj, p.d, p.map);
+    tc_prep_omega<<<dim3(32, p.H), 256, 0, st>>>(omega, img, p.H, p.nproj, p.d, p.map,
+                                                 p.omega_rows ? p.omega_rows : p.nproj);
     FAVOR_LAUNCH_CHECK();
 
     if (nstate > 0) {

@@ -22,7 +22,10 @@
  *     E[phi(q).phi(k)] = exp(q.k)                                             (r = 2m)
  *       -- "Kernel Feature Maps", section 3 (the additional scaling that turns
  *          the Gaussian-kernel estimate into a softmax-kernel estimate).
- *   ReLU and the softmax-scaled map run on the fp32 SIMT kernels.
+ *   ReLU and the softmax-scaled map run on the fp32 SIMT kernels.  A head of
+ *   r = 64 features (positive m = 64, sin/cos m = 32, ELU+1 d = 64) runs on
+ *   the tensor-core kernels as one of 128 with every projection taken twice:
+ *   numerator and denominator both double, so out is the same.
  *
  *   non-causal:  out_i = phi(q_i)^T (sum_j phi(k_j) v_j^T) / phi(q_i)^T (sum_j phi(k_j))
  *       -- Performer page In[25] (performer_attention, with eps = 0) and the
@@ -36,7 +39,8 @@
  * per-head running key maximum); both cancel exactly in the ratio.
  *
  * Range of the tensor-core path (favor_attn_forward and its variants; the
- * fp32 entry points compute every feature in fp32 and have no such limit).
+ * fp32 entry points compute every feature in fp32, where the same underflow
+ * comes only for a key some e^80 below the head's largest key feature).
  * Its MMA operands are fp16, whose finite range is 2^-24 .. 65504:
  *   - q, k and v values must be finite with |x| <= 65280 (the largest bf16
  *     value below fp16's 65504);

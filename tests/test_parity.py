@@ -183,6 +183,39 @@ def test_split_heads_many_segments(m, fmap):
     check_bf16(e, f"m={m} map={fmap}")
 
 
+WIDENED = [(MAP_POSITIVE, 64, 64), (MAP_POSITIVE, 128, 64), (MAP_TRIG, 64, 32), (MAP_ELU1, 64, 64)]
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["noncausal", "causal"])
+@pytest.mark.parametrize("fmap,d,m", WIDENED, ids=["pos-d64", "pos-d128", "trig-d64", "elu1-d64"])
+def test_r64_heads_on_the_tensor_cores(fmap, d, m, causal):
+    """r = 64 features run on the tensor-core kernels as r = 128 with every
+    projection taken twice (numerator and denominator double, the ratio does
+    not change): the tensor-core kernels must run, and the rows must meet the
+    bf16 bar against the oracle's r = 64 result."""
+    import favor_random_feature_gb300 as fv
+    w = SWEEP16K.with_(feature_map=fmap, d=d, dv=d, m=m, omega="iid")
+    inp = make_inputs(w, L=700, B=1, H=2)
+    if fmap == MAP_TRIG:
+        inp = scaled_inputs(inp, 0.25)
+    fv.favor_stats_enable(True)
+    try:
+        out = run_gpu(inp, causal, fmap)
+        st = fv.favor_stats_read()
+    finally:
+        fv.favor_stats_enable(False)
+    assert st.dominant_kernel.decode().startswith("tc_"), st.dominant_kernel
+    ref = oracle_ref(inp, causal, fmap)
+    if fmap == MAP_TRIG:
+        kap = causal_trig_condition(inp) if causal else trig_condition(inp)
+        good = kap <= 10
+        assert good.mean() > 0.5
+        e = row_errors(out[good][:, None, None, :], ref[good][:, None, None, :])
+    else:
+        e = row_errors(out, ref)
+    check_bf16(e, f"r=64 map={fmap} d={d}")
+
+
 def test_causal_first_row_is_v0_and_last_row_matches_noncausal():
     inp = make_inputs(CAUSAL8K, L=300, B=1, H=2)
     oc = run_gpu(inp, True, MAP_POSITIVE)
@@ -292,8 +325,9 @@ def test_full_size_sweep_sampled(m):
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("w,causal,kernel", [(CAUSAL8K, True, "tc_causal"),
                                              (NC4096, False, "tc_state"),
-                                             (SWEEP16K.with_(m=128), True, "tc_causal")],
-                         ids=["causal", "noncausal", "d128"])
+                                             (SWEEP16K.with_(m=128), True, "tc_causal"),
+                                             (SWEEP16K.with_(m=64), True, "tc_causal")],
+                         ids=["causal", "noncausal", "d128", "d128-r64"])
 def test_tensor_core_path_taken(w, causal, kernel):
     import favor_random_feature_gb300 as fv
     inp = make_inputs(w, L=512, B=1, H=2)

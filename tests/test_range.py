@@ -11,7 +11,7 @@ the fp32 bar."""
 import numpy as np
 import pytest
 
-from favor_inputs import CAUSAL8K, MAP_POSITIVE, bf16_bits, bf16_to_f32, make_inputs
+from favor_inputs import CAUSAL8K, MAP_POSITIVE, SWEEP16K, bf16_bits, bf16_to_f32, make_inputs
 from parity_util import oracle_ref, row_errors, run_gpu, to_device
 
 pytestmark = pytest.mark.gpu
@@ -65,11 +65,11 @@ def _f32_entry(inp, causal):
     return run_gpu(f, causal, MAP_POSITIVE)
 
 
-def wide_spread_inputs():
+def wide_spread_inputs(w=CAUSAL8K):
     """Keys in blocks of 128 scaled x0.5, x1 and x2.5 around N(0,1) d^-1/4, one
     key per chunk scaled x4 at position 120 (after the chunk's other keys), and
     values with a few entries near +-6e4."""
-    inp = make_inputs(CAUSAL8K, L=L, B=1, H=2)
+    inp = make_inputs(w, L=L, B=1, H=2)
     k = inp.k32.copy()
     scale = np.resize(np.repeat([0.5, 1.0, 2.5], 128), L).astype(np.float32)
     k *= scale[None, None, :, None]
@@ -77,32 +77,40 @@ def wide_spread_inputs():
     v = inp.v32.copy()
     rng = np.random.default_rng(123)
     idx = rng.choice(L, 6, replace=False)
-    v[0, 0, idx, rng.integers(0, 64, 6)] = np.float32(6.0e4) * np.sign(rng.standard_normal(6)).astype(np.float32)
+    v[0, 0, idx, rng.integers(0, v.shape[-1], 6)] = np.float32(6.0e4) * np.sign(rng.standard_normal(6)).astype(np.float32)
     return _with(inp, k=k, v=v)
 
 
-@pytest.mark.parametrize("causal", [True, False], ids=["causal", "noncausal"])
-def test_wide_key_norm_spread_meets_the_bar(causal):
+@pytest.mark.parametrize("causal,w", [(True, CAUSAL8K), (False, CAUSAL8K), (True, SWEEP16K)],
+                         ids=["causal", "noncausal", "causal-split"])
+def test_wide_key_norm_spread_meets_the_bar(causal, w):
     import favor_random_feature_gb300 as fv
-    inp = wide_spread_inputs()
+    inp = wide_spread_inputs(w)
     out, st = _call_status(inp, causal)
     assert st == fv.FAVOR_OK, fv.strerror(st)
     e = row_errors(out, oracle_ref(inp, causal, MAP_POSITIVE))
     assert e.max() <= BF16_MAX and e.mean() <= BF16_MEAN, (e.max(), e.mean())
 
 
-@pytest.mark.parametrize("causal", [True, False], ids=["causal", "noncausal"])
-def test_key_on_a_projection_row_reports_range(causal):
-    """A key equal to the longest row of omega has a feature about e^45 above
-    the other keys': theirs underflow fp16 at its reference while queries
-    that barely see it still need them.  The call must say so; the fp32 entry
-    point computes the same values within the fp32 bar."""
+@pytest.mark.parametrize("causal,w", [(True, CAUSAL8K), (False, CAUSAL8K), (True, SWEEP16K)],
+                         ids=["causal", "noncausal", "causal-split"])
+def test_key_on_a_projection_row_reports_range(causal, w):
+    """A key along the longest row w_f of omega, k = a w_f, has the feature
+    exp(|w_f|^2 (a - a^2/2)) against about e^0 for the other keys: a = 1 at
+    d = 64 (|w_f|^2 / 2 ~ 48), a < 1 at d = 128 so that the gap is also e^48
+    (at a = 1 it would be ~e^90, past fp32's own e^-87).  The other keys'
+    features underflow fp16 at its reference while queries that barely see
+    it still need them.  The call must say so; the fp32 entry point computes
+    the same values within the fp32 bar."""
     import favor_random_feature_gb300 as fv
-    inp = make_inputs(CAUSAL8K, L=L, B=1, H=2)
+    inp = make_inputs(w, L=L, B=1, H=2)
     k = inp.k32.copy()
     for h in range(2):
         f = int(np.argmax(np.linalg.norm(inp.omega[h], axis=1)))
-        k[0, h, 500] = inp.omega[h, f]
+        n2 = float(np.sum(inp.omega[h, f].astype(np.float64) ** 2))
+        gap = min(n2 / 2, 48.5)
+        a = 1.0 - np.sqrt(1.0 - 2.0 * gap / n2)
+        k[0, h, 500] = a * inp.omega[h, f]
     inp = _with(inp, k=k)
     _, st = _call_status(inp, causal)
     assert st == fv.FAVOR_ERR_RANGE, fv.strerror(st)
@@ -111,14 +119,15 @@ def test_key_on_a_projection_row_reports_range(causal):
 
 
 @pytest.mark.parametrize("which", ["q", "k", "v"])
-def test_operand_beyond_fp16_reports_range(which):
+@pytest.mark.parametrize("w", [CAUSAL8K, SWEEP16K], ids=["whole", "split"])
+def test_operand_beyond_fp16_reports_range(which, w):
     """A value of 7e4 (bf16 69632) has no finite fp16 image."""
     import favor_random_feature_gb300 as fv
-    inp = make_inputs(CAUSAL8K, L=300, B=1, H=2)
+    inp = make_inputs(w, L=300, B=1, H=2)
     x = getattr(inp, which + "32").copy()
     x[0, 1, 77, 5] = 7.0e4
     inp = _with(inp, **{which: x})
-    for causal in (True, False):
+    for causal in ((True, False) if w is CAUSAL8K else (True,)):
         _, st = _call_status(inp, causal)
         assert st == fv.FAVOR_ERR_RANGE, (which, causal, fv.strerror(st))
 

@@ -39,6 +39,13 @@ def test_noalloc_matches_forward_on_two_calls_in_a_row():
                 (make_inputs(NC4096, L=1500, B=2, H=2), False)])
 
 
+def test_noalloc_matches_forward_on_r64_heads():
+    """m = 64 (each projection taken twice on the tensor cores) through both
+    entry points: the same widened problem, the same bits."""
+    _same_bits([(make_inputs(CAUSAL8K.with_(m=64), L=1500, B=2, H=2), True),
+                (make_inputs(NC4096.with_(m=64), L=1100, B=1, H=3), False)])
+
+
 def test_noalloc_at_the_benchmark_shapes():
     """B=4, H=16, L=8192 causal and B=8, H=12, L=4096 non-causal (d=dv=64,
     m=256): both fit the array and return FAVOR_OK with the same bits."""
