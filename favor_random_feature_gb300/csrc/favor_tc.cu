@@ -1500,6 +1500,7 @@ constexpr int kPcP = 0, kPcAV = 128, kPcA = 208, kPcDX = 336, kPcDD = 400, kPcS 
 // small-area float offsets of the split scan
 constexpr int kSpRedM = 1696, kSpRedV = 1728, kSpBars = 1760, kSpTslot = 1800, kSpAbort = 1802, kSpSmall = 1808;
 constexpr int kSpNumBars = 18;
+static_assert(kSpBars + 2 * kSpNumBars <= kSpTslot, "the split scan's mbarriers overlap the TMEM slot");
 
 template <int NC, int MAP, bool OB16>
 __device__ void split_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem, const CUtensorMap *tm_q,
@@ -2147,10 +2148,14 @@ tc_causal_split(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 // ---------------------------------------------------------------------------
 // tc_output: non-causal rows, warp-specialised like tc_causal.  The grid is a
 // flat list of (head, dv tile, 128-row chunk) units split evenly over about
-// one CTA per SM; a CTA reloads W and the state operand when its units move to
-// another head.  Per unit: P_Q = Q W^T (N = all projections) -> phi(Q) packed
-// into TMEM -> D = phi(Q) [sigma KV | sigma z] (N = 64 + 16, B MN-major) ->
-// out = D[:, :64] / D[:, 64] (sigma cancels).
+// one CTA per SM; a CTA reloads W when its units move to another head and the
+// state operand when they move to another (head, dv tile).  Per unit: P_Q =
+// Q W^T (N = all projections) -> phi(Q) packed into TMEM -> D = phi(Q)
+// [sigma KV | sigma z] (N = 64 + 16, B MN-major) -> out = D[:, :64] / D[:, 64]
+// (sigma cancels).
+// The units are pipelined by one: the epilogue forms the features of unit
+// i + 1 in registers while the tensor core computes D(i), then writes the
+// output of unit i and stores phi_Q(i + 1) into the columns D(i) has read.
 // ---------------------------------------------------------------------------
 struct OutputArgs {
     Geo g;
@@ -2162,6 +2167,10 @@ struct OutputArgs {
 };
 
 constexpr int kOutThreads = 32 + kEpi;
+// the small block, in floats: row maxima [2][4][128] (by unit parity), the
+// mbarriers, the TMEM slot, the abort flag
+constexpr int kOutBars = 1024, kOutNumBars = 9, kOutSlot = 1044, kOutAbort = 1046, kOutSmall = 1048;
+static_assert(kOutBars + 2 * kOutNumBars <= kOutSlot, "tc_output's mbarriers overlap the TMEM slot");
 
 template <int NC, int MAP>
 __device__ void output_body(const OutputArgs &a, uint8_t *sm, uint32_t tmem,
@@ -2176,11 +2185,11 @@ __device__ void output_body(const OutputArgs &a, uint8_t *sm, uint32_t tmem,
     const uint32_t xb = (uint32_t)kC * g.d * 2;
     uint8_t *w = sm + a.o_w, *sbuf = sm + a.o_s, *xs = sm + a.o_x, *stage = sm + a.o_stage;
     float *small = reinterpret_cast<float *>(sm + a.o_small);
-    float *part = small;            // [4][128]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(small + 544);
+    float *part = small;            // [2][4][128]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(small + kOutBars);
     uint64_t *bar_w = &bars[0], *bar_x = &bars[1] /*[2]*/, *bar_pq = &bars[3], *bar_d = &bars[4],
-             *e_x = &bars[5], *e_q = &bars[6];
-    volatile int *abortp = reinterpret_cast<volatile int *>(small + 570);
+             *bar_s = &bars[5], *e_x = &bars[6], *e_p = &bars[7], *e_q = &bars[8];
+    volatile int *abortp = reinterpret_cast<volatile int *>(small + kOutAbort);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // TMEM: projections [0, nproj) | D = [phi_Q sigma KV | phi_Q sigma z] [256, 336) |
     // phi_Q packed [336, 336 + r/2)
@@ -2195,14 +2204,17 @@ __device__ void output_body(const OutputArgs &a, uint8_t *sm, uint32_t tmem,
         if (lane == 0 && n > 0) {
             const uint32_t w_s = smem_u32(w), s_s = smem_u32(sbuf), xs_s = smem_u32(xs);
             const uint32_t wbytes = (uint32_t)g.nproj * g.d * 2, atom = (uint32_t)g.r * 128;
-            int wphase = 0;
-            auto load_operands = [&](int u) {
+            int wphase = 0, sphase = 0;
+            auto load_w = [&](int u) {
+                mbar_arrive_expect_tx(bar_w, wbytes);
+                bulk_load(w, a.omg + (size_t)(unit_bh(u) % a.H) * wbytes, wbytes, bar_w);
+            };
+            auto load_state = [&](int u) {
                 const int bh = unit_bh(u), dvt = unit_dvt(u);
-                mbar_arrive_expect_tx(bar_w, wbytes + 2 * atom);
-                bulk_load(w, a.omg + (size_t)(bh % a.H) * wbytes, wbytes, bar_w);
+                mbar_arrive_expect_tx(bar_s, 2 * atom);
                 const uint8_t *img = a.sop + (size_t)bh * (nvb + 1) * atom;
-                bulk_load(sbuf, img + (size_t)dvt * atom, atom, bar_w);
-                bulk_load(sbuf + atom, img + (size_t)nvb * atom, atom, bar_w);
+                bulk_load(sbuf, img + (size_t)dvt * atom, atom, bar_s);
+                bulk_load(sbuf + atom, img + (size_t)nvb * atom, atom, bar_s);
             };
             auto load_q = [&](int i) {
                 const int u = u0 + i, s = i % nq;
@@ -2221,7 +2233,8 @@ __device__ void output_body(const OutputArgs &a, uint8_t *sm, uint32_t tmem,
             auto key_of = [&](int u) { return unit_bh(u) * nvb + unit_dvt(u); };
             for (int i = 0; i < min(n, nq); ++i) load_q(i);
             grid_dep_wait();   // the W and state images come from the kernels before this one
-            load_operands(u0);
+            load_w(u0);
+            load_state(u0);
             alive = ewait(bar_w, wphase & 1, abortp) && ewait(e_x, 0, abortp);
             ++wphase;
             if (alive) {
@@ -2232,7 +2245,27 @@ __device__ void output_body(const OutputArgs &a, uint8_t *sm, uint32_t tmem,
                 // P_Q(i) done: its Q slot takes unit i + nq
                 if (!(alive = ewait(bar_pq, i & 1, abortp))) break;
                 if (i + nq < n) load_q(i + nq);
+                if (i + 1 < n) {
+                    if (unit_bh(u0 + i + 1) != unit_bh(u0 + i)) {
+                        // P_Q(i) was the last reader of the old W
+                        load_w(u0 + i + 1);
+                        if (!(alive = ewait(bar_w, wphase & 1, abortp))) break;
+                        ++wphase;
+                    }
+                    // the epilogue holds P(i) in registers and has converted Q(i + 1)
+                    if (!(alive = ewait(e_p, i & 1, abortp) && ewait(e_x, (i + 1) & 1, abortp))) break;
+                    tc_fence_after();
+                    issue_pq(i + 1);
+                }
+                // phi_Q(i) is in TMEM (and the epilogue has read D(i - 1))
                 if (!(alive = ewait(e_q, i & 1, abortp))) break;
+                if (i == 0 || key_of(u0 + i) != key_of(u0 + i - 1)) {
+                    // D(i - 1) was the last reader of the old state operand
+                    if (i > 0 && !(alive = ewait(bar_d, (i - 1) & 1, abortp))) break;
+                    if (i > 0) load_state(u0 + i);
+                    if (!(alive = ewait(bar_s, sphase & 1, abortp))) break;
+                    ++sphase;
+                }
                 tc_fence_after();
                 {
                     // D = phi_Q [sigma KV | sigma z] (B MN-major: the state atom, then the z atom)
@@ -2241,19 +2274,6 @@ __device__ void output_body(const OutputArgs &a, uint8_t *sm, uint32_t tmem,
                         mma_f16_ts(tmem + kColD, tmem + kColPhi + 8 * kk, smem_desc(s_s + kk * 2048, atom, 1024),
                                    idesc, kk > 0);
                     mma_commit(bar_d);
-                }
-                if (i + 1 < n) {
-                    if (key_of(u0 + i + 1) != key_of(u0 + i)) {
-                        // new head / dv tile: every MMA on the old operands completes first
-                        if (!(alive = ewait(bar_d, i & 1, abortp))) break;
-                        load_operands(u0 + i + 1);
-                        if (!(alive = ewait(bar_w, wphase & 1, abortp))) break;
-                        ++wphase;
-                    }
-                    // P_Q(i + 1) while the epilogue turns D(i) into the output
-                    if (!(alive = ewait(e_x, (i + 1) & 1, abortp))) break;
-                    tc_fence_after();
-                    issue_pq(i + 1);
                 }
             }
             if (!alive) set_status(a.status, FAVOR_ERR_TIMEOUT);
@@ -2273,72 +2293,9 @@ __device__ void output_body(const OutputArgs &a, uint8_t *sm, uint32_t tmem,
         mbar_arrive(e_x);
         return ok;
     };
-    if (n > 0) alive = convert_x(0);
-    const uint32_t pcol = tm_addr(tmem, q, NC * j);
-    for (int i = 0; i < n; ++i) {
+    // the output of unit i from D(i)
+    auto write_output = [&](int i) {
         const int u = u0 + i;
-        // ---- query features -> phi_Q packed in TMEM [kColPhi, kColPhi + r/2) ----
-        alive &= ewait(bar_pq, i & 1, abortp);
-        tc_fence_after();
-        if constexpr (MAP == FAVOR_MAP_POSITIVE) {
-            float mx = -INFINITY;
-#pragma unroll
-            for (int b = 0; b < NC / 32; ++b) {
-                float t32[32];
-                tmem_ld32(pcol + 32 * b, t32);
-                tmem_ld_wait();
-                mx = fmaxf(mx, max_of(t32));
-            }
-            part[j * 128 + row] = mx;
-            group_sync(kEpi);
-            const float qoff = fmaxf(fmaxf(part[row], part[128 + row]), fmaxf(part[256 + row], part[384 + row])) - kShift;
-#pragma unroll
-            for (int b = 0; b < NC / 16; ++b) {
-                float t16[16];
-                tmem_ld16(pcol + 16 * b, t16);
-                tmem_ld_wait();
-                uint32_t o[8];
-#pragma unroll
-                for (int k2 = 0; k2 < 8; ++k2) o[k2] = pack_half2(ex2(t16[2 * k2] - qoff), ex2(t16[2 * k2 + 1] - qoff));
-                tmem_st8(tm_addr(tmem, q, kColPhi + (NC * j + 16 * b) / 2), o);
-            }
-        } else if constexpr (MAP == FAVOR_MAP_TRIG) {
-            const int fs = 128 * ((NC * j) / 64) + (NC * j) % 64;
-#pragma unroll
-            for (int b = 0; b < NC / 16; ++b) {
-                float t16[16];
-                tmem_ld16(pcol + 16 * b, t16);
-                tmem_ld_wait();
-                uint32_t os[8], oc[8];
-#pragma unroll
-                for (int k2 = 0; k2 < 8; ++k2) {
-                    float s0, c0, s1, c1;
-                    sincos_reduced(t16[2 * k2], s0, c0);
-                    sincos_reduced(t16[2 * k2 + 1], s1, c1);
-                    os[k2] = pack_half2(s0, s1);
-                    oc[k2] = pack_half2(c0, c1);
-                }
-                tmem_st8(tm_addr(tmem, q, kColPhi + (fs + 16 * b) / 2), os);
-                tmem_st8(tm_addr(tmem, q, kColPhi + (fs + 64 + 16 * b) / 2), oc);
-            }
-        } else {
-#pragma unroll
-            for (int b = 0; b < NC / 16; ++b) {
-                float t16[16];
-                tmem_ld16(pcol + 16 * b, t16);
-                tmem_ld_wait();
-                uint32_t o[8];
-#pragma unroll
-                for (int k2 = 0; k2 < 8; ++k2) o[k2] = pack_half2(elu1(t16[2 * k2]), elu1(t16[2 * k2 + 1]));
-                tmem_st8(tm_addr(tmem, q, kColPhi + (NC * j + 16 * b) / 2), o);
-            }
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(e_q);   // also: the projections have been read
-        // ---- next unit's Q tile (while the tensor core computes D and P_Q) ----
-        if (i + 1 < n) alive &= convert_x(i + 1);
-        // ---- output ----
         alive &= ewait(bar_d, i & 1, abortp);
         tc_fence_after();
         float dn[16], dd, qs = 0.f;
@@ -2379,7 +2336,99 @@ __device__ void output_body(const OutputArgs &a, uint8_t *sm, uint32_t tmem,
                 tma_store_3d(tm_out, stage + kBlk, 64 * unit_dvt(u) + 32, unit_c(u) * kC, unit_bh(u));
             bulk_commit();
         }
+    };
+    if (n > 0) alive = convert_x(0);
+    const uint32_t pcol = tm_addr(tmem, q, NC * j);
+    // packed fp16 features of the thread's row: NC / 2 pairs (the sin/cos map:
+    // NC / 2 sine pairs, then NC / 2 cosine pairs)
+    constexpr int NH = MAP == FAVOR_MAP_TRIG ? NC : NC / 2;
+    for (int i = 0; i < n; ++i) {
+        // ---- query features of unit i -> registers ----
+        alive &= ewait(bar_pq, i & 1, abortp);
+        tc_fence_after();
+        uint32_t hp[NH];
+        if constexpr (MAP == FAVOR_MAP_POSITIVE) {
+            float mx = -INFINITY;
+#pragma unroll
+            for (int b = 0; b < NC / 32; ++b) {
+                float t32[32];
+                tmem_ld32(pcol + 32 * b, t32);
+                tmem_ld_wait();
+                mx = fmaxf(mx, max_of(t32));
+            }
+            float *pm = part + (i & 1) * 512;
+            pm[j * 128 + row] = mx;
+            group_sync(kEpi);
+            const float qoff = fmaxf(fmaxf(pm[row], pm[128 + row]), fmaxf(pm[256 + row], pm[384 + row])) - kShift;
+#pragma unroll
+            for (int b = 0; b < NC / 16; ++b) {
+                float t16[16];
+                tmem_ld16(pcol + 16 * b, t16);
+                tmem_ld_wait();
+#pragma unroll
+                for (int k2 = 0; k2 < 8; ++k2)
+                    hp[8 * b + k2] = pack_half2(ex2(t16[2 * k2] - qoff), ex2(t16[2 * k2 + 1] - qoff));
+            }
+        } else if constexpr (MAP == FAVOR_MAP_TRIG) {
+#pragma unroll
+            for (int b = 0; b < NC / 16; ++b) {
+                float t16[16];
+                tmem_ld16(pcol + 16 * b, t16);
+                tmem_ld_wait();
+#pragma unroll
+                for (int k2 = 0; k2 < 8; ++k2) {
+                    float s0, c0, s1, c1;
+                    sincos_reduced(t16[2 * k2], s0, c0);
+                    sincos_reduced(t16[2 * k2 + 1], s1, c1);
+                    hp[8 * b + k2] = pack_half2(s0, s1);
+                    hp[NC / 2 + 8 * b + k2] = pack_half2(c0, c1);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int b = 0; b < NC / 16; ++b) {
+                float t16[16];
+                tmem_ld16(pcol + 16 * b, t16);
+                tmem_ld_wait();
+#pragma unroll
+                for (int k2 = 0; k2 < 8; ++k2) hp[8 * b + k2] = pack_half2(elu1(t16[2 * k2]), elu1(t16[2 * k2 + 1]));
+            }
+        }
+        tc_fence_before();
+        mbar_arrive(e_p);   // the projections have been read: P_Q(i + 1) may overwrite them
+        // ---- next unit's Q tile (while the tensor core computes D(i - 1) and P_Q(i + 1)) ----
+        if (i + 1 < n) alive &= convert_x(i + 1);
+        // ---- output of unit i - 1; D(i - 1) has then read phi_Q(i - 1) ----
+        if (i > 0) write_output(i - 1);
+        // ---- phi_Q(i) -> TMEM [kColPhi, kColPhi + r/2) ----
+        if constexpr (MAP == FAVOR_MAP_TRIG) {
+            // projection p: sine at feature 128 (p / 64) + p % 64, cosine 64 further
+            const int fs = 128 * ((NC * j) / 64) + (NC * j) % 64;
+#pragma unroll
+            for (int b = 0; b < NC / 16; ++b) {
+                uint32_t os[8], oc[8];
+#pragma unroll
+                for (int k2 = 0; k2 < 8; ++k2) {
+                    os[k2] = hp[8 * b + k2];
+                    oc[k2] = hp[NC / 2 + 8 * b + k2];
+                }
+                tmem_st8(tm_addr(tmem, q, kColPhi + (fs + 16 * b) / 2), os);
+                tmem_st8(tm_addr(tmem, q, kColPhi + (fs + 64 + 16 * b) / 2), oc);
+            }
+        } else {
+#pragma unroll
+            for (int b = 0; b < NC / 16; ++b) {
+                uint32_t o[8];
+#pragma unroll
+                for (int k2 = 0; k2 < 8; ++k2) o[k2] = hp[8 * b + k2];
+                tmem_st8(tm_addr(tmem, q, kColPhi + (NC * j + 16 * b) / 2), o);
+            }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(e_q);
     }
+    if (n > 0) write_output(n - 1);
     if (e == 0) bulk_wait0();
     if (!alive) set_status(a.status, FAVOR_ERR_TIMEOUT);
 }
@@ -2390,13 +2439,13 @@ tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *small = reinterpret_cast<float *>(sm + a.o_small);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(small + 544);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(small + 568);
-    volatile int *abortp = reinterpret_cast<volatile int *>(small + 570);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(small + kOutBars);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(small + kOutSlot);
+    volatile int *abortp = reinterpret_cast<volatile int *>(small + kOutAbort);
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 5; ++i) mbar_init(&bars[i], 1);
-        for (int i = 5; i < 7; ++i) mbar_init(&bars[i], kEpi);
+        for (int i = 0; i < 6; ++i) mbar_init(&bars[i], 1);
+        for (int i = 6; i < kOutNumBars; ++i) mbar_init(&bars[i], kEpi);
         fence_mbar_init();
         *abortp = 0;
     }
@@ -2531,7 +2580,7 @@ OutputLayout output_layout(const Geo &g) {
         l.o_s = o; o = align1k(o + 2u * g.r * 128);             // state atom + z atom
         l.o_x = o; o = align1k(o + (uint32_t)nq * kC * g.d * 2);
         l.o_stage = o; o = align1k(o + 2 * kBlk);
-        l.o_small = o; o = align1k(o + 576 * 4);
+        l.o_small = o; o = align1k(o + kOutSmall * 4);
         l.bytes = o + 1024;
         l.nq = nq;
         if (l.bytes <= kSmemMax) break;
