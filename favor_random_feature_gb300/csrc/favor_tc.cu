@@ -285,13 +285,16 @@ __device__ __forceinline__ float cvt_chunk16_sq(uint8_t *p, float &amax) {
 // tiles (all of a head's features where TMEM holds them), so each K and V
 // tile is converted once for all of them.
 // Warp 0 lane 0 issues every TMA copy and MMA; warps 1..16 (the epilogue
-// group) convert tiles and compute features, warp w on TMEM lane quarter
-// w % 4 and projection quarter (w - 1) / 4.  The epilogue reads the
-// projections of chunk c into registers and hands TMEM back at once, so the
-// tensor core projects chunk c + 1 while the features of c are formed, and
-// the state update of c runs while the epilogue starts on c + 1.
+// group) compute features, warp w on TMEM lane quarter w % 4 and projection
+// quarter (w - 1) / 4; warps 17..20 (the converters, one thread per row)
+// turn each K and V tile into fp16 in place as soon as it lands, with the key
+// norms and the range checks.  The epilogue reads the projections of chunk c
+// into registers and hands TMEM back at once, so the tensor core projects
+// chunk c + 1 while the features of c are formed, and the state update of c
+// runs while the epilogue starts on c + 1.
 // ---------------------------------------------------------------------------
-constexpr int kStateThreads = 32 + kEpi;
+constexpr int kStateConv = 128;
+constexpr int kStateThreads = 32 + kEpi + kStateConv;
 
 struct StateArgs {
     Geo g;
@@ -348,19 +351,27 @@ __device__ __forceinline__ void state_body(const CUtensorMap *tm_k, const CUtens
     uint8_t *w = sm + a.o_w, *xk = sm + a.o_xk, *xv = sm + a.o_xv, *phk = sm + a.o_phk;
     float *small = reinterpret_cast<float *>(sm + a.o_small);
     float *nk = small;              // [3][128] half key norms, by chunk % 3
+    float *cred = small + 384;      // [4] the converters' max |v|
     float *red = small + 768;       // [32]
     uint64_t *bars = reinterpret_cast<uint64_t *>(small + 800);
+    // e_x: K(c) converted, one barrier per K buffer (c % NSK): the converters
+    // may run NSK tiles ahead of the thread that waits, and a barrier must not
+    // complete twice before it looks.  e_n: the norms of chunk c (by c % 3,
+    // the slot they use).  e_v: V(c) converted (by c % 2; NSV <= 2).
     uint64_t *bar_w = &bars[0], *bar_pk = &bars[1], *bar_s = &bars[2], *bar_v = &bars[3] /*[2]*/,
-             *bar_k = &bars[5] /*[3]*/, *e_x = &bars[8] /*[2]*/, *e_pk = &bars[10], *e_k = &bars[11];
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(small + 834);
-    volatile int *abortp = reinterpret_cast<volatile int *>(small + 836);
+             *bar_k = &bars[5] /*[3]*/, *e_x = &bars[8] /*[3]*/, *e_pk = &bars[11], *e_k = &bars[12],
+             *e_n = &bars[13] /*[3]*/, *e_v = &bars[16] /*[2]*/;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(small + 836);
+    volatile int *abortp = reinterpret_cast<volatile int *>(small + 838);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int col_s = 256;          // state tile t at col_s + t (dv + 16): dv values, then 16 copies of z
     const int sw = g.dv + 16;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < 8; ++i) mbar_init(&bars[i], 1);
-        for (int i = 8; i < 12; ++i) mbar_init(&bars[i], kEpi);
+        for (int i = 8; i < 11; ++i) mbar_init(&bars[i], kStateConv);
+        for (int i = 11; i < 13; ++i) mbar_init(&bars[i], kEpi);
+        for (int i = 13; i < 18; ++i) mbar_init(&bars[i], kStateConv);
         fence_mbar_init();
         *abortp = 0;
     }
@@ -410,9 +421,6 @@ __device__ __forceinline__ void state_body(const CUtensorMap *tm_k, const CUtens
             grid_dep_wait();
             mbar_arrive_expect_tx(bar_w, wbytes);
             bulk_load(w, a.omg + (size_t)head * g.nproj * g.d * 2 + (size_t)fg * wbytes, wbytes, bar_w);
-            // e_x alternates between two barriers by chunk parity: with three K
-            // buffers the epilogue may convert K(c + 2) before this thread
-            // looks at K(c + 1), and one barrier would then have moved on twice
             alive = ewait(bar_w, 0, abortp) && ewait(&e_x[0], 0, abortp);
             if (alive) {
                 tc_fence_after();
@@ -423,13 +431,13 @@ __device__ __forceinline__ void state_body(const CUtensorMap *tm_k, const CUtens
                     // the epilogue holds P(c) in registers (so P(c) is done and
                     // K buffer c % NSK is free) and has converted K(c + 1)
                     if (!(alive = ewait(e_pk, c & 1, abortp) &&
-                                  ewait(&e_x[(c + 1) & 1], ((c + 1) >> 1) & 1, abortp)))
+                                  ewait(&e_x[(c + 1) % NSK], ((c + 1) / NSK) & 1, abortp)))
                         break;
                     tc_fence_after();
                     issue_proj(c + 1);
                     if (c + NSK < nchunk) load_k(c + NSK);
                 }
-                if (!(alive = ewait(e_k, c & 1, abortp))) break;
+                if (!(alive = ewait(e_k, c & 1, abortp) && ewait(&e_v[c & 1], (c >> 1) & 1, abortp))) break;
                 tc_fence_after();
                 {
                     const uint32_t idesc = idesc_f16(128, sw, 1, 1);
@@ -449,12 +457,61 @@ __device__ __forceinline__ void state_body(const CUtensorMap *tm_k, const CUtens
             }
             if (!alive) set_status(a.status, FAVOR_ERR_TIMEOUT);
         }
+    } else if (warp > kEpi / 32) {
+        // converters: thread r owns row r of every K and V tile; K(c + 1)
+        // comes before V(c) (the projection of c + 1 is wanted first)
+        const int r = threadIdx.x - 32 - kEpi;
+        float vmax = 0.f;
+        auto convert_k = [&](int c) {
+            alive &= ewait(&bar_k[c % NSK], (c / NSK) & 1, abortp);
+            uint8_t *tile = xk + (size_t)(c % NSK) * xkb + r * 128;
+            float ss = 0.f, kmax = 0.f;
+            for (int b = 0; b < nd; ++b)
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) ss += cvt_chunk16_sq(tile + b * kBlk + ((ch ^ (r & 7)) << 4), kmax);
+            if (kmax > kMaxOperand) flag_range(a.status);
+            nk[(c % 3) * 128 + r] = 0.5f * kLog2e * ss;
+            fence_async_smem();
+            mbar_arrive(&e_x[c % NSK]);
+            mbar_arrive(&e_n[c % 3]);
+        };
+        auto convert_v = [&](int c) {
+            alive &= ewait(&bar_v[c % NSV], (c / NSV) & 1, abortp);
+            uint8_t *tile = xv + (size_t)(c % NSV) * a.xv_stride + r * 128;
+            for (int b = 0; b < nvb; ++b)
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    uint4 *p4 = reinterpret_cast<uint4 *>(tile + b * kBlk + ((ch ^ (r & 7)) << 4));
+                    const uint4 u = *p4;
+                    const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+                    uint32_t o[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float lo = __uint_as_float(w4[i] << 16), hi = __uint_as_float(w4[i] & 0xffff0000u);
+                        vmax = fmax3(vmax, fabsf(lo), fabsf(hi));
+                        o[i] = pack_half2(lo, hi);
+                    }
+                    *p4 = make_uint4(o[0], o[1], o[2], o[3]);
+                }
+            fence_async_smem();
+            mbar_arrive(&e_v[c & 1]);
+        };
+        if (nchunk > 0) convert_k(0);
+        for (int c = 0; c < nchunk; ++c) {
+            if (c + 1 < nchunk) convert_k(c + 1);
+            convert_v(c);
+        }
+        // max |v| of the piece for the epilogue's meta and the range check
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
+        if (lane == 0) cred[r >> 5] = vmax;
+        named_sync(2, kEpi + kStateConv);
+        if (!alive) set_status(a.status, FAVOR_ERR_TIMEOUT);
     } else {
         const int e = threadIdx.x - 32, ew = e >> 5;
         const int q = (ew + 1) & 3, j = ew >> 2;
         const int row = q * 32 + lane;
         float R = MAP == FAVOR_MAP_POSITIVE ? -INFINITY : 0.f;
-        float vmax = 0.f;
         // zero state and z
         {
             uint32_t zero[16];
@@ -464,37 +521,10 @@ __device__ __forceinline__ void state_body(const CUtensorMap *tm_k, const CUtens
                 for (int cc = 16 * j; cc < sw; cc += 64) tmem_st16(tm_addr(tmem, q, col_s + t * sw + cc), zero);
             tmem_st_wait();
         }
-        // K(c) -> fp16 and the half key norms: thread e takes row e / 4, chunks
-        // 2 (e % 4) and 2 (e % 4) + 1 of each 64-column block, the row's four
-        // threads being neighbouring lanes.  The norms of chunk c go to buffer
-        // c % 3, written at the start of iteration c - 1 and read in iteration
-        // c, with the vote's group barrier between (only the positive map
-        // reads them).
-        auto convert_k = [&](int c) -> bool {
-            bool ok = ewait(&bar_k[c % NSK], (c / NSK) & 1, abortp);
-            uint8_t *tile = xk + (size_t)(c % NSK) * xkb;
-            const int r = e >> 2, pp = e & 3;
-            float ss = 0.f, kmax = 0.f;
-            for (int b = 0; b < nd; ++b)
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
-                    ss += cvt_chunk16_sq(tile + b * kBlk + r * 128 + (((2 * pp + h) ^ (r & 7)) << 4), kmax);
-            if (kmax > kMaxOperand) flag_range(a.status);
-            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-            ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-            if (pp == 0) nk[(c % 3) * 128 + r] = 0.5f * kLog2e * ss;
-            fence_async_smem();
-            mbar_arrive(&e_x[c & 1]);
-            return ok;
-        };
-        if (nchunk > 0) alive = convert_k(0);
-        group_sync(kEpi);   // norms of chunk 0 visible
         for (int c = 0; c < nchunk; ++c) {
             const int tc0 = t_begin + c * kC;
             const int valid = min(kC, t_end - tc0);
             const bool ok = row < valid;
-            // K(c + 1) first: the tensor core is still on P(c)
-            if (c + 1 < nchunk) alive &= convert_k(c + 1);
             // P(c) -> registers (for the positive map after a first pass that
             // only takes the row maximum, so that the vote below holds no
             // projections); TMEM then goes back to the tensor core for P(c + 1)
@@ -520,6 +550,7 @@ __device__ __forceinline__ void state_body(const CUtensorMap *tm_k, const CUtens
             uint32_t hp[NH];
             float alpha = 1.f;
             if (MAP == FAVOR_MAP_POSITIVE) {
+                alive &= ewait(&e_n[c % 3], (c / 3) & 1, abortp);
                 const float nkr = nk[(c % 3) * 128 + row];
                 // a key whose largest feature would pass e^(shift + slack) at the
                 // current reference (always so before the first key) moves the
@@ -582,47 +613,57 @@ __device__ __forceinline__ void state_body(const CUtensorMap *tm_k, const CUtens
                     store_row_packed<32>(phk + (size_t)(f0 / 64) * kBlk, row, f0 % 64, hp + 16 * g32);
                 }
             }
-            // V(c) -> fp16
-            alive &= ewait(&bar_v[c % NSV], (c / NSV) & 1, abortp);
-            {
-                float am;
-                convert_tile_512<false, true>(xv + (size_t)(c % NSV) * a.xv_stride, nvb, e, am);
-                vmax = fmaxf(vmax, am);
-            }
             fence_async_smem();
             tc_fence_before();
             mbar_arrive(e_k);
         }
-        // the last state update, then S, z -> global with each tile's max |S| and max z
+        // the last state update, then S, z -> global with each tile's max |S|
+        // and max z.  The group's tiles are staged in shared memory (the K, V
+        // and feature buffers are free now) as their global rows [FT][128][dv + 1]
+        // (a warp's 32 rows fall on 32 different banks), then leave in one bulk copy.
         if (nchunk > 0) alive &= ewait(bar_s, (nchunk - 1) & 1, abortp);
         tc_fence_after();
         const bool write = alive && !*abortp;
-        const float vm = grp_max(vmax, red, ew);
+        named_sync(2, kEpi + kStateConv);   // the converters' max |v|
+        const float vm = fmaxf(fmaxf(cred[0], cred[1]), fmaxf(cred[2], cred[3]));
         if (e == 0 && vm > kMaxOperand) flag_range(a.status);
-        for (int t = 0; t < FT; ++t) {
-            const int ft = fg * FT + t;
-            const int f = ft * 128 + row;
-            float *dst = a.state + (((size_t)bh * a.npieces + piece) * g.r + f) * (g.dv + 1);
-            float smax = 0.f, zval = 0.f;
+        float *stg = reinterpret_cast<float *>(xk);
+        float smax[2] = {0.f, 0.f}, zval[2] = {0.f, 0.f};
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            if (t >= FT) break;
+            float *srow = stg + ((size_t)t * 128 + row) * (g.dv + 1);
             for (int cc = 16 * j; cc < g.dv; cc += 64) {
                 float v[16];
                 tmem_ld16(tm_addr(tmem, q, col_s + t * sw + cc), v);
                 tmem_ld_wait();
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    smax = fmaxf(smax, fabsf(v[i]));
-                    if (write) dst[cc + i] = v[i];
+                    smax[t] = fmaxf(smax[t], fabsf(v[i]));
+                    srow[cc + i] = v[i];
                 }
             }
             if (j == 0) {
                 float v[16];
                 tmem_ld16(tm_addr(tmem, q, col_s + t * sw + g.dv), v);
                 tmem_ld_wait();
-                zval = fabsf(v[0]);
-                if (write) dst[g.dv] = v[0];
+                zval[t] = fabsf(v[0]);
+                srow[g.dv] = v[0];
             }
-            const float sm_all = grp_max(smax, red, ew);
-            const float zm = grp_max(zval, red, ew);
+        }
+        fence_async_smem();
+        group_sync(kEpi);
+        if (write && e == 0) {
+            float *dst = a.state + (((size_t)bh * a.npieces + piece) * g.r + (size_t)fg * FT * 128) * (g.dv + 1);
+            bulk_store(dst, stg, (uint32_t)FT * 128 * (g.dv + 1) * 4);
+            bulk_commit();
+        }
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            if (t >= FT) break;
+            const int ft = fg * FT + t;
+            const float sm_all = grp_max(smax[t], red, ew);
+            const float zm = grp_max(zval[t], red, ew);
             if (write && e == 0) {
                 float *m = a.meta + (((size_t)bh * a.npieces + piece) * g.n_ft + ft) * 4;
                 m[0] = R;
@@ -631,6 +672,7 @@ __device__ __forceinline__ void state_body(const CUtensorMap *tm_k, const CUtens
                 m[3] = sm_all;
             }
         }
+        if (write && e == 0) bulk_wait0();
         if (!write) set_status(a.status, FAVOR_ERR_TIMEOUT);
     }
     tc_fence_before();
@@ -2562,7 +2604,9 @@ StateLayout state_layout(const Geo &g) {
             l.nks = op[0];
             l.nvs = op[1];
             l.FT = FT;
-            if (l.bytes <= kSmemMax) return l;
+            // the final states are staged in [o_xk, o_small)
+            const bool stage_fits = (size_t)FT * 128 * (g.dv + 1) * 4 <= (size_t)(l.o_small - l.o_xk);
+            if (l.bytes <= kSmemMax && stage_fits) return l;
         }
     }
     return l;

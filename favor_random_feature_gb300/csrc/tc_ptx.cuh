@@ -175,6 +175,14 @@ __device__ __forceinline__ void bulk_wait_read0() {
 // committed stores complete
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// plain bulk copy shared -> global (16-byte aligned addresses, size % 16 == 0),
+// completed through the bulk groups (bulk_commit, bulk_wait0)
+__device__ __forceinline__ void bulk_store(void *dst, const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
+                 "r"(smem_u32(src)), "r"(bytes)
+                 : "memory");
+}
+
 // plain bulk copy global -> shared (16-byte aligned addresses, size % 16 == 0)
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
     asm volatile(
@@ -372,6 +380,11 @@ __device__ __forceinline__ void setmaxnreg_dec() {
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void group_sync(int n) {
     asm volatile("bar.sync 1, %0;" ::"r"(n) : "memory");
+}
+
+// named barrier `id` over `n` threads
+__device__ __forceinline__ void named_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
 // group-wide AND of a predicate (named barrier 1)

@@ -346,6 +346,32 @@ def test_tensor_core_path_taken(w, causal, kernel):
 # between: every bounded wait must still be met (a wait that runs out sets
 # the device status) and the result must not change from call to call
 # ---------------------------------------------------------------------------
+@pytest.mark.parametrize("w,causal", [(NC4096, False), (CAUSAL8K, True), (SWEEP16K, True)],
+                         ids=["noncausal", "causal", "causal-split"])
+def test_soak_status_stays_clean(w, causal):
+    """Thousands of full-size calls queued without a host synchronisation:
+    a wait whose barrier phase could be overtaken (a producer running ahead
+    of its consumer) shows up as FAVOR_ERR_TIMEOUT in the status word."""
+    import time
+    import torch
+    import favor_random_feature_gb300 as fv
+    inp = make_inputs(w)
+    q, k, v, om = to_device(inp)
+    stream = torch.cuda.current_stream()
+    out = torch.empty((w.B, w.H, w.L, w.dv), dtype=torch.float32, device="cuda")
+    fv.favor_get_device_status(stream)
+    t0, n = time.time(), 0
+    while time.time() - t0 < 3.0:
+        for _ in range(100):
+            rc = fv.favor_attn_forward(q, k, v, om, out, w.B, w.H, w.L, w.d, w.dv, w.m, int(causal), MAP_POSITIVE,
+                                       stream)
+            assert rc == fv.FAVOR_OK, fv.strerror(rc)
+        torch.cuda.synchronize()
+        n += 100
+    st = fv.favor_get_device_status(stream)
+    assert st == fv.FAVOR_OK, (n, fv.strerror(st))
+
+
 @pytest.mark.parametrize("w,causal", [(NC4096, False), (CAUSAL8K, True)], ids=["noncausal", "causal"])
 def test_back_to_back_calls(w, causal):
     import torch
