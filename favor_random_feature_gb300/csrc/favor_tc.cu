@@ -852,6 +852,7 @@ constexpr uint32_t kKbBlk = kKbRows * 128;       // one 64-feature block of the 
 constexpr int kKbS = 128, kKbZ = 192, kKbOne = 193;   // first rows of sigma S^T, sigma z, ones
 // small-area float offsets of the barriers, TMEM slot, abort flag; total size
 constexpr int kCausalBars = 1696, kCausalTslot = 1728, kCausalAbort = 1730, kCausalSmall = 1736;
+static_assert(kCausalBars + 2 * 15 <= kCausalTslot, "the scan's mbarriers overlap the TMEM slot");
 // r split: each row of a CTA's partial result travels as 68 floats (64 num,
 // den, log2 scale, row sum of the query features, pad)
 constexpr int kPartFloats = 68;
@@ -922,7 +923,8 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
     float *red = small + 1664;     // [32]
     uint64_t *bars = reinterpret_cast<uint64_t *>(small + kCausalBars);
     uint64_t *bar_w = &bars[0], *bar_x = &bars[1], *bar_v = &bars[2], *bar_pk = &bars[3],
-             *bar_pq = &bars[4], *bar_a = &bars[5], *bar_av = &bars[6], *bar_st = &bars[13];
+             *bar_pq = &bars[4], *bar_a = &bars[5], *bar_av = &bars[6], *bar_st = &bars[13],
+             *bar_in = &bars[14];
     uint64_t *e_x = &bars[7], *e_pk = &bars[8], *e_q = &bars[9], *e_v = &bars[10],
              *e_b = &bars[11], *e_out = &bars[12];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1040,14 +1042,6 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
     const int e = threadIdx.x - 32, ew = e >> 5;
     const int q = (ew + 1) & 3, j = ew >> 2;
     const int row = q * 32 + lane;
-    // the ones row (its accumulator column is the row sum of the query
-    // features, for the range check) and the pad rows after it (they feed
-    // accumulator columns never read)
-    for (int i = e; i < (g.r / 64) * 15 * 8; i += kEpi) {
-        const int blk = i / 120, rr = kKbOne + (i % 120) / 8, ch = i % 8;
-        const uint32_t one = rr == kKbOne ? 0x3C003C00u : 0u;
-        *reinterpret_cast<uint4 *>(kb + (size_t)blk * kKbBlk + rr * 128 + ch * 16) = make_uint4(one, one, one, one);
-    }
     float R = MAP == FAVOR_MAP_POSITIVE ? -INFINITY : 0.f, zmax = 0.f, vmax = 0.f;
     float s0[16], s1[16], z0 = 0.f, z1 = 0.f;   // this thread's part of the initial state
 #pragma unroll
@@ -1120,6 +1114,40 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
     // one finish; the state of the earlier segments is theirs
     if (nchunk > 0) alive = convert_x(0);
     grid_dep_wait();
+    // The states of the earlier segments come through shared memory: bulk
+    // copies of this CTA's state rows [nft x 128][dv + 1] (all of them, or
+    // 128 or 64 at a time, as the KB area holds them) into the KB area, which
+    // the scan takes over only after this; each thread then reads 16 values
+    // of its row (rows 65 or 129 words apart fall on different banks)
+    // instead of 16 scalar loads from global memory.
+    const uint32_t row_floats = (uint32_t)g.dv + 1;
+    const int span = nft * 128;
+    const int kb_rows = (int)((uint32_t)(g.r / 64) * kKbBlk / (row_floats * 4u));
+    const int unit = span <= kb_rows ? span : (128 <= kb_rows ? 128 : 64);
+    float *stg = reinterpret_cast<float *>(kb);
+    int sphase = 0;
+    bool staged = false;
+    auto take = [&](int lr, float (&sv)[16], float &zv, float sc) {
+        const float *rp = stg + (size_t)lr * row_floats;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) sv[i] += rp[64 * dvt + 16 * j + i] * sc;
+        if (j == 0) zv += rp[g.dv] * sc;
+    };
+    // src: row 0 of this CTA's first feature tile; rows of tile t scaled by sc_t
+    auto take_span = [&](const float *src, float sc0, float sc1) {
+        for (int u = 0; u < span; u += unit) {
+            if (staged) group_sync(kEpi);   // the previous staging has been read
+            if (e == 0) {
+                mbar_arrive_expect_tx(bar_in, (uint32_t)unit * row_floats * 4u);
+                bulk_load(stg, src + (size_t)u * row_floats, (uint32_t)unit * row_floats * 4u, bar_in);
+            }
+            alive &= ewait(bar_in, sphase & 1, abortp);
+            ++sphase;
+            staged = true;
+            if (row >= u && row < u + unit) take(row - u, s0, z0, sc0);
+            if (nft == 2 && 128 + row >= u && 128 + row < u + unit) take(128 + row - u, s1, z1, sc1);
+        }
+    };
     if (seg > 0 && a.direct) {
         // the state after segments 0 .. seg-1 (pieces 0 .. seg pps - 1),
         // combined here at the largest of their key references (few segments:
@@ -1146,38 +1174,27 @@ __device__ void causal_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem,
         if (MAP == FAVOR_MAP_POSITIVE) R = Rs;
         const size_t per = (size_t)a.r_full * (g.dv + 1);
         for (int gi = 0; gi < npin; ++gi) {
-            const float *st = a.state + ((size_t)bh * a.nstate + gi) * per + (size_t)ft0 * 128 * (g.dv + 1);
-            const float sc0 = scale(gi, 0), sc1 = nft == 2 ? scale(gi, 1) : 0.f;
-            const float *r0 = st + (size_t)row * (g.dv + 1), *r1 = st + (size_t)(128 + row) * (g.dv + 1);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) s0[i] += r0[64 * dvt + 16 * j + i] * sc0;
-            if (nft == 2) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) s1[i] += r1[64 * dvt + 16 * j + i] * sc1;
-            }
-            if (j == 0) {
-                z0 += r0[g.dv] * sc0;
-                if (nft == 2) z1 += r1[g.dv] * sc1;
-            }
+            const float *st = a.state + ((size_t)bh * a.nstate + gi) * per + (size_t)ft0 * 128 * row_floats;
+            take_span(st, scale(gi, 0), nft == 2 ? scale(gi, 1) : 0.f);
         }
     } else if (seg > 0) {
         const float *m = a.meta_in + ((size_t)bh * a.nseg + seg) * 4;
         R = m[0];
         zmax = m[1];
         vmax = m[2];
-        const float *src = a.s_in + (((size_t)bh * a.nseg + seg) * a.r_full + (size_t)ft0 * 128) * (g.dv + 1);
-        const float *r0 = src + (size_t)row * (g.dv + 1), *r1 = src + (size_t)(128 + row) * (g.dv + 1);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) s0[i] = r0[64 * dvt + 16 * j + i];
-        if (nft == 2) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) s1[i] = r1[64 * dvt + 16 * j + i];
-        }
-        if (j == 0) {
-            z0 = r0[g.dv];
-            if (nft == 2) z1 = r1[g.dv];
-        }
+        take_span(a.s_in + (((size_t)bh * a.nseg + seg) * a.r_full + (size_t)ft0 * 128) * row_floats, 1.f, 1.f);
     }
+    // the KB area is the scan's from here: every staged row has been read
+    if (staged) group_sync(kEpi);
+    // the ones row (its accumulator column is the row sum of the query
+    // features, for the range check) and the pad rows after it (they feed
+    // accumulator columns never read)
+    for (int i = e; i < (g.r / 64) * 15 * 8; i += kEpi) {
+        const int blk = i / 120, rr = kKbOne + (i % 120) / 8, ch = i % 8;
+        const uint32_t one = rr == kKbOne ? 0x3C003C00u : 0u;
+        *reinterpret_cast<uint4 *>(kb + (size_t)blk * kKbBlk + rr * 128 + ch * 16) = make_uint4(one, one, one, one);
+    }
+    fence_async_smem();
     // initial state into TMEM: tile t, lanes = features, 16 value columns per thread
     {
         uint32_t u[16];
@@ -1473,6 +1490,7 @@ tc_causal(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         for (int i = 0; i < 7; ++i) mbar_init(&bars[i], 1);
         for (int i = 7; i < 13; ++i) mbar_init(&bars[i], kEpi);
         mbar_init(&bars[13], 1);
+        mbar_init(&bars[14], 1);
         fence_mbar_init();
     }
     // ones atom after the V tile: the z column of S += phi_K^T [V | 1] and
@@ -1568,7 +1586,7 @@ __device__ void split_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem, cons
     uint64_t *b_w = &bars[0], *b_x = &bars[1], *b_v = &bars[2], *b_pk = &bars[3], *b_pq = &bars[4],
              *b_a = &bars[5], *b_s = &bars[6], *b_av = &bars[7];
     uint64_t *e_x = &bars[9], *e_pk = &bars[10], *e_q = &bars[11], *e_v = &bars[12], *e_b = &bars[13];
-    uint64_t *bar_free = &bars[16];
+    uint64_t *bar_free = &bars[16], *bar_in = &bars[8];
     // receive slot s: its barrier, its numerators and its per-row scalars
     const int nslots = a.nslots;
     const size_t slot_floats = (size_t)(rs - 1) * rpo * kPartFloats;
@@ -1696,12 +1714,6 @@ __device__ void split_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem, cons
     const int e = threadIdx.x - 32, ew = e >> 5;
     const int q = (ew + 1) & 3, j = ew >> 2;
     const int row = q * 32 + lane;
-    // the ones row and the pad rows of every KB block
-    for (int i = e; i < (g.r / 64) * 15 * 8; i += kEpi) {
-        const int blk = i / 120, rr = kKbOne + (i % 120) / 8, ch = i % 8;
-        const uint32_t one = rr == kKbOne ? 0x3C003C00u : 0u;
-        *reinterpret_cast<uint4 *>(kb + (size_t)blk * kKbBlk + rr * 128 + ch * 16) = make_uint4(one, one, one, one);
-    }
     float R = MAP == FAVOR_MAP_POSITIVE ? -INFINITY : 0.f, zmax = 0.f, vmax = 0.f, sigma = 1.f;
     float qoff_next = 0.f;                  // query row offset of the chunk whose features are held
     constexpr int NH = MAP == FAVOR_MAP_TRIG ? NC : NC / 2;
@@ -1904,6 +1916,32 @@ __device__ void split_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem, cons
     // one finish; the state of the earlier segments is theirs
     if (nchunk > 0) alive &= convert_x(0);
     grid_dep_wait();
+    // The states of the earlier segments come through shared memory, as in
+    // tc_causal: bulk copies of the slice's 128 state rows [dv + 1] (all, or
+    // 64 at a time) into the KB area, then 16 values of its row per thread.
+    const uint32_t row_floats = (uint32_t)g.dv + 1;
+    const int unit = (int)((uint32_t)(g.r / 64) * kKbBlk / (row_floats * 4u)) >= 128 ? 128 : 64;
+    float *stg = reinterpret_cast<float *>(kb);
+    int sphase = 0;
+    bool staged = false;
+    auto take_span = [&](const float *src, float sc) {
+        for (int u = 0; u < 128; u += unit) {
+            if (staged) group_sync(kEpi);   // the previous staging has been read
+            if (e == 0) {
+                mbar_arrive_expect_tx(bar_in, (uint32_t)unit * row_floats * 4u);
+                bulk_load(stg, src + (size_t)u * row_floats, (uint32_t)unit * row_floats * 4u, bar_in);
+            }
+            alive &= ewait(bar_in, sphase & 1, abortp);
+            ++sphase;
+            staged = true;
+            if (row >= u && row < u + unit) {
+                const float *rp = stg + (size_t)(row - u) * row_floats;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) s0[i] += rp[64 * dvt + 16 * j + i] * sc;
+                if (j == 0) z0 += rp[g.dv] * sc;
+            }
+        }
+    };
     if (seg > 0 && a.direct) {
         const int npin = seg * a.pps;
         const float *meta = a.meta + (size_t)bh * a.nstate * nft_full * 4 + (size_t)ft0 * 4;
@@ -1919,24 +1957,25 @@ __device__ void split_body(const CausalArgs &a, uint8_t *sm, uint32_t tmem, cons
         };
         for (int gi = 0; gi < npin; ++gi) zmax += meta[gi * nft_full * 4 + 1] * scale(gi);
         if (MAP == FAVOR_MAP_POSITIVE) R = Rs;
-        const size_t per = (size_t)a.r_full * (g.dv + 1);
-        for (int gi = 0; gi < npin; ++gi) {
-            const float *r0 = a.state + ((size_t)bh * a.nstate + gi) * per + (size_t)(ft0 * 128 + row) * (g.dv + 1);
-            const float sc0 = scale(gi);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) s0[i] += r0[64 * dvt + 16 * j + i] * sc0;
-            if (j == 0) z0 += r0[g.dv] * sc0;
-        }
+        const size_t per = (size_t)a.r_full * row_floats;
+        for (int gi = 0; gi < npin; ++gi)
+            take_span(a.state + ((size_t)bh * a.nstate + gi) * per + (size_t)ft0 * 128 * row_floats, scale(gi));
     } else if (seg > 0) {
         const float *m = a.meta_in + ((size_t)bh * a.nseg + seg) * 4;
         R = m[0];
         zmax = m[1];
         vmax = m[2];
-        const float *r0 = a.s_in + (((size_t)bh * a.nseg + seg) * a.r_full + (size_t)ft0 * 128 + row) * (g.dv + 1);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) s0[i] = r0[64 * dvt + 16 * j + i];
-        if (j == 0) z0 = r0[g.dv];
+        take_span(a.s_in + (((size_t)bh * a.nseg + seg) * a.r_full + (size_t)ft0 * 128) * row_floats, 1.f);
     }
+    // the KB area is the scan's from here: every staged row has been read
+    if (staged) group_sync(kEpi);
+    // the ones row and the pad rows of every KB block
+    for (int i = e; i < (g.r / 64) * 15 * 8; i += kEpi) {
+        const int blk = i / 120, rr = kKbOne + (i % 120) / 8, ch = i % 8;
+        const uint32_t one = rr == kKbOne ? 0x3C003C00u : 0u;
+        *reinterpret_cast<uint4 *>(kb + (size_t)blk * kKbBlk + rr * 128 + ch * 16) = make_uint4(one, one, one, one);
+    }
+    fence_async_smem();
     {
         uint32_t u[16];
 #pragma unroll
