@@ -722,21 +722,22 @@ struct CombineArgs {
     int nout;              // causal: scan segments
 };
 
+constexpr int kCombineMaxTiles = 512;   // pieces x feature tiles: at most 64 x 8
+
 __global__ void tc_combine(const CombineArgs a) {
     grid_dep_launch();
     grid_dep_wait();
     const Geo &g = a.g;
     const int bh = blockIdx.x;
     const int upto = a.causal ? (blockIdx.y + 1) * a.pps : a.nseg;   // pieces [0, upto)
-    constexpr int kMaxScale = 256;
-    __shared__ float scale[kMaxScale];
+    __shared__ float scale[kCombineMaxTiles];
     __shared__ float sh[4];   // R*, z bound, |S| bound, vmax
-    __shared__ float msh[kMaxScale * 4];
-    const int nsc = upto * g.n_ft;
+    __shared__ float msh[kCombineMaxTiles * 4];
+    const int nsc = upto * g.n_ft;   // <= kCombineMaxTiles (checked on the host)
     {
         // the segment tiles' (R, max z, max|v|, max|S|), loaded by all threads at once
         const float *mg = a.meta + (size_t)bh * a.nseg * g.n_ft * 4;
-        for (int i = threadIdx.x; i < min(nsc, kMaxScale) * 4; i += blockDim.x) msh[i] = mg[i];
+        for (int i = threadIdx.x; i < nsc * 4; i += blockDim.x) msh[i] = mg[i];
         __syncthreads();
     }
     const float *meta = msh;
@@ -753,7 +754,7 @@ __global__ void tc_combine(const CombineArgs a) {
                 const float *m = meta + (gi * g.n_ft + t) * 4;
                 float sc = 1.f;
                 if (g.map == FAVOR_MAP_POSITIVE) sc = (m[0] == -INFINITY || R == -INFINITY) ? 0.f : ex2(m[0] - R);
-                if (gi * g.n_ft + t < kMaxScale) scale[gi * g.n_ft + t] = sc;
+                scale[gi * g.n_ft + t] = sc;
                 zt = fmaxf(zt, m[1] * sc);
                 st = fmaxf(st, m[3] * sc);
             }
@@ -2937,6 +2938,8 @@ int tc_run(const void *q, const void *k, const void *v, const float *omega, floa
     const Geo g = make_geo(p);
     const Plan pl = make_plan(p);
     if (ws_bytes < pl.bytes) return FAVOR_ERR_UNSUPPORTED;
+    // the combine holds one scale per (piece, feature tile)
+    if ((size_t)std::max(1, pl.nstate) * g.n_ft > (size_t)kCombineMaxTiles) return FAVOR_ERR_UNSUPPORTED;
     const int nvb = pl.nvb, nchunk = pl.nchunk, G = pl.G, seg_len = pl.seg_len,
               nstate = pl.nstate;
     const int sms = num_sms();

@@ -216,6 +216,16 @@ def test_r64_heads_on_the_tensor_cores(fmap, d, m, causal):
     check_bf16(e, f"r=64 map={fmap} d={d}")
 
 
+def test_split_heads_many_pieces():
+    """r = 1024 (eight-CTA clusters) on one head of 38 chunks: 19 segments
+    whose states come in 36 pieces of 8 feature tiles, 288 (piece, tile)
+    scales in the combine pass."""
+    w = SWEEP16K.with_(m=1024, d=64, dv=64)
+    inp = make_inputs(w, L=38 * 128, B=1, H=1)
+    e = row_errors(run_gpu(inp, True, MAP_POSITIVE), oracle_ref(inp, True, MAP_POSITIVE))
+    check_bf16(e, "m=1024 d=64 L=4864")
+
+
 def test_causal_first_row_is_v0_and_last_row_matches_noncausal():
     inp = make_inputs(CAUSAL8K, L=300, B=1, H=2)
     oc = run_gpu(inp, True, MAP_POSITIVE)
