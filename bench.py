@@ -46,12 +46,11 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM traffic (read + write bytes per launch) of a kernel from one ncu capture
 # (profiles/), valid while the kernel's source section is unchanged.
 TRAFFIC = {
-    ("tc_causal", "causal8k"): (309.77e6, "b342a4e72dc8da19"),
-    ("tc_causal", "long64k"): (309.42e6, "b342a4e72dc8da19"),
-    ("tc_causal_split", "sweep16k"): (308.60e6, "4671b0818f53bae7"),
-    ("tc_state", "causal8k"): (69.16e6, "04ebd75748b1e0cb"),
-    ("tc_state", "nc4096"): (105.07e6, "04ebd75748b1e0cb"),
-    ("tc_output", "nc4096"): (103.11e6, "ac0c6b17332a4531"),
+    ("tc_causal", "causal8k"): (309.65e6, "bf625141d5c0677b"),
+    ("tc_causal_split", "sweep16k"): (308.31e6, "6187aa4fa5316de2"),
+    ("tc_state", "causal8k"): (68.93e6, "219f9714fc031c6e"),
+    ("tc_state", "nc4096"): (104.77e6, "219f9714fc031c6e"),
+    ("tc_output", "nc4096"): (102.45e6, "60759cfc8dee8c7e"),
     ("decode_step", "decode_b256"): (496.87e6, "74c42f3d2b49b28e"),
 }
 KERNEL_SECTIONS = {   # kernel: (source file, first line of its section, first line after it)
