@@ -47,6 +47,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # (profiles/), valid while the kernel's source section is unchanged.
 TRAFFIC = {
     ("tc_causal", "causal8k"): (309.65e6, "bf625141d5c0677b"),
+    ("tc_causal", "long64k"): (309.21e6, "bf625141d5c0677b"),
     ("tc_causal_split", "sweep16k"): (308.31e6, "6187aa4fa5316de2"),
     ("tc_state", "causal8k"): (68.93e6, "219f9714fc031c6e"),
     ("tc_state", "nc4096"): (104.77e6, "219f9714fc031c6e"),
