@@ -216,6 +216,21 @@ def test_r64_heads_on_the_tensor_cores(fmap, d, m, causal):
     check_bf16(e, f"r=64 map={fmap} d={d}")
 
 
+@pytest.mark.parametrize("m,B", [(256, 2), (512, 1)], ids=["pairs", "quads"])
+def test_split_heads_two_segments(m, B):
+    """Two segments per head in the feature-split scan (d = dv = 128; the
+    benchmark's launch shape for m = 256): the second segment's clusters sum
+    the piece states of the first in their prologue (no combine pass)."""
+    w = SWEEP16K.with_(m=m)
+    inp = make_inputs(w, L=2048, B=B, H=8)
+    BH = B * 8
+    heads = [0, BH // 2 + 1, BH - 1]
+    out = run_gpu(inp, True, MAP_POSITIVE)
+    ref = oracle_ref(inp, True, MAP_POSITIVE, heads=heads)
+    e = row_errors(out.reshape(BH, 2048, w.dv)[heads], ref.reshape(BH, 2048, w.dv)[heads])
+    check_bf16(e, f"m={m} two segments")
+
+
 def test_split_heads_many_pieces():
     """r = 1024 (eight-CTA clusters) on one head of 38 chunks: 19 segments
     whose states come in 36 pieces of 8 feature tiles, 288 (piece, tile)
