@@ -19,6 +19,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 
 constexpr int kHostGroups = 8;   // head groups of the host-buffer entry point
+constexpr int kHostGroupsMax = kHostGroups + 2;   // the last group split twice
 
 struct DeviceState {
     void *ws = nullptr;
@@ -28,7 +29,7 @@ struct DeviceState {
     int *status = nullptr;     // device address of g_device_status
     // host-API copy streams and their events (created on first use)
     cudaStream_t s_in = nullptr, s_out = nullptr;
-    cudaEvent_t ev_in[kHostGroups] = {}, ev_done[kHostGroups] = {}, ev_out = nullptr;
+    cudaEvent_t ev_in[kHostGroupsMax] = {}, ev_done[kHostGroupsMax] = {}, ev_out = nullptr;
 };
 
 std::mutex g_mu;
@@ -293,6 +294,20 @@ int host_groups(int B, int H, HostGroup *g) {
                 if (h1 > h0) g[n++] = {b, 1, h0, h1 - h0};
             }
     }
+    // Nothing overlaps the last group's compute and copy-out: make it small.
+    // Whole batches give up their last batch, and a group of one batch of
+    // four or more heads its last quarter of heads.
+    if (n > 0 && g[n - 1].nb > 1) {
+        HostGroup &l = g[n - 1];
+        g[n++] = {l.b0 + l.nb - 1, 1, 0, H};
+        --l.nb;
+    }
+    if (n > 0 && g[n - 1].nb == 1 && g[n - 1].nh >= 4) {
+        HostGroup &l = g[n - 1];
+        const int q = l.nh / 4;
+        g[n++] = {l.b0, 1, l.h0 + l.nh - q, q};
+        l.nh -= q;
+    }
     return n;
 }
 
@@ -301,7 +316,7 @@ int host_streams(DeviceState &s) {
     bool ok = cudaStreamCreateWithFlags(&s.s_in, cudaStreamNonBlocking) == cudaSuccess &&
               cudaStreamCreateWithFlags(&s.s_out, cudaStreamNonBlocking) == cudaSuccess &&
               cudaEventCreateWithFlags(&s.ev_out, cudaEventDisableTiming) == cudaSuccess;
-    for (int i = 0; ok && i < kHostGroups; ++i)
+    for (int i = 0; ok && i < kHostGroupsMax; ++i)
         ok = cudaEventCreateWithFlags(&s.ev_in[i], cudaEventDisableTiming) == cudaSuccess &&
              cudaEventCreateWithFlags(&s.ev_done[i], cudaEventDisableTiming) == cudaSuccess;
     if (!ok) {
@@ -340,7 +355,7 @@ extern "C" int favor_attn_forward_host(const void *q, const void *k, const void 
     char *dq = cv.take<char>(qb), *dk = cv.take<char>(qb), *dvp = cv.take<char>(vb);
     float *dw = omega ? reinterpret_cast<float *>(cv.take<char>(wb)) : nullptr;
     float *dout = reinterpret_cast<float *>(cv.take<char>(ob));
-    HostGroup grp[kHostGroups];
+    HostGroup grp[kHostGroupsMax];
     const int ng = host_groups(B, H, grp);
     const char *hq = static_cast<const char *>(q), *hk = static_cast<const char *>(k),
                *hv = static_cast<const char *>(v);

@@ -293,8 +293,10 @@ def test_feature_map_entry(fmap):
         assert np.allclose(got[0, h], want, rtol=1e-4, atol=3e-5 * np.abs(want).max())
 
 
-@pytest.mark.parametrize("B,H,L,causal", [(1, 2, 500, True), (4, 3, 300, True), (6, 2, 257, False), (1, 1, 129, True)],
-                         ids=["heads-split", "batch-groups", "uneven-batches", "one-head"])
+@pytest.mark.parametrize("B,H,L,causal", [(1, 2, 500, True), (4, 3, 300, True), (6, 2, 257, False), (1, 1, 129, True),
+                                          (2, 16, 300, True), (16, 4, 130, False)],
+                         ids=["heads-split", "batch-groups", "uneven-batches", "one-head", "last-quarter",
+                              "last-batch-and-quarter"])
 def test_host_entry_matches_oracle(B, H, L, causal):
     """The host-buffer entry point copies in, computes and copies out head
     groups (whole batches, or head ranges of one batch) on overlapping streams;
