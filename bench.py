@@ -51,6 +51,7 @@ TRAFFIC = {
     ("tc_causal_split", "sweep16k"): (308.31e6, "6187aa4fa5316de2"),
     ("tc_state", "causal8k"): (68.93e6, "219f9714fc031c6e"),
     ("tc_state", "nc4096"): (104.77e6, "219f9714fc031c6e"),
+    ("tc_state", "long64k_nc"): (138.46e6, "219f9714fc031c6e"),
     ("tc_output", "nc4096"): (102.45e6, "60759cfc8dee8c7e"),
     ("decode_step", "decode_b256"): (496.87e6, "74c42f3d2b49b28e"),
 }

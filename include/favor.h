@@ -132,10 +132,12 @@ int favor_attn_forward(const void *q, const void *k, const void *v, const float 
  * memory, held on every GPU that loads the library until the process exits.
  * Returns FAVOR_ERR_UNSUPPORTED for a shape the tensor-core kernels do not
  * cover or whose scratch (per-head fp16 W image, segment or piece states,
- * the non-causal state image) exceeds 32 MiB: with d=dv=64, m=256 the
- * benchmark shapes B=4, H=16, L=8192 causal (about 9 MB) and B=8, H=12,
- * L=4096 non-causal (about 26 MB) fit; B=1, H=8, L=65536 causal, whose many
- * segments per head carry many states, does not.  The first
+ * the non-causal state image) exceeds 32 MiB.  The benchmark shapes fit:
+ * with d=dv=64, m=256, B=4, H=16, L=8192 causal (about 9 MB), B=8, H=12,
+ * L=4096 non-causal (about 26 MB) and B=1, H=8, L=65536 either way (about
+ * 20 MB: 19 segments per head, their states and the combined states); with
+ * d=dv=128, m=256, B=2, H=8, L=16384 causal.  256 heads of L=65536 do not
+ * (their segment states alone take hundreds of MB).  The first
  * call on a device looks the array's device address up (make it before any
  * stream capture).  All calls share the array: calls whose kernels overlap
  * on the GPU race on it.  Nothing in it needs clearing between calls. */

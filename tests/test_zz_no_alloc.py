@@ -5,12 +5,12 @@ synchronisation).  It runs the tensor-core path on a fixed 32 MiB scratch
 array inside the library, so on the same inputs it must give exactly the
 bits favor_attn_forward gives (same kernels, same plan).  Checked on two
 calls in a row (different inputs and modes, so stale scratch from the first
-call would show in the second), at reduced sizes and at the full benchmark
-shapes the header says fit.  This file is collected last; its refusal of
+call would show in the second), at reduced sizes and at every full benchmark
+shape (the header says they fit).  This file is collected last; its refusal of
 oversized shapes is checked on the CPU (tests/test_abi.py)."""
 import pytest
 
-from favor_inputs import CAUSAL8K, MAP_POSITIVE, NC4096, make_inputs
+from favor_inputs import CAUSAL8K, LONG64K, MAP_POSITIVE, NC4096, SWEEP16K, make_inputs
 from parity_util import run_gpu
 
 pytestmark = pytest.mark.gpu
@@ -50,3 +50,11 @@ def test_noalloc_at_the_benchmark_shapes():
     """B=4, H=16, L=8192 causal and B=8, H=12, L=4096 non-causal (d=dv=64,
     m=256): both fit the array and return FAVOR_OK with the same bits."""
     _same_bits([(make_inputs(CAUSAL8K), True), (make_inputs(NC4096), False)])
+
+
+def test_noalloc_at_the_long_and_wide_shapes():
+    """B=1, H=8, L=65536 (19 segments per head: piece states and the combined
+    states) both ways, and B=2, H=8, L=16384, d=dv=128 (the feature-split
+    scan): they fit the array too."""
+    long = make_inputs(LONG64K)
+    _same_bits([(long, True), (long, False), (make_inputs(SWEEP16K), True)])
