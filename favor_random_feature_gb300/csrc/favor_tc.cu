@@ -16,14 +16,21 @@
 //   keys:    every key of a head shares one reference R (a running maximum of
 //            w_f.k - |k|^2/2, raised only when a chunk exceeds it by more than
 //            e^2; the state is rescaled when it moves), plus the same e^8.
-// Those offsets keep every fp16 feature in [e^-20, e^10].  The intra-chunk
-// matrix is normalised per row by a power of two before it is rounded to
-// fp16, and the state operand by a power of two bounded from the running key
-// mass; both factors are divided out in fp32.
+// Those offsets keep every fp16 feature at most e^10.  There is no lower
+// bound: a key whose features lie far below the head's reference (about e^-18
+// or more below its largest key feature so far) flushes to zero in fp16.  The
+// kernels check the denominators they form against that flush level (and every
+// operand against fp16's largest value) and report FAVOR_ERR_RANGE through the
+// device status word when an input leaves the range.  The intra-chunk matrix
+// is normalised per row by a power of two before it is rounded to fp16, and
+// the state operand by a power of two bounded from the running key mass; both
+// factors are divided out in fp32.
 //
 // Kernels: tc_prep_omega (fp16 image of W), tc_state (segment states),
 // tc_combine (fixed-order sums / exclusive prefixes of the segment states),
-// tc_output (non-causal rows), tc_causal (the chunked causal scan).
+// tc_output (non-causal rows), tc_causal (the chunked causal scan) and
+// tc_causal_split (the same scan with a head's features split over the CTAs
+// of a cluster).
 #include <cmath>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
