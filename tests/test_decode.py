@@ -171,13 +171,15 @@ CASES = [   # (workload, feature map, m or None, L0, T)
     (CAUSAL8K, MAP_TRIG, 256, 129, 3),           # r = 512: a cluster of 8
     (CAUSAL8K, MAP_RELU, None, 200, 4),
     (CAUSAL8K.with_(omega="iid"), MAP_TRIG_SOFTMAX, 64, 150, 3),
+    (CAUSAL8K, MAP_POSITIVE, 64, 200, 3),         # r = 64: one 64-feature tile
+    (CAUSAL8K, MAP_ELU1, None, 200, 3),           # r = d = 64
 ]
 
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("w,fmap,m,L0,T", CASES,
                          ids=["pos", "pos_dv128", "trig_r256", "elu_d128", "pos_r768", "trig_r512", "relu",
-                              "trig_softmax"])
+                              "trig_softmax", "pos_r64", "elu_d64"])
 @pytest.mark.parametrize("f32", [False, True], ids=["bf16", "f32"])
 def test_state_then_decode(w, fmap, m, L0, T, f32):
     w = w.with_(feature_map=fmap, **({"m": m} if m else {}))
