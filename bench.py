@@ -33,8 +33,8 @@ SIMT_KERNELS = ("chunk_rows", "simt_project", "simt_features", "simt_key_scale",
 
 
 def metric_for(name, w, causal):
-    """The headline workload keeps the baseline's metric string; the others
-    name their own shape."""
+    """The headline workload keeps the published headline metric string; the
+    others name their own shape."""
     if name == "causal8k" and w.name == "causal8k":
         return METRIC
     return (f"FAVOR+ fwd tokens/sec (B·H·L/s) on {name}: L={w.L} "
@@ -398,7 +398,7 @@ def run_ours(args):
     d2h = hout.nbytes
 
     if simt:
-        # the fp32 SIMT path: the roofline is the step's (the benchmark spec's three
+        # the fp32 SIMT path: the roofline is the step's (the method's three
         # bounds); the dominant kernel's fp32-ALU fraction goes under simt_alu
         roofline = {
             "bound": binding, "achieved": step_quantity[0] / (ms / 1000.0), "peak": step_quantity[1],
