@@ -540,7 +540,7 @@ extern "C" void favor_release_workspace(void) {
             cudaStreamDestroy(s.s_in);
             cudaStreamDestroy(s.s_out);
             cudaEventDestroy(s.ev_out);
-            for (int i = 0; i < kHostGroups; ++i) {
+            for (int i = 0; i < kHostGroupsMax; ++i) {
                 cudaEventDestroy(s.ev_in[i]);
                 cudaEventDestroy(s.ev_done[i]);
             }

@@ -162,14 +162,18 @@ int favor_attn_forward_f32(const float *q, const float *k, const float *v, const
 /* End-to-end variant of favor_attn_forward on HOST buffers (q/k/v bf16 bits,
  * omega and out fp32; pinned memory gives the fastest copies).  Copies the
  * inputs to a library-owned device staging area, runs the forward pass and
- * copies out back, in up to eight groups of whole heads (whole batches, or
- * head ranges of one batch) whose copies run on two library-owned streams
- * while the caller's `stream` computes the neighbouring groups; each group
- * is a separate forward pass (its rows agree with one device-buffer call to
- * within the bf16 parity bar, not bit for bit).  Starts after the work queued
- * on `stream`, synchronises `stream` before returning.  Not for use inside a
- * stream capture, nor from two threads at once on one device.  Returns
- * favor_status_t. */
+ * copies out back, in up to ten groups of whole heads (whole batches, or
+ * head ranges of one batch; the last group small) whose copies run on two
+ * library-owned streams while the caller's `stream` computes the neighbouring
+ * groups; each group is a separate forward pass (its rows agree with one
+ * device-buffer call to within the bf16 parity bar, not bit for bit).  Starts
+ * after the work queued on `stream`, synchronises `stream` before returning.
+ * Not for use inside a stream capture, nor from two threads at once on one
+ * device.  The host buffers must hold the full [B][H][L][...] extents the
+ * sizes name, like memcpy's: the copies read and write exactly that much, and
+ * on a system where the GPU reaches pageable host memory through the CPU's
+ * page tables a short buffer faults the copy engine, not just the process.
+ * Returns favor_status_t. */
 int favor_attn_forward_host(const void *q, const void *k, const void *v, const float *omega,
                             float *out, int B, int H, int L, int d, int dv, int m, int causal,
                             int feature_map, cudaStream_t stream);

@@ -315,6 +315,32 @@ def test_host_entry_matches_oracle(B, H, L, causal):
     check_bf16(row_errors(run_gpu(inp, causal, MAP_POSITIVE), ref), "device entry")
 
 
+@pytest.mark.parametrize("fmap", [MAP_TRIG, MAP_ELU1], ids=["trig", "elu1"])
+def test_host_entry_other_maps(fmap):
+    """The host-buffer entry point passes the feature map through to every
+    head group: sin/cos (inputs scaled so the kernel is O(1), rows with
+    condition <= 10 scored) and ELU+1 (no omega)."""
+    import favor_random_feature_gb300 as fv
+    inp = make_inputs(CAUSAL8K.with_(feature_map=fmap, m=64 if fmap == MAP_ELU1 else 128), L=400, B=2, H=8)
+    if fmap == MAP_TRIG:
+        inp = scaled_inputs(inp, 0.25)
+    w = inp.w   # the shape of the arrays: the host entry point copies exactly that much
+    out = np.full((w.B, w.H, w.L, w.dv), np.nan, dtype=np.float32)
+    om = None if fmap == MAP_ELU1 else np.ascontiguousarray(inp.omega, dtype=np.float32)
+    rc = fv.favor_attn_forward_host(inp.q, inp.k, inp.v, om, out, w.B, w.H, w.L, w.d, w.dv,
+                                    w.m if fmap != MAP_ELU1 else w.d, 1, fmap)
+    assert rc == 0, fv.strerror(rc)
+    ref = oracle_ref(inp, True, fmap)
+    got = out.astype(np.float64)
+    if fmap == MAP_TRIG:
+        good = causal_trig_condition(inp) <= 10
+        assert good.mean() > 0.5
+        e = row_errors(got[good][:, None, None, :], ref[good][:, None, None, :])
+    else:
+        e = row_errors(got, ref)
+    check_bf16(e, f"host entry map={fmap}")
+
+
 # ---------------------------------------------------------------------------
 # full sizes, in the benchmark's launch configuration; oracle on sampled heads
 # ---------------------------------------------------------------------------
@@ -453,7 +479,10 @@ def test_relu_and_softmax_scaled_trig(fmap, causal, dtype):
     (NC4096.with_(omega="iid"), False, MAP_TRIG_SOFTMAX, 333),
     (SWEEP16K, True, MAP_POSITIVE, 700),     # feature-split scan (clusters of 2)
     (SWEEP16K.with_(m=512), True, MAP_POSITIVE, 700),   # clusters of 4, one receive slot
-], ids=["causal", "noncausal", "trig_causal", "relu_simt", "trig_softmax_simt", "split2", "split4"])
+    (CAUSAL8K.with_(m=64), True, MAP_POSITIVE, 700),    # r = 64 widened to 128
+    (NC4096.with_(m=64), False, MAP_POSITIVE, 700),
+], ids=["causal", "noncausal", "trig_causal", "relu_simt", "trig_softmax_simt", "split2", "split4", "r64_causal",
+        "r64_noncausal"])
 def test_bf16_output(w, causal, fmap, L):
     import torch
     import favor_random_feature_gb300 as fv
