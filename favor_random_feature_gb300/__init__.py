@@ -45,6 +45,7 @@ EXPORTS = (
     "favor_stats_enable",
     "favor_stats_read",
     "favor_probe_ex2_rate",
+    "favor_check_sincos",
     "favor_state_floats",
     "favor_attn_state",
     "favor_attn_state_f32",
@@ -102,6 +103,8 @@ def lib() -> ctypes.CDLL:
         L.favor_stats_read.restype = i
         L.favor_probe_ex2_rate.argtypes = [ctypes.POINTER(ctypes.c_double), vp]
         L.favor_probe_ex2_rate.restype = i
+        L.favor_check_sincos.argtypes = [vp, vp, vp, i, vp]
+        L.favor_check_sincos.restype = i
         L.favor_state_floats.argtypes = [i, i, i, i]
         L.favor_state_floats.restype = i
         for name in ("favor_attn_state", "favor_attn_state_f32"):
@@ -208,6 +211,10 @@ def favor_stats_read() -> FavorStats:
     if rc != FAVOR_OK:
         raise FavorError(rc, "favor_stats_read")
     return st
+
+
+def favor_check_sincos(x, s, c, n, stream=None) -> int:
+    return lib().favor_check_sincos(_ptr(x), _ptr(s), _ptr(c), int(n), _stream(stream))
 
 
 def favor_probe_ex2_rate(stream=None) -> float:

@@ -416,6 +416,16 @@ extern "C" int favor_get_device_status(cudaStream_t stream) {
     return h;
 }
 
+extern "C" int favor_check_sincos(const float *x, float *s, float *c, int n, cudaStream_t stream) {
+    if (n < 0) return FAVOR_ERR_INVALID_ARG;
+    if (n == 0) return FAVOR_OK;
+    int rc;
+    if ((rc = check_ptr(x, false)) || (rc = check_ptr(s, false)) || (rc = check_ptr(c, false))) return rc;
+    const size_t b = (size_t)n * sizeof(float);
+    if (overlaps(s, b, x, b) || overlaps(c, b, x, b) || overlaps(s, b, c, b)) return FAVOR_ERR_INVALID_ARG;
+    return tc_sincos_check(x, s, c, n, stream);
+}
+
 extern "C" int favor_wait_expiry_check(long long limit_cycles, cudaStream_t stream) {
     if (limit_cycles < 1 || limit_cycles > (1ll << 31)) return FAVOR_ERR_INVALID_ARG;
     int *sp = device_status_ptr();

@@ -64,6 +64,9 @@ int simt_feature_map(const void *x, bool bf16_in, const float *omega, float *phi
 // Tensor-core path (tcgen05, fp16 operands, fp32 accumulation); returns
 // FAVOR_ERR_UNSUPPORTED for shapes it does not cover.
 bool tc_supported(const Problem &p);
+// the tensor-core epilogues' sin/cos (one range reduction + the fast sincos)
+// on n device values
+int tc_sincos_check(const float *x, float *s, float *c, int n, cudaStream_t st);
 // A head of r = 64 features (positive m = 64, sin/cos m = 32, ELU+1 d = 64) as
 // one of 128 with every projection taken twice: numerator and denominator
 // both double, so the result is the same.  Other problems unchanged.

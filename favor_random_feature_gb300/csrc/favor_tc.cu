@@ -163,6 +163,13 @@ __device__ __forceinline__ void sincos_reduced(float x, float &s, float &c) {
 // ELU + 1 ("Kernel Feature Maps" section 1); p is x itself here.
 __device__ __forceinline__ float elu1(float p) { return p > 0.f ? p + 1.f : ex2(p * kLog2e); }
 
+// sincos_reduced on n arguments, for the accuracy test of the reduction
+__global__ void sincos_check_kernel(const float *__restrict__ x, float *__restrict__ s, float *__restrict__ c,
+                                    int n) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+        sincos_reduced(x[i], s[i], c[i]);
+}
+
 // ---------------------------------------------------------------------------
 // W image: fp16, 128B-swizzled MN-major atoms [d][64] per 64 projections
 // (the B operand of P = X W^T with K = d), scaled by log2(e) for the
@@ -2896,6 +2903,11 @@ int launch_state(const Problem &p, const Geo &g, const Plan &pl, const uint8_t *
 }  // namespace
 
 size_t tc_scratch_bytes(const Problem &p) { return make_plan(p).bytes; }
+
+int tc_sincos_check(const float *x, float *s, float *c, int n, cudaStream_t st) {
+    sincos_check_kernel<<<std::max(1, std::min((n + 255) / 256, 1024)), 256, 0, st>>>(x, s, c, n);
+    return cuda_status(cudaGetLastError());
+}
 
 int tc_wait_expiry(long long limit_cycles, int *status, cudaStream_t st) {
     wait_expiry_kernel<<<1, 1, 0, st>>>(status, limit_cycles);

@@ -333,6 +333,15 @@ int favor_stats_read(favor_stats_t *out);
  * it waits for the timing to finish.  Returns favor_status_t. */
 int favor_probe_ex2_rate(double *ex2_per_second, cudaStream_t stream);
 
+/* Test hook, no counterpart on the pages: the sine and cosine the
+ * tensor-core kernels use for the sin/cos features (FAVOR_MAP_TRIG), on n
+ * device values x[i] -> s[i], c[i] (fp32, device pointers, 16-byte aligned,
+ * not overlapping).  The argument is reduced by 2 pi in three parts
+ * (Cody-Waite: n = rint(x / 2 pi), then x - n p1 - n p2 - n p3 with p1 holding
+ * 8 significant bits, so n p1 is exact for |n| < 2^16) and the fast sincos of the remainder
+ * in [-pi, pi] follows.  Asynchronous on `stream`.  Returns favor_status_t. */
+int favor_check_sincos(const float *x, float *s, float *c, int n, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
