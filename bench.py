@@ -6,7 +6,8 @@ in HBM.  Default workload: causal, B=4, H=16, L=8192, d=dv=64, m=256,
 block-orthogonal omega, bf16 inputs (synthetic, seeded).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload causal8k|nc4096|long64k|long64k_nc|sweep16k]
+                  [--workload causal8k|nc4096|long64k|long64k_nc|sweep16k|sweep16k_m512|
+                              decode8k|decode_b256|causal8k_bwd|nc4096_bwd]
 
 --impl reference times the float64 CPU oracle (the slow, obviously correct
 statement of the method) on bounded samples of the same workload.
@@ -49,6 +50,8 @@ TRAFFIC = {
     ("tc_causal", "causal8k"): (309.65e6, "bf625141d5c0677b"),
     ("tc_causal", "long64k"): (309.21e6, "bf625141d5c0677b"),
     ("tc_causal_split", "sweep16k"): (308.31e6, "6187aa4fa5316de2"),
+    # captured on the first 8 of 16 heads, scaled by heads
+    ("tc_causal_split", "sweep16k_m512"): (285.4e6, "6187aa4fa5316de2"),
     ("tc_state", "causal8k"): (68.93e6, "219f9714fc031c6e"),
     ("tc_state", "nc4096"): (104.77e6, "219f9714fc031c6e"),
     ("tc_state", "long64k_nc"): (138.46e6, "219f9714fc031c6e"),
@@ -95,6 +98,7 @@ def workload(name):
         "long64k": (LONG64K, True),
         "long64k_nc": (LONG64K, False),
         "sweep16k": (SWEEP16K, True),
+        "sweep16k_m512": (SWEEP16K.with_(m=512), True),
     }
     return table[name]
 
@@ -836,7 +840,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="causal8k",
-                    choices=["causal8k", "nc4096", "long64k", "long64k_nc", "sweep16k", "decode8k",
+                    choices=["causal8k", "nc4096", "long64k", "long64k_nc", "sweep16k", "sweep16k_m512", "decode8k",
                              "decode_b256", "causal8k_bwd", "nc4096_bwd"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--heads", type=int, default=0,
