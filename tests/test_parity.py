@@ -363,14 +363,18 @@ def test_full_size_sampled_heads(w, causal, heads):
     assert np.isfinite(out).all()
 
 
-@pytest.mark.parametrize("m", [64, 512])
-def test_full_size_sweep_sampled(m):
+@pytest.mark.parametrize("m,heads", [(64, [5]), (128, [5]), (256, [5, 14]), (512, [5])])
+def test_full_size_sweep_sampled(m, heads):
+    """B=2, H=8, L=16384, d=dv=128 at full size in the launch configuration
+    the benchmark times (m = 256: two-slice clusters, two segments; m = 512:
+    four-slice clusters, one segment; m = 64, 128: whole heads)."""
     w = SWEEP16K.with_(m=m)
     inp = make_inputs(w)
     out = run_gpu(inp, True, MAP_POSITIVE)
-    ref = oracle_ref(inp, True, MAP_POSITIVE, heads=[5])
-    e = row_errors(out.reshape(16, w.L, w.dv)[[5]], ref.reshape(16, w.L, w.dv)[[5]])
+    ref = oracle_ref(inp, True, MAP_POSITIVE, heads=heads)
+    e = row_errors(out.reshape(16, w.L, w.dv)[heads], ref.reshape(16, w.L, w.dv)[heads])
     check_bf16(e, w.name)
+    assert np.isfinite(out).all()
 
 
 # ---------------------------------------------------------------------------
