@@ -377,6 +377,26 @@ def test_full_size_sweep_sampled(m, heads):
     assert np.isfinite(out).all()
 
 
+@pytest.mark.parametrize("fmap,m", [(MAP_ELU1, 128), (MAP_TRIG, 256)], ids=["elu1", "trig-m256"])
+def test_full_size_sweep_other_maps(fmap, m):
+    """Config 5's other maps at full size (B=2, H=8, L=16384, d=dv=128):
+    ELU+1 (r = d = 128, whole heads) and sin/cos at m = 256 (r = 512,
+    four-slice clusters), the latter on inputs scaled so the kernel is O(1)
+    with the rows of condition <= 10 scored on the plain metric."""
+    w = SWEEP16K.with_(feature_map=fmap, m=m)
+    inp = make_inputs(w)
+    if fmap == MAP_TRIG:
+        inp = scaled_inputs(inp, 0.25)
+    heads = [5]
+    out = run_gpu(inp, True, fmap).reshape(16, w.L, w.dv)[heads]
+    ref = oracle_ref(inp, True, fmap, heads=heads).reshape(16, w.L, w.dv)[heads]
+    if fmap == MAP_TRIG:
+        good = causal_trig_condition(inp, heads=heads).reshape(16, w.L)[heads] <= 10
+        assert good.mean() > 0.5
+        out, ref = out[good], ref[good]
+    check_bf16(row_errors(out, ref), f"{w.name} map={fmap} full size")
+
+
 # ---------------------------------------------------------------------------
 # the bf16 entry point runs the tensor-core kernels for the benchmark shapes
 # ---------------------------------------------------------------------------
