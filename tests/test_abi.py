@@ -84,6 +84,10 @@ def call(**kw):
     (dict(dv=256), fv.FAVOR_ERR_UNSUPPORTED),
     (dict(m=100), fv.FAVOR_ERR_UNSUPPORTED),
     (dict(feature_map=2, m=32), fv.FAVOR_ERR_INVALID_ARG),   # elu1 needs m == d
+    # a tensor of 2^31 elements or more: past the int32 element offsets
+    (dict(B=64, H=8, L=65536), fv.FAVOR_ERR_UNSUPPORTED),            # 2^25 rows x d = 64
+    (dict(B=32, H=8, L=65536, dv=128), fv.FAVOR_ERR_UNSUPPORTED),    # 2^24 rows x dv = 128
+    (dict(B=1, H=1, L=2 ** 30, d=32, dv=32), fv.FAVOR_ERR_UNSUPPORTED),
 ])
 def test_host_validation(lib, kw, want):
     assert call(**kw) == want

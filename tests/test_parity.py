@@ -397,6 +397,47 @@ def test_full_size_sweep_other_maps(fmap, m):
     check_bf16(row_errors(out, ref), f"{w.name} map={fmap} full size")
 
 
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "noncausal"])
+def test_largest_accepted_shape(causal):
+    """63 batch copies of the long64k heads (B = 63, H = 8, L = 65536, d = dv
+    = 64, m = 256): q, k, v and out each hold 2.11e9 elements, just under the
+    int32 element offsets the entry points accept (one batch more is refused
+    on the host, tests/test_abi.py), and out spans 8.5 GB, so a 32-bit byte
+    offset anywhere on the path would go wrong.  Every head is planned and
+    computed the same way wherever it sits (one segment per head causal; the
+    same pieces non-causal), so every batch copy must equal batch 0 bit for
+    bit; batch 0 meets the bar against the oracle on sampled heads."""
+    import torch
+    import favor_random_feature_gb300 as fv
+    inp = make_inputs(LONG64K)
+    w = inp.w
+    B = 63
+    q0, k0, v0, om = to_device(inp)
+    q = q0.expand(B, -1, -1, -1).contiguous()
+    k = k0.expand(B, -1, -1, -1).contiguous()
+    v = v0.expand(B, -1, -1, -1).contiguous()
+    del q0, k0, v0
+    assert 2 ** 31 - q.numel() <= 2 ** 25 and B * w.H * w.L * w.dv * 4 > 2 ** 32
+    out = torch.empty((B, w.H, w.L, w.dv), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    try:
+        rc = fv.favor_attn_forward(q, k, v, om, out, B, w.H, w.L, w.d, w.dv, w.m, int(causal), MAP_POSITIVE,
+                                   stream)
+        assert rc == fv.FAVOR_OK, fv.strerror(rc)
+        st = fv.favor_get_device_status(stream)
+        assert st == fv.FAVOR_OK, fv.strerror(st)
+        same = [b for b in range(1, B) if torch.equal(out[b], out[0])]
+        assert len(same) == B - 1, sorted(set(range(1, B)) - set(same))
+        got = out[0].cpu().numpy().astype(np.float64)
+    finally:
+        del q, k, v, out
+        torch.cuda.empty_cache()
+    heads = [0, 7]
+    ref = oracle_ref(inp, causal, MAP_POSITIVE, heads=heads)
+    check_bf16(row_errors(got[heads], ref.reshape(w.H, w.L, w.dv)[heads]), "B=63 copies of long64k")
+
+
+
 # ---------------------------------------------------------------------------
 # the bf16 entry point runs the tensor-core kernels for the benchmark shapes
 # ---------------------------------------------------------------------------
