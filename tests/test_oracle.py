@@ -21,7 +21,8 @@ GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 # ---------------------------------------------------------------------------
 def kernel_positive_closed(q, k, om):
     """(1/m) sum_i exp(w_i.(q+k) - (|q|^2+|k|^2)/2): the product of two
-    positive features written as one sum (spec closed form)."""
+    positive features written as one sum, exp(-(|q|^2 + |k|^2)/2) times the
+    mean of exp(w_i.(q + k)) (Performer page, the phi(x) equation)."""
     m = om.shape[0]
     s = om @ (q + k)
     return np.sum(np.exp(s - (q @ q + k @ k) / 2.0)) / m
@@ -279,6 +280,26 @@ def test_constant_values_reproduced():
     for causal in (False, True):
         out = oracle.forward(inp.q32, inp.k32, v, inp.omega, causal=causal)
         assert np.allclose(out, v, rtol=1e-13, atol=1e-12)
+
+
+@pytest.mark.parametrize("fmap", [MAP_POSITIVE, MAP_ELU1, MAP_TRIG], ids=["positive", "elu1", "trig"])
+def test_zero_keys_give_the_mean_of_the_values(fmap):
+    """Every key zero: phi(0) is the same vector for every key (1/sqrt(m) for
+    the positive map, ones for ELU+1, [0, 1, 0, 1, ...]/sqrt(m) for sin/cos),
+    so each query weighs the keys it sees equally whatever q and omega are:
+    out_i = mean of v_0..v_i (causal), the mean of all v (non-causal)."""
+    w = CAUSAL8K.with_(feature_map=fmap, m=64 if fmap == MAP_ELU1 else 256)
+    inp = make_inputs(w, L=50, B=1, H=2)
+    q = inp.q32 * (0.25 if fmap == MAP_TRIG else 1.0)   # sin/cos: keep sum_i cos(w_i.q) away from 0
+    k = np.zeros_like(inp.k32)
+    v = inp.v32.astype(np.float64)
+    om = None if fmap == MAP_ELU1 else inp.omega
+    want_c = np.cumsum(v, axis=2) / np.arange(1, v.shape[2] + 1)[:, None]
+    want_n = np.broadcast_to(v.mean(axis=2, keepdims=True), v.shape)
+    assert np.allclose(oracle.forward(q, k, inp.v32, om, causal=True, feature_map=fmap), want_c,
+                       rtol=1e-11, atol=1e-12)
+    assert np.allclose(oracle.forward(q, k, inp.v32, om, causal=False, feature_map=fmap), want_n,
+                       rtol=1e-11, atol=1e-12)
 
 
 def test_permuting_omega_rows_is_invariant():

@@ -269,6 +269,33 @@ def test_constant_values():
         assert np.allclose(out, inp.v32, rtol=5e-3, atol=5e-3)
 
 
+@pytest.mark.parametrize("causal", [False, True], ids=["noncausal", "causal"])
+@pytest.mark.parametrize("fmap,w", [(MAP_POSITIVE, CAUSAL8K), (MAP_ELU1, CAUSAL8K.with_(m=64)),
+                                    (MAP_POSITIVE, NC4096.with_(dtype="f32"))],
+                         ids=["positive", "elu1", "positive-f32"])
+def test_zero_keys_give_the_mean_of_the_values(fmap, w, causal):
+    """With every key zero, every key has the same features (1/sqrt(m) each for
+    the positive map, all ones for ELU+1), so every query weighs the keys it
+    sees equally whatever q and omega are: out_i is the mean of v over keys
+    0..i (causal) or over all keys (non-causal).  A closed form, not the
+    oracle; the tensor-core path (bf16) and the fp32 path."""
+    from favor_inputs import bf16_bits
+    inp = make_inputs(w.with_(feature_map=fmap), L=700, B=1, H=2)
+    inp.k32 = np.zeros_like(inp.k32)
+    inp.k = bf16_bits(inp.k32) if w.dtype == "bf16" else inp.k32
+    out = run_gpu(inp, causal, fmap)
+    v = inp.v32.astype(np.float64)
+    if causal:
+        want = np.cumsum(v, axis=2) / np.arange(1, v.shape[2] + 1)[:, None]
+    else:
+        want = np.broadcast_to(v.mean(axis=2, keepdims=True), v.shape)
+    e = row_errors(out, want)
+    if w.dtype == "bf16":
+        check_bf16(e, f"zero keys map={fmap} causal={causal}")
+    else:
+        assert e.max() <= F32_MAX, e.max()
+
+
 # ---------------------------------------------------------------------------
 # the other entry points
 # ---------------------------------------------------------------------------
