@@ -2818,11 +2818,13 @@ Plan make_plan(const Problem &p) {
     pl.nfg = g.n_ft / state_layout(g).FT;
     const int sms = num_sms();
     if (p.causal) {
-        // scan segments: whole 128-token chunks, about one CTA per SM (a
-        // split head takes rs CTAs per segment)
+        // scan segments: whole 128-token chunks, at most one CTA per SM (a
+        // split head takes rs CTAs per segment).  A scan CTA holds most of an
+        // SM's shared memory, so CTAs past the SM count would run as a second
+        // wave as long as the first.
         pl.rs = causal_split(p);
         const int rs = std::max(1, pl.rs);
-        int G = (int)std::lround((double)sms / ((double)p.BH * pl.nvb * rs));
+        int G = (int)(sms / ((long long)p.BH * pl.nvb * rs));
         // at most 64 segments: the combine keeps one scale per (piece, feature tile)
         G = std::max(1, std::min(std::min(G, pl.nchunk), 64));
         const int seg_chunks = (pl.nchunk + G - 1) / G;
