@@ -6,7 +6,7 @@ in HBM.  Default workload: causal, B=4, H=16, L=8192, d=dv=64, m=256,
 block-orthogonal omega, bf16 inputs (synthetic, seeded).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload causal8k|nc4096|long64k|long64k_nc|sweep16k|sweep16k_m512|
+                  [--workload causal8k|nc4096|long64k|long64k_nc|sweep16k|sweep16k_m128|sweep16k_m512|
                               decode8k|decode_b256|causal8k_bwd|nc4096_bwd]
 
 --impl reference times the float64 CPU oracle (the slow, obviously correct
@@ -98,6 +98,7 @@ def workload(name):
         "long64k": (LONG64K, True),
         "long64k_nc": (LONG64K, False),
         "sweep16k": (SWEEP16K, True),
+        "sweep16k_m128": (SWEEP16K.with_(m=128), True),
         "sweep16k_m512": (SWEEP16K.with_(m=512), True),
     }
     return table[name]
@@ -840,7 +841,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="causal8k",
-                    choices=["causal8k", "nc4096", "long64k", "long64k_nc", "sweep16k", "sweep16k_m512", "decode8k",
+                    choices=["causal8k", "nc4096", "long64k", "long64k_nc", "sweep16k", "sweep16k_m128", "sweep16k_m512",
+                             "decode8k",
                              "decode_b256", "causal8k_bwd", "nc4096_bwd"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--heads", type=int, default=0,
