@@ -51,6 +51,7 @@ TRAFFIC = {
     ("tc_causal", "long64k"): (309.21e6, "bf625141d5c0677b"),
     ("tc_causal_split", "sweep16k"): (308.31e6, "6187aa4fa5316de2"),
     # captured on the first 8 of 16 heads, scaled by heads
+    ("tc_causal", "sweep16k_m128"): (270.6e6, "bf625141d5c0677b"),
     ("tc_causal_split", "sweep16k_m512"): (285.4e6, "6187aa4fa5316de2"),
     ("tc_state", "causal8k"): (68.93e6, "219f9714fc031c6e"),
     ("tc_state", "nc4096"): (104.77e6, "219f9714fc031c6e"),
