@@ -122,36 +122,38 @@ def test_elu1_features_piecewise():
 @pytest.mark.parametrize("fmap", [MAP_POSITIVE, MAP_TRIG, MAP_ELU1, MAP_RELU, MAP_TRIG_SOFTMAX])
 def test_bruteforce_kernel_attention(causal, fmap):
     rng = np.random.default_rng(11 + fmap)
-    H, L, d, dv, m = 2, 40, 16, 8, 32
-    q = rng.standard_normal((1, H, L, d)) * d ** -0.25
-    k = rng.standard_normal((1, H, L, d)) * d ** -0.25
-    v = rng.standard_normal((1, H, L, dv))
+    B, H, L, d, dv, m = 2, 2, 40, 16, 8, 32     # two batches of two heads: the [B][H] layout
+    q = rng.standard_normal((B, H, L, d)) * d ** -0.25
+    k = rng.standard_normal((B, H, L, d)) * d ** -0.25
+    v = rng.standard_normal((B, H, L, dv))
     if fmap in (MAP_TRIG, MAP_TRIG_SOFTMAX):
         # small inputs keep the trig denominators well away from zero
         q *= 0.3
         k *= 0.3
     om = rng.standard_normal((H, m, d)) if fmap not in (MAP_ELU1, MAP_RELU) else None
     out = oracle.forward(q, k, v, om, causal=causal, feature_map=fmap)
-    for h in range(H):
-        A = np.empty((L, L))
-        for i in range(L):
-            for j in range(L):
-                if fmap == MAP_POSITIVE:
-                    A[i, j] = kernel_positive_closed(q[0, h, i], k[0, h, j], om[h])
-                elif fmap == MAP_TRIG:
-                    A[i, j] = kernel_trig_closed(q[0, h, i], k[0, h, j], om[h])
-                elif fmap == MAP_TRIG_SOFTMAX:
-                    qi, kj = q[0, h, i], k[0, h, j]
-                    A[i, j] = math.exp((qi @ qi + kj @ kj) / 2) * kernel_trig_closed(qi, kj, om[h])
-                elif fmap == MAP_RELU:
-                    A[i, j] = np.maximum(q[0, h, i], 0) @ np.maximum(k[0, h, j], 0)
-                else:
-                    fq = np.where(q[0, h, i] > 0, q[0, h, i] + 1.0, np.exp(q[0, h, i]))
-                    fk = np.where(k[0, h, j] > 0, k[0, h, j] + 1.0, np.exp(k[0, h, j]))
-                    A[i, j] = fq @ fk
-        ref = brute_attention(A, v[0, h], causal)
-        err = np.max(np.abs(out[0, h] - ref)) / np.max(np.abs(ref))
-        assert err <= 1e-12, err
+    for b in range(B):
+        for h in range(H):
+            A = np.empty((L, L))
+            for i in range(L):
+                qi = q[b, h, i]
+                for j in range(L):
+                    kj = k[b, h, j]
+                    if fmap == MAP_POSITIVE:
+                        A[i, j] = kernel_positive_closed(qi, kj, om[h])
+                    elif fmap == MAP_TRIG:
+                        A[i, j] = kernel_trig_closed(qi, kj, om[h])
+                    elif fmap == MAP_TRIG_SOFTMAX:
+                        A[i, j] = math.exp((qi @ qi + kj @ kj) / 2) * kernel_trig_closed(qi, kj, om[h])
+                    elif fmap == MAP_RELU:
+                        A[i, j] = np.maximum(qi, 0) @ np.maximum(kj, 0)
+                    else:
+                        fq = np.where(qi > 0, qi + 1.0, np.exp(qi))
+                        fk = np.where(kj > 0, kj + 1.0, np.exp(kj))
+                        A[i, j] = fq @ fk
+            ref = brute_attention(A, v[b, h], causal)
+            err = np.max(np.abs(out[b, h] - ref)) / np.max(np.abs(ref))
+            assert err <= 1e-12, (b, h, err)
 
 
 def test_causal_reduces_to_noncausal_at_last_row_and_v0_at_first():

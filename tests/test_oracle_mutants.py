@@ -60,6 +60,8 @@ MUTANTS = {
         ("for (int t = 0; t < d; ++t) v[t] -= dot * qj[t];", "for (int t = 0; t < d; ++t) v[t] += dot * qj[t];"),
     "block-orthogonal rows scaled by |g|^2 instead of |g|":
         ("const double chi = sqrt(ss);", "const double chi = ss;"),
+    "forward: a flat head index decoded as [H][B] (the wrong head's omega)":
+        ("int h = bh % H;", "int h = bh / B;"),
 }
 
 # the child: point the oracle package at the copy's source and build folder,
