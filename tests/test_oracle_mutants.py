@@ -62,6 +62,12 @@ MUTANTS = {
         ("const double chi = sqrt(ss);", "const double chi = ss;"),
     "forward: a flat head index decoded as [H][B] (the wrong head's omega)":
         ("int h = bh % H;", "int h = bh / B;"),
+    "trig map: each pair stored as [cos, sin] (the output cannot see it)":
+        ("pt[2 * i] = scale * sin(proj);\n                pt[2 * i + 1] = scale * cos(proj);",
+         "pt[2 * i] = scale * cos(proj);\n                pt[2 * i + 1] = scale * sin(proj);"),
+    "forward: a query's features taken from the key row":
+        ("rc = oracle_features(q + (size_t)i * d, omega, 1, d, m, map, phiq);",
+         "rc = oracle_features(k + (size_t)i * d, omega, 1, d, m, map, phiq);"),
 }
 
 # the child: point the oracle package at the copy's source and build folder,
