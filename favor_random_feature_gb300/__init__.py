@@ -46,6 +46,7 @@ EXPORTS = (
     "favor_stats_read",
     "favor_probe_ex2_rate",
     "favor_check_sincos",
+    "favor_plan_info",
     "favor_state_floats",
     "favor_attn_state",
     "favor_attn_state_f32",
@@ -105,6 +106,8 @@ def lib() -> ctypes.CDLL:
         L.favor_probe_ex2_rate.restype = i
         L.favor_check_sincos.argtypes = [vp, vp, vp, i, vp]
         L.favor_check_sincos.restype = i
+        L.favor_plan_info.argtypes = [i] * 9 + [vp]
+        L.favor_plan_info.restype = i
         L.favor_state_floats.argtypes = [i, i, i, i]
         L.favor_state_floats.restype = i
         for name in ("favor_attn_state", "favor_attn_state_f32"):
@@ -211,6 +214,15 @@ def favor_stats_read() -> FavorStats:
     if rc != FAVOR_OK:
         raise FavorError(rc, "favor_stats_read")
     return st
+
+
+def favor_plan_info(B, H, L, d, dv, m, causal, feature_map, sms):
+    """(status, plan): the tensor-core launch plan of a shape on `sms` SMs
+    (seven integers, the order include/favor.h gives)."""
+    plan = (ctypes.c_int * 7)()
+    rc = lib().favor_plan_info(int(B), int(H), int(L), int(d), int(dv), int(m), int(causal), int(feature_map),
+                               int(sms), ctypes.cast(plan, ctypes.c_void_p))
+    return rc, list(plan)
 
 
 def favor_check_sincos(x, s, c, n, stream=None) -> int:

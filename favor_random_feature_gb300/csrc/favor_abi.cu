@@ -416,6 +416,15 @@ extern "C" int favor_get_device_status(cudaStream_t stream) {
     return h;
 }
 
+extern "C" int favor_plan_info(int B, int H, int L, int d, int dv, int m, int causal, int feature_map, int sms,
+                               int *plan) {
+    Problem p;
+    int rc = make_problem(B, H, L, d, dv, m, causal, feature_map, &p);
+    if (rc) return rc;
+    if (!plan || sms < 1) return FAVOR_ERR_INVALID_ARG;
+    return tc_plan_info(p, sms, plan);
+}
+
 extern "C" int favor_check_sincos(const float *x, float *s, float *c, int n, cudaStream_t stream) {
     if (n < 0) return FAVOR_ERR_INVALID_ARG;
     if (n == 0) return FAVOR_OK;

@@ -78,6 +78,12 @@ int tc_forward(const void *q, const void *k, const void *v, const float *omega, 
 // Scratch bytes the tensor-core path needs for a problem, and the path run on
 // caller-provided scratch (FAVOR_ERR_UNSUPPORTED if ws_bytes is too small).
 size_t tc_scratch_bytes(const Problem &p);
+// the tensor-core launch plan of a shape on a device of `sms` SMs, without a
+// device: plan[7] = segments per head (causal) or key pieces per head, pieces
+// per segment, piece states per head, CTAs per head slice cluster, value
+// tiles, scan or output CTAs, state CTAs.  FAVOR_ERR_UNSUPPORTED for a shape
+// the tensor-core kernels do not take.
+int tc_plan_info(const Problem &p, int sms, int *plan);
 // One bounded mbarrier wait that nothing completes: it runs out after
 // limit_cycles clock cycles and records FAVOR_ERR_TIMEOUT in *status.
 int tc_wait_expiry(long long limit_cycles, int *status, cudaStream_t st);

@@ -31,6 +31,7 @@
 // tc_output (non-causal rows), tc_causal (the chunked causal scan) and
 // tc_causal_split (the same scan with a head's features split over the CTAs
 // of a cluster).
+#include <climits>
 #include <cmath>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -2778,7 +2779,9 @@ Problem tc_widen(const Problem &p) {
 
 bool tc_forward_supported(const Problem &p) { return tc_supported(tc_widen(p)); }
 
-bool tc_supported(const Problem &p) {
+namespace {
+// the shapes the tensor-core kernels take (the host's part of tc_supported)
+bool tc_shape_supported(const Problem &p) {
     // ReLU and the softmax-scaled Fourier map run on the SIMT kernels
     if (p.map == FAVOR_MAP_RELU || p.map == FAVOR_MAP_TRIG_SOFTMAX) return false;
     if (p.d != 64 && p.d != 128) return false;
@@ -2793,9 +2796,11 @@ bool tc_supported(const Problem &p) {
         if (p.r != 128 && p.r != 256) return false;
         if (output_layout(g).bytes > kSmemMax) return false;
     }
-    if (state_layout(g).bytes > kSmemMax) return false;
-    return encoder() != nullptr;
+    return state_layout(g).bytes <= kSmemMax;
 }
+}  // namespace
+
+bool tc_supported(const Problem &p) { return tc_shape_supported(p) && encoder() != nullptr; }
 
 namespace {
 struct Plan {
@@ -2810,13 +2815,13 @@ double state_cost(long ctas, int chunks, int sms) {
     return (double)((ctas + sms - 1) / sms) * (chunks + 2);
 }
 
-Plan make_plan(const Problem &p) {
+// The launch plan on a device of `sms` SMs (pure host arithmetic).
+Plan make_plan(const Problem &p, int sms) {
     const Geo g = make_geo(p);
     Plan pl;
     pl.nvb = p.dv / 64;
     pl.nchunk = (p.L + kC - 1) / kC;
     pl.nfg = g.n_ft / state_layout(g).FT;
-    const int sms = num_sms();
     if (p.causal) {
         // scan segments: whole 128-token chunks, at most one CTA per SM (a
         // split head takes rs CTAs per segment).  A scan CTA holds most of an
@@ -2882,6 +2887,8 @@ Plan make_plan(const Problem &p) {
     return pl;
 }
 
+Plan make_plan(const Problem &p) { return make_plan(p, num_sms()); }
+
 // The state pass over the plan's pieces (W image already written by
 // tc_prep_omega on the same stream).
 int launch_state(const Problem &p, const Geo &g, const Plan &pl, const uint8_t *img, float *state,
@@ -2905,6 +2912,24 @@ int launch_state(const Problem &p, const Geo &g, const Plan &pl, const uint8_t *
 }  // namespace
 
 size_t tc_scratch_bytes(const Problem &p) { return make_plan(p).bytes; }
+
+int tc_plan_info(const Problem &p0, int sms, int *plan) {
+    const Problem p = tc_widen(p0);
+    if (!tc_shape_supported(p)) return FAVOR_ERR_UNSUPPORTED;
+    const Plan pl = make_plan(p, sms);
+    const int rs = p.causal ? std::max(1, pl.rs) : 1;
+    plan[0] = pl.G;
+    plan[1] = pl.pps;
+    plan[2] = pl.nstate;
+    plan[3] = rs;
+    plan[4] = pl.nvb;
+    // the scan's CTAs (causal), or the persistent output kernel's (non-causal)
+    plan[5] = p.causal ? (int)std::min<long long>((long long)rs * pl.G * pl.nvb * p.BH, INT_MAX)
+                       : (int)std::min<long long>((long long)pl.nchunk * p.BH * pl.nvb, sms);
+    // the state pass's CTAs (0 when a causal head is one segment)
+    plan[6] = (int)std::min<long long>((long long)pl.nfg * pl.nstate * p.BH, INT_MAX);
+    return FAVOR_OK;
+}
 
 int tc_sincos_check(const float *x, float *s, float *c, int n, cudaStream_t st) {
     sincos_check_kernel<<<std::max(1, std::min((n + 255) / 256, 1024)), 256, 0, st>>>(x, s, c, n);

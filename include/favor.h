@@ -333,6 +333,24 @@ int favor_stats_read(favor_stats_t *out);
  * it waits for the timing to finish.  Returns favor_status_t. */
 int favor_probe_ex2_rate(double *ex2_per_second, cudaStream_t stream);
 
+/* Test hook, no counterpart on the pages: the launch plan the tensor-core
+ * path takes for a forward pass of this shape on a device of `sms` SMs,
+ * computed on the host without touching a device.  plan[7] receives:
+ *   [0] causal: scan segments per head; non-causal: key pieces per head
+ *   [1] causal: piece states per segment
+ *   [2] piece states per head (the state pass's pieces; 0 for a causal head
+ *       of one segment)
+ *   [3] CTAs of a cluster that split a head's features (1: whole heads)
+ *   [4] value tiles of 64 columns
+ *   [5] causal: CTAs of the scan; non-causal: CTAs of the persistent output
+ *       kernel
+ *   [6] CTAs of the state pass
+ * Returns FAVOR_ERR_INVALID_ARG / FAVOR_ERR_UNSUPPORTED as favor_attn_forward
+ * would for the shape, FAVOR_ERR_UNSUPPORTED as well for a shape the
+ * tensor-core kernels do not take (favor_attn_forward then runs the fp32 SIMT
+ * kernels), FAVOR_ERR_INVALID_ARG for a NULL plan or sms < 1. */
+int favor_plan_info(int B, int H, int L, int d, int dv, int m, int causal, int feature_map, int sms, int *plan);
+
 /* Test hook, no counterpart on the pages: the sine and cosine the
  * tensor-core kernels use for the sin/cos features (FAVOR_MAP_TRIG), on n
  * device values x[i] -> s[i], c[i] (fp32, device pointers, 16-byte aligned,
